@@ -1,0 +1,151 @@
+"""Seeded synthetic inputs for the four operations, shared by the library's
+benchmark and the tests (the only code both sides share).
+
+This module draws random numbers and nothing else: it holds none of the
+method's arithmetic. Every tensor is float32 (labels int32), drawn from NumPy's
+``default_rng(seed)`` (PCG64), the generator the "mojolearn" PyPI page uses in
+its quick start and the "MojoLearn 162M" model card names for initialisation
+(table "Training": ``default_rng(93261)``, N(0, 0.02), norm weights
+1 + N(0, 0.02)). Shapes follow the model card's table "Compared with GPT-3
+Small" (12 x 768, SwiGLU 2,048 wide, 50,257-id vocabulary, context 2,048,
+162,147,840 parameters) and the five workload configurations of this library.
+
+Draw order inside one seed is fixed and documented per function, so the same
+seed always yields the same bytes on every host.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+D_MODEL = 768
+D_FF = 2048
+VOCAB = 50257
+TOKENS = 8192            # 4 sequences x 2,048 tokens
+N_PARAMS = 162_147_840   # the 162M decoder's parameter count
+
+SEED_CFG1, SEED_CFG2, SEED_CFG3, SEED_CFG4, SEED_CFG5 = 0, 1, 2, 3, 4
+
+
+def uniform_pm1(rng: np.random.Generator, shape) -> np.ndarray:
+    """Uniform on [-1, 1) in float32 (exact: a 24-bit grid scaled by 2, minus 1)."""
+    return rng.random(shape, dtype=np.float32) * np.float32(2) - np.float32(1)
+
+
+def normal(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
+    z = rng.standard_normal(shape, dtype=np.float32)
+    if std != 1.0:
+        z *= np.float32(std)
+    return z
+
+
+# ------------------------------------------------------------------ GEMM
+def gemm_cfg1(seed: int = SEED_CFG1, n: int = 256):
+    """Fixed-order GEMM C = A B, M = N = K = 256, A and B uniform [-1, 1).
+    Draw order: A, then B."""
+    rng = np.random.default_rng(seed)
+    A = uniform_pm1(rng, (n, n))
+    B = uniform_pm1(rng, (n, n))
+    return [dict(name="gemm256", A=A, B=B, transA=False, transB=False)]
+
+
+def gemm_cfg2(seed: int = SEED_CFG2, tokens: int = 2048, d: int = 64,
+              hidden: int = 172, vocab: int = 256):
+    """Small byte-level LM step GEMMs: activations N(0, 1), weights N(0, 0.02).
+    Weights are K x N (row-major) except the logits head, stored
+    [vocab, d] = [out, in] and applied transposed.
+    Draw order: X, W_qkv, W_o, W_gate, W_up, H, W_down, W_head."""
+    rng = np.random.default_rng(seed)
+    X = normal(rng, (tokens, d))
+    W_qkv = normal(rng, (d, 3 * d), 0.02)
+    W_o = normal(rng, (d, d), 0.02)
+    W_gate = normal(rng, (d, hidden), 0.02)
+    W_up = normal(rng, (d, hidden), 0.02)
+    H = normal(rng, (tokens, hidden))
+    W_down = normal(rng, (hidden, d), 0.02)
+    W_head = normal(rng, (vocab, d), 0.02)
+    return [
+        dict(name="qkv", A=X, B=W_qkv, transA=False, transB=False),
+        dict(name="attn_out", A=X, B=W_o, transA=False, transB=False),
+        dict(name="swiglu_gate", A=X, B=W_gate, transA=False, transB=False),
+        dict(name="swiglu_up", A=X, B=W_up, transA=False, transB=False),
+        dict(name="swiglu_down", A=H, B=W_down, transA=False, transB=False),
+        dict(name="logits", A=X, B=W_head, transA=False, transB=True),
+    ]
+
+
+def gemm_cfg3(seed: int = SEED_CFG3, tokens: int = TOKENS, d: int = D_MODEL,
+              dff: int = D_FF, vocab: int = VOCAB):
+    """162M-decoder forward GEMMs. X tokens x 768 and H tokens x 2048 are N(0, 1);
+    weights N(0, 0.02), K x N row-major, except the LM head stored
+    [50257, 768] = [out, in] (the model card's Linear layout) and applied
+    transposed. Draw order: X, H, W_qkv, W_o, W_gate, W_up, W_down, W_head."""
+    rng = np.random.default_rng(seed)
+    X = normal(rng, (tokens, d))
+    H = normal(rng, (tokens, dff))
+    W_qkv = normal(rng, (d, 3 * d), 0.02)
+    W_o = normal(rng, (d, d), 0.02)
+    W_gate = normal(rng, (d, dff), 0.02)
+    W_up = normal(rng, (d, dff), 0.02)
+    W_down = normal(rng, (dff, d), 0.02)
+    W_head = normal(rng, (vocab, d), 0.02)
+    return [
+        dict(name="qkv", A=X, B=W_qkv, transA=False, transB=False),
+        dict(name="attn_out", A=X, B=W_o, transA=False, transB=False),
+        dict(name="swiglu_gate", A=X, B=W_gate, transA=False, transB=False),
+        dict(name="swiglu_up", A=X, B=W_up, transA=False, transB=False),
+        dict(name="swiglu_down", A=H, B=W_down, transA=False, transB=False),
+        dict(name="lm_head", A=X, B=W_head, transA=False, transB=True),
+    ]
+
+
+# ------------------------------------------------------------------ row ops
+def rowops_cfg4(seed: int = SEED_CFG4, rows: int = TOKENS, d: int = D_MODEL,
+                vocab: int = VOCAB, logit_std: float = 2.0):
+    """RMSNorm input x rows x 768 ~ N(0, 1), gain 1 + N(0, 0.02), eps 1e-6;
+    cross-entropy logits rows x 50257 ~ N(0, 2) (std 2), labels uniform int in
+    [0, vocab). Draw order: x, gain noise, logits, labels."""
+    rng = np.random.default_rng(seed)
+    x = normal(rng, (rows, d))
+    gain = np.float32(1) + normal(rng, (d,), 0.02)
+    logits = normal(rng, (rows, vocab), logit_std)
+    labels = rng.integers(0, vocab, size=rows, dtype=np.int32)
+    return dict(x=x, gain=gain, eps=np.float32(1e-6), logits=logits,
+                labels=labels)
+
+
+# ------------------------------------------------------------------ backward
+def dw_cfg5(seed: int = SEED_CFG5, tokens: int = TOKENS, d: int = D_MODEL,
+            dff: int = D_FF):
+    """Weight-gradient GEMMs dW = X^T dY contracting over the tokens:
+    X N(0, 1), dY N(0, 1e-3). Draw order: X1 (tokens x 768),
+    dY1 (tokens x 2304), X2 (tokens x 2048), dY2 (tokens x 768)."""
+    rng = np.random.default_rng(seed)
+    X1 = normal(rng, (tokens, d))
+    dY1 = normal(rng, (tokens, 3 * d), 1e-3)
+    X2 = normal(rng, (tokens, dff))
+    dY2 = normal(rng, (tokens, d), 1e-3)
+    return [
+        dict(name="dW_qkv", A=X1, B=dY1, transA=True, transB=False),
+        dict(name="dW_down", A=X2, B=dY2, transA=True, transB=False),
+    ]
+
+
+ADAMW_HP = dict(lr=6e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
+                step=251)
+
+
+def adamw_cfg5(seed: int = SEED_CFG5 + 100, n: int = N_PARAMS):
+    """AdamW state for n parameters: p ~ N(0, 0.02), g ~ N(0, 1e-3),
+    m ~ N(0, 1e-3), v = (N(0, 1e-3))^2 (warm moments, as step 251 implies).
+    Draw order: p, g, m, v-root. Hyperparameters: ADAMW_HP."""
+    rng = np.random.default_rng(seed)
+    p = normal(rng, (n,), 0.02)
+    g = normal(rng, (n,), 1e-3)
+    m = normal(rng, (n,), 1e-3)
+    v = normal(rng, (n,), 1e-3)
+    np.multiply(v, v, out=v)
+    return dict(p=p, g=g, m=m, v=v, **ADAMW_HP)
+
+
+def flops_gemm(M: int, N: int, K: int) -> int:
+    return 2 * M * N * K
