@@ -1,0 +1,563 @@
+#!/usr/bin/env python
+"""Benchmark of the bit-exact fixed-order FP32 hot path on GB300.
+
+One step = one pass of every operation of the path over one batch of the
+162M-decoder workloads (shapes from the "MojoLearn 162M" model card, table
+"Compared with GPT-3 Small"; 8,192 tokens = 4 x 2,048):
+  RMSNorm 8192 x 768 -> forward GEMMs (QKV 768x2304, out 768x768, SwiGLU gate and
+  up 768x2048, down 2048x768, LM head 768x50257 with the [out, in] weight) ->
+  softmax cross-entropy over 8192 x 50257 logits (loss, mean, dlogits) ->
+  weight-gradient GEMMs X^T dY over the 8,192 tokens (768x2304, 2048x768) ->
+  AdamW over 162,147,840 parameters.
+Inputs are synthetic and seeded (bitwise_reproducible_fp32_gb300.inputs).
+
+value: fixed-order FP32 GEMM TFLOP/s = the step's GEMM FLOPs / the GEMM kernels'
+device time (CUDA events on the launching stream). The reduce/AdamW rates are
+under "ops". L2 is flushed (a 512 MB write) before every timed step.
+
+--impl reference times the CPU oracle (the path's only reference
+implementation) on a bounded sample of the same workload, on this host's cores.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bitwise_reproducible_fp32_gb300 import inputs  # noqa: E402
+
+METRIC = ("bit-exact fixed-order FP32 GEMM TFLOP/s (% FP32 FMA peak); "
+          "reduce/AdamW GB/s")
+WORKLOAD = ("162M-decoder FP32 step: RMSNorm 8192x768, forward GEMMs "
+            "(8192 tokens; 768x2304, 768x768, 2x 768x2048, 2048x768, LM head "
+            "768x50257), softmax cross-entropy 8192x50257 with dlogits and mean, "
+            "dW GEMMs over 8192 tokens (768x2304, 2048x768), AdamW 162,147,840 params")
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+
+
+def fp32_peak_tflops(sm_mhz: float, sms: int = SM_COUNT) -> float:
+    """CUDA-core FP32 FMA peak: SMs x 128 lanes x 2 flops x clock."""
+    return sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+# ------------------------------------------------------------------ workload
+def gemm_list():
+    fwd = inputs.gemm_cfg3()
+    dw = inputs.dw_cfg5()
+    return fwd, dw
+
+
+def gemm_dims(p):
+    A, B = p["A"], p["B"]
+    M = A.shape[1] if p["transA"] else A.shape[0]
+    K = A.shape[0] if p["transA"] else A.shape[1]
+    N = B.shape[0] if p["transB"] else B.shape[1]
+    return M, N, K
+
+
+def bytes_rmsnorm(rows, D):
+    return rows * D * 8 + D * 4 + rows * 4
+
+
+def bytes_xent(rows, V, dlogits=True):
+    return rows * V * 4 * (2 if dlogits else 1) + rows * 12
+
+
+def bytes_adamw(n):
+    return n * 28
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from bitwise_reproducible_fp32_gb300 import build as libbuild
+    from bitwise_reproducible_fp32_gb300 import detlib
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    libbuild.build()
+    detlib.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    t_setup = time.time()
+    fwd, dw = gemm_list()
+    r4 = inputs.rowops_cfg4()
+    aw = inputs.adamw_cfg5()
+    host = dict(fwd=fwd, dw=dw, r4=r4, aw=aw)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    # device-resident inputs (shared tensors uploaded once)
+    cache = {}
+
+    def dev_of(a):
+        k = id(a)
+        if k not in cache:
+            cache[k] = up(a)
+        return cache[k]
+
+    g_fwd = [(p, dev_of(p["A"]), dev_of(p["B"])) for p in fwd]
+    g_dw = [(p, dev_of(p["A"]), dev_of(p["B"])) for p in dw]
+    c_fwd = [torch.empty(gemm_dims(p)[:2], dtype=torch.float32, device=dev) for p in fwd]
+    c_dw = [torch.empty(gemm_dims(p)[:2], dtype=torch.float32, device=dev) for p in dw]
+    x4, gain4 = up(r4["x"]), up(r4["gain"])
+    y4 = torch.empty_like(x4)
+    inv4 = torch.empty(x4.shape[0], dtype=torch.float32, device=dev)
+    logits, labels = up(r4["logits"]), up(r4["labels"])
+    loss = torch.empty(logits.shape[0], dtype=torch.float32, device=dev)
+    lmean = torch.empty(1, dtype=torch.float32, device=dev)
+    dlog = torch.empty_like(logits)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    P, G, Mm, Vv = (up(aw[k]) for k in ("p", "g", "m", "v"))
+    hp = {k: aw[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")}
+    flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)  # 512 MB
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup
+
+    rows4, D4 = r4["x"].shape
+    V = r4["logits"].shape[1]
+    n_params = aw["p"].size
+    gemm_flops_fwd = [inputs.flops_gemm(*gemm_dims(p)) for p in fwd]
+    gemm_flops_dw = [inputs.flops_gemm(*gemm_dims(p)) for p in dw]
+    gemm_flops = sum(gemm_flops_fwd) + sum(gemm_flops_dw)
+    lm_idx = [p["name"] for p in fwd].index("lm_head")
+    launches_per_step = 1 + len(fwd) + 2 + len(dw) + 1
+
+    segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "gemm_dw", "adamw"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record()
+        mark(0)
+        detlib.detrmsnorm_f32(x4, gain4, float(r4["eps"]), y=y4, inv_rms=inv4)
+        mark(1)
+        for i, (p, A, B) in enumerate(g_fwd):
+            if i == lm_idx:
+                continue
+            detlib.detgemm_f32(A, B, c_fwd[i], transA=p["transA"], transB=p["transB"])
+        mark(2)
+        p, A, B = g_fwd[lm_idx]
+        detlib.detgemm_f32(A, B, c_fwd[lm_idx], transA=p["transA"], transB=p["transB"])
+        mark(3)
+        detlib.detxent_f32(logits, labels, loss=loss, loss_mean=lmean, dlogits=dlog,
+                           dscale=1.0 / rows4, dev_status=status)
+        mark(4)
+        for i, (p, A, B) in enumerate(g_dw):
+            detlib.detgemm_f32(A, B, c_dw[i], transA=p["transA"], transB=p["transB"])
+        mark(5)
+        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
+        mark(6)
+
+    import torch.distributed as dist
+    distributed = world > 1
+
+    def barrier():
+        if distributed:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    barrier()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    events = []
+    barrier()
+    t0 = time.time()
+    for _ in range(args.steps):
+        flush.fill_(float(len(events)))          # L2 flush, outside the events
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        step(ev)
+        events.append(ev)
+    barrier()
+    wall = time.time() - t0
+    clocks = sampler.stop()
+
+    seg_ms = {s: 0.0 for s in segs}
+    for ev in events:
+        for i, s in enumerate(segs):
+            seg_ms[s] += ev[i].elapsed_time(ev[i + 1])
+    step_ms = sum(seg_ms.values()) / args.steps
+    gemm_ms = (seg_ms["gemm_fwd_other"] + seg_ms["gemm_lm_head"] + seg_ms["gemm_dw"]) / args.steps
+    lm_ms = seg_ms["gemm_lm_head"] / args.steps
+
+    # max over ranks of the per-step device times
+    if distributed:
+        t = torch.tensor([step_ms, gemm_ms, lm_ms] + [seg_ms[s] for s in segs],
+                         dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, gemm_ms, lm_ms = t[0].item(), t[1].item(), t[2].item()
+        for i, s in enumerate(segs):
+            seg_ms[s] = t[3 + i].item()
+
+    if int(status.item()) != 0:
+        raise SystemExit("cross-entropy reported an out-of-range label")
+    if detlib.det_watchdog_status() != 0:
+        raise SystemExit("a bounded device wait gave up during the run")
+
+    result = None
+    if rank == 0:
+        peaks, peak_kind = measured_peaks()
+        hbm = float(peaks["hbm_gbs"])
+        smax = float(peaks.get("sm_max_mhz", 2070.0))
+        fma_peak = fp32_peak_tflops(smax)
+        per = lambda s: seg_ms[s] / args.steps / 1e3   # seconds a step
+        gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12 * world
+        lm_flops = gemm_flops_fwd[lm_idx]
+        lm_tflops = lm_flops / (lm_ms / 1e3) / 1e12
+        ops = {
+            "gemm_all": {"tflops": gemm_tflops / world, "frac_fp32_peak": gemm_tflops / world / fma_peak,
+                         "ms": gemm_ms},
+            "gemm_lm_head": {"tflops": lm_tflops, "frac_fp32_peak": lm_tflops / fma_peak,
+                             "ms": lm_ms},
+            "gemm_fwd_other": {"tflops": (sum(gemm_flops_fwd) - lm_flops) / per("gemm_fwd_other") / 1e12,
+                               "ms": per("gemm_fwd_other") * 1e3},
+            "gemm_dw": {"tflops": sum(gemm_flops_dw) / per("gemm_dw") / 1e12,
+                        "ms": per("gemm_dw") * 1e3},
+            "rmsnorm": {"gbs": bytes_rmsnorm(rows4, D4) / per("rmsnorm") / 1e9,
+                        "frac_hbm": bytes_rmsnorm(rows4, D4) / per("rmsnorm") / 1e9 / hbm,
+                        "ms": per("rmsnorm") * 1e3},
+            "xent": {"gbs": bytes_xent(rows4, V) / per("xent") / 1e9,
+                     "frac_hbm": bytes_xent(rows4, V) / per("xent") / 1e9 / hbm,
+                     "ms": per("xent") * 1e3},
+            "adamw": {"gbs": bytes_adamw(n_params) / per("adamw") / 1e9,
+                      "frac_hbm": bytes_adamw(n_params) / per("adamw") / 1e9 / hbm,
+                      "ms": per("adamw") * 1e3},
+        }
+        traffic = load_traffic()
+        result = {
+            "metric": METRIC,
+            "value": round(gemm_tflops, 4),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(step_ms, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded numpy PCG64, shapes of the 162M model card)",
+            "config": {"workload": WORKLOAD, "tokens": rows4, "d_model": D4, "vocab": V,
+                       "params": int(n_params), "parallelism": f"replicas{world}",
+                       "l2": "flushed (512 MB write) before every timed step"},
+            "roofline": {"bound": "alu", "kernel": "gemm_kernel (LM head, 8192x50257x768)",
+                         "achieved": round(lm_tflops, 4),
+                         "peak": round(fma_peak, 3), "unit": "TFLOP/s",
+                         "frac": round(lm_tflops / fma_peak, 4),
+                         "peak_kind": f"FP32 FFMA: {SM_COUNT} SMs x 128 lanes x 2 x "
+                                      f"{smax:.0f} MHz ({peak_kind} max clock)",
+                         "traffic": traffic.get("gemm_lm_head")},
+            "rooflines": {
+                "rmsnorm": {"bound": "hbm", "achieved": round(ops["rmsnorm"]["gbs"], 1),
+                            "peak": hbm, "unit": "GB/s",
+                            "frac": round(ops["rmsnorm"]["frac_hbm"], 4),
+                            "traffic": traffic.get("rmsnorm")},
+                "xent": {"bound": "hbm", "achieved": round(ops["xent"]["gbs"], 1),
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": round(ops["xent"]["frac_hbm"], 4),
+                         "traffic": traffic.get("xent")},
+                "adamw": {"bound": "hbm", "achieved": round(ops["adamw"]["gbs"], 1),
+                          "peak": hbm, "unit": "GB/s",
+                          "frac": round(ops["adamw"]["frac_hbm"], 4),
+                          "traffic": traffic.get("adamw")},
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+            "ops": ops,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "setup_s": round(setup_s, 1),
+            "timed_wall_s": round(wall, 3),
+        }
+        if not args.skip_e2e:
+            result["e2e"] = e2e_leg(args, dev, host, gemm_flops)
+        if not args.skip_cpu and world == 1:
+            result["cpu_baseline"] = cpu_baseline(args)
+    return result
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, when present and
+    current (profiles/traffic.json; null otherwise)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return {}
+    try:
+        return {k: v for k, v in json.load(open(path)).get("per_launch_bytes", {}).items()}
+    except (OSError, ValueError):
+        return {}
+
+
+def e2e_leg(args, dev, host, gemm_flops):
+    """The same step through the public API with pinned host buffers: every
+    input copied host->device and every output device->host inside the timed
+    region, each step."""
+    import torch
+
+    from bitwise_reproducible_fp32_gb300 import detlib
+
+    fwd, dw, r4, aw = host["fwd"], host["dw"], host["r4"], host["aw"]
+    pinned = {}
+
+    def pin(a):
+        k = id(a)
+        if k not in pinned:
+            t = torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+            pinned[k] = (t, torch.empty(t.shape, dtype=t.dtype, device=dev))
+        return pinned[k]
+
+    srcs = []
+    for p in fwd + dw:
+        srcs += [pin(p["A"]), pin(p["B"])]
+    for k in ("x", "gain", "logits", "labels"):
+        srcs.append(pin(r4[k]))
+    for k in ("p", "g", "m", "v"):
+        srcs.append(pin(aw[k]))
+    uniq = list({id(s[0]): s for s in srcs}.values())
+    h2d = sum(t.numel() * t.element_size() for t, _ in uniq)
+
+    outs_dev = [torch.empty(gemm_dims(p)[:2], dtype=torch.float32, device=dev)
+                for p in fwd + dw]
+    rows4, D4 = r4["x"].shape
+    V = r4["logits"].shape[1]
+    y4 = torch.empty((rows4, D4), dtype=torch.float32, device=dev)
+    inv4 = torch.empty(rows4, dtype=torch.float32, device=dev)
+    loss = torch.empty(rows4, dtype=torch.float32, device=dev)
+    lmean = torch.empty(1, dtype=torch.float32, device=dev)
+    dlog = torch.empty((rows4, V), dtype=torch.float32, device=dev)
+    dev_outs = outs_dev + [y4, inv4, loss, lmean, dlog]
+    host_outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_outs]
+    pmv_host = [torch.empty(aw[k].shape, dtype=torch.float32).pin_memory()
+                for k in ("p", "m", "v")]
+    d2h = sum(t.numel() * 4 for t in host_outs) + sum(t.numel() * 4 for t in pmv_host)
+    hp = {k: aw[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")}
+
+    def one_step():
+        for t, d in uniq:
+            d.copy_(t, non_blocking=True)
+        g = lambda a: pin(a)[1]
+        for i, p in enumerate(fwd + dw):
+            detlib.detgemm_f32(g(p["A"]), g(p["B"]), outs_dev[i], transA=p["transA"],
+                               transB=p["transB"])
+        detlib.detrmsnorm_f32(g(r4["x"]), g(r4["gain"]), float(r4["eps"]), y=y4,
+                              inv_rms=inv4)
+        detlib.detxent_f32(g(r4["logits"]), g(r4["labels"]), loss=loss, loss_mean=lmean,
+                           dlogits=dlog, dscale=1.0 / rows4)
+        P, G, M, Vv = (g(aw[k]) for k in ("p", "g", "m", "v"))
+        detlib.detadamw_f32(P, G, M, Vv, **hp)
+        for h, d in zip(host_outs, dev_outs):
+            h.copy_(d, non_blocking=True)
+        for h, d in zip(pmv_host, (P, M, Vv)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        one_step()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 5))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(gemm_flops / dt / 1e12, 4), "unit": "TFLOP/s",
+            "ms_per_step": round(dt * 1e3, 3), "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------------ oracle legs
+def oracle_sample(budget_s: float):
+    """Times the CPU oracle on bounded samples of the step's operations, on all
+    host cores. Returns the rates and a description."""
+    import oracle
+
+    oracle.build()
+    cores = oracle.nthreads_default()
+    fwd, _ = gemm_list()
+    lm = [p for p in fwd if p["name"] == "lm_head"][0]
+    rates = {}
+    # GEMM: rows of the LM head until the time budget is spent
+    rows_done, t_g, flops = 0, 0.0, 0
+    step_rows = max(cores, 16)
+    while t_g < budget_s * 0.6 and rows_done + step_rows <= lm["A"].shape[0]:
+        a = np.ascontiguousarray(lm["A"][rows_done:rows_done + step_rows])
+        t0 = time.perf_counter()
+        oracle.gemm(a, lm["B"], transB=True, nthreads=cores)
+        t_g += time.perf_counter() - t0
+        rows_done += step_rows
+        flops += 2 * step_rows * lm["B"].shape[0] * lm["B"].shape[1]
+    rates["gemm_tflops"] = flops / t_g / 1e12
+    r4 = inputs.rowops_cfg4(rows=cores * 4)
+    t0 = time.perf_counter()
+    oracle.xent(r4["logits"], r4["labels"], with_dlogits=True, nthreads=cores)
+    dt = time.perf_counter() - t0
+    rates["xent_gbs"] = bytes_xent(*r4["logits"].shape) / dt / 1e9
+    t0 = time.perf_counter()
+    oracle.rmsnorm(r4["x"], r4["gain"], eps=r4["eps"], nthreads=cores)
+    dt = time.perf_counter() - t0
+    rates["rmsnorm_gbs"] = bytes_rmsnorm(*r4["x"].shape) / dt / 1e9
+    n = 20_000_000
+    a = inputs.adamw_cfg5(n=n)
+    t0 = time.perf_counter()
+    oracle.adamw(a["p"], a["g"], a["m"], a["v"], a["lr"], a["beta1"], a["beta2"],
+                 a["eps"], a["weight_decay"], a["step"], nthreads=cores)
+    dt = time.perf_counter() - t0
+    rates["adamw_gbs"] = bytes_adamw(n) / dt / 1e9
+    sample = (f"LM-head GEMM rows 0..{rows_done - 1} of 8192 (x 50257 x 768, "
+              f"{flops / 1e9:.1f} GFLOP); xent {r4['logits'].shape[0]} rows x 50257 "
+              f"with dlogits; RMSNorm {r4['x'].shape[0]} rows; AdamW {n} params")
+    return rates, cores, sample
+
+
+def cpu_baseline(args):
+    rates, cores, sample = oracle_sample(budget_s=args.cpu_budget)
+    return {"value": round(rates["gemm_tflops"], 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "sample": sample,
+            "ops": {k: round(v, 4) for k, v in rates.items()}}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, on a bounded sample of
+    the workload each step."""
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        oracle_sample(budget_s=0.5)
+    vals, last = [], None
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        last = oracle_sample(budget_s=max(1.0, args.cpu_budget / max(args.steps, 1)))
+        vals.append(last[0]["gemm_tflops"])
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    rates, cores, sample = last
+    return {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "impl": "reference", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded numpy PCG64)",
+            "config": {"workload": WORKLOAD, "parallelism": f"replicas{world}",
+                       "sample_per_step": sample},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
+                             "cores": cores, "sample": sample,
+                             "ops": {k: round(v, 4) for k, v in rates.items()}},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle GEMM work in the CPU baseline")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

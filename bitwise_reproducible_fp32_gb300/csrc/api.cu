@@ -1,0 +1,193 @@
+// api.cu -- the C ABI of libdetfp32 (declared in include/detfp32.h).
+//
+// Every entry point checks the profile, the device and its arguments on the
+// host, then launches on the caller's stream and returns without
+// synchronising. A profile the library does not implement is refused by name
+// (DET_ERR_PROFILE), never run as something close: the "mojolearn" PyPI page,
+// section "Which families offer which tiers", asks for a named error rather
+// than a weaker result.
+#include <algorithm>
+#include <atomic>
+
+#include "det_internal.cuh"
+
+namespace det {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];       // 0: unknown
+std::atomic<int> g_device_ok[kMaxDevices];      // 0 unknown, 1 ok, 2 refused
+
+det_status check_profile(const det_profile_v1 *p) {
+    if (!p) return DET_ERR_INVALID_ARG;
+    if (p->version != DET_PROFILE_VERSION || p->k_chunk != uint32_t(kKChunk) ||
+        p->rms_lanes != uint32_t(kRmsLanes) || p->xent_lanes != uint32_t(kXentLanes) ||
+        p->lane_group != uint32_t(kGroup) || p->flags != 0)
+        return DET_ERR_PROFILE;
+    return DET_OK;
+}
+
+det_status check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DET_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return DET_ERR_UNSUPPORTED_DEVICE;
+    int st = g_device_ok[dev].load(std::memory_order_relaxed);
+    if (st == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return DET_ERR_CUDA;
+        g_sm_count[dev].store(sms, std::memory_order_relaxed);
+        st = (major == 10 && minor == 3) ? 1 : 2;
+        g_device_ok[dev].store(st, std::memory_order_relaxed);
+    }
+    return st == 1 ? DET_OK : DET_ERR_UNSUPPORTED_DEVICE;
+}
+
+det_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DET_OK : DET_ERR_CUDA; }
+
+constexpr int64_t kDimMax = 0x7fffffff;   // dimensions below 2^31
+}  // namespace
+
+int sm_count_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        const int n = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (n > 0) return n;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            sms > 0) {
+            g_sm_count[dev].store(sms, std::memory_order_relaxed);
+            return sms;
+        }
+    }
+    return 152;
+}
+
+}  // namespace det
+
+using namespace det;
+
+DET_API void det_profile_default(det_profile_v1 *p) {
+    if (!p) return;
+    p->version = DET_PROFILE_VERSION;
+    p->k_chunk = kKChunk;
+    p->rms_lanes = kRmsLanes;
+    p->xent_lanes = kXentLanes;
+    p->lane_group = kGroup;
+    p->flags = 0;
+}
+
+DET_API const char *det_status_string(int status) {
+    switch (status) {
+        case DET_OK: return "DET_OK";
+        case DET_ERR_INVALID_ARG: return "DET_ERR_INVALID_ARG: invalid argument";
+        case DET_ERR_PROFILE: return "DET_ERR_PROFILE: numerical profile not implemented";
+        case DET_ERR_UNSUPPORTED_DEVICE:
+            return "DET_ERR_UNSUPPORTED_DEVICE: current device is not sm_103";
+        case DET_ERR_ALIGNMENT: return "DET_ERR_ALIGNMENT: misaligned buffer";
+        case DET_ERR_WORKSPACE: return "DET_ERR_WORKSPACE: workspace too small";
+        case DET_ERR_TIMEOUT: return "DET_ERR_TIMEOUT: a bounded device wait gave up";
+        case DET_ERR_CUDA: return "DET_ERR_CUDA: CUDA runtime error";
+        default: return "unknown det_status";
+    }
+}
+
+DET_API det_status detgemm_f32(const det_profile_v1 *prof, int transA, int transB,
+                               int64_t M, int64_t N, int64_t K, const float *A,
+                               int64_t lda, const float *B, int64_t ldb, float *C,
+                               int64_t ldc, void *workspace, size_t workspace_bytes,
+                               det_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (M < 0 || N < 0 || K < 0 || M > kDimMax || N > kDimMax || K > kDimMax)
+        return DET_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DET_OK;
+    const int64_t a_row = transA ? M : K, b_row = transB ? K : N;
+    if (ldc < N || lda < std::max<int64_t>(a_row, 1) || ldb < std::max<int64_t>(b_row, 1))
+        return DET_ERR_INVALID_ARG;
+    if (!C || (K > 0 && (!A || !B))) return DET_ERR_INVALID_ARG;
+    const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+    if (tiles > kDimMax) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    GemmArgs a;
+    a.M = M; a.N = N; a.K = K; a.lda = lda; a.ldb = ldb; a.ldc = ldc;
+    a.A = A; a.B = B; a.C = C; a.transA = transA != 0; a.transB = transB != 0;
+    return from_cuda(launch_gemm(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detrmsnorm_f32(const det_profile_v1 *prof, int64_t rows, int64_t D,
+                                  const float *x, int64_t ldx, const float *gain,
+                                  float eps, float *y, int64_t ldy, float *inv_rms,
+                                  det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (rows < 0 || D < 1 || D > kDimMax) return DET_ERR_INVALID_ARG;
+    if (rows == 0) return DET_OK;
+    if (ldx < D || ldy < D || !x || !gain || !y) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_rmsnorm(rows, D, x, ldx, gain, eps, y, ldy, inv_rms,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detxent_f32(const det_profile_v1 *prof, int64_t rows, int64_t V,
+                               const float *logits, int64_t ld, const int32_t *labels,
+                               float *loss, float *loss_mean, float *dlogits, int64_t ldd,
+                               float dscale, int32_t *dev_status, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (rows < 0 || V < 1 || V > kDimMax) return DET_ERR_INVALID_ARG;
+    if (rows == 0) return DET_OK;
+    if (ld < V || !logits || !labels || !loss) return DET_ERR_INVALID_ARG;
+    if (dlogits && ldd < V) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_xent(rows, V, logits, ld, labels, loss, loss_mean, dlogits,
+                                 ldd, dscale, dev_status,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detadamw_f32(const det_profile_v1 *prof, int64_t n, float *p,
+                                const float *g, float *m, float *v,
+                                const det_adamw_hp *hp, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (n < 0 || !hp || hp->step < 1) return DET_ERR_INVALID_ARG;
+    if (n == 0) return DET_OK;
+    if (!p || !g || !m || !v) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_adamw(n, p, g, m, v, *hp, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static det_status exp_log(const det_profile_v1 *prof, int64_t n, const float *x, float *y,
+                          det_stream_t stream, int is_log) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (n < 0) return DET_ERR_INVALID_ARG;
+    if (n == 0) return DET_OK;
+    if (!x || !y) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_exp_map(n, x, y, is_log, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detexp_f32(const det_profile_v1 *prof, int64_t n, const float *x,
+                              float *y, det_stream_t stream) {
+    return exp_log(prof, n, x, y, stream, 0);
+}
+
+DET_API det_status detlog_f32(const det_profile_v1 *prof, int64_t n, const float *x,
+                              float *y, det_stream_t stream) {
+    return exp_log(prof, n, x, y, stream, 1);
+}
+
+DET_API det_status det_watchdog_status(int32_t *code, int clear) {
+    if (!code) return DET_ERR_INVALID_ARG;
+    unsigned int c = 0;
+    cudaError_t e = gemm_watchdog(&c, clear);
+    *code = int32_t(c);
+    return from_cuda(e);
+}

@@ -1,0 +1,113 @@
+// det_internal.cuh -- internal declarations and device helpers of libdetfp32.
+// Not installed; the public ABI is include/detfp32.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "detfp32.h"
+
+#define DET_API extern "C" __attribute__((visibility("default")))
+
+namespace det {
+
+// ---------------------------------------------------------------- profile v1
+constexpr int kKChunk = 256;     // GEMM k-chunk width
+constexpr int kRmsLanes = 32;    // chains per RMSNorm row / per mean
+constexpr int kXentLanes = 256;  // chains per cross-entropy row
+constexpr int kGroup = 4;        // consecutive elements per chain per sweep
+
+// A bounded device wait gives up after this long (the longest legitimate wait
+// in the library is one TMA tile, microseconds).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Watchdog bits (det_watchdog_status).
+constexpr unsigned int kWatchdogGemm = 1u;
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error; arguments are validated by
+// the C-ABI layer before these run.
+struct GemmArgs {
+    int64_t M, N, K, lda, ldb, ldc;
+    const float *A, *B;
+    float *C;
+    int transA, transB;
+};
+cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s);
+cudaError_t gemm_watchdog(unsigned int *code, int clear);
+
+cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
+                           const float *gain, float eps, float *y, int64_t ldy,
+                           float *inv_rms, cudaStream_t s);
+cudaError_t launch_xent(int64_t rows, int64_t V, const float *logits, int64_t ld,
+                        const int32_t *labels, float *loss, float *loss_mean,
+                        float *dlogits, int64_t ldd, float dscale,
+                        int32_t *dev_status, cudaStream_t s);
+cudaError_t launch_exp_map(int64_t n, const float *x, float *y, int is_log,
+                           cudaStream_t s);
+cudaError_t launch_adamw(int64_t n, float *p, const float *g, float *m, float *v,
+                         const det_adamw_hp &hp, cudaStream_t s);
+
+int sm_count_current_device();
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete, giving up after
+// kWaitLimitNs. Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// 2-D tiled TMA load into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map,
+                                            int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+}  // namespace det

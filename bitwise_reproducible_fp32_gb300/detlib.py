@@ -1,0 +1,249 @@
+"""ctypes binding over libdetfp32.so (include/detfp32.h).
+
+Argument marshalling only: each function takes torch CUDA tensors, reads their
+shapes, strides, data pointers and the current stream, and calls the C entry
+point of the same name. All arithmetic runs in the library's kernels. A missing
+library, a CPU tensor or a non-OK status raises; nothing falls back to another
+implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdetfp32.so")
+
+DET_OK = 0
+STATUS_NAMES = {0: "DET_OK", 1: "DET_ERR_INVALID_ARG", 2: "DET_ERR_PROFILE",
+                3: "DET_ERR_UNSUPPORTED_DEVICE", 4: "DET_ERR_ALIGNMENT",
+                5: "DET_ERR_WORKSPACE", 6: "DET_ERR_TIMEOUT", 7: "DET_ERR_CUDA"}
+
+
+class DetError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn}: {msg}")
+        self.status = status
+
+
+class Profile(ctypes.Structure):
+    """det_profile_v1."""
+    _fields_ = [("version", ctypes.c_uint32), ("k_chunk", ctypes.c_uint32),
+                ("rms_lanes", ctypes.c_uint32), ("xent_lanes", ctypes.c_uint32),
+                ("lane_group", ctypes.c_uint32), ("flags", ctypes.c_uint32)]
+
+
+class AdamWHP(ctypes.Structure):
+    """det_adamw_hp."""
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float),
+                ("beta2", ctypes.c_float), ("eps", ctypes.c_float),
+                ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+# (name, restype, argtypes) of every exported function
+_vp, _i64, _int, _f = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+_PROF = ctypes.POINTER(Profile)
+SIGNATURES = [
+    ("det_profile_default", None, [_PROF]),
+    ("det_status_string", ctypes.c_char_p, [_int]),
+    ("detgemm_f32", _int, [_PROF, _int, _int, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
+                           _vp, _i64, _vp, ctypes.c_size_t, _vp]),
+    ("detrmsnorm_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _f, _vp, _i64, _vp,
+                              _vp]),
+    ("detxent_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i64, _f,
+                           _vp, _vp]),
+    ("detadamw_f32", _int, [_PROF, _i64, _vp, _vp, _vp, _vp, ctypes.POINTER(AdamWHP),
+                            _vp]),
+    ("detexp_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
+    ("detlog_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
+    ("det_watchdog_status", _int, [ctypes.POINTER(ctypes.c_int32), _int]),
+]
+
+
+def load(path: str = LIB_PATH):
+    """Loads the library (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        for name, res, args in SIGNATURES:
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def det_profile_default() -> Profile:
+    p = Profile()
+    load().det_profile_default(ctypes.byref(p))
+    return p
+
+
+def det_status_string(status: int) -> str:
+    return load().det_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != DET_OK:
+        raise DetError(fn, status, det_status_string(status))
+
+
+def _prof(profile):
+    return ctypes.byref(profile if profile is not None else det_profile_default())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p()
+
+
+def _cuda_f32(t, name, ndim=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32 (the profile is FP32 only), got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D")
+    if ndim == 2 and t.numel() > 0 and t.stride(1) != 1:
+        raise ValueError(f"{name} rows must be contiguous (stride(1) == 1)")
+    if ndim in (None, 1) and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ld(t):
+    return t.stride(0) if t.dim() == 2 and t.shape[0] > 0 else max(t.shape[-1], 1)
+
+
+# ---------------------------------------------------------------- GEMM
+def detgemm_f32(A, B, C=None, transA=False, transB=False, profile=None, stream=None):
+    """C = op(A) @ op(B) under the profile. A, B row-major 2-D float32 CUDA
+    tensors (transA: A is K x M; transB: B is N x K). Returns C."""
+    import torch
+    _cuda_f32(A, "A", 2)
+    _cuda_f32(B, "B", 2)
+    M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])
+    Kb, N = (B.shape[1], B.shape[0]) if transB else (B.shape[0], B.shape[1])
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _cuda_f32(C, "C", 2)
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {M} x {N}")
+    st = load().detgemm_f32(_prof(profile), int(bool(transA)), int(bool(transB)), M, N,
+                            K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
+                            ctypes.c_void_p(), 0, _stream(stream))
+    _check("detgemm_f32", st)
+    return C
+
+
+# ---------------------------------------------------------------- RMSNorm
+def detrmsnorm_f32(x, gain, eps=1e-6, y=None, inv_rms=None, want_inv_rms=True,
+                   profile=None, stream=None):
+    """Returns (y, inv_rms or None)."""
+    import torch
+    _cuda_f32(x, "x", 2)
+    _cuda_f32(gain, "gain", 1)
+    rows, D = x.shape
+    if y is None:
+        y = torch.empty((rows, D), dtype=torch.float32, device=x.device)
+    _cuda_f32(y, "y", 2)
+    if inv_rms is None and want_inv_rms:
+        inv_rms = torch.empty(rows, dtype=torch.float32, device=x.device)
+    st = load().detrmsnorm_f32(_prof(profile), rows, D, _ptr(x), _ld(x), _ptr(gain),
+                               ctypes.c_float(eps), _ptr(y), _ld(y), _ptr(inv_rms),
+                               _stream(stream))
+    _check("detrmsnorm_f32", st)
+    return y, inv_rms
+
+
+# ---------------------------------------------------------------- cross-entropy
+def detxent_f32(logits, labels, loss=None, want_mean=False, loss_mean=None,
+                dlogits=None, want_dlogits=False, dscale=None, dev_status=None,
+                profile=None, stream=None):
+    """Returns (loss, loss_mean or None, dlogits or None). dscale defaults to
+    1/rows. dev_status: optional int32 CUDA tensor of one element."""
+    import torch
+    _cuda_f32(logits, "logits", 2)
+    if labels.dtype != torch.int32 or labels.device.type != "cuda":
+        raise TypeError("labels must be an int32 CUDA tensor")
+    rows, V = logits.shape
+    if loss is None:
+        loss = torch.empty(rows, dtype=torch.float32, device=logits.device)
+    if loss_mean is None and want_mean:
+        loss_mean = torch.empty(1, dtype=torch.float32, device=logits.device)
+    if dlogits is None and want_dlogits:
+        dlogits = torch.empty((rows, V), dtype=torch.float32, device=logits.device)
+    if dscale is None:
+        dscale = 1.0 / max(rows, 1)
+    if dev_status is not None and (dev_status.dtype != torch.int32
+                                   or dev_status.device.type != "cuda"):
+        raise TypeError("dev_status must be an int32 CUDA tensor")
+    st = load().detxent_f32(_prof(profile), rows, V, _ptr(logits), _ld(logits),
+                            _ptr(labels), _ptr(loss), _ptr(loss_mean), _ptr(dlogits),
+                            _ld(dlogits) if dlogits is not None else V,
+                            ctypes.c_float(dscale), _ptr(dev_status), _stream(stream))
+    _check("detxent_f32", st)
+    return loss, loss_mean, dlogits
+
+
+# ---------------------------------------------------------------- AdamW
+def detadamw_f32(p, g, m, v, lr, beta1, beta2, eps, weight_decay, step,
+                 profile=None, stream=None):
+    """In-place AdamW update of p, m, v (1-D float32 CUDA tensors)."""
+    for t, name in ((p, "p"), (g, "g"), (m, "m"), (v, "v")):
+        _cuda_f32(t, name, 1)
+    n = p.numel()
+    if not (g.numel() == m.numel() == v.numel() == n):
+        raise ValueError("p, g, m, v must have the same length")
+    hp = AdamWHP(lr, beta1, beta2, eps, weight_decay, int(step))
+    st = load().detadamw_f32(_prof(profile), n, _ptr(p), _ptr(g), _ptr(m), _ptr(v),
+                             ctypes.byref(hp), _stream(stream))
+    _check("detadamw_f32", st)
+    return p, m, v
+
+
+# ---------------------------------------------------------------- exp / log
+def detexp_f32(x, y=None, profile=None, stream=None):
+    import torch
+    _cuda_f32(x, "x")
+    if y is None:
+        y = torch.empty_like(x)
+    st = load().detexp_f32(_prof(profile), x.numel(), _ptr(x), _ptr(y), _stream(stream))
+    _check("detexp_f32", st)
+    return y
+
+
+def detlog_f32(x, y=None, profile=None, stream=None):
+    import torch
+    _cuda_f32(x, "x")
+    if y is None:
+        y = torch.empty_like(x)
+    st = load().detlog_f32(_prof(profile), x.numel(), _ptr(x), _ptr(y), _stream(stream))
+    _check("detlog_f32", st)
+    return y
+
+
+def det_watchdog_status(clear: bool = False) -> int:
+    code = ctypes.c_int32()
+    _check("det_watchdog_status",
+           load().det_watchdog_status(ctypes.byref(code), int(bool(clear))))
+    return code.value

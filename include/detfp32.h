@@ -1,0 +1,215 @@
+/*
+ * detfp32.h -- C ABI of the bit-exact fixed-order FP32 library for GB300
+ * (sm_103a): libdetfp32.so.
+ *
+ * What it computes. Four operations of FP32 transformer training, under one
+ * frozen numerical profile, so that the result bits depend only on the inputs,
+ * the shapes and the profile version. They do not depend on the launch
+ * configuration, the stream, the tiling or the run. The profile fixes
+ * reduction order, partitioning, FMA policy, flush-to-zero behaviour, the
+ * spellings of exp and log, and tie rules ("mojolearn" PyPI page, section
+ * "What bitwise identity means, and why it is not the default"; the same list
+ * in "The exact scope of the claim"). Profile v1's values are stated at each
+ * entry point below.
+ *
+ * Conventions shared by every entry point.
+ *  - Pointers named as device pointers must be device memory of the current
+ *    CUDA device (cudaMalloc, or torch's caching allocator). The caller owns
+ *    all memory. The library allocates nothing and keeps no state between
+ *    calls, except a per-device watchdog word (det_watchdog_status).
+ *  - Matrices are row-major float32 with an explicit row stride (ld*, in
+ *    elements, >= the row length).
+ *  - `stream` is a cudaStream_t; NULL means the legacy default stream. Every
+ *    call is asynchronous on that stream: it validates its arguments on the
+ *    host, launches, and returns without synchronising.
+ *  - The return value is a det_status. Argument, profile and device checks
+ *    are synchronous. A failed launch returns DET_ERR_CUDA. Nothing throws or
+ *    exits across the ABI.
+ *  - float32 only; there is no other precision and no fallback path. The
+ *    pages' FP32-only claim is in "The exact scope of the claim".
+ *  - Subnormals are kept everywhere: no flush-to-zero, no fast math.
+ */
+#ifndef DETFP32_H
+#define DETFP32_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Identical to cudaStream_t. */
+typedef struct CUstream_st *det_stream_t;
+
+#define DET_PROFILE_VERSION 1u
+
+/* The numerical profile the caller asks for. Version 1 is the only one
+ * implemented; every field must hold its v1 value, or the call is refused
+ * with DET_ERR_PROFILE. A change to any value would change result bits, so
+ * the library never runs an unlisted profile. The pages require the same:
+ * refusal by a named error, never a weaker result ("mojolearn" PyPI page,
+ * "Which families offer which tiers"). */
+typedef struct det_profile_v1 {
+    uint32_t version;     /* 1 */
+    uint32_t k_chunk;     /* 256: GEMM k-chunk width */
+    uint32_t rms_lanes;   /* 32: chains per RMSNorm row (and per mean) */
+    uint32_t xent_lanes;  /* 256: chains per cross-entropy row */
+    uint32_t lane_group;  /* 4: consecutive elements a chain owns per sweep */
+    uint32_t flags;       /* 0: no FTZ, no fast math (no other value exists) */
+} det_profile_v1;
+
+typedef enum det_status {
+    DET_OK = 0,
+    DET_ERR_INVALID_ARG = 1,        /* null pointer, negative size, ld too small */
+    DET_ERR_PROFILE = 2,            /* profile version or field not implemented */
+    DET_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+    DET_ERR_ALIGNMENT = 4,          /* reserved */
+    DET_ERR_WORKSPACE = 5,          /* workspace too small or misaligned */
+    DET_ERR_TIMEOUT = 6,            /* a device-side bounded wait gave up */
+    DET_ERR_CUDA = 7                /* a CUDA runtime call or launch failed */
+} det_status;
+
+/* Fills *p with profile v1. */
+void det_profile_default(det_profile_v1 *p);
+
+/* Static description of a status code (never NULL). */
+const char *det_status_string(int status);
+
+/* Fixed-order GEMM: C = op(A) * op(B), with op(X) = X or X^T.
+ *
+ * Profile v1 (a1-a3): for each C[i,j] and each 256-wide chunk c of k
+ * ([256c, min(256c+256, K))), P_c is a sequential fmaf chain that starts at
+ * +0.0f and runs over k in ascending order: acc = fmaf(opA[i,k], opB[k,j], acc).
+ * Then C[i,j] = P_0 + P_1 + ... summed left to right (the first partial taken
+ * as is). K == 0 gives C = +0. The bits depend only on (M, N, K, the operand
+ * values, the profile), never on tiling or launch configuration.
+ *
+ * transA == 0: A is M x K row-major, row stride lda >= K.
+ * transA != 0: A is stored K x M row-major (lda >= M), and op(A) = A^T; this
+ *              is the weight-gradient form dW = X^T dY (contraction over the
+ *              tokens).
+ * transB == 0: B is K x N row-major, ldb >= N.
+ * transB != 0: B is stored N x K row-major (ldb >= K), op(B) = B^T; this is
+ *              the [out_features, in_features] Linear layout.
+ * C: M x N row-major, ldc >= N, device pointer, must not overlap A or B.
+ * workspace / workspace_bytes: reserved for split-K, pass NULL / 0.
+ *
+ * Errors: DET_ERR_INVALID_ARG for negative sizes, a dimension >= 2^31, an ld
+ * below its row length or null pointers with nonzero sizes. A TMA wait that
+ * exceeds its bound makes the kernel skip its stores and record a code that
+ * det_watchdog_status() returns. */
+det_status detgemm_f32(const det_profile_v1 *prof, int transA, int transB,
+                       int64_t M, int64_t N, int64_t K,
+                       const float *A, int64_t lda,
+                       const float *B, int64_t ldb,
+                       float *C, int64_t ldc,
+                       void *workspace, size_t workspace_bytes,
+                       det_stream_t stream);
+
+/* RMSNorm over `rows` rows of D floats: y = (x * r) * gain, with
+ * r = 1.0f / sqrtf(ss / (float)D + eps). "MojoLearn 162M" model card, table
+ * "Compared with GPT-3 Small": RMSNorm, eps 1e-6, pre-norm.
+ *
+ * Profile v1 (a4): ss is the sum of squares over 32 chains. Chain l owns the
+ * 4-element groups g of the row with g mod 32 == l and accumulates
+ * s_l = fmaf(x_j, x_j, s_l) from +0 in ascending j. The chains are then folded
+ * by an xor butterfly with offsets 16, 8, 4, 2, 1 (s_l = s_l + s_{l^off}). The
+ * divisions and the square root are IEEE round-to-nearest; there is no rsqrt.
+ *
+ * x: rows x D, row stride ldx >= D (device). gain: D floats (device).
+ * y: rows x D, ldy >= D (device; may equal x when ldy == ldx, in place).
+ * inv_rms: rows floats receiving r (device) or NULL. D must be >= 1; rows may
+ * be 0 (no work). */
+det_status detrmsnorm_f32(const det_profile_v1 *prof, int64_t rows, int64_t D,
+                          const float *x, int64_t ldx, const float *gain,
+                          float eps, float *y, int64_t ldy, float *inv_rms,
+                          det_stream_t stream);
+
+/* Softmax cross-entropy per row of V logits, with an optional gradient and an
+ * optional mean. Cross entropy is on the verified path in "mojolearn"
+ * (andrewhendel.com), "Handing training off between vendors".
+ *
+ * Profile v1 (a5): m = max_j x_j (order-free; bit-inert for finite inputs).
+ * e_j = exp(x_j - m), with the profile's exp (detexp_f32). S is the sum of the
+ * e_j over 256 chains (chain l owns the 4-element groups g with
+ * g mod 256 == l, plain adds from +0 in ascending j), folded by the xor
+ * butterfly 16, 8, 4, 2, 1, 32, 64, 128. loss = log(S) - (x_y - m), with the
+ * profile's log (detlog_f32).
+ * dlogits (optional): d_j = (e_j * (1.0f / S) - [j == y]) * dscale.
+ * loss_mean (optional): the 32-chain tree (groups of 4, plain adds) over the
+ * rows' losses, divided by (float)rows.
+ *
+ * logits: rows x V, row stride ld >= V (device; the rows need not be 16-byte
+ *         aligned).
+ * labels: rows int32 (device).
+ * loss:   rows floats (device).
+ * loss_mean: 1 float (device) or NULL.
+ * dlogits: rows x V, stride ldd >= V (device) or NULL; it may alias logits
+ *          when ldd == ld.
+ * dev_status: one int32 (device) or NULL. A label outside [0, V) sets bit 0
+ *          (atomic OR; the library never clears it), and that row's loss and
+ *          dlogits row are NaN.
+ * V >= 1; rows may be 0. */
+det_status detxent_f32(const det_profile_v1 *prof, int64_t rows, int64_t V,
+                       const float *logits, int64_t ld, const int32_t *labels,
+                       float *loss, float *loss_mean, float *dlogits,
+                       int64_t ldd, float dscale, int32_t *dev_status,
+                       det_stream_t stream);
+
+/* AdamW hyperparameters for one update (host struct, read during the call).
+ * "MojoLearn 162M" model card, table "Training": AdamW, beta (0.9, 0.95),
+ * eps 1e-8, weight decay 0.1, no gradient clipping; lr from the schedule. */
+typedef struct det_adamw_hp {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay;
+    int64_t step;         /* 1-based step number t (>= 1) */
+} det_adamw_hp;
+
+/* One AdamW update of n parameters, in place on p, m, v (device arrays of n
+ * floats; g read-only). Decoupled decay applied to every element.
+ *
+ * Profile v1 (a6): bc1 = 1 - beta1^t and bc2 = 1 - beta2^t, with beta^t the
+ * product of t-1 sequential float multiplications; then per element
+ *   m' = fmaf(beta1, m, (1 - beta1) * g)
+ *   v' = fmaf(beta2, v, (1 - beta2) * (g * g))
+ *   u  = (m' / bc1) / (sqrtf(v' / bc2) + eps)
+ *   p' = fmaf(-lr, u, p * (1 - lr * weight_decay))
+ * where (1 - beta1), (1 - beta2) and (1 - lr * weight_decay) are rounded to
+ * float once each. n may be 0. */
+det_status detadamw_f32(const det_profile_v1 *prof, int64_t n, float *p,
+                        const float *g, float *m, float *v,
+                        const det_adamw_hp *hp, det_stream_t stream);
+
+/* Elementwise profile exp / log over n floats (device x -> device y; y may
+ * equal x). These are the spellings the cross-entropy uses
+ * ("mojolearn" PyPI page, section "What bitwise identity means...": the
+ * spellings of exp and log are part of the profile).
+ *
+ * exp (v1): NaN -> NaN; x > 0x1.62e42ep+6 -> +Inf; x < -104 -> +0; otherwise
+ * n = rintf(x * log2(e)) (ties to even), r = x - n ln2 in two fmaf steps
+ * (ln2 split in two floats), a degree-7 Taylor polynomial in r by fmaf
+ * Horner, then scaling by 2^n with a single rounding.
+ * log (v1): x < 0 or NaN -> NaN, 0 -> -Inf, +Inf -> +Inf; otherwise
+ * x = 2^e f with f in (sqrt(1/2), sqrt 2), u = f - 1, s = u / (2 + u),
+ * log f = u - (h - s (h + R)) with h = u^2/2 and R the atanh series to z^5
+ * in z = s^2, and log x = e ln2 + log f by two fmaf steps. */
+det_status detexp_f32(const det_profile_v1 *prof, int64_t n, const float *x,
+                      float *y, det_stream_t stream);
+det_status detlog_f32(const det_profile_v1 *prof, int64_t n, const float *x,
+                      float *y, det_stream_t stream);
+
+/* Reads, and optionally clears, the current device's watchdog word.
+ * *code == 0 means no bounded device wait has ever given up; otherwise bit k
+ * identifies the kernel family that gave up (bit 0: GEMM operand staging).
+ * This call synchronises the device (it copies from device memory). */
+det_status det_watchdog_status(int32_t *code, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DETFP32_H */

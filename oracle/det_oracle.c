@@ -347,7 +347,8 @@ static void xent_rows(int64_t lo, int64_t hi, int tix, void *c) {
             continue;
         }
         float m = x[0];
-        for (int64_t j = 1; j < q->V; ++j) if (x[j] > m) m = x[j];
+        /* max, NaN-propagating: a NaN anywhere in the row makes m NaN */
+        for (int64_t j = 1; j < q->V; ++j) if (x[j] > m || x[j] != x[j]) m = x[j];
         for (int l = 0; l < q->lanes; ++l) s[l] = 0.0f;
         for (int64_t j = 0; j < q->V; ++j) {
             int l = (int)((j / q->group) % q->lanes);

@@ -1,0 +1,113 @@
+"""The C-ABI library builds, loads without a GPU, exports every function that
+include/detfp32.h declares, and refuses bad profiles and arguments on the host
+before touching any device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bitwise_reproducible_fp32_gb300 import build, detlib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "detfp32.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return detlib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(det\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("detgemm_f32", "detrmsnorm_f32", "detxent_f32", "detadamw_f32",
+                 "detexp_f32", "detlog_f32", "det_profile_default",
+                 "det_status_string", "det_watchdog_status"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the binding wraps each of them under the same name
+    wrapped = {n for n, _, _ in detlib.SIGNATURES}
+    assert set(declared_functions()) <= wrapped
+
+
+def test_only_the_boundary_is_exported(lib):
+    # internal C++ symbols are hidden (-fvisibility=hidden); only det* is public
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", detlib.LIB_PATH],
+                         capture_output=True, text=True).stdout
+    public = [l.split()[-1] for l in out.splitlines() if " T " in l]
+    assert public and all(n.startswith("det") for n in public), public
+
+
+def test_profile_default_and_strings(lib):
+    p = detlib.det_profile_default()
+    assert (p.version, p.k_chunk, p.rms_lanes, p.xent_lanes, p.lane_group, p.flags) == (
+        1, 256, 32, 256, 4, 0)
+    assert detlib.det_status_string(0) == "DET_OK"
+    assert "PROFILE" in detlib.det_status_string(2)
+    assert detlib.det_status_string(99) == "unknown det_status"
+
+
+@pytest.mark.parametrize("field,value", [("version", 2), ("k_chunk", 128),
+                                         ("rms_lanes", 64), ("xent_lanes", 32),
+                                         ("lane_group", 1), ("flags", 1)])
+def test_unknown_profile_is_refused_by_name(lib, field, value):
+    p = detlib.det_profile_default()
+    setattr(p, field, value)
+    null = ctypes.c_void_p()
+    st = lib.detgemm_f32(ctypes.byref(p), 0, 0, 4, 4, 4, null, 4, null, 4, null, 4,
+                         null, 0, null)
+    assert st == 2
+    hp = detlib.AdamWHP(1e-3, 0.9, 0.95, 1e-8, 0.1, 1)
+    assert lib.detadamw_f32(ctypes.byref(p), 4, null, null, null, null,
+                            ctypes.byref(hp), null) == 2
+    assert lib.detexp_f32(ctypes.byref(p), 4, null, null, null) == 2
+    assert lib.detxent_f32(ctypes.byref(p), 1, 4, null, 4, null, null, null, null, 4,
+                           ctypes.c_float(1.0), null, null) == 2
+    assert lib.detrmsnorm_f32(ctypes.byref(p), 1, 4, null, 4, null,
+                              ctypes.c_float(1e-6), null, 4, null, null) == 2
+
+
+def test_bad_arguments_are_refused_on_the_host(lib):
+    p = ctypes.byref(detlib.det_profile_default())
+    null = ctypes.c_void_p()
+    dummy = ctypes.c_void_p(0x1000)
+    # negative sizes, ld below the row length, null pointers, >= 2^31 dims
+    assert lib.detgemm_f32(p, 0, 0, -1, 4, 4, dummy, 4, dummy, 4, dummy, 4, null, 0, null) == 1
+    assert lib.detgemm_f32(p, 0, 0, 4, 4, 8, dummy, 7, dummy, 4, dummy, 4, null, 0, null) == 1
+    assert lib.detgemm_f32(p, 1, 0, 9, 4, 8, dummy, 8, dummy, 4, dummy, 4, null, 0, null) == 1
+    assert lib.detgemm_f32(p, 0, 1, 4, 4, 8, dummy, 8, dummy, 7, dummy, 4, null, 0, null) == 1
+    assert lib.detgemm_f32(p, 0, 0, 4, 4, 8, null, 8, dummy, 4, dummy, 4, null, 0, null) == 1
+    assert lib.detgemm_f32(p, 0, 0, 2 ** 31, 4, 8, dummy, 8, dummy, 4, dummy, 4, null, 0,
+                           null) == 1
+    # empty problems are a successful no-op without any device call
+    assert lib.detgemm_f32(p, 0, 0, 0, 4, 8, null, 8, null, 4, null, 4, null, 0, null) == 0
+    assert lib.detrmsnorm_f32(p, 3, 0, dummy, 4, dummy, ctypes.c_float(1e-6), dummy, 4,
+                              null, null) == 1
+    assert lib.detrmsnorm_f32(p, 0, 8, null, 8, null, ctypes.c_float(1e-6), null, 8, null,
+                              null) == 0
+    assert lib.detxent_f32(p, 2, 0, dummy, 4, dummy, dummy, null, null, 4,
+                           ctypes.c_float(1.0), null, null) == 1
+    assert lib.detxent_f32(p, 2, 8, dummy, 8, dummy, dummy, null, dummy, 7,
+                           ctypes.c_float(1.0), null, null) == 1
+    hp = detlib.AdamWHP(1e-3, 0.9, 0.95, 1e-8, 0.1, 0)
+    assert lib.detadamw_f32(p, 4, dummy, dummy, dummy, dummy, ctypes.byref(hp), null) == 1
+    assert lib.detexp_f32(p, -1, dummy, dummy, null) == 1
+    assert lib.detexp_f32(p, 0, null, null, null) == 0
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(TypeError):
+        detlib.detgemm_f32(torch.zeros(2, 2), torch.zeros(2, 2))
