@@ -87,6 +87,23 @@ def bytes_adamw(n):
     return n * 28
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings (every rank gets the result). The
+    only collective of the benchmark: the path itself has no exchange, each
+    rank runs an independent replica of the step."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def replica_throughput(work_per_rank, world, slowest_ms):
+    """Whole-job rate: the work all replicas did over the slowest one's time."""
+    return work_per_rank * world / (slowest_ms / 1e3)
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -177,6 +194,11 @@ def run_ours(args, rank, world, local_rank):
     g_dw = [(p, dev_of(p["A"]), dev_of(p["B"])) for p in dw]
     c_fwd = [torch.empty(gemm_dims(p)[:2], dtype=torch.float32, device=dev) for p in fwd]
     c_dw = [torch.empty(gemm_dims(p)[:2], dtype=torch.float32, device=dev) for p in dw]
+    # caller-owned split-K workspaces (None where the library needs none)
+    ws_fwd = [detlib.gemm_workspace(*gemm_dims(p), p["transA"], p["transB"], device=dev)
+              for p in fwd]
+    ws_dw = [detlib.gemm_workspace(*gemm_dims(p), p["transA"], p["transB"], device=dev)
+             for p in dw]
     x4, gain4 = up(r4["x"]), up(r4["gain"])
     y4 = torch.empty_like(x4)
     inv4 = torch.empty(x4.shape[0], dtype=torch.float32, device=dev)
@@ -198,7 +220,9 @@ def run_ours(args, rank, world, local_rank):
     gemm_flops_dw = [inputs.flops_gemm(*gemm_dims(p)) for p in dw]
     gemm_flops = sum(gemm_flops_fwd) + sum(gemm_flops_dw)
     lm_idx = [p["name"] for p in fwd].index("lm_head")
-    launches_per_step = 1 + len(fwd) + 2 + len(dw) + 1
+    # one launch per GEMM, plus the split-K second pass where a workspace is used
+    launches_per_step = (1 + len(fwd) + sum(w is not None for w in ws_fwd) + 2 + len(dw)
+                         + sum(w is not None for w in ws_dw) + 1)
 
     segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "gemm_dw", "adamw"]
 
@@ -212,16 +236,19 @@ def run_ours(args, rank, world, local_rank):
         for i, (p, A, B) in enumerate(g_fwd):
             if i == lm_idx:
                 continue
-            detlib.detgemm_f32(A, B, c_fwd[i], transA=p["transA"], transB=p["transB"])
+            detlib.detgemm_f32(A, B, c_fwd[i], transA=p["transA"], transB=p["transB"],
+                               workspace=ws_fwd[i])
         mark(2)
         p, A, B = g_fwd[lm_idx]
-        detlib.detgemm_f32(A, B, c_fwd[lm_idx], transA=p["transA"], transB=p["transB"])
+        detlib.detgemm_f32(A, B, c_fwd[lm_idx], transA=p["transA"], transB=p["transB"],
+                           workspace=ws_fwd[lm_idx])
         mark(3)
         detlib.detxent_f32(logits, labels, loss=loss, loss_mean=lmean, dlogits=dlog,
                            dscale=1.0 / rows4, dev_status=status)
         mark(4)
         for i, (p, A, B) in enumerate(g_dw):
-            detlib.detgemm_f32(A, B, c_dw[i], transA=p["transA"], transB=p["transB"])
+            detlib.detgemm_f32(A, B, c_dw[i], transA=p["transA"], transB=p["transB"],
+                               workspace=ws_dw[i])
         mark(5)
         detlib.detadamw_f32(P, G, Mm, Vv, **hp)
         mark(6)
@@ -263,12 +290,10 @@ def run_ours(args, rank, world, local_rank):
 
     # max over ranks of the per-step device times
     if distributed:
-        t = torch.tensor([step_ms, gemm_ms, lm_ms] + [seg_ms[s] for s in segs],
-                         dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, gemm_ms, lm_ms = t[0].item(), t[1].item(), t[2].item()
+        vals = max_over_ranks([step_ms, gemm_ms, lm_ms] + [seg_ms[s] for s in segs], dev)
+        step_ms, gemm_ms, lm_ms = vals[:3]
         for i, s in enumerate(segs):
-            seg_ms[s] = t[3 + i].item()
+            seg_ms[s] = vals[3 + i]
 
     if int(status.item()) != 0:
         raise SystemExit("cross-entropy reported an out-of-range label")
@@ -282,7 +307,7 @@ def run_ours(args, rank, world, local_rank):
         smax = float(peaks.get("sm_max_mhz", 2070.0))
         fma_peak = fp32_peak_tflops(smax)
         per = lambda s: seg_ms[s] / args.steps / 1e3   # seconds a step
-        gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12 * world
+        gemm_tflops = replica_throughput(gemm_flops, world, gemm_ms) / 1e12
         lm_flops = gemm_flops_fwd[lm_idx]
         lm_tflops = lm_flops / (lm_ms / 1e3) / 1e12
         ops = {
@@ -397,6 +422,8 @@ def e2e_leg(args, dev, host, gemm_flops):
 
     outs_dev = [torch.empty(gemm_dims(p)[:2], dtype=torch.float32, device=dev)
                 for p in fwd + dw]
+    wss = [detlib.gemm_workspace(*gemm_dims(p), p["transA"], p["transB"], device=dev)
+           for p in fwd + dw]
     rows4, D4 = r4["x"].shape
     V = r4["logits"].shape[1]
     y4 = torch.empty((rows4, D4), dtype=torch.float32, device=dev)
@@ -417,7 +444,7 @@ def e2e_leg(args, dev, host, gemm_flops):
         g = lambda a: pin(a)[1]
         for i, p in enumerate(fwd + dw):
             detlib.detgemm_f32(g(p["A"]), g(p["B"]), outs_dev[i], transA=p["transA"],
-                               transB=p["transB"])
+                               transB=p["transB"], workspace=wss[i])
         detlib.detrmsnorm_f32(g(r4["x"]), g(r4["gain"]), float(r4["eps"]), y=y4,
                               inv_rms=inv4)
         detlib.detxent_f32(g(r4["logits"]), g(r4["labels"]), loss=loss, loss_mean=lmean,
@@ -526,8 +553,8 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")

@@ -96,13 +96,27 @@ DET_API const char *det_status_string(int status) {
     }
 }
 
+DET_API det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA,
+                                           int transB, int64_t M, int64_t N, int64_t K,
+                                           size_t *bytes) {
+    (void)transA;
+    (void)transB;
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (!bytes || M < 0 || N < 0 || K < 0 || M > kDimMax || N > kDimMax || K > kDimMax)
+        return DET_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (M == 0 || N == 0 || K == 0) return DET_OK;
+    if ((st = check_device()) != DET_OK) return st;
+    *bytes = gemm_plan(M, N, K, sm_count_current_device()).workspace_bytes;
+    return DET_OK;
+}
+
 DET_API det_status detgemm_f32(const det_profile_v1 *prof, int transA, int transB,
                                int64_t M, int64_t N, int64_t K, const float *A,
                                int64_t lda, const float *B, int64_t ldb, float *C,
                                int64_t ldc, void *workspace, size_t workspace_bytes,
                                det_stream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
     if (M < 0 || N < 0 || K < 0 || M > kDimMax || N > kDimMax || K > kDimMax)
@@ -118,7 +132,8 @@ DET_API det_status detgemm_f32(const det_profile_v1 *prof, int transA, int trans
     GemmArgs a;
     a.M = M; a.N = N; a.K = K; a.lda = lda; a.ldb = ldb; a.ldc = ldc;
     a.A = A; a.B = B; a.C = C; a.transA = transA != 0; a.transB = transB != 0;
-    return from_cuda(launch_gemm(a, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_gemm(a, workspace, workspace_bytes,
+                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
 DET_API det_status detrmsnorm_f32(const det_profile_v1 *prof, int64_t rows, int64_t D,
@@ -145,6 +160,7 @@ DET_API det_status detxent_f32(const det_profile_v1 *prof, int64_t rows, int64_t
     if (rows == 0) return DET_OK;
     if (ld < V || !logits || !labels || !loss) return DET_ERR_INVALID_ARG;
     if (dlogits && ldd < V) return DET_ERR_INVALID_ARG;
+    if (dlogits && dlogits == logits && ldd != ld) return DET_ERR_INVALID_ARG;
     if ((st = check_device()) != DET_OK) return st;
     return from_cuda(launch_xent(rows, V, logits, ld, labels, loss, loss_mean, dlogits,
                                  ldd, dscale, dev_status,

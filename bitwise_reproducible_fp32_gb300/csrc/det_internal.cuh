@@ -34,7 +34,16 @@ struct GemmArgs {
     float *C;
     int transA, transB;
 };
-cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s);
+struct GemmPlan {
+    int split;             // 1: chunk partials through the workspace
+    int units_per_tile;    // chunk groups a tile is cut into
+    int kt_per_unit;       // k-tiles a unit computes
+    int nchunks;
+    size_t workspace_bytes;
+};
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms);
+cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_bytes,
+                        cudaStream_t s);
 cudaError_t gemm_watchdog(unsigned int *code, int clear);
 
 cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,

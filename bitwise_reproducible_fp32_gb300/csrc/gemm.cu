@@ -14,18 +14,28 @@
 // bits require FFMA.
 //
 // Design for GB300:
-//  * CTA tile 128 x 128, k-tile 32 (divides the 256-wide chunk, so chunk
-//    boundaries fall on k-tile boundaries), 256 threads, 8 x 8 outputs per
+//  * Shared memory bandwidth sets the register tile. A 16-byte shared load
+//    costs 4 wavefronts of the SM's one-wavefront-a-clock pipe, while the 4
+//    sub-partitions issue 4 warp-FFMAs a clock. With a TM x TN register tile a
+//    thread loads TM + TN floats per k for TM*TN FFMAs, so 8 x 8 saturates the
+//    pipe exactly at full FFMA rate; 16 x 8 leaves it 25% headroom. So: CTA
+//    tile 256 x 128, 256 threads (2 x 4 warps of 128 x 32), 16 x 8 outputs a
 //    thread, one CTA per SM (up to 255 registers a thread).
-//  * Operand tiles arrive by TMA (cp.async.bulk.tensor) into a 4-stage ring
-//    with one mbarrier per stage; thread 0 is the producer. Tiles whose k is
-//    the contiguous dimension use the 128-byte swizzle, so 16-byte shared loads
-//    of 4 consecutive k for 8 different rows are bank-conflict free; tiles
-//    whose m/n is contiguous are stored plain and read as float4 along m/n.
-//  * Per 4-wide k group a thread issues 16 LDS.128 and 256 FFMA (6% of issue).
+//  * k-tile 32 divides the 256-wide chunk, so chunk boundaries fall on k-tile
+//    boundaries. Operand tiles arrive by TMA (cp.async.bulk.tensor) into a
+//    2-stage ring (48 KB a stage) with one mbarrier per stage; thread 0 is the
+//    producer. Tiles whose k is contiguous use the 128-byte swizzle, so
+//    16-byte loads of 4 consecutive k from 8 different rows are free of bank
+//    conflicts; tiles whose m/n is contiguous are stored plain and read as
+//    float4 along m/n.
+//  * Per 4-wide k group a thread issues 24 LDS.128 and 512 FFMA; one operand's
+//    4-k fragment is held while the other streams.
 //  * Chunk partials: the running left-to-right total lives in shared memory
-//    (64 KB), touched once per 256 k, which keeps registers for the operand
-//    fragments.
+//    (128 KB), touched once per 256 k, which keeps registers for the
+//    accumulators and fragments.
+//  * Persistent: one CTA per SM walks its tiles; the k-tiles of consecutive
+//    tiles share the stage ring, so the next tile's loads overlap the
+//    epilogue.
 //  * Operands whose base or row stride is not 16-byte aligned (TMA cannot
 //    describe them) take the same kernel with a plain-load producer; the
 //    arithmetic, and so the bits, are identical.
@@ -42,29 +52,41 @@
 namespace det {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int BK = 32;
-constexpr int STAGES = 4;
+#ifndef DET_GEMM_TM
+#define DET_GEMM_TM 16
+#endif
+#ifndef DET_GEMM_STAGES
+#define DET_GEMM_STAGES 2
+#endif
+constexpr int TM = DET_GEMM_TM;                 // outputs a thread: TM x TN
+constexpr int TN = 8;
+constexpr int WTM = 8 * TM;                     // warp tile rows (8 lanes along m)
+constexpr int BM = 2 * WTM;                     // CTA tile rows (op(A) rows)
+constexpr int BN = 128;                         // CTA tile columns
+constexpr int BK = 32;                          // k-tile
+constexpr int STAGES = DET_GEMM_STAGES;
+static_assert(TM % 4 == 0 && BM <= 256, "TMA box and m/n-contiguous fragment loads");
 constexpr int THREADS = 256;
 constexpr int TILES_PER_CHUNK = kKChunk / BK;   // 8
-constexpr int TILE_FLOATS = BM * BK;            // 4096 (BN == BM)
-constexpr int STAGE_FLOATS = 2 * TILE_FLOATS;   // A tile then B tile
-constexpr int TOTAL_FLOAT4 = THREADS * 16;      // 64 running totals a thread
+constexpr int A_FLOATS = BM * BK;               // 8192
+constexpr int B_FLOATS = BN * BK;               // 4096
+constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
+constexpr int TOTAL_FLOAT4 = THREADS * TM * TN / 4;   // running totals
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_FLOATS * 4 +
                               size_t(TOTAL_FLOAT4) * 16 + STAGES * 8;
 static_assert(kKChunk % BK == 0, "chunk boundaries must fall on k-tiles");
+static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
 
 __device__ unsigned int g_gemm_watchdog;
 
-// Shared-memory float index of element (row r, k) of a 128 x 32 operand tile.
-// KMAJ: rows of 32 k (128 bytes), 16-byte chunk q of row r stored at chunk
-// q ^ (r & 7) -- the TMA 128-byte swizzle pattern. Otherwise: rows of 128
+// Shared-memory float index of element (row r, k) of an operand tile with R
+// rows. KMAJ: rows of 32 k (128 bytes); 16-byte chunk q of row r is stored at
+// chunk q ^ (r & 7), the TMA 128-byte swizzle pattern. Otherwise one row of R
 // m/n values for each k.
-template <bool KMAJ>
+template <bool KMAJ, int R>
 __device__ __forceinline__ int tile_idx(int r, int k) {
     if (KMAJ) return r * 32 + ((((k >> 2) ^ (r & 7)) << 2) | (k & 3));
-    return k * 128 + r;
+    return k * R + r;
 }
 
 struct KArgs {
@@ -75,37 +97,42 @@ struct KArgs {
     int mt, nt;        // tiles along M and N
     int m_fast;        // tile order
     int vec_store;     // C rows 16-byte aligned
+    // Work units. Without split, a unit is a tile over all of K. With split,
+    // a unit is (tile, group of consecutive 256-wide chunks); it writes every
+    // chunk partial P_c of the tile to the workspace in the tile-blocked layout
+    // of ws_index(), and a second kernel adds them left to right into C.
+    int split;
+    int units_per_tile;
+    int kt_per_unit;   // multiple of the k-tiles a chunk spans
+    float4 *W;
 };
 
-// Loads the operand fragments of k group q (k = 4q .. 4q+3 of the tile) and
-// runs the 256 FFMAs: acc[r][c] = fmaf(a[r][kk], b[c][kk], acc[r][c]) for
-// kk ascending.
+// Workspace layout of split mode: float4 slot of (chunk c, tile t, accumulator
+// quad q of the thread, thread tid), consecutive threads adjacent so each
+// store instruction writes 4 KB contiguously.
+constexpr int QUADS = TM * TN / 4;   // 32
+__device__ __forceinline__ int64_t ws_index(int c, int ntiles, int t, int q, int tid) {
+    return ((int64_t(c) * ntiles + t) * QUADS + q) * THREADS + tid;
+}
+
+// One 4-wide k group q (k = 4q .. 4q+3 of the k-tile): for every accumulator,
+// acc[r][c] = fmaf(a[r][kk], b[c][kk], acc[r][c]) with kk = 0, 1, 2, 3 in that
+// order. The order across different accumulators is free, so each layout
+// gets the loop nest that keeps the fewest fragment registers live. A
+// k-contiguous tile yields the 4 k of one row per 16-byte load; an
+// m/n-contiguous tile yields 4 rows of one k.
+//   thread rows (op(A)): KMAJ arow + 8r;  else arow + (r & 3) + 32 (r >> 2)
+//   thread cols (op(B)): KMAJ bcol + 4c;  else bcol + (c & 3) + 16 (c >> 2)
 template <bool A_KM, bool B_KM>
 __device__ __forceinline__ void mma_group(const float *__restrict__ As,
                                           const float *__restrict__ Bs, int q,
                                           int arow, int bcol, int lm, int ln,
-                                          float (&acc)[8][8]) {
-    float a[8][4], b[8][4];
-    if (A_KM) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const float4 v = *reinterpret_cast<const float4 *>(
-                As + (arow + 8 * r) * 32 + ((q ^ lm) << 2));
-            a[r][0] = v.x; a[r][1] = v.y; a[r][2] = v.z; a[r][3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const float *p = As + (4 * q + kk) * 128 + arow;
-            const float4 lo = *reinterpret_cast<const float4 *>(p);
-            const float4 hi = *reinterpret_cast<const float4 *>(p + 32);
-            a[0][kk] = lo.x; a[1][kk] = lo.y; a[2][kk] = lo.z; a[3][kk] = lo.w;
-            a[4][kk] = hi.x; a[5][kk] = hi.y; a[6][kk] = hi.z; a[7][kk] = hi.w;
-        }
-    }
+                                          float (&acc)[TM][TN]) {
+    // B fragment: 8 columns x 4 k
+    float b[TN][4];
     if (B_KM) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < TN; ++c) {
             const int sw = ln + 4 * (c & 1);          // (bcol + 4c) & 7
             const float4 v = *reinterpret_cast<const float4 *>(
                 Bs + (bcol + 4 * c) * 32 + ((q ^ sw) << 2));
@@ -114,65 +141,182 @@ __device__ __forceinline__ void mma_group(const float *__restrict__ As,
     } else {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const float *p = Bs + (4 * q + kk) * 128 + bcol;
-            const float4 lo = *reinterpret_cast<const float4 *>(p);
-            const float4 hi = *reinterpret_cast<const float4 *>(p + 16);
+            const float *pb = Bs + (4 * q + kk) * BN + bcol;
+            const float4 lo = *reinterpret_cast<const float4 *>(pb);
+            const float4 hi = *reinterpret_cast<const float4 *>(pb + 16);
             b[0][kk] = lo.x; b[1][kk] = lo.y; b[2][kk] = lo.z; b[3][kk] = lo.w;
             b[4][kk] = hi.x; b[5][kk] = hi.y; b[6][kk] = hi.z; b[7][kk] = hi.w;
         }
     }
+    if (A_KM) {
+        // A streamed one row (4 k) at a time
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
+        for (int r = 0; r < TM; ++r) {
+            const float4 v = *reinterpret_cast<const float4 *>(
+                As + (arow + 8 * r) * 32 + ((q ^ lm) << 2));
+            const float a[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+            for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                acc[r][c] = __fmaf_rn(a[r][kk], b[c][kk], acc[r][c]);
+                for (int c = 0; c < TN; ++c)
+                    acc[r][c] = __fmaf_rn(a[kk], b[c][kk], acc[r][c]);
+        }
+    } else {
+        // A streamed one k (16 rows) at a time
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float *pa = As + (4 * q + kk) * BM + arow;
+            float a[TM];
+#pragma unroll
+            for (int h = 0; h < TM / 4; ++h) {
+                const float4 v = *reinterpret_cast<const float4 *>(pa + 32 * h);
+                a[4 * h] = v.x; a[4 * h + 1] = v.y; a[4 * h + 2] = v.z; a[4 * h + 3] = v.w;
+            }
+#pragma unroll
+            for (int r = 0; r < TM; ++r)
+#pragma unroll
+                for (int c = 0; c < TN; ++c)
+                    acc[r][c] = __fmaf_rn(a[r], b[c][kk], acc[r][c]);
+        }
+    }
+}
+
+// The thread's r-th row of op(A) and c-th column of op(B), tile-relative.
+template <bool A_KM>
+__device__ __forceinline__ int row_of(int arow, int r) {
+    return A_KM ? arow + 8 * r : arow + (r & 3) + (r >> 2) * 32;
+}
+template <bool B_KM>
+__device__ __forceinline__ int col_of(int bcol, int c) {
+    return B_KM ? bcol + 4 * c : bcol + (c & 3) + (c >> 2) * 16;
 }
 
 // The last k-tile when K is not a multiple of 32: k ascending up to kcount.
 template <bool A_KM, bool B_KM>
 __device__ __forceinline__ void mma_partial(const float *__restrict__ As,
-                                         const float *__restrict__ Bs, int kcount,
-                                         const int (&rows)[8], const int (&cols)[8],
-                                         float (&acc)[8][8]) {
+                                            const float *__restrict__ Bs, int kcount,
+                                            int arow, int bcol, float (&acc)[TM][TN]) {
     for (int k = 0; k < kcount; ++k) {
-        float a[8], b[8];
+        float a[TM], b[TN];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) a[r] = As[tile_idx<A_KM>(rows[r], k)];
+        for (int r = 0; r < TM; ++r) a[r] = As[tile_idx<A_KM, BM>(row_of<A_KM>(arow, r), k)];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) b[c] = Bs[tile_idx<B_KM>(cols[c], k)];
+        for (int c = 0; c < TN; ++c) b[c] = Bs[tile_idx<B_KM, BN>(col_of<B_KM>(bcol, c), k)];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int r = 0; r < TM; ++r)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) acc[r][c] = __fmaf_rn(a[r], b[c], acc[r][c]);
+            for (int c = 0; c < TN; ++c) acc[r][c] = __fmaf_rn(a[r], b[c], acc[r][c]);
     }
 }
 
-// Plain-load producer: the whole CTA copies one 128 x 32 tile into the same
-// layout TMA would produce, zero-filling outside the matrix.
-template <bool KMAJ>
+// Plain-load producer: the whole CTA copies one R x 32 tile into the layout
+// TMA would produce, zero-filling outside the matrix.
+template <bool KMAJ, int R>
 __device__ __forceinline__ void load_tile_plain(float *dst, const float *src,
                                                 int64_t ld, int rows_total,
                                                 int k_total, int r0, int k0,
                                                 int tid) {
 #pragma unroll 4
-    for (int e = tid; e < TILE_FLOATS; e += THREADS) {
+    for (int e = tid; e < R * BK; e += THREADS) {
         int r, k;
         if (KMAJ) { r = e >> 5; k = e & 31; }        // consecutive threads: consecutive k
-        else      { k = e >> 7; r = e & 127; }       // consecutive threads: consecutive m/n
+        else      { k = e / R; r = e % R; }          // consecutive threads: consecutive m/n
         const int gr = r0 + r, gk = k0 + k;
         float v = 0.0f;
         if (gr < rows_total && gk < k_total)
             v = KMAJ ? src[int64_t(gr) * ld + gk] : src[int64_t(gk) * ld + gr];
-        dst[tile_idx<KMAJ>(r, k)] = v;
+        dst[tile_idx<KMAJ, R>(r, k)] = v;
     }
 }
 
-template <bool A_KM, bool B_KM, bool TMA>
+// Issues the TMA loads of k-tile kt of the tile at (m0, n0) into stage `st`.
+template <bool A_KM, bool B_KM>
+__device__ __forceinline__ void issue_stage(float *st, uint64_t *bar_ptr,
+                                            const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                            int m0, int n0, int kt) {
+    const uint32_t bar = smem_u32(bar_ptr);
+    mbar_arrive_expect_tx(bar, STAGE_FLOATS * 4);
+    const int k0 = kt * BK;
+    if (A_KM) tma_load_2d(smem_u32(st), tmA, k0, m0, bar);
+    else      tma_load_2d(smem_u32(st), tmA, m0, k0, bar);
+    if (B_KM) tma_load_2d(smem_u32(st + A_FLOATS), tmB, k0, n0, bar);
+    else      tma_load_2d(smem_u32(st + A_FLOATS), tmB, n0, k0, bar);
+}
+
+// Unit u: tiles run fastest, so concurrent CTAs share one k range (and, for
+// the tiles, the smaller operand's blocks), keeping the working set in L2.
+struct Unit {
+    int t, m0, n0, kt0, kt1;
+};
+
+__device__ __forceinline__ Unit unit_of(const KArgs &p, int u, int nkt) {
+    const int ntiles = p.mt * p.nt;
+    const int t = u % ntiles, g = u / ntiles;
+    int mb, nb;
+    if (p.m_fast) { mb = t % p.mt; nb = t / p.mt; }
+    else          { nb = t % p.nt; mb = t / p.nt; }
+    Unit w;
+    w.t = t;
+    w.m0 = mb * BM;
+    w.n0 = nb * BN;
+    w.kt0 = g * p.kt_per_unit;
+    w.kt1 = min(nkt, w.kt0 + p.kt_per_unit);
+    return w;
+}
+
+// Stores a TM x TN register tile at rows m0 + row r, cols n0 + col c of a
+// row-major M x N matrix with row stride ld (bounds-checked).
+template <bool A_KM, bool B_KM>
+__device__ __forceinline__ void store_tile(const float (&acc)[TM][TN], float *base,
+                                           int64_t ld, int M, int N, int m0, int n0,
+                                           int arow, int bcol, int vec) {
+#pragma unroll
+    for (int r = 0; r < TM; ++r) {
+        const int i = m0 + row_of<A_KM>(arow, r);
+        if (i >= M) continue;
+        float *crow = base + int64_t(i) * ld;
+        if (!B_KM && vec) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = n0 + col_of<B_KM>(bcol, 4 * h);
+                if (j + 3 < N) {
+                    *reinterpret_cast<float4 *>(crow + j) =
+                        make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2],
+                                    acc[r][4 * h + 3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (j + c < N) crow[j + c] = acc[r][4 * h + c];
+                }
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < TN; ++c) {
+                const int j = n0 + col_of<B_KM>(bcol, c);
+                if (j < N) crow[j] = acc[r][c];
+            }
+        }
+    }
+}
+
+// Persistent: CTA b computes tiles b, b + gridDim.x, ... The k-tiles of all its
+// tiles form one sequence through the stage ring, so the loads of the next
+// tile are in flight while the current one finishes and stores.
+// Producer bookkeeping (thread 0 only), kept in shared memory so it costs no
+// registers in the other threads.
+struct Producer {
+    int ui;          // index of the unit being issued, among this CTA's units
+    int kt;          // next k-tile of that unit
+    int more;        // units left to issue
+    int count;       // k-tiles issued so far
+    Unit u;
+};
+
+template <bool A_KM, bool B_KM, bool TMA, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB, const KArgs p) {
+    __shared__ Producer prod;
     extern __shared__ unsigned char smem_raw[];
     float *smem = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -182,164 +326,187 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int wm = warp >> 2, wn = warp & 3;
-    const int lm = lane >> 2, ln = lane & 3;
+    const int wm = warp >> 2, wn = warp & 3;     // 2 x 4 warps, warp tile WTM x 32
+    const int lm = lane >> 2, ln = lane & 3;     // 8 x 4 lanes
 
-    int mb, nb;
-    if (p.m_fast) { mb = blockIdx.x % p.mt; nb = blockIdx.x / p.mt; }
-    else          { nb = blockIdx.x % p.nt; mb = blockIdx.x / p.nt; }
-    const int m0 = mb * BM, n0 = nb * BN;
-
-    // the thread's 8 rows of op(A) and 8 columns of op(B), tile-relative
-    const int arow = A_KM ? wm * 64 + lm : wm * 64 + lm * 4;
+    const int arow = A_KM ? wm * WTM + lm : wm * WTM + lm * 4;
     const int bcol = B_KM ? wn * 32 + ln : wn * 32 + ln * 4;
-    int rows[8], cols[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) rows[r] = A_KM ? arow + 8 * r : arow + (r & 3) + (r >> 2) * 32;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) cols[c] = B_KM ? bcol + 4 * c : bcol + (c & 3) + (c >> 2) * 16;
 
+    const int nunits = p.mt * p.nt * p.units_per_tile;
+    const int my_units = (nunits - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);
     const int nkt = (p.K + BK - 1) / BK;
-    const int nchunks = (p.K + kKChunk - 1) / kKChunk;
 
-    float acc[8][8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[r][c] = 0.0f;
-
-    constexpr uint32_t kStageBytes = STAGE_FLOATS * 4;
-    int issued = 0;   // producer (thread 0): tiles issued so far
+    // producer (thread 0): issues the next k-tile of its unit sequence into a slot
+    auto issue_next = [&](int slot) {
+        issue_stage<A_KM, B_KM>(stages + slot * STAGE_FLOATS, &full[slot], &tmA, &tmB,
+                                prod.u.m0, prod.u.n0, prod.kt);
+        ++prod.count;
+        if (++prod.kt == prod.u.kt1) {
+            if (++prod.ui < my_units) {
+                prod.u = unit_of(p, blockIdx.x + prod.ui * gridDim.x, nkt);
+                prod.kt = prod.u.kt0;
+            } else {
+                prod.more = 0;
+            }
+        }
+    };
     if (TMA) {
         if (tid == 0) {
             for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&full[s]), 1);
             fence_mbar_init();
+            prod.ui = 0;
+            prod.count = 0;
+            prod.more = my_units > 0;
+            if (prod.more) {
+                prod.u = unit_of(p, blockIdx.x, nkt);
+                prod.kt = prod.u.kt0;
+            }
+            for (int s = 0; s < STAGES && prod.more; ++s) issue_next(s);
         }
         __syncthreads();
-        if (tid == 0) {
-            for (; issued < STAGES && issued < nkt; ++issued) {
-                float *st = stages + issued * STAGE_FLOATS;
-                const uint32_t bar = smem_u32(&full[issued]);
-                mbar_arrive_expect_tx(bar, kStageBytes);
-                const int k0 = issued * BK;
-                if (A_KM) tma_load_2d(smem_u32(st), &tmA, k0, m0, bar);
-                else      tma_load_2d(smem_u32(st), &tmA, m0, k0, bar);
-                if (B_KM) tma_load_2d(smem_u32(st + TILE_FLOATS), &tmB, k0, n0, bar);
-                else      tma_load_2d(smem_u32(st + TILE_FLOATS), &tmB, n0, k0, bar);
-            }
-        }
     }
 
+    int64_t it = 0;            // consumer position in the k-tile sequence
     bool aborted = false;
-    int kt = 0;
-    for (; kt < nkt; ++kt) {
-        const int s = TMA ? kt % STAGES : 0;
-        const float *As = stages + s * STAGE_FLOATS;
-        const float *Bs = As + TILE_FLOATS;
-        int ok = 1;
-        if (TMA) {
-            ok = mbar_wait_bounded(smem_u32(&full[s]), (kt / STAGES) & 1);
-        } else {
-            __syncthreads();   // everyone is done with the previous tile
-            load_tile_plain<A_KM>(stages, p.A, p.lda, p.M, p.K, m0, kt * BK, tid);
-            load_tile_plain<B_KM>(stages + TILE_FLOATS, p.B, p.ldb, p.N, p.K, n0,
-                                  kt * BK, tid);
-            __syncthreads();
-        }
-        if (ok) {
-            const int kcount = min(BK, p.K - kt * BK);
-            if (kcount == BK) {
+    for (int ui = 0; ui < my_units && !aborted; ++ui) {
+        const Unit w = unit_of(p, blockIdx.x + ui * gridDim.x, nkt);
+        float acc[TM][TN];
 #pragma unroll
-                for (int q = 0; q < BK / 4; ++q)
-                    mma_group<A_KM, B_KM>(As, Bs, q, arow, bcol, lm, ln, acc);
+        for (int r = 0; r < TM; ++r)
+#pragma unroll
+            for (int c = 0; c < TN; ++c) acc[r][c] = 0.0f;
+
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
+            const int s = TMA ? int(it % STAGES) : 0;
+            const float *As = stages + s * STAGE_FLOATS;
+            const float *Bs = As + A_FLOATS;
+            int ok = 1;
+            if (TMA) {
+                ok = mbar_wait_bounded(smem_u32(&full[s]), uint32_t(it / STAGES) & 1u);
             } else {
-                mma_partial<A_KM, B_KM>(As, Bs, kcount, rows, cols, acc);
+                __syncthreads();   // everyone is done with the previous k-tile
+                load_tile_plain<A_KM, BM>(stages, p.A, p.lda, p.M, p.K, w.m0, kt * BK, tid);
+                load_tile_plain<B_KM, BN>(stages + A_FLOATS, p.B, p.ldb, p.N, p.K, w.n0,
+                                          kt * BK, tid);
+                __syncthreads();
             }
-        }
-        // chunk boundary: fold the finished partial into the running total
-        const bool last = (kt == nkt - 1);
-        if (((kt + 1) % TILES_PER_CHUNK == 0) || last) {
-            const int chunk = kt / TILES_PER_CHUNK;
-            if (!(chunk == 0 && last)) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float4 &t = totals[(r * 2 + h) * THREADS + tid];
-                        float *a4 = &acc[r][4 * h];
-                        if (chunk == 0) {
-                            t = make_float4(a4[0], a4[1], a4[2], a4[3]);
-                        } else {
-                            float4 v = t;
-                            v.x = __fadd_rn(v.x, a4[0]);
-                            v.y = __fadd_rn(v.y, a4[1]);
-                            v.z = __fadd_rn(v.z, a4[2]);
-                            v.w = __fadd_rn(v.w, a4[3]);
-                            if (last) { a4[0] = v.x; a4[1] = v.y; a4[2] = v.z; a4[3] = v.w; }
-                            else t = v;
-                        }
-                    }
-                if (!last) {
-#pragma unroll
-                    for (int r = 0; r < 8; ++r)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) acc[r][c] = 0.0f;
+            if (ok) {
+                const int kcount = min(BK, p.K - kt * BK);
+                if (kcount == BK) {
+#pragma unroll 1
+                    for (int q = 0; q < BK / 4; ++q)
+                        mma_group<A_KM, B_KM>(As, Bs, q, arow, bcol, lm, ln, acc);
+                } else {
+                    mma_partial<A_KM, B_KM>(As, Bs, kcount, arow, bcol, acc);
                 }
             }
-        }
-        if (TMA) {
-            if (__syncthreads_or(!ok)) { aborted = true; break; }
-            if (tid == 0 && issued < nkt) {
-                float *st = stages + s * STAGE_FLOATS;
-                const uint32_t bar = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(bar, kStageBytes);
-                const int k0 = issued * BK;
-                if (A_KM) tma_load_2d(smem_u32(st), &tmA, k0, m0, bar);
-                else      tma_load_2d(smem_u32(st), &tmA, m0, k0, bar);
-                if (B_KM) tma_load_2d(smem_u32(st + TILE_FLOATS), &tmB, k0, n0, bar);
-                else      tma_load_2d(smem_u32(st + TILE_FLOATS), &tmB, n0, k0, bar);
-                ++issued;
+            const bool last = (kt == nkt - 1);
+            if (((kt + 1) % TILES_PER_CHUNK == 0) || last) {
+                const int chunk = kt / TILES_PER_CHUNK;
+                if (SPLIT) {
+                    // split: every chunk partial goes to the workspace
+                    if (ok) {
+                        const int ntiles = p.mt * p.nt;
+#pragma unroll
+                        for (int r = 0; r < TM; ++r)
+#pragma unroll
+                            for (int h = 0; h < TN / 4; ++h)
+                                __stcg(p.W + ws_index(chunk, ntiles, w.t, r * (TN / 4) + h, tid),
+                                       make_float4(acc[r][4 * h], acc[r][4 * h + 1],
+                                                   acc[r][4 * h + 2], acc[r][4 * h + 3]));
+                    }
+#pragma unroll
+                    for (int r = 0; r < TM; ++r)
+#pragma unroll
+                        for (int c = 0; c < TN; ++c) acc[r][c] = 0.0f;
+                } else if (!(chunk == 0 && last)) {
+                    // fold the finished partial into the running total; after the
+                    // last chunk acc holds the result
+#pragma unroll
+                    for (int r = 0; r < TM; ++r)
+#pragma unroll
+                        for (int h = 0; h < TN / 4; ++h) {
+                            float4 &t = totals[(r * (TN / 4) + h) * THREADS + tid];
+                            float *a4 = &acc[r][4 * h];
+                            if (chunk == 0) {
+                                t = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                            } else {
+                                float4 v = t;
+                                v.x = __fadd_rn(v.x, a4[0]);
+                                v.y = __fadd_rn(v.y, a4[1]);
+                                v.z = __fadd_rn(v.z, a4[2]);
+                                v.w = __fadd_rn(v.w, a4[3]);
+                                if (last) { a4[0] = v.x; a4[1] = v.y; a4[2] = v.z; a4[3] = v.w; }
+                                else t = v;
+                            }
+                        }
+                    if (!last) {
+#pragma unroll
+                        for (int r = 0; r < TM; ++r)
+#pragma unroll
+                            for (int c = 0; c < TN; ++c) acc[r][c] = 0.0f;
+                    }
+                }
+            }
+            if (TMA) {
+                if (__syncthreads_or(!ok)) { aborted = true; ++it; break; }
+                if (tid == 0 && prod.more) issue_next(s);
             }
         }
+        if (aborted) break;
+        // epilogue (the next unit's loads are already in flight)
+        if (!SPLIT)
+            store_tile<A_KM, B_KM>(acc, p.C, p.ldc, p.M, p.N, w.m0, w.n0, arow, bcol,
+                                   p.vec_store);
     }
-    (void)nchunks;
 
-    if (TMA && aborted) {
-        if (tid == 0) {
-            atomicOr(&g_gemm_watchdog, kWatchdogGemm);
-            // let the copies still in flight land before the CTA exits
-            for (int t = kt; t < issued; ++t)
-                (void)mbar_wait_bounded(smem_u32(&full[t % STAGES]), (t / STAGES) & 1);
+    if (TMA && aborted && tid == 0) {
+        atomicOr(&g_gemm_watchdog, kWatchdogGemm);
+        // let the copies still in flight land before the CTA exits: sequence
+        // positions it-1 .. prod.count-1 may still be pending
+        for (int64_t t = it - 1; t < prod.count; ++t)
+            (void)mbar_wait_bounded(smem_u32(&full[t % STAGES]), uint32_t(t / STAGES) & 1u);
+    }
+}
+
+// Split-K second pass: C[i,j] = ((P_0 + P_1) + P_2) + ... over the chunk
+// partials in the workspace, left to right. One thread per workspace quad:
+// it sums the quad over the chunks and scatters the 4 outputs to the rows and
+// columns the GEMM thread that wrote it owns.
+__global__ void chunk_sum_kernel(KArgs p, int nchunks, int a_km, int b_km) {
+    const int ntiles = p.mt * p.nt;
+    const int64_t slots = int64_t(ntiles) * QUADS * THREADS;
+    const int64_t cstride = slots;      // one chunk's worth of quads
+    for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < slots;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        float4 t = __ldcs(p.W + e);
+        for (int c = 1; c < nchunks; ++c) {
+            const float4 v = __ldcs(p.W + c * cstride + e);
+            t.x = __fadd_rn(t.x, v.x);
+            t.y = __fadd_rn(t.y, v.y);
+            t.z = __fadd_rn(t.z, v.z);
+            t.w = __fadd_rn(t.w, v.w);
         }
-        return;
-    }
-
-    // epilogue: C[m0 + rows[r], n0 + cols[c]]
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int i = m0 + rows[r];
+        const int tid = int(e % THREADS);
+        const int q = int((e / THREADS) % QUADS);
+        const int tile = int(e / (int64_t(THREADS) * QUADS));
+        int mb, nb;
+        if (p.m_fast) { mb = tile % p.mt; nb = tile / p.mt; }
+        else          { nb = tile % p.nt; mb = tile / p.nt; }
+        const int warp = tid >> 5, lane = tid & 31;
+        const int wm = warp >> 2, wn = warp & 3, lm = lane >> 2, ln = lane & 3;
+        const int r = q / (TN / 4), h = q % (TN / 4);
+        const int arow = a_km ? wm * WTM + lm : wm * WTM + lm * 4;
+        const int bcol = b_km ? wn * 32 + ln : wn * 32 + ln * 4;
+        const int i = mb * BM + (a_km ? arow + 8 * r : arow + (r & 3) + (r >> 2) * 32);
         if (i >= p.M) continue;
         float *crow = p.C + int64_t(i) * p.ldc;
-        if (!B_KM && p.vec_store) {
+        const float v[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int j = n0 + cols[4 * h];
-                if (j + 3 < p.N) {
-                    *reinterpret_cast<float4 *>(crow + j) =
-                        make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2],
-                                    acc[r][4 * h + 3]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (j + c < p.N) crow[j + c] = acc[r][4 * h + c];
-                }
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int j = n0 + cols[c];
-                if (j < p.N) crow[j] = acc[r][c];
-            }
+        for (int cc = 0; cc < 4; ++cc) {
+            const int c = 4 * h + cc;
+            const int j = nb * BN + (b_km ? bcol + 4 * c : bcol + (c & 3) + (c >> 2) * 16);
+            if (j < p.N) crow[j] = v[cc];
         }
     }
 }
@@ -371,17 +538,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 // A 2-D fp32 tensor map over a row-major matrix (inner = contiguous extent,
-// outer = rows, ld = row stride in elements) with a 32 x 128 or 128 x 32 box.
+// outer = rows, ld = row stride in elements). A k-contiguous operand gets a
+// 32 (k) x R box with the 128-byte swizzle; an m/n-contiguous one an R x 32
+// box, unswizzled. R = the tile's extent along m or n.
 bool make_map(CUtensorMap *map, const float *base, int64_t inner, int64_t outer,
-              int64_t ld, bool kmajor_box) {
+              int64_t ld, bool kmajor_box, int R) {
     auto enc = encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
     cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
     cuuint32_t box[2];
     CUtensorMapSwizzle swz;
-    if (kmajor_box) { box[0] = 32; box[1] = 128; swz = CU_TENSOR_MAP_SWIZZLE_128B; }
-    else            { box[0] = 128; box[1] = 32; swz = CU_TENSOR_MAP_SWIZZLE_NONE; }
+    if (kmajor_box) { box[0] = 32; box[1] = cuuint32_t(R); swz = CU_TENSOR_MAP_SWIZZLE_128B; }
+    else            { box[0] = cuuint32_t(R); box[1] = 32; swz = CU_TENSOR_MAP_SWIZZLE_NONE; }
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
@@ -398,11 +567,12 @@ bool tma_ok(const float *base, int64_t ld) {
 template <bool A_KM, bool B_KM, bool TMA>
 cudaError_t launch_variant(const CUtensorMap &ma, const CUtensorMap &mb, const KArgs &k,
                            cudaStream_t s) {
-    auto kern = gemm_kernel<A_KM, B_KM, TMA>;
+    auto kern = k.split ? gemm_kernel<A_KM, B_KM, TMA, true> : gemm_kernel<A_KM, B_KM, TMA, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    const unsigned grid = unsigned(int64_t(k.mt) * k.nt);
+    const int64_t units = int64_t(k.mt) * k.nt * k.units_per_tile;
+    const unsigned grid = unsigned(std::min<int64_t>(units, sm_count_current_device()));
     kern<<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, k);
     return cudaGetLastError();
 }
@@ -418,13 +588,61 @@ cudaError_t launch_layout(bool a_km, bool b_km, const CUtensorMap &ma,
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
+// Work plan: whether to split K across CTAs and into how many chunk groups.
+// A split unit computes whole 256-wide chunks, so the bits never depend on the
+// plan. The cost model counts k-tile steps of the most loaded SM (a k-tile
+// step of a 256 x 128 tile is ~6 us at the FFMA rate this kernel sustains) and
+// adds the workspace traffic (each partial written once and read once) at
+// HBM speed.
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms) {
+    GemmPlan pl{};
+    const int64_t T = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t nkt = (K + BK - 1) / BK;
+    const int64_t nchunks = (K + kKChunk - 1) / kKChunk;
+    pl.split = 0;
+    pl.units_per_tile = 1;
+    pl.kt_per_unit = int(nkt);
+    pl.nchunks = int(nchunks);
+    pl.workspace_bytes = 0;
+    if (M == 0 || N == 0 || K == 0 || nchunks < 2) return pl;
+    const double kt_step_s = 6.0e-6, hbm_bps = 6.0e12;
+    double best = double((T + sms - 1) / sms) * double(nkt) * kt_step_s;
+    for (int64_t S = 2; S <= nchunks; ++S) {
+        const int64_t G = (nchunks + S - 1) / S;              // chunks a unit
+        const int64_t S_eff = (nchunks + G - 1) / G;
+        if (S_eff != S) continue;                             // same as a smaller S
+        const int64_t units = T * S_eff;
+        const double compute = double((units + sms - 1) / sms) *
+                               double(std::min<int64_t>(G * TILES_PER_CHUNK, nkt)) * kt_step_s;
+        const double ws = double(nchunks) * double(T) * BM * BN * 4.0;
+        const double cost = compute + (2.0 * ws + double(M) * double(N) * 4.0) / hbm_bps;
+        if (cost < 0.97 * best) {
+            best = cost;
+            pl.split = 1;
+            pl.units_per_tile = int(S_eff);
+            pl.kt_per_unit = int(G * TILES_PER_CHUNK);
+            pl.workspace_bytes = size_t(ws);
+        }
+    }
+    return pl;
+}
+
+cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_bytes,
+                        cudaStream_t s) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
     if (a.K == 0) {
         const int64_t total = a.M * a.N;
         const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 32);
         fill_zero_kernel<<<unsigned(blocks), 256, 0, s>>>(a.C, a.ldc, a.M, a.N);
         return cudaGetLastError();
+    }
+    const int sms = sm_count_current_device();
+    GemmPlan pl = gemm_plan(a.M, a.N, a.K, sms);
+    if (pl.split && (workspace == nullptr || workspace_bytes < pl.workspace_bytes ||
+                     reinterpret_cast<uintptr_t>(workspace) % 16 != 0)) {
+        pl = GemmPlan{};          // no usable workspace: one unit per tile
+        pl.units_per_tile = 1;
+        pl.kt_per_unit = int((a.K + BK - 1) / BK);
     }
     KArgs k;
     k.M = int(a.M); k.N = int(a.N); k.K = int(a.K);
@@ -434,18 +652,27 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s) {
     k.nt = int((a.N + BN - 1) / BN);
     k.m_fast = a.M <= a.N;
     k.vec_store = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && (a.ldc % 4 == 0);
+    k.split = pl.split;
+    k.units_per_tile = pl.units_per_tile;
+    k.kt_per_unit = pl.kt_per_unit;
+    k.W = static_cast<float4 *>(pl.split ? workspace : nullptr);
     // op(A) is k-contiguous when A is not transposed; op(B) when B is.
     const bool a_km = !a.transA, b_km = a.transB != 0;
     CUtensorMap ma{}, mb{};
     bool tma = tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb);
     if (tma) {
-        tma = a_km ? make_map(&ma, a.A, a.K, a.M, a.lda, true)
-                   : make_map(&ma, a.A, a.M, a.K, a.lda, false);
-        tma = tma && (b_km ? make_map(&mb, a.B, a.K, a.N, a.ldb, true)
-                           : make_map(&mb, a.B, a.N, a.K, a.ldb, false));
+        tma = a_km ? make_map(&ma, a.A, a.K, a.M, a.lda, true, BM)
+                   : make_map(&ma, a.A, a.M, a.K, a.lda, false, BM);
+        tma = tma && (b_km ? make_map(&mb, a.B, a.K, a.N, a.ldb, true, BN)
+                           : make_map(&mb, a.B, a.N, a.K, a.ldb, false, BN));
     }
-    if (tma) return launch_layout<true>(a_km, b_km, ma, mb, k, s);
-    return launch_layout<false>(a_km, b_km, ma, mb, k, s);
+    cudaError_t e = tma ? launch_layout<true>(a_km, b_km, ma, mb, k, s)
+                        : launch_layout<false>(a_km, b_km, ma, mb, k, s);
+    if (e != cudaSuccess || !pl.split) return e;
+    const int64_t slots = int64_t(k.mt) * k.nt * QUADS * THREADS;
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((slots + 255) / 256, int64_t(sms) * 8));
+    chunk_sum_kernel<<<unsigned(blocks), 256, 0, s>>>(k, pl.nchunks, a_km, b_km);
+    return cudaGetLastError();
 }
 
 cudaError_t gemm_watchdog(unsigned int *code, int clear) {

@@ -52,6 +52,8 @@ SIGNATURES = [
     ("det_status_string", ctypes.c_char_p, [_int]),
     ("detgemm_f32", _int, [_PROF, _int, _int, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
                            _vp, _i64, _vp, ctypes.c_size_t, _vp]),
+    ("detgemm_workspace_bytes", _int, [_PROF, _int, _int, _i64, _i64, _i64,
+                                       ctypes.POINTER(ctypes.c_size_t)]),
     ("detrmsnorm_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _f, _vp, _i64, _vp,
                               _vp]),
     ("detxent_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i64, _f,
@@ -133,9 +135,31 @@ def _ld(t):
 
 
 # ---------------------------------------------------------------- GEMM
-def detgemm_f32(A, B, C=None, transA=False, transB=False, profile=None, stream=None):
+def detgemm_workspace_bytes(M, N, K, transA=False, transB=False, profile=None) -> int:
+    n = ctypes.c_size_t()
+    _check("detgemm_workspace_bytes",
+           load().detgemm_workspace_bytes(_prof(profile), int(bool(transA)),
+                                          int(bool(transB)), int(M), int(N), int(K),
+                                          ctypes.byref(n)))
+    return n.value
+
+
+def gemm_workspace(M, N, K, transA=False, transB=False, device="cuda"):
+    """A caller-owned workspace tensor of the size detgemm_f32 can use for
+    this shape (None when it needs none)."""
+    import torch
+    n = detgemm_workspace_bytes(M, N, K, transA, transB)
+    if n == 0:
+        return None
+    return torch.empty((n + 3) // 4, dtype=torch.float32, device=device)
+
+
+def detgemm_f32(A, B, C=None, transA=False, transB=False, workspace=None, profile=None,
+                stream=None):
     """C = op(A) @ op(B) under the profile. A, B row-major 2-D float32 CUDA
-    tensors (transA: A is K x M; transB: B is N x K). Returns C."""
+    tensors (transA: A is K x M; transB: B is N x K). workspace: optional
+    float32 CUDA tensor (see gemm_workspace); the bits do not depend on it.
+    Returns C."""
     import torch
     _cuda_f32(A, "A", 2)
     _cuda_f32(B, "B", 2)
@@ -148,9 +172,13 @@ def detgemm_f32(A, B, C=None, transA=False, transB=False, profile=None, stream=N
     _cuda_f32(C, "C", 2)
     if tuple(C.shape) != (M, N):
         raise ValueError(f"C must be {M} x {N}")
+    ws_ptr, ws_bytes = ctypes.c_void_p(), 0
+    if workspace is not None:
+        _cuda_f32(workspace, "workspace")
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * 4
     st = load().detgemm_f32(_prof(profile), int(bool(transA)), int(bool(transB)), M, N,
                             K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
-                            ctypes.c_void_p(), 0, _stream(stream))
+                            ws_ptr, ws_bytes, _stream(stream))
     _check("detgemm_f32", st)
     return C
 

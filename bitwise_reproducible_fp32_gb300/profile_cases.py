@@ -1,0 +1,78 @@
+"""Runs one operation of the path on a fixed, seeded case, a few times, so a
+profiler can capture a chosen launch (ncu -k ... -s ... -c ...).
+
+  python -m bitwise_reproducible_fp32_gb300.profile_cases CASE [--reps R]
+
+Cases keep the device footprint at a few hundred MB, above the 129 MB L2 so
+DRAM counters mean something:
+  lm_head   GEMM 1024 x 50257 x 768, weight [50257, 768] transposed
+  qkv       GEMM 8192 x 2304 x 768
+  dw_qkv    GEMM X^T dY, 768 x 2304 over 8192 tokens
+  xent      cross-entropy 1024 x 50257 with dlogits and mean
+  rmsnorm   RMSNorm 8192 x 768
+  adamw     AdamW over 32 Mi parameters
+Each run is one warm-up launch followed by R launches (default 2).
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import numpy as np
+
+
+def main(argv=None):
+    import torch
+
+    from bitwise_reproducible_fp32_gb300 import build, detlib, inputs
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["lm_head", "qkv", "dw_qkv", "xent", "rmsnorm", "adamw"])
+    ap.add_argument("--reps", type=int, default=2)
+    a = ap.parse_args(argv)
+    build.build()
+    detlib.load()
+    dev = torch.device("cuda", 0)
+    up = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    if a.case in ("lm_head", "qkv"):
+        probs = {p["name"]: p for p in inputs.gemm_cfg3(tokens=1024 if a.case == "lm_head" else 8192)}
+        p = probs[a.case]
+        A, B = up(p["A"]), up(p["B"])
+        M = p["A"].shape[0]
+        N = p["B"].shape[0] if p["transB"] else p["B"].shape[1]
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+        run = lambda: detlib.detgemm_f32(A, B, C, transA=p["transA"], transB=p["transB"])
+    elif a.case == "dw_qkv":
+        p = inputs.dw_cfg5()[0]
+        A, B = up(p["A"]), up(p["B"])
+        C = torch.empty((p["A"].shape[1], p["B"].shape[1]), dtype=torch.float32, device=dev)
+        ws = detlib.gemm_workspace(C.shape[0], C.shape[1], p["A"].shape[0], True, False)
+        run = lambda: detlib.detgemm_f32(A, B, C, transA=True, workspace=ws)
+    elif a.case in ("xent", "rmsnorm"):
+        r = inputs.rowops_cfg4(rows=1024 if a.case == "xent" else 8192)
+        if a.case == "xent":
+            X, L = up(r["logits"]), up(r["labels"])
+            D = torch.empty_like(X)
+            loss = torch.empty(X.shape[0], dtype=torch.float32, device=dev)
+            mean = torch.empty(1, dtype=torch.float32, device=dev)
+            run = lambda: detlib.detxent_f32(X, L, loss=loss, loss_mean=mean, dlogits=D)
+        else:
+            x, g = up(r["x"]), up(r["gain"])
+            y = torch.empty_like(x)
+            inv = torch.empty(x.shape[0], dtype=torch.float32, device=dev)
+            run = lambda: detlib.detrmsnorm_f32(x, g, float(r["eps"]), y=y, inv_rms=inv)
+    else:
+        w = inputs.adamw_cfg5(n=32 * 1024 * 1024)
+        P, G, M_, V_ = (up(w[k]) for k in ("p", "g", "m", "v"))
+        hp = {k: w[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")}
+        run = lambda: detlib.detadamw_f32(P, G, M_, V_, **hp)
+
+    for _ in range(1 + a.reps):
+        run()
+    torch.cuda.synchronize()
+    print(f"{a.case}: {1 + a.reps} launches done")
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -94,7 +94,14 @@ const char *det_status_string(int status);
  * transB != 0: B is stored N x K row-major (ldb >= K), op(B) = B^T; this is
  *              the [out_features, in_features] Linear layout.
  * C: M x N row-major, ldc >= N, device pointer, must not overlap A or B.
- * workspace / workspace_bytes: reserved for split-K, pass NULL / 0.
+ * workspace / workspace_bytes: optional device scratch (16-byte aligned, not
+ *   overlapping A, B or C). With at least detgemm_workspace_bytes() bytes the
+ *   library may cut K into groups of whole 256-wide chunks computed by
+ *   different CTAs: each chunk partial P_c is written to the workspace and a
+ *   second kernel adds them left to right. With NULL, or too few bytes, every
+ *   output's chunks are computed by one thread. The result bits are the same
+ *   either way; only the speed differs. Calls that share a workspace must be
+ *   ordered (one stream).
  *
  * Errors: DET_ERR_INVALID_ARG for negative sizes, a dimension >= 2^31, an ld
  * below its row length or null pointers with nonzero sizes. A TMA wait that
@@ -107,6 +114,13 @@ det_status detgemm_f32(const det_profile_v1 *prof, int transA, int transB,
                        float *C, int64_t ldc,
                        void *workspace, size_t workspace_bytes,
                        det_stream_t stream);
+
+/* Workspace that detgemm_f32 can use for this shape on the current device
+ * (0 when splitting K would not help), written to *bytes. Same argument rules
+ * as detgemm_f32; a host-only query apart from reading the device's SM
+ * count. */
+det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA, int transB,
+                                   int64_t M, int64_t N, int64_t K, size_t *bytes);
 
 /* RMSNorm over `rows` rows of D floats: y = (x * r) * gain, with
  * r = 1.0f / sqrtf(ss / (float)D + eps). "MojoLearn 162M" model card, table
@@ -146,8 +160,9 @@ det_status detrmsnorm_f32(const det_profile_v1 *prof, int64_t rows, int64_t D,
  * labels: rows int32 (device).
  * loss:   rows floats (device).
  * loss_mean: 1 float (device) or NULL.
- * dlogits: rows x V, stride ldd >= V (device) or NULL; it may alias logits
- *          when ldd == ld.
+ * dlogits: rows x V, stride ldd >= V (device) or NULL. It may be exactly
+ *          logits (same pointer and ldd == ld: computed in place); any other
+ *          overlap with logits is not allowed.
  * dev_status: one int32 (device) or NULL. A label outside [0, V) sets bit 0
  *          (atomic OR; the library never clears it), and that row's loss and
  *          dlogits row are NaN.

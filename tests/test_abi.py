@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for want in ("detgemm_f32", "detrmsnorm_f32", "detxent_f32", "detadamw_f32",
+    for want in ("detgemm_f32", "detgemm_workspace_bytes", "detrmsnorm_f32", "detxent_f32", "detadamw_f32",
                  "detexp_f32", "detlog_f32", "det_profile_default",
                  "det_status_string", "det_watchdog_status"):
         assert want in names

@@ -1,0 +1,54 @@
+"""The multi-GPU path of bench.py on CPU: world_size 2 over gloo. Each rank is
+an independent replica; the only collective takes the max of the per-rank
+timings, and the whole-job rate divides all replicas' work by the slowest."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port),
+                      RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank 1 is the slow replica on the first timing, rank 0 on the second
+        mine = [10.0 + rank, 5.0 - rank, 7.0]
+        got = bench.max_over_ranks(mine, torch.device("cpu"))
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    import socket
+
+    import torch.multiprocessing as mp
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert out[0] == out[1] == [11.0, 5.0, 7.0]
+
+
+def test_replica_throughput():
+    sys.path.insert(0, ROOT)
+    import bench
+    # two replicas of 1 TFLOP each, the slower taking 100 ms: 20 TFLOP/s
+    assert bench.replica_throughput(1e12, 2, 100.0) == pytest.approx(2e13)
+    assert bench.replica_throughput(1e12, 1, 100.0) == pytest.approx(1e13)

@@ -32,19 +32,25 @@ def wide_random(rng, shape):
     return x
 
 
-def run_case(M, N, K, transA, transB, layout_a, layout_b, layout_c, seed, wide=False):
+def run_case(M, N, K, transA, transB, layout_a, layout_b, layout_c, seed, wide=False,
+             workspaces=(False, True)):
+    """Checks every layout/workspace combination against the oracle; the
+    workspace (split-K over whole chunks) must not change a bit."""
     rng = np.random.default_rng(seed)
     gen = (lambda s: wide_random(rng, s)) if wide else (
         lambda s: rng.standard_normal(s).astype(F))
     A = gen((K, M) if transA else (M, K))
     B = gen((N, K) if transB else (K, N))
     want = oracle.gemm(A, B, transA=transA, transB=transB)
-    C = empty_dev(M, N, layout_c)
-    detlib.detgemm_f32(to_dev(A, layout_a), to_dev(B, layout_b), C, transA=transA,
-                       transB=transB)
-    torch.cuda.synchronize()
-    assert_bitwise(host(C), want,
-                   f"M={M} N={N} K={K} tA={transA} tB={transB} {layout_a}/{layout_b}/{layout_c}")
+    Ad, Bd = to_dev(A, layout_a), to_dev(B, layout_b)
+    for use_ws in workspaces:
+        ws = detlib.gemm_workspace(M, N, K, transA, transB) if use_ws else None
+        C = empty_dev(M, N, layout_c)
+        detlib.detgemm_f32(Ad, Bd, C, transA=transA, transB=transB, workspace=ws)
+        torch.cuda.synchronize()
+        assert_bitwise(host(C), want,
+                       f"M={M} N={N} K={K} tA={transA} tB={transB} "
+                       f"{layout_a}/{layout_b}/{layout_c} workspace={ws is not None}")
 
 
 SHAPES = [
@@ -70,6 +76,27 @@ def test_signed_zero_underflow_and_wide_exponents(dev, transA, transB):
     for layout in ("padded", "offset"):
         run_case(70, 90, 777, bool(transA), bool(transB), layout, layout, layout, 5,
                  wide=True)
+
+
+def test_split_plan_is_used_where_it_helps(dev):
+    # few tiles and many chunks: the weight-gradient shapes split K
+    assert detlib.detgemm_workspace_bytes(768, 2304, 8192, True, False) > 0
+    assert detlib.detgemm_workspace_bytes(2048, 768, 8192, True, False) > 0
+    # plenty of tiles: the LM head does not
+    assert detlib.detgemm_workspace_bytes(8192, 50257, 768, False, True) == 0
+    # one chunk: nothing to split
+    assert detlib.detgemm_workspace_bytes(64, 64, 256) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 200, 1300), (129, 77, 2049), (512, 384, 4096),
+                                   (33, 1000, 777)])
+@pytest.mark.parametrize("transA,transB", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_split_k_same_bits(dev, M, N, K, transA, transB):
+    assert detlib.detgemm_workspace_bytes(M, N, K, transA, transB) > 0
+    run_case(M, N, K, bool(transA), bool(transB), "padded", "padded", "padded",
+             M * 31 + K)
+    run_case(M, N, K, bool(transA), bool(transB), "offset", "dense", "offset",
+             M * 37 + K, wide=True)
 
 
 def test_crafted_profile_cases(dev):
@@ -131,8 +158,12 @@ def check_rows(p, C_dev, rows):
 def test_cfg3_full_size_sampled(dev):
     probs = inputs.gemm_cfg3()
     for p in probs:
+        M = p["A"].shape[0]
+        K = p["A"].shape[1]
+        N = p["B"].shape[0] if p["transB"] else p["B"].shape[1]
+        ws = detlib.gemm_workspace(M, N, K, p["transA"], p["transB"])
         C = detlib.detgemm_f32(to_dev(p["A"]), to_dev(p["B"]), transA=p["transA"],
-                               transB=p["transB"])
+                               transB=p["transB"], workspace=ws)
         n = 10 if p["name"] == "lm_head" else 26
         check_rows(p, C, sampled_rows(C.shape[0], n, 3))
         del C
@@ -140,8 +171,15 @@ def test_cfg3_full_size_sampled(dev):
 
 def test_cfg5_dw_full_size_sampled(dev):
     for p in inputs.dw_cfg5():
-        C = detlib.detgemm_f32(to_dev(p["A"]), to_dev(p["B"]), transA=True)
-        check_rows(p, C, sampled_rows(C.shape[0], 18, 4))
+        M, N, K = p["A"].shape[1], p["B"].shape[1], p["A"].shape[0]
+        ws = detlib.gemm_workspace(M, N, K, True, False)
+        assert ws is not None
+        A, B = to_dev(p["A"]), to_dev(p["B"])
+        C = detlib.detgemm_f32(A, B, transA=True, workspace=ws)
+        rows = sampled_rows(C.shape[0], 18, 4)
+        check_rows(p, C, rows)
+        C2 = detlib.detgemm_f32(A, B, transA=True)          # no workspace
+        assert_bitwise(host(C2), host(C), p["name"] + " with vs without workspace")
 
 
 def test_repeatable_across_runs_and_streams(dev):

@@ -104,6 +104,34 @@ def test_xent_bad_labels_nan_inf_rows_and_status(dev):
     assert int(host(status)[0]) == 0
 
 
+@pytest.mark.parametrize("lx,ld_", [("dense", "offset"), ("offset", "dense"),
+                                     ("padded", "offset")])
+def test_xent_logits_and_dlogits_aligned_differently(dev, lx, ld_):
+    rng = np.random.default_rng(79)
+    rows, V = 9, 2051
+    x = (2 * rng.standard_normal((rows, V))).astype(F)
+    lab = rng.integers(0, V, size=rows, dtype=np.int32)
+    loss_w, d_w, _ = oracle.xent(x, lab, with_dlogits=True, dscale=F(0.25))
+    d = empty_dev(rows, V, ld_)
+    loss, _, _ = detlib.detxent_f32(to_dev(x, lx), to_dev(lab), dlogits=d, dscale=0.25)
+    assert_bitwise(host(loss), loss_w)
+    assert_bitwise(host(d), d_w)
+
+
+def test_xent_deep_underflow_row(dev):
+    # logits spread so that x - m runs through the subnormal and zero range
+    V = 4099
+    x = np.linspace(0.0, -120.0, V, dtype=F)[None, :].repeat(3, axis=0)
+    x[1] = x[1][::-1]
+    x[2, ::7] = F(-np.inf)
+    x[2, 1] = F(0.0)
+    lab = np.array([0, V - 1, 1], np.int32)
+    loss_w, d_w, _ = oracle.xent(x, lab, with_dlogits=True)
+    loss, _, d = detlib.detxent_f32(to_dev(x), to_dev(lab), want_dlogits=True)
+    assert_bitwise(host(loss), loss_w)
+    assert_bitwise(host(d), d_w)
+
+
 def test_xent_dlogits_in_place(dev):
     rng = np.random.default_rng(78)
     x = (2 * rng.standard_normal((4, 777))).astype(F)
