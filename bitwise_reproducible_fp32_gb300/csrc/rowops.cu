@@ -91,11 +91,6 @@ __device__ __forceinline__ float det_log(float x) {
     return __fmaf_rn(ef, kLn2Hi, __fmaf_rn(ef, kLn2Lo, lf));
 }
 
-// NaN-propagating max (the profile's max: any NaN in a row makes m NaN).
-__device__ __forceinline__ float nan_max(float a, float b) {
-    return (a != a || a > b) ? a : b;
-}
-
 __device__ __forceinline__ float warp_butterfly_sum(float s) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
@@ -187,20 +182,20 @@ __global__ void __launch_bounds__(kRmsWarps * 32)
 }
 
 // ---------------------------------------------------------------- cross-entropy
-// exp for arguments d <= 0 (or -inf), never NaN: the same bits as det_exp(d).
-// n = rint(t) is formed as (t + 1.5 2^23) - 1.5 2^23, which rounds t to an
-// integer with ties to even for |t| < 2^22; it can differ from rintf only in
-// the sign of a zero n, which reaches the result only through r = d - n ln2
-// and the polynomial's products with r, where it is inert. When n >= -125 the
-// scaling p 2^n is exact and is done on the exponent bits; otherwise (deep
-// underflow, -inf) the general routine runs.
+// exp for arguments d <= 0 (or -inf), never NaN, without branches: the same
+// bits as det_exp(d) whenever the returned n satisfies n >= -125; otherwise the
+// caller must use det_exp(d). n = rint(t) is formed as (t + 1.5 2^23) -
+// 1.5 2^23, which rounds t to an integer with ties to even for |t| < 2^22; it
+// can differ from rintf only in the sign of a zero n, which reaches the
+// result only through r = d - n ln2 and the polynomial's products with r,
+// where it is inert. For n >= -125 the scaling p 2^n is exact and is done on
+// the exponent bits.
 constexpr float kRoundMagic = 0x1.8p23f;
 
-__device__ __forceinline__ float det_exp_le0(float d) {
+__device__ __forceinline__ float exp_le0_fast(float d, int &ni) {
     const float t = __fmul_rn(d, kLog2e);
     const float tm = __fadd_rn(t, kRoundMagic);
-    const int ni = __float_as_int(tm) - __float_as_int(kRoundMagic);
-    if (ni < -125) return det_exp(d);
+    ni = __float_as_int(tm) - __float_as_int(kRoundMagic);
     const float n = __fsub_rn(tm, kRoundMagic);
     float r = __fmaf_rn(-n, kLn2Hi, d);
     r = __fmaf_rn(-n, kLn2Lo, r);
@@ -213,6 +208,19 @@ __device__ __forceinline__ float det_exp_le0(float d) {
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
     return __int_as_float(__float_as_int(p) + int(unsigned(ni) << 23));
+}
+
+// The general exp as an out-of-line call, for the rarely taken paths of the
+// cross-entropy (deep underflow, -inf, non-finite maxima), so they cost no
+// registers in the hot loops.
+__device__ __noinline__ float det_exp_call(float x) { return det_exp(x); }
+
+// The profile's row max: NaN if any element is NaN, else the largest (ties
+// between +0 and -0 are bit-inert for the loss and dlogits).
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
@@ -232,37 +240,261 @@ __device__ __forceinline__ float4 ld4_policy(const float *p, uint64_t pol) {
                  : "l"(p), "l"(pol));
     return v;
 }
+__device__ __forceinline__ void st4_policy(float *p, float4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
+                 : "memory");
+}
 __device__ __forceinline__ void st_policy(float *p, float v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol)
                  : "memory");
 }
 
 // One 256-thread CTA per row at a time (thread l = chain l of the 256-chain
-// profile), a persistent grid of two CTAs an SM. Per row:
-//  1. m = max over the row: 16-byte loads of the row's 16-byte-aligned
-//     granules (elements outside the row masked), kept in L2 (evict_last);
-//  2. chain sums: chain l reads its logical groups 4g..4g+3 (g = l, l+256, ...)
-//     from the aligned granule g and, through a lane shuffle, granule g+1;
-//     e_j = exp(x_j - m) is added in ascending j and, when dlogits is
-//     requested (and does not alias the logits), written to dlogits[j];
+// profile), a persistent grid of two CTAs an SM so a row's re-reads hit L2.
+// Rows of 50,257 floats start anywhere mod 16 bytes; each row is processed by
+// xent_row<H> with its misalignment H (elements) known at compile time.
+// Granule q of a row is the 16-byte aligned float4 holding elements
+// 4q - H .. 4q + 3 - H; the profile's group g (elements 4g .. 4g+3) is the last
+// 4 - H elements of granule g and the first H of granule g + 1.
+//  1. m = max over the granules (elements outside the row masked), loads kept
+//     in L2 (evict_last);
+//  2. chain l loads granule g (g = l, l + 256, ...), computes its 4 exps,
+//     stores them to the dlogits row (one 16-byte store where the two rows
+//     share their alignment), takes the first H exps of granule g + 1 from
+//     lane l + 1 by shuffles (lane 31 computes them itself) and adds group g's
+//     4 exps to its chain in ascending order;
 //  3. the butterfly 16..1 by shuffles, 32/64/128 through shared memory; thread
 //     0 forms loss = log(S) - (x_y - m);
-//  4. dlogits: d_j = (e_j * (1/S) - [j == y]) * dscale over the dlogits row's
-//     granules, reading back e_j (or recomputing it in place).
-// Rows with a non-finite max or a bad label take the general element-wise
-// code, which performs the same operations.
+//  4. d_j = (e_j * (1/S) - [j == y]) * dscale over the dlogits granules.
+// Main sweeps have no bounds checks; the first and last granules take a
+// checked path with the same arithmetic. Rows with a non-finite max, a bad
+// label, or dlogits equal to the logits recompute e_j element-wise instead of
+// storing it.
 constexpr int kXentThreads = 256;
-constexpr int kU = 8;    // independent 16-byte loads a thread keeps in flight
-constexpr int kU2 = 4;   // sweeps of the chain pass loaded ahead
+constexpr int kU = 4;    // independent 16-byte loads a thread keeps in flight
 static_assert(kXentThreads == kXentLanes, "one thread per chain");
 
-__device__ __forceinline__ float4 pick_group(float4 c0, float4 c1, int h) {
-    switch (h) {
-        case 0: return c0;
-        case 1: return make_float4(c0.y, c0.z, c0.w, c1.x);
-        case 2: return make_float4(c0.z, c0.w, c1.x, c1.y);
-        default: return make_float4(c0.w, c1.x, c1.y, c1.z);
+__device__ __forceinline__ float dl_of(float e, float inv, float dscale) {
+    return __fmul_rn(__fmul_rn(e, inv), dscale);        // e * inv - 0 == e * inv
+}
+__device__ __forceinline__ float dl_of_label(float e, float inv, float dscale) {
+    return __fmul_rn(__fsub_rn(__fmul_rn(e, inv), 1.0f), dscale);
+}
+
+// exp(v - m) for the 4 lanes of a granule; d <= 0 for every element of a row
+// with a finite max. Rare deep-underflow elements take the general routine.
+__device__ __forceinline__ float4 exp4(float4 v, float m) {
+    const float d0 = __fsub_rn(v.x, m), d1 = __fsub_rn(v.y, m);
+    const float d2 = __fsub_rn(v.z, m), d3 = __fsub_rn(v.w, m);
+    int n0, n1, n2, n3;
+    float4 e;
+    e.x = exp_le0_fast(d0, n0);
+    e.y = exp_le0_fast(d1, n1);
+    e.z = exp_le0_fast(d2, n2);
+    e.w = exp_le0_fast(d3, n3);
+    if (min(min(n0, n1), min(n2, n3)) < -125) {
+        if (n0 < -125) e.x = det_exp_call(d0);
+        if (n1 < -125) e.y = det_exp_call(d1);
+        if (n2 < -125) e.z = det_exp_call(d2);
+        if (n3 < -125) e.w = det_exp_call(d3);
     }
+    return e;
+}
+
+// The profile's group g (elements 4g .. 4g+3) from granule g (cur) and
+// granule g + 1 (nxt): the last 4 - H elements of cur, then the first H of nxt.
+template <int H>
+__device__ __forceinline__ float4 group_of(float4 cur, float4 nxt) {
+    if (H == 0) return cur;
+    if (H == 1) return make_float4(cur.y, cur.z, cur.w, nxt.x);
+    if (H == 2) return make_float4(cur.z, cur.w, nxt.x, nxt.y);
+    return make_float4(cur.w, nxt.x, nxt.y, nxt.z);
+}
+
+__device__ __forceinline__ float comp(float4 v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Granule g+1 for lanes 0..30 comes from the next lane; lane 31 loaded it.
+template <int H>
+__device__ __forceinline__ float4 next_granule(float4 c0, float4 own_next, int lane) {
+    float4 c1 = own_next;
+    if (H != 0) {
+        const float a = __shfl_down_sync(0xffffffffu, c0.x, 1);
+        const float b = H > 1 ? __shfl_down_sync(0xffffffffu, c0.y, 1) : 0.f;
+        const float d = H > 2 ? __shfl_down_sync(0xffffffffu, c0.z, 1) : 0.f;
+        if (lane != 31) c1 = make_float4(a, b, d, 0.f);
+    }
+    return c1;
+}
+
+// A sweep with bounds checks (the first sweep, the row's end, non-finite
+// maxima): the same operations as the fast sweep, element by element. Returns
+// the updated chain value.
+template <int H>
+__device__ __noinline__ float xent_checked_sweep(const float *xa, int V, int g, float m,
+                                                 bool finite_m, float *drow, bool store_e,
+                                                 float s, uint64_t keep) {
+    const int lane = threadIdx.x & 31;
+    const int ngroups = (V + 3) >> 2;
+    float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), own = c0;
+    if (4 * g - H < V) c0 = *reinterpret_cast<const float4 *>(xa + 4 * g);
+    if (H != 0 && lane == 31 && 4 * (g + 1) - H < V)
+        own = *reinterpret_cast<const float4 *>(xa + 4 * (g + 1));
+    const float4 v = group_of<H>(c0, next_granule<H>(c0, own, lane));
+    if (g < ngroups) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int j = 4 * g + k;
+            if (j < V) {
+                const float e = det_exp_call(__fsub_rn(comp(v, k), m));
+                s = __fadd_rn(s, e);
+                if (store_e) st_policy(drow + j, e, keep);
+            }
+        }
+    }
+    (void)finite_m;
+    return s;
+}
+
+template <int H>
+__device__ __noinline__ void xent_row(const float *x, int V, int y, float *drow, bool in_place,
+                                         float dscale, float *loss_out, float *red, float *bcast,
+                                         uint64_t keep, uint64_t drop) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float *xa = x - H;                        // 16-byte aligned
+    const int nch = (V + H + 3) >> 2;               // granules touching the row
+    const int q_lo = H == 0 ? 0 : 1;                // granules fully inside the row:
+    const int q_hi = (V + H) >> 2;                  //   [q_lo, q_hi)
+    // 1. m = max (order-free, NaN-propagating)
+    float m = x[0];
+    for (int q0 = q_lo + tid; q0 < q_hi; q0 += kXentThreads * kU) {
+        float4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int q = q0 + u * kXentThreads;
+            if (q < q_hi) v[u] = ld4_policy(xa + 4 * q, keep);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (q0 + u * kXentThreads < q_hi)
+                m = max_nan(m, max_nan(max_nan(v[u].x, v[u].y), max_nan(v[u].z, v[u].w)));
+    }
+    if (tid < 2) {      // the partial granules at the two ends
+        const int q = tid == 0 ? 0 : q_hi;
+        if ((tid == 0 && q_lo == 1) || (tid == 1 && q_hi < nch && q_hi >= q_lo)) {
+            const float4 v = *reinterpret_cast<const float4 *>(xa + 4 * q);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 4 * q - H + i;
+                if (j >= 0 && j < V) m = max_nan(m, comp(v, i));
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = max_nan(__shfl_xor_sync(0xffffffffu, m, off), m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (tid == 0) {
+        float mm = red[0];
+        for (int w = 1; w < kXentThreads / 32; ++w) mm = max_nan(red[w], mm);
+        *bcast = mm;
+    }
+    __syncthreads();
+    m = *bcast;
+    const bool finite_m = fabsf(m) <= 3.402823466e38f;     // false for NaN / inf
+    const bool store_e = drow != nullptr && !in_place && finite_m;
+    const int hd = drow ? int((reinterpret_cast<uintptr_t>(drow) >> 2) & 3) : 0;
+    float *da = drow ? drow - hd : nullptr;          // 16-byte aligned dlogits row
+
+    // 2. chain sums: sweep t covers groups g = tid + 256 t
+    float s = 0.0f;
+    const int ngroups = (V + 3) >> 2;
+    const int t_all = (ngroups + kXentThreads - 1) / kXentThreads;
+    // sweeps 1 .. t_fast-1 have every group full and inside the row
+    const int t_fast = finite_m ? (V >> 2) / kXentThreads : 0;
+    s = xent_checked_sweep<H>(xa, V, tid, m, finite_m, drow, store_e, s, keep);
+    for (int t = 1; t < t_fast; ++t) {
+        const int g = tid + t * kXentThreads;
+        const float4 c0 = ld4_policy(xa + 4 * g, drop);
+        float4 own = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (H != 0 && lane == 31) own = ld4_policy(xa + 4 * (g + 1), drop);
+        const float4 v = group_of<H>(c0, next_granule<H>(c0, own, lane));
+        const float4 e = exp4(v, m);
+        s = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(s, e.x), e.y), e.z), e.w);
+        if (store_e) {
+            float *dp = drow + 4 * g;
+            st_policy(dp, e.x, keep); st_policy(dp + 1, e.y, keep);
+            st_policy(dp + 2, e.z, keep); st_policy(dp + 3, e.w, keep);
+        }
+    }
+    for (int t = t_fast < 1 ? 1 : t_fast; t < t_all; ++t)
+        s = xent_checked_sweep<H>(xa, V, tid + t * kXentThreads, m, finite_m, drow, store_e, s,
+                                  keep);
+    // 3. butterfly: 16..1 in the warp, then 32, 64, 128 across warps
+    s = warp_butterfly_sum(s);
+    __syncthreads();    // red[] reuse
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+        const float a01 = __fadd_rn(red[0], red[1]), a23 = __fadd_rn(red[2], red[3]);
+        const float a45 = __fadd_rn(red[4], red[5]), a67 = __fadd_rn(red[6], red[7]);
+        const float S = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
+        *bcast = S;
+        *loss_out = __fsub_rn(det_log(S), __fsub_rn(x[y], m));
+    }
+    __syncthreads();
+    // 4. dlogits
+    if (drow) {
+        const float inv = __fdiv_rn(1.0f, *bcast);
+        if (store_e) {
+            const int dq_lo = hd == 0 ? 0 : 1, dq_hi = (V + hd) >> 2, dch = (V + hd + 3) >> 2;
+            for (int q0 = dq_lo + tid; q0 < dq_hi; q0 += kXentThreads * kU) {
+                float4 es[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int q = q0 + u * kXentThreads;
+                    if (q < dq_hi) es[u] = ld4_policy(da + 4 * q, drop);
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int q = q0 + u * kXentThreads;
+                    if (q >= dq_hi) break;
+                    const float4 e = es[u];
+                    float4 o = make_float4(dl_of(e.x, inv, dscale), dl_of(e.y, inv, dscale),
+                                           dl_of(e.z, inv, dscale), dl_of(e.w, inv, dscale));
+                    const unsigned k = unsigned(y - (4 * q - hd));
+                    if (k < 4) {      // the label's element: rare
+                        if (k == 0) o.x = dl_of_label(e.x, inv, dscale);
+                        if (k == 1) o.y = dl_of_label(e.y, inv, dscale);
+                        if (k == 2) o.z = dl_of_label(e.z, inv, dscale);
+                        if (k == 3) o.w = dl_of_label(e.w, inv, dscale);
+                    }
+                    __stcs(reinterpret_cast<float4 *>(da + 4 * q), o);
+                }
+            }
+            if (tid < 2) {    // the partial granules at the two ends
+                const int q = tid == 0 ? 0 : dq_hi;
+                if ((tid == 0 && dq_lo == 1) || (tid == 1 && dq_hi < dch && dq_hi >= dq_lo)) {
+                    for (int i = 0; i < 4; ++i) {
+                        const int j = 4 * q - hd + i;
+                        if (j >= 0 && j < V) {
+                            const float e = drow[j];
+                            drow[j] = j == y ? dl_of_label(e, inv, dscale) : dl_of(e, inv, dscale);
+                        }
+                    }
+                }
+            }
+        } else {
+            // in place, or a non-finite max: recompute e_j element-wise
+            for (int j = tid; j < V; j += kXentThreads) {
+                const float e = det_exp_call(__fsub_rn(x[j], m));
+                drow[j] = __fmul_rn(__fsub_rn(__fmul_rn(e, inv), j == y ? 1.0f : 0.0f), dscale);
+            }
+        }
+    }
+    __syncthreads();    // bcast / red reuse by the next row
 }
 
 __global__ void __launch_bounds__(kXentThreads, 2)
@@ -271,187 +503,29 @@ __global__ void __launch_bounds__(kXentThreads, 2)
                 float *dlogits, int64_t ldd, float dscale, int32_t *dev_status) {
     __shared__ float red[kXentThreads / 32];
     __shared__ float bcast;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const uint64_t keep = l2_policy_evict_last();
     const uint64_t drop = l2_policy_evict_first();
-    const int64_t ngroups = (V + 3) / 4;
     const bool in_place = dlogits != nullptr && dlogits == logits;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
         const float *x = logits + row * ld;
         const int64_t y = labels[row];
+        float *drow = dlogits ? dlogits + row * ldd : nullptr;
         if (y < 0 || y >= V) {
             if (tid == 0) {
                 loss[row] = __uint_as_float(0x7fc00000u);
                 if (dev_status) atomicOr(reinterpret_cast<int *>(dev_status), 1);
             }
-            if (dlogits) {
-                float *d = dlogits + row * ldd;
-                for (int64_t j = tid; j < V; j += kXentThreads)
-                    d[j] = __uint_as_float(0x7fc00000u);
-            }
+            if (drow)
+                for (int64_t j = tid; j < V; j += kXentThreads) drow[j] = __uint_as_float(0x7fc00000u);
             continue;   // uniform across the CTA
         }
-        const int h = int((reinterpret_cast<uintptr_t>(x) >> 2) & 3);
-        const float *xa = x - h;                     // 16-byte aligned
-        const int64_t nchunks = (V + h + 3) / 4;     // granules touching the row
-        // 1. m = max (order-free, NaN-propagating); kU independent loads in
-        // flight a thread
-        float m = x[0];
-        for (int64_t q0 = tid; q0 < nchunks; q0 += int64_t(kXentThreads) * kU) {
-            float4 v[kU];
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int64_t q = q0 + int64_t(u) * kXentThreads;
-                if (q < nchunks) v[u] = ld4_policy(xa + 4 * q, keep);
-            }
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int64_t q = q0 + int64_t(u) * kXentThreads;
-                if (q >= nchunks) break;
-                const int64_t j0 = 4 * q - h;
-                if (j0 >= 0 && j0 + 3 < V) {
-                    m = nan_max(v[u].x, m); m = nan_max(v[u].y, m);
-                    m = nan_max(v[u].z, m); m = nan_max(v[u].w, m);
-                } else {
-                    if (j0 >= 0 && j0 < V) m = nan_max(v[u].x, m);
-                    if (j0 + 1 >= 0 && j0 + 1 < V) m = nan_max(v[u].y, m);
-                    if (j0 + 2 >= 0 && j0 + 2 < V) m = nan_max(v[u].z, m);
-                    if (j0 + 3 >= 0 && j0 + 3 < V) m = nan_max(v[u].w, m);
-                }
-            }
+        switch (int((reinterpret_cast<uintptr_t>(x) >> 2) & 3)) {
+            case 0: xent_row<0>(x, int(V), int(y), drow, in_place, dscale, loss + row, red, &bcast, keep, drop); break;
+            case 1: xent_row<1>(x, int(V), int(y), drow, in_place, dscale, loss + row, red, &bcast, keep, drop); break;
+            case 2: xent_row<2>(x, int(V), int(y), drow, in_place, dscale, loss + row, red, &bcast, keep, drop); break;
+            default: xent_row<3>(x, int(V), int(y), drow, in_place, dscale, loss + row, red, &bcast, keep, drop); break;
         }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-            m = nan_max(__shfl_xor_sync(0xffffffffu, m, off), m);
-        if (lane == 0) red[warp] = m;
-        __syncthreads();
-        if (tid == 0) {
-            float mm = red[0];
-            for (int w = 1; w < kXentThreads / 32; ++w) mm = nan_max(red[w], mm);
-            bcast = mm;
-        }
-        __syncthreads();
-        m = bcast;
-        const bool finite_m = fabsf(m) <= 3.402823466e38f;   // false for NaN / inf
-        float *drow = dlogits ? dlogits + row * ldd : nullptr;
-        const bool store_e = drow != nullptr && !in_place && finite_m;
-
-        // 2. chain sums over the logical groups, kU2 sweeps' loads in flight
-        float s = 0.0f;
-        const int64_t titers = (ngroups + kXentThreads - 1) / kXentThreads;
-        for (int64_t t0 = 0; t0 < titers; t0 += kU2) {
-          float4 c0s[kU2], c1s[kU2];
-#pragma unroll
-          for (int u = 0; u < kU2; ++u) {
-            const int64_t g = tid + (t0 + u) * kXentThreads;
-            c0s[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            c1s[u] = c0s[u];
-            if (t0 + u < titers && 4 * g - h < V) c0s[u] = ld4_policy(xa + 4 * g, drop);
-            if (h != 0 && lane == 31 && t0 + u < titers && 4 * (g + 1) - h < V)
-                c1s[u] = ld4_policy(xa + 4 * (g + 1), drop);
-          }
-#pragma unroll
-          for (int u = 0; u < kU2; ++u) {
-            if (t0 + u >= titers) break;    // uniform across the CTA
-            const int64_t g = tid + (t0 + u) * kXentThreads;
-            const float4 c0 = c0s[u];
-            float4 c1 = c1s[u];
-            if (h != 0) {
-                const float nx = __shfl_down_sync(0xffffffffu, c0.x, 1);
-                const float ny = __shfl_down_sync(0xffffffffu, c0.y, 1);
-                const float nz = __shfl_down_sync(0xffffffffu, c0.z, 1);
-                if (lane != 31) { c1.x = nx; c1.y = ny; c1.z = nz; }
-            }
-            if (g < ngroups) {
-                const float4 v = pick_group(c0, c1, h);
-                const int64_t j0 = 4 * g;
-                if (finite_m) {
-                    float e[4];
-                    e[0] = det_exp_le0(__fsub_rn(v.x, m));
-                    e[1] = det_exp_le0(__fsub_rn(v.y, m));
-                    e[2] = det_exp_le0(__fsub_rn(v.z, m));
-                    e[3] = det_exp_le0(__fsub_rn(v.w, m));
-                    const int cnt = j0 + 3 < V ? 4 : int(V - j0);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (k < cnt) s = __fadd_rn(s, e[k]);
-                    if (store_e) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            if (k < cnt) st_policy(drow + j0 + k, e[k], keep);
-                    }
-                } else {
-                    const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (j0 + k < V) s = __fadd_rn(s, det_exp(__fsub_rn(vv[k], m)));
-                }
-            }
-          }
-        }
-        // 3. butterfly: 16..1 in the warp, then 32, 64, 128 across warps
-        s = warp_butterfly_sum(s);
-        __syncthreads();    // red[] reuse
-        if (lane == 0) red[warp] = s;
-        __syncthreads();
-        if (tid == 0) {
-            const float a01 = __fadd_rn(red[0], red[1]), a23 = __fadd_rn(red[2], red[3]);
-            const float a45 = __fadd_rn(red[4], red[5]), a67 = __fadd_rn(red[6], red[7]);
-            const float S = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
-            bcast = S;
-            loss[row] = __fsub_rn(det_log(S), __fsub_rn(x[y], m));
-        }
-        __syncthreads();
-        // 4. dlogits
-        if (drow) {
-            const float inv = __fdiv_rn(1.0f, bcast);
-            if (store_e) {
-                const int hd = int((reinterpret_cast<uintptr_t>(drow) >> 2) & 3);
-                float *da = drow - hd;
-                const int64_t dchunks = (V + hd + 3) / 4;
-                for (int64_t q0 = tid; q0 < dchunks; q0 += int64_t(kXentThreads) * kU) {
-                  float4 es[kU];
-#pragma unroll
-                  for (int u = 0; u < kU; ++u) {
-                    const int64_t q = q0 + int64_t(u) * kXentThreads;
-                    const int64_t j0 = 4 * q - hd;
-                    if (q < dchunks && j0 >= 0 && j0 + 3 < V) es[u] = ld4_policy(da + 4 * q, drop);
-                  }
-#pragma unroll
-                  for (int u = 0; u < kU; ++u) {
-                    const int64_t q = q0 + int64_t(u) * kXentThreads;
-                    if (q >= dchunks) break;
-                    const int64_t j0 = 4 * q - hd;
-                    if (j0 >= 0 && j0 + 3 < V) {
-                        const float4 e = es[u];
-                        float4 o;
-                        o.x = __fmul_rn(__fsub_rn(__fmul_rn(e.x, inv), j0 == y ? 1.0f : 0.0f), dscale);
-                        o.y = __fmul_rn(__fsub_rn(__fmul_rn(e.y, inv), j0 + 1 == y ? 1.0f : 0.0f), dscale);
-                        o.z = __fmul_rn(__fsub_rn(__fmul_rn(e.z, inv), j0 + 2 == y ? 1.0f : 0.0f), dscale);
-                        o.w = __fmul_rn(__fsub_rn(__fmul_rn(e.w, inv), j0 + 3 == y ? 1.0f : 0.0f), dscale);
-                        __stcs(reinterpret_cast<float4 *>(da + 4 * q), o);
-                    } else {
-                        for (int k = 0; k < 4; ++k) {
-                            const int64_t j = j0 + k;
-                            if (j >= 0 && j < V) {
-                                const float e = da[4 * q + k];
-                                da[4 * q + k] = __fmul_rn(
-                                    __fsub_rn(__fmul_rn(e, inv), j == y ? 1.0f : 0.0f), dscale);
-                            }
-                        }
-                    }
-                  }
-                }
-            } else {
-                // in place, or a non-finite max: recompute e_j element-wise
-                for (int64_t j = tid; j < V; j += kXentThreads) {
-                    const float e = det_exp(__fsub_rn(x[j], m));
-                    drow[j] = __fmul_rn(__fsub_rn(__fmul_rn(e, inv), j == y ? 1.0f : 0.0f),
-                                        dscale);
-                }
-            }
-        }
-        __syncthreads();    // bcast / red reuse by the next row
     }
 }
 
