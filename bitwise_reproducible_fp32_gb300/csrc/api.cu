@@ -136,6 +136,32 @@ DET_API det_status detgemm_f32(const det_profile_v1 *prof, int transA, int trans
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+DET_API det_status detgemm_f32_noalloc(const det_profile_v1 *prof, int transA, int transB,
+                                       int64_t M, int64_t N, int64_t K, const float *A,
+                                       int64_t lda, const float *B, int64_t ldb, float *C,
+                                       int64_t ldc, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (M < 0 || N < 0 || K < 0 || M > kDimMax || N > kDimMax || K > kDimMax)
+        return DET_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DET_OK;
+    const int64_t a_row = transA ? M : K, b_row = transB ? K : N;
+    if (ldc < N || lda < std::max<int64_t>(a_row, 1) || ldb < std::max<int64_t>(b_row, 1))
+        return DET_ERR_INVALID_ARG;
+    if (!C || (K > 0 && (!A || !B))) return DET_ERR_INVALID_ARG;
+    const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+    if (tiles > kDimMax) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    GemmArgs a;
+    a.M = M; a.N = N; a.K = K; a.lda = lda; a.ldb = ldb; a.ldc = ldc;
+    a.A = A; a.B = B; a.C = C; a.transA = transA != 0; a.transB = transB != 0;
+    bool too_big = false;
+    const cudaError_t e =
+        launch_gemm_noalloc(a, &too_big, reinterpret_cast<cudaStream_t>(stream));
+    if (too_big) return DET_ERR_WORKSPACE;
+    return from_cuda(e);
+}
+
 DET_API det_status detrmsnorm_f32(const det_profile_v1 *prof, int64_t rows, int64_t D,
                                   const float *x, int64_t ldx, const float *gain,
                                   float eps, float *y, int64_t ldy, float *inv_rms,

@@ -45,6 +45,7 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms);
 cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_bytes,
                         cudaStream_t s);
 cudaError_t gemm_watchdog(unsigned int *code, int clear);
+cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s);
 
 cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
                            const float *gain, float eps, float *y, int64_t ldy,

@@ -675,6 +675,58 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- no-allocation variant
+// Some callers cannot allocate device memory at the moment they multiply: code
+// running inside another framework's memory pool, where every allocation must
+// go through that pool, or a latency-critical loop where cudaMalloc's implicit
+// device synchronisation is not acceptable. For them detgemm_f32_noalloc runs
+// the split-K GEMM with its chunk partials in this fixed, file-scope scratch
+// array instead of a caller workspace. The array exists on every device that
+// loads this library, for the life of the process.
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;   // 64 MiB
+static __device__ __align__(256) float4 g_static_scratch[kStaticScratchBytes / 16];
+
+namespace {
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64];   // per device: the array's device address, once looked up
+}  // namespace
+
+// The device address of g_static_scratch on the current device. Looked up
+// once per device (the host-side name of a __device__ array is not a device
+// address), with that device current.
+static cudaError_t static_scratch(void **ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *ptr = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s) {
+    *too_big = false;
+    const GemmPlan pl = gemm_plan(a.M, a.N, a.K, sm_count_current_device());
+    if (pl.workspace_bytes > kStaticScratchBytes) {
+        *too_big = true;
+        return cudaSuccess;
+    }
+    void *scratch = nullptr;
+    if (pl.split) {
+        const cudaError_t e = static_scratch(&scratch);
+        if (e != cudaSuccess) return e;
+    }
+    // every slot of the scratch that the second pass reads is written first by
+    // this call, so nothing needs clearing between calls
+    return launch_gemm(a, scratch, pl.split ? kStaticScratchBytes : 0, s);
+}
+
 cudaError_t gemm_watchdog(unsigned int *code, int clear) {
     cudaError_t e = cudaMemcpyFromSymbol(code, g_gemm_watchdog, sizeof(unsigned int));
     if (e != cudaSuccess) return e;

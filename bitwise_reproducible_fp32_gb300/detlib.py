@@ -54,6 +54,8 @@ SIGNATURES = [
                            _vp, _i64, _vp, ctypes.c_size_t, _vp]),
     ("detgemm_workspace_bytes", _int, [_PROF, _int, _int, _i64, _i64, _i64,
                                        ctypes.POINTER(ctypes.c_size_t)]),
+    ("detgemm_f32_noalloc", _int, [_PROF, _int, _int, _i64, _i64, _i64, _vp, _i64, _vp,
+                                   _i64, _vp, _i64, _vp]),
     ("detrmsnorm_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _f, _vp, _i64, _vp,
                               _vp]),
     ("detxent_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i64, _f,
@@ -180,6 +182,29 @@ def detgemm_f32(A, B, C=None, transA=False, transB=False, workspace=None, profil
                             K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
                             ws_ptr, ws_bytes, _stream(stream))
     _check("detgemm_f32", st)
+    return C
+
+
+def detgemm_f32_noalloc(A, B, C, transA=False, transB=False, profile=None, stream=None):
+    """detgemm_f32 without any device allocation, for callers that cannot
+    allocate when they multiply (inside another framework's memory pool, or
+    in a loop that must not synchronise on cudaMalloc). C must be given; the
+    split-K scratch is the library's built-in 64 MiB array, shared by every
+    call on the device, so calls must not overlap on the GPU. Shapes that
+    would need more scratch raise DetError (DET_ERR_WORKSPACE)."""
+    _cuda_f32(A, "A", 2)
+    _cuda_f32(B, "B", 2)
+    _cuda_f32(C, "C", 2)
+    M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])
+    Kb, N = (B.shape[1], B.shape[0]) if transB else (B.shape[0], B.shape[1])
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {M} x {N}")
+    st = load().detgemm_f32_noalloc(_prof(profile), int(bool(transA)), int(bool(transB)),
+                                    M, N, K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C),
+                                    _ld(C), _stream(stream))
+    _check("detgemm_f32_noalloc", st)
     return C
 
 

@@ -122,6 +122,36 @@ det_status detgemm_f32(const det_profile_v1 *prof, int transA, int transB,
 det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA, int transB,
                                    int64_t M, int64_t N, int64_t K, size_t *bytes);
 
+/* detgemm_f32 for callers that cannot allocate device memory when they
+ * multiply: code that runs inside another framework's memory pool, where
+ * every allocation must go through that pool, or a latency-critical loop
+ * where cudaMalloc's implicit device synchronisation is not acceptable. The
+ * pages have no counterpart to this entry point; it only changes where the
+ * split-K scratch lives.
+ *
+ * Same arguments, arithmetic and result bits as detgemm_f32. Where
+ * detgemm_f32 would use a workspace, this call uses a scratch array built into
+ * the library instead: 64 MiB of device memory that every device which loads
+ * the library holds until the process exits. The call itself allocates
+ * nothing (no cudaMalloc, no allocating library routine).
+ *
+ * Limits and sharing:
+ *  - A shape whose split plan needs more than 64 MiB (detgemm_workspace_bytes
+ *    above 67,108,864) is refused with DET_ERR_WORKSPACE; nothing is launched.
+ *    Shapes that need no scratch always run.
+ *  - Every call on a device shares the one array, which keeps the previous
+ *    call's contents. A call writes every scratch element it reads, so no
+ *    clearing is needed, but calls whose kernels overlap on the GPU (two
+ *    streams, or concurrent host threads) race on the array: order them.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current). Make that first call before any
+ *    stream capture begins. */
+det_status detgemm_f32_noalloc(const det_profile_v1 *prof, int transA, int transB,
+                               int64_t M, int64_t N, int64_t K,
+                               const float *A, int64_t lda,
+                               const float *B, int64_t ldb,
+                               float *C, int64_t ldc, det_stream_t stream);
+
 /* RMSNorm over `rows` rows of D floats: y = (x * r) * gain, with
  * r = 1.0f / sqrtf(ss / (float)D + eps). "MojoLearn 162M" model card, table
  * "Compared with GPT-3 Small": RMSNorm, eps 1e-6, pre-norm.

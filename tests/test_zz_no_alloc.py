@@ -1,0 +1,50 @@
+"""detgemm_f32_noalloc: the GEMM for callers that cannot allocate device
+memory when they multiply (inside another framework's memory pool, or in a loop
+that must not synchronise on cudaMalloc). It must give the same bits as
+detgemm_f32 and refuse shapes whose split-K scratch exceeds its built-in
+64 MiB array. This file is collected last on purpose."""
+import numpy as np
+import pytest
+
+from bitcmp import assert_bitwise
+from bitwise_reproducible_fp32_gb300 import detlib
+from gpu_util import empty_dev, host, need_gpu, to_dev, torch
+
+pytestmark = pytest.mark.gpu
+F = np.float32
+
+CASES = [
+    # (M, N, K, transA, transB): the first three split K through the scratch
+    (300, 200, 1300, False, False),
+    (512, 384, 4096, True, False),
+    (129, 77, 2049, False, True),
+    (64, 64, 256, False, False),     # one chunk: no scratch needed
+]
+
+
+def test_noalloc_same_bits_as_detgemm_f32_two_calls_in_a_row():
+    need_gpu()
+    rng = np.random.default_rng(2024)
+    for M, N, K, tA, tB in CASES:
+        A = rng.standard_normal((K, M) if tA else (M, K)).astype(F)
+        B = rng.standard_normal((N, K) if tB else (K, N)).astype(F)
+        Ad, Bd = to_dev(A), to_dev(B)
+        ws = detlib.gemm_workspace(M, N, K, tA, tB)
+        ref = host(detlib.detgemm_f32(Ad, Bd, transA=tA, transB=tB, workspace=ws))
+        for call in range(2):
+            C = empty_dev(M, N)
+            detlib.detgemm_f32_noalloc(Ad, Bd, C, transA=tA, transB=tB)
+            torch.cuda.synchronize()
+            assert_bitwise(host(C), ref, f"M={M} N={N} K={K} call {call}")
+
+
+def test_noalloc_refuses_shapes_beyond_its_scratch():
+    need_gpu()
+    M, N, K = 768, 2304, 8192      # needs ~221 MB of split-K scratch
+    assert detlib.detgemm_workspace_bytes(M, N, K, True, False) > 64 * 2 ** 20
+    A = torch.zeros((K, M), dtype=torch.float32, device="cuda")
+    B = torch.zeros((K, N), dtype=torch.float32, device="cuda")
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    with pytest.raises(detlib.DetError) as err:
+        detlib.detgemm_f32_noalloc(A, B, C, transA=True)
+    assert err.value.status == 5      # DET_ERR_WORKSPACE
