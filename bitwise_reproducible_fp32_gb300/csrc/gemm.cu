@@ -73,7 +73,7 @@ constexpr int B_FLOATS = BN * BK;               // 4096
 constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
 constexpr int TOTAL_FLOAT4 = THREADS * TM * TN / 4;   // running totals
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_FLOATS * 4 +
-                              size_t(TOTAL_FLOAT4) * 16 + STAGES * 8;
+                              size_t(TOTAL_FLOAT4) * 16 + 2 * STAGES * 8;
 static_assert(kKChunk % BK == 0, "chunk boundaries must fall on k-tiles");
 static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
 
@@ -317,12 +317,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB, const KArgs p) {
     __shared__ Producer prod;
+    __shared__ volatile int abort_flag;
     extern __shared__ unsigned char smem_raw[];
     float *smem = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *stages = smem;
     float4 *totals = reinterpret_cast<float4 *>(smem + STAGES * STAGE_FLOATS);
-    uint64_t *full = reinterpret_cast<uint64_t *>(totals + TOTAL_FLOAT4);
+    uint64_t *full = reinterpret_cast<uint64_t *>(totals + TOTAL_FLOAT4);   // data landed
+    uint64_t *empty = full + STAGES;                 // all 8 warps done reading
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -352,7 +354,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     if (TMA) {
         if (tid == 0) {
-            for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&full[s]), 1);
+            for (int s = 0; s < STAGES; ++s) {
+                mbar_init(smem_u32(&full[s]), 1);
+                mbar_init(smem_u32(&empty[s]), THREADS / 32);
+            }
+            abort_flag = 0;
             fence_mbar_init();
             prod.ui = 0;
             prod.count = 0;
@@ -382,7 +388,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float *Bs = As + A_FLOATS;
             int ok = 1;
             if (TMA) {
-                ok = mbar_wait_bounded(smem_u32(&full[s]), uint32_t(it / STAGES) & 1u);
+                ok = mbar_wait_or_abort(smem_u32(&full[s]), uint32_t(it / STAGES) & 1u,
+                                        &abort_flag);
             } else {
                 __syncthreads();   // everyone is done with the previous k-tile
                 load_tile_plain<A_KM, BM>(stages, p.A, p.lda, p.M, p.K, w.m0, kt * BK, tid);
@@ -449,8 +456,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (TMA) {
-                if (__syncthreads_or(!ok)) { aborted = true; ++it; break; }
-                if (tid == 0 && prod.more) issue_next(s);
+                // release the stage: one arrival a warp. No CTA-wide barrier: the
+                // producer (thread 0) waits for the 8 arrivals before refilling
+                // this stage, and the other warps only ever wait for data.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+                if (tid == 0 && prod.more && !abort_flag) {
+                    if (mbar_wait_or_abort(smem_u32(&empty[s]), uint32_t(it / STAGES) & 1u,
+                                           &abort_flag))
+                        issue_next(s);
+                }
+                __syncwarp();
+                if (!ok || abort_flag) { aborted = true; ++it; break; }
             }
         }
         if (aborted) break;
@@ -461,10 +478,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     if (TMA && aborted && tid == 0) {
+        // every warp sees the shared abort flag within one k-tile and leaves its
+        // loop. Thread 0 records the event and lets the last copy issued on
+        // each stage land before it exits (the CTA's shared memory lives until
+        // its last thread exits); each wait is bounded.
         atomicOr(&g_gemm_watchdog, kWatchdogGemm);
-        // let the copies still in flight land before the CTA exits: sequence
-        // positions it-1 .. prod.count-1 may still be pending
-        for (int64_t t = it - 1; t < prod.count; ++t)
+        for (int64_t t = prod.count > STAGES ? prod.count - STAGES : 0; t < prod.count; ++t)
             (void)mbar_wait_bounded(smem_u32(&full[t % STAGES]), uint32_t(t / STAGES) & 1u);
     }
 }
