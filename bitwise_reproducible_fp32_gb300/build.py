@@ -66,8 +66,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if log.strip():
                 print(log, file=sys.stderr)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp,
-           *[o for o, _ in results]]
+    # --no-undefined: an unresolved symbol fails the build, not the first load
+    cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-Xlinker", "--no-undefined",
+           "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -228,8 +228,9 @@ DET_API det_status detlog_f32(const det_profile_v1 *prof, int64_t n, const float
 
 DET_API det_status det_watchdog_status(int32_t *code, int clear) {
     if (!code) return DET_ERR_INVALID_ARG;
-    unsigned int c = 0;
+    unsigned int c = 0, c2 = 0;
     cudaError_t e = gemm_watchdog(&c, clear);
-    *code = int32_t(c);
+    if (e == cudaSuccess) e = rowops_watchdog(&c2, clear);
+    *code = int32_t(c | c2);
     return from_cuda(e);
 }

@@ -23,7 +23,8 @@ constexpr int kGroup = 4;        // consecutive elements per chain per sweep
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Watchdog bits (det_watchdog_status).
-constexpr unsigned int kWatchdogGemm = 1u;
+constexpr unsigned int kWatchdogGemm = 1u;   // GEMM operand staging
+// bit 1 (2u): cross-entropy row staging, defined in rowops.cu
 
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error; arguments are validated by
@@ -47,6 +48,7 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
 cudaError_t gemm_watchdog(unsigned int *code, int clear);
 cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s);
 
+cudaError_t rowops_watchdog(unsigned int *code, int clear);
 cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
                            const float *gain, float eps, float *y, int64_t ldy,
                            float *inv_rms, cudaStream_t s);

@@ -108,51 +108,60 @@ __device__ __forceinline__ float warp_butterfly_sum(float s) {
 constexpr int kRmsWarps = 8;
 constexpr int kRmsMaxNG = 8;
 
-template <int NG>
-__global__ void __launch_bounds__(kRmsWarps * 32, (NG <= 4 ? 7 : NG <= 6 ? 6 : 4))
+template <int NG, int RPW>
+__global__ void __launch_bounds__(kRmsWarps * 32, 4)
     rmsnorm_vec_kernel(int64_t rows, int64_t D, const float *__restrict__ x, int64_t ldx,
                        const float *__restrict__ gain, float eps, float *__restrict__ y,
                        int64_t ldy, float *__restrict__ inv_rms) {
+    // RPW rows a warp: every row's loads are issued before any is used
     const int lane = threadIdx.x & 31;
-    const int64_t row = int64_t(blockIdx.x) * kRmsWarps + (threadIdx.x >> 5);
-    if (row >= rows) return;
-    const float4 *xr = reinterpret_cast<const float4 *>(x + row * ldx);
+    const int64_t row0 = (int64_t(blockIdx.x) * kRmsWarps + (threadIdx.x >> 5)) * RPW;
     const int ngroups = int(D >> 2);
-    float4 v[NG];
+    float4 v[RPW][NG];
 #pragma unroll
-    for (int t = 0; t < NG; ++t) {
-        const int g = lane + 32 * t;
-        if (g < ngroups) v[t] = __ldcs(xr + g);
-    }
-    float s = 0.0f;
+    for (int q = 0; q < RPW; ++q) {
+        if (row0 + q >= rows) break;
+        const float4 *xr = reinterpret_cast<const float4 *>(x + (row0 + q) * ldx);
 #pragma unroll
-    for (int t = 0; t < NG; ++t) {
-        if (lane + 32 * t < ngroups) {
-            s = __fmaf_rn(v[t].x, v[t].x, s);
-            s = __fmaf_rn(v[t].y, v[t].y, s);
-            s = __fmaf_rn(v[t].z, v[t].z, s);
-            s = __fmaf_rn(v[t].w, v[t].w, s);
+        for (int t = 0; t < NG; ++t) {
+            const int g = lane + 32 * t;
+            if (g < ngroups) v[q][t] = __ldcs(xr + g);
         }
     }
-    const float ss = warp_butterfly_sum(s);
-    const float r =
-        __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, __ll2float_rn(D)), eps)));
-    float4 *yr = reinterpret_cast<float4 *>(y + row * ldy);
     const float4 *g4 = reinterpret_cast<const float4 *>(gain);
+    const float Df = __ll2float_rn(D);
 #pragma unroll
-    for (int t = 0; t < NG; ++t) {
-        const int g = lane + 32 * t;
-        if (g < ngroups) {
-            const float4 gg = __ldg(g4 + g);
-            float4 o;
-            o.x = __fmul_rn(__fmul_rn(v[t].x, r), gg.x);
-            o.y = __fmul_rn(__fmul_rn(v[t].y, r), gg.y);
-            o.z = __fmul_rn(__fmul_rn(v[t].z, r), gg.z);
-            o.w = __fmul_rn(__fmul_rn(v[t].w, r), gg.w);
-            __stcs(yr + g, o);
+    for (int q = 0; q < RPW; ++q) {
+        const int64_t row = row0 + q;
+        if (row >= rows) break;
+        float s = 0.0f;
+#pragma unroll
+        for (int t = 0; t < NG; ++t) {
+            if (lane + 32 * t < ngroups) {
+                s = __fmaf_rn(v[q][t].x, v[q][t].x, s);
+                s = __fmaf_rn(v[q][t].y, v[q][t].y, s);
+                s = __fmaf_rn(v[q][t].z, v[q][t].z, s);
+                s = __fmaf_rn(v[q][t].w, v[q][t].w, s);
+            }
         }
+        const float ss = warp_butterfly_sum(s);
+        const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, Df), eps)));
+        float4 *yr = reinterpret_cast<float4 *>(y + row * ldy);
+#pragma unroll
+        for (int t = 0; t < NG; ++t) {
+            const int g = lane + 32 * t;
+            if (g < ngroups) {
+                const float4 gg = __ldg(g4 + g);
+                float4 o;
+                o.x = __fmul_rn(__fmul_rn(v[q][t].x, r), gg.x);
+                o.y = __fmul_rn(__fmul_rn(v[q][t].y, r), gg.y);
+                o.z = __fmul_rn(__fmul_rn(v[q][t].z, r), gg.z);
+                o.w = __fmul_rn(__fmul_rn(v[q][t].w, r), gg.w);
+                __stcs(yr + g, o);
+            }
+        }
+        if (inv_rms && lane == 0) inv_rms[row] = r;
     }
-    if (inv_rms && lane == 0) inv_rms[row] = r;
 }
 
 __global__ void __launch_bounds__(kRmsWarps * 32)
@@ -273,6 +282,7 @@ __device__ __forceinline__ void st_policy(float *p, float v, uint64_t pol) {
 // storing it.
 constexpr int kXentThreads = 256;
 constexpr int kU = 4;    // independent 16-byte loads a thread keeps in flight
+constexpr int kP = 4;    // chain-pass sweeps loaded ahead
 static_assert(kXentThreads == kXentLanes, "one thread per chain");
 
 __device__ __forceinline__ float dl_of(float e, float inv, float dscale) {
@@ -358,16 +368,15 @@ __device__ __noinline__ float xent_checked_sweep(const float *xa, int V, int g, 
     return s;
 }
 
+// Pass 1: this thread's share of the row max over granules (order-free,
+// NaN-propagating); the granules fully inside the row are read kU at a time
+// and kept in L2 for pass 2.
 template <int H>
-__device__ __noinline__ void xent_row(const float *x, int V, int y, float *drow, bool in_place,
-                                         float dscale, float *loss_out, float *red, float *bcast,
-                                         uint64_t keep, uint64_t drop) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float *xa = x - H;                        // 16-byte aligned
-    const int nch = (V + H + 3) >> 2;               // granules touching the row
-    const int q_lo = H == 0 ? 0 : 1;                // granules fully inside the row:
-    const int q_hi = (V + H) >> 2;                  //   [q_lo, q_hi)
-    // 1. m = max (order-free, NaN-propagating)
+__device__ __noinline__ float xent_max_part(const float *x, int V, uint64_t keep) {
+    const int tid = threadIdx.x;
+    const float *xa = x - H;
+    const int nch = (V + H + 3) >> 2;
+    const int q_lo = H == 0 ? 0 : 1, q_hi = (V + H) >> 2;   // granules inside the row
     float m = x[0];
     for (int q0 = q_lo + tid; q0 < q_hi; q0 += kXentThreads * kU) {
         float4 v[kU];
@@ -392,6 +401,108 @@ __device__ __noinline__ void xent_row(const float *x, int V, int y, float *drow,
             }
         }
     }
+    return m;
+}
+
+// Pass 2: chain tid's sum over its groups g = tid + 256 t, storing each e_j to
+// drow when store_e.
+template <int H>
+__device__ __noinline__ float xent_chain(const float *x, int V, float m, bool finite_m,
+                                         float *drow, bool store_e, uint64_t keep,
+                                         uint64_t drop) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const float *xa = x - H;
+    float s = 0.0f;
+    const int ngroups = (V + 3) >> 2;
+    const int t_all = (ngroups + kXentThreads - 1) / kXentThreads;
+    // sweeps 1 .. t_fast-1 have every group full and inside the row
+    const int t_fast = finite_m ? (V >> 2) / kXentThreads : 0;
+    s = xent_checked_sweep<H>(xa, V, tid, m, finite_m, drow, store_e, s, keep);
+    // fast sweeps, kP at a time: all their loads are issued before any is used
+    for (int t0 = 1; t0 < t_fast; t0 += kP) {
+        float4 c0[kP], own[kP];
+#pragma unroll
+        for (int u = 0; u < kP; ++u) {
+            const int g = tid + (t0 + u) * kXentThreads;
+            own[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t0 + u < t_fast) {
+                c0[u] = ld4_policy(xa + 4 * g, drop);
+                if (H != 0 && lane == 31) own[u] = ld4_policy(xa + 4 * (g + 1), drop);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kP; ++u) {
+            if (t0 + u >= t_fast) break;             // uniform across the CTA
+            const int g = tid + (t0 + u) * kXentThreads;
+            const float4 v = group_of<H>(c0[u], next_granule<H>(c0[u], own[u], lane));
+            const float4 e = exp4(v, m);
+            s = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(s, e.x), e.y), e.z), e.w);
+            if (store_e) {
+                float *dp = drow + 4 * g;
+                st_policy(dp, e.x, keep); st_policy(dp + 1, e.y, keep);
+                st_policy(dp + 2, e.z, keep); st_policy(dp + 3, e.w, keep);
+            }
+        }
+    }
+    for (int t = t_fast < 1 ? 1 : t_fast; t < t_all; ++t)
+        s = xent_checked_sweep<H>(xa, V, tid + t * kXentThreads, m, finite_m, drow, store_e, s,
+                                  keep);
+    return s;
+}
+
+// Pass 4: d_j = (e_j * inv - [j == y]) * dscale over the dlogits row, reading
+// back the e_j that pass 2 stored.
+__device__ __noinline__ void xent_dlogits_from_e(float *drow, int V, int y, float inv,
+                                                 float dscale, uint64_t drop) {
+    const int tid = threadIdx.x;
+    const int hd = int((reinterpret_cast<uintptr_t>(drow) >> 2) & 3);
+    float *da = drow - hd;                           // 16-byte aligned
+    const int dq_lo = hd == 0 ? 0 : 1, dq_hi = (V + hd) >> 2, dch = (V + hd + 3) >> 2;
+    for (int q0 = dq_lo + tid; q0 < dq_hi; q0 += kXentThreads * kU) {
+        float4 es[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int q = q0 + u * kXentThreads;
+            if (q < dq_hi) es[u] = ld4_policy(da + 4 * q, drop);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int q = q0 + u * kXentThreads;
+            if (q >= dq_hi) break;
+            const float4 e = es[u];
+            float4 o = make_float4(dl_of(e.x, inv, dscale), dl_of(e.y, inv, dscale),
+                                   dl_of(e.z, inv, dscale), dl_of(e.w, inv, dscale));
+            const unsigned k = unsigned(y - (4 * q - hd));
+            if (k < 4) {      // the label's element: rare
+                if (k == 0) o.x = dl_of_label(e.x, inv, dscale);
+                if (k == 1) o.y = dl_of_label(e.y, inv, dscale);
+                if (k == 2) o.z = dl_of_label(e.z, inv, dscale);
+                if (k == 3) o.w = dl_of_label(e.w, inv, dscale);
+            }
+            __stcs(reinterpret_cast<float4 *>(da + 4 * q), o);
+        }
+    }
+    if (tid < 2) {    // the partial granules at the two ends
+        const int q = tid == 0 ? 0 : dq_hi;
+        if ((tid == 0 && dq_lo == 1) || (tid == 1 && dq_hi < dch && dq_hi >= dq_lo)) {
+            for (int i = 0; i < 4; ++i) {
+                const int j = 4 * q - hd + i;
+                if (j >= 0 && j < V) {
+                    const float e = drow[j];
+                    drow[j] = j == y ? dl_of_label(e, inv, dscale) : dl_of(e, inv, dscale);
+                }
+            }
+        }
+    }
+}
+
+template <int H>
+__device__ __forceinline__ void xent_row(const float *x, int V, int y, float *drow, bool in_place,
+                                         float dscale, float *loss_out, float *red, float *bcast,
+                                         uint64_t keep, uint64_t drop) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // 1. m = max
+    float m = xent_max_part<H>(x, V, keep);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) m = max_nan(__shfl_xor_sync(0xffffffffu, m, off), m);
     if (lane == 0) red[warp] = m;
@@ -405,33 +516,8 @@ __device__ __noinline__ void xent_row(const float *x, int V, int y, float *drow,
     m = *bcast;
     const bool finite_m = fabsf(m) <= 3.402823466e38f;     // false for NaN / inf
     const bool store_e = drow != nullptr && !in_place && finite_m;
-    const int hd = drow ? int((reinterpret_cast<uintptr_t>(drow) >> 2) & 3) : 0;
-    float *da = drow ? drow - hd : nullptr;          // 16-byte aligned dlogits row
-
-    // 2. chain sums: sweep t covers groups g = tid + 256 t
-    float s = 0.0f;
-    const int ngroups = (V + 3) >> 2;
-    const int t_all = (ngroups + kXentThreads - 1) / kXentThreads;
-    // sweeps 1 .. t_fast-1 have every group full and inside the row
-    const int t_fast = finite_m ? (V >> 2) / kXentThreads : 0;
-    s = xent_checked_sweep<H>(xa, V, tid, m, finite_m, drow, store_e, s, keep);
-    for (int t = 1; t < t_fast; ++t) {
-        const int g = tid + t * kXentThreads;
-        const float4 c0 = ld4_policy(xa + 4 * g, drop);
-        float4 own = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (H != 0 && lane == 31) own = ld4_policy(xa + 4 * (g + 1), drop);
-        const float4 v = group_of<H>(c0, next_granule<H>(c0, own, lane));
-        const float4 e = exp4(v, m);
-        s = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(s, e.x), e.y), e.z), e.w);
-        if (store_e) {
-            float *dp = drow + 4 * g;
-            st_policy(dp, e.x, keep); st_policy(dp + 1, e.y, keep);
-            st_policy(dp + 2, e.z, keep); st_policy(dp + 3, e.w, keep);
-        }
-    }
-    for (int t = t_fast < 1 ? 1 : t_fast; t < t_all; ++t)
-        s = xent_checked_sweep<H>(xa, V, tid + t * kXentThreads, m, finite_m, drow, store_e, s,
-                                  keep);
+    // 2. chain sums
+    float s = xent_chain<H>(x, V, m, finite_m, drow, store_e, keep, drop);
     // 3. butterfly: 16..1 in the warp, then 32, 64, 128 across warps
     s = warp_butterfly_sum(s);
     __syncthreads();    // red[] reuse
@@ -449,43 +535,7 @@ __device__ __noinline__ void xent_row(const float *x, int V, int y, float *drow,
     if (drow) {
         const float inv = __fdiv_rn(1.0f, *bcast);
         if (store_e) {
-            const int dq_lo = hd == 0 ? 0 : 1, dq_hi = (V + hd) >> 2, dch = (V + hd + 3) >> 2;
-            for (int q0 = dq_lo + tid; q0 < dq_hi; q0 += kXentThreads * kU) {
-                float4 es[kU];
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int q = q0 + u * kXentThreads;
-                    if (q < dq_hi) es[u] = ld4_policy(da + 4 * q, drop);
-                }
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int q = q0 + u * kXentThreads;
-                    if (q >= dq_hi) break;
-                    const float4 e = es[u];
-                    float4 o = make_float4(dl_of(e.x, inv, dscale), dl_of(e.y, inv, dscale),
-                                           dl_of(e.z, inv, dscale), dl_of(e.w, inv, dscale));
-                    const unsigned k = unsigned(y - (4 * q - hd));
-                    if (k < 4) {      // the label's element: rare
-                        if (k == 0) o.x = dl_of_label(e.x, inv, dscale);
-                        if (k == 1) o.y = dl_of_label(e.y, inv, dscale);
-                        if (k == 2) o.z = dl_of_label(e.z, inv, dscale);
-                        if (k == 3) o.w = dl_of_label(e.w, inv, dscale);
-                    }
-                    __stcs(reinterpret_cast<float4 *>(da + 4 * q), o);
-                }
-            }
-            if (tid < 2) {    // the partial granules at the two ends
-                const int q = tid == 0 ? 0 : dq_hi;
-                if ((tid == 0 && dq_lo == 1) || (tid == 1 && dq_hi < dch && dq_hi >= dq_lo)) {
-                    for (int i = 0; i < 4; ++i) {
-                        const int j = 4 * q - hd + i;
-                        if (j >= 0 && j < V) {
-                            const float e = drow[j];
-                            drow[j] = j == y ? dl_of_label(e, inv, dscale) : dl_of(e, inv, dscale);
-                        }
-                    }
-                }
-            }
+            xent_dlogits_from_e(drow, V, y, inv, dscale, drop);
         } else {
             // in place, or a non-finite max: recompute e_j element-wise
             for (int j = tid; j < V; j += kXentThreads) {
@@ -529,6 +579,213 @@ __global__ void __launch_bounds__(kXentThreads, 2)
     }
 }
 
+// ---------------------------------------------------------------- cross-entropy, row in shared memory
+// For rows that fit in shared memory (V up to ~58,000 floats: the 162M model's
+// 50,257-id vocabulary is 201 KB), one 1024-thread CTA per SM keeps the whole
+// row on chip, so DRAM sees one read of the logits and one write of dlogits:
+//  A. the row's 16-byte granules arrive by TMA bulk copies (two halves, each
+//     on its own mbarrier); the next row's halves are copied in while this
+//     row's dlogits are written out;
+//  B. m = max over the granules (NaN-propagating, elements outside the row
+//     masked);
+//  C. e = exp(x - m) in place, element-wise, by all 32 warps;
+//  D. chains 0..255 add their groups' e values in ascending order from shared
+//     memory; butterfly; loss = log(S) - (x_y - m);
+//  E. d_j = (e_j (1/S) - [j == y]) dscale, written as 16-byte granules where
+//     the dlogits row shares the logits row's alignment.
+// The operations and their order are those of the register kernel below.
+constexpr int kXsThreads = 1024;
+constexpr int kXsMaxGranules = 14400;            // 230,400 bytes of row buffer
+constexpr int kXsPiece = 1024;                   // granules per bulk copy (16 KB)
+constexpr unsigned kWatchdogXent = 2u;
+
+__device__ unsigned int g_rowops_watchdog;
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Thread 0: copies granules [q0, q1) of the row whose aligned base is xa into
+// the same granules of buf, completing on bar.
+__device__ __forceinline__ void load_granules(float4 *buf, const float *xa, int q0, int q1,
+                                              uint64_t *bar) {
+    const uint32_t b = smem_u32(bar);
+    mbar_arrive_expect_tx(b, uint32_t(q1 - q0) * 16u);
+    for (int q = q0; q < q1; q += kXsPiece) {
+        const int n = min(kXsPiece, q1 - q);
+        bulk_load(smem_u32(buf + q), xa + 4 * q, uint32_t(n) * 16u, b);
+    }
+}
+
+__global__ void __launch_bounds__(kXsThreads, 1)
+    xent_smem_kernel(int64_t rows, int V, const float *logits, int64_t ld,
+                     const int32_t *__restrict__ labels, float *__restrict__ loss,
+                     float *dlogits, int64_t ldd, float dscale, int32_t *dev_status) {
+    extern __shared__ float4 buf[];
+    __shared__ uint64_t bar[2];
+    __shared__ float red[32];
+    __shared__ float bcast;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int split = ((V + 3) >> 2) / 2;           // granules of half 0, every row
+    auto aligned_row = [&](int64_t r) {
+        const float *x = logits + r * ld;
+        return x - int((reinterpret_cast<uintptr_t>(x) >> 2) & 3);
+    };
+    auto granules = [&](int64_t r) {
+        const float *x = logits + r * ld;
+        return (V + int((reinterpret_cast<uintptr_t>(x) >> 2) & 3) + 3) >> 2;
+    };
+    if (tid == 0) {
+        mbar_init(smem_u32(&bar[0]), 1);
+        mbar_init(smem_u32(&bar[1]), 1);
+        fence_mbar_init();
+        if (int64_t(blockIdx.x) < rows) {
+            load_granules(buf, aligned_row(blockIdx.x), 0, split, &bar[0]);
+            load_granules(buf, aligned_row(blockIdx.x), split, granules(blockIdx.x), &bar[1]);
+        }
+    }
+    __syncthreads();
+    int k = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++k) {
+        const float *x = logits + row * ld;
+        const int h = int((reinterpret_cast<uintptr_t>(x) >> 2) & 3);
+        const int nch = (V + h + 3) >> 2;
+        const int64_t next = row + gridDim.x;
+        const int y32 = labels[row];
+        const bool bad = y32 < 0 || y32 >= V;
+        const int y = y32;
+        float *drow = dlogits ? dlogits + row * ldd : nullptr;
+        // A. the row has landed (both halves)
+        bool ok = mbar_wait_bounded(smem_u32(&bar[0]), uint32_t(k) & 1u);
+        ok = mbar_wait_bounded(smem_u32(&bar[1]), uint32_t(k) & 1u) && ok;
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(&g_rowops_watchdog, kWatchdogXent);
+                (void)mbar_wait_bounded(smem_u32(&bar[0]), uint32_t(k) & 1u);
+                (void)mbar_wait_bounded(smem_u32(&bar[1]), uint32_t(k) & 1u);
+            }
+            return;
+        }
+        float inv = 0.0f;
+        bool vec_out = false;
+        if (!bad) {
+            // B. max
+            float m = x[0];
+            for (int q = tid; q < nch; q += kXsThreads) {
+                const float4 v = buf[q];
+                const int j0 = 4 * q - h;
+                if (j0 >= 0 && j0 + 3 < V) {
+                    m = max_nan(m, max_nan(max_nan(v.x, v.y), max_nan(v.z, v.w)));
+                } else {
+                    if (j0 >= 0 && j0 < V) m = max_nan(m, v.x);
+                    if (j0 + 1 >= 0 && j0 + 1 < V) m = max_nan(m, v.y);
+                    if (j0 + 2 >= 0 && j0 + 2 < V) m = max_nan(m, v.z);
+                    if (j0 + 3 >= 0 && j0 + 3 < V) m = max_nan(m, v.w);
+                }
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                m = max_nan(__shfl_xor_sync(0xffffffffu, m, off), m);
+            if (lane == 0) red[warp] = m;
+            __syncthreads();
+            if (tid == 0) {
+                float mm = red[0];
+                for (int w = 1; w < kXsThreads / 32; ++w) mm = max_nan(red[w], mm);
+                bcast = mm;
+            }
+            __syncthreads();
+            m = bcast;
+            const bool finite_m = fabsf(m) <= 3.402823466e38f;
+            // C. e = exp(x - m) in place (elements outside the row are never read)
+            if (finite_m) {
+                for (int q = tid; q < nch; q += kXsThreads) buf[q] = exp4(buf[q], m);
+            } else {
+                for (int q = tid; q < nch; q += kXsThreads) {
+                    const float4 v = buf[q];
+                    buf[q] = make_float4(det_exp_call(__fsub_rn(v.x, m)), det_exp_call(__fsub_rn(v.y, m)),
+                                         det_exp_call(__fsub_rn(v.z, m)), det_exp_call(__fsub_rn(v.w, m)));
+                }
+            }
+            __syncthreads();
+            // D. the 256 chains, groups g = l, l + 256, ... in ascending order
+            const float *ef = reinterpret_cast<const float *>(buf) + h;   // e of element j at ef[j]
+            if (tid < kXentLanes) {
+                float s = 0.0f;
+                const int ngroups = (V + 3) >> 2, gfull = V >> 2;
+                int g = tid;
+                for (; g < gfull; g += kXentLanes) {
+                    const float *p = ef + 4 * g;
+                    s = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(s, p[0]), p[1]), p[2]), p[3]);
+                }
+                if (g < ngroups)
+                    for (int j = 4 * g; j < V; ++j) s = __fadd_rn(s, ef[j]);
+                s = warp_butterfly_sum(s);
+                if (lane == 0) red[warp] = s;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                const float a01 = __fadd_rn(red[0], red[1]), a23 = __fadd_rn(red[2], red[3]);
+                const float a45 = __fadd_rn(red[4], red[5]), a67 = __fadd_rn(red[6], red[7]);
+                const float S = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
+                bcast = S;
+                loss[row] = __fsub_rn(det_log(S), __fsub_rn(x[y], m));
+            }
+            __syncthreads();
+            inv = __fdiv_rn(1.0f, bcast);
+            vec_out = drow != nullptr &&
+                      int((reinterpret_cast<uintptr_t>(drow) >> 2) & 3) == h;
+        } else {
+            if (tid == 0) {
+                loss[row] = __uint_as_float(0x7fc00000u);
+                if (dev_status) atomicOr(reinterpret_cast<int *>(dev_status), 1);
+            }
+        }
+        // E. dlogits, half 0 then half 1; each half's buffer is refilled with
+        // the next row as soon as it is free
+        for (int hf = 0; hf < 2; ++hf) {
+            const int q0 = hf == 0 ? 0 : split, q1 = hf == 0 ? split : nch;
+            if (drow) {
+                for (int q = q0 + tid; q < q1; q += kXsThreads) {
+                    const int j0 = 4 * q - h;
+                    if (bad) {
+                        for (int i = 0; i < 4; ++i)
+                            if (j0 + i >= 0 && j0 + i < V) drow[j0 + i] = __uint_as_float(0x7fc00000u);
+                        continue;
+                    }
+                    const float4 e = buf[q];
+                    float4 o = make_float4(dl_of(e.x, inv, dscale), dl_of(e.y, inv, dscale),
+                                           dl_of(e.z, inv, dscale), dl_of(e.w, inv, dscale));
+                    const unsigned kk = unsigned(y - j0);
+                    if (kk < 4) {
+                        if (kk == 0) o.x = dl_of_label(e.x, inv, dscale);
+                        if (kk == 1) o.y = dl_of_label(e.y, inv, dscale);
+                        if (kk == 2) o.z = dl_of_label(e.z, inv, dscale);
+                        if (kk == 3) o.w = dl_of_label(e.w, inv, dscale);
+                    }
+                    if (vec_out && j0 >= 0 && j0 + 3 < V) {
+                        __stcs(reinterpret_cast<float4 *>(drow + j0), o);
+                    } else {
+                        if (j0 >= 0 && j0 < V) drow[j0] = o.x;
+                        if (j0 + 1 >= 0 && j0 + 1 < V) drow[j0 + 1] = o.y;
+                        if (j0 + 2 >= 0 && j0 + 2 < V) drow[j0 + 2] = o.z;
+                        if (j0 + 3 >= 0 && j0 + 3 < V) drow[j0 + 3] = o.w;
+                    }
+                }
+            }
+            __syncthreads();
+            if (tid == 0 && next < rows) {
+                if (hf == 0) load_granules(buf, aligned_row(next), 0, split, &bar[0]);
+                else load_granules(buf, aligned_row(next), split, granules(next), &bar[1]);
+            }
+        }
+    }
+}
+
+
 // Mean of n floats: 32 chains (groups of 4, plain adds), butterfly, / n.
 // The CTA stages blocks of kMeanBlock floats in shared memory with coalesced
 // loads; warp 0 then runs the 32 chains over the block. kMeanBlock is a
@@ -570,6 +827,16 @@ __global__ void exp_map_kernel(int64_t n, const float *x, float *y, int is_log) 
 
 }  // namespace
 
+cudaError_t rowops_watchdog(unsigned int *code, int clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_rowops_watchdog, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    if (clear && *code) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_rowops_watchdog, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
+
 cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
                            const float *gain, float eps, float *y, int64_t ldy,
                            float *inv_rms, cudaStream_t s) {
@@ -584,15 +851,18 @@ cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
         rmsnorm_kernel<<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms);
         return cudaGetLastError();
     }
+    // two rows a warp up to 6 groups a lane (D <= 768), one beyond
+    const int64_t blocks2 = (rows + 2 * kRmsWarps - 1) / (2 * kRmsWarps);
+    const dim3 grid2{unsigned(blocks2)};
     switch ((D + 127) / 128) {
-        case 1: rmsnorm_vec_kernel<1><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
-        case 2: rmsnorm_vec_kernel<2><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
-        case 3: rmsnorm_vec_kernel<3><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
-        case 4: rmsnorm_vec_kernel<4><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
-        case 5: rmsnorm_vec_kernel<5><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
-        case 6: rmsnorm_vec_kernel<6><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
-        case 7: rmsnorm_vec_kernel<7><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
-        default: rmsnorm_vec_kernel<8><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
+        case 1: rmsnorm_vec_kernel<1, 2><<<grid2, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
+        case 2: rmsnorm_vec_kernel<2, 2><<<grid2, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
+        case 3: rmsnorm_vec_kernel<3, 2><<<grid2, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
+        case 4: rmsnorm_vec_kernel<4, 2><<<grid2, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
+        case 5: rmsnorm_vec_kernel<5, 2><<<grid2, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
+        case 6: rmsnorm_vec_kernel<6, 2><<<grid2, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
+        case 7: rmsnorm_vec_kernel<7, 1><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
+        default: rmsnorm_vec_kernel<8, 1><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
     }
     return cudaGetLastError();
 }
@@ -602,10 +872,22 @@ cudaError_t launch_xent(int64_t rows, int64_t V, const float *logits, int64_t ld
                         float *dlogits, int64_t ldd, float dscale, int32_t *dev_status,
                         cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    const int64_t grid = std::min<int64_t>(rows, int64_t(sm_count_current_device()) * 2);
-    xent_kernel<<<unsigned(grid), kXentThreads, 0, s>>>(rows, V, logits, ld, labels, loss,
-                                                        dlogits, ldd, dscale, dev_status);
-    cudaError_t e = cudaGetLastError();
+    const int64_t max_granules = (V + 3 + 3) / 4 + 1;
+    cudaError_t e;
+    if (max_granules <= kXsMaxGranules) {
+        const size_t smem = size_t(max_granules) * 16;
+        e = cudaFuncSetAttribute(xent_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem));
+        if (e != cudaSuccess) return e;
+        const int64_t grid = std::min<int64_t>(rows, int64_t(sm_count_current_device()));
+        xent_smem_kernel<<<unsigned(grid), kXsThreads, smem, s>>>(
+            rows, int(V), logits, ld, labels, loss, dlogits, ldd, dscale, dev_status);
+    } else {
+        const int64_t grid = std::min<int64_t>(rows, int64_t(sm_count_current_device()) * 2);
+        xent_kernel<<<unsigned(grid), kXentThreads, 0, s>>>(rows, V, logits, ld, labels, loss,
+                                                            dlogits, ldd, dscale, dev_status);
+    }
+    e = cudaGetLastError();
     if (e != cudaSuccess || !loss_mean) return e;
     mean_kernel<<<1, kMeanThreads, 0, s>>>(rows, loss, loss_mean);
     return cudaGetLastError();

@@ -250,7 +250,8 @@ det_status detlog_f32(const det_profile_v1 *prof, int64_t n, const float *x,
 
 /* Reads, and optionally clears, the current device's watchdog word.
  * *code == 0 means no bounded device wait has ever given up; otherwise bit k
- * identifies the kernel family that gave up (bit 0: GEMM operand staging).
+ * identifies the kernel family that gave up (bit 0: GEMM operand staging,
+ * bit 1: cross-entropy row staging).
  * This call synchronises the device (it copies from device memory). */
 det_status det_watchdog_status(int32_t *code, int clear);
 

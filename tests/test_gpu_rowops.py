@@ -132,6 +132,22 @@ def test_xent_deep_underflow_row(dev):
     assert_bitwise(host(d), d_w)
 
 
+@pytest.mark.parametrize("layout", ["dense", "offset"])
+def test_xent_rows_longer_than_shared_memory(dev, layout):
+    # rows of more than ~57,600 floats take the register/L2 kernel
+    rng = np.random.default_rng(81)
+    rows, V = 3, 60001
+    x = (2 * rng.standard_normal((rows, V))).astype(F)
+    x[1, 7] = F(-np.inf)
+    lab = np.array([0, V - 1, 31337], np.int32)
+    loss_w, d_w, _ = oracle.xent(x, lab, with_dlogits=True)
+    d = empty_dev(rows, V, layout)
+    loss, _, _ = detlib.detxent_f32(to_dev(x, layout), to_dev(lab), dlogits=d,
+                                    dscale=float(F(1 / rows)))
+    assert_bitwise(host(loss), loss_w)
+    assert_bitwise(host(d), d_w)
+
+
 def test_xent_dlogits_in_place(dev):
     rng = np.random.default_rng(78)
     x = (2 * rng.standard_normal((4, 777))).astype(F)
