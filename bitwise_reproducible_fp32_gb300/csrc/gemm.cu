@@ -609,10 +609,31 @@ cudaError_t launch_layout(bool a_km, bool b_km, const CUtensorMap &ma,
 
 // Work plan: whether to split K across CTAs and into how many chunk groups.
 // A split unit computes whole 256-wide chunks, so the bits never depend on the
-// plan. The cost model counts k-tile steps of the most loaded SM (a k-tile
-// step of a 256 x 128 tile is ~6 us at the FFMA rate this kernel sustains) and
-// adds the workspace traffic (each partial written once and read once) at
-// HBM speed.
+// plan. The cost model takes the k-tile steps of the most loaded CTA under the
+// kernel's round-robin unit order (units run tiles-fastest, so a CTA's units
+// cycle through the chunk groups and the last, shorter group is counted as
+// such) at ~6 us a step of a 256 x 128 tile, and adds the workspace traffic
+// (each partial written once and read once) at HBM speed plus the second
+// pass's launch.
+namespace {
+double busiest_cta_steps(int64_t T, int64_t S, int64_t G, int64_t nkt, int sms) {
+    const int64_t units = T * S;
+    const int64_t grid = std::min<int64_t>(units, sms);
+    double worst = 0.0;
+    // CTA b takes units b, b + grid, ...; unit u belongs to group u / T
+    for (int64_t b = 0; b < grid; ++b) {
+        double steps = 0.0;
+        for (int64_t u = b; u < units; u += grid) {
+            const int64_t g = u / T;
+            const int64_t kt0 = g * G * TILES_PER_CHUNK;
+            steps += double(std::min<int64_t>(nkt, kt0 + G * TILES_PER_CHUNK) - kt0);
+        }
+        worst = std::max(worst, steps);
+    }
+    return worst;
+}
+}  // namespace
+
 GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms) {
     GemmPlan pl{};
     const int64_t T = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
@@ -623,18 +644,18 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms) {
     pl.kt_per_unit = int(nkt);
     pl.nchunks = int(nchunks);
     pl.workspace_bytes = 0;
-    if (M == 0 || N == 0 || K == 0 || nchunks < 2) return pl;
-    const double kt_step_s = 6.0e-6, hbm_bps = 6.0e12;
-    double best = double((T + sms - 1) / sms) * double(nkt) * kt_step_s;
+    if (M == 0 || N == 0 || K == 0 || nchunks < 2 || sms < 1) return pl;
+    // enough tiles to fill every SM several times over: splitting cannot pay
+    if (T >= int64_t(sms) * 16) return pl;
+    const double kt_step_s = 6.0e-6, hbm_bps = 6.0e12, launch_s = 5.0e-6;
+    double best = busiest_cta_steps(T, 1, nchunks, nkt, sms) * kt_step_s;
     for (int64_t S = 2; S <= nchunks; ++S) {
         const int64_t G = (nchunks + S - 1) / S;              // chunks a unit
         const int64_t S_eff = (nchunks + G - 1) / G;
         if (S_eff != S) continue;                             // same as a smaller S
-        const int64_t units = T * S_eff;
-        const double compute = double((units + sms - 1) / sms) *
-                               double(std::min<int64_t>(G * TILES_PER_CHUNK, nkt)) * kt_step_s;
         const double ws = double(nchunks) * double(T) * BM * BN * 4.0;
-        const double cost = compute + (2.0 * ws + double(M) * double(N) * 4.0) / hbm_bps;
+        const double cost = busiest_cta_steps(T, S_eff, G, nkt, sms) * kt_step_s +
+                            (2.0 * ws + double(M) * double(N) * 4.0) / hbm_bps + launch_s;
         if (cost < 0.97 * best) {
             best = cost;
             pl.split = 1;

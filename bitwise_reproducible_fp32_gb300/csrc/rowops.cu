@@ -621,6 +621,36 @@ __device__ __forceinline__ void load_granules(float4 *buf, const float *xa, int 
     }
 }
 
+// Stage D for a row with misalignment H: chain l (< 256) adds the exps of its
+// groups g = l, l + 256, ... in ascending order. Group g is the last 4 - H
+// elements of granule g and the first H of granule g + 1; both granules are
+// read with 16-byte loads (consecutive chains, consecutive granules: no bank
+// conflicts), one sweep ahead of the adds.
+template <int H>
+__device__ __noinline__ float xent_smem_chain(const float4 *buf, int V) {
+    const int l = threadIdx.x;
+    const int ngroups = (V + 3) >> 2, gfull = V >> 2;
+    float s = 0.0f;
+    int g = l;
+    if (g < gfull) {
+        float4 c0 = buf[g], c1 = H ? buf[g + 1] : c0;
+        for (; g < gfull; g += kXentLanes) {
+            const int gn = g + kXentLanes;
+            float4 n0 = c0, n1 = c1;
+            if (gn < gfull) { n0 = buf[gn]; if (H) n1 = buf[gn + 1]; }
+            const float4 v = group_of<H>(c0, c1);
+            s = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(s, v.x), v.y), v.z), v.w);
+            c0 = n0;
+            c1 = n1;
+        }
+    }
+    if (g < ngroups) {     // the last, partial group
+        const float *ef = reinterpret_cast<const float *>(buf) + H;
+        for (int j = 4 * g; j < V; ++j) s = __fadd_rn(s, ef[j]);
+    }
+    return s;
+}
+
 __global__ void __launch_bounds__(kXsThreads, 1)
     xent_smem_kernel(int64_t rows, int V, const float *logits, int64_t ld,
                      const int32_t *__restrict__ labels, float *__restrict__ loss,
@@ -659,9 +689,27 @@ __global__ void __launch_bounds__(kXsThreads, 1)
         const bool bad = y32 < 0 || y32 >= V;
         const int y = y32;
         float *drow = dlogits ? dlogits + row * ldd : nullptr;
-        // A. the row has landed (both halves)
-        bool ok = mbar_wait_bounded(smem_u32(&bar[0]), uint32_t(k) & 1u);
-        ok = mbar_wait_bounded(smem_u32(&bar[1]), uint32_t(k) & 1u) && ok;
+        // A/B. each half of the row as it lands; its share of the max meanwhile
+        float m = x[0];
+        bool ok = true;
+        for (int hf = 0; hf < 2; ++hf) {
+            ok = mbar_wait_bounded(smem_u32(&bar[hf]), uint32_t(k) & 1u) && ok;
+            const int q0 = hf == 0 ? 0 : split, q1 = hf == 0 ? split : nch;
+            if (!bad && ok) {
+                for (int q = q0 + tid; q < q1; q += kXsThreads) {
+                    const float4 v = buf[q];
+                    const int j0 = 4 * q - h;
+                    if (j0 >= 0 && j0 + 3 < V) {
+                        m = max_nan(m, max_nan(max_nan(v.x, v.y), max_nan(v.z, v.w)));
+                    } else {
+                        if (j0 >= 0 && j0 < V) m = max_nan(m, v.x);
+                        if (j0 + 1 >= 0 && j0 + 1 < V) m = max_nan(m, v.y);
+                        if (j0 + 2 >= 0 && j0 + 2 < V) m = max_nan(m, v.z);
+                        if (j0 + 3 >= 0 && j0 + 3 < V) m = max_nan(m, v.w);
+                    }
+                }
+            }
+        }
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
                 atomicOr(&g_rowops_watchdog, kWatchdogXent);
@@ -673,20 +721,6 @@ __global__ void __launch_bounds__(kXsThreads, 1)
         float inv = 0.0f;
         bool vec_out = false;
         if (!bad) {
-            // B. max
-            float m = x[0];
-            for (int q = tid; q < nch; q += kXsThreads) {
-                const float4 v = buf[q];
-                const int j0 = 4 * q - h;
-                if (j0 >= 0 && j0 + 3 < V) {
-                    m = max_nan(m, max_nan(max_nan(v.x, v.y), max_nan(v.z, v.w)));
-                } else {
-                    if (j0 >= 0 && j0 < V) m = max_nan(m, v.x);
-                    if (j0 + 1 >= 0 && j0 + 1 < V) m = max_nan(m, v.y);
-                    if (j0 + 2 >= 0 && j0 + 2 < V) m = max_nan(m, v.z);
-                    if (j0 + 3 >= 0 && j0 + 3 < V) m = max_nan(m, v.w);
-                }
-            }
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1)
                 m = max_nan(__shfl_xor_sync(0xffffffffu, m, off), m);
@@ -712,17 +746,14 @@ __global__ void __launch_bounds__(kXsThreads, 1)
             }
             __syncthreads();
             // D. the 256 chains, groups g = l, l + 256, ... in ascending order
-            const float *ef = reinterpret_cast<const float *>(buf) + h;   // e of element j at ef[j]
             if (tid < kXentLanes) {
-                float s = 0.0f;
-                const int ngroups = (V + 3) >> 2, gfull = V >> 2;
-                int g = tid;
-                for (; g < gfull; g += kXentLanes) {
-                    const float *p = ef + 4 * g;
-                    s = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(s, p[0]), p[1]), p[2]), p[3]);
+                float s;
+                switch (h) {
+                    case 0: s = xent_smem_chain<0>(buf, V); break;
+                    case 1: s = xent_smem_chain<1>(buf, V); break;
+                    case 2: s = xent_smem_chain<2>(buf, V); break;
+                    default: s = xent_smem_chain<3>(buf, V); break;
                 }
-                if (g < ngroups)
-                    for (int j = 4 * g; j < V; ++j) s = __fadd_rn(s, ef[j]);
                 s = warp_butterfly_sum(s);
                 if (lane == 0) red[warp] = s;
             }
