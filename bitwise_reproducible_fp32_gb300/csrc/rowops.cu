@@ -292,22 +292,88 @@ __device__ __forceinline__ float dl_of_label(float e, float inv, float dscale) {
     return __fmul_rn(__fsub_rn(__fmul_rn(e, inv), 1.0f), dscale);
 }
 
+// Packed FP32 pairs (sm_100+ add/sub/mul/fma .f32x2): each half is rounded
+// exactly as the scalar operation (round to nearest even, no flush), so a
+// pair of scalar chains can share one instruction without changing a bit --
+// except that a packed multiply must not feed a packed add or subtract (see
+// exp2_le0_fast).
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+    f32x2 d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 splat2(float v) { return pack2(v, v); }
+
+// exp_le0_fast on a pair: d = x - m, then the same rounded steps as the scalar
+// routine on both halves at once; n ln2 enters as n (-LN2_HI), which is the
+// same product as (-n) LN2_HI. Returns the pair and the two n.
+// t = d LOG2E is formed by two scalar multiplies: a packed multiply whose
+// result feeds a packed add was measured to round like a fused multiply-add
+// (t not rounded on its own) at the ties of rint(t), which moves n there.
+__device__ __forceinline__ f32x2 exp2_le0_fast(f32x2 x, f32x2 m2, int &n0, int &n1) {
+    const f32x2 d = sub2(x, m2);
+    float d0, d1;
+    unpack2(d, d0, d1);
+    const f32x2 t = pack2(__fmul_rn(d0, kLog2e), __fmul_rn(d1, kLog2e));
+    const f32x2 tm = add2(t, splat2(kRoundMagic));
+    const f32x2 n = sub2(tm, splat2(kRoundMagic));
+    f32x2 r = fma2(n, splat2(-kLn2Hi), d);
+    r = fma2(n, splat2(-kLn2Lo), r);
+    f32x2 p = fma2(splat2(kC7), r, splat2(kC6));
+    p = fma2(p, r, splat2(kC5));
+    p = fma2(p, r, splat2(kC4));
+    p = fma2(p, r, splat2(kC3));
+    p = fma2(p, r, splat2(kC2));
+    p = fma2(p, r, splat2(1.0f));
+    p = fma2(p, r, splat2(1.0f));
+    float t0, t1, p0, p1;
+    unpack2(tm, t0, t1);
+    unpack2(p, p0, p1);
+    n0 = __float_as_int(t0) - __float_as_int(kRoundMagic);
+    n1 = __float_as_int(t1) - __float_as_int(kRoundMagic);
+    return pack2(__int_as_float(__float_as_int(p0) + int(unsigned(n0) << 23)),
+                 __int_as_float(__float_as_int(p1) + int(unsigned(n1) << 23)));
+}
+
 // exp(v - m) for the 4 lanes of a granule; d <= 0 for every element of a row
 // with a finite max. Rare deep-underflow elements take the general routine.
 __device__ __forceinline__ float4 exp4(float4 v, float m) {
-    const float d0 = __fsub_rn(v.x, m), d1 = __fsub_rn(v.y, m);
-    const float d2 = __fsub_rn(v.z, m), d3 = __fsub_rn(v.w, m);
+    const f32x2 m2 = splat2(m);
     int n0, n1, n2, n3;
+    const f32x2 e01 = exp2_le0_fast(pack2(v.x, v.y), m2, n0, n1);
+    const f32x2 e23 = exp2_le0_fast(pack2(v.z, v.w), m2, n2, n3);
     float4 e;
-    e.x = exp_le0_fast(d0, n0);
-    e.y = exp_le0_fast(d1, n1);
-    e.z = exp_le0_fast(d2, n2);
-    e.w = exp_le0_fast(d3, n3);
+    unpack2(e01, e.x, e.y);
+    unpack2(e23, e.z, e.w);
     if (min(min(n0, n1), min(n2, n3)) < -125) {
-        if (n0 < -125) e.x = det_exp_call(d0);
-        if (n1 < -125) e.y = det_exp_call(d1);
-        if (n2 < -125) e.z = det_exp_call(d2);
-        if (n3 < -125) e.w = det_exp_call(d3);
+        if (n0 < -125) e.x = det_exp_call(__fsub_rn(v.x, m));
+        if (n1 < -125) e.y = det_exp_call(__fsub_rn(v.y, m));
+        if (n2 < -125) e.z = det_exp_call(__fsub_rn(v.z, m));
+        if (n3 < -125) e.w = det_exp_call(__fsub_rn(v.w, m));
     }
     return e;
 }
@@ -609,6 +675,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// Asks L2 to fetch granules [0, n) of the row whose aligned base is xa. Every
+// granule holds at least one element of the row, so no byte outside the
+// row's pages is touched.
+__device__ __forceinline__ void prefetch_granules_l2(const float *xa, int n) {
+    for (int q = 0; q < n; q += kXsPiece) {
+        const int c = min(kXsPiece, n - q);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(xa + 4 * q),
+                     "r"(uint32_t(c) * 16u)
+                     : "memory");
+    }
+}
+
 // Thread 0: copies granules [q0, q1) of the row whose aligned base is xa into
 // the same granules of buf, completing on bar.
 __device__ __forceinline__ void load_granules(float4 *buf, const float *xa, int q0, int q1,
@@ -689,6 +767,7 @@ __global__ void __launch_bounds__(kXsThreads, 1)
         const bool bad = y32 < 0 || y32 >= V;
         const int y = y32;
         float *drow = dlogits ? dlogits + row * ldd : nullptr;
+        if (tid == 0 && next < rows) prefetch_granules_l2(aligned_row(next), granules(next));
         // A/B. each half of the row as it lands; its share of the max meanwhile
         float m = x[0];
         bool ok = true;
@@ -775,6 +854,7 @@ __global__ void __launch_bounds__(kXsThreads, 1)
                 if (dev_status) atomicOr(reinterpret_cast<int *>(dev_status), 1);
             }
         }
+        const f32x2 inv2 = splat2(inv), dscale2 = splat2(dscale);
         // E. dlogits, half 0 then half 1; each half's buffer is refilled with
         // the next row as soon as it is free
         for (int hf = 0; hf < 2; ++hf) {
@@ -788,8 +868,9 @@ __global__ void __launch_bounds__(kXsThreads, 1)
                         continue;
                     }
                     const float4 e = buf[q];
-                    float4 o = make_float4(dl_of(e.x, inv, dscale), dl_of(e.y, inv, dscale),
-                                           dl_of(e.z, inv, dscale), dl_of(e.w, inv, dscale));
+                    float4 o;      // dl_of on both pairs
+                    unpack2(mul2(mul2(pack2(e.x, e.y), inv2), dscale2), o.x, o.y);
+                    unpack2(mul2(mul2(pack2(e.z, e.w), inv2), dscale2), o.z, o.w);
                     const unsigned kk = unsigned(y - j0);
                     if (kk < 4) {
                         if (kk == 0) o.x = dl_of_label(e.x, inv, dscale);

@@ -132,6 +132,47 @@ def test_xent_deep_underflow_row(dev):
     assert_bitwise(host(d), d_w)
 
 
+def exp_tie_arguments():
+    """Floats d <= 0 with fl(d * LOG2E) exactly at a tie k + 1/2 of rint, and
+    their neighbours: where an exp that rounds t = d LOG2E differently (or not
+    at all) picks the other n and lands one ulp away."""
+    log2e = np.float32(1.4426950408889634)
+    out = []
+    for k in range(-151, 0):
+        c = np.float32((k + 0.5) / 1.4426950408889634)
+        bits = c.view(np.int32) + np.arange(-400, 401, dtype=np.int32)
+        d = bits.view(F)
+        t = d * log2e                      # float32 product, rounded once
+        ties = np.nonzero(t == F(k + 0.5))[0]
+        for i in ties:
+            out.extend(d[max(i - 1, 0):i + 2])
+    return np.unique(np.array(out, F))
+
+
+def test_xent_exp_rounding_ties(dev):
+    d = exp_tie_arguments()
+    assert d.size > 100
+    # known inputs where one spelling of the packed exp went one ulp off
+    # (row max 0, and row max 7.25)
+    extra = np.array([0xc2a70c69, 0xc2490340, 0xc283013c, 0xc14214ca, 0xc25f3183,
+                      0xc0d2b77c, 0xc158430d, 0xc16e7150], np.uint32).view(F)
+    extra2 = np.array([0xc29463bc, 0xc29300d8, 0xc0f4e2a0, 0xc0f4e2a1, 0xc0f4e29f,
+                       0xc2988c69, 0xc22c0340, 0xc09c2994], np.uint32).view(F)
+    V = d.size + extra.size + 1
+    x = np.zeros((2, V), F)
+    x[0, 1:] = np.concatenate([d, extra])
+    x[1, 0] = F(7.25)
+    x[1, 1:] = np.concatenate([d + F(7.25), extra2, np.full(extra.size - extra2.size, -1.0, F)])
+    lab = np.array([0, 3], np.int32)
+    loss_w, d_w, _ = oracle.xent(x, lab, with_dlogits=True)
+    for dscale in (1.0, 0.375):
+        loss, _, dl = detlib.detxent_f32(to_dev(x), to_dev(lab), want_dlogits=True,
+                                         dscale=dscale)
+        loss_w, d_w, _ = oracle.xent(x, lab, with_dlogits=True, dscale=F(dscale))
+        assert_bitwise(host(loss), loss_w, f"loss dscale={dscale}")
+        assert_bitwise(host(dl), d_w, f"dlogits dscale={dscale}")
+
+
 @pytest.mark.parametrize("layout", ["dense", "offset"])
 def test_xent_rows_longer_than_shared_memory(dev, layout):
     # rows of more than ~57,600 floats take the register/L2 kernel
