@@ -123,8 +123,82 @@ __device__ __forceinline__ int64_t ws_index(int c, int ntiles, int t, int q, int
 // m/n-contiguous tile yields 4 rows of one k.
 //   thread rows (op(A)): KMAJ arow + 8r;  else arow + (r & 3) + 32 (r >> 2)
 //   thread cols (op(B)): KMAJ bcol + 4c;  else bcol + (c & 3) + 16 (c >> 2)
+// Packed FP32 pairs (sm_100+ fma.rn.f32x2): two accumulators of a row, columns
+// 2c2 and 2c2 + 1, advance by one instruction. Each half is rounded exactly
+// as fmaf, so every accumulator still follows its own ascending-k chain; the
+// pair only halves the issue slots the FFMA stream takes.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+    f32x2 d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// B with m/n contiguous (B_KM false): one 16-byte load holds columns
+// {c, c+1, c+2, c+3} at one k, i.e. two column pairs ready for fma.rn.f32x2;
+// A's value is paired with itself. A k-contiguous B would need its pairs
+// assembled from two loads; that layout (the LM head's W^T) measured faster
+// with scalar FFMA, so it keeps mma_group_scalar.
+template <bool A_KM>
+__device__ __forceinline__ void mma_group_packed(const float *__restrict__ As,
+                                                 const float *__restrict__ Bs, int q,
+                                                 int arow, int bcol, int lm,
+                                                 float (&acc)[TM][TN]) {
+    f32x2 b[TN / 2][4];      // b[c2][kk] = columns {2c2, 2c2 + 1} at k = 4q + kk
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const float *pb = Bs + (4 * q + kk) * BN + bcol;
+        const ulonglong2 lo = *reinterpret_cast<const ulonglong2 *>(pb);
+        const ulonglong2 hi = *reinterpret_cast<const ulonglong2 *>(pb + 16);
+        b[0][kk] = lo.x; b[1][kk] = lo.y; b[2][kk] = hi.x; b[3][kk] = hi.y;
+    }
+    auto row_step = [&](int r, float a, int kk) {
+        const f32x2 aa = pack2(a, a);
+#pragma unroll
+        for (int c2 = 0; c2 < TN / 2; ++c2) {
+            f32x2 v = pack2(acc[r][2 * c2], acc[r][2 * c2 + 1]);
+            v = fma2(aa, b[c2][kk], v);
+            unpack2(v, acc[r][2 * c2], acc[r][2 * c2 + 1]);
+        }
+    };
+    if (A_KM) {
+        // A streamed one row (4 k) at a time
+#pragma unroll
+        for (int r = 0; r < TM; ++r) {
+            const float4 v = *reinterpret_cast<const float4 *>(
+                As + (arow + 8 * r) * 32 + ((q ^ lm) << 2));
+            row_step(r, v.x, 0);
+            row_step(r, v.y, 1);
+            row_step(r, v.z, 2);
+            row_step(r, v.w, 3);
+        }
+    } else {
+        // A streamed one k (16 rows) at a time
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float *pa = As + (4 * q + kk) * BM + arow;
+            float a[TM];
+#pragma unroll
+            for (int h = 0; h < TM / 4; ++h) {
+                const float4 v = *reinterpret_cast<const float4 *>(pa + 32 * h);
+                a[4 * h] = v.x; a[4 * h + 1] = v.y; a[4 * h + 2] = v.z; a[4 * h + 3] = v.w;
+            }
+#pragma unroll
+            for (int r = 0; r < TM; ++r) row_step(r, a[r], kk);
+        }
+    }
+}
+
 template <bool A_KM, bool B_KM>
-__device__ __forceinline__ void mma_group(const float *__restrict__ As,
+__device__ __forceinline__ void mma_group_scalar(const float *__restrict__ As,
                                           const float *__restrict__ Bs, int q,
                                           int arow, int bcol, int lm, int ln,
                                           float (&acc)[TM][TN]) {
@@ -179,6 +253,15 @@ __device__ __forceinline__ void mma_group(const float *__restrict__ As,
                     acc[r][c] = __fmaf_rn(a[r], b[c][kk], acc[r][c]);
         }
     }
+}
+
+template <bool A_KM, bool B_KM>
+__device__ __forceinline__ void mma_group(const float *__restrict__ As,
+                                          const float *__restrict__ Bs, int q,
+                                          int arow, int bcol, int lm, int ln,
+                                          float (&acc)[TM][TN]) {
+    if (B_KM) mma_group_scalar<A_KM, B_KM>(As, Bs, q, arow, bcol, lm, ln, acc);
+    else      mma_group_packed<A_KM>(As, Bs, q, arow, bcol, lm, acc);
 }
 
 // The thread's r-th row of op(A) and c-th column of op(B), tile-relative.
