@@ -24,6 +24,7 @@ TOKENS = 8192            # 4 sequences x 2,048 tokens
 N_PARAMS = 162_147_840   # the 162M decoder's parameter count
 
 SEED_CFG1, SEED_CFG2, SEED_CFG3, SEED_CFG4, SEED_CFG5 = 0, 1, 2, 3, 4
+SEED_RMS_BWD = 5   # the backward row-op inputs (their own stream)
 
 
 def uniform_pm1(rng: np.random.Generator, shape) -> np.ndarray:
@@ -113,7 +114,26 @@ def rowops_cfg4(seed: int = SEED_CFG4, rows: int = TOKENS, d: int = D_MODEL,
                 labels=labels)
 
 
+def rmsnorm_cfg4(seed: int = SEED_CFG4, rows: int = TOKENS, d: int = D_MODEL):
+    """The RMSNorm part of rowops_cfg4 alone (the same x and gain: the first
+    two draws of the same stream), without the 1.6 GB of logits."""
+    rng = np.random.default_rng(seed)
+    x = normal(rng, (rows, d))
+    gain = np.float32(1) + normal(rng, (d,), 0.02)
+    return dict(x=x, gain=gain, eps=np.float32(1e-6))
+
+
 # ------------------------------------------------------------------ backward
+def rmsnorm_bwd_cfg4(seed: int = SEED_RMS_BWD, rows: int = TOKENS, d: int = D_MODEL):
+    """RMSNorm backward at the cfg4 RMSNorm shape: x and gain of rmsnorm_cfg4,
+    and the upstream gradient dy rows x 768 ~ N(0, 1e-3) from its own stream
+    (the scale of the weight-gradient configuration's dY)."""
+    f = rmsnorm_cfg4(rows=rows, d=d)
+    rng = np.random.default_rng(seed)
+    f["dy"] = normal(rng, (rows, d), 1e-3)
+    return f
+
+
 def dw_cfg5(seed: int = SEED_CFG5, tokens: int = TOKENS, d: int = D_MODEL,
             dff: int = D_FF):
     """Weight-gradient GEMMs dW = X^T dY contracting over the tokens:

@@ -81,6 +81,8 @@ def _load():
                                    i64, f32p, i64, i64, c_int]
         lib.detor_rmsnorm.argtypes = [i64, i64, f32p, i64, f32p, ctypes.c_float,
                                       f32p, i64, f32p, c_int, c_int, c_int]
+        lib.detor_rmsnorm_bwd.argtypes = [i64, i64, f32p, i64, f32p, f32p, f32p, i64,
+                                          f32p, i64, f32p, c_int, c_int, i64, c_int]
         lib.detor_xent.restype = i64
         lib.detor_xent.argtypes = [i64, i64, f32p, i64, i32p, f32p, f32p, i64,
                                    ctypes.c_float, c_int, c_int, c_int]
@@ -189,6 +191,26 @@ def rmsnorm(x, gain, eps=1e-6, lanes=RMS_LANES, group=LANE_GROUP,
                           np.float32(eps), _fp(y), D, _fp(inv), lanes, group,
                           _threads(nthreads))
     return y, inv
+
+
+def rmsnorm_bwd(x, gain, inv_rms, dy, lanes=RMS_LANES, group=LANE_GROUP,
+                k_chunk=K_CHUNK, nthreads=None):
+    """(dx, dgain) of RMSNorm under the profile, from the forward's inv_rms
+    (det_oracle.c: dx = (h - xhat q) r with h = dy g, xhat = x r and q the
+    lane-chain mean of h xhat; dgain = the chunked contraction of dy xhat over
+    the rows)."""
+    x = np.ascontiguousarray(_f32(x))
+    dy = np.ascontiguousarray(_f32(dy))
+    gain = np.ascontiguousarray(_f32(gain))
+    inv = np.ascontiguousarray(_f32(inv_rms))
+    rows, D = x.shape
+    assert dy.shape == (rows, D) and gain.shape == (D,) and inv.shape == (rows,)
+    dx = np.empty((rows, D), np.float32)
+    dgain = np.empty(D, np.float32)
+    _load().detor_rmsnorm_bwd(rows, D, _fp(x), D, _fp(gain), _fp(inv), _fp(dy), D,
+                              _fp(dx), D, _fp(dgain), lanes, group, int(k_chunk),
+                              _threads(nthreads))
+    return dx, dgain
 
 
 # ---------------------------------------------------------------- xent

@@ -315,6 +315,88 @@ void detor_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
 }
 
 /* ------------------------------------------------------------------------ */
+/* RMSNorm backward                                                          */
+/* ------------------------------------------------------------------------ */
+/* The gradient of y_j = (x_j r) g_j with r = 1/sqrt(mean(x^2) + eps), in the
+ * textbook form dx = r (h - xhat mean(h xhat)), h = dy g, xhat = x r, and
+ * dgain_j = sum over rows of dy_j xhat_j. Per row, with r the forward's
+ * inv_rms (readings R20-R24 of the design notes):
+ *   xhat_j = x_j * r;  h_j = dy_j * g_j                (one rounding each)
+ *   dot    = the lane sums of fmaf(h_j, xhat_j, .)    (lane l owning groups g
+ *            with g mod lanes == l, ascending j, from +0) folded by the
+ *            butterfly -- the forward's sum-of-squares arrangement
+ *   q      = dot / D
+ *   dx_j   = (h_j - xhat_j * q) * r                   (three roundings)
+ * dgain_j is a contraction over the rows, so it takes the GEMM's spelling: for
+ * each k_chunk-wide chunk of rows an fmaf chain of dy_ij * xhat_ij from +0 in
+ * ascending i, the chunk partials added left to right (the first as is). It
+ * is therefore the diagonal of the profile's GEMM xhat^T dy. */
+typedef struct {
+    int64_t rows, D, ldx, lddy, lddx, kc;
+    const float *x, *gain, *inv, *dy;
+    float *dx, *dgain;
+    int lanes, group;
+} rmsb_ctx;
+
+static void rmsb_rows(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    rmsb_ctx *q = (rmsb_ctx *)c;
+    float s[1024];
+    for (int64_t r = lo; r < hi; ++r) {
+        const float *x = q->x + r * q->ldx;
+        const float *dy = q->dy + r * q->lddy;
+        const float rr = q->inv[r];
+        for (int l = 0; l < q->lanes; ++l) s[l] = 0.0f;
+        for (int64_t j = 0; j < q->D; ++j) {
+            int l = (int)((j / q->group) % q->lanes);
+            float xhat = x[j] * rr;
+            float h = dy[j] * q->gain[j];
+            s[l] = fmaf(h, xhat, s[l]);           /* each lane: ascending j */
+        }
+        float dot = butterfly(s, q->lanes);
+        float qm = dot / (float)q->D;
+        float *dx = q->dx + r * q->lddx;
+        for (int64_t j = 0; j < q->D; ++j) {
+            float xhat = x[j] * rr;
+            float h = dy[j] * q->gain[j];
+            float p = xhat * qm;
+            float d = h - p;
+            dx[j] = d * rr;
+        }
+    }
+}
+
+static void rmsb_cols(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    rmsb_ctx *q = (rmsb_ctx *)c;
+    for (int64_t j = lo; j < hi; ++j) {
+        float total = 0.0f;                       /* no rows: the empty sum, +0 */
+        for (int64_t c0 = 0; c0 < q->rows; c0 += q->kc) {
+            int64_t c1 = c0 + q->kc < q->rows ? c0 + q->kc : q->rows;
+            float acc = 0.0f;                     /* every chunk starts from +0 */
+            for (int64_t i = c0; i < c1; ++i) {
+                float xhat = q->x[i * q->ldx + j] * q->inv[i];
+                acc = fmaf(q->dy[i * q->lddy + j], xhat, acc);
+            }
+            if (c0 == 0) total = acc;             /* first partial taken as is */
+            else total = total + acc;             /* then left to right */
+        }
+        q->dgain[j] = total;
+    }
+}
+
+void detor_rmsnorm_bwd(int64_t rows, int64_t D, const float *x, int64_t ldx,
+                       const float *gain, const float *inv_rms, const float *dy,
+                       int64_t lddy, float *dx, int64_t lddx, float *dgain,
+                       int lanes, int group, int64_t k_chunk, int nthreads) {
+    if (lanes < 1 || lanes > 1024 || group < 1 || D < 1 || k_chunk < 1) return;
+    rmsb_ctx c = {rows, D, ldx, lddy, lddx, k_chunk, x, gain, inv_rms, dy, dx, dgain,
+                  lanes, group};
+    parallel_for(rows, nthreads, rmsb_rows, &c);
+    if (dgain) parallel_for(D, nthreads, rmsb_cols, &c);
+}
+
+/* ------------------------------------------------------------------------ */
 /* softmax cross-entropy                                                     */
 /* ------------------------------------------------------------------------ */
 /* Per row: m = max_j x_j; e_j = exp(x_j - m); S = the lane sums of e_j (plain

@@ -55,6 +55,13 @@ void detor_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
                    const float *gain, float eps, float *y, int64_t ldy,
                    float *inv_rms, int lanes, int group, int nthreads);
 
+/* RMSNorm backward (see det_oracle.c): dx (rows x D, row stride lddx) and
+ * dgain (D) from x, gain, the forward's inv_rms and dy. */
+void detor_rmsnorm_bwd(int64_t rows, int64_t D, const float *x, int64_t ldx,
+                       const float *gain, const float *inv_rms, const float *dy,
+                       int64_t lddy, float *dx, int64_t lddx, float *dgain,
+                       int lanes, int group, int64_t k_chunk, int nthreads);
+
 /* Softmax cross-entropy per row (see det_oracle.c). dlogits may be NULL.
  * Returns the number of rows whose label was out of range (their loss, and
  * their dlogits row if requested, are NaN). */
