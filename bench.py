@@ -7,6 +7,7 @@ One step = one pass of every operation of the path over one batch of the
   RMSNorm 8192 x 768 -> forward GEMMs (QKV 768x2304, out 768x768, SwiGLU gate and
   up 768x2048, down 2048x768, LM head 768x50257 with the [out, in] weight) ->
   softmax cross-entropy over 8192 x 50257 logits (loss, mean, dlogits) ->
+  RMSNorm backward 8192 x 768 (dx, dgain) ->
   weight-gradient GEMMs X^T dY over the 8,192 tokens (768x2304, 2048x768) ->
   AdamW over 162,147,840 parameters.
 Inputs are synthetic and seeded (bitwise_reproducible_fp32_gb300.inputs).
@@ -77,6 +78,11 @@ def gemm_dims(p):
 
 def bytes_rmsnorm(rows, D):
     return rows * D * 8 + D * 4 + rows * 4
+
+
+def bytes_rmsnorm_bwd(rows, D):
+    # read x, dy; write dx; gain, inv_rms, dgain
+    return 12 * rows * D + 8 * D + 4 * rows
 
 
 def bytes_xent(rows, V, dlogits=True):
@@ -175,8 +181,9 @@ def run_ours(args, rank, world, local_rank):
     t_setup = time.time()
     fwd, dw = gemm_list()
     r4 = inputs.rowops_cfg4()
+    rb = inputs.rmsnorm_bwd_cfg4()
     aw = inputs.adamw_cfg5()
-    host = dict(fwd=fwd, dw=dw, r4=r4, aw=aw)
+    host = dict(fwd=fwd, dw=dw, r4=r4, rb=rb, aw=aw)
 
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -207,6 +214,11 @@ def run_ours(args, rank, world, local_rank):
     lmean = torch.empty(1, dtype=torch.float32, device=dev)
     dlog = torch.empty_like(logits)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    dy4 = up(rb["dy"])
+    dx4 = torch.empty_like(dy4)
+    dgain4 = torch.empty(x4.shape[1], dtype=torch.float32, device=dev)
+    ws_rb = torch.empty((detlib.detrmsnorm_bwd_workspace_bytes(*x4.shape) + 3) // 4,
+                        dtype=torch.float32, device=dev)
     P, G, Mm, Vv = (up(aw[k]) for k in ("p", "g", "m", "v"))
     hp = {k: aw[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")}
     # L2 flush: write 512 MB, then read another 512 MB so the L2 holds clean
@@ -224,10 +236,13 @@ def run_ours(args, rank, world, local_rank):
     gemm_flops = sum(gemm_flops_fwd) + sum(gemm_flops_dw)
     lm_idx = [p["name"] for p in fwd].index("lm_head")
     # one launch per GEMM, plus the split-K second pass where a workspace is used
-    launches_per_step = (1 + len(fwd) + sum(w is not None for w in ws_fwd) + 2 + len(dw)
+    # rmsnorm; one launch per GEMM plus the split-K second pass where a
+    # workspace is used; xent + mean; the RMSNorm backward's two; AdamW
+    launches_per_step = (1 + len(fwd) + sum(w is not None for w in ws_fwd) + 2 + 2 + len(dw)
                          + sum(w is not None for w in ws_dw) + 1)
 
-    segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "gemm_dw", "adamw"]
+    segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "rmsnorm_bwd", "gemm_dw",
+            "adamw"]
 
     def step(ev=None):
         def mark(i):
@@ -249,12 +264,14 @@ def run_ours(args, rank, world, local_rank):
         detlib.detxent_f32(logits, labels, loss=loss, loss_mean=lmean, dlogits=dlog,
                            dscale=1.0 / rows4, dev_status=status)
         mark(4)
+        detlib.detrmsnorm_bwd_f32(x4, gain4, inv4, dy4, dx=dx4, dgain=dgain4, workspace=ws_rb)
+        mark(5)
         for i, (p, A, B) in enumerate(g_dw):
             detlib.detgemm_f32(A, B, c_dw[i], transA=p["transA"], transB=p["transB"],
                                workspace=ws_dw[i])
-        mark(5)
-        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
         mark(6)
+        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
+        mark(7)
 
     import torch.distributed as dist
     distributed = world > 1
@@ -280,7 +297,7 @@ def run_ours(args, rank, world, local_rank):
     t0 = time.time()
     for _ in range(args.steps):
         flush_l2(float(len(events)))             # L2 flush, outside the events
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(segs) + 1)]
         step(ev)
         events.append(ev)
     barrier()
@@ -329,6 +346,9 @@ def run_ours(args, rank, world, local_rank):
             "rmsnorm": {"gbs": bytes_rmsnorm(rows4, D4) / per("rmsnorm") / 1e9,
                         "frac_hbm": bytes_rmsnorm(rows4, D4) / per("rmsnorm") / 1e9 / hbm,
                         "ms": per("rmsnorm") * 1e3},
+            "rmsnorm_bwd": {"gbs": bytes_rmsnorm_bwd(rows4, D4) / per("rmsnorm_bwd") / 1e9,
+                            "frac_hbm": bytes_rmsnorm_bwd(rows4, D4) / per("rmsnorm_bwd") / 1e9 / hbm,
+                            "ms": per("rmsnorm_bwd") * 1e3},
             "xent": {"gbs": bytes_xent(rows4, V) / per("xent") / 1e9,
                      "frac_hbm": bytes_xent(rows4, V) / per("xent") / 1e9 / hbm,
                      "ms": per("xent") * 1e3},
@@ -366,6 +386,10 @@ def run_ours(args, rank, world, local_rank):
                             "peak": hbm, "unit": "GB/s",
                             "frac": round(ops["rmsnorm"]["frac_hbm"], 4),
                             "traffic": traffic.get("rmsnorm")},
+                "rmsnorm_bwd": {"bound": "hbm", "achieved": round(ops["rmsnorm_bwd"]["gbs"], 1),
+                                "peak": hbm, "unit": "GB/s",
+                                "frac": round(ops["rmsnorm_bwd"]["frac_hbm"], 4),
+                                "traffic": traffic.get("rmsnorm_bwd")},
                 "xent": {"bound": "hbm", "achieved": round(ops["xent"]["gbs"], 1),
                          "peak": hbm, "unit": "GB/s",
                          "frac": round(ops["xent"]["frac_hbm"], 4),
@@ -408,7 +432,7 @@ def e2e_leg(args, dev, host, gemm_flops):
 
     from bitwise_reproducible_fp32_gb300 import detlib
 
-    fwd, dw, r4, aw = host["fwd"], host["dw"], host["r4"], host["aw"]
+    fwd, dw, r4, rb, aw = host["fwd"], host["dw"], host["r4"], host["rb"], host["aw"]
     pinned = {}
 
     def pin(a):
@@ -423,6 +447,7 @@ def e2e_leg(args, dev, host, gemm_flops):
         srcs += [pin(p["A"]), pin(p["B"])]
     for k in ("x", "gain", "logits", "labels"):
         srcs.append(pin(r4[k]))
+    srcs.append(pin(rb["dy"]))
     for k in ("p", "g", "m", "v"):
         srcs.append(pin(aw[k]))
     uniq = list({id(s[0]): s for s in srcs}.values())
@@ -439,7 +464,11 @@ def e2e_leg(args, dev, host, gemm_flops):
     loss = torch.empty(rows4, dtype=torch.float32, device=dev)
     lmean = torch.empty(1, dtype=torch.float32, device=dev)
     dlog = torch.empty((rows4, V), dtype=torch.float32, device=dev)
-    dev_outs = outs_dev + [y4, inv4, loss, lmean, dlog]
+    dx4 = torch.empty((rows4, D4), dtype=torch.float32, device=dev)
+    dgain4 = torch.empty(D4, dtype=torch.float32, device=dev)
+    ws_rb = torch.empty((detlib.detrmsnorm_bwd_workspace_bytes(rows4, D4) + 3) // 4,
+                        dtype=torch.float32, device=dev)
+    dev_outs = outs_dev + [y4, inv4, loss, lmean, dlog, dx4, dgain4]
     host_outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_outs]
     pmv_host = [torch.empty(aw[k].shape, dtype=torch.float32).pin_memory()
                 for k in ("p", "m", "v")]
@@ -457,6 +486,8 @@ def e2e_leg(args, dev, host, gemm_flops):
                               inv_rms=inv4)
         detlib.detxent_f32(g(r4["logits"]), g(r4["labels"]), loss=loss, loss_mean=lmean,
                            dlogits=dlog, dscale=1.0 / rows4)
+        detlib.detrmsnorm_bwd_f32(g(r4["x"]), g(r4["gain"]), inv4, g(rb["dy"]), dx=dx4,
+                                  dgain=dgain4, workspace=ws_rb)
         P, G, M, Vv = (g(aw[k]) for k in ("p", "g", "m", "v"))
         detlib.detadamw_f32(P, G, M, Vv, **hp)
         for h, d in zip(host_outs, dev_outs):
@@ -509,6 +540,12 @@ def oracle_sample(budget_s: float):
     oracle.rmsnorm(r4["x"], r4["gain"], eps=r4["eps"], nthreads=cores)
     dt = time.perf_counter() - t0
     rates["rmsnorm_gbs"] = bytes_rmsnorm(*r4["x"].shape) / dt / 1e9
+    rb = inputs.rmsnorm_bwd_cfg4(rows=512)          # two 256-row chunks
+    _, inv = oracle.rmsnorm(rb["x"], rb["gain"], eps=rb["eps"], nthreads=cores)
+    t0 = time.perf_counter()
+    oracle.rmsnorm_bwd(rb["x"], rb["gain"], inv, rb["dy"], nthreads=cores)
+    dt = time.perf_counter() - t0
+    rates["rmsnorm_bwd_gbs"] = bytes_rmsnorm_bwd(*rb["x"].shape) / dt / 1e9
     n = 20_000_000
     a = inputs.adamw_cfg5(n=n)
     t0 = time.perf_counter()
@@ -518,7 +555,8 @@ def oracle_sample(budget_s: float):
     rates["adamw_gbs"] = bytes_adamw(n) / dt / 1e9
     sample = (f"LM-head GEMM rows 0..{rows_done - 1} of 8192 (x 50257 x 768, "
               f"{flops / 1e9:.1f} GFLOP); xent {r4['logits'].shape[0]} rows x 50257 "
-              f"with dlogits; RMSNorm {r4['x'].shape[0]} rows; AdamW {n} params")
+              f"with dlogits; RMSNorm {r4['x'].shape[0]} rows; RMSNorm backward 512 rows; "
+              f"AdamW {n} params")
     return rates, cores, sample
 
 

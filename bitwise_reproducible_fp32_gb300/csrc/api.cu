@@ -176,6 +176,38 @@ DET_API det_status detrmsnorm_f32(const det_profile_v1 *prof, int64_t rows, int6
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+DET_API det_status detrmsnorm_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t rows,
+                                                  int64_t D, size_t *bytes) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (!bytes || rows < 0 || rows > kDimMax || D < 1 || D > kDimMax) return DET_ERR_INVALID_ARG;
+    *bytes = rmsnorm_bwd_workspace_bytes(rows, D);
+    return DET_OK;
+}
+
+DET_API det_status detrmsnorm_bwd_f32(const det_profile_v1 *prof, int64_t rows, int64_t D,
+                                      const float *x, int64_t ldx, const float *gain,
+                                      const float *inv_rms, const float *dy, int64_t lddy,
+                                      float *dx, int64_t lddx, float *dgain, void *workspace,
+                                      size_t workspace_bytes, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (rows < 0 || rows > kDimMax || D < 1 || D > kDimMax || !dgain) return DET_ERR_INVALID_ARG;
+    if (rows > 0) {
+        if (ldx < D || lddy < D || lddx < D || !x || !gain || !inv_rms || !dy || !dx)
+            return DET_ERR_INVALID_ARG;
+        if (dx == dy && lddx != lddy) return DET_ERR_INVALID_ARG;
+        const size_t need = rmsnorm_bwd_workspace_bytes(rows, D);
+        if (need > 0 && (!workspace || workspace_bytes < need ||
+                         reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
+            return DET_ERR_WORKSPACE;
+    }
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_rmsnorm_bwd(rows, D, x, ldx, gain, inv_rms, dy, lddy, dx, lddx,
+                                        dgain, static_cast<float *>(workspace),
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 DET_API det_status detxent_f32(const det_profile_v1 *prof, int64_t rows, int64_t V,
                                const float *logits, int64_t ld, const int32_t *labels,
                                float *loss, float *loss_mean, float *dlogits, int64_t ldd,
@@ -230,7 +262,9 @@ DET_API det_status det_watchdog_status(int32_t *code, int clear) {
     if (!code) return DET_ERR_INVALID_ARG;
     unsigned int c = 0, c2 = 0;
     cudaError_t e = gemm_watchdog(&c, clear);
+    unsigned int c3 = 0;
     if (e == cudaSuccess) e = rowops_watchdog(&c2, clear);
-    *code = int32_t(c | c2);
+    if (e == cudaSuccess) e = rmsbwd_watchdog(&c3, clear);
+    *code = int32_t(c | c2 | c3);
     return from_cuda(e);
 }

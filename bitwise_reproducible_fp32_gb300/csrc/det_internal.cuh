@@ -49,6 +49,14 @@ cudaError_t gemm_watchdog(unsigned int *code, int clear);
 cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s);
 
 cudaError_t rowops_watchdog(unsigned int *code, int clear);
+cudaError_t rmsbwd_watchdog(unsigned int *code, int clear);
+
+// 2-D fp32 TMA descriptor over a row-major matrix: inner = contiguous extent,
+// outer = rows, ld = row stride (elements); out-of-range boxes read zeros.
+bool make_tensor_map_2d(CUtensorMap *map, const float *base, int64_t inner, int64_t outer,
+                        int64_t ld, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
+// Whether TMA can describe a matrix at base with row stride ld (16-byte rules).
+bool tma_operand_ok(const float *base, int64_t ld);
 cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
                            const float *gain, float eps, float *y, int64_t ldy,
                            float *inv_rms, cudaStream_t s);
@@ -56,6 +64,11 @@ cudaError_t launch_xent(int64_t rows, int64_t V, const float *logits, int64_t ld
                         const int32_t *labels, float *loss, float *loss_mean,
                         float *dlogits, int64_t ldd, float dscale,
                         int32_t *dev_status, cudaStream_t s);
+size_t rmsnorm_bwd_workspace_bytes(int64_t rows, int64_t D);
+cudaError_t launch_rmsnorm_bwd(int64_t rows, int64_t D, const float *x, int64_t ldx,
+                               const float *gain, const float *inv_rms, const float *dy,
+                               int64_t lddy, float *dx, int64_t lddx, float *dgain,
+                               float *workspace, cudaStream_t s);
 cudaError_t launch_exp_map(int64_t n, const float *x, float *y, int is_log,
                            cudaStream_t s);
 cudaError_t launch_adamw(int64_t n, float *p, const float *g, float *m, float *v,
@@ -139,6 +152,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple
+// of 16), completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
 

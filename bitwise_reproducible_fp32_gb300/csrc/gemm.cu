@@ -645,26 +645,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 // box, unswizzled. R = the tile's extent along m or n.
 bool make_map(CUtensorMap *map, const float *base, int64_t inner, int64_t outer,
               int64_t ld, bool kmajor_box, int R) {
-    auto enc = encoder();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
-    cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
-    cuuint32_t box[2];
-    CUtensorMapSwizzle swz;
-    if (kmajor_box) { box[0] = 32; box[1] = cuuint32_t(R); swz = CU_TENSOR_MAP_SWIZZLE_128B; }
-    else            { box[0] = cuuint32_t(R); box[1] = 32; swz = CU_TENSOR_MAP_SWIZZLE_NONE; }
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
-                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return kmajor_box ? make_tensor_map_2d(map, base, inner, outer, ld, 32, uint32_t(R), true)
+                      : make_tensor_map_2d(map, base, inner, outer, ld, uint32_t(R), 32, false);
 }
 
-bool tma_ok(const float *base, int64_t ld) {
-    return (reinterpret_cast<uintptr_t>(base) % 16 == 0) && (ld % 4 == 0) &&
-           (ld * 4 < (int64_t(1) << 40));
-}
+bool tma_ok(const float *base, int64_t ld) { return tma_operand_ok(base, ld); }
 
 template <bool A_KM, bool B_KM, bool TMA>
 cudaError_t launch_variant(const CUtensorMap &ma, const CUtensorMap &mb, const KArgs &k,
@@ -689,6 +674,26 @@ cudaError_t launch_layout(bool a_km, bool b_km, const CUtensorMap &ma,
 }
 
 }  // namespace
+
+bool make_tensor_map_2d(CUtensorMap *map, const float *base, int64_t inner, int64_t outer,
+                        int64_t ld, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+    cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
+                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool tma_operand_ok(const float *base, int64_t ld) {
+    return (reinterpret_cast<uintptr_t>(base) % 16 == 0) && (ld % 4 == 0) &&
+           (ld * 4 < (int64_t(1) << 40));
+}
 
 // Work plan: whether to split K across CTAs and into how many chunk groups.
 // A split unit computes whole 256-wide chunks, so the bits never depend on the

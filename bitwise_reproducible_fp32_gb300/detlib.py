@@ -58,6 +58,10 @@ SIGNATURES = [
                                    _i64, _vp, _i64, _vp]),
     ("detrmsnorm_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _f, _vp, _i64, _vp,
                               _vp]),
+    ("detrmsnorm_bwd_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _i64, _vp,
+                                  _i64, _vp, _vp, ctypes.c_size_t, _vp]),
+    ("detrmsnorm_bwd_workspace_bytes", _int, [_PROF, _i64, _i64,
+                                              ctypes.POINTER(ctypes.c_size_t)]),
     ("detxent_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i64, _f,
                            _vp, _vp]),
     ("detadamw_f32", _int, [_PROF, _i64, _vp, _vp, _vp, _vp, ctypes.POINTER(AdamWHP),
@@ -226,6 +230,41 @@ def detrmsnorm_f32(x, gain, eps=1e-6, y=None, inv_rms=None, want_inv_rms=True,
                                _stream(stream))
     _check("detrmsnorm_f32", st)
     return y, inv_rms
+
+
+def detrmsnorm_bwd_workspace_bytes(rows, D, profile=None) -> int:
+    n = ctypes.c_size_t(0)
+    _check("detrmsnorm_bwd_workspace_bytes",
+           load().detrmsnorm_bwd_workspace_bytes(_prof(profile), rows, D, ctypes.byref(n)))
+    return n.value
+
+
+def detrmsnorm_bwd_f32(x, gain, inv_rms, dy, dx=None, dgain=None, workspace=None,
+                       profile=None, stream=None):
+    """RMSNorm backward from the forward's inv_rms. Returns (dx, dgain).
+    workspace: float32 CUDA tensor of at least detrmsnorm_bwd_workspace_bytes
+    bytes; allocated here when needed and not given."""
+    import torch
+    _cuda_f32(x, "x", 2)
+    _cuda_f32(dy, "dy", 2)
+    _cuda_f32(gain, "gain", 1)
+    _cuda_f32(inv_rms, "inv_rms", 1)
+    rows, D = x.shape
+    if dx is None:
+        dx = torch.empty((rows, D), dtype=torch.float32, device=x.device)
+    if dgain is None:
+        dgain = torch.empty(D, dtype=torch.float32, device=x.device)
+    _cuda_f32(dx, "dx", 2)
+    _cuda_f32(dgain, "dgain", 1)
+    need = detrmsnorm_bwd_workspace_bytes(rows, D, profile)
+    if workspace is None and need > 0:
+        workspace = torch.empty((need + 3) // 4, dtype=torch.float32, device=x.device)
+    wbytes = workspace.numel() * 4 if workspace is not None else 0
+    st = load().detrmsnorm_bwd_f32(_prof(profile), rows, D, _ptr(x), _ld(x), _ptr(gain),
+                                   _ptr(inv_rms), _ptr(dy), _ld(dy), _ptr(dx), _ld(dx),
+                                   _ptr(dgain), _ptr(workspace), wbytes, _stream(stream))
+    _check("detrmsnorm_bwd_f32", st)
+    return dx, dgain
 
 
 # ---------------------------------------------------------------- cross-entropy

@@ -10,6 +10,7 @@ DRAM counters mean something:
   dw_qkv    GEMM X^T dY, 768 x 2304 over 8192 tokens
   xent      cross-entropy 1024 x 50257 with dlogits and mean
   rmsnorm   RMSNorm 8192 x 768
+  rms_bwd   RMSNorm backward 8192 x 768 (dx, dgain)
   adamw     AdamW over 32 Mi parameters
 Each run is one warm-up launch followed by R launches (default 2).
 """
@@ -27,7 +28,8 @@ def main(argv=None):
     from bitwise_reproducible_fp32_gb300 import build, detlib, inputs
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["lm_head", "qkv", "dw_qkv", "xent", "rmsnorm", "adamw"])
+    ap.add_argument("case", choices=["lm_head", "qkv", "dw_qkv", "xent", "rmsnorm", "rms_bwd",
+                                    "adamw"])
     ap.add_argument("--reps", type=int, default=2)
     a = ap.parse_args(argv)
     build.build()
@@ -62,6 +64,15 @@ def main(argv=None):
             y = torch.empty_like(x)
             inv = torch.empty(x.shape[0], dtype=torch.float32, device=dev)
             run = lambda: detlib.detrmsnorm_f32(x, g, float(r["eps"]), y=y, inv_rms=inv)
+    elif a.case == "rms_bwd":
+        f = inputs.rmsnorm_bwd_cfg4()
+        x, g, dy = up(f["x"]), up(f["gain"]), up(f["dy"])
+        _, inv = detlib.detrmsnorm_f32(x, g, float(f["eps"]))
+        dx = torch.empty_like(x)
+        dgain = torch.empty(x.shape[1], dtype=torch.float32, device=dev)
+        ws = torch.empty((detlib.detrmsnorm_bwd_workspace_bytes(*x.shape) + 3) // 4,
+                         dtype=torch.float32, device=dev)
+        run = lambda: detlib.detrmsnorm_bwd_f32(x, g, inv, dy, dx=dx, dgain=dgain, workspace=ws)
     else:
         w = inputs.adamw_cfg5(n=32 * 1024 * 1024)
         P, G, M_, V_ = (up(w[k]) for k in ("p", "g", "m", "v"))

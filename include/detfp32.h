@@ -171,6 +171,51 @@ det_status detrmsnorm_f32(const det_profile_v1 *prof, int64_t rows, int64_t D,
                           float eps, float *y, int64_t ldy, float *inv_rms,
                           det_stream_t stream);
 
+/* RMSNorm backward: the gradients of y = (x * r) * gain with respect to x and
+ * gain, given the upstream gradient dy and the forward's r (inv_rms). The
+ * pages define the forward ("MojoLearn 162M" model card, table "Compared with
+ * GPT-3 Small") and fix, for every operation of training, the reduction order
+ * and partitioning ("mojolearn" PyPI page, section "What bitwise identity
+ * means, and why it is not the default"); they print no backward spelling.
+ *
+ * Profile v1, per row (r = inv_rms[row]):
+ *   xhat_j = x_j * r,  h_j = dy_j * gain_j         (each rounded once)
+ *   dot    = sum of h_j * xhat_j by the forward's arrangement: 32 chains of
+ *            fmaf over the 4-element groups g with g mod 32 == l, from +0 in
+ *            ascending j, folded by the xor butterfly 16, 8, 4, 2, 1
+ *   q      = dot / (float)D                         (IEEE division)
+ *   dx_j   = (h_j - xhat_j * q) * r                 (three roundings)
+ * and dgain_j, a contraction over the rows, in the GEMM's spelling: for each
+ * 256-row chunk an fmaf chain of dy_ij * xhat_ij from +0 in ascending row,
+ * the chunk partials added left to right (the first as is). dgain is thus the
+ * diagonal of detgemm_f32's xhat^T dy. rows == 0 writes dgain = +0.
+ *
+ * x, dy: rows x D, row strides ldx, lddy >= D (device). gain: D floats,
+ * inv_rms: rows floats (device). dx: rows x D, lddx >= D (device); it may
+ * equal dy when lddx == lddy (in place) and must not overlap x, gain or
+ * inv_rms otherwise. dgain: D floats (device), written.
+ * workspace / workspace_bytes: device scratch, 16-byte aligned, of at least
+ * detrmsnorm_bwd_workspace_bytes() bytes (0 when rows <= 256), not
+ * overlapping any other argument: the chunk partials of dgain. Calls that
+ * share a workspace must be ordered (one stream).
+ *
+ * Errors: DET_ERR_INVALID_ARG for negative rows, D < 1, a dimension >= 2^31,
+ * a stride below D or a null pointer that the shape needs; DET_ERR_WORKSPACE
+ * when the workspace is needed and missing, too small or misaligned. A TMA
+ * wait that exceeds its bound makes the kernel skip its stores and record
+ * bit 2 of det_watchdog_status(). */
+det_status detrmsnorm_bwd_f32(const det_profile_v1 *prof, int64_t rows, int64_t D,
+                              const float *x, int64_t ldx, const float *gain,
+                              const float *inv_rms, const float *dy, int64_t lddy,
+                              float *dx, int64_t lddx, float *dgain,
+                              void *workspace, size_t workspace_bytes,
+                              det_stream_t stream);
+
+/* Workspace detrmsnorm_bwd_f32 needs for rows x D, written to *bytes:
+ * ceil(rows / 256) * D floats when rows > 256, else 0. Host-only. */
+det_status detrmsnorm_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t rows,
+                                          int64_t D, size_t *bytes);
+
 /* Softmax cross-entropy per row of V logits, with an optional gradient and an
  * optional mean. Cross entropy is on the verified path in "mojolearn"
  * (andrewhendel.com), "Handing training off between vendors".
@@ -251,7 +296,7 @@ det_status detlog_f32(const det_profile_v1 *prof, int64_t n, const float *x,
 /* Reads, and optionally clears, the current device's watchdog word.
  * *code == 0 means no bounded device wait has ever given up; otherwise bit k
  * identifies the kernel family that gave up (bit 0: GEMM operand staging,
- * bit 1: cross-entropy row staging).
+ * bit 1: cross-entropy row staging, bit 2: RMSNorm-backward tile staging).
  * This call synchronises the device (it copies from device memory). */
 det_status det_watchdog_status(int32_t *code, int clear);
 

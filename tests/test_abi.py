@@ -28,6 +28,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("detgemm_f32", "detgemm_workspace_bytes", "detrmsnorm_f32", "detxent_f32", "detadamw_f32",
+                 "detrmsnorm_bwd_f32", "detrmsnorm_bwd_workspace_bytes",
                  "detexp_f32", "detlog_f32", "det_profile_default",
                  "det_status_string", "det_watchdog_status"):
         assert want in names
@@ -77,6 +78,10 @@ def test_unknown_profile_is_refused_by_name(lib, field, value):
                            ctypes.c_float(1.0), null, null) == 2
     assert lib.detrmsnorm_f32(ctypes.byref(p), 1, 4, null, 4, null,
                               ctypes.c_float(1e-6), null, 4, null, null) == 2
+    assert lib.detrmsnorm_bwd_f32(ctypes.byref(p), 1, 4, null, 4, null, null, null, 4,
+                                  null, 4, null, null, 0, null) == 2
+    n = ctypes.c_size_t(7)
+    assert lib.detrmsnorm_bwd_workspace_bytes(ctypes.byref(p), 1000, 8, ctypes.byref(n)) == 2
 
 
 def test_bad_arguments_are_refused_on_the_host(lib):
@@ -101,6 +106,21 @@ def test_bad_arguments_are_refused_on_the_host(lib):
                            ctypes.c_float(1.0), null, null) == 1
     assert lib.detxent_f32(p, 2, 8, dummy, 8, dummy, dummy, null, dummy, 7,
                            ctypes.c_float(1.0), null, null) == 1
+    # RMSNorm backward: D < 1, stride below D, null gain, dx == dy with other
+    # strides, a missing or short workspace past one 256-row chunk
+    rb = lib.detrmsnorm_bwd_f32
+    assert rb(p, 4, 0, dummy, 4, dummy, dummy, dummy, 4, dummy, 4, dummy, null, 0, null) == 1
+    assert rb(p, 4, 8, dummy, 7, dummy, dummy, dummy, 8, dummy, 8, dummy, null, 0, null) == 1
+    assert rb(p, 4, 8, dummy, 8, null, dummy, dummy, 8, dummy, 8, dummy, null, 0, null) == 1
+    assert rb(p, 4, 8, dummy, 8, dummy, dummy, dummy, 8, dummy, 12, dummy, null, 0, null) == 1
+    assert rb(p, 4, 8, dummy, 8, dummy, dummy, dummy, 8, dummy, 8, null, null, 0, null) == 1
+    assert rb(p, 300, 8, dummy, 8, dummy, dummy, dummy, 8, dummy, 8, dummy, null, 0, null) == 5
+    assert rb(p, 300, 8, dummy, 8, dummy, dummy, dummy, 8, dummy, 8, dummy, dummy, 63,
+              null) == 5
+    n = ctypes.c_size_t(7)
+    assert lib.detrmsnorm_bwd_workspace_bytes(p, 256, 768, ctypes.byref(n)) == 0 and n.value == 0
+    assert lib.detrmsnorm_bwd_workspace_bytes(p, 8192, 768, ctypes.byref(n)) == 0
+    assert n.value == 32 * 768 * 4
     hp = detlib.AdamWHP(1e-3, 0.9, 0.95, 1e-8, 0.1, 0)
     assert lib.detadamw_f32(p, 4, dummy, dummy, dummy, dummy, ctypes.byref(hp), null) == 1
     assert lib.detexp_f32(p, -1, dummy, dummy, null) == 1
