@@ -43,7 +43,8 @@ METRIC = ("bit-exact fixed-order FP32 GEMM TFLOP/s (% FP32 FMA peak); "
 WORKLOAD = ("162M-decoder FP32 step: RMSNorm 8192x768, forward GEMMs "
             "(8192 tokens; 768x2304, 768x768, 2x 768x2048, 2048x768, LM head "
             "768x50257), softmax cross-entropy 8192x50257 with dlogits and mean, "
-            "dW GEMMs over 8192 tokens (768x2304, 2048x768), AdamW 162,147,840 params")
+            "RMSNorm backward 8192x768 (dx, dgain), dW GEMMs over 8192 tokens "
+            "(768x2304, 2048x768), AdamW 162,147,840 params")
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
 
