@@ -81,6 +81,9 @@ def _load():
                                    i64, f32p, i64, i64, c_int]
         lib.detor_rmsnorm.argtypes = [i64, i64, f32p, i64, f32p, ctypes.c_float,
                                       f32p, i64, f32p, c_int, c_int, c_int]
+        lib.detor_gemm_acc.argtypes = [c_int, c_int, i64, i64, i64, f32p, i64, f32p,
+                                       i64, f32p, i64, i64, c_int]
+        lib.detor_shardsum.argtypes = [i64, i64, f32p, i64, ctypes.c_float, f32p, c_int]
         lib.detor_rmsnorm_bwd.argtypes = [i64, i64, f32p, i64, f32p, f32p, f32p, i64,
                                           f32p, i64, f32p, c_int, c_int, i64, c_int]
         lib.detor_xent.restype = i64
@@ -174,6 +177,33 @@ def gemm(A, B, transA=False, transB=False, k_chunk=K_CHUNK, nthreads=None,
                        A.strides[0] // 4, _fp(B), B.strides[0] // 4, _fp(C),
                        C.strides[0] // 4, int(k_chunk), _threads(nthreads))
     return C
+
+
+def gemm_acc(C, A, B, transA=False, transB=False, k_chunk=K_CHUNK, nthreads=None):
+    """C + op(A) op(B) under the profile (beta = 1): a new array."""
+    A = np.ascontiguousarray(_f32(A))
+    B = np.ascontiguousarray(_f32(B))
+    M, K = (A.shape[1], A.shape[0]) if transA else A.shape
+    Kb, N = (B.shape[1], B.shape[0]) if transB else B.shape
+    assert K == Kb
+    out = np.array(_f32(C), dtype=np.float32, order="C", copy=True)
+    assert out.shape == (M, N)
+    _load().detor_gemm_acc(int(transA), int(transB), M, N, K, _fp(A), A.strides[0] // 4,
+                           _fp(B), B.strides[0] // 4, _fp(out), N, int(k_chunk),
+                           _threads(nthreads))
+    return out
+
+
+def shardsum(shards, scale=1.0, nthreads=None):
+    """scale * (((g_0 + g_1) + g_2) + ...) over the first axis of shards
+    (S x n), left to right."""
+    g = np.ascontiguousarray(_f32(shards))
+    S = g.shape[0]
+    flat = g.reshape(S, -1)
+    out = np.empty(flat.shape[1], np.float32)
+    _load().detor_shardsum(S, flat.shape[1], _fp(flat), flat.shape[1], np.float32(scale),
+                           _fp(out), _threads(nthreads))
+    return out.reshape(g.shape[1:])
 
 
 # ---------------------------------------------------------------- RMSNorm

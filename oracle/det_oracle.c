@@ -253,6 +253,53 @@ void detor_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
     parallel_for(M, nthreads, gemm_rows, &g);
 }
 
+/* Gradient accumulation (beta = 1): the new product is formed exactly as
+ * detor_gemm forms it, then added to the old C once, C on the left, so that
+ * accumulating shard after shard gives the same bits as the left-to-right
+ * shard sum below. */
+void detor_gemm_acc(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                    const float *A, int64_t lda, const float *B, int64_t ldb,
+                    float *C, int64_t ldc, int64_t k_chunk, int nthreads) {
+    if (k_chunk <= 0 || M <= 0 || N <= 0) return;
+    float *R = (float *)malloc(sizeof(float) * (size_t)M * (size_t)N);
+    if (!R) return;
+    detor_gemm(transA, transB, M, N, K, A, lda, B, ldb, R, N, k_chunk, nthreads);
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) C[i * ldc + j] = C[i * ldc + j] + R[i * N + j];
+    free(R);
+}
+
+/* ------------------------------------------------------------------------ */
+/* fixed-order shard gradient sum                                            */
+/* ------------------------------------------------------------------------ */
+/* "MojoLearn 162M" model card, table "Training": 64 logical shards, each a
+ * mean over 4 x 2,048 tokens; the shard gradients are summed in a fixed order.
+ * Reading: left to right over the shard index, one rounding per addition, then
+ * one multiply by the caller's scale (1/64 for the mean of 64 shards, exact). */
+typedef struct {
+    int64_t S, ld;
+    const float *g;
+    float scale;
+    float *out;
+} shard_ctx;
+
+static void shard_range(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    shard_ctx *q = (shard_ctx *)c;
+    for (int64_t i = lo; i < hi; ++i) {
+        float t = q->g[i];                        /* shard 0 as is */
+        for (int64_t s = 1; s < q->S; ++s) t = t + q->g[s * q->ld + i];
+        q->out[i] = t * q->scale;
+    }
+}
+
+void detor_shardsum(int64_t nshards, int64_t n, const float *shards, int64_t ld,
+                    float scale, float *out, int nthreads) {
+    if (nshards < 1 || n < 1) return;
+    shard_ctx c = {nshards, ld, shards, scale, out};
+    parallel_for(n, nthreads, shard_range, &c);
+}
+
 /* ------------------------------------------------------------------------ */
 /* the profile's fixed reduction tree over `lanes` chain sums               */
 /* ------------------------------------------------------------------------ */

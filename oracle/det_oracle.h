@@ -55,6 +55,17 @@ void detor_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
                    const float *gain, float eps, float *y, int64_t ldy,
                    float *inv_rms, int lanes, int group, int nthreads);
 
+/* C = C + op(A) op(B): the profile GEMM's result R (chunk partials left to
+ * right) added to the old C by one rounded addition, C on the left. */
+void detor_gemm_acc(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                    const float *A, int64_t lda, const float *B, int64_t ldb,
+                    float *C, int64_t ldc, int64_t k_chunk, int nthreads);
+
+/* out[i] = scale * (((g_0[i] + g_1[i]) + g_2[i]) + ... + g_{S-1}[i]) over the
+ * S shards g_s = shards + s * ld, left to right, one rounding each. */
+void detor_shardsum(int64_t nshards, int64_t n, const float *shards, int64_t ld,
+                    float scale, float *out, int nthreads);
+
 /* RMSNorm backward (see det_oracle.c): dx (rows x D, row stride lddx) and
  * dgain (D) from x, gain, the forward's inv_rms and dy. */
 void detor_rmsnorm_bwd(int64_t rows, int64_t D, const float *x, int64_t ldx,
