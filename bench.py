@@ -9,6 +9,7 @@ One step = one pass of every operation of the path over one batch of the
   softmax cross-entropy over 8192 x 50257 logits (loss, mean, dlogits) ->
   RMSNorm backward 8192 x 768 (dx, dgain) ->
   weight-gradient GEMMs X^T dY over the 8,192 tokens (768x2304, 2048x768) ->
+  fixed-order sum of 64 gathered shard gradients of the 768x2304 weight ->
   AdamW over 162,147,840 parameters.
 Inputs are synthetic and seeded (bitwise_reproducible_fp32_gb300.inputs).
 
@@ -44,7 +45,8 @@ WORKLOAD = ("162M-decoder FP32 step: RMSNorm 8192x768, forward GEMMs "
             "(8192 tokens; 768x2304, 768x768, 2x 768x2048, 2048x768, LM head "
             "768x50257), softmax cross-entropy 8192x50257 with dlogits and mean, "
             "RMSNorm backward 8192x768 (dx, dgain), dW GEMMs over 8192 tokens "
-            "(768x2304, 2048x768), AdamW 162,147,840 params")
+            "(768x2304, 2048x768), fixed-order sum of 64 shard gradients of the "
+            "768x2304 weight, AdamW 162,147,840 params")
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
 
@@ -84,6 +86,10 @@ def bytes_rmsnorm(rows, D):
 def bytes_rmsnorm_bwd(rows, D):
     # read x, dy; write dx; gain, inv_rms, dgain
     return 12 * rows * D + 8 * D + 4 * rows
+
+
+def bytes_shardsum(nshards, n):
+    return 4 * nshards * n + 4 * n
 
 
 def bytes_xent(rows, V, dlogits=True):
@@ -183,8 +189,9 @@ def run_ours(args, rank, world, local_rank):
     fwd, dw = gemm_list()
     r4 = inputs.rowops_cfg4()
     rb = inputs.rmsnorm_bwd_cfg4()
+    sg = inputs.shard_grads()
     aw = inputs.adamw_cfg5()
-    host = dict(fwd=fwd, dw=dw, r4=r4, rb=rb, aw=aw)
+    host = dict(fwd=fwd, dw=dw, r4=r4, rb=rb, sg=sg, aw=aw)
 
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -220,6 +227,8 @@ def run_ours(args, rank, world, local_rank):
     dgain4 = torch.empty(x4.shape[1], dtype=torch.float32, device=dev)
     ws_rb = torch.empty((detlib.detrmsnorm_bwd_workspace_bytes(*x4.shape) + 3) // 4,
                         dtype=torch.float32, device=dev)
+    shards = up(sg)
+    gsum = torch.empty(sg.shape[1], dtype=torch.float32, device=dev)
     P, G, Mm, Vv = (up(aw[k]) for k in ("p", "g", "m", "v"))
     hp = {k: aw[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")}
     # L2 flush: write 512 MB, then read another 512 MB so the L2 holds clean
@@ -238,12 +247,13 @@ def run_ours(args, rank, world, local_rank):
     lm_idx = [p["name"] for p in fwd].index("lm_head")
     # one launch per GEMM, plus the split-K second pass where a workspace is used
     # rmsnorm; one launch per GEMM plus the split-K second pass where a
-    # workspace is used; xent + mean; the RMSNorm backward's two; AdamW
+    # workspace is used; xent + mean; the RMSNorm backward's two; the shard
+    # sum; AdamW
     launches_per_step = (1 + len(fwd) + sum(w is not None for w in ws_fwd) + 2 + 2 + len(dw)
-                         + sum(w is not None for w in ws_dw) + 1)
+                         + sum(w is not None for w in ws_dw) + 1 + 1)
 
     segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "rmsnorm_bwd", "gemm_dw",
-            "adamw"]
+            "shard_sum", "adamw"]
 
     def step(ev=None):
         def mark(i):
@@ -271,8 +281,10 @@ def run_ours(args, rank, world, local_rank):
             detlib.detgemm_f32(A, B, c_dw[i], transA=p["transA"], transB=p["transB"],
                                workspace=ws_dw[i])
         mark(6)
-        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
+        detlib.detshardsum_f32(shards, scale=1.0 / shards.shape[0], out=gsum)
         mark(7)
+        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
+        mark(8)
 
     import torch.distributed as dist
     distributed = world > 1
@@ -350,6 +362,9 @@ def run_ours(args, rank, world, local_rank):
             "rmsnorm_bwd": {"gbs": bytes_rmsnorm_bwd(rows4, D4) / per("rmsnorm_bwd") / 1e9,
                             "frac_hbm": bytes_rmsnorm_bwd(rows4, D4) / per("rmsnorm_bwd") / 1e9 / hbm,
                             "ms": per("rmsnorm_bwd") * 1e3},
+            "shard_sum": {"gbs": bytes_shardsum(*sg.shape) / per("shard_sum") / 1e9,
+                          "frac_hbm": bytes_shardsum(*sg.shape) / per("shard_sum") / 1e9 / hbm,
+                          "ms": per("shard_sum") * 1e3},
             "xent": {"gbs": bytes_xent(rows4, V) / per("xent") / 1e9,
                      "frac_hbm": bytes_xent(rows4, V) / per("xent") / 1e9 / hbm,
                      "ms": per("xent") * 1e3},
@@ -391,6 +406,10 @@ def run_ours(args, rank, world, local_rank):
                                 "peak": hbm, "unit": "GB/s",
                                 "frac": round(ops["rmsnorm_bwd"]["frac_hbm"], 4),
                                 "traffic": traffic.get("rmsnorm_bwd")},
+                "shard_sum": {"bound": "hbm", "achieved": round(ops["shard_sum"]["gbs"], 1),
+                              "peak": hbm, "unit": "GB/s",
+                              "frac": round(ops["shard_sum"]["frac_hbm"], 4),
+                              "traffic": traffic.get("shard_sum")},
                 "xent": {"bound": "hbm", "achieved": round(ops["xent"]["gbs"], 1),
                          "peak": hbm, "unit": "GB/s",
                          "frac": round(ops["xent"]["frac_hbm"], 4),
@@ -433,7 +452,7 @@ def e2e_leg(args, dev, host, gemm_flops):
 
     from bitwise_reproducible_fp32_gb300 import detlib
 
-    fwd, dw, r4, rb, aw = host["fwd"], host["dw"], host["r4"], host["rb"], host["aw"]
+    fwd, dw, r4, rb, sg, aw = (host[k] for k in ("fwd", "dw", "r4", "rb", "sg", "aw"))
     pinned = {}
 
     def pin(a):
@@ -449,6 +468,7 @@ def e2e_leg(args, dev, host, gemm_flops):
     for k in ("x", "gain", "logits", "labels"):
         srcs.append(pin(r4[k]))
     srcs.append(pin(rb["dy"]))
+    srcs.append(pin(sg))
     for k in ("p", "g", "m", "v"):
         srcs.append(pin(aw[k]))
     uniq = list({id(s[0]): s for s in srcs}.values())
@@ -469,7 +489,8 @@ def e2e_leg(args, dev, host, gemm_flops):
     dgain4 = torch.empty(D4, dtype=torch.float32, device=dev)
     ws_rb = torch.empty((detlib.detrmsnorm_bwd_workspace_bytes(rows4, D4) + 3) // 4,
                         dtype=torch.float32, device=dev)
-    dev_outs = outs_dev + [y4, inv4, loss, lmean, dlog, dx4, dgain4]
+    gsum = torch.empty(sg.shape[1], dtype=torch.float32, device=dev)
+    dev_outs = outs_dev + [y4, inv4, loss, lmean, dlog, dx4, dgain4, gsum]
     host_outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_outs]
     pmv_host = [torch.empty(aw[k].shape, dtype=torch.float32).pin_memory()
                 for k in ("p", "m", "v")]
@@ -489,6 +510,7 @@ def e2e_leg(args, dev, host, gemm_flops):
                            dlogits=dlog, dscale=1.0 / rows4)
         detlib.detrmsnorm_bwd_f32(g(r4["x"]), g(r4["gain"]), inv4, g(rb["dy"]), dx=dx4,
                                   dgain=dgain4, workspace=ws_rb)
+        detlib.detshardsum_f32(g(sg), scale=1.0 / sg.shape[0], out=gsum)
         P, G, M, Vv = (g(aw[k]) for k in ("p", "g", "m", "v"))
         detlib.detadamw_f32(P, G, M, Vv, **hp)
         for h, d in zip(host_outs, dev_outs):
@@ -547,6 +569,11 @@ def oracle_sample(budget_s: float):
     oracle.rmsnorm_bwd(rb["x"], rb["gain"], inv, rb["dy"], nthreads=cores)
     dt = time.perf_counter() - t0
     rates["rmsnorm_bwd_gbs"] = bytes_rmsnorm_bwd(*rb["x"].shape) / dt / 1e9
+    sg = inputs.shard_grads(n=200_000)
+    t0 = time.perf_counter()
+    oracle.shardsum(sg, scale=1.0 / sg.shape[0], nthreads=cores)
+    dt = time.perf_counter() - t0
+    rates["shard_sum_gbs"] = bytes_shardsum(*sg.shape) / dt / 1e9
     n = 20_000_000
     a = inputs.adamw_cfg5(n=n)
     t0 = time.perf_counter()
@@ -557,7 +584,7 @@ def oracle_sample(budget_s: float):
     sample = (f"LM-head GEMM rows 0..{rows_done - 1} of 8192 (x 50257 x 768, "
               f"{flops / 1e9:.1f} GFLOP); xent {r4['logits'].shape[0]} rows x 50257 "
               f"with dlogits; RMSNorm {r4['x'].shape[0]} rows; RMSNorm backward 512 rows; "
-              f"AdamW {n} params")
+              f"shard sum 64 x 200000; AdamW {n} params")
     return rates, cores, sample
 
 

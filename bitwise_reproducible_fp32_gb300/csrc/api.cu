@@ -112,11 +112,11 @@ DET_API det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int trans
     return DET_OK;
 }
 
-DET_API det_status detgemm_f32(const det_profile_v1 *prof, int transA, int transB,
-                               int64_t M, int64_t N, int64_t K, const float *A,
-                               int64_t lda, const float *B, int64_t ldb, float *C,
-                               int64_t ldc, void *workspace, size_t workspace_bytes,
-                               det_stream_t stream) {
+namespace {
+det_status gemm_entry(const det_profile_v1 *prof, int transA, int transB, int64_t M,
+                      int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                      int64_t ldb, float *C, int64_t ldc, void *workspace,
+                      size_t workspace_bytes, det_stream_t stream, int accumulate) {
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
     if (M < 0 || N < 0 || K < 0 || M > kDimMax || N > kDimMax || K > kDimMax)
@@ -132,8 +132,46 @@ DET_API det_status detgemm_f32(const det_profile_v1 *prof, int transA, int trans
     GemmArgs a;
     a.M = M; a.N = N; a.K = K; a.lda = lda; a.ldb = ldb; a.ldc = ldc;
     a.A = A; a.B = B; a.C = C; a.transA = transA != 0; a.transB = transB != 0;
+    a.accumulate = accumulate;
     return from_cuda(launch_gemm(a, workspace, workspace_bytes,
                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+DET_API det_status detgemm_f32(const det_profile_v1 *prof, int transA, int transB,
+                               int64_t M, int64_t N, int64_t K, const float *A,
+                               int64_t lda, const float *B, int64_t ldb, float *C,
+                               int64_t ldc, void *workspace, size_t workspace_bytes,
+                               det_stream_t stream) {
+    return gemm_entry(prof, transA, transB, M, N, K, A, lda, B, ldb, C, ldc, workspace,
+                      workspace_bytes, stream, 0);
+}
+
+DET_API det_status detgemm_acc_f32(const det_profile_v1 *prof, int transA, int transB,
+                                   int64_t M, int64_t N, int64_t K, const float *A,
+                                   int64_t lda, const float *B, int64_t ldb, float *C,
+                                   int64_t ldc, void *workspace, size_t workspace_bytes,
+                                   det_stream_t stream) {
+    return gemm_entry(prof, transA, transB, M, N, K, A, lda, B, ldb, C, ldc, workspace,
+                      workspace_bytes, stream, 1);
+}
+
+DET_API det_status detshardsum_f32(const det_profile_v1 *prof, int64_t nshards, int64_t n,
+                                   const float *shards, int64_t ld, float scale, float *out,
+                                   det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (nshards < 1 || nshards > kDimMax || n < 0 || n > (int64_t(1) << 40))
+        return DET_ERR_INVALID_ARG;
+    if (n == 0) return DET_OK;
+    if (ld < n || !shards || !out) return DET_ERR_INVALID_ARG;
+    // out may be shard 0 itself; it must not overlap any other shard
+    const float *end = shards + (nshards - 1) * ld + n;
+    if (out != shards && out + n > shards && out < end) return DET_ERR_INVALID_ARG;
+    if (out == shards && nshards > 1 && ld < n) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_shardsum(nshards, n, shards, ld, scale, out,
+                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 DET_API det_status detgemm_f32_noalloc(const det_profile_v1 *prof, int transA, int transB,

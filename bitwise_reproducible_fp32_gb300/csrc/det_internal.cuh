@@ -34,6 +34,7 @@ struct GemmArgs {
     const float *A, *B;
     float *C;
     int transA, transB;
+    int accumulate = 0;    // C = C + op(A) op(B) (beta = 1)
 };
 struct GemmPlan {
     int split;             // 1: chunk partials through the workspace
@@ -69,6 +70,8 @@ cudaError_t launch_rmsnorm_bwd(int64_t rows, int64_t D, const float *x, int64_t 
                                const float *gain, const float *inv_rms, const float *dy,
                                int64_t lddy, float *dx, int64_t lddx, float *dgain,
                                float *workspace, cudaStream_t s);
+cudaError_t launch_shardsum(int64_t nshards, int64_t n, const float *shards, int64_t ld,
+                            float scale, float *out, cudaStream_t s);
 cudaError_t launch_exp_map(int64_t n, const float *x, float *y, int is_log,
                            cudaStream_t s);
 cudaError_t launch_adamw(int64_t n, float *p, const float *g, float *m, float *v,
@@ -154,6 +157,42 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
 }
+
+// Packed FP32 pairs (sm_100+ add/sub/mul/fma .rn.f32x2): each half is rounded
+// exactly as the scalar operation (round to nearest even, no flush), so two
+// independent scalar chains can share one instruction without changing a bit
+// -- except that a packed multiply must not feed a packed add or subtract: that
+// pair was measured to round as if fused.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+    f32x2 d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 splat2(float v) { return pack2(v, v); }
 
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple
 // of 16), completing on an mbarrier.

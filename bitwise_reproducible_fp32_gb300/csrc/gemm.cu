@@ -105,6 +105,7 @@ struct KArgs {
     int units_per_tile;
     int kt_per_unit;   // multiple of the k-tiles a chunk spans
     float4 *W;
+    int accumulate;    // C = C + result (beta = 1): one rounded add, C on the left
 };
 
 // Workspace layout of split mode: float4 slot of (chunk c, tile t, accumulator
@@ -123,24 +124,11 @@ __device__ __forceinline__ int64_t ws_index(int c, int ntiles, int t, int q, int
 // m/n-contiguous tile yields 4 rows of one k.
 //   thread rows (op(A)): KMAJ arow + 8r;  else arow + (r & 3) + 32 (r >> 2)
 //   thread cols (op(B)): KMAJ bcol + 4c;  else bcol + (c & 3) + 16 (c >> 2)
-// Packed FP32 pairs (sm_100+ fma.rn.f32x2): two accumulators of a row, columns
-// 2c2 and 2c2 + 1, advance by one instruction. Each half is rounded exactly
-// as fmaf, so every accumulator still follows its own ascending-k chain; the
-// pair only halves the issue slots the FFMA stream takes.
-typedef unsigned long long f32x2;
-__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
-    f32x2 d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
-    return d;
-}
-__device__ __forceinline__ void unpack2(f32x2 v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
-    f32x2 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
+// Packed FP32 pairs (fma.rn.f32x2, det_internal.cuh): two accumulators of a
+// row, columns 2c2 and 2c2 + 1, advance by one instruction. Each half is
+// rounded exactly as fmaf, so every accumulator still follows its own
+// ascending-k chain; the pair only halves the issue slots the FFMA stream
+// takes.
 
 // B with m/n contiguous (B_KM false): one 16-byte load holds columns
 // {c, c+1, c+2, c+3} at one k, i.e. two column pairs ready for fma.rn.f32x2;
@@ -348,11 +336,13 @@ __device__ __forceinline__ Unit unit_of(const KArgs &p, int u, int nkt) {
 }
 
 // Stores a TM x TN register tile at rows m0 + row r, cols n0 + col c of a
-// row-major M x N matrix with row stride ld (bounds-checked).
+// row-major M x N matrix with row stride ld (bounds-checked); with accum, each
+// output becomes C + result.
 template <bool A_KM, bool B_KM>
 __device__ __forceinline__ void store_tile(const float (&acc)[TM][TN], float *base,
                                            int64_t ld, int M, int N, int m0, int n0,
-                                           int arow, int bcol, int vec) {
+                                           int arow, int bcol, int vec, int accum) {
+    auto out = [accum](float *p, float v) { *p = accum ? __fadd_rn(*p, v) : v; };
 #pragma unroll
     for (int r = 0; r < TM; ++r) {
         const int i = m0 + row_of<A_KM>(arow, r);
@@ -363,20 +353,25 @@ __device__ __forceinline__ void store_tile(const float (&acc)[TM][TN], float *ba
             for (int h = 0; h < 2; ++h) {
                 const int j = n0 + col_of<B_KM>(bcol, 4 * h);
                 if (j + 3 < N) {
-                    *reinterpret_cast<float4 *>(crow + j) =
-                        make_float4(acc[r][4 * h], acc[r][4 * h + 1], acc[r][4 * h + 2],
-                                    acc[r][4 * h + 3]);
+                    float4 v = make_float4(acc[r][4 * h], acc[r][4 * h + 1],
+                                           acc[r][4 * h + 2], acc[r][4 * h + 3]);
+                    if (accum) {
+                        const float4 o = *reinterpret_cast<const float4 *>(crow + j);
+                        v = make_float4(__fadd_rn(o.x, v.x), __fadd_rn(o.y, v.y),
+                                        __fadd_rn(o.z, v.z), __fadd_rn(o.w, v.w));
+                    }
+                    *reinterpret_cast<float4 *>(crow + j) = v;
                 } else {
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        if (j + c < N) crow[j + c] = acc[r][4 * h + c];
+                        if (j + c < N) out(crow + j + c, acc[r][4 * h + c]);
                 }
             }
         } else {
 #pragma unroll
             for (int c = 0; c < TN; ++c) {
                 const int j = n0 + col_of<B_KM>(bcol, c);
-                if (j < N) crow[j] = acc[r][c];
+                if (j < N) out(crow + j, acc[r][c]);
             }
         }
     }
@@ -557,7 +552,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // epilogue (the next unit's loads are already in flight)
         if (!SPLIT)
             store_tile<A_KM, B_KM>(acc, p.C, p.ldc, p.M, p.N, w.m0, w.n0, arow, bcol,
-                                   p.vec_store);
+                                   p.vec_store, p.accumulate);
     }
 
     if (TMA && aborted && tid == 0) {
@@ -608,18 +603,18 @@ __global__ void chunk_sum_kernel(KArgs p, int nchunks, int a_km, int b_km) {
         for (int cc = 0; cc < 4; ++cc) {
             const int c = 4 * h + cc;
             const int j = nb * BN + (b_km ? bcol + 4 * c : bcol + (c & 3) + (c >> 2) * 16);
-            if (j < p.N) crow[j] = v[cc];
+            if (j < p.N) crow[j] = p.accumulate ? __fadd_rn(crow[j], v[cc]) : v[cc];
         }
     }
 }
 
-// K == 0: the empty sum, +0 everywhere.
-__global__ void fill_zero_kernel(float *C, int64_t ldc, int64_t M, int64_t N) {
+// K == 0: the empty sum, +0 everywhere (C + 0 when accumulating).
+__global__ void fill_zero_kernel(float *C, int64_t ldc, int64_t M, int64_t N, int accum) {
     const int64_t total = M * N;
     for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total;
          e += int64_t(gridDim.x) * blockDim.x) {
         const int64_t i = e / N, j = e - i * N;
-        C[i * ldc + j] = 0.0f;
+        C[i * ldc + j] = accum ? __fadd_rn(C[i * ldc + j], 0.0f) : 0.0f;
     }
 }
 
@@ -761,7 +756,7 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
     if (a.K == 0) {
         const int64_t total = a.M * a.N;
         const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 32);
-        fill_zero_kernel<<<unsigned(blocks), 256, 0, s>>>(a.C, a.ldc, a.M, a.N);
+        fill_zero_kernel<<<unsigned(blocks), 256, 0, s>>>(a.C, a.ldc, a.M, a.N, a.accumulate);
         return cudaGetLastError();
     }
     const int sms = sm_count_current_device();
@@ -784,6 +779,7 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
     k.units_per_tile = pl.units_per_tile;
     k.kt_per_unit = pl.kt_per_unit;
     k.W = static_cast<float4 *>(pl.split ? workspace : nullptr);
+    k.accumulate = a.accumulate;
     // op(A) is k-contiguous when A is not transposed; op(B) when B is.
     const bool a_km = !a.transA, b_km = a.transB != 0;
     CUtensorMap ma{}, mb{};

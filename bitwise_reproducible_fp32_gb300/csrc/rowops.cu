@@ -292,42 +292,6 @@ __device__ __forceinline__ float dl_of_label(float e, float inv, float dscale) {
     return __fmul_rn(__fsub_rn(__fmul_rn(e, inv), 1.0f), dscale);
 }
 
-// Packed FP32 pairs (sm_100+ add/sub/mul/fma .f32x2): each half is rounded
-// exactly as the scalar operation (round to nearest even, no flush), so a
-// pair of scalar chains can share one instruction without changing a bit --
-// except that a packed multiply must not feed a packed add or subtract (see
-// exp2_le0_fast).
-typedef unsigned long long f32x2;
-__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
-    f32x2 d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
-    return d;
-}
-__device__ __forceinline__ void unpack2(f32x2 v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
-    f32x2 d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
-    f32x2 d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
-    f32x2 d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
-    f32x2 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ f32x2 splat2(float v) { return pack2(v, v); }
-
 // exp_le0_fast on a pair: d = x - m, then the same rounded steps as the scalar
 // routine on both halves at once; n ln2 enters as n (-LN2_HI), which is the
 // same product as (-n) LN2_HI. Returns the pair and the two n.

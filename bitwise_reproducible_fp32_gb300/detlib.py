@@ -52,6 +52,9 @@ SIGNATURES = [
     ("det_status_string", ctypes.c_char_p, [_int]),
     ("detgemm_f32", _int, [_PROF, _int, _int, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
                            _vp, _i64, _vp, ctypes.c_size_t, _vp]),
+    ("detgemm_acc_f32", _int, [_PROF, _int, _int, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
+                               _vp, _i64, _vp, ctypes.c_size_t, _vp]),
+    ("detshardsum_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _f, _vp, _vp]),
     ("detgemm_workspace_bytes", _int, [_PROF, _int, _int, _i64, _i64, _i64,
                                        ctypes.POINTER(ctypes.c_size_t)]),
     ("detgemm_f32_noalloc", _int, [_PROF, _int, _int, _i64, _i64, _i64, _vp, _i64, _vp,
@@ -187,6 +190,47 @@ def detgemm_f32(A, B, C=None, transA=False, transB=False, workspace=None, profil
                             ws_ptr, ws_bytes, _stream(stream))
     _check("detgemm_f32", st)
     return C
+
+
+def detgemm_acc_f32(A, B, C, transA=False, transB=False, workspace=None, profile=None,
+                    stream=None):
+    """C = C + op(A) @ op(B) (beta = 1) under the profile, in place. Returns C."""
+    _cuda_f32(A, "A", 2)
+    _cuda_f32(B, "B", 2)
+    _cuda_f32(C, "C", 2)
+    M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])
+    Kb, N = (B.shape[1], B.shape[0]) if transB else (B.shape[0], B.shape[1])
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {M} x {N}")
+    ws_ptr, ws_bytes = ctypes.c_void_p(), 0
+    if workspace is not None:
+        _cuda_f32(workspace, "workspace")
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * 4
+    st = load().detgemm_acc_f32(_prof(profile), int(bool(transA)), int(bool(transB)), M, N,
+                                K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
+                                ws_ptr, ws_bytes, _stream(stream))
+    _check("detgemm_acc_f32", st)
+    return C
+
+
+def detshardsum_f32(shards, scale=1.0, out=None, profile=None, stream=None):
+    """scale * (((g_0 + g_1) + g_2) + ...) over the rows of shards (S x n, a
+    2-D float32 CUDA tensor: one gathered shard gradient a row). Returns out
+    (n floats; it may be shards[0])."""
+    import torch
+    _cuda_f32(shards, "shards", 2)
+    S, n = shards.shape
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=shards.device)
+    _cuda_f32(out, "out")
+    if out.numel() != n or (out.dim() > 1 and not out.is_contiguous()):
+        raise ValueError(f"out must hold {n} contiguous floats")
+    st = load().detshardsum_f32(_prof(profile), S, n, _ptr(shards), _ld(shards),
+                                ctypes.c_float(scale), _ptr(out), _stream(stream))
+    _check("detshardsum_f32", st)
+    return out
 
 
 def detgemm_f32_noalloc(A, B, C, transA=False, transB=False, profile=None, stream=None):

@@ -25,6 +25,8 @@ N_PARAMS = 162_147_840   # the 162M decoder's parameter count
 
 SEED_CFG1, SEED_CFG2, SEED_CFG3, SEED_CFG4, SEED_CFG5 = 0, 1, 2, 3, 4
 SEED_RMS_BWD = 5   # the backward row-op inputs (their own stream)
+SEED_SHARDS = 6    # shard gradients for the fixed-order shard sum
+N_SHARDS = 64      # the 162M model card's logical shards a step
 
 
 def uniform_pm1(rng: np.random.Generator, shape) -> np.ndarray:
@@ -148,6 +150,15 @@ def dw_cfg5(seed: int = SEED_CFG5, tokens: int = TOKENS, d: int = D_MODEL,
         dict(name="dW_qkv", A=X1, B=dY1, transA=True, transB=False),
         dict(name="dW_down", A=X2, B=dY2, transA=True, transB=False),
     ]
+
+
+def shard_grads(seed: int = SEED_SHARDS, nshards: int = N_SHARDS,
+                n: int = D_MODEL * 3 * D_MODEL):
+    """nshards gathered shard gradients of one weight (default: the 768 x 2304
+    QKV weight), each N(0, 1e-3) -- the scale of dY here, standing in for a
+    per-shard mean gradient. One draw: an nshards x n array."""
+    rng = np.random.default_rng(seed)
+    return normal(rng, (nshards, n), 1e-3)
 
 
 ADAMW_HP = dict(lr=6e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,

@@ -11,6 +11,7 @@ DRAM counters mean something:
   xent      cross-entropy 1024 x 50257 with dlogits and mean
   rmsnorm   RMSNorm 8192 x 768
   rms_bwd   RMSNorm backward 8192 x 768 (dx, dgain)
+  shardsum  fixed-order sum of 64 shard gradients of 768 x 2304
   adamw     AdamW over 32 Mi parameters
 Each run is one warm-up launch followed by R launches (default 2).
 """
@@ -29,7 +30,7 @@ def main(argv=None):
 
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["lm_head", "qkv", "dw_qkv", "xent", "rmsnorm", "rms_bwd",
-                                    "adamw"])
+                                    "shardsum", "adamw"])
     ap.add_argument("--reps", type=int, default=2)
     a = ap.parse_args(argv)
     build.build()
@@ -73,6 +74,10 @@ def main(argv=None):
         ws = torch.empty((detlib.detrmsnorm_bwd_workspace_bytes(*x.shape) + 3) // 4,
                          dtype=torch.float32, device=dev)
         run = lambda: detlib.detrmsnorm_bwd_f32(x, g, inv, dy, dx=dx, dgain=dgain, workspace=ws)
+    elif a.case == "shardsum":
+        g = up(inputs.shard_grads())
+        out = torch.empty(g.shape[1], dtype=torch.float32, device=dev)
+        run = lambda: detlib.detshardsum_f32(g, scale=1.0 / g.shape[0], out=out)
     else:
         w = inputs.adamw_cfg5(n=32 * 1024 * 1024)
         P, G, M_, V_ = (up(w[k]) for k in ("p", "g", "m", "v"))

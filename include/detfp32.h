@@ -115,6 +115,42 @@ det_status detgemm_f32(const det_profile_v1 *prof, int transA, int transB,
                        void *workspace, size_t workspace_bytes,
                        det_stream_t stream);
 
+/* Gradient accumulation (beta = 1): C = C + op(A) op(B). The product is formed
+ * exactly as detgemm_f32 forms it (256-wide chunk chains from +0, partials
+ * added left to right) and then added to the old C by one rounded addition,
+ * so accumulating the shards of a batch one after another gives the same bits
+ * as detshardsum_f32 over their separate products ("MojoLearn 162M" model
+ * card, table "Training": shard gradients summed in a fixed order). The pages
+ * print no spelling of the accumulation; this is profile v1's reading.
+ *
+ * Arguments, layout, workspace and errors as detgemm_f32; C is read and
+ * written (K == 0 gives C + 0). */
+det_status detgemm_acc_f32(const det_profile_v1 *prof, int transA, int transB,
+                           int64_t M, int64_t N, int64_t K,
+                           const float *A, int64_t lda,
+                           const float *B, int64_t ldb,
+                           float *C, int64_t ldc,
+                           void *workspace, size_t workspace_bytes,
+                           det_stream_t stream);
+
+/* Fixed-order sum of gathered shard gradients ("MojoLearn 162M" model card,
+ * table "Training": 64 logical shards, each a mean over 4 x 2,048 tokens,
+ * summed in a fixed order). Profile v1 reads the order as left to right:
+ *   out[i] = scale * (((g_0[i] + g_1[i]) + g_2[i]) + ... + g_{S-1}[i])
+ * one rounding per addition and one multiply (scale = 1/64 gives the mean of
+ * 64 shards exactly). A multi-device caller gathers the shard gradients
+ * unreduced (an all-gather moves bytes only) and calls this; a collective's
+ * own reduction must not be used, because its order is not the profile's.
+ *
+ * shards: nshards x n floats, shard s at shards + s * ld, ld >= n (device).
+ * out: n floats (device); it may be shard 0 itself and must not overlap any
+ * other shard. nshards >= 1; n may be 0 (no work).
+ * Errors: DET_ERR_INVALID_ARG for nshards < 1, n < 0, ld < n, null pointers
+ * with n > 0, or an overlap other than out == shards. */
+det_status detshardsum_f32(const det_profile_v1 *prof, int64_t nshards, int64_t n,
+                           const float *shards, int64_t ld, float scale, float *out,
+                           det_stream_t stream);
+
 /* Workspace that detgemm_f32 can use for this shape on the current device
  * (0 when splitting K would not help), written to *bytes. Same argument rules
  * as detgemm_f32; a host-only query apart from reading the device's SM

@@ -29,6 +29,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("detgemm_f32", "detgemm_workspace_bytes", "detrmsnorm_f32", "detxent_f32", "detadamw_f32",
                  "detrmsnorm_bwd_f32", "detrmsnorm_bwd_workspace_bytes",
+                 "detgemm_acc_f32", "detshardsum_f32",
                  "detexp_f32", "detlog_f32", "det_profile_default",
                  "det_status_string", "det_watchdog_status"):
         assert want in names
@@ -82,6 +83,10 @@ def test_unknown_profile_is_refused_by_name(lib, field, value):
                                   null, 4, null, null, 0, null) == 2
     n = ctypes.c_size_t(7)
     assert lib.detrmsnorm_bwd_workspace_bytes(ctypes.byref(p), 1000, 8, ctypes.byref(n)) == 2
+    assert lib.detgemm_acc_f32(ctypes.byref(p), 0, 0, 4, 4, 4, null, 4, null, 4, null, 4,
+                               null, 0, null) == 2
+    assert lib.detshardsum_f32(ctypes.byref(p), 2, 4, null, 4, ctypes.c_float(1.0), null,
+                               null) == 2
 
 
 def test_bad_arguments_are_refused_on_the_host(lib):
@@ -121,6 +126,19 @@ def test_bad_arguments_are_refused_on_the_host(lib):
     assert lib.detrmsnorm_bwd_workspace_bytes(p, 256, 768, ctypes.byref(n)) == 0 and n.value == 0
     assert lib.detrmsnorm_bwd_workspace_bytes(p, 8192, 768, ctypes.byref(n)) == 0
     assert n.value == 32 * 768 * 4
+    # accumulating GEMM: the GEMM's rules; shard sum: counts, strides, overlap
+    assert lib.detgemm_acc_f32(p, 0, 0, 4, 4, 8, dummy, 7, dummy, 4, dummy, 4, null, 0,
+                               null) == 1
+    assert lib.detgemm_acc_f32(p, 0, 0, 0, 4, 8, null, 8, null, 4, null, 4, null, 0, null) == 0
+    ss = lib.detshardsum_f32
+    one = ctypes.c_float(1.0)
+    assert ss(p, 0, 8, dummy, 8, one, dummy, null) == 1
+    assert ss(p, 2, -1, dummy, 8, one, dummy, null) == 1
+    assert ss(p, 2, 8, dummy, 7, one, dummy, null) == 1
+    assert ss(p, 2, 8, null, 8, one, dummy, null) == 1
+    assert ss(p, 2, 8, ctypes.c_void_p(0x1000), 8, one, ctypes.c_void_p(0x1000 + 4 * 8),
+              null) == 1                                   # out over shard 1
+    assert ss(p, 2, 0, null, 0, one, null, null) == 0
     hp = detlib.AdamWHP(1e-3, 0.9, 0.95, 1e-8, 0.1, 0)
     assert lib.detadamw_f32(p, 4, dummy, dummy, dummy, dummy, ctypes.byref(hp), null) == 1
     assert lib.detexp_f32(p, -1, dummy, dummy, null) == 1

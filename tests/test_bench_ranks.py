@@ -52,3 +52,55 @@ def test_replica_throughput():
     # two replicas of 1 TFLOP each, the slower taking 100 ms: 20 TFLOP/s
     assert bench.replica_throughput(1e12, 2, 100.0) == pytest.approx(2e13)
     assert bench.replica_throughput(1e12, 1, 100.0) == pytest.approx(1e13)
+
+
+def _shard_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port),
+                      RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import oracle
+    from bitwise_reproducible_fp32_gb300 import inputs, shards
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        g = inputs.shard_grads(nshards=8, n=5003)
+        k = 8 // world
+        local = torch.from_numpy(np.ascontiguousarray(g[rank * k:(rank + 1) * k]))
+        out = shards.ordered_shard_mean(
+            local, sum_fn=lambda x, s: torch.from_numpy(oracle.shardsum(x.numpy(), scale=s)))
+        q.put((rank, out.numpy().tobytes()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_gathered_shard_sum_gloo_world2():
+    # two ranks, four shards each: gathering unreduced in global shard order
+    # and summing left to right gives, on every rank, the bits of one device's
+    # sum of all eight shards
+    import socket
+
+    import numpy as np
+    import torch.multiprocessing as mp
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from bitwise_reproducible_fp32_gb300 import inputs
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_shard_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    want = oracle.shardsum(inputs.shard_grads(nshards=8, n=5003), scale=1.0 / 8).tobytes()
+    assert out[0] == out[1] == want
