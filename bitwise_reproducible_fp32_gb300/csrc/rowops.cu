@@ -661,18 +661,37 @@ __device__ __forceinline__ void load_granules(float4 *buf, const float *xa, int 
 // elements of granule g and the first H of granule g + 1; both granules are
 // read with 16-byte loads (consecutive chains, consecutive granules: no bank
 // conflicts), one sweep ahead of the adds.
+// 16-byte load from shared memory by shared-window address: the chain runs in
+// an out-of-line function, where a plain pointer would compile to a generic
+// load (slower, and tracked as a long-latency access).
+__device__ __forceinline__ float4 lds4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float lds1(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
 template <int H>
-__device__ __noinline__ float xent_smem_chain(const float4 *buf, int V) {
+__device__ __noinline__ float xent_smem_chain(uint32_t buf, int V) {
     const int l = threadIdx.x;
     const int ngroups = (V + 3) >> 2, gfull = V >> 2;
     float s = 0.0f;
     int g = l;
     if (g < gfull) {
-        float4 c0 = buf[g], c1 = H ? buf[g + 1] : c0;
+        float4 c0 = lds4(buf + 16u * g), c1 = H ? lds4(buf + 16u * (g + 1)) : c0;
         for (; g < gfull; g += kXentLanes) {
             const int gn = g + kXentLanes;
             float4 n0 = c0, n1 = c1;
-            if (gn < gfull) { n0 = buf[gn]; if (H) n1 = buf[gn + 1]; }
+            if (gn < gfull) {
+                n0 = lds4(buf + 16u * gn);
+                if (H) n1 = lds4(buf + 16u * (gn + 1));
+            }
             const float4 v = group_of<H>(c0, c1);
             s = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(s, v.x), v.y), v.z), v.w);
             c0 = n0;
@@ -680,8 +699,7 @@ __device__ __noinline__ float xent_smem_chain(const float4 *buf, int V) {
         }
     }
     if (g < ngroups) {     // the last, partial group
-        const float *ef = reinterpret_cast<const float *>(buf) + H;
-        for (int j = 4 * g; j < V; ++j) s = __fadd_rn(s, ef[j]);
+        for (int j = 4 * g; j < V; ++j) s = __fadd_rn(s, lds1(buf + 4u * (j + H)));
     }
     return s;
 }
@@ -785,10 +803,10 @@ __global__ void __launch_bounds__(kXsThreads, 1)
             if (tid < kXentLanes) {
                 float s;
                 switch (h) {
-                    case 0: s = xent_smem_chain<0>(buf, V); break;
-                    case 1: s = xent_smem_chain<1>(buf, V); break;
-                    case 2: s = xent_smem_chain<2>(buf, V); break;
-                    default: s = xent_smem_chain<3>(buf, V); break;
+                    case 0: s = xent_smem_chain<0>(smem_u32(buf), V); break;
+                    case 1: s = xent_smem_chain<1>(smem_u32(buf), V); break;
+                    case 2: s = xent_smem_chain<2>(smem_u32(buf), V); break;
+                    default: s = xent_smem_chain<3>(smem_u32(buf), V); break;
                 }
                 s = warp_butterfly_sum(s);
                 if (lane == 0) red[warp] = s;
