@@ -81,6 +81,20 @@ def _load():
                                    i64, f32p, i64, i64, c_int]
         lib.detor_rmsnorm.argtypes = [i64, i64, f32p, i64, f32p, ctypes.c_float,
                                       f32p, i64, f32p, c_int, c_int, c_int]
+        for name in ("detor_sin", "detor_cos"):
+            getattr(lib, name).restype = ctypes.c_float
+            getattr(lib, name).argtypes = [ctypes.c_float]
+        lib.detor_sin_n.argtypes = [i64, f32p, f32p, c_int]
+        lib.detor_cos_n.argtypes = [i64, f32p, f32p, c_int]
+        lib.detor_rope.argtypes = [i64, i64, i64, f32p, i64, i64, ctypes.c_float, c_int]
+        lib.detor_sincos_ulp_scan.restype = ctypes.c_double
+        lib.detor_sincos_ulp_scan.argtypes = [c_int, ctypes.c_uint32, ctypes.c_uint32,
+                                              ctypes.c_uint32, c_int,
+                                              ctypes.POINTER(ctypes.c_uint32)]
+        lib.detor_swiglu.argtypes = [i64, f32p, f32p, f32p, c_int]
+        lib.detor_add.argtypes = [i64, f32p, f32p, f32p, c_int]
+        lib.detor_softmax_causal.argtypes = [i64, i64, f32p, i64, ctypes.c_float, i64, f32p,
+                                             i64, c_int, c_int, c_int]
         lib.detor_gemm_acc.argtypes = [c_int, c_int, i64, i64, i64, f32p, i64, f32p,
                                        i64, f32p, i64, i64, c_int]
         lib.detor_shardsum.argtypes = [i64, i64, f32p, i64, ctypes.c_float, f32p, c_int]
@@ -192,6 +206,71 @@ def gemm_acc(C, A, B, transA=False, transB=False, k_chunk=K_CHUNK, nthreads=None
                            _fp(B), B.strides[0] // 4, _fp(out), N, int(k_chunk),
                            _threads(nthreads))
     return out
+
+
+def sin(x, nthreads=None) -> np.ndarray:
+    x = np.ascontiguousarray(_f32(x))
+    y = np.empty_like(x)
+    _load().detor_sin_n(x.size, _fp(x), _fp(y), _threads(nthreads))
+    return y
+
+
+def cos(x, nthreads=None) -> np.ndarray:
+    x = np.ascontiguousarray(_f32(x))
+    y = np.empty_like(x)
+    _load().detor_cos_n(x.size, _fp(x), _fp(y), _threads(nthreads))
+    return y
+
+
+def sincos_ulp_scan(which, lo_bits, hi_bits, step=1, nthreads=None):
+    """(max error, worst input bits) of sin (which 0) or cos (1) over the bit
+    patterns [lo, hi) stepping by step; ulps of the true value where it is at
+    least 2^-6, ulps of 2^-6 nearer the zeros."""
+    w = ctypes.c_uint32()
+    m = _load().detor_sincos_ulp_scan(which, lo_bits, hi_bits, step, _threads(nthreads),
+                                      ctypes.byref(w))
+    return m, w.value
+
+
+def rope(x, heads, head_dim, seq_len, theta=10000.0, nthreads=None):
+    """Rotary embedding of the rows of x (rows x heads*head_dim), row t at
+    position t mod seq_len: a new array."""
+    out = np.array(_f32(x), dtype=np.float32, order="C", copy=True)
+    rows = out.shape[0]
+    _load().detor_rope(rows, heads, head_dim, _fp(out), out.shape[1], seq_len,
+                       np.float32(theta), _threads(nthreads))
+    return out
+
+
+def swiglu(gate, up, nthreads=None):
+    """(gate / (1 + exp(-gate))) * up element-wise under the profile."""
+    g = np.ascontiguousarray(_f32(gate))
+    u = np.ascontiguousarray(_f32(up))
+    assert g.shape == u.shape
+    out = np.empty_like(g)
+    _load().detor_swiglu(g.size, _fp(g), _fp(u), _fp(out), _threads(nthreads))
+    return out
+
+
+def add(a, b, nthreads=None):
+    """a + b element-wise, one rounding."""
+    a = np.ascontiguousarray(_f32(a))
+    b = np.ascontiguousarray(_f32(b))
+    assert a.shape == b.shape
+    out = np.empty_like(a)
+    _load().detor_add(a.size, _fp(a), _fp(b), _fp(out), _threads(nthreads))
+    return out
+
+
+def softmax_causal(s, scale=1.0, diag=0, lanes=XENT_LANES, group=LANE_GROUP, nthreads=None):
+    """Row r keeps columns j <= r + diag of s * scale; the profile's softmax
+    over them (the cross-entropy's 256-chain sum); masked columns +0."""
+    s = np.ascontiguousarray(_f32(s))
+    rows, cols = s.shape
+    p = np.empty_like(s)
+    _load().detor_softmax_causal(rows, cols, _fp(s), cols, np.float32(scale), int(diag),
+                                 _fp(p), cols, lanes, group, _threads(nthreads))
+    return p
 
 
 def shardsum(shards, scale=1.0, nthreads=None):

@@ -213,6 +213,25 @@ void detor_log_n(int64_t n, const float *x, float *y, int nthreads) {
     parallel_for(n, nthreads, log_range, &c);
 }
 
+static void sin_range(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    map_ctx *m = (map_ctx *)c;
+    for (int64_t i = lo; i < hi; ++i) m->y[i] = detor_sin(m->x[i]);
+}
+static void cos_range(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    map_ctx *m = (map_ctx *)c;
+    for (int64_t i = lo; i < hi; ++i) m->y[i] = detor_cos(m->x[i]);
+}
+void detor_sin_n(int64_t n, const float *x, float *y, int nthreads) {
+    map_ctx c = {x, y};
+    parallel_for(n, nthreads, sin_range, &c);
+}
+void detor_cos_n(int64_t n, const float *x, float *y, int nthreads) {
+    map_ctx c = {x, y};
+    parallel_for(n, nthreads, cos_range, &c);
+}
+
 /* ------------------------------------------------------------------------ */
 /* fixed-order GEMM                                                          */
 /* ------------------------------------------------------------------------ */
@@ -267,6 +286,140 @@ void detor_gemm_acc(int transA, int transB, int64_t M, int64_t N, int64_t K,
     for (int64_t i = 0; i < M; ++i)
         for (int64_t j = 0; j < N; ++j) C[i * ldc + j] = C[i * ldc + j] + R[i * N + j];
     free(R);
+}
+
+/* ------------------------------------------------------------------------ */
+/* sin and cos (v1 spelling)                                                 */
+/* ------------------------------------------------------------------------ */
+/* The pages fix that the transcendental spellings are part of the profile and
+ * print none; the model card's rotary positions ("MojoLearn 162M", table
+ * "Compared with GPT-3 Small": rotary, theta = 10,000) need sin and cos.
+ * Reading R31 of the design notes, Cody & Waite's reduction with Taylor
+ * polynomials:
+ *   k = rint(x * 2/pi) (ties to even); r = x - k pi/2 by three fmaf steps with
+ *   pi/2 split in three floats; z = r * r;
+ *   sin_r = fmaf(r, z * Ps(z), r), Ps = Horner of the Taylor terms 1/3! .. 1/9!
+ *   cos_r = fmaf(Pc(z), z, 1),  Pc = Horner of the terms 1/2! .. 1/10!
+ *   then the quadrant k mod 4 picks +-sin_r or +-cos_r.
+ * Zero returns x for sin and 1 for cos; |x| > 2^20 and NaN give NaN. Every
+ * constant is the float nearest to its definition. */
+static const float TWO_OVER_PI = 0x1.45f306p-1f;
+static const float PIO2_1 = 0x1.921fb6p+0f, PIO2_2 = -0x1.777a5cp-25f;
+static const float PIO2_3 = -0x1.ee59dap-50f;
+static const float S3F = -0x1.555556p-3f, S5F = 0x1.111112p-7f;
+static const float S7F = -0x1.a01a02p-13f, S9F = 0x1.71de3ap-19f;
+static const float C2F = -0x1p-1f, C4F = 0x1.555556p-5f, C6F = -0x1.6c16c2p-10f;
+static const float C8F = 0x1.a01a02p-16f, C10F = -0x1.27e4fcp-22f;
+static const float TRIG_MAX = 0x1p20f;
+
+static void sincos_v1(float x, float *sn, float *cs) {
+    if (x != x || fabsf(x) > TRIG_MAX) { *sn = NAN; *cs = NAN; return; }
+    if (x == 0.0f) { *sn = x; *cs = 1.0f; return; }
+    float k = rintf(x * TWO_OVER_PI);
+    float r = fmaf(-k, PIO2_1, x);
+    r = fmaf(-k, PIO2_2, r);
+    r = fmaf(-k, PIO2_3, r);
+    float z = r * r;
+    float ps = S9F;
+    ps = fmaf(ps, z, S7F);
+    ps = fmaf(ps, z, S5F);
+    ps = fmaf(ps, z, S3F);
+    float s = fmaf(r, z * ps, r);
+    float pc = C10F;
+    pc = fmaf(pc, z, C8F);
+    pc = fmaf(pc, z, C6F);
+    pc = fmaf(pc, z, C4F);
+    pc = fmaf(pc, z, C2F);
+    float c = fmaf(pc, z, 1.0f);
+    int q = (int)k & 3;
+    *sn = q == 0 ? s : q == 1 ? c : q == 2 ? -s : -c;
+    *cs = q == 0 ? c : q == 1 ? -s : q == 2 ? -c : s;
+}
+
+float detor_sin(float x) { float s, c; sincos_v1(x, &s, &c); return s; }
+float detor_cos(float x) { float s, c; sincos_v1(x, &s, &c); return c; }
+
+/* ------------------------------------------------------------------------ */
+/* rotary position embedding                                                 */
+/* ------------------------------------------------------------------------ */
+/* Reading R30: pairs (x_2i, x_2i+1) of each head (the rotary paper's
+ * pairing) turn by a = pos * w_i, w_i = exp((-(2i / d)) * log(theta)) with the
+ * profile's exp and log, each step rounded once; then
+ *   y_2i = x_2i * c - x_2i+1 * s,  y_2i+1 = x_2i * s + x_2i+1 * c
+ * (each product rounded, then the subtraction or addition). */
+typedef struct {
+    int64_t heads, d, ldx, seq;
+    float *x;
+    float theta;
+} rope_ctx;
+
+static void rope_rows(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    rope_ctx *q = (rope_ctx *)c;
+    const float L = detor_log(q->theta);
+    for (int64_t t = lo; t < hi; ++t) {
+        const float pos = (float)(t % q->seq);
+        for (int64_t i = 0; i < q->d / 2; ++i) {
+            const float e = (float)(2 * i) / (float)q->d;
+            const float w = detor_exp(-e * L);
+            const float a = pos * w;
+            float sn, cs;
+            sincos_v1(a, &sn, &cs);
+            for (int64_t h = 0; h < q->heads; ++h) {
+                float *p = q->x + t * q->ldx + h * q->d + 2 * i;
+                const float x0 = p[0], x1 = p[1];
+                p[0] = x0 * cs - x1 * sn;
+                p[1] = x0 * sn + x1 * cs;
+            }
+        }
+    }
+}
+
+void detor_rope(int64_t rows, int64_t heads, int64_t head_dim, float *x, int64_t ldx,
+                int64_t seq_len, float theta, int nthreads) {
+    if (head_dim < 2 || head_dim % 2 || seq_len < 1 || heads < 1) return;
+    rope_ctx c = {heads, head_dim, ldx, seq_len, x, theta};
+    parallel_for(rows, nthreads, rope_rows, &c);
+}
+
+/* ------------------------------------------------------------------------ */
+/* element-wise block operations                                             */
+/* ------------------------------------------------------------------------ */
+/* "MojoLearn 162M" model card, table "Compared with GPT-3 Small": SwiGLU
+ * feed-forward (2,048 wide), pre-norm residual blocks. Readings (design notes
+ * R27, R28): silu(g) = g / (1 + exp(-g)) with the profile's exp, IEEE
+ * division, then the product with the up projection; the residual add is one
+ * rounded addition. */
+typedef struct {
+    const float *a, *b;
+    float *out;
+} ew_ctx;
+
+static void swiglu_range(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    ew_ctx *q = (ew_ctx *)c;
+    for (int64_t i = lo; i < hi; ++i) {
+        float g = q->a[i];
+        float den = 1.0f + detor_exp(-g);
+        float silu = g / den;
+        q->out[i] = silu * q->b[i];
+    }
+}
+
+static void add_range(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    ew_ctx *q = (ew_ctx *)c;
+    for (int64_t i = lo; i < hi; ++i) q->out[i] = q->a[i] + q->b[i];
+}
+
+void detor_swiglu(int64_t n, const float *gate, const float *up, float *out, int nthreads) {
+    ew_ctx c = {gate, up, out};
+    parallel_for(n, nthreads, swiglu_range, &c);
+}
+
+void detor_add(int64_t n, const float *a, const float *b, float *out, int nthreads) {
+    ew_ctx c = {a, b, out};
+    parallel_for(n, nthreads, add_range, &c);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -497,6 +650,58 @@ static void xent_rows(int64_t lo, int64_t hi, int tix, void *c) {
     q->bad[tix] = bad;
 }
 
+/* ------------------------------------------------------------------------ */
+/* causal softmax of attention scores                                        */
+/* ------------------------------------------------------------------------ */
+/* The cross-entropy's row spelling applied to attention probabilities
+ * (design notes R29): row r keeps the columns j < n_r = min(cols, r + diag + 1);
+ * x_j = s_j * scale (one rounding; 1/8 for 64-wide heads, exact);
+ * m = max (NaN-propagating); e_j = exp(x_j - m); S = the lanes-chain sum of
+ * e_j folded by the butterfly; p_j = e_j * (1 / S); masked columns p_j = +0.
+ * A row with no column kept is +0 throughout. */
+typedef struct {
+    int64_t cols, lds, ldp, diag;
+    const float *s;
+    float scale;
+    float *p;
+    int lanes, group;
+} smax_ctx;
+
+static void smax_rows(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    smax_ctx *q = (smax_ctx *)c;
+    float acc[1024];
+    for (int64_t r = lo; r < hi; ++r) {
+        const float *s = q->s + r * q->lds;
+        float *p = q->p + r * q->ldp;
+        int64_t nr = r + q->diag + 1;
+        if (nr > q->cols) nr = q->cols;
+        if (nr < 0) nr = 0;
+        for (int64_t j = nr; j < q->cols; ++j) p[j] = 0.0f;
+        if (nr == 0) continue;
+        float m = s[0] * q->scale;
+        for (int64_t j = 1; j < nr; ++j) {
+            float x = s[j] * q->scale;
+            if (x > m || x != x) m = x;
+        }
+        for (int l = 0; l < q->lanes; ++l) acc[l] = 0.0f;
+        for (int64_t j = 0; j < nr; ++j) {
+            int l = (int)((j / q->group) % q->lanes);
+            acc[l] = acc[l] + detor_exp(s[j] * q->scale - m);
+        }
+        float inv = 1.0f / butterfly(acc, q->lanes);
+        for (int64_t j = 0; j < nr; ++j) p[j] = detor_exp(s[j] * q->scale - m) * inv;
+    }
+}
+
+void detor_softmax_causal(int64_t rows, int64_t cols, const float *s, int64_t lds,
+                          float scale, int64_t diag, float *p, int64_t ldp, int lanes,
+                          int group, int nthreads) {
+    if (lanes < 1 || lanes > 1024 || group < 1 || cols < 1) return;
+    smax_ctx c = {cols, lds, ldp, diag, s, scale, p, lanes, group};
+    parallel_for(rows, nthreads, smax_rows, &c);
+}
+
 int64_t detor_xent(int64_t rows, int64_t V, const float *logits, int64_t ld,
                    const int32_t *labels, float *loss, float *dlogits,
                    int64_t ldd, float dscale, int lanes, int group, int nthreads) {
@@ -626,6 +831,51 @@ static void ulp_scan(int is_log, uint32_t lo_bits, uint32_t hi_bits, int nthread
         if (s->worst[k] > *max_ulp) { *max_ulp = s->worst[k]; *worst_bits = s->worst_bits[k]; }
     }
     free(s);
+}
+
+/* sin / cos: which = 0 sin, 1 cos. The error is in ulps of the true value
+ * where |true| >= 2^-6, and in ulps of 2^-6 (an absolute error of 2^-29)
+ * nearer the zeros, where an ulp of the tiny true value measures nothing a
+ * rotation cares about. Inputs step through the bit patterns [lo, hi). */
+typedef struct {
+    uint32_t lo, step;
+    int which;
+    double worst[MAX_THREADS];
+    uint32_t worst_bits[MAX_THREADS];
+} tscan_ctx;
+
+static void tscan_range(int64_t lo, int64_t hi, int tix, void *c) {
+    tscan_ctx *s = (tscan_ctx *)c;
+    double worst = 0.0;
+    uint32_t wb = 0;
+    for (int64_t i = lo; i < hi; ++i) {
+        uint32_t bits = s->lo + (uint32_t)(i * (int64_t)s->step);
+        float x = u2f(bits);
+        if (x != x || fabsf(x) > TRIG_MAX) continue;
+        double ref = s->which ? cos((double)x) : sin((double)x);
+        float y = s->which ? detor_cos(x) : detor_sin(x);
+        double unit = fabs(ref) >= 0x1p-6 ? float_ulp_at(ref) : 0x1p-29;
+        double err = (y != y) ? INFINITY : fabs((double)y - ref) / unit;
+        if (err > worst) { worst = err; wb = bits; }
+    }
+    s->worst[tix] = worst;
+    s->worst_bits[tix] = wb;
+}
+
+double detor_sincos_ulp_scan(int which, uint32_t lo, uint32_t hi, uint32_t step,
+                             int nthreads, uint32_t *worst) {
+    *worst = 0;
+    if (hi <= lo || step == 0) return -1.0;
+    tscan_ctx *s = (tscan_ctx *)calloc(1, sizeof(tscan_ctx));
+    if (!s) return -1.0;
+    s->lo = lo; s->step = step; s->which = which;
+    for (int k = 0; k < MAX_THREADS; ++k) s->worst[k] = -1.0;
+    parallel_for(((int64_t)hi - (int64_t)lo + step - 1) / step, nthreads, tscan_range, s);
+    double m = -1.0;
+    for (int k = 0; k < MAX_THREADS; ++k)
+        if (s->worst[k] > m) { m = s->worst[k]; *worst = s->worst_bits[k]; }
+    free(s);
+    return m;
 }
 
 void detor_exp_ulp_scan(uint32_t lo_bits, uint32_t hi_bits, int nthreads,

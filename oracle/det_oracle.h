@@ -35,9 +35,22 @@ int detor_fp_env_ok(void);
 float detor_exp(float x);
 float detor_log(float x);
 
+/* The profile's sin and cos spellings (det_oracle.c), defined for
+ * |x| <= 2^20; NaN outside and for NaN. */
+float detor_sin(float x);
+float detor_cos(float x);
+
 /* Elementwise maps over n floats. */
 void detor_exp_n(int64_t n, const float *x, float *y, int nthreads);
 void detor_log_n(int64_t n, const float *x, float *y, int nthreads);
+void detor_sin_n(int64_t n, const float *x, float *y, int nthreads);
+void detor_cos_n(int64_t n, const float *x, float *y, int nthreads);
+
+/* Rotary position embedding in place (det_oracle.c): rows of `heads` heads of
+ * head_dim floats, row t at position t mod seq_len; pairs (2i, 2i + 1) of a
+ * head turn by the angle pos * theta^(-2i / head_dim). */
+void detor_rope(int64_t rows, int64_t heads, int64_t head_dim, float *x, int64_t ldx,
+                int64_t seq_len, float theta, int nthreads);
 
 /* Fixed-order GEMM: C = op(A) * op(B), op = optional transpose of a row-major
  * operand. Each C[i,j] is a sequential fmaf chain from +0 over each k_chunk-wide
@@ -65,6 +78,25 @@ void detor_gemm_acc(int transA, int transB, int64_t M, int64_t N, int64_t K,
  * S shards g_s = shards + s * ld, left to right, one rounding each. */
 void detor_shardsum(int64_t nshards, int64_t n, const float *shards, int64_t ld,
                     float scale, float *out, int nthreads);
+
+/* Max ulp error of detor_sin (which = 0) or detor_cos (which = 1) against
+ * the C library's double sin/cos over the floats [lo, hi) stepping by `step`
+ * bit patterns; the worst input goes to *worst. */
+double detor_sincos_ulp_scan(int which, uint32_t lo, uint32_t hi, uint32_t step,
+                             int nthreads, uint32_t *worst);
+
+/* SwiGLU's gate: out = (g / (1 + exp(-g))) * u element-wise (det_oracle.c). */
+void detor_swiglu(int64_t n, const float *gate, const float *up, float *out, int nthreads);
+
+/* Residual add: out = a + b element-wise, one rounding. */
+void detor_add(int64_t n, const float *a, const float *b, float *out, int nthreads);
+
+/* Causal softmax of attention scores (det_oracle.c): row r keeps the columns
+ * j <= r + diag of x = s * scale; p = exp(x - max) * (1 / S) with S the
+ * lanes-chain sum; masked columns are +0. */
+void detor_softmax_causal(int64_t rows, int64_t cols, const float *s, int64_t lds,
+                          float scale, int64_t diag, float *p, int64_t ldp, int lanes,
+                          int group, int nthreads);
 
 /* RMSNorm backward (see det_oracle.c): dx (rows x D, row stride lddx) and
  * dgain (D) from x, gain, the forward's inv_rms and dy. */
