@@ -10,6 +10,8 @@ One step = one pass of every operation of the path over one batch of the
   RMSNorm backward 8192 x 768 (dx, dgain) ->
   weight-gradient GEMMs X^T dY over the 8,192 tokens (768x2304, 2048x768) ->
   fixed-order sum of 64 gathered shard gradients of the 768x2304 weight ->
+  one pre-norm decoder block forward (RMSNorm, QKV, RoPE, causal attention,
+  out projection, residual, RMSNorm, SwiGLU, down projection, residual) ->
   AdamW over 162,147,840 parameters.
 Inputs are synthetic and seeded (bitwise_reproducible_fp32_gb300.inputs).
 
@@ -46,7 +48,8 @@ WORKLOAD = ("162M-decoder FP32 step: RMSNorm 8192x768, forward GEMMs "
             "768x50257), softmax cross-entropy 8192x50257 with dlogits and mean, "
             "RMSNorm backward 8192x768 (dx, dgain), dW GEMMs over 8192 tokens "
             "(768x2304, 2048x768), fixed-order sum of 64 shard gradients of the "
-            "768x2304 weight, AdamW 162,147,840 params")
+            "768x2304 weight, one decoder block forward (4x2048 tokens, RoPE, causal "
+            "attention 12x64, SwiGLU), AdamW 162,147,840 params")
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
 
@@ -190,8 +193,9 @@ def run_ours(args, rank, world, local_rank):
     r4 = inputs.rowops_cfg4()
     rb = inputs.rmsnorm_bwd_cfg4()
     sg = inputs.shard_grads()
+    bc = inputs.block_cfg()
     aw = inputs.adamw_cfg5()
-    host = dict(fwd=fwd, dw=dw, r4=r4, rb=rb, sg=sg, aw=aw)
+    host = dict(fwd=fwd, dw=dw, r4=r4, rb=rb, sg=sg, bc=bc, aw=aw)
 
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -229,6 +233,11 @@ def run_ours(args, rank, world, local_rank):
                         dtype=torch.float32, device=dev)
     shards = up(sg)
     gsum = torch.empty(sg.shape[1], dtype=torch.float32, device=dev)
+    from bitwise_reproducible_fp32_gb300 import block as blockmod
+    blk = blockmod.Block(bc["batch"], bc["seq"], bc["x"].shape[1], bc["W_gate"].shape[1],
+                         inputs.N_HEADS, dev)
+    bx = up(bc["x"])
+    bw = {k: up(bc[k]) for k in ("g1", "W_qkv", "W_o", "g2", "W_gate", "W_up", "W_down")}
     P, G, Mm, Vv = (up(aw[k]) for k in ("p", "g", "m", "v"))
     hp = {k: aw[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")}
     # L2 flush: write 512 MB, then read another 512 MB so the L2 holds clean
@@ -249,11 +258,17 @@ def run_ours(args, rank, world, local_rank):
     # rmsnorm; one launch per GEMM plus the split-K second pass where a
     # workspace is used; xent + mean; the RMSNorm backward's two; the shard
     # sum; AdamW
+    # one block forward: 2 RMSNorms, 5 GEMMs (+ split passes), RoPE, 3 launches
+    # an attention head (QK^T, softmax, PV + its split pass), 2 adds, SwiGLU
+    n_heads_total = bc["batch"] * inputs.N_HEADS
+    pv_split = detlib.detgemm_workspace_bytes(bc["seq"], 64, bc["seq"]) > 0
+    block_launches = (2 + 5 + sum(v is not None for v in blk.ws.values()) + 1
+                      + n_heads_total * (3 + int(pv_split)) + 2 + 1)
     launches_per_step = (1 + len(fwd) + sum(w is not None for w in ws_fwd) + 2 + 2 + len(dw)
-                         + sum(w is not None for w in ws_dw) + 1 + 1)
+                         + sum(w is not None for w in ws_dw) + 1 + block_launches + 1)
 
     segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "rmsnorm_bwd", "gemm_dw",
-            "shard_sum", "adamw"]
+            "shard_sum", "block_fwd", "adamw"]
 
     def step(ev=None):
         def mark(i):
@@ -283,8 +298,10 @@ def run_ours(args, rank, world, local_rank):
         mark(6)
         detlib.detshardsum_f32(shards, scale=1.0 / shards.shape[0], out=gsum)
         mark(7)
-        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
+        blk.forward(bx, bw)
         mark(8)
+        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
+        mark(9)
 
     import torch.distributed as dist
     distributed = world > 1
@@ -362,6 +379,9 @@ def run_ours(args, rank, world, local_rank):
             "rmsnorm_bwd": {"gbs": bytes_rmsnorm_bwd(rows4, D4) / per("rmsnorm_bwd") / 1e9,
                             "frac_hbm": bytes_rmsnorm_bwd(rows4, D4) / per("rmsnorm_bwd") / 1e9 / hbm,
                             "ms": per("rmsnorm_bwd") * 1e3},
+            "block_fwd": {"tflops": blk.flops() / per("block_fwd") / 1e12,
+                          "frac_fp32_peak": blk.flops() / per("block_fwd") / 1e12 / fma_peak,
+                          "ms": per("block_fwd") * 1e3},
             "shard_sum": {"gbs": bytes_shardsum(*sg.shape) / per("shard_sum") / 1e9,
                           "frac_hbm": bytes_shardsum(*sg.shape) / per("shard_sum") / 1e9 / hbm,
                           "ms": per("shard_sum") * 1e3},

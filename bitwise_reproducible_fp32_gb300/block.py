@@ -1,0 +1,66 @@
+"""The forward of one pre-norm decoder block through the library's operations
+("MojoLearn 162M" model card, table "Compared with GPT-3 Small": 768 wide,
+12 heads of 64, rotary positions with theta = 10,000, RMSNorm eps 1e-6,
+pre-norm, SwiGLU 2,048 wide, no biases):
+
+    h   = RMSNorm(x, g1)
+    qkv = h W_qkv;  Q, K turned by the rotary embedding
+    a   = causal attention(Q, K, V), scale 1/sqrt(64)
+    x1  = x + a W_o
+    h2  = RMSNorm(x1, g2)
+    y   = x1 + (silu(h2 W_gate) * (h2 W_up)) W_down
+
+Every step is one call of the C ABI (detlib); this module only sequences them
+and owns the intermediate buffers. Weights are K x N row-major, as the
+GEMMs take them.
+"""
+from __future__ import annotations
+
+
+class Block:
+    """Buffers and workspaces for one block's forward at a fixed shape."""
+
+    def __init__(self, batch, seq, d_model, d_ff, heads, device, eps=1e-6, theta=10000.0):
+        import torch
+
+        from bitwise_reproducible_fp32_gb300 import detlib
+        self.B, self.T, self.D, self.Fd, self.H = batch, seq, d_model, d_ff, heads
+        self.hd = d_model // heads
+        self.eps, self.theta = eps, theta
+        n = batch * seq
+        e = lambda *s: torch.empty(s, dtype=torch.float32, device=device)  # noqa: E731
+        self.h, self.inv1 = e(n, d_model), e(n)
+        self.qkv, self.att, self.o = e(n, 3 * d_model), e(n, d_model), e(n, d_model)
+        self.x1, self.h2, self.inv2 = e(n, d_model), e(n, d_model), e(n)
+        self.gate, self.up, self.dn = e(n, d_ff), e(n, d_ff), e(n, d_model)
+        self.y = e(n, d_model)
+        ws = lambda M, N, K: detlib.gemm_workspace(M, N, K, False, False, device=device)  # noqa: E731
+        self.ws = {"qkv": ws(n, 3 * d_model, d_model), "o": ws(n, d_model, d_model),
+                   "ff": ws(n, d_ff, d_model), "down": ws(n, d_model, d_ff)}
+        self.att_ws = e((detlib.detattention_workspace_bytes(seq, self.hd) + 3) // 4)
+
+    def flops(self):
+        n, D, Fd = self.B * self.T, self.D, self.Fd
+        gemm = 2 * n * (D * 3 * D + D * D + 2 * D * Fd + Fd * D)
+        attn = 2 * 2 * self.B * self.H * self.T * self.T * self.hd
+        return gemm + attn
+
+    def forward(self, x, w):
+        """x: (batch * seq) x d_model; w: g1, W_qkv, W_o, g2, W_gate, W_up,
+        W_down (device tensors). Returns y (this object's buffer)."""
+        from bitwise_reproducible_fp32_gb300 import detlib as L
+        L.detrmsnorm_f32(x, w["g1"], self.eps, y=self.h, inv_rms=self.inv1)
+        L.detgemm_f32(self.h, w["W_qkv"], self.qkv, workspace=self.ws["qkv"])
+        L.detrope_f32(self.qkv, heads=2 * self.H, head_dim=self.hd, seq_len=self.T,
+                      theta=self.theta)
+        L.detattention_f32(self.qkv, self.B, self.T, self.H, self.hd, out=self.att,
+                           workspace=self.att_ws)
+        L.detgemm_f32(self.att, w["W_o"], self.o, workspace=self.ws["o"])
+        L.detadd_f32(x, self.o, out=self.x1)
+        L.detrmsnorm_f32(self.x1, w["g2"], self.eps, y=self.h2, inv_rms=self.inv2)
+        L.detgemm_f32(self.h2, w["W_gate"], self.gate, workspace=self.ws["ff"])
+        L.detgemm_f32(self.h2, w["W_up"], self.up, workspace=self.ws["ff"])
+        L.detswiglu_f32(self.gate, self.up, out=self.gate)
+        L.detgemm_f32(self.gate, w["W_down"], self.dn, workspace=self.ws["down"])
+        L.detadd_f32(self.x1, self.dn, out=self.y)
+        return self.y

@@ -156,6 +156,161 @@ DET_API det_status detgemm_acc_f32(const det_profile_v1 *prof, int transA, int t
                       workspace_bytes, stream, 1);
 }
 
+// ---------------------------------------------------------------- block forward
+namespace {
+bool overlaps(const float *a, int64_t na, const float *b, int64_t nb) {
+    return a < b + nb && b < a + na;
+}
+}  // namespace
+
+DET_API det_status detswiglu_f32(const det_profile_v1 *prof, int64_t n, const float *gate,
+                                 const float *up, float *out, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (n < 0) return DET_ERR_INVALID_ARG;
+    if (n == 0) return DET_OK;
+    if (!gate || !up || !out) return DET_ERR_INVALID_ARG;
+    if ((out != gate && overlaps(out, n, gate, n)) || (out != up && overlaps(out, n, up, n)))
+        return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_swiglu(n, gate, up, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detadd_f32(const det_profile_v1 *prof, int64_t n, const float *a,
+                              const float *b, float *out, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (n < 0) return DET_ERR_INVALID_ARG;
+    if (n == 0) return DET_OK;
+    if (!a || !b || !out) return DET_ERR_INVALID_ARG;
+    if ((out != a && overlaps(out, n, a, n)) || (out != b && overlaps(out, n, b, n)))
+        return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_add(n, a, b, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detsoftmax_causal_f32(const det_profile_v1 *prof, int64_t rows,
+                                         int64_t cols, const float *scores, int64_t lds,
+                                         float scale, int64_t diag, int64_t period, float *p,
+                                         int64_t ldp, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (rows < 0 || cols < 1 || cols > kDimMax || period < 1) return DET_ERR_INVALID_ARG;
+    if (rows == 0) return DET_OK;
+    if (lds < cols || ldp < cols || !scores || !p) return DET_ERR_INVALID_ARG;
+    if (p == scores && ldp != lds) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_softmax_causal(rows, cols, scores, lds, scale, diag, period, p, ldp,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detrope_f32(const det_profile_v1 *prof, int64_t rows, int64_t heads,
+                               int64_t head_dim, float *x, int64_t ldx, int64_t seq_len,
+                               float theta, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (rows < 0 || heads < 1 || head_dim < 2 || head_dim % 2 || head_dim > 65536 ||
+        heads > 65536 || seq_len < 1)
+        return DET_ERR_INVALID_ARG;
+    if (rows == 0) return DET_OK;
+    if (!x || ldx < heads * head_dim) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_rope(rows, int(heads), int(head_dim), x, ldx, seq_len, theta,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detsin_f32(const det_profile_v1 *prof, int64_t n, const float *x, float *y,
+                              det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (n < 0) return DET_ERR_INVALID_ARG;
+    if (n == 0) return DET_OK;
+    if (!x || !y) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_sincos_map(n, x, y, 0, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detcos_f32(const det_profile_v1 *prof, int64_t n, const float *x, float *y,
+                              det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (n < 0) return DET_ERR_INVALID_ARG;
+    if (n == 0) return DET_OK;
+    if (!x || !y) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_sincos_map(n, x, y, 1, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Causal attention over one packed QKV activation: for every sequence b and
+// head h, S = Q_bh K_bh^T (profile GEMM), P = the causal softmax of S * scale,
+// O_bh = P V_bh (profile GEMM), each head one after the other through one
+// seq x seq score buffer in the workspace.
+namespace {
+size_t attention_ws(int64_t seq, int64_t head_dim, size_t *gemm_ws) {
+    *gemm_ws = gemm_plan(seq, head_dim, seq, sm_count_current_device()).workspace_bytes;
+    return (size_t(seq) * size_t(seq) * 4 + 255) / 256 * 256 + *gemm_ws;
+}
+}  // namespace
+
+DET_API det_status detattention_workspace_bytes(const det_profile_v1 *prof, int64_t seq,
+                                                int64_t head_dim, size_t *bytes) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (!bytes || seq < 1 || seq > 65536 || head_dim < 1 || head_dim > 65536)
+        return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    size_t g = 0;
+    *bytes = attention_ws(seq, head_dim, &g);
+    return DET_OK;
+}
+
+DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
+                                    int64_t heads, int64_t head_dim, const float *qkv,
+                                    int64_t ldqkv, float scale, float *out, int64_t ldout,
+                                    void *workspace, size_t workspace_bytes,
+                                    det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (batch < 0 || seq < 1 || seq > 65536 || heads < 1 || head_dim < 1 || head_dim > 65536 ||
+        heads > 65536)
+        return DET_ERR_INVALID_ARG;
+    if (batch == 0) return DET_OK;
+    if (!qkv || !out || ldqkv < 3 * heads * head_dim || ldout < heads * head_dim)
+        return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    size_t gws = 0;
+    const size_t need = attention_ws(seq, head_dim, &gws);
+    if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+        return DET_ERR_WORKSPACE;
+    float *scores = static_cast<float *>(workspace);
+    void *pv_ws = gws ? static_cast<char *>(workspace) + (need - gws) : nullptr;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t hd = heads * head_dim;
+    for (int64_t b = 0; b < batch; ++b) {
+        const float *base = qkv + b * seq * ldqkv;
+        for (int64_t h = 0; h < heads; ++h) {
+            GemmArgs qk;
+            qk.M = seq; qk.N = seq; qk.K = head_dim;
+            qk.A = base + h * head_dim; qk.lda = ldqkv;
+            qk.B = base + hd + h * head_dim; qk.ldb = ldqkv;
+            qk.C = scores; qk.ldc = seq;
+            qk.transA = 0; qk.transB = 1;
+            cudaError_t e = launch_gemm(qk, nullptr, 0, s);
+            if (e == cudaSuccess)
+                e = launch_softmax_causal(seq, seq, scores, seq, scale, 0, seq, scores, seq, s);
+            if (e != cudaSuccess) return DET_ERR_CUDA;
+            GemmArgs pv;
+            pv.M = seq; pv.N = head_dim; pv.K = seq;
+            pv.A = scores; pv.lda = seq;
+            pv.B = base + 2 * hd + h * head_dim; pv.ldb = ldqkv;
+            pv.C = out + b * seq * ldout + h * head_dim; pv.ldc = ldout;
+            pv.transA = 0; pv.transB = 0;
+            if (launch_gemm(pv, pv_ws, gws, s) != cudaSuccess) return DET_ERR_CUDA;
+        }
+    }
+    return DET_OK;
+}
+
 DET_API det_status detshardsum_f32(const det_profile_v1 *prof, int64_t nshards, int64_t n,
                                    const float *shards, int64_t ld, float scale, float *out,
                                    det_stream_t stream) {

@@ -70,6 +70,16 @@ cudaError_t launch_rmsnorm_bwd(int64_t rows, int64_t D, const float *x, int64_t 
                                const float *gain, const float *inv_rms, const float *dy,
                                int64_t lddy, float *dx, int64_t lddx, float *dgain,
                                float *workspace, cudaStream_t s);
+cudaError_t launch_swiglu(int64_t n, const float *g, const float *u, float *out,
+                          cudaStream_t s);
+cudaError_t launch_add(int64_t n, const float *a, const float *b, float *out, cudaStream_t s);
+cudaError_t launch_softmax_causal(int64_t rows, int64_t cols, const float *sc, int64_t lds,
+                                  float scale, int64_t diag, int64_t period, float *p,
+                                  int64_t ldp, cudaStream_t s);
+cudaError_t launch_rope(int64_t rows, int heads, int head_dim, float *x, int64_t ldx,
+                        int64_t seq_len, float theta, cudaStream_t s);
+cudaError_t launch_sincos_map(int64_t n, const float *x, float *y, int want_cos,
+                              cudaStream_t s);
 cudaError_t launch_shardsum(int64_t nshards, int64_t n, const float *shards, int64_t ld,
                             float scale, float *out, cudaStream_t s);
 cudaError_t launch_exp_map(int64_t n, const float *x, float *y, int is_log,

@@ -19,77 +19,10 @@
 #include <algorithm>
 
 #include "det_internal.cuh"
+#include "det_math.cuh"
 
 namespace det {
 namespace {
-
-// ---------------------------------------------------------------- exp / log
-// exp constants: each the float nearest to its definition. LOG2E = 1/ln 2,
-// LN2_HI = ln 2, LN2_LO = ln 2 - LN2_HI, C_k = 1/k!.
-constexpr float kLog2e = 0x1.715476p+0f;
-constexpr float kLn2Hi = 0x1.62e430p-1f;
-constexpr float kLn2Lo = -0x1.05c610p-29f;
-constexpr float kC2 = 0x1p-1f, kC3 = 0x1.555556p-3f, kC4 = 0x1.555556p-5f;
-constexpr float kC5 = 0x1.111112p-7f, kC6 = 0x1.6c16c2p-10f, kC7 = 0x1.a01a02p-13f;
-constexpr float kExpHi = 0x1.62e42ep+6f;   // largest float with a finite exp
-constexpr float kExpLo = -104.0f;          // below: +0
-// log constants: A_k = 2/k (k = 3..11 odd); the largest float below sqrt 2.
-constexpr float kA3 = 0x1.555556p-1f, kA5 = 0x1.99999ap-2f, kA7 = 0x1.24924ap-2f;
-constexpr float kA9 = 0x1.c71c72p-3f, kA11 = 0x1.745d18p-3f;
-constexpr unsigned kSqrt2Bits = 0x3fb504f3u;
-
-__device__ __forceinline__ float pow2i(int e) {   // 2^e, -126 <= e <= 127
-    return __uint_as_float(unsigned(e + 127) << 23);
-}
-
-__device__ __forceinline__ float det_exp(float x) {
-    if (x != x) return __fadd_rn(x, x);
-    if (x > kExpHi) return __uint_as_float(0x7f800000u);
-    if (x < kExpLo) return 0.0f;
-    const float t = __fmul_rn(x, kLog2e);
-    const float n = rintf(t);                 // round half to even
-    float r = __fmaf_rn(-n, kLn2Hi, x);
-    r = __fmaf_rn(-n, kLn2Lo, r);
-    float p = kC7;
-    p = __fmaf_rn(p, r, kC6);
-    p = __fmaf_rn(p, r, kC5);
-    p = __fmaf_rn(p, r, kC4);
-    p = __fmaf_rn(p, r, kC3);
-    p = __fmaf_rn(p, r, kC2);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    const int ni = __float2int_rn(n);         // |n| <= 150, exact
-    if (ni > 127) return __fmul_rn(__fadd_rn(p, p), pow2i(127));
-    if (ni < -126) return __fmul_rn(__fmul_rn(p, pow2i(ni + 64)), pow2i(-64));
-    return __fmul_rn(p, pow2i(ni));
-}
-
-__device__ __forceinline__ float det_log(float x) {
-    if (x != x) return __fadd_rn(x, x);
-    if (x < 0.0f) return __uint_as_float(0x7fc00000u);
-    if (x == 0.0f) return __uint_as_float(0xff800000u);
-    if (x == __uint_as_float(0x7f800000u)) return x;
-    int e = 0;
-    if (x < 0x1p-126f) { x = __fmul_rn(x, 0x1p23f); e = -23; }
-    const unsigned b = __float_as_uint(x);
-    e += int(b >> 23) - 127;
-    unsigned fb = (b & 0x007fffffu) | 0x3f800000u;
-    if (fb > kSqrt2Bits) { fb -= 0x00800000u; e += 1; }
-    const float f = __uint_as_float(fb);
-    const float u = __fsub_rn(f, 1.0f);
-    const float s = __fdiv_rn(u, __fadd_rn(2.0f, u));
-    const float z = __fmul_rn(s, s);
-    float R = kA11;
-    R = __fmaf_rn(R, z, kA9);
-    R = __fmaf_rn(R, z, kA7);
-    R = __fmaf_rn(R, z, kA5);
-    R = __fmaf_rn(R, z, kA3);
-    R = __fmul_rn(R, z);
-    const float h = __fmul_rn(__fmul_rn(0.5f, u), u);
-    const float lf = __fsub_rn(u, __fsub_rn(h, __fmul_rn(s, __fadd_rn(h, R))));
-    const float ef = __int2float_rn(e);
-    return __fmaf_rn(ef, kLn2Hi, __fmaf_rn(ef, kLn2Lo, lf));
-}
 
 __device__ __forceinline__ float warp_butterfly_sum(float s) {
 #pragma unroll

@@ -71,6 +71,16 @@ SIGNATURES = [
                             _vp]),
     ("detexp_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
     ("detlog_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
+    ("detswiglu_f32", _int, [_PROF, _i64, _vp, _vp, _vp, _vp]),
+    ("detadd_f32", _int, [_PROF, _i64, _vp, _vp, _vp, _vp]),
+    ("detsoftmax_causal_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _f, _i64, _i64, _vp, _i64,
+                                     _vp]),
+    ("detrope_f32", _int, [_PROF, _i64, _i64, _i64, _vp, _i64, _i64, _f, _vp]),
+    ("detsin_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
+    ("detcos_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
+    ("detattention_f32", _int, [_PROF, _i64, _i64, _i64, _i64, _vp, _i64, _f, _vp, _i64, _vp,
+                                ctypes.c_size_t, _vp]),
+    ("detattention_workspace_bytes", _int, [_PROF, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
     ("det_watchdog_status", _int, [ctypes.POINTER(ctypes.c_int32), _int]),
 ]
 
@@ -309,6 +319,122 @@ def detrmsnorm_bwd_f32(x, gain, inv_rms, dy, dx=None, dgain=None, workspace=None
                                    _ptr(dgain), _ptr(workspace), wbytes, _stream(stream))
     _check("detrmsnorm_bwd_f32", st)
     return dx, dgain
+
+
+# ---------------------------------------------------------------- block forward
+def _flat(t, name):
+    _cuda_f32(t, name)
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def detswiglu_f32(gate, up, out=None, profile=None, stream=None):
+    """(gate / (1 + exp(-gate))) * up element-wise. Returns out."""
+    import torch
+    _flat(gate, "gate")
+    _flat(up, "up")
+    if gate.shape != up.shape:
+        raise ValueError("gate and up differ in shape")
+    if out is None:
+        out = torch.empty_like(gate)
+    _flat(out, "out")
+    _check("detswiglu_f32", load().detswiglu_f32(_prof(profile), gate.numel(), _ptr(gate),
+                                                 _ptr(up), _ptr(out), _stream(stream)))
+    return out
+
+
+def detadd_f32(a, b, out=None, profile=None, stream=None):
+    """a + b element-wise, one rounding. Returns out."""
+    import torch
+    _flat(a, "a")
+    _flat(b, "b")
+    if a.shape != b.shape:
+        raise ValueError("a and b differ in shape")
+    if out is None:
+        out = torch.empty_like(a)
+    _flat(out, "out")
+    _check("detadd_f32", load().detadd_f32(_prof(profile), a.numel(), _ptr(a), _ptr(b),
+                                           _ptr(out), _stream(stream)))
+    return out
+
+
+def detsoftmax_causal_f32(scores, scale=1.0, diag=0, period=None, p=None, profile=None,
+                          stream=None):
+    """Causal softmax of a 2-D score tensor; row r keeps columns
+    j <= (r mod period) + diag. Returns p (may be scores, in place)."""
+    import torch
+    _cuda_f32(scores, "scores", 2)
+    rows, cols = scores.shape
+    if p is None:
+        p = torch.empty_like(scores)
+    _cuda_f32(p, "p", 2)
+    period = rows if period is None else period
+    st = load().detsoftmax_causal_f32(_prof(profile), rows, cols, _ptr(scores), _ld(scores),
+                                      ctypes.c_float(scale), int(diag), max(int(period), 1),
+                                      _ptr(p), _ld(p), _stream(stream))
+    _check("detsoftmax_causal_f32", st)
+    return p
+
+
+def detrope_f32(x, heads, head_dim, seq_len, theta=10000.0, profile=None, stream=None):
+    """Rotary embedding in place on the first heads * head_dim columns of the
+    rows of x (row t at position t mod seq_len). Returns x."""
+    _cuda_f32(x, "x", 2)
+    st = load().detrope_f32(_prof(profile), x.shape[0], heads, head_dim, _ptr(x), _ld(x),
+                            seq_len, ctypes.c_float(theta), _stream(stream))
+    _check("detrope_f32", st)
+    return x
+
+
+def detsin_f32(x, y=None, profile=None, stream=None):
+    return _sincos(x, y, profile, stream, "detsin_f32")
+
+
+def detcos_f32(x, y=None, profile=None, stream=None):
+    return _sincos(x, y, profile, stream, "detcos_f32")
+
+
+def _sincos(x, y, profile, stream, fn):
+    import torch
+    _flat(x, "x")
+    if y is None:
+        y = torch.empty_like(x)
+    _flat(y, "y")
+    _check(fn, getattr(load(), fn)(_prof(profile), x.numel(), _ptr(x), _ptr(y),
+                                   _stream(stream)))
+    return y
+
+
+def detattention_workspace_bytes(seq, head_dim, profile=None) -> int:
+    n = ctypes.c_size_t(0)
+    _check("detattention_workspace_bytes",
+           load().detattention_workspace_bytes(_prof(profile), seq, head_dim, ctypes.byref(n)))
+    return n.value
+
+
+def detattention_f32(qkv, batch, seq, heads, head_dim, scale=None, out=None, workspace=None,
+                     profile=None, stream=None):
+    """Causal attention over packed QKV rows (batch * seq rows of [Q | K | V]).
+    Returns out (batch * seq rows of heads * head_dim)."""
+    import torch
+    _cuda_f32(qkv, "qkv", 2)
+    if qkv.shape[0] != batch * seq:
+        raise ValueError("qkv must hold batch * seq rows")
+    if out is None:
+        out = torch.empty((batch * seq, heads * head_dim), dtype=torch.float32,
+                          device=qkv.device)
+    _cuda_f32(out, "out", 2)
+    if scale is None:
+        scale = 1.0 / float(head_dim) ** 0.5
+    if workspace is None:
+        workspace = torch.empty((detattention_workspace_bytes(seq, head_dim, profile) + 3) // 4,
+                                dtype=torch.float32, device=qkv.device)
+    st = load().detattention_f32(_prof(profile), batch, seq, heads, head_dim, _ptr(qkv),
+                                 _ld(qkv), ctypes.c_float(scale), _ptr(out), _ld(out),
+                                 _ptr(workspace), workspace.numel() * 4, _stream(stream))
+    _check("detattention_f32", st)
+    return out
 
 
 # ---------------------------------------------------------------- cross-entropy

@@ -27,6 +27,8 @@ SEED_CFG1, SEED_CFG2, SEED_CFG3, SEED_CFG4, SEED_CFG5 = 0, 1, 2, 3, 4
 SEED_RMS_BWD = 5   # the backward row-op inputs (their own stream)
 SEED_SHARDS = 6    # shard gradients for the fixed-order shard sum
 N_SHARDS = 64      # the 162M model card's logical shards a step
+SEED_BLOCK = 7     # one decoder block's input and weights
+N_HEADS = 12
 
 
 def uniform_pm1(rng: np.random.Generator, shape) -> np.ndarray:
@@ -159,6 +161,25 @@ def shard_grads(seed: int = SEED_SHARDS, nshards: int = N_SHARDS,
     per-shard mean gradient. One draw: an nshards x n array."""
     rng = np.random.default_rng(seed)
     return normal(rng, (nshards, n), 1e-3)
+
+
+def block_cfg(seed: int = SEED_BLOCK, batch: int = 4, seq: int = 2048, d: int = D_MODEL,
+              dff: int = D_FF):
+    """One pre-norm decoder block at the 162M shape: x (batch*seq) x d ~ N(0, 1);
+    gains 1 + N(0, 0.02); W_qkv d x 3d, W_o d x d, W_gate and W_up d x dff,
+    W_down dff x d ~ N(0, 0.02) (the model card's initialisation), K x N
+    row-major. Draw order: x, g1, W_qkv, W_o, g2, W_gate, W_up, W_down."""
+    rng = np.random.default_rng(seed)
+    x = normal(rng, (batch * seq, d))
+    g1 = np.float32(1) + normal(rng, (d,), 0.02)
+    W_qkv = normal(rng, (d, 3 * d), 0.02)
+    W_o = normal(rng, (d, d), 0.02)
+    g2 = np.float32(1) + normal(rng, (d,), 0.02)
+    W_gate = normal(rng, (d, dff), 0.02)
+    W_up = normal(rng, (d, dff), 0.02)
+    W_down = normal(rng, (dff, d), 0.02)
+    return dict(x=x, g1=g1, W_qkv=W_qkv, W_o=W_o, g2=g2, W_gate=W_gate, W_up=W_up,
+                W_down=W_down, batch=batch, seq=seq)
 
 
 ADAMW_HP = dict(lr=6e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,

@@ -329,6 +329,73 @@ det_status detexp_f32(const det_profile_v1 *prof, int64_t n, const float *x,
 det_status detlog_f32(const det_profile_v1 *prof, int64_t n, const float *x,
                       float *y, det_stream_t stream);
 
+/* ------------------------------------------------------------------ block forward
+ * The rest of a decoder block's forward ("MojoLearn 162M" model card, table
+ * "Compared with GPT-3 Small": 12 heads of 64, rotary positions with
+ * theta = 10,000, SwiGLU 2,048 wide, pre-norm residual blocks). The pages fix
+ * the profile's reduction order and transcendental spellings but print none
+ * of these; the v1 readings are stated with each call. All pointers are
+ * device pointers; calls are asynchronous on `stream`. */
+
+/* SwiGLU's gate: out[i] = (g[i] / (1 + exp(-g[i]))) * up[i], with the
+ * profile's exp, IEEE division, each operation rounded once. n floats each;
+ * out may equal gate or up and must not otherwise overlap them. */
+det_status detswiglu_f32(const det_profile_v1 *prof, int64_t n, const float *gate,
+                         const float *up, float *out, det_stream_t stream);
+
+/* Residual add: out[i] = a[i] + b[i], one rounding. out may equal a or b. */
+det_status detadd_f32(const det_profile_v1 *prof, int64_t n, const float *a,
+                      const float *b, float *out, det_stream_t stream);
+
+/* Causal softmax of attention scores, row by row: row r keeps the columns
+ * j <= (r mod period) + diag of x = scores * scale (one rounding); then the
+ * cross-entropy's spelling: m = the row max (NaN-propagating), e = exp(x - m),
+ * S = the 256-chain sum (chain l owns the 4-element groups g mod 256 == l, in
+ * ascending order) folded by the xor butterfly, p = e * (1 / S). Masked
+ * columns are +0; a row that keeps no column is +0 throughout.
+ * scores: rows x cols, lds >= cols; p: rows x cols, ldp >= cols; p may equal
+ * scores when ldp == lds (in place). period >= 1 (the rows of one square score
+ * matrix: its query index is r mod period). */
+det_status detsoftmax_causal_f32(const det_profile_v1 *prof, int64_t rows, int64_t cols,
+                                 const float *scores, int64_t lds, float scale, int64_t diag,
+                                 int64_t period, float *p, int64_t ldp, det_stream_t stream);
+
+/* Rotary position embedding, in place: row t of x holds `heads` heads of
+ * head_dim floats (row stride ldx >= heads * head_dim) at position
+ * pos = t mod seq_len. Pair (2i, 2i+1) of every head turns by
+ * a = pos * w_i, w_i = exp(-((float)(2i) / (float)head_dim) * log(theta)) with
+ * the profile's exp and log: y0 = x0 cos a - x1 sin a, y1 = x0 sin a +
+ * x1 cos a (products rounded, then the difference or sum). head_dim even. */
+det_status detrope_f32(const det_profile_v1 *prof, int64_t rows, int64_t heads,
+                       int64_t head_dim, float *x, int64_t ldx, int64_t seq_len, float theta,
+                       det_stream_t stream);
+
+/* The profile's sin and cos over n floats (v1): k = rint(x 2/pi) (ties to
+ * even); r = x - k pi/2 by three fmaf steps with pi/2 split in three floats;
+ * z = r^2; sin_r = fmaf(r, z Ps(z), r) and cos_r = fmaf(Pc(z), z, 1) with the
+ * Taylor terms to degree 9 and 10 by fmaf Horner; the quadrant k mod 4 picks
+ * the signs. sin(+-0) = +-0, cos(+-0) = 1; |x| > 2^20 and NaN give NaN. */
+det_status detsin_f32(const det_profile_v1 *prof, int64_t n, const float *x, float *y,
+                      det_stream_t stream);
+det_status detcos_f32(const det_profile_v1 *prof, int64_t n, const float *x, float *y,
+                      det_stream_t stream);
+
+/* Causal self-attention over a packed QKV activation: qkv holds batch
+ * sequences of seq rows; a row is [Q | K | V], each heads x head_dim, row stride
+ * ldqkv >= 3 heads head_dim. For every sequence and head:
+ * S = Q K^T (detgemm_f32's arithmetic), P = detsoftmax_causal_f32(S, scale,
+ * diag 0), O = P V (detgemm_f32's arithmetic), written to out (batch seq rows
+ * of heads x head_dim, row stride ldout >= heads head_dim). The heads run one
+ * after the other through a seq x seq score buffer in the workspace (at least
+ * detattention_workspace_bytes, 256-byte aligned). out must not overlap qkv
+ * or the workspace. */
+det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
+                            int64_t heads, int64_t head_dim, const float *qkv, int64_t ldqkv,
+                            float scale, float *out, int64_t ldout, void *workspace,
+                            size_t workspace_bytes, det_stream_t stream);
+det_status detattention_workspace_bytes(const det_profile_v1 *prof, int64_t seq,
+                                        int64_t head_dim, size_t *bytes);
+
 /* Reads, and optionally clears, the current device's watchdog word.
  * *code == 0 means no bounded device wait has ever given up; otherwise bit k
  * identifies the kernel family that gave up (bit 0: GEMM operand staging,

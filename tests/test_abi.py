@@ -29,7 +29,9 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("detgemm_f32", "detgemm_workspace_bytes", "detrmsnorm_f32", "detxent_f32", "detadamw_f32",
                  "detrmsnorm_bwd_f32", "detrmsnorm_bwd_workspace_bytes",
-                 "detgemm_acc_f32", "detshardsum_f32",
+                 "detgemm_acc_f32", "detshardsum_f32", "detswiglu_f32", "detadd_f32",
+                 "detsoftmax_causal_f32", "detrope_f32", "detsin_f32", "detcos_f32",
+                 "detattention_f32", "detattention_workspace_bytes",
                  "detexp_f32", "detlog_f32", "det_profile_default",
                  "det_status_string", "det_watchdog_status"):
         assert want in names
@@ -87,6 +89,9 @@ def test_unknown_profile_is_refused_by_name(lib, field, value):
                                null, 0, null) == 2
     assert lib.detshardsum_f32(ctypes.byref(p), 2, 4, null, 4, ctypes.c_float(1.0), null,
                                null) == 2
+    assert lib.detswiglu_f32(ctypes.byref(p), 4, null, null, null, null) == 2
+    assert lib.detrope_f32(ctypes.byref(p), 4, 2, 64, null, 128, 4, ctypes.c_float(1e4),
+                           null) == 2
 
 
 def test_bad_arguments_are_refused_on_the_host(lib):
@@ -139,6 +144,26 @@ def test_bad_arguments_are_refused_on_the_host(lib):
     assert ss(p, 2, 8, ctypes.c_void_p(0x1000), 8, one, ctypes.c_void_p(0x1000 + 4 * 8),
               null) == 1                                   # out over shard 1
     assert ss(p, 2, 0, null, 0, one, null, null) == 0
+    # block forward: sizes, strides, periods, head shapes, overlaps, workspace
+    d0 = ctypes.c_void_p(0x1000)
+    assert lib.detswiglu_f32(p, -1, dummy, dummy, dummy, null) == 1
+    assert lib.detswiglu_f32(p, 8, d0, dummy, ctypes.c_void_p(0x1000 + 4), null) == 1
+    assert lib.detswiglu_f32(p, 0, null, null, null, null) == 0
+    assert lib.detadd_f32(p, 8, null, dummy, dummy, null) == 1
+    sm = lib.detsoftmax_causal_f32
+    assert sm(p, 4, 0, dummy, 4, one, 0, 4, dummy, 4, null) == 1
+    assert sm(p, 4, 8, dummy, 7, one, 0, 4, dummy, 8, null) == 1
+    assert sm(p, 4, 8, dummy, 8, one, 0, 0, dummy, 8, null) == 1
+    assert sm(p, 4, 8, dummy, 8, one, 0, 4, dummy, 12, null) == 1      # p == scores, ld differ
+    rp = lib.detrope_f32
+    assert rp(p, 4, 2, 63, dummy, 200, 4, ctypes.c_float(1e4), null) == 1   # odd head_dim
+    assert rp(p, 4, 2, 64, dummy, 127, 4, ctypes.c_float(1e4), null) == 1   # ld < heads*d
+    assert rp(p, 4, 2, 64, dummy, 128, 0, ctypes.c_float(1e4), null) == 1   # seq_len 0
+    assert lib.detsin_f32(p, -1, dummy, dummy, null) == 1
+    at = lib.detattention_f32
+    assert at(p, 1, 16, 2, 8, dummy, 47, one, dummy, 16, dummy, 1 << 20, null) == 1
+    assert at(p, 1, 16, 2, 8, dummy, 48, one, dummy, 15, dummy, 1 << 20, null) == 1
+    assert at(p, 0, 16, 2, 8, null, 48, one, null, 16, null, 0, null) == 0
     hp = detlib.AdamWHP(1e-3, 0.9, 0.95, 1e-8, 0.1, 0)
     assert lib.detadamw_f32(p, 4, dummy, dummy, dummy, dummy, ctypes.byref(hp), null) == 1
     assert lib.detexp_f32(p, -1, dummy, dummy, null) == 1
