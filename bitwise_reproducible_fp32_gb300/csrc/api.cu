@@ -219,6 +219,21 @@ DET_API det_status detrope_f32(const det_profile_v1 *prof, int64_t rows, int64_t
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+DET_API det_status detembedding_f32(const det_profile_v1 *prof, int64_t ntok, int64_t dim,
+                                    const float *table, int64_t ldt, int64_t vocab,
+                                    const int32_t *tokens, float *out, int64_t ldo,
+                                    int32_t *dev_status, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (ntok < 0 || dim < 1 || dim > kDimMax || vocab < 1 || vocab > kDimMax)
+        return DET_ERR_INVALID_ARG;
+    if (ntok == 0) return DET_OK;
+    if (!table || !tokens || !out || ldt < dim || ldo < dim) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_embedding(ntok, dim, table, ldt, vocab, tokens, out, ldo, dev_status,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 DET_API det_status detsin_f32(const det_profile_v1 *prof, int64_t n, const float *x, float *y,
                               det_stream_t stream) {
     det_status st = check_profile(prof);

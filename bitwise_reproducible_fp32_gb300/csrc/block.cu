@@ -172,6 +172,25 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Embedding rows: out[t] = table[token[t]] (copies, exact). A token outside
+// [0, vocab) writes a NaN row and sets the caller's status word.
+__global__ void __launch_bounds__(256)
+    embedding_kernel(int64_t ntok, int64_t dim, const float *table, int64_t ldt, int64_t vocab,
+                     const int32_t *tokens, float *out, int64_t ldo, int32_t *status) {
+    const int64_t total = ntok * dim;
+    for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = e / dim, j = e - t * dim;
+        const int64_t id = tokens[t];
+        if (id < 0 || id >= vocab) {
+            out[t * ldo + j] = __uint_as_float(0x7fc00000u);
+            if (status && j == 0) atomicOr(reinterpret_cast<int *>(status), 1);
+        } else {
+            out[t * ldo + j] = table[id * ldt + j];
+        }
+    }
+}
+
 __global__ void sincos_map_kernel(int64_t n, const float *x, float *y, int want_cos) {
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
          i += int64_t(gridDim.x) * blockDim.x) {
@@ -219,6 +238,16 @@ cudaError_t launch_rope(int64_t rows, int heads, int head_dim, float *x, int64_t
     if (rows == 0) return cudaSuccess;
     rope_kernel<<<unsigned(ew_blocks(rows * (head_dim / 2))), 256, 0, s>>>(
         rows, heads, head_dim, x, ldx, seq_len, theta);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_embedding(int64_t ntok, int64_t dim, const float *table, int64_t ldt,
+                             int64_t vocab, const int32_t *tokens, float *out, int64_t ldo,
+                             int32_t *status, cudaStream_t s) {
+    if (ntok == 0) return cudaSuccess;
+    embedding_kernel<<<unsigned(ew_blocks(ntok * dim)), 256, 0, s>>>(ntok, dim, table, ldt,
+                                                                     vocab, tokens, out, ldo,
+                                                                     status);
     return cudaGetLastError();
 }
 

@@ -78,6 +78,9 @@ cudaError_t launch_softmax_causal(int64_t rows, int64_t cols, const float *sc, i
                                   int64_t ldp, cudaStream_t s);
 cudaError_t launch_rope(int64_t rows, int heads, int head_dim, float *x, int64_t ldx,
                         int64_t seq_len, float theta, cudaStream_t s);
+cudaError_t launch_embedding(int64_t ntok, int64_t dim, const float *table, int64_t ldt,
+                             int64_t vocab, const int32_t *tokens, float *out, int64_t ldo,
+                             int32_t *status, cudaStream_t s);
 cudaError_t launch_sincos_map(int64_t n, const float *x, float *y, int want_cos,
                               cudaStream_t s);
 cudaError_t launch_shardsum(int64_t nshards, int64_t n, const float *shards, int64_t ld,

@@ -76,6 +76,7 @@ SIGNATURES = [
     ("detsoftmax_causal_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _f, _i64, _i64, _vp, _i64,
                                      _vp]),
     ("detrope_f32", _int, [_PROF, _i64, _i64, _i64, _vp, _i64, _i64, _f, _vp]),
+    ("detembedding_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp]),
     ("detsin_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
     ("detcos_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
     ("detattention_f32", _int, [_PROF, _i64, _i64, _i64, _i64, _vp, _i64, _f, _vp, _i64, _vp,
@@ -385,6 +386,24 @@ def detrope_f32(x, heads, head_dim, seq_len, theta=10000.0, profile=None, stream
                             seq_len, ctypes.c_float(theta), _stream(stream))
     _check("detrope_f32", st)
     return x
+
+
+def detembedding_f32(table, tokens, out=None, dev_status=None, profile=None, stream=None):
+    """Rows of table (vocab x dim) picked by the int32 tokens. Returns out."""
+    import torch
+    _cuda_f32(table, "table", 2)
+    if tokens.dtype != torch.int32 or tokens.device.type != "cuda" or not tokens.is_contiguous():
+        raise TypeError("tokens must be a contiguous int32 CUDA tensor")
+    vocab, dim = table.shape
+    n = tokens.numel()
+    if out is None:
+        out = torch.empty((n, dim), dtype=torch.float32, device=table.device)
+    _cuda_f32(out, "out", 2)
+    st = load().detembedding_f32(_prof(profile), n, dim, _ptr(table), _ld(table), vocab,
+                                 _ptr(tokens), _ptr(out), _ld(out), _ptr(dev_status),
+                                 _stream(stream))
+    _check("detembedding_f32", st)
+    return out
 
 
 def detsin_f32(x, y=None, profile=None, stream=None):

@@ -182,6 +182,34 @@ def block_cfg(seed: int = SEED_BLOCK, batch: int = 4, seq: int = 2048, d: int = 
                 W_down=W_down, batch=batch, seq=seq)
 
 
+def byte_lm_cfg2(seed: int = SEED_CFG2 + 100, batch: int = 16, seq: int = 128, d: int = 64,
+                 dff: int = 172, vocab: int = 256, blocks: int = 2):
+    """The small byte-level language model at the byte-LM GEMM shapes (16 x 128
+    tokens, 64 wide, SwiGLU 172, 256 byte ids, two blocks): byte tokens uniform in
+    [0, 256) for 129 positions a sequence (inputs: the first 128, labels: the
+    last 128); embedding and LM head (the head stored [vocab, d]) N(0, 0.02);
+    per block g1, W_qkv, W_o, g2, W_gate, W_up, W_down as block_cfg draws them.
+    Draw order: tokens, embedding, each block's weights, the head."""
+    rng = np.random.default_rng(seed)
+    toks = rng.integers(0, vocab, size=(batch, seq + 1), dtype=np.int32)
+    emb = normal(rng, (vocab, d), 0.02)
+    blks = []
+    for _ in range(blocks):
+        g1 = np.float32(1) + normal(rng, (d,), 0.02)
+        W_qkv = normal(rng, (d, 3 * d), 0.02)
+        W_o = normal(rng, (d, d), 0.02)
+        g2 = np.float32(1) + normal(rng, (d,), 0.02)
+        W_gate = normal(rng, (d, dff), 0.02)
+        W_up = normal(rng, (d, dff), 0.02)
+        W_down = normal(rng, (dff, d), 0.02)
+        blks.append(dict(g1=g1, W_qkv=W_qkv, W_o=W_o, g2=g2, W_gate=W_gate, W_up=W_up,
+                         W_down=W_down))
+    head = normal(rng, (vocab, d), 0.02)
+    return dict(tokens=np.ascontiguousarray(toks[:, :seq]).reshape(-1),
+                labels=np.ascontiguousarray(toks[:, 1:]).reshape(-1), emb=emb, blocks=blks,
+                head=head, batch=batch, seq=seq, d=d, dff=dff, vocab=vocab, heads=4)
+
+
 ADAMW_HP = dict(lr=6e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
                 step=251)
 

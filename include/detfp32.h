@@ -370,6 +370,15 @@ det_status detrope_f32(const det_profile_v1 *prof, int64_t rows, int64_t heads,
                        int64_t head_dim, float *x, int64_t ldx, int64_t seq_len, float theta,
                        det_stream_t stream);
 
+/* Token embedding: out[t] = table[tokens[t]] for t < ntok (rows of dim
+ * floats; table is vocab x dim with row stride ldt, out has row stride ldo).
+ * A copy, so exact. A token outside [0, vocab) writes a NaN row and ORs 1
+ * into *dev_status (device int32, may be NULL). */
+det_status detembedding_f32(const det_profile_v1 *prof, int64_t ntok, int64_t dim,
+                            const float *table, int64_t ldt, int64_t vocab,
+                            const int32_t *tokens, float *out, int64_t ldo,
+                            int32_t *dev_status, det_stream_t stream);
+
 /* The profile's sin and cos over n floats (v1): k = rint(x 2/pi) (ties to
  * even); r = x - k pi/2 by three fmaf steps with pi/2 split in three floats;
  * z = r^2; sin_r = fmaf(r, z Ps(z), r) and cos_r = fmaf(Pc(z), z, 1) with the

@@ -48,6 +48,10 @@ def cards():
     out["cfg5_small/adamw_p"] = card(pp)
     out["cfg5_small/adamw_m"] = card(mm)
     out["cfg5_small/adamw_v"] = card(vv)
+    # the byte-level LM forward at the byte-LM GEMM shapes, stage by stage
+    import oracle_models
+    for name, v in oracle_models.byte_lm_forward(inputs.byte_lm_cfg2()).items():
+        out[f"byte_lm/{name}"] = card(v)
     return out
 
 

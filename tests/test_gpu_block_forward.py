@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 
 import oracle
+import oracle_models
 from bitcmp import assert_bitwise
 from bitwise_reproducible_fp32_gb300 import block, inputs
 from gpu_util import host, need_gpu, to_dev, torch
@@ -20,28 +21,7 @@ def dev():
 
 
 def oracle_block(c, heads):
-    x = c["x"]
-    B, T = c["batch"], c["seq"]
-    D = x.shape[1]
-    hd = D // heads
-    h, _ = oracle.rmsnorm(x, c["g1"], eps=1e-6)
-    qkv = oracle.gemm(h, c["W_qkv"])
-    qk = oracle.rope(qkv[:, :2 * D], 2 * heads, hd, seq_len=T)
-    qkv = np.concatenate([qk, qkv[:, 2 * D:]], axis=1)
-    att = np.empty((B * T, D), F)
-    for b in range(B):
-        r = slice(b * T, (b + 1) * T)
-        for hh in range(heads):
-            Q = qkv[r, hh * hd:(hh + 1) * hd]
-            K = qkv[r, D + hh * hd:D + (hh + 1) * hd]
-            V = qkv[r, 2 * D + hh * hd:2 * D + (hh + 1) * hd]
-            P = oracle.softmax_causal(oracle.gemm(Q, K, transB=True),
-                                      scale=float(F(1.0 / np.sqrt(hd))))
-            att[r, hh * hd:(hh + 1) * hd] = oracle.gemm(P, V)
-    x1 = oracle.add(x, oracle.gemm(att, c["W_o"]))
-    h2, _ = oracle.rmsnorm(x1, c["g2"], eps=1e-6)
-    s = oracle.swiglu(oracle.gemm(h2, c["W_gate"]), oracle.gemm(h2, c["W_up"]))
-    return oracle.add(x1, oracle.gemm(s, c["W_down"]))
+    return oracle_models.block(c["x"], c, c["batch"], c["seq"], heads)
 
 
 def run(c, heads, dff):
