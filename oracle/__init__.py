@@ -91,6 +91,11 @@ def _load():
         lib.detor_sincos_ulp_scan.argtypes = [c_int, ctypes.c_uint32, ctypes.c_uint32,
                                               ctypes.c_uint32, c_int,
                                               ctypes.POINTER(ctypes.c_uint32)]
+        lib.detor_swiglu_bwd.argtypes = [i64, f32p, f32p, f32p, f32p, f32p, c_int]
+        lib.detor_softmax_causal_bwd.argtypes = [i64, i64, f32p, f32p, i64, ctypes.c_float,
+                                                 i64, f32p, c_int, c_int, c_int]
+        lib.detor_rope_bwd.argtypes = [i64, i64, i64, f32p, i64, i64, ctypes.c_float, c_int]
+        lib.detor_embedding_bwd.argtypes = [i64, i64, i32p, f32p, i64, f32p, c_int]
         lib.detor_swiglu.argtypes = [i64, f32p, f32p, f32p, c_int]
         lib.detor_add.argtypes = [i64, f32p, f32p, f32p, c_int]
         lib.detor_softmax_causal.argtypes = [i64, i64, f32p, i64, ctypes.c_float, i64, f32p,
@@ -250,6 +255,48 @@ def swiglu(gate, up, nthreads=None):
     out = np.empty_like(g)
     _load().detor_swiglu(g.size, _fp(g), _fp(u), _fp(out), _threads(nthreads))
     return out
+
+
+def swiglu_bwd(gate, up, dh, nthreads=None):
+    """(d_gate, d_up) of h = (g / (1 + exp(-g))) * u under the profile."""
+    g = np.ascontiguousarray(_f32(gate))
+    u = np.ascontiguousarray(_f32(up))
+    d = np.ascontiguousarray(_f32(dh))
+    dg, du = np.empty_like(g), np.empty_like(g)
+    _load().detor_swiglu_bwd(g.size, _fp(g), _fp(u), _fp(d), _fp(dg), _fp(du),
+                             _threads(nthreads))
+    return dg, du
+
+
+def softmax_causal_bwd(p, dp, scale=1.0, diag=0, lanes=XENT_LANES, group=LANE_GROUP,
+                       nthreads=None):
+    """dS from P and dP (row r keeps columns j <= r + diag)."""
+    p = np.ascontiguousarray(_f32(p))
+    dp = np.ascontiguousarray(_f32(dp))
+    rows, cols = p.shape
+    ds = np.empty_like(p)
+    _load().detor_softmax_causal_bwd(rows, cols, _fp(p), _fp(dp), cols, np.float32(scale),
+                                     int(diag), _fp(ds), lanes, group, _threads(nthreads))
+    return ds
+
+
+def rope_bwd(dy, heads, head_dim, seq_len, theta=10000.0, nthreads=None):
+    """The rotary embedding's backward: each pair turned by -a. A new array."""
+    out = np.array(_f32(dy), dtype=np.float32, order="C", copy=True)
+    _load().detor_rope_bwd(out.shape[0], heads, head_dim, _fp(out), out.shape[1], seq_len,
+                           np.float32(theta), _threads(nthreads))
+    return out
+
+
+def embedding_bwd(tokens, dx, vocab, nthreads=None):
+    """dE: per id, the left-to-right sum of its tokens' gradient rows."""
+    t = np.ascontiguousarray(np.asarray(tokens, np.int32))
+    d = np.ascontiguousarray(_f32(dx))
+    de = np.empty((vocab, d.shape[1]), np.float32)
+    _load().detor_embedding_bwd(t.size, d.shape[1],
+                                t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _fp(d),
+                                vocab, _fp(de), _threads(nthreads))
+    return de
 
 
 def add(a, b, nthreads=None):

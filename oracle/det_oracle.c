@@ -351,6 +351,7 @@ typedef struct {
     int64_t heads, d, ldx, seq;
     float *x;
     float theta;
+    int backward;
 } rope_ctx;
 
 static void rope_rows(int64_t lo, int64_t hi, int tix, void *c) {
@@ -368,8 +369,13 @@ static void rope_rows(int64_t lo, int64_t hi, int tix, void *c) {
             for (int64_t h = 0; h < q->heads; ++h) {
                 float *p = q->x + t * q->ldx + h * q->d + 2 * i;
                 const float x0 = p[0], x1 = p[1];
-                p[0] = x0 * cs - x1 * sn;
-                p[1] = x0 * sn + x1 * cs;
+                if (!q->backward) {
+                    p[0] = x0 * cs - x1 * sn;
+                    p[1] = x0 * sn + x1 * cs;
+                } else {          /* the transpose: turn by -a (R35) */
+                    p[0] = x0 * cs + x1 * sn;
+                    p[1] = x1 * cs - x0 * sn;
+                }
             }
         }
     }
@@ -378,8 +384,49 @@ static void rope_rows(int64_t lo, int64_t hi, int tix, void *c) {
 void detor_rope(int64_t rows, int64_t heads, int64_t head_dim, float *x, int64_t ldx,
                 int64_t seq_len, float theta, int nthreads) {
     if (head_dim < 2 || head_dim % 2 || seq_len < 1 || heads < 1) return;
-    rope_ctx c = {heads, head_dim, ldx, seq_len, x, theta};
+    rope_ctx c = {heads, head_dim, ldx, seq_len, x, theta, 0};
     parallel_for(rows, nthreads, rope_rows, &c);
+}
+
+/* Rotary backward (design notes R35): the forward's angles; the gradient pair
+ * turns by -a: dx0 = dy0 * c + dy1 * s, dx1 = dy1 * c - dy0 * s. */
+void detor_rope_bwd(int64_t rows, int64_t heads, int64_t head_dim, float *x, int64_t ldx,
+                    int64_t seq_len, float theta, int nthreads) {
+    if (head_dim < 2 || head_dim % 2 || seq_len < 1 || heads < 1) return;
+    rope_ctx c = {heads, head_dim, ldx, seq_len, x, theta, 1};
+    parallel_for(rows, nthreads, rope_rows, &c);
+}
+
+/* Embedding backward (design notes R36): per id v and column j, the tokens'
+ * gradients in ascending token order, the first as is, then left to right. */
+typedef struct {
+    int64_t ntok, dim;
+    const int32_t *tok;
+    const float *dx;
+    float *de;
+} embb_ctx;
+
+static void embb_range(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    embb_ctx *q = (embb_ctx *)c;
+    for (int64_t v = lo; v < hi; ++v) {
+        for (int64_t j = 0; j < q->dim; ++j) {
+            float t = 0.0f;
+            int first = 1;
+            for (int64_t k = 0; k < q->ntok; ++k) {
+                if (q->tok[k] != v) continue;
+                t = first ? q->dx[k * q->dim + j] : t + q->dx[k * q->dim + j];
+                first = 0;
+            }
+            q->de[v * q->dim + j] = t;
+        }
+    }
+}
+
+void detor_embedding_bwd(int64_t ntok, int64_t dim, const int32_t *tokens, const float *dx,
+                         int64_t vocab, float *de, int nthreads) {
+    embb_ctx c = {ntok, dim, tokens, dx, de};
+    parallel_for(vocab, nthreads, embb_range, &c);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -415,6 +462,36 @@ static void add_range(int64_t lo, int64_t hi, int tix, void *c) {
 void detor_swiglu(int64_t n, const float *gate, const float *up, float *out, int nthreads) {
     ew_ctx c = {gate, up, out};
     parallel_for(n, nthreads, swiglu_range, &c);
+}
+
+/* SwiGLU backward (design notes R33): with e = exp(-g), den = 1 + e,
+ * silu = g / den (the forward's value) and sig = 1 / den,
+ *   d_up   = dh * silu
+ *   d_gate = (dh * u) * (sig * (1 + g * (1 - sig)))
+ * every operation rounded once, in that order. */
+typedef struct {
+    const float *g, *u, *dh;
+    float *dg, *du;
+} swb_ctx;
+
+static void swiglu_bwd_range(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    swb_ctx *q = (swb_ctx *)c;
+    for (int64_t i = lo; i < hi; ++i) {
+        float g = q->g[i];
+        float den = 1.0f + detor_exp(-g);
+        float silu = g / den;
+        float sig = 1.0f / den;
+        float ds = sig * (1.0f + g * (1.0f - sig));
+        q->du[i] = q->dh[i] * silu;
+        q->dg[i] = (q->dh[i] * q->u[i]) * ds;
+    }
+}
+
+void detor_swiglu_bwd(int64_t n, const float *gate, const float *up, const float *dh,
+                      float *d_gate, float *d_up, int nthreads) {
+    swb_ctx c = {gate, up, dh, d_gate, d_up};
+    parallel_for(n, nthreads, swiglu_bwd_range, &c);
 }
 
 void detor_add(int64_t n, const float *a, const float *b, float *out, int nthreads) {
@@ -692,6 +769,48 @@ static void smax_rows(int64_t lo, int64_t hi, int tix, void *c) {
         float inv = 1.0f / butterfly(acc, q->lanes);
         for (int64_t j = 0; j < nr; ++j) p[j] = detor_exp(s[j] * q->scale - m) * inv;
     }
+}
+
+/* Causal softmax backward (design notes R34): per row, over the kept columns
+ * j < n_r, dot = the lanes-chain sum of fmaf(dP_j, P_j, .) (lane l owning
+ * groups g mod lanes == l, ascending, from +0) folded by the butterfly; then
+ * dS_j = (P_j * (dP_j - dot)) * scale; masked columns +0. */
+typedef struct {
+    int64_t cols, ld, diag;
+    const float *p, *dp;
+    float scale;
+    float *ds;
+    int lanes, group;
+} smaxb_ctx;
+
+static void smaxb_rows(int64_t lo, int64_t hi, int tix, void *c) {
+    (void)tix;
+    smaxb_ctx *q = (smaxb_ctx *)c;
+    float acc[1024];
+    for (int64_t r = lo; r < hi; ++r) {
+        const float *p = q->p + r * q->ld, *dp = q->dp + r * q->ld;
+        float *ds = q->ds + r * q->ld;
+        int64_t nr = r + q->diag + 1;
+        if (nr > q->cols) nr = q->cols;
+        if (nr < 0) nr = 0;
+        for (int64_t j = nr; j < q->cols; ++j) ds[j] = 0.0f;
+        if (nr == 0) continue;
+        for (int l = 0; l < q->lanes; ++l) acc[l] = 0.0f;
+        for (int64_t j = 0; j < nr; ++j) {
+            int l = (int)((j / q->group) % q->lanes);
+            acc[l] = fmaf(dp[j], p[j], acc[l]);
+        }
+        float dot = butterfly(acc, q->lanes);
+        for (int64_t j = 0; j < nr; ++j) ds[j] = (p[j] * (dp[j] - dot)) * q->scale;
+    }
+}
+
+void detor_softmax_causal_bwd(int64_t rows, int64_t cols, const float *p, const float *dp,
+                              int64_t ld, float scale, int64_t diag, float *ds, int lanes,
+                              int group, int nthreads) {
+    if (lanes < 1 || lanes > 1024 || group < 1 || cols < 1) return;
+    smaxb_ctx c = {cols, ld, diag, p, dp, scale, ds, lanes, group};
+    parallel_for(rows, nthreads, smaxb_rows, &c);
 }
 
 void detor_softmax_causal(int64_t rows, int64_t cols, const float *s, int64_t lds,

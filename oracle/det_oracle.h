@@ -88,6 +88,26 @@ double detor_sincos_ulp_scan(int which, uint32_t lo, uint32_t hi, uint32_t step,
 /* SwiGLU's gate: out = (g / (1 + exp(-g))) * u element-wise (det_oracle.c). */
 void detor_swiglu(int64_t n, const float *gate, const float *up, float *out, int nthreads);
 
+/* SwiGLU backward (det_oracle.c): d_gate and d_up from gate, up and the
+ * upstream gradient dh. */
+void detor_swiglu_bwd(int64_t n, const float *gate, const float *up, const float *dh,
+                      float *d_gate, float *d_up, int nthreads);
+
+/* Causal softmax backward: dS from the probabilities P and dP, row r keeping
+ * the columns j <= r + diag; masked columns +0. */
+void detor_softmax_causal_bwd(int64_t rows, int64_t cols, const float *p, const float *dp,
+                              int64_t ld, float scale, int64_t diag, float *ds, int lanes,
+                              int group, int nthreads);
+
+/* Rotary embedding backward in place: the pairs turned by -a. */
+void detor_rope_bwd(int64_t rows, int64_t heads, int64_t head_dim, float *x, int64_t ldx,
+                    int64_t seq_len, float theta, int nthreads);
+
+/* Embedding backward: dE[v] = the left-to-right sum of dX[t] over the tokens
+ * t (ascending) with tokens[t] == v; +0 for ids no token uses. */
+void detor_embedding_bwd(int64_t ntok, int64_t dim, const int32_t *tokens, const float *dx,
+                         int64_t vocab, float *de, int nthreads);
+
 /* Residual add: out = a + b element-wise, one rounding. */
 void detor_add(int64_t n, const float *a, const float *b, float *out, int nthreads);
 
