@@ -12,6 +12,8 @@ One step = one pass of every operation of the path over one batch of the
   fixed-order sum of 64 gathered shard gradients of the 768x2304 weight ->
   one pre-norm decoder block forward (RMSNorm, QKV, RoPE, causal attention,
   out projection, residual, RMSNorm, SwiGLU, down projection, residual) ->
+  one training step of the byte-level LM (16 x 128 tokens, two blocks of 64:
+  forward, backward, AdamW) ->
   AdamW over 162,147,840 parameters.
 Inputs are synthetic and seeded (bitwise_reproducible_fp32_gb300.inputs).
 
@@ -49,7 +51,8 @@ WORKLOAD = ("162M-decoder FP32 step: RMSNorm 8192x768, forward GEMMs "
             "RMSNorm backward 8192x768 (dx, dgain), dW GEMMs over 8192 tokens "
             "(768x2304, 2048x768), fixed-order sum of 64 shard gradients of the "
             "768x2304 weight, one decoder block forward (4x2048 tokens, RoPE, causal "
-            "attention 12x64, SwiGLU), AdamW 162,147,840 params")
+            "attention 12x64, SwiGLU), one byte-level LM training step (16x128 tokens, "
+            "2 blocks of 64), AdamW 162,147,840 params")
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
 
@@ -194,6 +197,7 @@ def run_ours(args, rank, world, local_rank):
     rb = inputs.rmsnorm_bwd_cfg4()
     sg = inputs.shard_grads()
     bc = inputs.block_cfg()
+    bl = inputs.byte_lm_cfg2()
     aw = inputs.adamw_cfg5()
     host = dict(fwd=fwd, dw=dw, r4=r4, rb=rb, sg=sg, bc=bc, aw=aw)
 
@@ -238,6 +242,12 @@ def run_ours(args, rank, world, local_rank):
                          inputs.N_HEADS, dev)
     bx = up(bc["x"])
     bw = {k: up(bc[k]) for k in ("g1", "W_qkv", "W_o", "g2", "W_gate", "W_up", "W_down")}
+    from bitwise_reproducible_fp32_gb300 import byte_lm
+    bld = dict(bl)
+    bld["tokens"] = torch.from_numpy(bl["tokens"]).to(dev)
+    bld["labels"] = torch.from_numpy(bl["labels"]).to(dev)
+    bld["emb"], bld["head"] = up(bl["emb"]), up(bl["head"])
+    bld["blocks"] = [{k: up(v) for k, v in b.items()} for b in bl["blocks"]]
     P, G, Mm, Vv = (up(aw[k]) for k in ("p", "g", "m", "v"))
     hp = {k: aw[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")}
     # L2 flush: write 512 MB, then read another 512 MB so the L2 holds clean
@@ -264,11 +274,22 @@ def run_ours(args, rank, world, local_rank):
     pv_split = detlib.detgemm_workspace_bytes(bc["seq"], 64, bc["seq"]) > 0
     block_launches = (2 + 5 + sum(v is not None for v in blk.ws.values()) + 1
                       + n_heads_total * (3 + int(pv_split)) + 2 + 1)
+    # the byte-level LM step: the embedding, 2 forward blocks (11 launches and
+    # 3 a head), the head GEMM, the cross-entropy and its mean, the head's two
+    # backward GEMMs, 2 backward blocks (18 launches and 7 a head, plus split
+    # passes), the embedding backward, and one AdamW launch per parameter
+    # tensor (2 + 7 a block); checked against an ncu launch list of one step
+    nb, nh = len(bl["blocks"]), bl["batch"] * bl["heads"]
+    hd_b = bl["d"] // bl["heads"]
+    pv_b = int(detlib.detgemm_workspace_bytes(bl["seq"], hd_b, bl["seq"]) > 0)
+    byte_lm_launches = (1 + nb * (11 + nh * (3 + pv_b)) + 1 + 2 + 2
+                        + nb * (18 + nh * (7 + 3 * pv_b)) + 1 + 2 + 7 * nb)
     launches_per_step = (1 + len(fwd) + sum(w is not None for w in ws_fwd) + 2 + 2 + len(dw)
-                         + sum(w is not None for w in ws_dw) + 1 + block_launches + 1)
+                         + sum(w is not None for w in ws_dw) + 1 + block_launches
+                         + byte_lm_launches + 1)
 
     segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "rmsnorm_bwd", "gemm_dw",
-            "shard_sum", "block_fwd", "adamw"]
+            "shard_sum", "block_fwd", "byte_lm_step", "adamw"]
 
     def step(ev=None):
         def mark(i):
@@ -300,8 +321,10 @@ def run_ours(args, rank, world, local_rank):
         mark(7)
         blk.forward(bx, bw)
         mark(8)
-        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
+        byte_lm.train_step(bld, dev, inputs.BYTE_LM_HP)
         mark(9)
+        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
+        mark(10)
 
     import torch.distributed as dist
     distributed = world > 1
@@ -382,6 +405,8 @@ def run_ours(args, rank, world, local_rank):
             "block_fwd": {"tflops": blk.flops() / per("block_fwd") / 1e12,
                           "frac_fp32_peak": blk.flops() / per("block_fwd") / 1e12 / fma_peak,
                           "ms": per("block_fwd") * 1e3},
+            "byte_lm_step": {"ms": per("byte_lm_step") * 1e3,
+                             "tokens_per_s": bl["batch"] * bl["seq"] / per("byte_lm_step")},
             "shard_sum": {"gbs": bytes_shardsum(*sg.shape) / per("shard_sum") / 1e9,
                           "frac_hbm": bytes_shardsum(*sg.shape) / per("shard_sum") / 1e9 / hbm,
                           "ms": per("shard_sum") * 1e3},

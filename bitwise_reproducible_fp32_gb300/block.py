@@ -32,7 +32,7 @@ class Block:
         self.h, self.inv1 = e(n, d_model), e(n)
         self.qkv, self.att, self.o = e(n, 3 * d_model), e(n, d_model), e(n, d_model)
         self.x1, self.h2, self.inv2 = e(n, d_model), e(n, d_model), e(n)
-        self.gate, self.up, self.dn = e(n, d_ff), e(n, d_ff), e(n, d_model)
+        self.gate, self.up, self.s, self.dn = e(n, d_ff), e(n, d_ff), e(n, d_ff), e(n, d_model)
         self.y = e(n, d_model)
         ws = lambda M, N, K: detlib.gemm_workspace(M, N, K, False, False, device=device)  # noqa: E731
         self.ws = {"qkv": ws(n, 3 * d_model, d_model), "o": ws(n, d_model, d_model),
@@ -60,7 +60,44 @@ class Block:
         L.detrmsnorm_f32(self.x1, w["g2"], self.eps, y=self.h2, inv_rms=self.inv2)
         L.detgemm_f32(self.h2, w["W_gate"], self.gate, workspace=self.ws["ff"])
         L.detgemm_f32(self.h2, w["W_up"], self.up, workspace=self.ws["ff"])
-        L.detswiglu_f32(self.gate, self.up, out=self.gate)
-        L.detgemm_f32(self.gate, w["W_down"], self.dn, workspace=self.ws["down"])
+        L.detswiglu_f32(self.gate, self.up, out=self.s)
+        L.detgemm_f32(self.s, w["W_down"], self.dn, workspace=self.ws["down"])
         L.detadd_f32(self.x1, self.dn, out=self.y)
         return self.y
+
+    def backward(self, x, w, dy):
+        """Gradients of the block's forward from dy (the gradient of its
+        output), with the activations this object kept. Returns (dx, grads)
+        with grads named as the weights (g1, W_qkv, W_o, g2, W_gate, W_up,
+        W_down). Readings: a residual's gradient first in every sum of
+        gradients; the gate's contribution to dh2 first, then up's (as the
+        forward used them)."""
+        import torch
+
+        from bitwise_reproducible_fp32_gb300 import detlib as L
+        n, D, Fd = self.B * self.T, self.D, self.Fd
+        e = lambda *s: torch.empty(s, dtype=torch.float32, device=dy.device)  # noqa: E731
+        g = {}
+        tA = lambda A, B, C=None: L.detgemm_f32(A, B, C, transA=True)          # noqa: E731
+        tB = lambda A, B, C=None: L.detgemm_f32(A, B, C, transB=True)          # noqa: E731
+        # y = x1 + s W_down
+        ds = tB(dy, w["W_down"])
+        g["W_down"] = tA(self.s, dy)
+        d_gate, d_up = L.detswiglu_bwd_f32(self.gate, self.up, ds)
+        dh2 = tB(d_gate, w["W_gate"])
+        L.detgemm_acc_f32(d_up, w["W_up"], dh2, transB=True)
+        g["W_gate"] = tA(self.h2, d_gate)
+        g["W_up"] = tA(self.h2, d_up)
+        dx1_b, g["g2"] = L.detrmsnorm_bwd_f32(self.x1, w["g2"], self.inv2, dh2)
+        dx1 = L.detadd_f32(dy, dx1_b)
+        # x1 = x + att W_o
+        d_att = tB(dx1, w["W_o"])
+        g["W_o"] = tA(self.att, dx1)
+        dqkv = L.detattention_bwd_f32(self.qkv, d_att, self.B, self.T, self.H, self.hd)
+        L.detrope_bwd_f32(dqkv, heads=2 * self.H, head_dim=self.hd, seq_len=self.T,
+                          theta=self.theta)
+        dh = tB(dqkv, w["W_qkv"])
+        g["W_qkv"] = tA(self.h, dqkv)
+        dx_b, g["g1"] = L.detrmsnorm_bwd_f32(x, w["g1"], self.inv1, dh)
+        dx = L.detadd_f32(dx1, dx_b)
+        return dx, g

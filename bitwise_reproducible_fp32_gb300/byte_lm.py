@@ -1,37 +1,89 @@
-"""Forward and loss of the small byte-level language model (the pages' "two
-transformer blocks, byte level"; "mojolearn" PyPI page, section "Handing
-training off between vendors"), at the byte-LM GEMM shapes: 16 x 128 tokens,
-64 wide, 4 heads of 16, SwiGLU 172, 256 byte ids. Pre-norm blocks, no final
-norm, an untied LM head stored [vocab, d] (the 162M model card's layout).
-Every stage is a C-ABI call; `stages` names each stage's output so identity
-cards (raw-bit hashes per stage) can be compared with the oracle's.
+"""Forward, backward and AdamW update of the small byte-level language model
+(the pages' "two transformer blocks, byte level", trained with "embedding,
+transformer forward and backward, cross entropy, and AdamW"; "mojolearn" PyPI
+page, section "Handing training off between vendors"), at the byte-LM GEMM
+shapes: 16 x 128 tokens, 64 wide, 4 heads of 16, SwiGLU 172, 256 byte ids.
+Pre-norm blocks, no final norm, an untied LM head stored [vocab, d].
+
+Every stage is a C-ABI call; the returned stage dict names each stage's output
+so identity cards (raw-bit hashes per stage) can be compared with the
+oracle's.
 """
 from __future__ import annotations
 
+PARAMS = ("g1", "W_qkv", "W_o", "g2", "W_gate", "W_up", "W_down")
 
-def forward(cfg_dev, device):
-    """cfg_dev: the byte_lm_cfg2 tensors on the device (tokens, labels int32;
-    emb, head and each block's weights float32). Returns the ordered stage
-    dict: embedding, block0, block1, ..., logits, loss, loss_mean."""
+
+def train_step(c, device, hp):
+    """One training step. c: the byte_lm_cfg2 tensors on the device; hp: AdamW
+    hyperparameters (lr, beta1, beta2, eps, weight_decay, step). The moments
+    start at zero. Returns the ordered stage dict: the forward's outputs, the
+    gradients, then every parameter and moment after the update."""
     import torch
 
-    from bitwise_reproducible_fp32_gb300 import block, detlib
-    B, T, d = cfg_dev["batch"], cfg_dev["seq"], cfg_dev["d"]
+    from bitwise_reproducible_fp32_gb300 import block, detlib as L
+    B, T, d = c["batch"], c["seq"], c["d"]
+    ntok = B * T
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    stages = {}
-    x = detlib.detembedding_f32(cfg_dev["emb"], cfg_dev["tokens"], dev_status=status)
-    stages["embedding"] = x
-    blocks = [block.Block(B, T, d, cfg_dev["dff"], cfg_dev["heads"], device)
-              for _ in cfg_dev["blocks"]]
-    for i, (blk, w) in enumerate(zip(blocks, cfg_dev["blocks"])):
-        x = blk.forward(x, w)          # each block owns its output buffer
-        stages[f"block{i}"] = x
-    logits = detlib.detgemm_f32(x, cfg_dev["head"], transB=True)
-    stages["logits"] = logits
-    loss, mean, _ = detlib.detxent_f32(logits, cfg_dev["labels"], want_mean=True,
-                                       dev_status=status)
-    stages["loss"] = loss
-    stages["loss_mean"] = mean
+    st = {}
+    # forward
+    x0 = L.detembedding_f32(c["emb"], c["tokens"], dev_status=status)
+    st["embedding"] = x0
+    blocks = [block.Block(B, T, d, c["dff"], c["heads"], device) for _ in c["blocks"]]
+    xs = [x0]
+    for i, (blk, w) in enumerate(zip(blocks, c["blocks"])):
+        xs.append(blk.forward(xs[-1], w))
+        st[f"block{i}"] = xs[-1]
+    logits = L.detgemm_f32(xs[-1], c["head"], transB=True)
+    st["logits"] = logits
+    loss, mean, dlogits = L.detxent_f32(logits, c["labels"], want_mean=True, want_dlogits=True,
+                                        dscale=1.0 / ntok, dev_status=status)
+    st["loss"], st["loss_mean"], st["dlogits"] = loss, mean, dlogits
+    # backward
+    grads = {"head": L.detgemm_f32(dlogits, xs[-1], transA=True)}
+    dx = L.detgemm_f32(dlogits, c["head"])
+    for i in reversed(range(len(blocks))):
+        dx, g = blocks[i].backward(xs[i], c["blocks"][i], dx)
+        for k in PARAMS:
+            grads[f"block{i}.{k}"] = g[k]
+        st[f"d_block{i}_input"] = dx
+    grads["emb"] = L.detembedding_bwd_f32(c["tokens"], dx, c["vocab"])
+    for k in sorted(grads):
+        st[f"grad.{k}"] = grads[k]
+    # AdamW on every parameter (decay on all, no mask), moments from zero
+    params = {"head": c["head"], "emb": c["emb"]}
+    for i, w in enumerate(c["blocks"]):
+        for k in PARAMS:
+            params[f"block{i}.{k}"] = w[k]
+    for k in sorted(params):
+        p = params[k].clone()
+        m = torch.zeros_like(p)
+        v = torch.zeros_like(p)
+        L.detadamw_f32(p.view(-1), grads[k].contiguous().view(-1), m.view(-1), v.view(-1), **hp)
+        st[f"param.{k}"], st[f"m.{k}"], st[f"v.{k}"] = p, m, v
     if int(status.item()) != 0:
         raise ValueError("a token or label outside the vocabulary")
-    return stages
+    return st
+
+
+def forward(c, device):
+    """The forward stages alone (embedding, blocks, logits, loss, mean)."""
+    import torch
+
+    from bitwise_reproducible_fp32_gb300 import block, detlib as L
+    B, T, d = c["batch"], c["seq"], c["d"]
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    st = {}
+    x = L.detembedding_f32(c["emb"], c["tokens"], dev_status=status)
+    st["embedding"] = x
+    blocks = [block.Block(B, T, d, c["dff"], c["heads"], device) for _ in c["blocks"]]
+    for i, (blk, w) in enumerate(zip(blocks, c["blocks"])):
+        x = blk.forward(x, w)          # each block owns its output buffer
+        st[f"block{i}"] = x
+    logits = L.detgemm_f32(x, c["head"], transB=True)
+    st["logits"] = logits
+    loss, mean, _ = L.detxent_f32(logits, c["labels"], want_mean=True, dev_status=status)
+    st["loss"], st["loss_mean"] = loss, mean
+    if int(status.item()) != 0:
+        raise ValueError("a token or label outside the vocabulary")
+    return st

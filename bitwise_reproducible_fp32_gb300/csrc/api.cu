@@ -215,8 +215,72 @@ DET_API det_status detrope_f32(const det_profile_v1 *prof, int64_t rows, int64_t
     if (rows == 0) return DET_OK;
     if (!x || ldx < heads * head_dim) return DET_ERR_INVALID_ARG;
     if ((st = check_device()) != DET_OK) return st;
-    return from_cuda(launch_rope(rows, int(heads), int(head_dim), x, ldx, seq_len, theta,
+    return from_cuda(launch_rope(rows, int(heads), int(head_dim), x, ldx, seq_len, theta, 0,
                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detrope_bwd_f32(const det_profile_v1 *prof, int64_t rows, int64_t heads,
+                                   int64_t head_dim, float *dx, int64_t ldx, int64_t seq_len,
+                                   float theta, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (rows < 0 || heads < 1 || head_dim < 2 || head_dim % 2 || head_dim > 65536 ||
+        heads > 65536 || seq_len < 1)
+        return DET_ERR_INVALID_ARG;
+    if (rows == 0) return DET_OK;
+    if (!dx || ldx < heads * head_dim) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_rope(rows, int(heads), int(head_dim), dx, ldx, seq_len, theta, 1,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detswiglu_bwd_f32(const det_profile_v1 *prof, int64_t n, const float *gate,
+                                     const float *up, const float *dh, float *d_gate,
+                                     float *d_up, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (n < 0) return DET_ERR_INVALID_ARG;
+    if (n == 0) return DET_OK;
+    if (!gate || !up || !dh || !d_gate || !d_up) return DET_ERR_INVALID_ARG;
+    // the outputs may overwrite dh, element for element, but nothing else
+    for (const float *in : {gate, up})
+        for (const float *o : {static_cast<const float *>(d_gate), static_cast<const float *>(d_up)})
+            if (overlaps(o, n, in, n)) return DET_ERR_INVALID_ARG;
+    if (overlaps(d_gate, n, d_up, n)) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_swiglu_bwd(n, gate, up, dh, d_gate, d_up,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detsoftmax_causal_bwd_f32(const det_profile_v1 *prof, int64_t rows,
+                                             int64_t cols, const float *p, const float *dp,
+                                             int64_t ld, float scale, int64_t diag,
+                                             int64_t period, float *ds, int64_t ldd,
+                                             det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (rows < 0 || cols < 1 || cols > kDimMax || period < 1) return DET_ERR_INVALID_ARG;
+    if (rows == 0) return DET_OK;
+    if (ld < cols || ldd < cols || !p || !dp || !ds) return DET_ERR_INVALID_ARG;
+    if ((ds == dp || ds == p) && ldd != ld) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_softmax_causal_bwd(rows, cols, p, dp, ld, scale, diag, period, ds,
+                                               ldd, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+DET_API det_status detembedding_bwd_f32(const det_profile_v1 *prof, int64_t ntok, int64_t dim,
+                                        const int32_t *tokens, const float *dx, int64_t lddx,
+                                        int64_t vocab, float *de, int64_t ldde,
+                                        det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (ntok < 0 || dim < 1 || dim > kDimMax || vocab < 1 || vocab > kDimMax)
+        return DET_ERR_INVALID_ARG;
+    if (!de || ldde < dim || (ntok > 0 && (!tokens || !dx || lddx < dim)))
+        return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    return from_cuda(launch_embedding_bwd(ntok, dim, tokens, dx, lddx, vocab, de, ldde,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 DET_API det_status detembedding_f32(const det_profile_v1 *prof, int64_t ntok, int64_t dim,
@@ -321,6 +385,91 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
             pv.C = out + b * seq * ldout + h * head_dim; pv.ldc = ldout;
             pv.transA = 0; pv.transB = 0;
             if (launch_gemm(pv, pv_ws, gws, s) != cudaSuccess) return DET_ERR_CUDA;
+        }
+    }
+    return DET_OK;
+}
+
+// Backward of detattention_f32, head after head: P is recomputed by the
+// forward's spelling (S = Q K^T, the causal softmax), then
+//   dP = dO V^T, dV = P^T dO, dS = the softmax backward of (P, dP),
+//   dQ = dS K, dK = dS^T Q
+// with detgemm_f32's arithmetic for every product. The gradients are those of
+// the Q, K and V that the forward read (after any rotary embedding).
+namespace {
+size_t attention_bwd_ws(int64_t seq, int64_t head_dim, size_t *gemm_ws) {
+    *gemm_ws = gemm_plan(seq, head_dim, seq, sm_count_current_device()).workspace_bytes;
+    return 2 * ((size_t(seq) * size_t(seq) * 4 + 255) / 256 * 256) + *gemm_ws;
+}
+}  // namespace
+
+DET_API det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t seq,
+                                                    int64_t head_dim, size_t *bytes) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (!bytes || seq < 1 || seq > 65536 || head_dim < 1 || head_dim > 65536)
+        return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    size_t g = 0;
+    *bytes = attention_bwd_ws(seq, head_dim, &g);
+    return DET_OK;
+}
+
+DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
+                                        int64_t heads, int64_t head_dim, const float *qkv,
+                                        int64_t ldqkv, const float *dout, int64_t lddout,
+                                        float scale, float *dqkv, int64_t lddqkv,
+                                        void *workspace, size_t workspace_bytes,
+                                        det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (batch < 0 || seq < 1 || seq > 65536 || heads < 1 || head_dim < 1 || head_dim > 65536 ||
+        heads > 65536)
+        return DET_ERR_INVALID_ARG;
+    if (batch == 0) return DET_OK;
+    const int64_t hd = heads * head_dim;
+    if (!qkv || !dout || !dqkv || ldqkv < 3 * hd || lddout < hd || lddqkv < 3 * hd)
+        return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    size_t gws = 0;
+    const size_t need = attention_bwd_ws(seq, head_dim, &gws);
+    if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+        return DET_ERR_WORKSPACE;
+    const size_t tt = (size_t(seq) * size_t(seq) * 4 + 255) / 256 * 256;
+    float *P = static_cast<float *>(workspace);
+    float *dP = reinterpret_cast<float *>(static_cast<char *>(workspace) + tt);
+    void *gw = gws ? static_cast<char *>(workspace) + 2 * tt : nullptr;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    auto gemm = [&](int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int tA,
+                    const float *B, int64_t ldb, int tB, float *C, int64_t ldc, bool ws) {
+        GemmArgs a;
+        a.M = M; a.N = N; a.K = K; a.A = A; a.lda = lda; a.B = B; a.ldb = ldb;
+        a.C = C; a.ldc = ldc; a.transA = tA; a.transB = tB;
+        return launch_gemm(a, ws ? gw : nullptr, ws ? gws : 0, s);
+    };
+    for (int64_t b = 0; b < batch; ++b) {
+        const float *base = qkv + b * seq * ldqkv;
+        const float *dob = dout + b * seq * lddout;
+        float *dbase = dqkv + b * seq * lddqkv;
+        for (int64_t h = 0; h < heads; ++h) {
+            const float *Q = base + h * head_dim, *K = base + hd + h * head_dim;
+            const float *V = base + 2 * hd + h * head_dim, *dO = dob + h * head_dim;
+            float *dQ = dbase + h * head_dim, *dK = dbase + hd + h * head_dim;
+            float *dV = dbase + 2 * hd + h * head_dim;
+            cudaError_t e = gemm(seq, seq, head_dim, Q, ldqkv, 0, K, ldqkv, 1, P, seq, false);
+            if (e == cudaSuccess)
+                e = launch_softmax_causal(seq, seq, P, seq, scale, 0, seq, P, seq, s);
+            if (e == cudaSuccess)
+                e = gemm(seq, seq, head_dim, dO, lddout, 0, V, ldqkv, 1, dP, seq, false);
+            if (e == cudaSuccess)
+                e = gemm(seq, head_dim, seq, P, seq, 1, dO, lddout, 0, dV, lddqkv, true);
+            if (e == cudaSuccess)
+                e = launch_softmax_causal_bwd(seq, seq, P, dP, seq, scale, 0, seq, dP, seq, s);
+            if (e == cudaSuccess)
+                e = gemm(seq, head_dim, seq, dP, seq, 0, K, ldqkv, 0, dQ, lddqkv, true);
+            if (e == cudaSuccess)
+                e = gemm(seq, head_dim, seq, dP, seq, 1, Q, ldqkv, 0, dK, lddqkv, true);
+            if (e != cudaSuccess) return DET_ERR_CUDA;
         }
     }
     return DET_OK;

@@ -58,6 +58,24 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// SwiGLU backward: silu = g / den, sig = 1 / den, den = 1 + exp(-g);
+// d_up = dh silu; d_gate = (dh u) (sig (1 + g (1 - sig))).
+__global__ void __launch_bounds__(256)
+    swiglu_bwd_kernel(int64_t n, const float *__restrict__ g, const float *__restrict__ u,
+                      const float *__restrict__ dh, float *dg, float *du) {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const float gv = g[i], uv = u[i], d = dh[i];
+        const float den = __fadd_rn(1.0f, det_exp(-gv));
+        const float silu = __fdiv_rn(gv, den);
+        const float sig = __fdiv_rn(1.0f, den);
+        const float ds =
+            __fmul_rn(sig, __fadd_rn(1.0f, __fmul_rn(gv, __fsub_rn(1.0f, sig))));
+        du[i] = __fmul_rn(d, silu);
+        dg[i] = __fmul_rn(__fmul_rn(d, uv), ds);
+    }
+}
+
 __global__ void __launch_bounds__(256)
     add_kernel(int64_t n, const float *__restrict__ a, const float *__restrict__ b,
                float *out, int vec) {
@@ -144,11 +162,66 @@ __global__ void __launch_bounds__(kSmaxThreads)
     }
 }
 
+// Softmax backward, one row per CTA, thread l = chain l: dot = the 256 chains
+// of fmaf(dP_j, P_j, .) over the kept columns, folded like the forward's sum;
+// then dS_j = (P_j (dP_j - dot)) scale; masked columns +0.
+__global__ void __launch_bounds__(kSmaxThreads)
+    softmax_causal_bwd_kernel(int64_t rows, int64_t cols, const float *p, const float *dp,
+                              int64_t ld, float scale, int64_t diag, int64_t period,
+                              float *ds, int64_t ldd) {
+    __shared__ float red[kSmaxThreads / 32];
+    const int l = threadIdx.x, lane = l & 31, warp = l >> 5;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float *pr = p + r * ld, *dpr = dp + r * ld;
+        float *dr = ds + r * ldd;
+        int64_t nr = (r % period) + diag + 1;
+        nr = nr < 0 ? 0 : (nr > cols ? cols : nr);
+        for (int64_t j = nr + l; j < cols; j += kSmaxThreads) dr[j] = 0.0f;
+        if (nr == 0) continue;
+        float c = 0.0f;
+        for (int64_t g = l; 4 * g < nr; g += kSmaxThreads) {
+            const int64_t j1 = 4 * g + 4 < nr ? 4 * g + 4 : nr;
+            for (int64_t j = 4 * g; j < j1; ++j) c = __fmaf_rn(dpr[j], pr[j], c);
+        }
+        c = butterfly32(c);
+        if (lane == 0) red[warp] = c;
+        __syncthreads();
+        const float a01 = __fadd_rn(red[0], red[1]), a23 = __fadd_rn(red[2], red[3]);
+        const float a45 = __fadd_rn(red[4], red[5]), a67 = __fadd_rn(red[6], red[7]);
+        const float dot = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
+        __syncthreads();
+        for (int64_t j = l; j < nr; j += kSmaxThreads)
+            dr[j] = __fmul_rn(__fmul_rn(pr[j], __fsub_rn(dpr[j], dot)), scale);
+    }
+}
+
+// Embedding backward: thread per (id, column); the tokens' gradient rows in
+// ascending token order, the first as is; +0 for an id no token uses.
+__global__ void __launch_bounds__(256)
+    embedding_bwd_kernel(int64_t ntok, int64_t dim, const int32_t *__restrict__ tokens,
+                         const float *__restrict__ dx, int64_t lddx, int64_t vocab, float *de,
+                         int64_t ldde) {
+    const int64_t total = vocab * dim;
+    for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t v = e / dim, j = e - v * dim;
+        float t = 0.0f;
+        bool first = true;
+        for (int64_t k = 0; k < ntok; ++k) {
+            if (tokens[k] != v) continue;
+            const float x = dx[k * lddx + j];
+            t = first ? x : __fadd_rn(t, x);
+            first = false;
+        }
+        de[v * ldde + j] = t;
+    }
+}
+
 // Thread per (row, pair i): a = pos * w_i, its sin and cos once, then the
-// pair turned in every head.
+// pair turned in every head (by -a for the backward).
 __global__ void __launch_bounds__(256)
     rope_kernel(int64_t rows, int heads, int d, float *x, int64_t ldx, int64_t seq,
-                float theta) {
+                float theta, int backward) {
     const int half = d / 2;
     const int64_t total = rows * half;
     const float L = det_log(theta);
@@ -166,8 +239,13 @@ __global__ void __launch_bounds__(256)
         for (int h = 0; h < heads; ++h) {
             float *q = row + h * d;
             const float x0 = q[0], x1 = q[1];
-            q[0] = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
-            q[1] = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs));
+            if (!backward) {
+                q[0] = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
+                q[1] = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs));
+            } else {
+                q[0] = __fadd_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
+                q[1] = __fsub_rn(__fmul_rn(x1, cs), __fmul_rn(x0, sn));
+            }
         }
     }
 }
@@ -234,10 +312,35 @@ cudaError_t launch_softmax_causal(int64_t rows, int64_t cols, const float *sc, i
 }
 
 cudaError_t launch_rope(int64_t rows, int heads, int head_dim, float *x, int64_t ldx,
-                        int64_t seq_len, float theta, cudaStream_t s) {
+                        int64_t seq_len, float theta, int backward, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
     rope_kernel<<<unsigned(ew_blocks(rows * (head_dim / 2))), 256, 0, s>>>(
-        rows, heads, head_dim, x, ldx, seq_len, theta);
+        rows, heads, head_dim, x, ldx, seq_len, theta, backward);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_bwd(int64_t n, const float *g, const float *u, const float *dh,
+                              float *dg, float *du, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    swiglu_bwd_kernel<<<unsigned(ew_blocks(n)), 256, 0, s>>>(n, g, u, dh, dg, du);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_causal_bwd(int64_t rows, int64_t cols, const float *p,
+                                      const float *dp, int64_t ld, float scale, int64_t diag,
+                                      int64_t period, float *ds, int64_t ldd, cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>(rows, int64_t(sm_count_current_device()) * 8);
+    softmax_causal_bwd_kernel<<<unsigned(blocks), kSmaxThreads, 0, s>>>(
+        rows, cols, p, dp, ld, scale, diag, period, ds, ldd);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_embedding_bwd(int64_t ntok, int64_t dim, const int32_t *tokens,
+                                 const float *dx, int64_t lddx, int64_t vocab, float *de,
+                                 int64_t ldde, cudaStream_t s) {
+    embedding_bwd_kernel<<<unsigned(ew_blocks(vocab * dim)), 256, 0, s>>>(
+        ntok, dim, tokens, dx, lddx, vocab, de, ldde);
     return cudaGetLastError();
 }
 

@@ -77,7 +77,15 @@ cudaError_t launch_softmax_causal(int64_t rows, int64_t cols, const float *sc, i
                                   float scale, int64_t diag, int64_t period, float *p,
                                   int64_t ldp, cudaStream_t s);
 cudaError_t launch_rope(int64_t rows, int heads, int head_dim, float *x, int64_t ldx,
-                        int64_t seq_len, float theta, cudaStream_t s);
+                        int64_t seq_len, float theta, int backward, cudaStream_t s);
+cudaError_t launch_swiglu_bwd(int64_t n, const float *g, const float *u, const float *dh,
+                              float *dg, float *du, cudaStream_t s);
+cudaError_t launch_softmax_causal_bwd(int64_t rows, int64_t cols, const float *p,
+                                      const float *dp, int64_t ld, float scale, int64_t diag,
+                                      int64_t period, float *ds, int64_t ldd, cudaStream_t s);
+cudaError_t launch_embedding_bwd(int64_t ntok, int64_t dim, const int32_t *tokens,
+                                 const float *dx, int64_t lddx, int64_t vocab, float *de,
+                                 int64_t ldde, cudaStream_t s);
 cudaError_t launch_embedding(int64_t ntok, int64_t dim, const float *table, int64_t ldt,
                              int64_t vocab, const int32_t *tokens, float *out, int64_t ldo,
                              int32_t *status, cudaStream_t s);

@@ -82,6 +82,15 @@ SIGNATURES = [
     ("detattention_f32", _int, [_PROF, _i64, _i64, _i64, _i64, _vp, _i64, _f, _vp, _i64, _vp,
                                 ctypes.c_size_t, _vp]),
     ("detattention_workspace_bytes", _int, [_PROF, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
+    ("detswiglu_bwd_f32", _int, [_PROF, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    ("detsoftmax_causal_bwd_f32", _int, [_PROF, _i64, _i64, _vp, _vp, _i64, _f, _i64, _i64,
+                                         _vp, _i64, _vp]),
+    ("detrope_bwd_f32", _int, [_PROF, _i64, _i64, _i64, _vp, _i64, _i64, _f, _vp]),
+    ("detembedding_bwd_f32", _int, [_PROF, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _i64, _vp]),
+    ("detattention_bwd_f32", _int, [_PROF, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _f,
+                                    _vp, _i64, _vp, ctypes.c_size_t, _vp]),
+    ("detattention_bwd_workspace_bytes", _int, [_PROF, _i64, _i64,
+                                                ctypes.POINTER(ctypes.c_size_t)]),
     ("det_watchdog_status", _int, [ctypes.POINTER(ctypes.c_int32), _int]),
 ]
 
@@ -454,6 +463,94 @@ def detattention_f32(qkv, batch, seq, heads, head_dim, scale=None, out=None, wor
                                  _ptr(workspace), workspace.numel() * 4, _stream(stream))
     _check("detattention_f32", st)
     return out
+
+
+# ---------------------------------------------------------------- block backward
+def detswiglu_bwd_f32(gate, up, dh, d_gate=None, d_up=None, profile=None, stream=None):
+    """Returns (d_gate, d_up) of h = silu(gate) * up."""
+    import torch
+    for t, n in ((gate, "gate"), (up, "up"), (dh, "dh")):
+        _flat(t, n)
+    d_gate = torch.empty_like(gate) if d_gate is None else _flat(d_gate, "d_gate")
+    d_up = torch.empty_like(gate) if d_up is None else _flat(d_up, "d_up")
+    st = load().detswiglu_bwd_f32(_prof(profile), gate.numel(), _ptr(gate), _ptr(up), _ptr(dh),
+                                  _ptr(d_gate), _ptr(d_up), _stream(stream))
+    _check("detswiglu_bwd_f32", st)
+    return d_gate, d_up
+
+
+def detsoftmax_causal_bwd_f32(p, dp, scale=1.0, diag=0, period=None, ds=None, profile=None,
+                              stream=None):
+    """dS of the causal softmax from P and dP (same layout). Returns ds."""
+    import torch
+    _cuda_f32(p, "p", 2)
+    _cuda_f32(dp, "dp", 2)
+    rows, cols = p.shape
+    if _ld(p) != _ld(dp):
+        raise ValueError("p and dp must share a row stride")
+    ds = torch.empty_like(p) if ds is None else ds
+    _cuda_f32(ds, "ds", 2)
+    period = rows if period is None else period
+    st = load().detsoftmax_causal_bwd_f32(_prof(profile), rows, cols, _ptr(p), _ptr(dp), _ld(p),
+                                          ctypes.c_float(scale), int(diag),
+                                          max(int(period), 1), _ptr(ds), _ld(ds),
+                                          _stream(stream))
+    _check("detsoftmax_causal_bwd_f32", st)
+    return ds
+
+
+def detrope_bwd_f32(dx, heads, head_dim, seq_len, theta=10000.0, profile=None, stream=None):
+    """The rotary backward in place on dx's first heads * head_dim columns."""
+    _cuda_f32(dx, "dx", 2)
+    st = load().detrope_bwd_f32(_prof(profile), dx.shape[0], heads, head_dim, _ptr(dx),
+                                _ld(dx), seq_len, ctypes.c_float(theta), _stream(stream))
+    _check("detrope_bwd_f32", st)
+    return dx
+
+
+def detembedding_bwd_f32(tokens, dx, vocab, de=None, profile=None, stream=None):
+    """Per-id ordered sums of the tokens' gradient rows. Returns de."""
+    import torch
+    _cuda_f32(dx, "dx", 2)
+    if tokens.dtype != torch.int32 or tokens.device.type != "cuda" or not tokens.is_contiguous():
+        raise TypeError("tokens must be a contiguous int32 CUDA tensor")
+    dim = dx.shape[1]
+    de = torch.empty((vocab, dim), dtype=torch.float32, device=dx.device) if de is None else de
+    _cuda_f32(de, "de", 2)
+    st = load().detembedding_bwd_f32(_prof(profile), tokens.numel(), dim, _ptr(tokens),
+                                     _ptr(dx), _ld(dx), vocab, _ptr(de), _ld(de),
+                                     _stream(stream))
+    _check("detembedding_bwd_f32", st)
+    return de
+
+
+def detattention_bwd_workspace_bytes(seq, head_dim, profile=None) -> int:
+    n = ctypes.c_size_t(0)
+    _check("detattention_bwd_workspace_bytes",
+           load().detattention_bwd_workspace_bytes(_prof(profile), seq, head_dim,
+                                                   ctypes.byref(n)))
+    return n.value
+
+
+def detattention_bwd_f32(qkv, dout, batch, seq, heads, head_dim, scale=None, dqkv=None,
+                         workspace=None, profile=None, stream=None):
+    """Gradients of the packed Q, K, V (the forward's input). Returns dqkv."""
+    import torch
+    _cuda_f32(qkv, "qkv", 2)
+    _cuda_f32(dout, "dout", 2)
+    dqkv = torch.empty_like(qkv) if dqkv is None else dqkv
+    _cuda_f32(dqkv, "dqkv", 2)
+    if scale is None:
+        scale = 1.0 / float(head_dim) ** 0.5
+    if workspace is None:
+        workspace = torch.empty((detattention_bwd_workspace_bytes(seq, head_dim, profile) + 3)
+                                // 4, dtype=torch.float32, device=qkv.device)
+    st = load().detattention_bwd_f32(_prof(profile), batch, seq, heads, head_dim, _ptr(qkv),
+                                     _ld(qkv), _ptr(dout), _ld(dout), ctypes.c_float(scale),
+                                     _ptr(dqkv), _ld(dqkv), _ptr(workspace),
+                                     workspace.numel() * 4, _stream(stream))
+    _check("detattention_bwd_f32", st)
+    return dqkv
 
 
 # ---------------------------------------------------------------- cross-entropy

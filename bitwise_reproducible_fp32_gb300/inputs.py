@@ -210,6 +210,9 @@ def byte_lm_cfg2(seed: int = SEED_CFG2 + 100, batch: int = 16, seq: int = 128, d
                 head=head, batch=batch, seq=seq, d=d, dff=dff, vocab=vocab, heads=4)
 
 
+# the byte-level LM step's update: the 162M card's AdamW at the first step
+BYTE_LM_HP = dict(lr=6e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1)
+
 ADAMW_HP = dict(lr=6e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
                 step=251)
 

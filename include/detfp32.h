@@ -405,6 +405,61 @@ det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, int64_t s
 det_status detattention_workspace_bytes(const det_profile_v1 *prof, int64_t seq,
                                         int64_t head_dim, size_t *bytes);
 
+/* ------------------------------------------------------------------ block backward
+ * The backward of the block operations, for the byte-level LM's training step
+ * (the pages train "embedding, transformer forward and backward, cross entropy,
+ * and AdamW" bit-identically; "mojolearn" PyPI page, section "Handing training
+ * off between vendors"; they print no backward spelling). */
+
+/* SwiGLU backward: with den = 1 + exp(-g), silu = g / den, sig = 1 / den:
+ * d_up = dh * silu, d_gate = (dh * up) * (sig * (1 + g * (1 - sig))), each
+ * operation rounded once in that order. n floats each; d_gate and d_up must
+ * not overlap each other, gate or up (either may be dh itself). */
+det_status detswiglu_bwd_f32(const det_profile_v1 *prof, int64_t n, const float *gate,
+                             const float *up, const float *dh, float *d_gate, float *d_up,
+                             det_stream_t stream);
+
+/* Causal softmax backward: over row r's kept columns (j <= (r mod period) +
+ * diag), dot = the 256-chain sum of fmaf(dP_j, P_j, .) (the forward's
+ * arrangement) folded by the butterfly; dS_j = (P_j * (dP_j - dot)) * scale;
+ * masked columns +0. p, dp: rows x cols with row stride ld; ds: row stride
+ * ldd; ds may equal dp or p when ldd == ld. */
+det_status detsoftmax_causal_bwd_f32(const det_profile_v1 *prof, int64_t rows, int64_t cols,
+                                     const float *p, const float *dp, int64_t ld, float scale,
+                                     int64_t diag, int64_t period, float *ds, int64_t ldd,
+                                     det_stream_t stream);
+
+/* Rotary backward, in place on a gradient laid out as detrope_f32's input:
+ * with the forward's angle a, dx0 = dy0 cos a + dy1 sin a,
+ * dx1 = dy1 cos a - dy0 sin a. */
+det_status detrope_bwd_f32(const det_profile_v1 *prof, int64_t rows, int64_t heads,
+                           int64_t head_dim, float *dx, int64_t ldx, int64_t seq_len,
+                           float theta, det_stream_t stream);
+
+/* Embedding backward: de[v] (vocab x dim, row stride ldde) = the gradient rows
+ * dx[t] (row stride lddx) of the tokens t with tokens[t] == v, added in
+ * ascending t, the first as is; +0 for an id no token uses. Every row of de
+ * is written. */
+det_status detembedding_bwd_f32(const det_profile_v1 *prof, int64_t ntok, int64_t dim,
+                                const int32_t *tokens, const float *dx, int64_t lddx,
+                                int64_t vocab, float *de, int64_t ldde, det_stream_t stream);
+
+/* Backward of detattention_f32: given the packed qkv the forward read and the
+ * gradient of its output (dout, batch seq rows of heads x head_dim), writes the
+ * gradients of Q, K and V into dqkv (same packed layout). Per sequence and
+ * head, P is recomputed by the forward's spelling; dP = dO V^T, dV = P^T dO,
+ * dS = detsoftmax_causal_bwd_f32(P, dP, scale), dQ = dS K, dK = dS^T Q, every
+ * product with detgemm_f32's arithmetic. The workspace (at least
+ * detattention_bwd_workspace_bytes, 256-byte aligned) holds two seq x seq
+ * buffers. dqkv must not overlap qkv, dout or the workspace. */
+det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
+                                int64_t heads, int64_t head_dim, const float *qkv,
+                                int64_t ldqkv, const float *dout, int64_t lddout, float scale,
+                                float *dqkv, int64_t lddqkv, void *workspace,
+                                size_t workspace_bytes, det_stream_t stream);
+det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t seq,
+                                            int64_t head_dim, size_t *bytes);
+
 /* Reads, and optionally clears, the current device's watchdog word.
  * *code == 0 means no bounded device wait has ever given up; otherwise bit k
  * identifies the kernel family that gave up (bit 0: GEMM operand staging,

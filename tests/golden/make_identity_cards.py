@@ -52,6 +52,9 @@ def cards():
     import oracle_models
     for name, v in oracle_models.byte_lm_forward(inputs.byte_lm_cfg2()).items():
         out[f"byte_lm/{name}"] = card(v)
+    # one whole training step of it (forward, backward, AdamW from zero moments)
+    for name, v in oracle_models.byte_lm_step(inputs.byte_lm_cfg2(), inputs.BYTE_LM_HP).items():
+        out[f"byte_lm_step/{name}"] = card(v)
     return out
 
 

@@ -31,7 +31,10 @@ def test_header_declares_the_boundary():
                  "detrmsnorm_bwd_f32", "detrmsnorm_bwd_workspace_bytes",
                  "detgemm_acc_f32", "detshardsum_f32", "detswiglu_f32", "detadd_f32",
                  "detsoftmax_causal_f32", "detrope_f32", "detsin_f32", "detcos_f32",
-                 "detattention_f32", "detattention_workspace_bytes",
+                 "detattention_f32", "detattention_workspace_bytes", "detembedding_f32",
+                 "detswiglu_bwd_f32", "detsoftmax_causal_bwd_f32", "detrope_bwd_f32",
+                 "detembedding_bwd_f32", "detattention_bwd_f32",
+                 "detattention_bwd_workspace_bytes",
                  "detexp_f32", "detlog_f32", "det_profile_default",
                  "det_status_string", "det_watchdog_status"):
         assert want in names
@@ -164,6 +167,16 @@ def test_bad_arguments_are_refused_on_the_host(lib):
     assert at(p, 1, 16, 2, 8, dummy, 47, one, dummy, 16, dummy, 1 << 20, null) == 1
     assert at(p, 1, 16, 2, 8, dummy, 48, one, dummy, 15, dummy, 1 << 20, null) == 1
     assert at(p, 0, 16, 2, 8, null, 48, one, null, 16, null, 0, null) == 0
+    # backward ops and the embedding
+    assert lib.detswiglu_bwd_f32(p, 8, d0, dummy, dummy, ctypes.c_void_p(0x1000 + 16), dummy,
+                                 null) == 1                      # d_gate over gate
+    assert lib.detsoftmax_causal_bwd_f32(p, 4, 8, dummy, dummy, 8, one, 0, 4, dummy, 12,
+                                         null) == 1
+    assert lib.detrope_bwd_f32(p, 4, 2, 63, dummy, 200, 4, ctypes.c_float(1e4), null) == 1
+    assert lib.detembedding_f32(p, 4, 8, dummy, 7, 10, dummy, dummy, 8, null, null) == 1
+    assert lib.detembedding_bwd_f32(p, 4, 8, dummy, dummy, 8, 10, dummy, 7, null) == 1
+    assert lib.detattention_bwd_f32(p, 1, 16, 2, 8, dummy, 48, dummy, 16, one, dummy, 47,
+                                    dummy, 1 << 20, null) == 1
     hp = detlib.AdamWHP(1e-3, 0.9, 0.95, 1e-8, 0.1, 0)
     assert lib.detadamw_f32(p, 4, dummy, dummy, dummy, dummy, ctypes.byref(hp), null) == 1
     assert lib.detexp_f32(p, -1, dummy, dummy, null) == 1

@@ -1,0 +1,110 @@
+"""GPU parity (0 ULP) of the backward operations against the oracle: SwiGLU's
+backward, the causal softmax backward (square, batched by period, shifted
+diagonals, in place), the rotary backward, the embedding backward (ids unused,
+repeated, ragged widths), and the attention backward (small in full and at the
+162M shape on sampled heads)."""
+import numpy as np
+import pytest
+
+import oracle
+from bitcmp import assert_bitwise
+from bitwise_reproducible_fp32_gb300 import detlib
+from gpu_util import host, need_gpu, to_dev, torch
+
+pytestmark = pytest.mark.gpu
+F = np.float32
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return need_gpu()
+
+
+@pytest.mark.parametrize("n", [1, 7, 1000, (1 << 20) + 5])
+def test_swiglu_bwd(dev, n):
+    rng = np.random.default_rng(n)
+    g = (3 * rng.standard_normal(n)).astype(F)
+    u = rng.standard_normal(n).astype(F)
+    dh = rng.standard_normal(n).astype(F)
+    if n > 6:
+        g[:6] = [0.0, -0.0, 100.0, -100.0, np.nan, 30.0]
+    dg, du = detlib.detswiglu_bwd_f32(to_dev(g), to_dev(u), to_dev(dh))
+    wg, wu = oracle.swiglu_bwd(g, u, dh)
+    assert_bitwise(host(dg), wg, "d_gate")
+    assert_bitwise(host(du), wu, "d_up")
+
+
+@pytest.mark.parametrize("rows,cols,diag", [(1, 1, 0), (5, 5, 0), (300, 300, 0),
+                                            (64, 2048, 1500), (257, 257, -3)])
+def test_softmax_bwd(dev, rows, cols, diag):
+    rng = np.random.default_rng(rows + cols)
+    s = (4 * rng.standard_normal((rows, cols))).astype(F)
+    p = oracle.softmax_causal(s, scale=0.125, diag=diag)
+    dp = rng.standard_normal((rows, cols)).astype(F)
+    want = oracle.softmax_causal_bwd(p, dp, scale=0.125, diag=diag)
+    got = detlib.detsoftmax_causal_bwd_f32(to_dev(p, "padded"), to_dev(dp, "padded"),
+                                           scale=0.125, diag=diag)
+    assert_bitwise(host(got), want)
+
+
+def test_softmax_bwd_batched_in_place(dev):
+    rng = np.random.default_rng(201)
+    mats = [(3 * rng.standard_normal((130, 130))).astype(F) for _ in range(3)]
+    ps = [oracle.softmax_causal(m, scale=0.25) for m in mats]
+    dps = [rng.standard_normal((130, 130)).astype(F) for _ in range(3)]
+    dpd = to_dev(np.concatenate(dps))
+    detlib.detsoftmax_causal_bwd_f32(to_dev(np.concatenate(ps)), dpd, scale=0.25, period=130,
+                                     ds=dpd)
+    want = np.concatenate([oracle.softmax_causal_bwd(p, d, scale=0.25) for p, d in zip(ps, dps)])
+    assert_bitwise(host(dpd), want)
+
+
+def test_rope_bwd(dev):
+    rng = np.random.default_rng(202)
+    T, H, d = 600, 6, 64
+    x = rng.standard_normal((T, 3 * H * d)).astype(F)
+    xd = to_dev(x)
+    detlib.detrope_bwd_f32(xd, heads=2 * H, head_dim=d, seq_len=300)
+    got = host(xd)
+    assert_bitwise(got[:, :2 * H * d], oracle.rope_bwd(x[:, :2 * H * d], 2 * H, d, seq_len=300))
+    assert_bitwise(got[:, 2 * H * d:], x[:, 2 * H * d:])
+
+
+@pytest.mark.parametrize("ntok,dim,vocab", [(1, 1, 1), (2048, 64, 256), (777, 9, 300),
+                                            (5000, 33, 7)])
+def test_embedding_bwd(dev, ntok, dim, vocab):
+    rng = np.random.default_rng(ntok + dim)
+    tok = rng.integers(0, max(vocab - 3, 1), size=ntok).astype(np.int32)
+    dx = rng.standard_normal((ntok, dim)).astype(F)
+    got = detlib.detembedding_bwd_f32(torch.from_numpy(tok).cuda(), to_dev(dx, "offset"), vocab)
+    assert_bitwise(host(got), oracle.embedding_bwd(tok, dx, vocab))
+
+
+def attention_bwd_oracle(qkv, dout, b, h, seq, heads, d, scale):
+    hd = heads * d
+    r = slice(b * seq, (b + 1) * seq)
+    Q, K, V = (qkv[r, o + h * d:o + (h + 1) * d] for o in (0, hd, 2 * hd))
+    dO = dout[r, h * d:(h + 1) * d]
+    P = oracle.softmax_causal(oracle.gemm(Q, K, transB=True), scale=scale)
+    dP = oracle.gemm(dO, V, transB=True)
+    dV = oracle.gemm(P, dO, transA=True)
+    dS = oracle.softmax_causal_bwd(P, dP, scale=scale)
+    return oracle.gemm(dS, K), oracle.gemm(dS, Q, transA=True), dV
+
+
+@pytest.mark.parametrize("B,T,H,d,checks", [(2, 100, 3, 16, None), (4, 2048, 12, 64,
+                                                                     [(0, 0), (3, 11)])])
+def test_attention_bwd(dev, B, T, H, d, checks):
+    rng = np.random.default_rng(T + H)
+    qkv = rng.standard_normal((B * T, 3 * H * d)).astype(F)
+    dout = rng.standard_normal((B * T, H * d)).astype(F)
+    scale = 1.0 / np.sqrt(d)
+    got = host(detlib.detattention_bwd_f32(to_dev(qkv), to_dev(dout), B, T, H, d))
+    pairs = checks or [(b, h) for b in range(B) for h in range(H)]
+    hd = H * d
+    for b, h in pairs:
+        dQ, dK, dV = attention_bwd_oracle(qkv, dout, b, h, T, H, d, float(F(scale)))
+        r = slice(b * T, (b + 1) * T)
+        assert_bitwise(got[r, h * d:(h + 1) * d], dQ, f"dQ b={b} h={h}")
+        assert_bitwise(got[r, hd + h * d:hd + (h + 1) * d], dK, f"dK b={b} h={h}")
+        assert_bitwise(got[r, 2 * hd + h * d:2 * hd + (h + 1) * d], dV, f"dV b={b} h={h}")

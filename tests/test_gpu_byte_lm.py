@@ -39,3 +39,22 @@ def test_byte_lm_forward_stage_cards(dev):
         assert_bitwise(got[name].reshape(want[name].shape), want[name], name)
         assert card(got[name]) == frozen[f"byte_lm/{name}"], name
     assert np.isfinite(got["loss_mean"]).all()
+
+
+def test_byte_lm_training_step_stage_cards(dev):
+    # forward, backward and AdamW: 73 stages, each bit-identical to the oracle's
+    # composition and to its frozen card
+    c = inputs.byte_lm_cfg2()
+    cd = dict(c)
+    cd["tokens"] = torch.from_numpy(c["tokens"]).cuda()
+    cd["labels"] = torch.from_numpy(c["labels"]).cuda()
+    cd["emb"], cd["head"] = to_dev(c["emb"]), to_dev(c["head"])
+    cd["blocks"] = [{k: to_dev(v) for k, v in b.items()} for b in c["blocks"]]
+    got = {k: host(v) for k, v in
+           byte_lm.train_step(cd, torch.device("cuda"), inputs.BYTE_LM_HP).items()}
+    want = oracle_models.byte_lm_step(c, inputs.BYTE_LM_HP)
+    frozen = json.load(open(os.path.join(GOLDEN, "identity_cards_v1.json")))["cards"]
+    assert list(got) == list(want)
+    for name in want:
+        assert_bitwise(got[name].reshape(want[name].shape), want[name], name)
+        assert card(got[name]) == frozen[f"byte_lm_step/{name}"], name
