@@ -99,7 +99,6 @@ DET_API const char *det_status_string(int status) {
 DET_API det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA,
                                            int transB, int64_t M, int64_t N, int64_t K,
                                            size_t *bytes) {
-    (void)transA;
     (void)transB;
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
@@ -108,7 +107,7 @@ DET_API det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int trans
     *bytes = 0;
     if (M == 0 || N == 0 || K == 0) return DET_OK;
     if ((st = check_device()) != DET_OK) return st;
-    *bytes = gemm_plan(M, N, K, sm_count_current_device()).workspace_bytes;
+    *bytes = gemm_plan(M, N, K, sm_count_current_device(), transA == 0).workspace_bytes;
     return DET_OK;
 }
 
@@ -326,7 +325,7 @@ DET_API det_status detcos_f32(const det_profile_v1 *prof, int64_t n, const float
 // seq x seq score buffer in the workspace.
 namespace {
 size_t attention_ws(int64_t seq, int64_t head_dim, size_t *gemm_ws) {
-    *gemm_ws = gemm_plan(seq, head_dim, seq, sm_count_current_device()).workspace_bytes;
+    *gemm_ws = gemm_plan(seq, head_dim, seq, sm_count_current_device(), true).workspace_bytes;
     return (size_t(seq) * size_t(seq) * 4 + 255) / 256 * 256 + *gemm_ws;
 }
 }  // namespace
@@ -398,7 +397,7 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
 // the Q, K and V that the forward read (after any rotary embedding).
 namespace {
 size_t attention_bwd_ws(int64_t seq, int64_t head_dim, size_t *gemm_ws) {
-    *gemm_ws = gemm_plan(seq, head_dim, seq, sm_count_current_device()).workspace_bytes;
+    *gemm_ws = gemm_plan(seq, head_dim, seq, sm_count_current_device(), true).workspace_bytes;
     return 2 * ((size_t(seq) * size_t(seq) * 4 + 255) / 256 * 256) + *gemm_ws;
 }
 }  // namespace

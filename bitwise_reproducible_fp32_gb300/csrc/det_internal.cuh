@@ -41,9 +41,11 @@ struct GemmPlan {
     int units_per_tile;    // chunk groups a tile is cut into
     int kt_per_unit;       // k-tiles a unit computes
     int nchunks;
+    int transpose_a;       // 1: op(A) is read from a K x M copy in the workspace
     size_t workspace_bytes;
 };
-GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms);
+// a_kmajor: op(A) is k-contiguous (transA == 0), the layout a copy can help.
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor);
 cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_bytes,
                         cudaStream_t s);
 cudaError_t gemm_watchdog(unsigned int *code, int clear);

@@ -28,8 +28,12 @@
 //    16-byte loads of 4 consecutive k from 8 different rows are free of bank
 //    conflicts; tiles whose m/n is contiguous are stored plain and read as
 //    float4 along m/n.
-//  * Per 4-wide k group a thread issues 24 LDS.128 and 512 FFMA; one operand's
-//    4-k fragment is held while the other streams.
+//  * Per 4-wide k group a thread issues 24 LDS.128 and 512 FMAs; one operand's
+//    4-k fragment is held while the other streams. The FMAs go out as packed
+//    pairs (fma.rn.f32x2, each half rounded as fmaf) where a 16-byte load
+//    yields the pairs: two rows of op(A) when A is m-contiguous, which
+//    measured fastest. A large GEMM with a k-contiguous A therefore first
+//    copies A transposed into the caller's workspace (transpose_kernel).
 //  * Chunk partials: the running left-to-right total lives in shared memory
 //    (128 KB), touched once per 256 k, which keeps registers for the
 //    accumulators and fragments.
@@ -133,8 +137,8 @@ __device__ __forceinline__ int64_t ws_index(int c, int ntiles, int t, int q, int
 // B with m/n contiguous (B_KM false): one 16-byte load holds columns
 // {c, c+1, c+2, c+3} at one k, i.e. two column pairs ready for fma.rn.f32x2;
 // A's value is paired with itself. A k-contiguous B would need its pairs
-// assembled from two loads; that layout (the LM head's W^T) measured faster
-// with scalar FFMA, so it keeps mma_group_scalar.
+// assembled from two loads, so with a k-contiguous A as well the scalar form
+// (mma_group_scalar) is used.
 template <bool A_KM>
 __device__ __forceinline__ void mma_group_packed(const float *__restrict__ As,
                                                  const float *__restrict__ Bs, int q,
@@ -243,13 +247,66 @@ __device__ __forceinline__ void mma_group_scalar(const float *__restrict__ As,
     }
 }
 
+// A with m contiguous (A_KM false): one 16-byte load holds rows {r, r+1, r+2,
+// r+3} at one k, i.e. two row pairs ready for fma.rn.f32x2; B's value is
+// paired with itself, TN splats a k against TM splats when pairing columns.
+template <bool B_KM>
+__device__ __forceinline__ void mma_group_mpair(const float *__restrict__ As,
+                                                const float *__restrict__ Bs, int q,
+                                                int arow, int bcol, int ln,
+                                                float (&acc)[TM][TN]) {
+    float b[TN][4];
+    if (B_KM) {
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            const int sw = ln + 4 * (c & 1);
+            const float4 v = *reinterpret_cast<const float4 *>(
+                Bs + (bcol + 4 * c) * 32 + ((q ^ sw) << 2));
+            b[c][0] = v.x; b[c][1] = v.y; b[c][2] = v.z; b[c][3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float *pb = Bs + (4 * q + kk) * BN + bcol;
+            const float4 lo = *reinterpret_cast<const float4 *>(pb);
+            const float4 hi = *reinterpret_cast<const float4 *>(pb + 16);
+            b[0][kk] = lo.x; b[1][kk] = lo.y; b[2][kk] = lo.z; b[3][kk] = lo.w;
+            b[4][kk] = hi.x; b[5][kk] = hi.y; b[6][kk] = hi.z; b[7][kk] = hi.w;
+        }
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const float *pa = As + (4 * q + kk) * BM + arow;
+        f32x2 a[TM / 2];     // a[r2] = rows {2r2, 2r2 + 1} of the thread at this k
+#pragma unroll
+        for (int h = 0; h < TM / 4; ++h) {
+            const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(pa + 32 * h);
+            a[2 * h] = v.x; a[2 * h + 1] = v.y;
+        }
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            const f32x2 bb = pack2(b[c][kk], b[c][kk]);
+#pragma unroll
+            for (int r2 = 0; r2 < TM / 2; ++r2) {
+                f32x2 v = pack2(acc[2 * r2][c], acc[2 * r2 + 1][c]);
+                v = fma2(a[r2], bb, v);
+                unpack2(v, acc[2 * r2][c], acc[2 * r2 + 1][c]);
+            }
+        }
+    }
+}
+
+// Measured on the 162M shapes: row pairs (A m-contiguous) beat column pairs
+// and scalar FFMA by 5-12%, which is why a k-contiguous A worth the copy is
+// transposed first (transpose_kernel, gemm_plan).
 template <bool A_KM, bool B_KM>
 __device__ __forceinline__ void mma_group(const float *__restrict__ As,
                                           const float *__restrict__ Bs, int q,
                                           int arow, int bcol, int lm, int ln,
                                           float (&acc)[TM][TN]) {
-    if (B_KM) mma_group_scalar<A_KM, B_KM>(As, Bs, q, arow, bcol, lm, ln, acc);
-    else      mma_group_packed<A_KM>(As, Bs, q, arow, bcol, lm, acc);
+    if (!A_KM)     mma_group_mpair<B_KM>(As, Bs, q, arow, bcol, ln, acc);
+    else if (B_KM) mma_group_scalar<A_KM, B_KM>(As, Bs, q, arow, bcol, lm, ln, acc);
+    else           mma_group_packed<A_KM>(As, Bs, q, arow, bcol, lm, acc);
 }
 
 // The thread's r-th row of op(A) and c-th column of op(B), tile-relative.
@@ -608,6 +665,29 @@ __global__ void chunk_sum_kernel(KArgs p, int nchunks, int a_km, int b_km) {
     }
 }
 
+// T = A^T: A is M x K (row stride lda), T is K x M (row stride ldt). Data
+// movement only, so the GEMM that reads T forms the same chains, bit for bit,
+// as one reading A. 32 x 32 tiles through shared memory (one padding column
+// against bank conflicts), both sides coalesced; the grid strides over tiles.
+__global__ void transpose_kernel(const float *__restrict__ A, int64_t lda, int M, int K,
+                                 float *__restrict__ T, int64_t ldt) {
+    __shared__ float tile[32][33];
+    const int64_t mtiles = (M + 31) / 32, ktiles = (K + 31) / 32;
+    for (int64_t t = blockIdx.x; t < mtiles * ktiles; t += gridDim.x) {
+        const int m0 = int(t / ktiles) * 32, k0 = int(t % ktiles) * 32;
+        __syncthreads();   // the previous tile's reads are done
+        for (int i = threadIdx.y; i < 32; i += 8) {
+            const int m = m0 + i, k = k0 + threadIdx.x;
+            if (m < M && k < K) tile[i][threadIdx.x] = A[int64_t(m) * lda + k];
+        }
+        __syncthreads();
+        for (int i = threadIdx.y; i < 32; i += 8) {
+            const int k = k0 + i, m = m0 + threadIdx.x;
+            if (k < K && m < M) T[int64_t(k) * ldt + m] = tile[threadIdx.x][i];
+        }
+    }
+}
+
 // K == 0: the empty sum, +0 everywhere (C + 0 when accumulating).
 __global__ void fill_zero_kernel(float *C, int64_t ldc, int64_t M, int64_t N, int accum) {
     const int64_t total = M * N;
@@ -717,8 +797,13 @@ double busiest_cta_steps(int64_t T, int64_t S, int64_t G, int64_t nkt, int sms) 
 }
 }  // namespace
 
-GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms) {
+// Row stride of the transposed copy of a k-contiguous A: M rounded up to 4
+// floats, so the copy's rows are 16-byte aligned for TMA.
+int64_t transposed_ld(int64_t M) { return (M + 3) / 4 * 4; }
+
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor) {
     GemmPlan pl{};
+    pl.transpose_a = 0;
     const int64_t T = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int64_t nkt = (K + BK - 1) / BK;
     const int64_t nchunks = (K + kKChunk - 1) / kKChunk;
@@ -727,10 +812,25 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms) {
     pl.kt_per_unit = int(nkt);
     pl.nchunks = int(nchunks);
     pl.workspace_bytes = 0;
-    if (M == 0 || N == 0 || K == 0 || nchunks < 2 || sms < 1) return pl;
-    // enough tiles to fill every SM several times over: splitting cannot pay
-    if (T >= int64_t(sms) * 16) return pl;
+    if (M == 0 || N == 0 || K == 0 || sms < 1) return pl;
     const double kt_step_s = 6.0e-6, hbm_bps = 6.0e12, launch_s = 5.0e-6;
+    // An unsplit GEMM whose A is k-contiguous runs ~8% faster on a transposed
+    // copy (row pairs, mma_group_mpair); take it where that gain, at ~48
+    // TFLOP/s, exceeds the copy's launch and its read and write at HBM speed.
+    auto consider_transpose = [&] {
+        if (!a_kmajor) return;
+        const double gain = 0.08 * 2.0 * double(M) * double(N) * double(K) / 48.0e12;
+        const double cost = launch_s + 8.0 * double(M) * double(K) / hbm_bps;
+        if (gain > cost) {
+            pl.transpose_a = 1;
+            pl.workspace_bytes = size_t(K) * size_t(transposed_ld(M)) * 4;
+        }
+    };
+    // enough tiles to fill every SM several times over: splitting cannot pay
+    if (nchunks < 2 || T >= int64_t(sms) * 16) {
+        consider_transpose();
+        return pl;
+    }
     double best = busiest_cta_steps(T, 1, nchunks, nkt, sms) * kt_step_s;
     for (int64_t S = 2; S <= nchunks; ++S) {
         const int64_t G = (nchunks + S - 1) / S;              // chunks a unit
@@ -747,6 +847,7 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms) {
             pl.workspace_bytes = size_t(ws);
         }
     }
+    if (!pl.split) consider_transpose();
     return pl;
 }
 
@@ -760,12 +861,28 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
         return cudaGetLastError();
     }
     const int sms = sm_count_current_device();
-    GemmPlan pl = gemm_plan(a.M, a.N, a.K, sms);
-    if (pl.split && (workspace == nullptr || workspace_bytes < pl.workspace_bytes ||
-                     reinterpret_cast<uintptr_t>(workspace) % 16 != 0)) {
+    GemmPlan pl = gemm_plan(a.M, a.N, a.K, sms, !a.transA);
+    if ((pl.split || pl.transpose_a) &&
+        (workspace == nullptr || workspace_bytes < pl.workspace_bytes ||
+         reinterpret_cast<uintptr_t>(workspace) % 16 != 0)) {
         pl = GemmPlan{};          // no usable workspace: one unit per tile
         pl.units_per_tile = 1;
         pl.kt_per_unit = int((a.K + BK - 1) / BK);
+    }
+    if (pl.transpose_a) {
+        // op(A) from the K x M copy: the transA form of the same product
+        float *T = static_cast<float *>(workspace);
+        const int64_t ldt = transposed_ld(a.M);
+        const int64_t tiles = ((a.M + 31) / 32) * ((a.K + 31) / 32);
+        const unsigned blocks = unsigned(std::min<int64_t>(tiles, int64_t(sms) * 16));
+        transpose_kernel<<<blocks, dim3(32, 8), 0, s>>>(a.A, a.lda, int(a.M), int(a.K), T, ldt);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        GemmArgs t = a;
+        t.A = T;
+        t.lda = ldt;
+        t.transA = 1;
+        return launch_gemm(t, nullptr, 0, s);
     }
     KArgs k;
     k.M = int(a.M); k.N = int(a.N); k.K = int(a.K);
@@ -836,19 +953,21 @@ static cudaError_t static_scratch(void **ptr) {
 
 cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s) {
     *too_big = false;
-    const GemmPlan pl = gemm_plan(a.M, a.N, a.K, sm_count_current_device());
-    if (pl.workspace_bytes > kStaticScratchBytes) {
+    const GemmPlan pl = gemm_plan(a.M, a.N, a.K, sm_count_current_device(), !a.transA);
+    if (pl.split && pl.workspace_bytes > kStaticScratchBytes) {
         *too_big = true;
         return cudaSuccess;
     }
+    // a transposed copy of A that does not fit is skipped: launch_gemm then
+    // reads A in place (same bits, a little slower)
     void *scratch = nullptr;
-    if (pl.split) {
+    if (pl.split || pl.transpose_a) {
         const cudaError_t e = static_scratch(&scratch);
         if (e != cudaSuccess) return e;
     }
-    // every slot of the scratch that the second pass reads is written first by
-    // this call, so nothing needs clearing between calls
-    return launch_gemm(a, scratch, pl.split ? kStaticScratchBytes : 0, s);
+    // every slot of the scratch that is read is written first by this call, so
+    // nothing needs clearing between calls
+    return launch_gemm(a, scratch, scratch ? kStaticScratchBytes : 0, s);
 }
 
 cudaError_t gemm_watchdog(unsigned int *code, int clear) {

@@ -98,10 +98,12 @@ const char *det_status_string(int status);
  *   overlapping A, B or C). With at least detgemm_workspace_bytes() bytes the
  *   library may cut K into groups of whole 256-wide chunks computed by
  *   different CTAs: each chunk partial P_c is written to the workspace and a
- *   second kernel adds them left to right. With NULL, or too few bytes, every
- *   output's chunks are computed by one thread. The result bits are the same
- *   either way; only the speed differs. Calls that share a workspace must be
- *   ordered (one stream).
+ *   second kernel adds them left to right. For a large product with transA ==
+ *   0 it may instead copy A transposed (K x M) into the workspace and read
+ *   that copy, which its FFMA loop consumes faster. With NULL, or too few
+ *   bytes, every output's chunks are computed by one thread from A in place.
+ *   The result bits are the same either way; only the speed differs. Calls
+ *   that share a workspace must be ordered (one stream).
  *
  * Errors: DET_ERR_INVALID_ARG for negative sizes, a dimension >= 2^31, an ld
  * below its row length or null pointers with nonzero sizes. A TMA wait that
@@ -172,9 +174,10 @@ det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA, int t
  * nothing (no cudaMalloc, no allocating library routine).
  *
  * Limits and sharing:
- *  - A shape whose split plan needs more than 64 MiB (detgemm_workspace_bytes
- *    above 67,108,864) is refused with DET_ERR_WORKSPACE; nothing is launched.
- *    Shapes that need no scratch always run.
+ *  - A shape whose split plan needs more than 64 MiB (a split-K workspace
+ *    above 67,108,864 bytes) is refused with DET_ERR_WORKSPACE; nothing is
+ *    launched. A transposed copy of A that needs more than 64 MiB is skipped
+ *    (A is read in place). Shapes that need no scratch always run.
  *  - Every call on a device shares the one array, which keeps the previous
  *    call's contents. A call writes every scratch element it reads, so no
  *    clearing is needed, but calls whose kernels overlap on the GPU (two

@@ -82,10 +82,24 @@ def test_split_plan_is_used_where_it_helps(dev):
     # few tiles and many chunks: the weight-gradient shapes split K
     assert detlib.detgemm_workspace_bytes(768, 2304, 8192, True, False) > 0
     assert detlib.detgemm_workspace_bytes(2048, 768, 8192, True, False) > 0
-    # plenty of tiles: the LM head does not
-    assert detlib.detgemm_workspace_bytes(8192, 50257, 768, False, True) == 0
-    # one chunk: nothing to split
+    # plenty of tiles: the LM head does not split, but reads a transposed copy
+    # of X (768 x 8192 floats) from the workspace
+    assert detlib.detgemm_workspace_bytes(8192, 50257, 768, False, True) == 768 * 8192 * 4
+    # ... which an m-contiguous A does not need
+    assert detlib.detgemm_workspace_bytes(8192, 50257, 768, True, True) == 0
+    # one chunk and a small product: neither
     assert detlib.detgemm_workspace_bytes(64, 64, 256) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(517, 6000, 700), (1000, 4000, 600)])
+@pytest.mark.parametrize("transB", [0, 1])
+def test_transposed_a_copy_same_bits(dev, M, N, K, transB):
+    # large enough that a k-contiguous A is copied transposed into the
+    # workspace (row stride M rounded up to 4 floats); ragged M and K
+    assert detlib.detgemm_workspace_bytes(M, N, K, False, transB) == K * ((M + 3) // 4 * 4) * 4
+    run_case(M, N, K, False, bool(transB), "padded", "padded", "padded", M + K + transB)
+    run_case(M, N, K, False, bool(transB), "dense", "offset", "offset", M + K + transB + 1,
+             wide=True)
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 200, 1300), (129, 77, 2049), (512, 384, 4096),

@@ -19,6 +19,7 @@ CASES = [
     (512, 384, 4096, True, False),
     (129, 77, 2049, False, True),
     (64, 64, 256, False, False),     # one chunk: no scratch needed
+    (517, 6000, 700, False, True),   # A copied transposed into the scratch
 ]
 
 
@@ -48,3 +49,19 @@ def test_noalloc_refuses_shapes_beyond_its_scratch():
     with pytest.raises(detlib.DetError) as err:
         detlib.detgemm_f32_noalloc(A, B, C, transA=True)
     assert err.value.status == 5      # DET_ERR_WORKSPACE
+
+
+def test_noalloc_skips_a_transposed_copy_beyond_its_scratch():
+    need_gpu()
+    # the copy of A would take 24,576 x 768 floats (75 MB): A is read in place
+    M, N, K = 24576, 2048, 768
+    assert detlib.detgemm_workspace_bytes(M, N, K, False, False) > 64 * 2 ** 20
+    rng = np.random.default_rng(77)
+    A = rng.standard_normal((M, K)).astype(F)
+    B = rng.standard_normal((K, N)).astype(F)
+    Ad, Bd = to_dev(A), to_dev(B)
+    ref = host(detlib.detgemm_f32(Ad, Bd, workspace=detlib.gemm_workspace(M, N, K)))
+    C = empty_dev(M, N)
+    detlib.detgemm_f32_noalloc(Ad, Bd, C)
+    torch.cuda.synchronize()
+    assert_bitwise(host(C), ref, "no-alloc without the transposed copy")
