@@ -264,28 +264,38 @@ def run_ours(args, rank, world, local_rank):
     gemm_flops_dw = [inputs.flops_gemm(*gemm_dims(p)) for p in dw]
     gemm_flops = sum(gemm_flops_fwd) + sum(gemm_flops_dw)
     lm_idx = [p["name"] for p in fwd].index("lm_head")
-    # one launch per GEMM, plus the split-K second pass where a workspace is used
-    # rmsnorm; one launch per GEMM plus the split-K second pass where a
-    # workspace is used; xent + mean; the RMSNorm backward's two; the shard
-    # sum; AdamW
-    # one block forward: 2 RMSNorms, 5 GEMMs (+ split passes), RoPE, 3 launches
-    # an attention head (QK^T, softmax, PV + its split pass), 2 adds, SwiGLU
-    n_heads_total = bc["batch"] * inputs.N_HEADS
-    pv_split = detlib.detgemm_workspace_bytes(bc["seq"], 64, bc["seq"]) > 0
-    block_launches = (2 + 5 + sum(v is not None for v in blk.ws.values()) + 1
-                      + n_heads_total * (3 + int(pv_split)) + 2 + 1)
+    # A GEMM is one launch, plus one where it uses its workspace (the split-K
+    # second pass, or the transposed copy of A). Attention is 3 launches a
+    # group of heads forward and 7 backward. Checked against an ncu launch
+    # list of one step.
+    def gemm_n(ws):
+        return 1 + int(ws is not None)
+
+    def attn_groups_count(batch, seq, heads):
+        per_head, cap = seq * seq * 4, 1 << 30
+        if heads * per_head <= cap:
+            fit = max(1, min(cap // (heads * per_head), (1 << 20) // heads))
+            gb = -(-batch // -(-batch // fit))
+            return -(-batch // gb)
+        fit = max(1, cap // per_head)
+        gh = -(-heads // -(-heads // fit))
+        return batch * -(-heads // gh)
+
+    # one block forward: 2 RMSNorms, 5 GEMMs, RoPE, attention, 2 adds, SwiGLU
+    g162 = attn_groups_count(bc["batch"], bc["seq"], inputs.N_HEADS)
+    block_launches = (2 + sum(gemm_n(blk.ws[k]) for k in ("qkv", "o", "ff", "ff", "down"))
+                      + 1 + 3 * g162 + 2 + 1)
     # the byte-level LM step: the embedding, 2 forward blocks (11 launches and
-    # 3 a head), the head GEMM, the cross-entropy and its mean, the head's two
-    # backward GEMMs, 2 backward blocks (18 launches and 7 a head, plus split
-    # passes), the embedding backward, and one AdamW launch per parameter
-    # tensor (2 + 7 a block); checked against an ncu launch list of one step
-    nb, nh = len(bl["blocks"]), bl["batch"] * bl["heads"]
-    hd_b = bl["d"] // bl["heads"]
-    pv_b = int(detlib.detgemm_workspace_bytes(bl["seq"], hd_b, bl["seq"]) > 0)
-    byte_lm_launches = (1 + nb * (11 + nh * (3 + pv_b)) + 1 + 2 + 2
-                        + nb * (18 + nh * (7 + 3 * pv_b)) + 1 + 2 + 7 * nb)
-    launches_per_step = (1 + len(fwd) + sum(w is not None for w in ws_fwd) + 2 + 2 + len(dw)
-                         + sum(w is not None for w in ws_dw) + 1 + block_launches
+    # the attention), the head GEMM, the cross-entropy and its mean, the head's
+    # two backward GEMMs, 2 backward blocks (18 launches and the attention's
+    # backward), the embedding backward, and one AdamW launch per parameter
+    # tensor (2 + 7 a block); no GEMM of this step uses a workspace
+    nb = len(bl["blocks"])
+    gb = attn_groups_count(bl["batch"], bl["seq"], bl["heads"])
+    byte_lm_launches = (1 + nb * (11 + 3 * gb) + 1 + 2 + 2
+                        + nb * (18 + 7 * gb) + 1 + 2 + 7 * nb)
+    launches_per_step = (1 + sum(gemm_n(w) for w in ws_fwd) + 2 + 2
+                         + sum(gemm_n(w) for w in ws_dw) + 1 + block_launches
                          + byte_lm_launches + 1)
 
     segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "rmsnorm_bwd", "gemm_dw",

@@ -37,7 +37,8 @@ class Block:
         ws = lambda M, N, K: detlib.gemm_workspace(M, N, K, False, False, device=device)  # noqa: E731
         self.ws = {"qkv": ws(n, 3 * d_model, d_model), "o": ws(n, d_model, d_model),
                    "ff": ws(n, d_ff, d_model), "down": ws(n, d_model, d_ff)}
-        self.att_ws = e((detlib.detattention_workspace_bytes(seq, self.hd) + 3) // 4)
+        self.att_ws = e((detlib.detattention_workspace_bytes(batch, seq, heads, self.hd) + 3)
+                        // 4)
 
     def flops(self):
         n, D, Fd = self.B * self.T, self.D, self.Fd

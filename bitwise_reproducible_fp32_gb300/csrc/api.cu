@@ -319,26 +319,119 @@ DET_API det_status detcos_f32(const det_profile_v1 *prof, int64_t n, const float
     return from_cuda(launch_sincos_map(n, x, y, 1, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-// Causal attention over one packed QKV activation: for every sequence b and
-// head h, S = Q_bh K_bh^T (profile GEMM), P = the causal softmax of S * scale,
-// O_bh = P V_bh (profile GEMM), each head one after the other through one
-// seq x seq score buffer in the workspace.
+// Causal attention over one packed QKV activation, a group of heads at a time:
+// S = Q_z K_z^T (profile GEMM) for every head z of the group in one batched
+// launch, skipping the score tiles above the diagonal that the softmax masks;
+// P = the causal softmax of S * scale over all the group's rows in one launch;
+// O_z = P_z V_z (profile GEMM) in one batched launch. Each head's bits are
+// those of its separate products.
 namespace {
-size_t attention_ws(int64_t seq, int64_t head_dim, size_t *gemm_ws) {
-    *gemm_ws = gemm_plan(seq, head_dim, seq, sm_count_current_device(), true).workspace_bytes;
-    return (size_t(seq) * size_t(seq) * 4 + 255) / 256 * 256 + *gemm_ws;
+// Heads go in groups whose score buffers together stay within 1 GiB: whole
+// sequences (all heads of gb sequences) when one sequence fits, else gh heads
+// of one sequence; groups are balanced in size.
+constexpr size_t kAttnScoreCap = size_t(1) << 30;
+struct AttnGroups {
+    int64_t gb, gh;       // sequences and heads a group spans (gb > 1 only when gh == heads)
+    size_t score_bytes;   // one score buffer of the largest group, 256-byte rounded
+};
+AttnGroups attention_groups(int64_t batch, int64_t seq, int64_t heads) {
+    const size_t per_head = size_t(seq) * size_t(seq) * 4;
+    AttnGroups g{};
+    if (size_t(heads) * per_head <= kAttnScoreCap) {
+        // (at most 2^20 products a group, so the launch's unit count fits an int)
+        const int64_t fit = std::max<int64_t>(
+            1, std::min<int64_t>(int64_t(kAttnScoreCap / (size_t(heads) * per_head)),
+                                 (int64_t(1) << 20) / heads));
+        const int64_t ngroups = (std::max<int64_t>(batch, 1) + fit - 1) / fit;
+        g.gb = (std::max<int64_t>(batch, 1) + ngroups - 1) / ngroups;
+        g.gh = heads;
+    } else {
+        const int64_t fit = std::max<int64_t>(1, int64_t(kAttnScoreCap / per_head));
+        const int64_t ngroups = (heads + fit - 1) / fit;
+        g.gb = 1;
+        g.gh = (heads + ngroups - 1) / ngroups;
+    }
+    g.score_bytes = (size_t(g.gb * g.gh) * per_head + 255) / 256 * 256;
+    return g;
+}
+
+// Walks the groups: f(b0, nb, h0, nh) for sequences b0 .. b0+nb-1 and heads
+// h0 .. h0+nh-1; stops at the first error.
+template <typename F>
+cudaError_t for_each_group(int64_t batch, int64_t heads, const AttnGroups &g, F f) {
+    for (int64_t b0 = 0; b0 < batch; b0 += g.gb)
+        for (int64_t h0 = 0; h0 < heads; h0 += g.gh) {
+            const cudaError_t e = f(b0, std::min(g.gb, batch - b0), h0, std::min(g.gh, heads - h0));
+            if (e != cudaSuccess) return e;
+        }
+    return cudaSuccess;
+}
+
+// One operand of the heads of a group inside a packed [batch * seq, ld]
+// buffer: the group's first head at column col0, sequence stride seq * ld,
+// head stride head_dim; the map spans the rest of the buffer.
+struct HeadOperand {
+    const float *base;
+    int64_t ld, rows, cols, zb, zh;
+};
+HeadOperand head_operand(const float *buf, int64_t ld, int64_t width, int64_t batch,
+                         int64_t seq, int64_t b0, int64_t col0, int64_t head_dim) {
+    HeadOperand o;
+    o.base = buf + b0 * seq * ld + col0;
+    o.ld = ld;
+    o.rows = (batch - b0) * seq;
+    o.cols = width - col0;
+    o.zb = seq * ld;
+    o.zh = head_dim;
+    return o;
+}
+
+// One batched profile GEMM over the products of a group: op(A) from a, op(B)
+// from b, C at c (base pointer, ldc, per-product strides).
+cudaError_t group_gemm(int64_t M, int64_t N, int64_t K, const HeadOperand &a, int tA,
+                       const HeadOperand &b, int tB, float *c, int64_t ldc, int64_t c_zb,
+                       int64_t c_zh, int64_t count, int64_t inner, int causal,
+                       cudaStream_t s) {
+    GemmArgs g;
+    g.M = M; g.N = N; g.K = K;
+    g.A = a.base; g.lda = a.ld; g.B = b.base; g.ldb = b.ld; g.C = c; g.ldc = ldc;
+    g.transA = tA; g.transB = tB;
+    GemmBatch bt;
+    bt.count = count; bt.inner = inner;
+    bt.a_zb = a.zb; bt.a_zh = a.zh; bt.b_zb = b.zb; bt.b_zh = b.zh;
+    bt.c_zb = c_zb; bt.c_zh = c_zh;
+    bt.a_rows = a.rows; bt.a_cols = a.cols; bt.b_rows = b.rows; bt.b_cols = b.cols;
+    bt.causal = causal;
+    return launch_gemm_batched(g, bt, s);
+}
+
+// The group's stacked seq x seq buffers (product z at rows z * seq) as an
+// operand.
+HeadOperand stacked(const float *buf, int64_t seq, int64_t nh, int64_t count) {
+    HeadOperand o;
+    o.base = buf;
+    o.ld = seq;
+    o.rows = count * seq;
+    o.cols = seq;
+    o.zb = nh * seq * seq;
+    o.zh = seq * seq;
+    return o;
+}
+
+bool attention_args_ok(int64_t batch, int64_t seq, int64_t heads, int64_t head_dim) {
+    return batch >= 0 && seq >= 1 && seq <= 65536 && heads >= 1 && heads <= 65536 &&
+           head_dim >= 1 && head_dim <= 65536 && batch <= kDimMax / seq &&
+           heads * head_dim <= kDimMax / 3;
 }
 }  // namespace
 
-DET_API det_status detattention_workspace_bytes(const det_profile_v1 *prof, int64_t seq,
-                                                int64_t head_dim, size_t *bytes) {
+DET_API det_status detattention_workspace_bytes(const det_profile_v1 *prof, int64_t batch,
+                                                int64_t seq, int64_t heads, int64_t head_dim,
+                                                size_t *bytes) {
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
-    if (!bytes || seq < 1 || seq > 65536 || head_dim < 1 || head_dim > 65536)
-        return DET_ERR_INVALID_ARG;
-    if ((st = check_device()) != DET_OK) return st;
-    size_t g = 0;
-    *bytes = attention_ws(seq, head_dim, &g);
+    if (!bytes || !attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
+    *bytes = attention_groups(batch, seq, heads).score_bytes;
     return DET_OK;
 }
 
@@ -349,68 +442,51 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
                                     det_stream_t stream) {
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
-    if (batch < 0 || seq < 1 || seq > 65536 || heads < 1 || head_dim < 1 || head_dim > 65536 ||
-        heads > 65536)
-        return DET_ERR_INVALID_ARG;
+    if (!attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
     if (batch == 0) return DET_OK;
-    if (!qkv || !out || ldqkv < 3 * heads * head_dim || ldout < heads * head_dim)
-        return DET_ERR_INVALID_ARG;
-    if ((st = check_device()) != DET_OK) return st;
-    size_t gws = 0;
-    const size_t need = attention_ws(seq, head_dim, &gws);
-    if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
-        return DET_ERR_WORKSPACE;
-    float *scores = static_cast<float *>(workspace);
-    void *pv_ws = gws ? static_cast<char *>(workspace) + (need - gws) : nullptr;
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t hd = heads * head_dim;
-    for (int64_t b = 0; b < batch; ++b) {
-        const float *base = qkv + b * seq * ldqkv;
-        for (int64_t h = 0; h < heads; ++h) {
-            GemmArgs qk;
-            qk.M = seq; qk.N = seq; qk.K = head_dim;
-            qk.A = base + h * head_dim; qk.lda = ldqkv;
-            qk.B = base + hd + h * head_dim; qk.ldb = ldqkv;
-            qk.C = scores; qk.ldc = seq;
-            qk.transA = 0; qk.transB = 1;
-            cudaError_t e = launch_gemm(qk, nullptr, 0, s);
-            if (e == cudaSuccess)
-                e = launch_softmax_causal(seq, seq, scores, seq, scale, 0, seq, scores, seq, s);
-            if (e != cudaSuccess) return DET_ERR_CUDA;
-            GemmArgs pv;
-            pv.M = seq; pv.N = head_dim; pv.K = seq;
-            pv.A = scores; pv.lda = seq;
-            pv.B = base + 2 * hd + h * head_dim; pv.ldb = ldqkv;
-            pv.C = out + b * seq * ldout + h * head_dim; pv.ldc = ldout;
-            pv.transA = 0; pv.transB = 0;
-            if (launch_gemm(pv, pv_ws, gws, s) != cudaSuccess) return DET_ERR_CUDA;
-        }
-    }
-    return DET_OK;
+    if (!qkv || !out || ldqkv < 3 * hd || ldout < hd) return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    const AttnGroups g = attention_groups(batch, seq, heads);
+    if (!workspace || workspace_bytes < g.score_bytes ||
+        reinterpret_cast<uintptr_t>(workspace) % 256)
+        return DET_ERR_WORKSPACE;
+    float *S = static_cast<float *>(workspace);
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = for_each_group(batch, heads, g, [&](int64_t b0, int64_t nb, int64_t h0,
+                                                              int64_t nh) {
+        const int64_t count = nb * nh;
+        const HeadOperand Q = head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, h0 * head_dim, head_dim);
+        const HeadOperand K = head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, hd + h0 * head_dim, head_dim);
+        const HeadOperand V = head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, 2 * hd + h0 * head_dim, head_dim);
+        const HeadOperand P = stacked(S, seq, nh, count);
+        cudaError_t r = group_gemm(seq, seq, head_dim, Q, 0, K, 1, S, seq, P.zb, P.zh, count, nh,
+                                   1, s);
+        if (r == cudaSuccess)
+            r = launch_softmax_causal(count * seq, seq, S, seq, scale, 0, seq, S, seq, s);
+        if (r == cudaSuccess)
+            r = group_gemm(seq, head_dim, seq, P, 0, V, 0, out + b0 * seq * ldout + h0 * head_dim,
+                           ldout, seq * ldout, head_dim, count, nh, 0, s);
+        return r;
+    });
+    return from_cuda(e);
 }
 
-// Backward of detattention_f32, head after head: P is recomputed by the
-// forward's spelling (S = Q K^T, the causal softmax), then
+// Backward of detattention_f32, a group of heads at a time: P is recomputed
+// by the forward's spelling (S = Q K^T, the causal softmax), then
 //   dP = dO V^T, dV = P^T dO, dS = the softmax backward of (P, dP),
 //   dQ = dS K, dK = dS^T Q
-// with detgemm_f32's arithmetic for every product. The gradients are those of
-// the Q, K and V that the forward read (after any rotary embedding).
-namespace {
-size_t attention_bwd_ws(int64_t seq, int64_t head_dim, size_t *gemm_ws) {
-    *gemm_ws = gemm_plan(seq, head_dim, seq, sm_count_current_device(), true).workspace_bytes;
-    return 2 * ((size_t(seq) * size_t(seq) * 4 + 255) / 256 * 256) + *gemm_ws;
-}
-}  // namespace
-
-DET_API det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t seq,
+// each one batched launch over the group, with detgemm_f32's arithmetic for
+// every product (the score products skip the tiles the softmax masks). The
+// gradients are those of the Q, K and V that the forward read (after any
+// rotary embedding).
+DET_API det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t batch,
+                                                    int64_t seq, int64_t heads,
                                                     int64_t head_dim, size_t *bytes) {
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
-    if (!bytes || seq < 1 || seq > 65536 || head_dim < 1 || head_dim > 65536)
-        return DET_ERR_INVALID_ARG;
-    if ((st = check_device()) != DET_OK) return st;
-    size_t g = 0;
-    *bytes = attention_bwd_ws(seq, head_dim, &g);
+    if (!bytes || !attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
+    *bytes = 2 * attention_groups(batch, seq, heads).score_bytes;
     return DET_OK;
 }
 
@@ -422,56 +498,52 @@ DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batc
                                         det_stream_t stream) {
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
-    if (batch < 0 || seq < 1 || seq > 65536 || heads < 1 || head_dim < 1 || head_dim > 65536 ||
-        heads > 65536)
-        return DET_ERR_INVALID_ARG;
+    if (!attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
     if (batch == 0) return DET_OK;
     const int64_t hd = heads * head_dim;
     if (!qkv || !dout || !dqkv || ldqkv < 3 * hd || lddout < hd || lddqkv < 3 * hd)
         return DET_ERR_INVALID_ARG;
     if ((st = check_device()) != DET_OK) return st;
-    size_t gws = 0;
-    const size_t need = attention_bwd_ws(seq, head_dim, &gws);
-    if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+    const AttnGroups g = attention_groups(batch, seq, heads);
+    if (!workspace || workspace_bytes < 2 * g.score_bytes ||
+        reinterpret_cast<uintptr_t>(workspace) % 256)
         return DET_ERR_WORKSPACE;
-    const size_t tt = (size_t(seq) * size_t(seq) * 4 + 255) / 256 * 256;
-    float *P = static_cast<float *>(workspace);
-    float *dP = reinterpret_cast<float *>(static_cast<char *>(workspace) + tt);
-    void *gw = gws ? static_cast<char *>(workspace) + 2 * tt : nullptr;
+    float *Pb = static_cast<float *>(workspace);
+    float *dPb = reinterpret_cast<float *>(static_cast<char *>(workspace) + g.score_bytes);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    auto gemm = [&](int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, int tA,
-                    const float *B, int64_t ldb, int tB, float *C, int64_t ldc, bool ws) {
-        GemmArgs a;
-        a.M = M; a.N = N; a.K = K; a.A = A; a.lda = lda; a.B = B; a.ldb = ldb;
-        a.C = C; a.ldc = ldc; a.transA = tA; a.transB = tB;
-        return launch_gemm(a, ws ? gw : nullptr, ws ? gws : 0, s);
-    };
-    for (int64_t b = 0; b < batch; ++b) {
-        const float *base = qkv + b * seq * ldqkv;
-        const float *dob = dout + b * seq * lddout;
-        float *dbase = dqkv + b * seq * lddqkv;
-        for (int64_t h = 0; h < heads; ++h) {
-            const float *Q = base + h * head_dim, *K = base + hd + h * head_dim;
-            const float *V = base + 2 * hd + h * head_dim, *dO = dob + h * head_dim;
-            float *dQ = dbase + h * head_dim, *dK = dbase + hd + h * head_dim;
-            float *dV = dbase + 2 * hd + h * head_dim;
-            cudaError_t e = gemm(seq, seq, head_dim, Q, ldqkv, 0, K, ldqkv, 1, P, seq, false);
-            if (e == cudaSuccess)
-                e = launch_softmax_causal(seq, seq, P, seq, scale, 0, seq, P, seq, s);
-            if (e == cudaSuccess)
-                e = gemm(seq, seq, head_dim, dO, lddout, 0, V, ldqkv, 1, dP, seq, false);
-            if (e == cudaSuccess)
-                e = gemm(seq, head_dim, seq, P, seq, 1, dO, lddout, 0, dV, lddqkv, true);
-            if (e == cudaSuccess)
-                e = launch_softmax_causal_bwd(seq, seq, P, dP, seq, scale, 0, seq, dP, seq, s);
-            if (e == cudaSuccess)
-                e = gemm(seq, head_dim, seq, dP, seq, 0, K, ldqkv, 0, dQ, lddqkv, true);
-            if (e == cudaSuccess)
-                e = gemm(seq, head_dim, seq, dP, seq, 1, Q, ldqkv, 0, dK, lddqkv, true);
-            if (e != cudaSuccess) return DET_ERR_CUDA;
-        }
-    }
-    return DET_OK;
+    const cudaError_t e = for_each_group(batch, heads, g, [&](int64_t b0, int64_t nb, int64_t h0,
+                                                              int64_t nh) {
+        const int64_t count = nb * nh;
+        auto in = [&](const float *buf, int64_t ld, int64_t width, int64_t col) {
+            return head_operand(buf, ld, width, batch, seq, b0, col + h0 * head_dim, head_dim);
+        };
+        const HeadOperand Q = in(qkv, ldqkv, 3 * hd, 0), K = in(qkv, ldqkv, 3 * hd, hd);
+        const HeadOperand V = in(qkv, ldqkv, 3 * hd, 2 * hd), dO = in(dout, lddout, hd, 0);
+        const HeadOperand P = stacked(Pb, seq, nh, count), dP = stacked(dPb, seq, nh, count);
+        float *dbase = dqkv + b0 * seq * lddqkv + h0 * head_dim;
+        const int64_t dzb = seq * lddqkv;
+        cudaError_t r = group_gemm(seq, seq, head_dim, Q, 0, K, 1, Pb, seq, P.zb, P.zh, count,
+                                   nh, 1, s);
+        if (r == cudaSuccess)
+            r = launch_softmax_causal(count * seq, seq, Pb, seq, scale, 0, seq, Pb, seq, s);
+        if (r == cudaSuccess)
+            r = group_gemm(seq, seq, head_dim, dO, 0, V, 1, dPb, seq, dP.zb, dP.zh, count, nh, 1,
+                           s);
+        if (r == cudaSuccess)   // dV = P^T dO
+            r = group_gemm(seq, head_dim, seq, P, 1, dO, 0, dbase + 2 * hd, lddqkv, dzb,
+                           head_dim, count, nh, 0, s);
+        if (r == cudaSuccess)   // dS in place of dP
+            r = launch_softmax_causal_bwd(count * seq, seq, Pb, dPb, seq, scale, 0, seq, dPb, seq,
+                                          s);
+        if (r == cudaSuccess)   // dQ = dS K
+            r = group_gemm(seq, head_dim, seq, dP, 0, K, 0, dbase, lddqkv, dzb, head_dim, count,
+                           nh, 0, s);
+        if (r == cudaSuccess)   // dK = dS^T Q
+            r = group_gemm(seq, head_dim, seq, dP, 1, Q, 0, dbase + hd, lddqkv, dzb, head_dim,
+                           count, nh, 0, s);
+        return r;
+    });
+    return from_cuda(e);
 }
 
 DET_API det_status detshardsum_f32(const det_profile_v1 *prof, int64_t nshards, int64_t n,

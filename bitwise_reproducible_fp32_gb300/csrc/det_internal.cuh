@@ -48,6 +48,20 @@ struct GemmPlan {
 GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor);
 cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_bytes,
                         cudaStream_t s);
+// A batch of products of one shape. Product z = zb * inner + zh (z < count)
+// reads op(A) at A + zb * a_zb + zh * a_zh, op(B) likewise, and writes C at
+// C + zb * c_zb + zh * c_zh. The A and B buffers are a_rows x a_cols and
+// b_rows x b_cols as stored (row strides lda, ldb), and every product's
+// operand lies inside them. causal: only the tiles holding an output with
+// j <= i are computed (the rest of C is left unwritten). Never split; the
+// bits of each product are detgemm_f32's.
+struct GemmBatch {
+    int64_t count = 1, inner = 1;
+    int64_t a_zb = 0, a_zh = 0, b_zb = 0, b_zh = 0, c_zb = 0, c_zh = 0;
+    int64_t a_rows = 0, a_cols = 0, b_rows = 0, b_cols = 0;
+    int causal = 0;
+};
+cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s);
 cudaError_t gemm_watchdog(unsigned int *code, int clear);
 cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s);
 

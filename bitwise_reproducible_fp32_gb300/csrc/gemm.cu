@@ -110,7 +110,27 @@ struct KArgs {
     int kt_per_unit;   // multiple of the k-tiles a chunk spans
     float4 *W;
     int accumulate;    // C = C + result (beta = 1): one rounded add, C on the left
+    // Batched products (never split): product z = zb * zinner + zh reads its
+    // operands and writes C at element offsets zb * X_zb + zh * X_zh from the
+    // base pointers; one tensor map spans each whole buffer and a TMA
+    // coordinate adds the offset's row (offset / ld) and column (offset % ld).
+    int zcount;        // 1: a single product
+    int zinner;
+    int64_t a_zb, a_zh, b_zb, b_zh, c_zb, c_zh;
+    // Causal: only the tiles holding some output with j <= i are computed
+    // (row-major over those tiles); the others are left unwritten.
+    int causal;
+    int live_tiles;    // tiles computed per product
 };
+
+__device__ __forceinline__ int64_t z_offset(int64_t zb_stride, int64_t zh_stride, int z,
+                                            int zinner) {
+    return int64_t(z / zinner) * zb_stride + int64_t(z % zinner) * zh_stride;
+}
+
+// Causal tile rows: tile row mb holds rows mb*BM .. mb*BM + BM - 1, so its
+// tiles nb with nb*BN <= mb*BM + BM - 1 hold an output with j <= i.
+__device__ __forceinline__ int causal_row_tiles(int mb, int nt);
 
 // Workspace layout of split mode: float4 slot of (chunk c, tile t, accumulator
 // quad q of the thread, thread tid), consecutive threads adjacent so each
@@ -358,33 +378,49 @@ __device__ __forceinline__ void load_tile_plain(float *dst, const float *src,
 }
 
 // Issues the TMA loads of k-tile kt of the tile at (m0, n0) into stage `st`.
+// (ar, ac), (br, bc): the row and column of the product's operands within
+// the buffers the tensor maps span (0 for a single product).
 template <bool A_KM, bool B_KM>
 __device__ __forceinline__ void issue_stage(float *st, uint64_t *bar_ptr,
                                             const CUtensorMap *tmA, const CUtensorMap *tmB,
-                                            int m0, int n0, int kt) {
+                                            int m0, int n0, int kt, int ar, int ac, int br,
+                                            int bc) {
     const uint32_t bar = smem_u32(bar_ptr);
     mbar_arrive_expect_tx(bar, STAGE_FLOATS * 4);
     const int k0 = kt * BK;
-    if (A_KM) tma_load_2d(smem_u32(st), tmA, k0, m0, bar);
-    else      tma_load_2d(smem_u32(st), tmA, m0, k0, bar);
-    if (B_KM) tma_load_2d(smem_u32(st + A_FLOATS), tmB, k0, n0, bar);
-    else      tma_load_2d(smem_u32(st + A_FLOATS), tmB, n0, k0, bar);
+    if (A_KM) tma_load_2d(smem_u32(st), tmA, ac + k0, ar + m0, bar);
+    else      tma_load_2d(smem_u32(st), tmA, ac + m0, ar + k0, bar);
+    if (B_KM) tma_load_2d(smem_u32(st + A_FLOATS), tmB, bc + k0, br + n0, bar);
+    else      tma_load_2d(smem_u32(st + A_FLOATS), tmB, bc + n0, br + k0, bar);
 }
 
 // Unit u: tiles run fastest, so concurrent CTAs share one k range (and, for
 // the tiles, the smaller operand's blocks), keeping the working set in L2.
 struct Unit {
-    int t, m0, n0, kt0, kt1;
+    int t, m0, n0, kt0, kt1, z;
 };
 
+__device__ __forceinline__ int causal_row_tiles(int mb, int nt) {
+    return min(nt, (mb * BM + BM - 1) / BN + 1);
+}
+
 __device__ __forceinline__ Unit unit_of(const KArgs &p, int u, int nkt) {
-    const int ntiles = p.mt * p.nt;
+    const int ntiles = p.live_tiles;
+    const int per_z = ntiles * p.units_per_tile;
+    const int z = u / per_z;
+    u -= z * per_z;
     const int t = u % ntiles, g = u / ntiles;
     int mb, nb;
-    if (p.m_fast) { mb = t % p.mt; nb = t / p.mt; }
-    else          { nb = t % p.nt; mb = t / p.nt; }
+    if (p.causal) {
+        mb = 0;
+        int first = 0;
+        while (first + causal_row_tiles(mb, p.nt) <= t) first += causal_row_tiles(mb++, p.nt);
+        nb = t - first;
+    } else if (p.m_fast) { mb = t % p.mt; nb = t / p.mt; }
+    else                 { nb = t % p.nt; mb = t / p.nt; }
     Unit w;
     w.t = t;
+    w.z = z;
     w.m0 = mb * BM;
     w.n0 = nb * BN;
     w.kt0 = g * p.kt_per_unit;
@@ -469,14 +505,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int arow = A_KM ? wm * WTM + lm : wm * WTM + lm * 4;
     const int bcol = B_KM ? wn * 32 + ln : wn * 32 + ln * 4;
 
-    const int nunits = p.mt * p.nt * p.units_per_tile;
+    const int nunits = p.live_tiles * p.units_per_tile * p.zcount;
     const int my_units = (nunits - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);
     const int nkt = (p.K + BK - 1) / BK;
 
     // producer (thread 0): issues the next k-tile of its unit sequence into a slot
     auto issue_next = [&](int slot) {
+        int ar = 0, ac = 0, br = 0, bc = 0;
+        if (p.zcount > 1) {
+            const int64_t ao = z_offset(p.a_zb, p.a_zh, prod.u.z, p.zinner);
+            const int64_t bo = z_offset(p.b_zb, p.b_zh, prod.u.z, p.zinner);
+            ar = int(ao / p.lda); ac = int(ao % p.lda);
+            br = int(bo / p.ldb); bc = int(bo % p.ldb);
+        }
         issue_stage<A_KM, B_KM>(stages + slot * STAGE_FLOATS, &full[slot], &tmA, &tmB,
-                                prod.u.m0, prod.u.n0, prod.kt);
+                                prod.u.m0, prod.u.n0, prod.kt, ar, ac, br, bc);
         ++prod.count;
         if (++prod.kt == prod.u.kt1) {
             if (++prod.ui < my_units) {
@@ -527,9 +570,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                                         &abort_flag);
             } else {
                 __syncthreads();   // everyone is done with the previous k-tile
-                load_tile_plain<A_KM, BM>(stages, p.A, p.lda, p.M, p.K, w.m0, kt * BK, tid);
-                load_tile_plain<B_KM, BN>(stages + A_FLOATS, p.B, p.ldb, p.N, p.K, w.n0,
-                                          kt * BK, tid);
+                load_tile_plain<A_KM, BM>(stages, p.A + z_offset(p.a_zb, p.a_zh, w.z, p.zinner),
+                                          p.lda, p.M, p.K, w.m0, kt * BK, tid);
+                load_tile_plain<B_KM, BN>(stages + A_FLOATS,
+                                          p.B + z_offset(p.b_zb, p.b_zh, w.z, p.zinner), p.ldb,
+                                          p.N, p.K, w.n0, kt * BK, tid);
                 __syncthreads();
             }
             if (ok) {
@@ -608,7 +653,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (aborted) break;
         // epilogue (the next unit's loads are already in flight)
         if (!SPLIT)
-            store_tile<A_KM, B_KM>(acc, p.C, p.ldc, p.M, p.N, w.m0, w.n0, arow, bcol,
+            store_tile<A_KM, B_KM>(acc, p.C + z_offset(p.c_zb, p.c_zh, w.z, p.zinner), p.ldc,
+                                   p.M, p.N, w.m0, w.n0, arow, bcol,
                                    p.vec_store, p.accumulate);
     }
 
@@ -733,7 +779,7 @@ cudaError_t launch_variant(const CUtensorMap &ma, const CUtensorMap &mb, const K
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    const int64_t units = int64_t(k.mt) * k.nt * k.units_per_tile;
+    const int64_t units = int64_t(k.live_tiles) * k.units_per_tile * k.zcount;
     const unsigned grid = unsigned(std::min<int64_t>(units, sm_count_current_device()));
     kern<<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, k);
     return cudaGetLastError();
@@ -897,6 +943,11 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
     k.kt_per_unit = pl.kt_per_unit;
     k.W = static_cast<float4 *>(pl.split ? workspace : nullptr);
     k.accumulate = a.accumulate;
+    k.zcount = 1;
+    k.zinner = 1;
+    k.a_zb = k.a_zh = k.b_zb = k.b_zh = k.c_zb = k.c_zh = 0;
+    k.causal = 0;
+    k.live_tiles = k.mt * k.nt;
     // op(A) is k-contiguous when A is not transposed; op(B) when B is.
     const bool a_km = !a.transA, b_km = a.transB != 0;
     CUtensorMap ma{}, mb{};
@@ -914,6 +965,62 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((slots + 255) / 256, int64_t(sms) * 8));
     chunk_sum_kernel<<<unsigned(blocks), 256, 0, s>>>(k, pl.nchunks, a_km, b_km);
     return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s) {
+    if (bt.count == 0 || a.M == 0 || a.N == 0) return cudaSuccess;
+    if (a.K == 0) {
+        for (int64_t z = 0; z < bt.count; ++z) {
+            const int64_t zb = z / bt.inner, zh = z % bt.inner;
+            const int64_t total = a.M * a.N;
+            const int64_t blocks = std::min<int64_t>((total + 255) / 256, 152 * 32);
+            fill_zero_kernel<<<unsigned(blocks), 256, 0, s>>>(
+                a.C + zb * bt.c_zb + zh * bt.c_zh, a.ldc, a.M, a.N, a.accumulate);
+        }
+        return cudaGetLastError();
+    }
+    const int sms = sm_count_current_device();
+    KArgs k;
+    k.M = int(a.M); k.N = int(a.N); k.K = int(a.K);
+    k.lda = a.lda; k.ldb = a.ldb; k.ldc = a.ldc;
+    k.A = a.A; k.B = a.B; k.C = a.C;
+    k.mt = int((a.M + BM - 1) / BM);
+    k.nt = int((a.N + BN - 1) / BN);
+    k.m_fast = a.M <= a.N;
+    k.split = 0;
+    k.units_per_tile = 1;
+    k.kt_per_unit = int((a.K + BK - 1) / BK);
+    k.W = nullptr;
+    k.accumulate = a.accumulate;
+    k.zcount = int(bt.count);
+    k.zinner = int(bt.inner);
+    k.a_zb = bt.a_zb; k.a_zh = bt.a_zh;
+    k.b_zb = bt.b_zb; k.b_zh = bt.b_zh;
+    k.c_zb = bt.c_zb; k.c_zh = bt.c_zh;
+    k.causal = bt.causal;
+    int64_t live = int64_t(k.mt) * k.nt;
+    if (bt.causal) {
+        live = 0;
+        for (int mb = 0; mb < k.mt; ++mb)
+            live += std::min<int64_t>(k.nt, (int64_t(mb) * BM + BM - 1) / BN + 1);
+    }
+    k.live_tiles = int(live);
+    const bool off4 = bt.a_zb % 4 == 0 && bt.a_zh % 4 == 0 && bt.b_zb % 4 == 0 &&
+                      bt.b_zh % 4 == 0;
+    k.vec_store = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && (a.ldc % 4 == 0) &&
+                  bt.c_zb % 4 == 0 && bt.c_zh % 4 == 0;
+    const bool a_km = !a.transA, b_km = a.transB != 0;
+    CUtensorMap ma{}, mb{};
+    // one map spans each whole buffer; a product's tile coordinates add its
+    // offset's row and column, which TMA needs on a 16-byte boundary
+    bool tma = off4 && tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb) && bt.a_rows < (int64_t(1) << 31) &&
+               bt.b_rows < (int64_t(1) << 31);
+    if (tma) {
+        tma = make_map(&ma, a.A, bt.a_cols, bt.a_rows, a.lda, a_km, BM) &&
+              make_map(&mb, a.B, bt.b_cols, bt.b_rows, a.ldb, b_km, BN);
+    }
+    return tma ? launch_layout<true>(a_km, b_km, ma, mb, k, s)
+               : launch_layout<false>(a_km, b_km, ma, mb, k, s);
 }
 
 // ---------------------------------------------------------------- no-allocation variant

@@ -81,7 +81,8 @@ SIGNATURES = [
     ("detcos_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
     ("detattention_f32", _int, [_PROF, _i64, _i64, _i64, _i64, _vp, _i64, _f, _vp, _i64, _vp,
                                 ctypes.c_size_t, _vp]),
-    ("detattention_workspace_bytes", _int, [_PROF, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
+    ("detattention_workspace_bytes", _int, [_PROF, _i64, _i64, _i64, _i64,
+                                            ctypes.POINTER(ctypes.c_size_t)]),
     ("detswiglu_bwd_f32", _int, [_PROF, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("detsoftmax_causal_bwd_f32", _int, [_PROF, _i64, _i64, _vp, _vp, _i64, _f, _i64, _i64,
                                          _vp, _i64, _vp]),
@@ -89,7 +90,7 @@ SIGNATURES = [
     ("detembedding_bwd_f32", _int, [_PROF, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _i64, _vp]),
     ("detattention_bwd_f32", _int, [_PROF, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _f,
                                     _vp, _i64, _vp, ctypes.c_size_t, _vp]),
-    ("detattention_bwd_workspace_bytes", _int, [_PROF, _i64, _i64,
+    ("detattention_bwd_workspace_bytes", _int, [_PROF, _i64, _i64, _i64, _i64,
                                                 ctypes.POINTER(ctypes.c_size_t)]),
     ("det_watchdog_status", _int, [ctypes.POINTER(ctypes.c_int32), _int]),
 ]
@@ -434,10 +435,11 @@ def _sincos(x, y, profile, stream, fn):
     return y
 
 
-def detattention_workspace_bytes(seq, head_dim, profile=None) -> int:
+def detattention_workspace_bytes(batch, seq, heads, head_dim, profile=None) -> int:
     n = ctypes.c_size_t(0)
     _check("detattention_workspace_bytes",
-           load().detattention_workspace_bytes(_prof(profile), seq, head_dim, ctypes.byref(n)))
+           load().detattention_workspace_bytes(_prof(profile), batch, seq, heads, head_dim,
+                                               ctypes.byref(n)))
     return n.value
 
 
@@ -456,8 +458,9 @@ def detattention_f32(qkv, batch, seq, heads, head_dim, scale=None, out=None, wor
     if scale is None:
         scale = 1.0 / float(head_dim) ** 0.5
     if workspace is None:
-        workspace = torch.empty((detattention_workspace_bytes(seq, head_dim, profile) + 3) // 4,
-                                dtype=torch.float32, device=qkv.device)
+        workspace = torch.empty(
+            (detattention_workspace_bytes(batch, seq, heads, head_dim, profile) + 3) // 4,
+            dtype=torch.float32, device=qkv.device)
     st = load().detattention_f32(_prof(profile), batch, seq, heads, head_dim, _ptr(qkv),
                                  _ld(qkv), ctypes.c_float(scale), _ptr(out), _ld(out),
                                  _ptr(workspace), workspace.numel() * 4, _stream(stream))
@@ -524,10 +527,10 @@ def detembedding_bwd_f32(tokens, dx, vocab, de=None, profile=None, stream=None):
     return de
 
 
-def detattention_bwd_workspace_bytes(seq, head_dim, profile=None) -> int:
+def detattention_bwd_workspace_bytes(batch, seq, heads, head_dim, profile=None) -> int:
     n = ctypes.c_size_t(0)
     _check("detattention_bwd_workspace_bytes",
-           load().detattention_bwd_workspace_bytes(_prof(profile), seq, head_dim,
+           load().detattention_bwd_workspace_bytes(_prof(profile), batch, seq, heads, head_dim,
                                                    ctypes.byref(n)))
     return n.value
 
@@ -543,8 +546,9 @@ def detattention_bwd_f32(qkv, dout, batch, seq, heads, head_dim, scale=None, dqk
     if scale is None:
         scale = 1.0 / float(head_dim) ** 0.5
     if workspace is None:
-        workspace = torch.empty((detattention_bwd_workspace_bytes(seq, head_dim, profile) + 3)
-                                // 4, dtype=torch.float32, device=qkv.device)
+        workspace = torch.empty(
+            (detattention_bwd_workspace_bytes(batch, seq, heads, head_dim, profile) + 3) // 4,
+            dtype=torch.float32, device=qkv.device)
     st = load().detattention_bwd_f32(_prof(profile), batch, seq, heads, head_dim, _ptr(qkv),
                                      _ld(qkv), _ptr(dout), _ld(dout), ctypes.c_float(scale),
                                      _ptr(dqkv), _ld(dqkv), _ptr(workspace),

@@ -397,16 +397,23 @@ det_status detcos_f32(const det_profile_v1 *prof, int64_t n, const float *x, flo
  * ldqkv >= 3 heads head_dim. For every sequence and head:
  * S = Q K^T (detgemm_f32's arithmetic), P = detsoftmax_causal_f32(S, scale,
  * diag 0), O = P V (detgemm_f32's arithmetic), written to out (batch seq rows
- * of heads x head_dim, row stride ldout >= heads head_dim). The heads run one
- * after the other through a seq x seq score buffer in the workspace (at least
- * detattention_workspace_bytes, 256-byte aligned). out must not overlap qkv
- * or the workspace. */
+ * of heads x head_dim, row stride ldout >= heads head_dim). The heads run in
+ * groups whose seq x seq score buffers share the workspace (at least
+ * detattention_workspace_bytes for the same batch, seq, heads and head_dim,
+ * 256-byte aligned; at most about 1 GiB): each step is one launch over a
+ * group, and the score tiles wholly above the diagonal, which the softmax
+ * masks, are not computed. Each head's bits are those of its separate
+ * products. out must not overlap qkv or the workspace. batch may be 0.
+ * Errors: DET_ERR_INVALID_ARG for seq or heads or head_dim outside 1..65536,
+ * batch * seq >= 2^31, strides below their row lengths or null pointers;
+ * DET_ERR_WORKSPACE for a missing, short or misaligned workspace. */
 det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
                             int64_t heads, int64_t head_dim, const float *qkv, int64_t ldqkv,
                             float scale, float *out, int64_t ldout, void *workspace,
                             size_t workspace_bytes, det_stream_t stream);
-det_status detattention_workspace_bytes(const det_profile_v1 *prof, int64_t seq,
-                                        int64_t head_dim, size_t *bytes);
+det_status detattention_workspace_bytes(const det_profile_v1 *prof, int64_t batch,
+                                        int64_t seq, int64_t heads, int64_t head_dim,
+                                        size_t *bytes);
 
 /* ------------------------------------------------------------------ block backward
  * The backward of the block operations, for the byte-level LM's training step
@@ -452,16 +459,19 @@ det_status detembedding_bwd_f32(const det_profile_v1 *prof, int64_t ntok, int64_
  * gradients of Q, K and V into dqkv (same packed layout). Per sequence and
  * head, P is recomputed by the forward's spelling; dP = dO V^T, dV = P^T dO,
  * dS = detsoftmax_causal_bwd_f32(P, dP, scale), dQ = dS K, dK = dS^T Q, every
- * product with detgemm_f32's arithmetic. The workspace (at least
- * detattention_bwd_workspace_bytes, 256-byte aligned) holds two seq x seq
- * buffers. dqkv must not overlap qkv, dout or the workspace. */
+ * product with detgemm_f32's arithmetic, each step one launch over a group of
+ * heads as in detattention_f32. The workspace (at least
+ * detattention_bwd_workspace_bytes, 256-byte aligned) holds two score
+ * buffers of a group. dqkv must not overlap qkv, dout or the workspace.
+ * Errors as detattention_f32. */
 det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
                                 int64_t heads, int64_t head_dim, const float *qkv,
                                 int64_t ldqkv, const float *dout, int64_t lddout, float scale,
                                 float *dqkv, int64_t lddqkv, void *workspace,
                                 size_t workspace_bytes, det_stream_t stream);
-det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t seq,
-                                            int64_t head_dim, size_t *bytes);
+det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t batch,
+                                            int64_t seq, int64_t heads, int64_t head_dim,
+                                            size_t *bytes);
 
 /* Reads, and optionally clears, the current device's watchdog word.
  * *code == 0 means no bounded device wait has ever given up; otherwise bit k
