@@ -287,13 +287,20 @@ def run_ours(args, rank, world, local_rank):
                       + 1 + 3 * g162 + 2 + 1)
     # the byte-level LM step: the embedding, 2 forward blocks (11 launches and
     # the attention), the head GEMM, the cross-entropy and its mean, the head's
-    # two backward GEMMs, 2 backward blocks (18 launches and the attention's
-    # backward), the embedding backward, and one AdamW launch per parameter
-    # tensor (2 + 7 a block); no GEMM of this step uses a workspace
+    # two backward GEMMs, 2 backward blocks (13 launches, 5 weight-gradient
+    # GEMMs and the attention's backward), the embedding backward, and one
+    # AdamW launch per parameter tensor (2 + 7 a block); only the
+    # weight-gradient GEMMs (K = all tokens) use workspaces
     nb = len(bl["blocks"])
     gb = attn_groups_count(bl["batch"], bl["seq"], bl["heads"])
-    byte_lm_launches = (1 + nb * (11 + 3 * gb) + 1 + 2 + 2
-                        + nb * (18 + 7 * gb) + 1 + 2 + 7 * nb)
+    ntok_b, d_b, f_b = bl["batch"] * bl["seq"], bl["d"], bl["dff"]
+
+    def dw_n(M, N):
+        return 1 + int(detlib.detgemm_workspace_bytes(M, N, ntok_b, True, False) > 0)
+    blk_dw = sum(dw_n(M, N) for M, N in ((f_b, d_b), (d_b, f_b), (d_b, f_b), (d_b, d_b),
+                                         (d_b, 3 * d_b)))
+    byte_lm_launches = (1 + nb * (11 + 3 * gb) + 1 + 2 + dw_n(bl["vocab"], d_b) + 1
+                        + nb * (13 + blk_dw + 7 * gb) + 1 + 2 + 7 * nb)
     launches_per_step = (1 + sum(gemm_n(w) for w in ws_fwd) + 2 + 2
                          + sum(gemm_n(w) for w in ws_dw) + 1 + block_launches
                          + byte_lm_launches + 1)

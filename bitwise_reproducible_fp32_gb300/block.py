@@ -39,6 +39,7 @@ class Block:
                    "ff": ws(n, d_ff, d_model), "down": ws(n, d_model, d_ff)}
         self.att_ws = e((detlib.detattention_workspace_bytes(batch, seq, heads, self.hd) + 3)
                         // 4)
+        self.ws_bwd = {}       # weight-gradient GEMM workspaces, by output shape
 
     def flops(self):
         n, D, Fd = self.B * self.T, self.D, self.Fd
@@ -79,7 +80,13 @@ class Block:
         n, D, Fd = self.B * self.T, self.D, self.Fd
         e = lambda *s: torch.empty(s, dtype=torch.float32, device=dy.device)  # noqa: E731
         g = {}
-        tA = lambda A, B, C=None: L.detgemm_f32(A, B, C, transA=True)          # noqa: E731
+        def tA(A, B):
+            # weight gradients contract over the tokens: K = batch * seq, few
+            # output tiles, so the GEMM splits K through a workspace
+            M, N = A.shape[1], B.shape[1]
+            if (M, N) not in self.ws_bwd:
+                self.ws_bwd[(M, N)] = L.gemm_workspace(M, N, n, True, False, device=dy.device)
+            return L.detgemm_f32(A, B, transA=True, workspace=self.ws_bwd[(M, N)])
         tB = lambda A, B, C=None: L.detgemm_f32(A, B, C, transB=True)          # noqa: E731
         # y = x1 + s W_down
         ds = tB(dy, w["W_down"])

@@ -40,7 +40,8 @@ def train_step(c, device, hp):
                                         dscale=1.0 / ntok, dev_status=status)
     st["loss"], st["loss_mean"], st["dlogits"] = loss, mean, dlogits
     # backward
-    grads = {"head": L.detgemm_f32(dlogits, xs[-1], transA=True)}
+    head_ws = L.gemm_workspace(c["vocab"], d, ntok, True, False, device=device)
+    grads = {"head": L.detgemm_f32(dlogits, xs[-1], transA=True, workspace=head_ws)}
     dx = L.detgemm_f32(dlogits, c["head"])
     for i in reversed(range(len(blocks))):
         dx, g = blocks[i].backward(xs[i], c["blocks"][i], dx)

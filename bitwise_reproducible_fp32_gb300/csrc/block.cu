@@ -195,25 +195,53 @@ __global__ void __launch_bounds__(kSmaxThreads)
     }
 }
 
-// Embedding backward: thread per (id, column); the tokens' gradient rows in
-// ascending token order, the first as is; +0 for an id no token uses.
+// Embedding backward: a CTA per id v. It scans the tokens 256 at a time,
+// lists the positions holding v in ascending order (warp ballots and a prefix
+// over the 8 warps), and thread j adds the listed gradient rows' column j to
+// its running sum in that order, the first as is; +0 for an id no token uses.
+// Columns go 1024 at a time, 4 a thread.
 __global__ void __launch_bounds__(256)
     embedding_bwd_kernel(int64_t ntok, int64_t dim, const int32_t *__restrict__ tokens,
                          const float *__restrict__ dx, int64_t lddx, int64_t vocab, float *de,
                          int64_t ldde) {
-    const int64_t total = vocab * dim;
-    for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total;
-         e += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t v = e / dim, j = e - v * dim;
-        float t = 0.0f;
-        bool first = true;
-        for (int64_t k = 0; k < ntok; ++k) {
-            if (tokens[k] != v) continue;
-            const float x = dx[k * lddx + j];
-            t = first ? x : __fadd_rn(t, x);
-            first = false;
+    __shared__ int32_t list[256];
+    __shared__ int wcount[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int64_t v = blockIdx.x; v < vocab; v += gridDim.x) {
+        for (int64_t j0 = 0; j0 < dim; j0 += 1024) {
+            float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            bool first = true;
+            for (int64_t k0 = 0; k0 < ntok; k0 += 256) {
+                const int64_t k = k0 + tid;
+                const bool hit = k < ntok && tokens[k] == v;
+                const unsigned m = __ballot_sync(0xffffffffu, hit);
+                if (lane == 0) wcount[warp] = __popc(m);
+                __syncthreads();
+                int before = 0, total = 0;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    before += w < warp ? wcount[w] : 0;
+                    total += wcount[w];
+                }
+                if (hit) list[before + __popc(m & ((1u << lane) - 1u))] = tid;
+                __syncthreads();
+                for (int i = 0; i < total; ++i) {
+                    const float *row = dx + (k0 + list[i]) * lddx;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int64_t j = j0 + tid + 256 * c;
+                        if (j < dim) t[c] = first ? row[j] : __fadd_rn(t[c], row[j]);
+                    }
+                    first = false;
+                }
+                __syncthreads();   // list and wcount are rewritten next
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int64_t j = j0 + tid + 256 * c;
+                if (j < dim) de[v * ldde + j] = t[c];
+            }
         }
-        de[v * ldde + j] = t;
     }
 }
 
@@ -339,8 +367,9 @@ cudaError_t launch_softmax_causal_bwd(int64_t rows, int64_t cols, const float *p
 cudaError_t launch_embedding_bwd(int64_t ntok, int64_t dim, const int32_t *tokens,
                                  const float *dx, int64_t lddx, int64_t vocab, float *de,
                                  int64_t ldde, cudaStream_t s) {
-    embedding_bwd_kernel<<<unsigned(ew_blocks(vocab * dim)), 256, 0, s>>>(
-        ntok, dim, tokens, dx, lddx, vocab, de, ldde);
+    const int64_t blocks = std::min<int64_t>(vocab, int64_t(sm_count_current_device()) * 8);
+    embedding_bwd_kernel<<<unsigned(blocks), 256, 0, s>>>(ntok, dim, tokens, dx, lddx, vocab,
+                                                         de, ldde);
     return cudaGetLastError();
 }
 

@@ -5,8 +5,9 @@ profiler can capture a chosen launch (ncu -k ... -s ... -c ...).
 
 Cases keep the device footprint at a few hundred MB, above the 129 MB L2 so
 DRAM counters mean something:
-  lm_head   GEMM 1024 x 50257 x 768, weight [50257, 768] transposed
-  qkv       GEMM 8192 x 2304 x 768
+  lm_head   GEMM 1024 x 50257 x 768, weight [50257, 768] transposed (with its
+            workspace: X is copied transposed first, as in the benchmark)
+  qkv       GEMM 8192 x 2304 x 768 (likewise)
   dw_qkv    GEMM X^T dY, 768 x 2304 over 8192 tokens
   xent      cross-entropy 1024 x 50257 with dlogits and mean
   rmsnorm   RMSNorm 8192 x 768
@@ -45,7 +46,10 @@ def main(argv=None):
         M = p["A"].shape[0]
         N = p["B"].shape[0] if p["transB"] else p["B"].shape[1]
         C = torch.empty((M, N), dtype=torch.float32, device=dev)
-        run = lambda: detlib.detgemm_f32(A, B, C, transA=p["transA"], transB=p["transB"])
+        K = p["A"].shape[1]
+        ws = detlib.gemm_workspace(M, N, K, p["transA"], p["transB"])
+        run = lambda: detlib.detgemm_f32(A, B, C, transA=p["transA"], transB=p["transB"],
+                                         workspace=ws)
     elif a.case == "dw_qkv":
         p = inputs.dw_cfg5()[0]
         A, B = up(p["A"]), up(p["B"])

@@ -71,7 +71,10 @@ def test_rope_bwd(dev):
 
 
 @pytest.mark.parametrize("ntok,dim,vocab", [(1, 1, 1), (2048, 64, 256), (777, 9, 300),
-                                            (5000, 33, 7)])
+                                            (5000, 33, 7),
+                                            # one id for every token (full 256-token
+                                            # lists), and columns beyond 1024 and 2048
+                                            (600, 2100, 1), (300, 1030, 40)])
 def test_embedding_bwd(dev, ntok, dim, vocab):
     rng = np.random.default_rng(ntok + dim)
     tok = rng.integers(0, max(vocab - 3, 1), size=ntok).astype(np.int32)
