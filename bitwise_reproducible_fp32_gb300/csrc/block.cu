@@ -30,8 +30,8 @@
 namespace det {
 namespace {
 
-constexpr int kSmaxThreads = 256;        // = the 256 chains
-static_assert(kSmaxThreads == kXentLanes, "one thread a chain");
+constexpr int kSmaxChains = 32 * 8;       // 8 chains a lane of a warp
+static_assert(kSmaxChains == kXentLanes, "the 256 chains of the row reductions");
 
 __global__ void __launch_bounds__(256)
     swiglu_kernel(int64_t n, const float *__restrict__ g, const float *__restrict__ u,
@@ -114,84 +114,262 @@ __device__ __forceinline__ float butterfly32(float s) {
     return s;
 }
 
-// One row per CTA, thread l = chain l: chain l owns the 4-element groups
-// g = l, l + 256, ... of the kept columns and adds their exps in ascending
-// order. Pass 1 the max, pass 2 the chains, pass 3 the probabilities (the
-// exps recomputed; rows of an attention batch stay in L1/L2 between passes).
-__global__ void __launch_bounds__(kSmaxThreads)
-    softmax_causal_kernel(int64_t rows, int64_t cols, const float *s, int64_t lds, float scale,
-                          int64_t diag, int64_t period, float *p, int64_t ldp) {
-    __shared__ float red[kSmaxThreads / 32];
-    const int l = threadIdx.x, lane = l & 31, warp = l >> 5;
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const float *sr = s + r * lds;
-        float *pr = p + r * ldp;
-        int64_t nr = (r % period) + diag + 1;
-        nr = nr < 0 ? 0 : (nr > cols ? cols : nr);
-        for (int64_t j = nr + l; j < cols; j += kSmaxThreads) pr[j] = 0.0f;
-        if (nr == 0) continue;     // uniform across the CTA
-        // pass 1: the max (its order is free)
-        float m = __fmul_rn(sr[0], scale);
-        for (int64_t j = l; j < nr; j += kSmaxThreads) m = max_nan2(m, __fmul_rn(sr[j], scale));
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-            m = max_nan2(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (lane == 0) red[warp] = m;
-        __syncthreads();
-        m = red[0];
-#pragma unroll
-        for (int w = 1; w < kSmaxThreads / 32; ++w) m = max_nan2(m, red[w]);
-        __syncthreads();
-        // pass 2: chain l over its groups, ascending
-        float c = 0.0f;
-        for (int64_t g = l; 4 * g < nr; g += kSmaxThreads) {
-            const int64_t j1 = 4 * g + 4 < nr ? 4 * g + 4 : nr;
-            for (int64_t j = 4 * g; j < j1; ++j)
-                c = __fadd_rn(c, det_exp(__fsub_rn(__fmul_rn(sr[j], scale), m)));
-        }
-        c = butterfly32(c);
-        if (lane == 0) red[warp] = c;
-        __syncthreads();
-        const float a01 = __fadd_rn(red[0], red[1]), a23 = __fadd_rn(red[2], red[3]);
-        const float a45 = __fadd_rn(red[4], red[5]), a67 = __fadd_rn(red[6], red[7]);
-        const float inv = __fdiv_rn(1.0f, __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67)));
-        __syncthreads();
-        // pass 3: p = e * (1 / S)
-        for (int64_t j = l; j < nr; j += kSmaxThreads)
-            pr[j] = __fmul_rn(det_exp(__fsub_rn(__fmul_rn(sr[j], scale), m)), inv);
+// The causal-softmax kernels give a row to a warp. Lane l carries chains
+// l + 32w (w = 0..7) of the 256, so chain ch still owns the 4-wide groups
+// g = ch, ch + 256, ... of the kept columns and adds them in ascending order;
+// the 32 chains of each w fold by the butterfly and the 8 totals by the tree
+// ((t0 + t1) + (t2 + t3)) + ((t4 + t5) + (t6 + t7)), as with a thread a chain
+// and a warp per 32 chains. Segment sg of a row (groups 256 sg .. 256 sg +
+// 255, columns 1024 sg ..) is held in registers for sg < kSmaxCache, so the
+// first 2048 columns (1024 in the backward, which holds two arrays) are read
+// once; later segments are read again.
+#ifndef DET_SMAX_CACHE
+#define DET_SMAX_CACHE 2
+#endif
+#ifndef DET_SMAX_MINB
+#define DET_SMAX_MINB 1
+#endif
+constexpr int kSmaxCache = DET_SMAX_CACHE;
+constexpr int kSmaxBwdCache = 1;
+constexpr int kSmaxWarps = 8;
+
+// Kept values of columns j .. j+3 (j a multiple of 4); columns >= nr are not
+// read and come back as 0.
+__device__ __forceinline__ float4 ld4_kept(const float *r, int64_t j, int64_t nr, bool vec) {
+    if (vec && j + 3 < nr) return *reinterpret_cast<const float4 *>(r + j);
+    float4 v;
+    v.x = j < nr ? r[j] : 0.0f;
+    v.y = j + 1 < nr ? r[j + 1] : 0.0f;
+    v.z = j + 2 < nr ? r[j + 2] : 0.0f;
+    v.w = j + 3 < nr ? r[j + 3] : 0.0f;
+    return v;
+}
+
+__device__ __forceinline__ void st4_kept(float *r, int64_t j, int64_t nr, bool vec, float4 v) {
+    if (vec && j + 3 < nr) {
+        *reinterpret_cast<float4 *>(r + j) = v;
+        return;
+    }
+    if (j < nr) r[j] = v.x;
+    if (j + 1 < nr) r[j + 1] = v.y;
+    if (j + 2 < nr) r[j + 2] = v.z;
+    if (j + 3 < nr) r[j + 3] = v.w;
+}
+
+// +0 in the masked columns nr .. cols-1 of a row, by the 32 lanes (16-byte
+// stores from the first 16-byte boundary at or after nr when vec). Columns
+// below nr are never touched.
+__device__ __forceinline__ void zero_masked(float *r, int64_t nr, int64_t cols, int lane,
+                                            bool vec) {
+    if (nr >= cols) return;
+    if (!vec) {
+        for (int64_t j = nr + lane; j < cols; j += 32) r[j] = 0.0f;
+        return;
+    }
+    const int64_t j4 = ((nr + 3) & ~int64_t(3)) < cols ? ((nr + 3) & ~int64_t(3)) : cols;
+    for (int64_t j = nr + lane; j < j4; j += 32) r[j] = 0.0f;
+    const int64_t jend = j4 + ((cols - j4) & ~int64_t(3));
+    for (int64_t j = j4 + 4 * lane; j < jend; j += 128)
+        *reinterpret_cast<float4 *>(r + j) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int64_t j = jend + lane; j < cols; j += 32) r[j] = 0.0f;
+}
+
+// Asks L2 to fetch floats [0, n) of a 16-byte aligned row, n a multiple of 4,
+// in pieces of at most 16 KB.
+__device__ __forceinline__ void prefetch_row_l2(const float *row, int64_t n) {
+    for (int64_t q = 0; q < n; q += 4096) {
+        const int64_t c = n - q < 4096 ? n - q : 4096;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row + q),
+                     "r"(uint32_t(c) * 4u)
+                     : "memory");
     }
 }
 
-// Softmax backward, one row per CTA, thread l = chain l: dot = the 256 chains
-// of fmaf(dP_j, P_j, .) over the kept columns, folded like the forward's sum;
-// then dS_j = (P_j (dP_j - dot)) scale; masked columns +0.
-__global__ void __launch_bounds__(kSmaxThreads)
+__device__ __forceinline__ float fold_chains(const float (&c)[8]) {
+    float t[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t[w] = butterfly32(c[w]);
+    return __fadd_rn(__fadd_rn(__fadd_rn(t[0], t[1]), __fadd_rn(t[2], t[3])),
+                     __fadd_rn(__fadd_rn(t[4], t[5]), __fadd_rn(t[6], t[7])));
+}
+
+__device__ __forceinline__ int64_t kept_columns(int64_t r, int64_t period, int64_t diag,
+                                                int64_t cols) {
+    const int64_t nr = (r % period) + diag + 1;
+    return nr < 0 ? 0 : (nr > cols ? cols : nr);
+}
+
+// Causal softmax: pass 1 the max of x = s * scale (order free), pass 2 the
+// chains of exp(x - max) (the cached values become the exps), pass 3
+// p = e * (1 / S).
+__global__ void __launch_bounds__(32 * kSmaxWarps, DET_SMAX_MINB)
+    softmax_causal_kernel(int64_t rows, int64_t cols, const float *s, int64_t lds, float scale,
+                          int64_t diag, int64_t period, float *p, int64_t ldp, int vec_s,
+                          int vec_p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = int64_t(gridDim.x) * kSmaxWarps;
+    for (int64_t r = int64_t(blockIdx.x) * kSmaxWarps + (threadIdx.x >> 5); r < rows;
+         r += nwarps) {
+        const float *sr = s + r * lds;
+        float *pr = p + r * ldp;
+        const int64_t nr = kept_columns(r, period, diag, cols);
+        // ask L2 for this warp's next row (its whole 16-byte granules of kept
+        // columns), so its loads find it there
+        if (vec_s && lane == 0 && r + nwarps < rows) {
+            const int64_t rn = r + nwarps;
+            prefetch_row_l2(s + rn * lds, kept_columns(rn, period, diag, cols) & ~int64_t(3));
+        }
+        zero_masked(pr, nr, cols, lane, vec_p);
+        if (nr == 0) continue;     // uniform across the warp
+        const int64_t nseg = (nr + 1023) / 1024;
+        float4 xc[kSmaxCache][8];
+        auto scaled = [&](int64_t j) {
+            float4 v = ld4_kept(sr, j, nr, vec_s);
+            v.x = __fmul_rn(v.x, scale); v.y = __fmul_rn(v.y, scale);
+            v.z = __fmul_rn(v.z, scale); v.w = __fmul_rn(v.w, scale);
+            return v;
+        };
+        auto col = [&](int64_t sg, int w) { return 4 * (int64_t(lane) + 32 * w + 256 * sg); };
+        // pass 1
+        float m = __fmul_rn(sr[0], scale);
+        auto take_max = [&](float4 v, int64_t j) {
+            if (j < nr) m = max_nan2(m, v.x);
+            if (j + 1 < nr) m = max_nan2(m, v.y);
+            if (j + 2 < nr) m = max_nan2(m, v.z);
+            if (j + 3 < nr) m = max_nan2(m, v.w);
+        };
+#pragma unroll
+        for (int sg = 0; sg < kSmaxCache; ++sg)
+            if (sg < nseg)
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    xc[sg][w] = scaled(col(sg, w));
+                    take_max(xc[sg][w], col(sg, w));
+                }
+        for (int64_t sg = kSmaxCache; sg < nseg; ++sg)
+            for (int w = 0; w < 8; ++w) take_max(scaled(col(sg, w)), col(sg, w));
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            m = max_nan2(m, __shfl_xor_sync(0xffffffffu, m, off));
+        // pass 2
+        float c[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) c[w] = 0.0f;
+        // with a finite max every x - m <= 0: the branch-free exp4 (same bits)
+        const bool finite_max = fabsf(m) <= 0x1.fffffep127f;
+        auto exps = [&](float4 &v, int64_t j, float &cw) {
+            if (finite_max) {
+                v = exp4(v, m);
+            } else {
+                v.x = det_exp_call(__fsub_rn(v.x, m));
+                v.y = det_exp_call(__fsub_rn(v.y, m));
+                v.z = det_exp_call(__fsub_rn(v.z, m));
+                v.w = det_exp_call(__fsub_rn(v.w, m));
+            }
+            if (j < nr) cw = __fadd_rn(cw, v.x);
+            if (j + 1 < nr) cw = __fadd_rn(cw, v.y);
+            if (j + 2 < nr) cw = __fadd_rn(cw, v.z);
+            if (j + 3 < nr) cw = __fadd_rn(cw, v.w);
+        };
+#pragma unroll
+        for (int sg = 0; sg < kSmaxCache; ++sg)
+            if (sg < nseg)
+#pragma unroll
+                for (int w = 0; w < 8; ++w) exps(xc[sg][w], col(sg, w), c[w]);
+        for (int64_t sg = kSmaxCache; sg < nseg; ++sg)
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                float4 v = scaled(col(sg, w));
+                exps(v, col(sg, w), c[w]);
+            }
+        const float inv = __fdiv_rn(1.0f, fold_chains(c));
+        // pass 3
+        auto prob = [&](float4 e) {
+            return make_float4(__fmul_rn(e.x, inv), __fmul_rn(e.y, inv), __fmul_rn(e.z, inv),
+                               __fmul_rn(e.w, inv));
+        };
+#pragma unroll
+        for (int sg = 0; sg < kSmaxCache; ++sg)
+            if (sg < nseg)
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    st4_kept(pr, col(sg, w), nr, vec_p, prob(xc[sg][w]));
+        for (int64_t sg = kSmaxCache; sg < nseg; ++sg)
+            for (int w = 0; w < 8; ++w) {
+                float4 v = scaled(col(sg, w));
+                float unused = 0.0f;
+                exps(v, col(sg, w), unused);
+                st4_kept(pr, col(sg, w), nr, vec_p, prob(v));
+            }
+    }
+}
+
+// Softmax backward: dot = the chains of fmaf(dP_j, P_j, .) over the kept
+// columns, folded as the forward's sum; dS_j = (P_j (dP_j - dot)) scale;
+// masked columns +0. ds may be dp itself (each dS_j is written after dP_j is
+// read).
+__global__ void __launch_bounds__(32 * kSmaxWarps)
     softmax_causal_bwd_kernel(int64_t rows, int64_t cols, const float *p, const float *dp,
                               int64_t ld, float scale, int64_t diag, int64_t period,
-                              float *ds, int64_t ldd) {
-    __shared__ float red[kSmaxThreads / 32];
-    const int l = threadIdx.x, lane = l & 31, warp = l >> 5;
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+                              float *ds, int64_t ldd, int vec_in, int vec_out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = int64_t(gridDim.x) * kSmaxWarps;
+    for (int64_t r = int64_t(blockIdx.x) * kSmaxWarps + (threadIdx.x >> 5); r < rows;
+         r += nwarps) {
         const float *pr = p + r * ld, *dpr = dp + r * ld;
         float *dr = ds + r * ldd;
-        int64_t nr = (r % period) + diag + 1;
-        nr = nr < 0 ? 0 : (nr > cols ? cols : nr);
-        for (int64_t j = nr + l; j < cols; j += kSmaxThreads) dr[j] = 0.0f;
-        if (nr == 0) continue;
-        float c = 0.0f;
-        for (int64_t g = l; 4 * g < nr; g += kSmaxThreads) {
-            const int64_t j1 = 4 * g + 4 < nr ? 4 * g + 4 : nr;
-            for (int64_t j = 4 * g; j < j1; ++j) c = __fmaf_rn(dpr[j], pr[j], c);
+        const int64_t nr = kept_columns(r, period, diag, cols);
+        if (vec_in && lane == 0 && r + nwarps < rows) {
+            const int64_t rn = r + nwarps, nn = kept_columns(rn, period, diag, cols) & ~int64_t(3);
+            prefetch_row_l2(p + rn * ld, nn);
+            prefetch_row_l2(dp + rn * ld, nn);
         }
-        c = butterfly32(c);
-        if (lane == 0) red[warp] = c;
-        __syncthreads();
-        const float a01 = __fadd_rn(red[0], red[1]), a23 = __fadd_rn(red[2], red[3]);
-        const float a45 = __fadd_rn(red[4], red[5]), a67 = __fadd_rn(red[6], red[7]);
-        const float dot = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
-        __syncthreads();
-        for (int64_t j = l; j < nr; j += kSmaxThreads)
-            dr[j] = __fmul_rn(__fmul_rn(pr[j], __fsub_rn(dpr[j], dot)), scale);
+        zero_masked(dr, nr, cols, lane, vec_out);
+        if (nr == 0) continue;
+        const int64_t nseg = (nr + 1023) / 1024;
+        float4 pc[kSmaxBwdCache][8], dc[kSmaxBwdCache][8];
+        auto col = [&](int64_t sg, int w) { return 4 * (int64_t(lane) + 32 * w + 256 * sg); };
+        float c[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) c[w] = 0.0f;
+        auto chain = [&](float4 pv, float4 dv, int64_t j, float &cw) {
+            if (j < nr) cw = __fmaf_rn(dv.x, pv.x, cw);
+            if (j + 1 < nr) cw = __fmaf_rn(dv.y, pv.y, cw);
+            if (j + 2 < nr) cw = __fmaf_rn(dv.z, pv.z, cw);
+            if (j + 3 < nr) cw = __fmaf_rn(dv.w, pv.w, cw);
+        };
+#pragma unroll
+        for (int sg = 0; sg < kSmaxBwdCache; ++sg)
+            if (sg < nseg)
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    pc[sg][w] = ld4_kept(pr, col(sg, w), nr, vec_in);
+                    dc[sg][w] = ld4_kept(dpr, col(sg, w), nr, vec_in);
+                    chain(pc[sg][w], dc[sg][w], col(sg, w), c[w]);
+                }
+        for (int64_t sg = kSmaxBwdCache; sg < nseg; ++sg)
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                chain(ld4_kept(pr, col(sg, w), nr, vec_in), ld4_kept(dpr, col(sg, w), nr, vec_in),
+                      col(sg, w), c[w]);
+        const float dot = fold_chains(c);
+        auto grad = [&](float4 pv, float4 dv) {
+            return make_float4(__fmul_rn(__fmul_rn(pv.x, __fsub_rn(dv.x, dot)), scale),
+                               __fmul_rn(__fmul_rn(pv.y, __fsub_rn(dv.y, dot)), scale),
+                               __fmul_rn(__fmul_rn(pv.z, __fsub_rn(dv.z, dot)), scale),
+                               __fmul_rn(__fmul_rn(pv.w, __fsub_rn(dv.w, dot)), scale));
+        };
+#pragma unroll
+        for (int sg = 0; sg < kSmaxBwdCache; ++sg)
+            if (sg < nseg)
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    st4_kept(dr, col(sg, w), nr, vec_out, grad(pc[sg][w], dc[sg][w]));
+        for (int64_t sg = kSmaxBwdCache; sg < nseg; ++sg)
+            for (int w = 0; w < 8; ++w)
+                st4_kept(dr, col(sg, w), nr, vec_out,
+                         grad(ld4_kept(pr, col(sg, w), nr, vec_in),
+                              ld4_kept(dpr, col(sg, w), nr, vec_in)));
     }
 }
 
@@ -333,9 +511,11 @@ cudaError_t launch_softmax_causal(int64_t rows, int64_t cols, const float *sc, i
                                   float scale, int64_t diag, int64_t period, float *p,
                                   int64_t ldp, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    const int64_t blocks = std::min<int64_t>(rows, int64_t(sm_count_current_device()) * 8);
-    softmax_causal_kernel<<<unsigned(blocks), kSmaxThreads, 0, s>>>(rows, cols, sc, lds, scale,
-                                                                   diag, period, p, ldp);
+    const int64_t blocks = std::min<int64_t>((rows + kSmaxWarps - 1) / kSmaxWarps,
+                                             int64_t(sm_count_current_device()) * 16);
+    const int vec_s = al16(sc) && lds % 4 == 0, vec_p = al16(p) && ldp % 4 == 0;
+    softmax_causal_kernel<<<unsigned(blocks), 32 * kSmaxWarps, 0, s>>>(
+        rows, cols, sc, lds, scale, diag, period, p, ldp, vec_s, vec_p);
     return cudaGetLastError();
 }
 
@@ -358,9 +538,11 @@ cudaError_t launch_softmax_causal_bwd(int64_t rows, int64_t cols, const float *p
                                       const float *dp, int64_t ld, float scale, int64_t diag,
                                       int64_t period, float *ds, int64_t ldd, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    const int64_t blocks = std::min<int64_t>(rows, int64_t(sm_count_current_device()) * 8);
-    softmax_causal_bwd_kernel<<<unsigned(blocks), kSmaxThreads, 0, s>>>(
-        rows, cols, p, dp, ld, scale, diag, period, ds, ldd);
+    const int64_t blocks = std::min<int64_t>((rows + kSmaxWarps - 1) / kSmaxWarps,
+                                             int64_t(sm_count_current_device()) * 16);
+    const int vec_in = al16(p) && al16(dp) && ld % 4 == 0, vec_out = al16(ds) && ldd % 4 == 0;
+    softmax_causal_bwd_kernel<<<unsigned(blocks), 32 * kSmaxWarps, 0, s>>>(
+        rows, cols, p, dp, ld, scale, diag, period, ds, ldd, vec_in, vec_out);
     return cudaGetLastError();
 }
 

@@ -14,6 +14,8 @@
 
 #include <stdint.h>
 
+#include "det_internal.cuh"
+
 namespace det {
 
 // ---------------------------------------------------------------- exp / log
@@ -56,6 +58,94 @@ __device__ __forceinline__ float det_exp(float x) {
     if (ni < -126) return __fmul_rn(__fmul_rn(p, pow2i(ni + 64)), pow2i(-64));
     return __fmul_rn(p, pow2i(ni));
 }
+
+// The fast forms below serve the row reductions (cross-entropy, the causal
+// softmax), whose exp arguments are x - max <= 0.
+namespace {
+// exp for arguments d <= 0 (or -inf), never NaN, without branches: the same
+// bits as det_exp(d) whenever the returned n satisfies n >= -125; otherwise the
+// caller must use det_exp(d). n = rint(t) is formed as (t + 1.5 2^23) -
+// 1.5 2^23, which rounds t to an integer with ties to even for |t| < 2^22; it
+// can differ from rintf only in the sign of a zero n, which reaches the
+// result only through r = d - n ln2 and the polynomial's products with r,
+// where it is inert. For n >= -125 the scaling p 2^n is exact and is done on
+// the exponent bits.
+constexpr float kRoundMagic = 0x1.8p23f;
+
+__device__ __forceinline__ float exp_le0_fast(float d, int &ni) {
+    const float t = __fmul_rn(d, kLog2e);
+    const float tm = __fadd_rn(t, kRoundMagic);
+    ni = __float_as_int(tm) - __float_as_int(kRoundMagic);
+    const float n = __fsub_rn(tm, kRoundMagic);
+    float r = __fmaf_rn(-n, kLn2Hi, d);
+    r = __fmaf_rn(-n, kLn2Lo, r);
+    float p = kC7;
+    p = __fmaf_rn(p, r, kC6);
+    p = __fmaf_rn(p, r, kC5);
+    p = __fmaf_rn(p, r, kC4);
+    p = __fmaf_rn(p, r, kC3);
+    p = __fmaf_rn(p, r, kC2);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    return __int_as_float(__float_as_int(p) + int(unsigned(ni) << 23));
+}
+
+// The general exp as an out-of-line call, for the rarely taken paths of the
+// row reductions (deep underflow, -inf, non-finite maxima), so they cost no
+// registers in the hot loops.
+__device__ __noinline__ float det_exp_call(float x) { return det_exp(x); }
+
+// exp_le0_fast on a pair: d = x - m, then the same rounded steps as the scalar
+// routine on both halves at once; n ln2 enters as n (-LN2_HI), which is the
+// same product as (-n) LN2_HI. Returns the pair and the two n.
+// t = d LOG2E is formed by two scalar multiplies: a packed multiply whose
+// result feeds a packed add was measured to round like a fused multiply-add
+// (t not rounded on its own) at the ties of rint(t), which moves n there.
+__device__ __forceinline__ f32x2 exp2_le0_fast(f32x2 x, f32x2 m2, int &n0, int &n1) {
+    const f32x2 d = sub2(x, m2);
+    float d0, d1;
+    unpack2(d, d0, d1);
+    const f32x2 t = pack2(__fmul_rn(d0, kLog2e), __fmul_rn(d1, kLog2e));
+    const f32x2 tm = add2(t, splat2(kRoundMagic));
+    const f32x2 n = sub2(tm, splat2(kRoundMagic));
+    f32x2 r = fma2(n, splat2(-kLn2Hi), d);
+    r = fma2(n, splat2(-kLn2Lo), r);
+    f32x2 p = fma2(splat2(kC7), r, splat2(kC6));
+    p = fma2(p, r, splat2(kC5));
+    p = fma2(p, r, splat2(kC4));
+    p = fma2(p, r, splat2(kC3));
+    p = fma2(p, r, splat2(kC2));
+    p = fma2(p, r, splat2(1.0f));
+    p = fma2(p, r, splat2(1.0f));
+    float t0, t1, p0, p1;
+    unpack2(tm, t0, t1);
+    unpack2(p, p0, p1);
+    n0 = __float_as_int(t0) - __float_as_int(kRoundMagic);
+    n1 = __float_as_int(t1) - __float_as_int(kRoundMagic);
+    return pack2(__int_as_float(__float_as_int(p0) + int(unsigned(n0) << 23)),
+                 __int_as_float(__float_as_int(p1) + int(unsigned(n1) << 23)));
+}
+
+// exp(v - m) for the 4 lanes of a granule; d <= 0 for every element of a row
+// with a finite max. Rare deep-underflow elements take the general routine.
+__device__ __forceinline__ float4 exp4(float4 v, float m) {
+    const f32x2 m2 = splat2(m);
+    int n0, n1, n2, n3;
+    const f32x2 e01 = exp2_le0_fast(pack2(v.x, v.y), m2, n0, n1);
+    const f32x2 e23 = exp2_le0_fast(pack2(v.z, v.w), m2, n2, n3);
+    float4 e;
+    unpack2(e01, e.x, e.y);
+    unpack2(e23, e.z, e.w);
+    if (min(min(n0, n1), min(n2, n3)) < -125) {
+        if (n0 < -125) e.x = det_exp_call(__fsub_rn(v.x, m));
+        if (n1 < -125) e.y = det_exp_call(__fsub_rn(v.y, m));
+        if (n2 < -125) e.z = det_exp_call(__fsub_rn(v.z, m));
+        if (n3 < -125) e.w = det_exp_call(__fsub_rn(v.w, m));
+    }
+    return e;
+}
+
+}  // namespace
 
 __device__ __forceinline__ float det_log(float x) {
     if (x != x) return __fadd_rn(x, x);

@@ -14,6 +14,8 @@ DRAM counters mean something:
   rms_bwd   RMSNorm backward 8192 x 768 (dx, dgain)
   shardsum  fixed-order sum of 64 shard gradients of 768 x 2304
   adamw     AdamW over 32 Mi parameters
+  softmax   causal softmax of 48 stacked 2048 x 2048 score matrices (the 162M
+            block's attention, 4 x 2048 tokens x 12 heads), in place
 Each run is one warm-up launch followed by R launches (default 2).
 """
 from __future__ import annotations
@@ -31,7 +33,7 @@ def main(argv=None):
 
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["lm_head", "qkv", "dw_qkv", "xent", "rmsnorm", "rms_bwd",
-                                    "shardsum", "adamw"])
+                                    "shardsum", "adamw", "softmax"])
     ap.add_argument("--reps", type=int, default=2)
     a = ap.parse_args(argv)
     build.build()
@@ -82,6 +84,10 @@ def main(argv=None):
         g = up(inputs.shard_grads())
         out = torch.empty(g.shape[1], dtype=torch.float32, device=dev)
         run = lambda: detlib.detshardsum_f32(g, scale=1.0 / g.shape[0], out=out)
+    elif a.case == "softmax":
+        g = torch.Generator(device=dev).manual_seed(5)
+        S = torch.randn((48 * 2048, 2048), generator=g, device=dev) * 4
+        run = lambda: detlib.detsoftmax_causal_f32(S, scale=0.125, period=2048, p=S)
     else:
         w = inputs.adamw_cfg5(n=32 * 1024 * 1024)
         P, G, M_, V_ = (up(w[k]) for k in ("p", "g", "m", "v"))

@@ -35,7 +35,8 @@ def test_swiglu_bwd(dev, n):
 
 
 @pytest.mark.parametrize("rows,cols,diag", [(1, 1, 0), (5, 5, 0), (300, 300, 0),
-                                            (64, 2048, 1500), (257, 257, -3)])
+                                            (64, 2048, 1500), (257, 257, -3),
+                                            (24, 2101, 2090)])
 def test_softmax_bwd(dev, rows, cols, diag):
     rng = np.random.default_rng(rows + cols)
     s = (4 * rng.standard_normal((rows, cols))).astype(F)
@@ -44,6 +45,18 @@ def test_softmax_bwd(dev, rows, cols, diag):
     want = oracle.softmax_causal_bwd(p, dp, scale=0.125, diag=diag)
     got = detlib.detsoftmax_causal_bwd_f32(to_dev(p, "padded"), to_dev(dp, "padded"),
                                            scale=0.125, diag=diag)
+    assert_bitwise(host(got), want)
+
+
+def test_softmax_bwd_long_rows_offset_layout(dev):
+    # past 1024 kept columns the backward reads P and dP again; unaligned rows
+    rng = np.random.default_rng(202)
+    s = (4 * rng.standard_normal((17, 1500))).astype(F)
+    p = oracle.softmax_causal(s, scale=0.125, diag=1400)
+    dp = rng.standard_normal((17, 1500)).astype(F)
+    want = oracle.softmax_causal_bwd(p, dp, scale=0.125, diag=1400)
+    got = detlib.detsoftmax_causal_bwd_f32(to_dev(p, "offset"), to_dev(dp, "offset"),
+                                           scale=0.125, diag=1400)
     assert_bitwise(host(got), want)
 
 

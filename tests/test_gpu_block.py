@@ -53,6 +53,18 @@ def test_softmax_causal(dev, rows, cols, scale, diag):
     assert_bitwise(host(got), want, f"{rows}x{cols} scale={scale} diag={diag}")
 
 
+@pytest.mark.parametrize("rows,cols,diag,layout", [(20, 3001, 2990, "offset"),
+                                                   (33, 2500, 2400, "padded"),
+                                                   (9, 4099, 4000, "dense")])
+def test_softmax_causal_long_rows(dev, rows, cols, diag, layout):
+    # rows past 2048 kept columns: the kernel reads those segments again
+    rng = np.random.default_rng(rows + cols)
+    s = (4 * rng.standard_normal((rows, cols))).astype(F)
+    want = oracle.softmax_causal(s, scale=0.125, diag=diag)
+    got = detlib.detsoftmax_causal_f32(to_dev(s, layout), scale=0.125, diag=diag)
+    assert_bitwise(host(got), want, f"{rows}x{cols} diag={diag} {layout}")
+
+
 def test_softmax_batched_by_period_in_place_and_specials(dev):
     rng = np.random.default_rng(91)
     mats = [(4 * rng.standard_normal((257, 257))).astype(F) for _ in range(3)]
