@@ -561,7 +561,6 @@ __global__ void __launch_bounds__(kXsThreads, 1)
     extern __shared__ float4 buf[];
     __shared__ uint64_t bar[2];
     __shared__ float red[32];
-    __shared__ float bcast;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = ((V + 3) >> 2) / 2;           // granules of half 0, every row
     auto aligned_row = [&](int64_t r) {
@@ -630,13 +629,12 @@ __global__ void __launch_bounds__(kXsThreads, 1)
                 m = max_nan(__shfl_xor_sync(0xffffffffu, m, off), m);
             if (lane == 0) red[warp] = m;
             __syncthreads();
-            if (tid == 0) {
-                float mm = red[0];
-                for (int w = 1; w < kXsThreads / 32; ++w) mm = max_nan(red[w], mm);
-                bcast = mm;
-            }
-            __syncthreads();
-            m = bcast;
+            // every warp folds the 32 warp maxima itself (the max's order is
+            // free: NaN wins, and a +0/-0 tie is bit-inert downstream)
+            m = red[lane];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                m = max_nan(__shfl_xor_sync(0xffffffffu, m, off), m);
             const bool finite_m = fabsf(m) <= 3.402823466e38f;
             // C. e = exp(x - m) in place (elements outside the row are never read)
             if (finite_m) {
@@ -662,15 +660,12 @@ __global__ void __launch_bounds__(kXsThreads, 1)
                 if (lane == 0) red[warp] = s;
             }
             __syncthreads();
-            if (tid == 0) {
-                const float a01 = __fadd_rn(red[0], red[1]), a23 = __fadd_rn(red[2], red[3]);
-                const float a45 = __fadd_rn(red[4], red[5]), a67 = __fadd_rn(red[6], red[7]);
-                const float S = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
-                bcast = S;
-                loss[row] = __fsub_rn(det_log(S), __fsub_rn(x[y], m));
-            }
-            __syncthreads();
-            inv = __fdiv_rn(1.0f, bcast);
+            // every thread folds the 8 chain-warp totals (the same tree)
+            const float a01 = __fadd_rn(red[0], red[1]), a23 = __fadd_rn(red[2], red[3]);
+            const float a45 = __fadd_rn(red[4], red[5]), a67 = __fadd_rn(red[6], red[7]);
+            const float S = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
+            if (tid == 0) loss[row] = __fsub_rn(det_log(S), __fsub_rn(x[y], m));
+            inv = __fdiv_rn(1.0f, S);
             vec_out = drow != nullptr &&
                       int((reinterpret_cast<uintptr_t>(drow) >> 2) & 3) == h;
         } else {
