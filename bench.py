@@ -265,9 +265,10 @@ def run_ours(args, rank, world, local_rank):
     gemm_flops = sum(gemm_flops_fwd) + sum(gemm_flops_dw)
     lm_idx = [p["name"] for p in fwd].index("lm_head")
     # A GEMM is one launch, plus one where it uses its workspace (the split-K
-    # second pass, or the transposed copy of A). Attention is 3 launches a
-    # group of heads forward and 7 backward. Checked against an ncu launch
-    # list of one step.
+    # second pass, or the transposed copy of A). Attention is 4 launches a
+    # group of heads forward (with the count of V's non-finite values) and 10
+    # backward (with those of dO, K and Q). Checked against an ncu launch list
+    # of one step.
     def gemm_n(ws):
         return 1 + int(ws is not None)
 
@@ -284,7 +285,7 @@ def run_ours(args, rank, world, local_rank):
     # one block forward: 2 RMSNorms, 5 GEMMs, RoPE, attention, 2 adds, SwiGLU
     g162 = attn_groups_count(bc["batch"], bc["seq"], inputs.N_HEADS)
     block_launches = (2 + sum(gemm_n(blk.ws[k]) for k in ("qkv", "o", "ff", "ff", "down"))
-                      + 1 + 3 * g162 + 2 + 1)
+                      + 1 + 4 * g162 + 2 + 1)
     # the byte-level LM step: the embedding, 2 forward blocks (11 launches and
     # the attention), the head GEMM, the cross-entropy and its mean, the head's
     # two backward GEMMs, 2 backward blocks (13 launches, 5 weight-gradient
@@ -299,8 +300,8 @@ def run_ours(args, rank, world, local_rank):
         return 1 + int(detlib.detgemm_workspace_bytes(M, N, ntok_b, True, False) > 0)
     blk_dw = sum(dw_n(M, N) for M, N in ((f_b, d_b), (d_b, f_b), (d_b, f_b), (d_b, d_b),
                                          (d_b, 3 * d_b)))
-    byte_lm_launches = (1 + nb * (11 + 3 * gb) + 1 + 2 + dw_n(bl["vocab"], d_b) + 1
-                        + nb * (13 + blk_dw + 7 * gb) + 1 + 2 + 7 * nb)
+    byte_lm_launches = (1 + nb * (11 + 4 * gb) + 1 + 2 + dw_n(bl["vocab"], d_b) + 1
+                        + nb * (13 + blk_dw + 10 * gb) + 1 + 2 + 7 * nb)
     launches_per_step = (1 + sum(gemm_n(w) for w in ws_fwd) + 2 + 2
                          + sum(gemm_n(w) for w in ws_dw) + 1 + block_launches
                          + byte_lm_launches + 1)

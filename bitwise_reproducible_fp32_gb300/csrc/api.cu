@@ -330,6 +330,7 @@ namespace {
 // sequences (all heads of gb sequences) when one sequence fits, else gh heads
 // of one sequence; groups are balanced in size.
 constexpr size_t kAttnScoreCap = size_t(1) << 30;
+constexpr size_t kAttnFlagBytes = 256;   // the non-finite counts, after the score buffers
 struct AttnGroups {
     int64_t gb, gh;       // sequences and heads a group spans (gb > 1 only when gh == heads)
     size_t score_bytes;   // one score buffer of the largest group, 256-byte rounded
@@ -391,7 +392,7 @@ HeadOperand head_operand(const float *buf, int64_t ld, int64_t width, int64_t ba
 cudaError_t group_gemm(int64_t M, int64_t N, int64_t K, const HeadOperand &a, int tA,
                        const HeadOperand &b, int tB, float *c, int64_t ldc, int64_t c_zb,
                        int64_t c_zh, int64_t count, int64_t inner, int causal,
-                       cudaStream_t s) {
+                       cudaStream_t s, int tri = 0, const int *tri_bad = nullptr) {
     GemmArgs g;
     g.M = M; g.N = N; g.K = K;
     g.A = a.base; g.lda = a.ld; g.B = b.base; g.ldb = b.ld; g.C = c; g.ldc = ldc;
@@ -402,6 +403,8 @@ cudaError_t group_gemm(int64_t M, int64_t N, int64_t K, const HeadOperand &a, in
     bt.c_zb = c_zb; bt.c_zh = c_zh;
     bt.a_rows = a.rows; bt.a_cols = a.cols; bt.b_rows = b.rows; bt.b_cols = b.cols;
     bt.causal = causal;
+    bt.tri = tri;
+    bt.tri_bad = tri_bad;
     return launch_gemm_batched(g, bt, s);
 }
 
@@ -418,6 +421,17 @@ HeadOperand stacked(const float *buf, int64_t seq, int64_t nh, int64_t count) {
     return o;
 }
 
+// Zeroes the n flag words, then counts each listed operand's non-finite
+// values into its word (the triangular skips of the products that read it
+// are taken only when the count is 0).
+cudaError_t count_nonfinite_heads(int *flags, const HeadOperand *ops, int n, int64_t rows,
+                                  int64_t cols, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(flags, 0, sizeof(int) * n, s);
+    for (int i = 0; i < n && e == cudaSuccess; ++i)
+        e = launch_count_nonfinite(rows, cols, ops[i].base, ops[i].ld, flags + i, s);
+    return e;
+}
+
 bool attention_args_ok(int64_t batch, int64_t seq, int64_t heads, int64_t head_dim) {
     return batch >= 0 && seq >= 1 && seq <= 65536 && heads >= 1 && heads <= 65536 &&
            head_dim >= 1 && head_dim <= 65536 && batch <= kDimMax / seq &&
@@ -431,7 +445,7 @@ DET_API det_status detattention_workspace_bytes(const det_profile_v1 *prof, int6
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
     if (!bytes || !attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
-    *bytes = attention_groups(batch, seq, heads).score_bytes;
+    *bytes = attention_groups(batch, seq, heads).score_bytes + kAttnFlagBytes;
     return DET_OK;
 }
 
@@ -448,10 +462,11 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
     if (!qkv || !out || ldqkv < 3 * hd || ldout < hd) return DET_ERR_INVALID_ARG;
     if ((st = check_device()) != DET_OK) return st;
     const AttnGroups g = attention_groups(batch, seq, heads);
-    if (!workspace || workspace_bytes < g.score_bytes ||
+    if (!workspace || workspace_bytes < g.score_bytes + kAttnFlagBytes ||
         reinterpret_cast<uintptr_t>(workspace) % 256)
         return DET_ERR_WORKSPACE;
     float *S = static_cast<float *>(workspace);
+    int *flags = reinterpret_cast<int *>(static_cast<char *>(workspace) + g.score_bytes);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t e = for_each_group(batch, heads, g, [&](int64_t b0, int64_t nb, int64_t h0,
                                                               int64_t nh) {
@@ -464,9 +479,11 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
                                    1, s);
         if (r == cudaSuccess)
             r = launch_softmax_causal(count * seq, seq, S, seq, scale, 0, seq, S, seq, s);
+        // P is +0 above the diagonal: with a finite V the chunks there are skipped
+        if (r == cudaSuccess) r = count_nonfinite_heads(flags, &V, 1, nb * seq, nh * head_dim, s);
         if (r == cudaSuccess)
             r = group_gemm(seq, head_dim, seq, P, 0, V, 0, out + b0 * seq * ldout + h0 * head_dim,
-                           ldout, seq * ldout, head_dim, count, nh, 0, s);
+                           ldout, seq * ldout, head_dim, count, nh, 0, s, 1, flags);
         return r;
     });
     return from_cuda(e);
@@ -486,7 +503,7 @@ DET_API det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, 
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
     if (!bytes || !attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
-    *bytes = 2 * attention_groups(batch, seq, heads).score_bytes;
+    *bytes = 2 * attention_groups(batch, seq, heads).score_bytes + kAttnFlagBytes;
     return DET_OK;
 }
 
@@ -505,11 +522,12 @@ DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batc
         return DET_ERR_INVALID_ARG;
     if ((st = check_device()) != DET_OK) return st;
     const AttnGroups g = attention_groups(batch, seq, heads);
-    if (!workspace || workspace_bytes < 2 * g.score_bytes ||
+    if (!workspace || workspace_bytes < 2 * g.score_bytes + kAttnFlagBytes ||
         reinterpret_cast<uintptr_t>(workspace) % 256)
         return DET_ERR_WORKSPACE;
     float *Pb = static_cast<float *>(workspace);
     float *dPb = reinterpret_cast<float *>(static_cast<char *>(workspace) + g.score_bytes);
+    int *flags = reinterpret_cast<int *>(static_cast<char *>(workspace) + 2 * g.score_bytes);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t e = for_each_group(batch, heads, g, [&](int64_t b0, int64_t nb, int64_t h0,
                                                               int64_t nh) {
@@ -529,18 +547,22 @@ DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batc
         if (r == cudaSuccess)
             r = group_gemm(seq, seq, head_dim, dO, 0, V, 1, dPb, seq, dP.zb, dP.zh, count, nh, 1,
                            s);
+        // P and dS are +0 above the diagonal, so P^T and dS^T below it: with
+        // finite dO, K and Q (flags 0, 1, 2) the chunks there are skipped
+        const HeadOperand finite[3] = {dO, K, Q};
+        if (r == cudaSuccess) r = count_nonfinite_heads(flags, finite, 3, nb * seq, nh * head_dim, s);
         if (r == cudaSuccess)   // dV = P^T dO
             r = group_gemm(seq, head_dim, seq, P, 1, dO, 0, dbase + 2 * hd, lddqkv, dzb,
-                           head_dim, count, nh, 0, s);
+                           head_dim, count, nh, 0, s, 2, flags);
         if (r == cudaSuccess)   // dS in place of dP
             r = launch_softmax_causal_bwd(count * seq, seq, Pb, dPb, seq, scale, 0, seq, dPb, seq,
                                           s);
         if (r == cudaSuccess)   // dQ = dS K
             r = group_gemm(seq, head_dim, seq, dP, 0, K, 0, dbase, lddqkv, dzb, head_dim, count,
-                           nh, 0, s);
+                           nh, 0, s, 1, flags + 1);
         if (r == cudaSuccess)   // dK = dS^T Q
             r = group_gemm(seq, head_dim, seq, dP, 1, Q, 0, dbase + hd, lddqkv, dzb, head_dim,
-                           count, nh, 0, s);
+                           count, nh, 0, s, 2, flags + 2);
         return r;
     });
     return from_cuda(e);

@@ -60,7 +60,16 @@ struct GemmBatch {
     int64_t a_zb = 0, a_zh = 0, b_zb = 0, b_zh = 0, c_zb = 0, c_zh = 0;
     int64_t a_rows = 0, a_cols = 0, b_rows = 0, b_cols = 0;
     int causal = 0;
+    // op(A) triangular with exact +0 outside (1: above the diagonal, 2: below;
+    // square products only): whole chunks of those zeros are skipped when
+    // *tri_bad == 0 at run time, i.e. when every op(B) value is finite.
+    int tri = 0;
+    const int *tri_bad = nullptr;
 };
+// Counts into *bad (atomically) the non-finite values of a rows x cols block
+// at base (row stride ld). *bad must be zeroed before.
+cudaError_t launch_count_nonfinite(int64_t rows, int64_t cols, const float *base, int64_t ld,
+                                   int *bad, cudaStream_t s);
 cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s);
 cudaError_t gemm_watchdog(unsigned int *code, int clear);
 cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s);

@@ -121,6 +121,15 @@ struct KArgs {
     // (row-major over those tiles); the others are left unwritten.
     int causal;
     int live_tiles;    // tiles computed per product
+    // Triangular op(A) (square, batched only): tri 1: op(A)[i][k] = +0 for
+    // k > i, so the chunks after a row tile's last row are skipped; tri 2:
+    // op(A)[i][k] = +0 for k < i, so the chunks before its first row are. A
+    // skipped chunk's partial would be +0 and leaves the left-to-right sum
+    // unchanged, but only when every op(B) value it meets is finite (0 * inf
+    // is NaN): the kernel skips only if *tri_bad == 0, a count of non-finite
+    // op(B) values written before the launch.
+    int tri;
+    const int *tri_bad;
 };
 
 __device__ __forceinline__ int64_t z_offset(int64_t zb_stride, int64_t zh_stride, int z,
@@ -404,14 +413,42 @@ __device__ __forceinline__ int causal_row_tiles(int mb, int nt) {
     return min(nt, (mb * BM + BM - 1) / BN + 1);
 }
 
-__device__ __forceinline__ Unit unit_of(const KArgs &p, int u, int nkt) {
+// BATCH: the kernel instance for batched products (z, causal and triangular
+// modes); the plain instance compiles none of that in.
+template <bool BATCH>
+__device__ __forceinline__ Unit unit_of(const KArgs &p, int u, int nkt, bool tri_on) {
+    if (BATCH && tri_on) {
+        // Triangular products (never split, never causal) differ in work by
+        // row tile: units go out in descending work (tri 1: last row tile
+        // first; tri 2: first row tile first), and every other full round of
+        // the grid runs backwards, so each CTA's units mix long and short.
+        const int G = int(gridDim.x), U = p.mt * p.nt * p.zcount;
+        const int j = u / G, b = u - j * G;
+        const int r = ((j & 1) && (j + 1) * G <= U) ? j * G + (G - 1 - b) : u;
+        const int per = p.zcount * p.nt;
+        const int level = r / per, rest = r - level * per;
+        const int mb = p.tri == 1 ? p.mt - 1 - level : level;
+        const int nb = rest % p.nt;
+        Unit w;
+        w.z = rest / p.nt;
+        w.t = mb * p.nt + nb;
+        w.m0 = mb * BM;
+        w.n0 = nb * BN;
+        w.kt0 = 0;
+        w.kt1 = nkt;
+        if (p.tri == 1)
+            w.kt1 = min(nkt, ((mb * BM + BM - 1) / kKChunk + 1) * TILES_PER_CHUNK);
+        else
+            w.kt0 = ((mb * BM) / kKChunk) * TILES_PER_CHUNK;
+        return w;
+    }
     const int ntiles = p.live_tiles;
     const int per_z = ntiles * p.units_per_tile;
-    const int z = u / per_z;
+    const int z = BATCH ? u / per_z : 0;
     u -= z * per_z;
     const int t = u % ntiles, g = u / ntiles;
     int mb, nb;
-    if (p.causal) {
+    if (BATCH && p.causal) {
         mb = 0;
         int first = 0;
         while (first + causal_row_tiles(mb, p.nt) <= t) first += causal_row_tiles(mb++, p.nt);
@@ -483,7 +520,7 @@ struct Producer {
     Unit u;
 };
 
-template <bool A_KM, bool B_KM, bool TMA, bool SPLIT>
+template <bool A_KM, bool B_KM, bool TMA, bool SPLIT, bool BATCH>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB, const KArgs p) {
@@ -508,11 +545,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int nunits = p.live_tiles * p.units_per_tile * p.zcount;
     const int my_units = (nunits - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);
     const int nkt = (p.K + BK - 1) / BK;
+    const bool tri_on = BATCH && p.tri != 0 && *p.tri_bad == 0;
 
     // producer (thread 0): issues the next k-tile of its unit sequence into a slot
     auto issue_next = [&](int slot) {
         int ar = 0, ac = 0, br = 0, bc = 0;
-        if (p.zcount > 1) {
+        if (BATCH && p.zcount > 1) {
             const int64_t ao = z_offset(p.a_zb, p.a_zh, prod.u.z, p.zinner);
             const int64_t bo = z_offset(p.b_zb, p.b_zh, prod.u.z, p.zinner);
             ar = int(ao / p.lda); ac = int(ao % p.lda);
@@ -523,7 +561,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         ++prod.count;
         if (++prod.kt == prod.u.kt1) {
             if (++prod.ui < my_units) {
-                prod.u = unit_of(p, blockIdx.x + prod.ui * gridDim.x, nkt);
+                prod.u = unit_of<BATCH>(p, blockIdx.x + prod.ui * gridDim.x, nkt, tri_on);
                 prod.kt = prod.u.kt0;
             } else {
                 prod.more = 0;
@@ -542,7 +580,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             prod.count = 0;
             prod.more = my_units > 0;
             if (prod.more) {
-                prod.u = unit_of(p, blockIdx.x, nkt);
+                prod.u = unit_of<BATCH>(p, blockIdx.x, nkt, tri_on);
                 prod.kt = prod.u.kt0;
             }
             for (int s = 0; s < STAGES && prod.more; ++s) issue_next(s);
@@ -553,7 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int64_t it = 0;            // consumer position in the k-tile sequence
     bool aborted = false;
     for (int ui = 0; ui < my_units && !aborted; ++ui) {
-        const Unit w = unit_of(p, blockIdx.x + ui * gridDim.x, nkt);
+        const Unit w = unit_of<BATCH>(p, blockIdx.x + ui * gridDim.x, nkt, tri_on);
         float acc[TM][TN];
 #pragma unroll
         for (int r = 0; r < TM; ++r)
@@ -570,10 +608,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                                         &abort_flag);
             } else {
                 __syncthreads();   // everyone is done with the previous k-tile
-                load_tile_plain<A_KM, BM>(stages, p.A + z_offset(p.a_zb, p.a_zh, w.z, p.zinner),
+                load_tile_plain<A_KM, BM>(stages,
+                                          p.A + (BATCH ? z_offset(p.a_zb, p.a_zh, w.z, p.zinner) : 0),
                                           p.lda, p.M, p.K, w.m0, kt * BK, tid);
                 load_tile_plain<B_KM, BN>(stages + A_FLOATS,
-                                          p.B + z_offset(p.b_zb, p.b_zh, w.z, p.zinner), p.ldb,
+                                          p.B + (BATCH ? z_offset(p.b_zb, p.b_zh, w.z, p.zinner) : 0),
+                                          p.ldb,
                                           p.N, p.K, w.n0, kt * BK, tid);
                 __syncthreads();
             }
@@ -587,7 +627,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mma_partial<A_KM, B_KM>(As, Bs, kcount, arow, bcol, acc);
                 }
             }
-            const bool last = (kt == nkt - 1);
+            // the unit's last k-tile; a batched tile's chunks run from w.kt0 (0
+            // unless skipped) to w.kt1 (nkt unless skipped)
+            const bool last = (SPLIT || !BATCH) ? (kt == nkt - 1) : (kt == w.kt1 - 1);
+            const int first_chunk = (SPLIT || !BATCH) ? 0 : w.kt0 / TILES_PER_CHUNK;
             if (((kt + 1) % TILES_PER_CHUNK == 0) || last) {
                 const int chunk = kt / TILES_PER_CHUNK;
                 if (SPLIT) {
@@ -606,7 +649,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int r = 0; r < TM; ++r)
 #pragma unroll
                         for (int c = 0; c < TN; ++c) acc[r][c] = 0.0f;
-                } else if (!(chunk == 0 && last)) {
+                } else if (!(chunk == first_chunk && last)) {
                     // fold the finished partial into the running total; after the
                     // last chunk acc holds the result
 #pragma unroll
@@ -615,7 +658,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int h = 0; h < TN / 4; ++h) {
                             float4 &t = totals[(r * (TN / 4) + h) * THREADS + tid];
                             float *a4 = &acc[r][4 * h];
-                            if (chunk == 0) {
+                            if (chunk == first_chunk) {
                                 t = make_float4(a4[0], a4[1], a4[2], a4[3]);
                             } else {
                                 float4 v = t;
@@ -653,7 +696,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (aborted) break;
         // epilogue (the next unit's loads are already in flight)
         if (!SPLIT)
-            store_tile<A_KM, B_KM>(acc, p.C + z_offset(p.c_zb, p.c_zh, w.z, p.zinner), p.ldc,
+            store_tile<A_KM, B_KM>(acc,
+                                   p.C + (BATCH ? z_offset(p.c_zb, p.c_zh, w.z, p.zinner) : 0),
+                                   p.ldc,
                                    p.M, p.N, w.m0, w.n0, arow, bcol,
                                    p.vec_store, p.accumulate);
     }
@@ -775,7 +820,10 @@ bool tma_ok(const float *base, int64_t ld) { return tma_operand_ok(base, ld); }
 template <bool A_KM, bool B_KM, bool TMA>
 cudaError_t launch_variant(const CUtensorMap &ma, const CUtensorMap &mb, const KArgs &k,
                            cudaStream_t s) {
-    auto kern = k.split ? gemm_kernel<A_KM, B_KM, TMA, true> : gemm_kernel<A_KM, B_KM, TMA, false>;
+    // batched products are never split
+    auto kern = k.split ? gemm_kernel<A_KM, B_KM, TMA, true, false>
+                : (k.zcount > 1 || k.causal || k.tri) ? gemm_kernel<A_KM, B_KM, TMA, false, true>
+                                                      : gemm_kernel<A_KM, B_KM, TMA, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(SMEM_BYTES));
     if (e != cudaSuccess) return e;
@@ -948,6 +996,8 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
     k.a_zb = k.a_zh = k.b_zb = k.b_zh = k.c_zb = k.c_zh = 0;
     k.causal = 0;
     k.live_tiles = k.mt * k.nt;
+    k.tri = 0;
+    k.tri_bad = nullptr;
     // op(A) is k-contiguous when A is not transposed; op(B) when B is.
     const bool a_km = !a.transA, b_km = a.transB != 0;
     CUtensorMap ma{}, mb{};
@@ -998,6 +1048,10 @@ cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStre
     k.b_zb = bt.b_zb; k.b_zh = bt.b_zh;
     k.c_zb = bt.c_zb; k.c_zh = bt.c_zh;
     k.causal = bt.causal;
+    // triangular skipping needs a square op(A) (every row tile then meets
+    // some k in range) and the flag
+    k.tri = (bt.tri && bt.tri_bad && a.M == a.K && !bt.causal) ? bt.tri : 0;
+    k.tri_bad = k.tri ? bt.tri_bad : nullptr;
     int64_t live = int64_t(k.mt) * k.nt;
     if (bt.causal) {
         live = 0;

@@ -400,10 +400,13 @@ det_status detcos_f32(const det_profile_v1 *prof, int64_t n, const float *x, flo
  * of heads x head_dim, row stride ldout >= heads head_dim). The heads run in
  * groups whose seq x seq score buffers share the workspace (at least
  * detattention_workspace_bytes for the same batch, seq, heads and head_dim,
- * 256-byte aligned; at most about 1 GiB): each step is one launch over a
- * group, and the score tiles wholly above the diagonal, which the softmax
- * masks, are not computed. Each head's bits are those of its separate
- * products. out must not overlap qkv or the workspace. batch may be 0.
+ * 256-byte aligned; at most about 1 GiB plus 256 bytes): each step is one
+ * launch over a group, and the score tiles wholly above the diagonal, which
+ * the softmax masks, are not computed. P is +0 above the diagonal, so in
+ * O = P V the 256-wide k-chunks past a row block's last row add +0 partials;
+ * they are skipped when the group's V is finite (counted on the device
+ * first), which leaves every bit unchanged. Each head's bits are those of
+ * its separate products. out must not overlap qkv or the workspace. batch may be 0.
  * Errors: DET_ERR_INVALID_ARG for seq or heads or head_dim outside 1..65536,
  * batch * seq >= 2^31, strides below their row lengths or null pointers;
  * DET_ERR_WORKSPACE for a missing, short or misaligned workspace. */
@@ -460,7 +463,8 @@ det_status detembedding_bwd_f32(const det_profile_v1 *prof, int64_t ntok, int64_
  * head, P is recomputed by the forward's spelling; dP = dO V^T, dV = P^T dO,
  * dS = detsoftmax_causal_bwd_f32(P, dP, scale), dQ = dS K, dK = dS^T Q, every
  * product with detgemm_f32's arithmetic, each step one launch over a group of
- * heads as in detattention_f32. The workspace (at least
+ * heads as in detattention_f32; dV, dQ and dK skip the +0 chunks of P and dS
+ * when dO, K and Q are finite. The workspace (at least
  * detattention_bwd_workspace_bytes, 256-byte aligned) holds two score
  * buffers of a group. dqkv must not overlap qkv, dout or the workspace.
  * Errors as detattention_f32. */

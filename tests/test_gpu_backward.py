@@ -108,12 +108,22 @@ def attention_bwd_oracle(qkv, dout, b, h, seq, heads, d, scale):
     return oracle.gemm(dS, K), oracle.gemm(dS, Q, transA=True), dV
 
 
-@pytest.mark.parametrize("B,T,H,d,checks", [(2, 100, 3, 16, None), (4, 2048, 12, 64,
-                                                                     [(0, 0), (3, 11)])])
-def test_attention_bwd(dev, B, T, H, d, checks):
+@pytest.mark.parametrize("B,T,H,d,checks,poison", [
+    (2, 100, 3, 16, None, None), (4, 2048, 12, 64, [(0, 0), (3, 11)], None),
+    # 3 chunks of k: dV, dQ and dK skip the +0 chunks of P and dS when dO, K and
+    # Q are finite, and must take them all when one holds an inf or a NaN
+    (1, 600, 2, 16, None, None), (1, 600, 2, 16, None, "dout"), (1, 600, 2, 16, None, "k"),
+    (1, 600, 2, 16, None, "q")])
+def test_attention_bwd(dev, B, T, H, d, checks, poison):
     rng = np.random.default_rng(T + H)
     qkv = rng.standard_normal((B * T, 3 * H * d)).astype(F)
     dout = rng.standard_normal((B * T, H * d)).astype(F)
+    if poison == "dout":
+        dout[500, 3] = np.inf
+    elif poison == "k":
+        qkv[520, H * d + 2] = np.nan
+    elif poison == "q":
+        qkv[10, 1] = -np.inf
     scale = 1.0 / np.sqrt(d)
     got = host(detlib.detattention_bwd_f32(to_dev(qkv), to_dev(dout), B, T, H, d))
     pairs = checks or [(b, h) for b in range(B) for h in range(H)]

@@ -142,6 +142,28 @@ def test_attention_small_in_full(dev):
             assert_bitwise(out[b * T:(b + 1) * T, h * d:(h + 1) * d], want, f"b={b} h={h}")
 
 
+@pytest.mark.parametrize("poison", [False, True])
+def test_attention_chunks_above_the_diagonal(dev, poison):
+    # 600 tokens: 3 chunks of k, so P.V skips the +0 chunks past each row
+    # block when V is finite. With an inf and a NaN in V (0 * inf = NaN) every
+    # chunk must be taken, as in the oracle.
+    rng = np.random.default_rng(95)
+    B, T, H, d = 2, 600, 2, 16
+    hd = H * d
+    qkv = rng.standard_normal((B * T, 3 * H * d)).astype(F)
+    if poison:
+        qkv[550, 2 * hd + 3] = np.inf              # sequence 0, head 0
+        qkv[T + 300, 2 * hd + d + 5] = np.nan      # sequence 1, head 1
+    out = host(detlib.detattention_f32(to_dev(qkv), B, T, H, d, scale=0.25))
+    for b in range(B):
+        for h in range(H):
+            want = attention_oracle(qkv, b, h, T, H, d, 0.25)
+            assert_bitwise(out[b * T:(b + 1) * T, h * d:(h + 1) * d], want,
+                           f"b={b} h={h} poison={poison}")
+    if poison:
+        assert np.isnan(out[:550, 3]).all()           # 0 * inf reached every row before it
+
+
 def test_attention_162m_shape_sampled_heads(dev):
     # 4 sequences of 2048 tokens, 12 heads of 64, scale 1/8: two heads checked
     rng = np.random.default_rng(95)
