@@ -173,6 +173,25 @@ def test_xent_exp_rounding_ties(dev):
         assert_bitwise(host(dl), d_w, f"dlogits dscale={dscale}")
 
 
+def test_xent_exp_ties_rows_without_underflow(dev):
+    # the ties of rint(d LOG2E) in rows whose every x - m is >= -86 (no element
+    # near underflow), max 0 and max 7.25
+    d = exp_tie_arguments()
+    d = d[d >= F(-85.9)]
+    assert d.size > 100
+    V = d.size + 1
+    x = np.zeros((2, V), F)
+    x[0, 1:] = d
+    x[1, 0] = F(7.25)
+    x[1, 1:] = d + F(7.25)
+    assert (x[1, 1:] - x[1, 0]).min() >= -86.0
+    lab = np.array([0, 5], np.int32)
+    loss_w, d_w, _ = oracle.xent(x, lab, with_dlogits=True, dscale=F(1.0))
+    loss, _, dl = detlib.detxent_f32(to_dev(x), to_dev(lab), want_dlogits=True, dscale=1.0)
+    assert_bitwise(host(loss), loss_w)
+    assert_bitwise(host(dl), d_w)
+
+
 @pytest.mark.parametrize("layout", ["dense", "offset"])
 def test_xent_rows_longer_than_shared_memory(dev, layout):
     # rows of more than ~57,600 floats take the register/L2 kernel
