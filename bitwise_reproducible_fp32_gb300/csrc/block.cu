@@ -119,15 +119,11 @@ __device__ __forceinline__ float butterfly32(float s) {
 // g = ch, ch + 256, ... of the kept columns and adds them in ascending order;
 // the 32 chains of each w fold by the butterfly and the 8 totals by the tree
 // ((t0 + t1) + (t2 + t3)) + ((t4 + t5) + (t6 + t7)), as with a thread a chain
-// and a warp per 32 chains. Segment sg of a row (groups 256 sg .. 256 sg +
-// 255, columns 1024 sg ..) is held in registers for sg < kSmaxCache, so the
-// first 2048 columns (1024 in the backward, which holds two arrays) are read
-// once; later segments are read again.
-// Two CTAs an SM (at most 128 registers a thread) measured fastest: 414 us
-// for 48 x 2048 rows of 2048 against 582 us at one CTA (206 registers) and
-// 426-481 us with one cached segment at three or four CTAs.
-constexpr int kSmaxMinBlocks = 2;
-constexpr int kSmaxCache = 2;
+// and a warp per 32 chains. Segment sg of a row is groups 256 sg .. 256 sg +
+// 255 (columns 1024 sg ..). The backward holds its first segment of P and dP
+// in registers (kSmaxBwdCache) and reads later segments again; the forward
+// reads its row in each pass (see there).
+constexpr int kSmaxMinBlocks = 4;     // the forward: 56 registers a thread
 constexpr int kSmaxBwdCache = 1;
 constexpr int kSmaxWarps = 8;
 
@@ -198,8 +194,12 @@ __device__ __forceinline__ int64_t kept_columns(int64_t r, int64_t period, int64
 }
 
 // Causal softmax: pass 1 the max of x = s * scale (order free), pass 2 the
-// chains of exp(x - max) (the cached values become the exps), pass 3
-// p = e * (1 / S).
+// chains of exp(x - max), pass 3 p = exp(x - max) * (1 / S), the exps formed
+// again (the same bits). Each pass reads the row again: it stays in L1
+// between the passes, and the warp's next row is prefetched into L2. Holding
+// the first 2048 columns in registers instead (128 a thread, two CTAs an SM)
+// measured slower: 416 against 373 us for 48 x 2048 rows of 2048 at 56
+// registers and four CTAs an SM (six or eight CTAs: 399 and 424 us).
 __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
     softmax_causal_kernel(int64_t rows, int64_t cols, const float *s, int64_t lds, float scale,
                           int64_t diag, int64_t period, float *p, int64_t ldp, int vec_s,
@@ -220,7 +220,6 @@ __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
         zero_masked(pr, nr, cols, lane, vec_p);
         if (nr == 0) continue;     // uniform across the warp
         const int64_t nseg = (nr + 1023) / 1024;
-        float4 xc[kSmaxCache][8];
         auto scaled = [&](int64_t j) {
             float4 v = ld4_kept(sr, j, nr, vec_s);
             v.x = __fmul_rn(v.x, scale); v.y = __fmul_rn(v.y, scale);
@@ -230,22 +229,15 @@ __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
         auto col = [&](int64_t sg, int w) { return 4 * (int64_t(lane) + 32 * w + 256 * sg); };
         // pass 1
         float m = __fmul_rn(sr[0], scale);
-        auto take_max = [&](float4 v, int64_t j) {
-            if (j < nr) m = max_nan2(m, v.x);
-            if (j + 1 < nr) m = max_nan2(m, v.y);
-            if (j + 2 < nr) m = max_nan2(m, v.z);
-            if (j + 3 < nr) m = max_nan2(m, v.w);
-        };
-#pragma unroll
-        for (int sg = 0; sg < kSmaxCache; ++sg)
-            if (sg < nseg)
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    xc[sg][w] = scaled(col(sg, w));
-                    take_max(xc[sg][w], col(sg, w));
-                }
-        for (int64_t sg = kSmaxCache; sg < nseg; ++sg)
-            for (int w = 0; w < 8; ++w) take_max(scaled(col(sg, w)), col(sg, w));
+        for (int64_t sg = 0; sg < nseg; ++sg)
+            for (int w = 0; w < 8; ++w) {
+                const int64_t j = col(sg, w);
+                const float4 v = scaled(j);
+                if (j < nr) m = max_nan2(m, v.x);
+                if (j + 1 < nr) m = max_nan2(m, v.y);
+                if (j + 2 < nr) m = max_nan2(m, v.z);
+                if (j + 3 < nr) m = max_nan2(m, v.w);
+            }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1)
             m = max_nan2(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -255,49 +247,31 @@ __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
         for (int w = 0; w < 8; ++w) c[w] = 0.0f;
         // with a finite max every x - m <= 0: the branch-free exp4 (same bits)
         const bool finite_max = fabsf(m) <= 0x1.fffffep127f;
-        auto exps = [&](float4 &v, int64_t j, float &cw) {
-            if (finite_max) {
-                v = exp4(v, m);
-            } else {
-                v.x = det_exp_call(__fsub_rn(v.x, m));
-                v.y = det_exp_call(__fsub_rn(v.y, m));
-                v.z = det_exp_call(__fsub_rn(v.z, m));
-                v.w = det_exp_call(__fsub_rn(v.w, m));
-            }
-            if (j < nr) cw = __fadd_rn(cw, v.x);
-            if (j + 1 < nr) cw = __fadd_rn(cw, v.y);
-            if (j + 2 < nr) cw = __fadd_rn(cw, v.z);
-            if (j + 3 < nr) cw = __fadd_rn(cw, v.w);
+        auto exps = [&](int64_t j) {
+            const float4 v = scaled(j);
+            if (finite_max) return exp4(v, m);
+            return make_float4(det_exp_call(__fsub_rn(v.x, m)), det_exp_call(__fsub_rn(v.y, m)),
+                               det_exp_call(__fsub_rn(v.z, m)), det_exp_call(__fsub_rn(v.w, m)));
         };
-#pragma unroll
-        for (int sg = 0; sg < kSmaxCache; ++sg)
-            if (sg < nseg)
-#pragma unroll
-                for (int w = 0; w < 8; ++w) exps(xc[sg][w], col(sg, w), c[w]);
-        for (int64_t sg = kSmaxCache; sg < nseg; ++sg)
+        for (int64_t sg = 0; sg < nseg; ++sg)
 #pragma unroll
             for (int w = 0; w < 8; ++w) {
-                float4 v = scaled(col(sg, w));
-                exps(v, col(sg, w), c[w]);
+                const int64_t j = col(sg, w);
+                const float4 e = exps(j);
+                if (j < nr) c[w] = __fadd_rn(c[w], e.x);
+                if (j + 1 < nr) c[w] = __fadd_rn(c[w], e.y);
+                if (j + 2 < nr) c[w] = __fadd_rn(c[w], e.z);
+                if (j + 3 < nr) c[w] = __fadd_rn(c[w], e.w);
             }
         const float inv = __fdiv_rn(1.0f, fold_chains(c));
         // pass 3
-        auto prob = [&](float4 e) {
-            return make_float4(__fmul_rn(e.x, inv), __fmul_rn(e.y, inv), __fmul_rn(e.z, inv),
-                               __fmul_rn(e.w, inv));
-        };
-#pragma unroll
-        for (int sg = 0; sg < kSmaxCache; ++sg)
-            if (sg < nseg)
-#pragma unroll
-                for (int w = 0; w < 8; ++w)
-                    st4_kept(pr, col(sg, w), nr, vec_p, prob(xc[sg][w]));
-        for (int64_t sg = kSmaxCache; sg < nseg; ++sg)
+        for (int64_t sg = 0; sg < nseg; ++sg)
             for (int w = 0; w < 8; ++w) {
-                float4 v = scaled(col(sg, w));
-                float unused = 0.0f;
-                exps(v, col(sg, w), unused);
-                st4_kept(pr, col(sg, w), nr, vec_p, prob(v));
+                const int64_t j = col(sg, w);
+                const float4 e = exps(j);
+                st4_kept(pr, j, nr, vec_p,
+                         make_float4(__fmul_rn(e.x, inv), __fmul_rn(e.y, inv),
+                                     __fmul_rn(e.z, inv), __fmul_rn(e.w, inv)));
             }
     }
 }
