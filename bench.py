@@ -14,6 +14,7 @@ One step = one pass of every operation of the path over one batch of the
   out projection, residual, RMSNorm, SwiGLU, down projection, residual) ->
   one training step of the byte-level LM (16 x 128 tokens, two blocks of 64:
   forward, backward, AdamW) ->
+  the 12-layer 162M decoder's forward with its loss (4 x 2048 tokens) ->
   AdamW over 162,147,840 parameters.
 Inputs are synthetic and seeded (bitwise_reproducible_fp32_gb300.inputs).
 
@@ -52,7 +53,8 @@ WORKLOAD = ("162M-decoder FP32 step: RMSNorm 8192x768, forward GEMMs "
             "(768x2304, 2048x768), fixed-order sum of 64 shard gradients of the "
             "768x2304 weight, one decoder block forward (4x2048 tokens, RoPE, causal "
             "attention 12x64, SwiGLU), one byte-level LM training step (16x128 tokens, "
-            "2 blocks of 64), AdamW 162,147,840 params")
+            "2 blocks of 64), the 12-layer 162M decoder forward with loss (4x2048 "
+            "tokens), AdamW 162,147,840 params")
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
 
@@ -248,6 +250,19 @@ def run_ours(args, rank, world, local_rank):
     bld["labels"] = torch.from_numpy(bl["labels"]).to(dev)
     bld["emb"], bld["head"] = up(bl["emb"]), up(bl["head"])
     bld["blocks"] = [{k: up(v) for k, v in b.items()} for b in bl["blocks"]]
+    # the 12-layer 162M decoder's forward (the byte-LM composition at the
+    # model card's shapes): weights resident, buffers and workspaces built once
+    dm = inputs.decoder_162m()
+    dmd = dict(dm)
+    dmd["tokens"] = torch.from_numpy(dm["tokens"]).to(dev)
+    dmd["labels"] = torch.from_numpy(dm["labels"]).to(dev)
+    dmd["emb"], dmd["head"] = up(dm["emb"]), up(dm["head"])
+    dmd["blocks"] = [{k: up(v) for k, v in b.items()} for b in dm["blocks"]]
+    dm_blocks = byte_lm.make_blocks(dmd, dev)
+    dm_ntok = dm["batch"] * dm["seq"]
+    dm_head_ws = detlib.gemm_workspace(dm_ntok, dm["vocab"], dm["d"], False, True, device=dev)
+    dm_flops = (len(dm_blocks) * dm_blocks[0].flops()
+                + inputs.flops_gemm(dm_ntok, dm["vocab"], dm["d"]))
     P, G, Mm, Vv = (up(aw[k]) for k in ("p", "g", "m", "v"))
     hp = {k: aw[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")}
     # L2 flush: write 512 MB, then read another 512 MB so the L2 holds clean
@@ -302,12 +317,15 @@ def run_ours(args, rank, world, local_rank):
                                          (d_b, 3 * d_b)))
     byte_lm_launches = (1 + nb * (11 + 4 * gb) + 1 + 2 + dw_n(bl["vocab"], d_b) + 1
                         + nb * (13 + blk_dw + 10 * gb) + 1 + 2 + 7 * nb)
+    # the 162M decoder forward: the embedding, 12 blocks as above, the head
+    # GEMM (with its transposed copy of the activations), cross-entropy + mean
+    decoder_launches = 1 + len(dm_blocks) * block_launches + gemm_n(dm_head_ws) + 2
     launches_per_step = (1 + sum(gemm_n(w) for w in ws_fwd) + 2 + 2
                          + sum(gemm_n(w) for w in ws_dw) + 1 + block_launches
-                         + byte_lm_launches + 1)
+                         + byte_lm_launches + decoder_launches + 1)
 
     segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "rmsnorm_bwd", "gemm_dw",
-            "shard_sum", "block_fwd", "byte_lm_step", "adamw"]
+            "shard_sum", "block_fwd", "byte_lm_step", "forward_162m", "adamw"]
 
     def step(ev=None):
         def mark(i):
@@ -341,8 +359,10 @@ def run_ours(args, rank, world, local_rank):
         mark(8)
         byte_lm.train_step(bld, dev, inputs.BYTE_LM_HP)
         mark(9)
-        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
+        byte_lm.forward(dmd, dev, blocks=dm_blocks, head_ws=dm_head_ws)
         mark(10)
+        detlib.detadamw_f32(P, G, Mm, Vv, **hp)
+        mark(11)
 
     import torch.distributed as dist
     distributed = world > 1
@@ -425,6 +445,10 @@ def run_ours(args, rank, world, local_rank):
                           "ms": per("block_fwd") * 1e3},
             "byte_lm_step": {"ms": per("byte_lm_step") * 1e3,
                              "tokens_per_s": bl["batch"] * bl["seq"] / per("byte_lm_step")},
+            "forward_162m": {"ms": per("forward_162m") * 1e3,
+                             "tokens_per_s": dm_ntok / per("forward_162m"),
+                             "tflops": dm_flops / per("forward_162m") / 1e12,
+                             "frac_fp32_peak": dm_flops / per("forward_162m") / 1e12 / fma_peak},
             "shard_sum": {"gbs": bytes_shardsum(*sg.shape) / per("shard_sum") / 1e9,
                           "frac_hbm": bytes_shardsum(*sg.shape) / per("shard_sum") / 1e9 / hbm,
                           "ms": per("shard_sum") * 1e3},

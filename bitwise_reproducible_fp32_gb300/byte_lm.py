@@ -67,21 +67,36 @@ def train_step(c, device, hp):
     return st
 
 
-def forward(c, device):
-    """The forward stages alone (embedding, blocks, logits, loss, mean)."""
+def make_blocks(c, device):
+    """The Block objects (activation buffers and GEMM workspaces) of a model
+    configuration, one a layer; built once, they serve every forward call."""
+    from bitwise_reproducible_fp32_gb300 import block
+    return [block.Block(c["batch"], c["seq"], c["d"], c["dff"], c["heads"], device)
+            for _ in c["blocks"]]
+
+
+def forward(c, device, blocks=None, head_ws=None):
+    """The forward stages alone (embedding, blocks, logits, loss, mean). The
+    same code runs the byte-level LM and the 12-layer 162M decoder (the two
+    share the architecture: pre-norm blocks, no final norm, untied head).
+    blocks / head_ws: prebuilt make_blocks() and the head GEMM's workspace
+    (built here when omitted)."""
     import torch
 
-    from bitwise_reproducible_fp32_gb300 import block, detlib as L
-    B, T, d = c["batch"], c["seq"], c["d"]
+    from bitwise_reproducible_fp32_gb300 import detlib as L
     status = torch.zeros(1, dtype=torch.int32, device=device)
     st = {}
     x = L.detembedding_f32(c["emb"], c["tokens"], dev_status=status)
     st["embedding"] = x
-    blocks = [block.Block(B, T, d, c["dff"], c["heads"], device) for _ in c["blocks"]]
+    if blocks is None:
+        blocks = make_blocks(c, device)
+    if head_ws is None:
+        head_ws = L.gemm_workspace(c["batch"] * c["seq"], c["vocab"], c["d"], False, True,
+                                   device=device)
     for i, (blk, w) in enumerate(zip(blocks, c["blocks"])):
         x = blk.forward(x, w)          # each block owns its output buffer
         st[f"block{i}"] = x
-    logits = L.detgemm_f32(x, c["head"], transB=True)
+    logits = L.detgemm_f32(x, c["head"], transB=True, workspace=head_ws)
     st["logits"] = logits
     loss, mean, _ = L.detxent_f32(logits, c["labels"], want_mean=True, dev_status=status)
     st["loss"], st["loss_mean"] = loss, mean

@@ -183,7 +183,7 @@ def block_cfg(seed: int = SEED_BLOCK, batch: int = 4, seq: int = 2048, d: int = 
 
 
 def byte_lm_cfg2(seed: int = SEED_CFG2 + 100, batch: int = 16, seq: int = 128, d: int = 64,
-                 dff: int = 172, vocab: int = 256, blocks: int = 2):
+                 dff: int = 172, vocab: int = 256, blocks: int = 2, heads: int = 4):
     """The small byte-level language model at the byte-LM GEMM shapes (16 x 128
     tokens, 64 wide, SwiGLU 172, 256 byte ids, two blocks): byte tokens uniform in
     [0, 256) for 129 positions a sequence (inputs: the first 128, labels: the
@@ -207,7 +207,18 @@ def byte_lm_cfg2(seed: int = SEED_CFG2 + 100, batch: int = 16, seq: int = 128, d
     head = normal(rng, (vocab, d), 0.02)
     return dict(tokens=np.ascontiguousarray(toks[:, :seq]).reshape(-1),
                 labels=np.ascontiguousarray(toks[:, 1:]).reshape(-1), emb=emb, blocks=blks,
-                head=head, batch=batch, seq=seq, d=d, dff=dff, vocab=vocab, heads=4)
+                head=head, batch=batch, seq=seq, d=d, dff=dff, vocab=vocab, heads=heads)
+
+
+def decoder_162m(layers: int = 12, batch: int = 4, seq: int = 2048, seed: int = 9):
+    """The 162M decoder ("MojoLearn 162M" model card, table "Compared with GPT-3
+    Small": 12 layers, 768 wide, 12 heads of 64, SwiGLU 2,048, context 2,048,
+    RMSNorm pre-norm with no final norm, untied 50,257-id embeddings,
+    162,147,840 parameters), drawn as byte_lm_cfg2 draws its model: token ids
+    uniform in [0, 50257) for seq + 1 positions a sequence, weights N(0, 0.02),
+    gains 1 + N(0, 0.02). `layers` and the token count can be cut for tests."""
+    return byte_lm_cfg2(seed=seed, batch=batch, seq=seq, d=D_MODEL, dff=D_FF, vocab=VOCAB,
+                        blocks=layers, heads=N_HEADS)
 
 
 # the byte-level LM step's update: the 162M card's AdamW at the first step
