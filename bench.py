@@ -134,7 +134,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # the raw samples (the JSON line carries their summary); the directory
+        # can be redirected with DET_BENCH_OUT
+        out = os.environ.get("DET_BENCH_OUT", os.path.join(ROOT, "bench_out"))
+        self.path = os.path.join(out, f"clocks_gpu{gpu_index}.csv")
 
     def start(self):
         try:
