@@ -149,11 +149,6 @@ __device__ __forceinline__ float4 ld4_policy(const float *p, uint64_t pol) {
                  : "l"(p), "l"(pol));
     return v;
 }
-__device__ __forceinline__ void st4_policy(float *p, float4 v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
-                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
-                 : "memory");
-}
 __device__ __forceinline__ void st_policy(float *p, float v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol)
                  : "memory");
