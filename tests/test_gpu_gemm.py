@@ -100,6 +100,9 @@ def test_transposed_a_copy_same_bits(dev, M, N, K, transB):
     run_case(M, N, K, False, bool(transB), "padded", "padded", "padded", M + K + transB)
     run_case(M, N, K, False, bool(transB), "dense", "offset", "offset", M + K + transB + 1,
              wide=True)
+    # an A whose rows are not 16-byte aligned: the copy moves it element by
+    # element, and the GEMM then stages the aligned copy by TMA
+    run_case(M, N, K, False, bool(transB), "offset", "padded", "padded", M + K + transB + 2)
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 200, 1300), (129, 77, 2049), (512, 384, 4096),
