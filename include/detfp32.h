@@ -153,10 +153,12 @@ det_status detshardsum_f32(const det_profile_v1 *prof, int64_t nshards, int64_t 
                            const float *shards, int64_t ld, float scale, float *out,
                            det_stream_t stream);
 
-/* Workspace that detgemm_f32 can use for this shape on the current device
- * (0 when splitting K would not help), written to *bytes. Same argument rules
- * as detgemm_f32; a host-only query apart from reading the device's SM
- * count. */
+/* Workspace that detgemm_f32 can use for this shape and layout on the
+ * current device, written to *bytes: the split-K chunk partials when
+ * splitting K helps, else, for a large product with transA == 0, the
+ * transposed copy of A (K x M, rows padded to 4 floats); 0 when neither
+ * helps. Same argument rules as detgemm_f32; a host-only query apart from
+ * reading the device's SM count. */
 det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA, int transB,
                                    int64_t M, int64_t N, int64_t K, size_t *bytes);
 
