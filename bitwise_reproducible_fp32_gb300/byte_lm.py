@@ -14,17 +14,23 @@ from __future__ import annotations
 PARAMS = ("g1", "W_qkv", "W_o", "g2", "W_gate", "W_up", "W_down")
 
 
-def train_step(c, device, hp):
+def train_step(c, device, hp, status=None):
     """One training step. c: the byte_lm_cfg2 tensors on the device; hp: AdamW
     hyperparameters (lr, beta1, beta2, eps, weight_decay, step). The moments
     start at zero. Returns the ordered stage dict: the forward's outputs, the
-    gradients, then every parameter and moment after the update."""
+    gradients, then every parameter and moment after the update.
+    status: an int32 device word of one element for the out-of-range token and
+    label flag; when given, the step issues no host synchronisation (the
+    caller reads the word), so it can be captured in a CUDA graph. Without it
+    the step checks the flag itself and raises."""
     import torch
 
     from bitwise_reproducible_fp32_gb300 import block, detlib as L
     B, T, d = c["batch"], c["seq"], c["d"]
     ntok = B * T
-    status = torch.zeros(1, dtype=torch.int32, device=device)
+    check = status is None
+    if check:
+        status = torch.zeros(1, dtype=torch.int32, device=device)
     st = {}
     # forward
     x0 = L.detembedding_f32(c["emb"], c["tokens"], dev_status=status)
@@ -62,7 +68,7 @@ def train_step(c, device, hp):
         v = torch.zeros_like(p)
         L.detadamw_f32(p.view(-1), grads[k].contiguous().view(-1), m.view(-1), v.view(-1), **hp)
         st[f"param.{k}"], st[f"m.{k}"], st[f"v.{k}"] = p, m, v
-    if int(status.item()) != 0:
+    if check and int(status.item()) != 0:
         raise ValueError("a token or label outside the vocabulary")
     return st
 

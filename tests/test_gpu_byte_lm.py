@@ -58,3 +58,31 @@ def test_byte_lm_training_step_stage_cards(dev):
     for name in want:
         assert_bitwise(got[name].reshape(want[name].shape), want[name], name)
         assert card(got[name]) == frozen[f"byte_lm_step/{name}"], name
+
+
+def test_byte_lm_training_step_replayed_from_a_cuda_graph(dev):
+    # the step captured once (its 120 launches) and replayed: the same 73
+    # stage cards as the eager step
+    c = inputs.byte_lm_cfg2()
+    cd = dict(c)
+    cd["tokens"] = torch.from_numpy(c["tokens"]).cuda()
+    cd["labels"] = torch.from_numpy(c["labels"]).cuda()
+    cd["emb"], cd["head"] = to_dev(c["emb"]), to_dev(c["head"])
+    cd["blocks"] = [{k: to_dev(v) for k, v in b.items()} for b in c["blocks"]]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    device = torch.device("cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):          # warm-up off the capture
+        byte_lm.train_step(cd, device, inputs.BYTE_LM_HP, status=status)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = byte_lm.train_step(cd, device, inputs.BYTE_LM_HP, status=status)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    frozen = json.load(open(os.path.join(GOLDEN, "identity_cards_v1.json")))["cards"]
+    for name, t in st.items():
+        assert card(host(t)) == frozen[f"byte_lm_step/{name}"], name
