@@ -109,6 +109,42 @@ def bytes_adamw(n):
 
 
 # ------------------------------------------------------------------ ranks
+def input_digests(groups):
+    """SHA-256 of each workload's input bytes, the arrays taken in the listed
+    order (shape and dtype included), so a result names exactly the inputs it
+    was measured on. groups: {name: [arrays]}."""
+    import hashlib
+    out = {}
+    for name, arrays in groups.items():
+        h = hashlib.sha256()
+        for a in arrays:
+            a = np.ascontiguousarray(a)
+            h.update(f"{a.dtype.str}{a.shape}".encode())
+            h.update(memoryview(a).cast("B"))
+        out[name] = h.hexdigest()
+    return out
+
+
+def workload_arrays(fwd, dw, r4, rb, sg, bc, bl, dm, aw):
+    """The input arrays of each bench workload, in draw order."""
+    def model(c):
+        arrs = [c["tokens"], c["labels"], c["emb"]]
+        for b in c["blocks"]:
+            arrs += [b[k] for k in ("g1", "W_qkv", "W_o", "g2", "W_gate", "W_up", "W_down")]
+        return arrs + [c["head"]]
+    return {
+        "gemm_forward": [a for p in fwd for a in (p["A"], p["B"])],
+        "gemm_dw": [a for p in dw for a in (p["A"], p["B"])],
+        "rowops": [r4[k] for k in ("x", "gain", "logits", "labels")],
+        "rmsnorm_bwd_dy": [rb["dy"]],
+        "shard_grads": [sg],
+        "block": [bc[k] for k in ("x", "g1", "W_qkv", "W_o", "g2", "W_gate", "W_up", "W_down")],
+        "byte_lm": model(bl),
+        "decoder_162m": model(dm),
+        "adamw": [aw[k] for k in ("p", "g", "m", "v")],
+    }
+
+
 def max_over_ranks(values, device):
     """Element-wise max of per-rank timings (every rank gets the result). The
     only collective of the benchmark: the path itself has no exchange, each
@@ -266,6 +302,7 @@ def run_ours(args, rank, world, local_rank):
     dm_head_ws = detlib.gemm_workspace(dm_ntok, dm["vocab"], dm["d"], False, True, device=dev)
     dm_flops = (len(dm_blocks) * dm_blocks[0].flops()
                 + inputs.flops_gemm(dm_ntok, dm["vocab"], dm["d"]))
+    digests = input_digests(workload_arrays(fwd, dw, r4, rb, sg, bc, bl, dm, aw))
     # the byte-level LM step is launch-bound (120 small launches): it runs as
     # a CUDA graph captured once, after an eager warm-up that builds its
     # buffers and workspaces
@@ -488,6 +525,7 @@ def run_ours(args, rank, world, local_rank):
             "vs_baseline": None,
             "dtype": "f32",
             "data": "synthetic (seeded numpy PCG64, shapes of the 162M model card)",
+            "input_sha256": digests,
             "config": {"workload": WORKLOAD, "tokens": rows4, "d_model": D4, "vocab": V,
                        "params": int(n_params), "parallelism": f"replicas{world}",
                        "l2": "flushed before every timed step (512 MB write, then 512 MB read "

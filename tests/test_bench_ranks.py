@@ -104,3 +104,27 @@ def test_gathered_shard_sum_gloo_world2():
         assert p.exitcode == 0
     want = oracle.shardsum(inputs.shard_grads(nshards=8, n=5003), scale=1.0 / 8).tobytes()
     assert out[0] == out[1] == want
+
+
+def test_input_digests_name_the_exact_inputs():
+    # the bench's per-workload SHA-256: stable, and changed by a value, the
+    # order of the arrays, or their shape
+    import hashlib
+
+    import numpy as np
+
+    import bench
+    a = np.arange(12, dtype=np.float32).reshape(3, 4)
+    b = np.ones(5, np.int32)
+    d = bench.input_digests({"w": [a, b]})["w"]
+    h = hashlib.sha256()
+    h.update(b"<f4(3, 4)")
+    h.update(a.tobytes())
+    h.update(b"<i4(5,)")
+    h.update(b.tobytes())
+    assert d == h.hexdigest()
+    assert bench.input_digests({"w": [b, a]})["w"] != d
+    assert bench.input_digests({"w": [a.reshape(4, 3), b]})["w"] != d
+    a2 = a.copy()
+    a2[1, 2] = np.nextafter(a2[1, 2], np.float32(np.inf))
+    assert bench.input_digests({"w": [a2, b]})["w"] != d
