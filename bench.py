@@ -464,6 +464,8 @@ def run_ours(args, rank, world, local_rank):
 
     if int(status.item()) != 0:
         raise SystemExit("cross-entropy reported an out-of-range label")
+    if int(bl_status.item()) != 0:
+        raise SystemExit("the byte-LM step reported an out-of-range token or label")
     if detlib.det_watchdog_status() != 0:
         raise SystemExit("a bounded device wait gave up during the run")
 

@@ -1,8 +1,10 @@
 """Builds libdetfp32.so in-tree from csrc/*.cu for sm_103a.
 
 The numerics flags are part of the profile: no FMA contraction of separate
-multiply/add (-fmad=false), no flush-to-zero (-ftz=false), IEEE division and
-square root (-prec-div=true -prec-sqrt=true), never --use_fast_math.
+multiply/add (-fmad=false on the device, -ffp-contract=off for the host code
+that forms AdamW's bias corrections), no flush-to-zero (-ftz=false), IEEE
+division and square root (-prec-div=true -prec-sqrt=true), never
+--use_fast_math.
 """
 from __future__ import annotations
 
@@ -29,7 +31,7 @@ def nvcc() -> str:
 
 def common_flags(extra=()):
     return [*ARCH, "-O3", "-lineinfo", "-std=c++17", *NUMERICS,
-            "-Xcompiler", "-fPIC,-fvisibility=hidden",
+            "-Xcompiler", "-fPIC,-fvisibility=hidden,-ffp-contract=off",
             "-I", os.path.join(ROOT, "include"), "-I", CSRC, *extra]
 
 

@@ -8,6 +8,12 @@
 //   m' = fmaf(b1, m, (1-b1) g);  v' = fmaf(b2, v, (1-b2)(g g))
 //   u  = (m'/bc1) / (sqrt(v'/bc2) + eps);  p' = fmaf(-lr, u, p (1 - lr wd))
 // with bc = 1 - b^t and b^t formed by t-1 sequential float products.
+// bc1 and bc2 are formed once on the host by adamw_bias_correction (exported
+// as det_adamw_bias_correction) and passed to the kernel, so the bias
+// corrections a caller can read through the C ABI are the ones every update
+// uses. Host float arithmetic is IEEE binary32 on both build targets
+// (x86-64 SSE, aarch64), and the library's host code is compiled without
+// contraction, so each product and the difference are rounded once.
 //
 // The kernel is HBM-bound (16 bytes read and 12 written a parameter): a
 // persistent grid of a few CTAs an SM walks the arrays as float4 with two
@@ -40,27 +46,14 @@ __device__ __forceinline__ void adamw_one(const Coef &c, float &p, float g, floa
 __global__ void __launch_bounds__(kThreads)
     adamw_kernel(int64_t n, float *__restrict__ P, const float *__restrict__ G,
                  float *__restrict__ M, float *__restrict__ Vv, float lr, float b1,
-                 float b2, float eps, float wd, int64_t step, int vec) {
-    __shared__ float sbc[2];
-    if (threadIdx.x == 0) {
-        // b^t by t-1 sequential products; once the product is 0 it stays 0
-        float p1 = b1, p2 = b2;
-        for (int64_t t = 2; t <= step; ++t) {
-            p1 = __fmul_rn(p1, b1);
-            p2 = __fmul_rn(p2, b2);
-            if (p1 == 0.0f && p2 == 0.0f) break;
-        }
-        sbc[0] = __fsub_rn(1.0f, p1);
-        sbc[1] = __fsub_rn(1.0f, p2);
-    }
-    __syncthreads();
+                 float b2, float eps, float wd, float bc1, float bc2, int vec) {
     Coef c;
     c.lr = lr; c.b1 = b1; c.b2 = b2; c.eps = eps;
     c.omb1 = __fsub_rn(1.0f, b1);
     c.omb2 = __fsub_rn(1.0f, b2);
     c.wdf = __fsub_rn(1.0f, __fmul_rn(lr, wd));
-    c.bc1 = sbc[0];
-    c.bc2 = sbc[1];
+    c.bc1 = bc1;
+    c.bc2 = bc2;
 
     const int64_t tid = blockIdx.x * int64_t(kThreads) + threadIdx.x;
     const int64_t nth = int64_t(gridDim.x) * kThreads;
@@ -108,6 +101,23 @@ __global__ void __launch_bounds__(kThreads)
 
 }  // namespace
 
+// beta^t by t-1 sequential float products, then 1 - beta^t, for both betas.
+// Once a product stops changing (0, 1, or a subnormal that beta maps to
+// itself) every later product is the same, so the loop may stop there: the
+// result is that of all t-1 products.
+void adamw_bias_correction(int64_t step, float beta1, float beta2, float *bc1, float *bc2) {
+    volatile float p1 = beta1, p2 = beta2;   // each product stored, so rounded once
+    for (int64_t t = 2; t <= step; ++t) {
+        const float n1 = p1 * beta1, n2 = p2 * beta2;
+        if (n1 == p1 && n2 == p2) break;
+        p1 = n1;
+        p2 = n2;
+    }
+    const float one = 1.0f;
+    *bc1 = one - p1;
+    *bc2 = one - p2;
+}
+
 cudaError_t launch_adamw(int64_t n, float *p, const float *g, float *m, float *v,
                          const det_adamw_hp &hp, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
@@ -116,9 +126,11 @@ cudaError_t launch_adamw(int64_t n, float *p, const float *g, float *m, float *v
     const int64_t want = (n / 4 + kThreads - 1) / kThreads;
     const int64_t blocks =
         std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sm_count_current_device()) * 4));
+    float bc1 = 0.0f, bc2 = 0.0f;
+    adamw_bias_correction(hp.step, hp.beta1, hp.beta2, &bc1, &bc2);
     adamw_kernel<<<unsigned(blocks), kThreads, 0, s>>>(n, p, g, m, v, hp.lr, hp.beta1,
                                                       hp.beta2, hp.eps, hp.weight_decay,
-                                                      hp.step, vec);
+                                                      bc1, bc2, vec);
     return cudaGetLastError();
 }
 

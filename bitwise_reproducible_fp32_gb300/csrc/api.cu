@@ -50,6 +50,9 @@ det_status check_device() {
 det_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DET_OK : DET_ERR_CUDA; }
 
 constexpr int64_t kDimMax = 0x7fffffff;   // dimensions below 2^31
+
+// An AdamW decay rate in [0, 1] (NaN fails).
+bool beta_ok(float b) { return b >= 0.0f && b <= 1.0f; }
 }  // namespace
 
 int sm_count_current_device() {
@@ -675,12 +678,21 @@ DET_API det_status detxent_f32(const det_profile_v1 *prof, int64_t rows, int64_t
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+DET_API det_status det_adamw_bias_correction(int64_t step, float beta1, float beta2,
+                                             float *bc1, float *bc2) {
+    if (step < 1 || !beta_ok(beta1) || !beta_ok(beta2) || !bc1 || !bc2)
+        return DET_ERR_INVALID_ARG;
+    adamw_bias_correction(step, beta1, beta2, bc1, bc2);
+    return DET_OK;
+}
+
 DET_API det_status detadamw_f32(const det_profile_v1 *prof, int64_t n, float *p,
                                 const float *g, float *m, float *v,
                                 const det_adamw_hp *hp, det_stream_t stream) {
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
-    if (n < 0 || !hp || hp->step < 1) return DET_ERR_INVALID_ARG;
+    if (n < 0 || !hp || hp->step < 1 || !beta_ok(hp->beta1) || !beta_ok(hp->beta2))
+        return DET_ERR_INVALID_ARG;
     if (n == 0) return DET_OK;
     if (!p || !g || !m || !v) return DET_ERR_INVALID_ARG;
     if ((st = check_device()) != DET_OK) return st;

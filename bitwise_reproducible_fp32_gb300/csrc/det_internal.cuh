@@ -122,6 +122,8 @@ cudaError_t launch_exp_map(int64_t n, const float *x, float *y, int is_log,
                            cudaStream_t s);
 cudaError_t launch_adamw(int64_t n, float *p, const float *g, float *m, float *v,
                          const det_adamw_hp &hp, cudaStream_t s);
+// Host: bc = 1 - beta^t for both betas (beta^t by t-1 sequential products).
+void adamw_bias_correction(int64_t step, float beta1, float beta2, float *bc1, float *bc2);
 
 int sm_count_current_device();
 

@@ -67,6 +67,8 @@ SIGNATURES = [
                                               ctypes.POINTER(ctypes.c_size_t)]),
     ("detxent_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i64, _f,
                            _vp, _vp]),
+    ("det_adamw_bias_correction", _int, [_i64, _f, _f, ctypes.POINTER(_f),
+                                         ctypes.POINTER(_f)]),
     ("detadamw_f32", _int, [_PROF, _i64, _vp, _vp, _vp, _vp, ctypes.POINTER(AdamWHP),
                             _vp]),
     ("detexp_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
@@ -588,6 +590,18 @@ def detxent_f32(logits, labels, loss=None, want_mean=False, loss_mean=None,
 
 
 # ---------------------------------------------------------------- AdamW
+def det_adamw_bias_correction(step, beta1, beta2):
+    """(bc1, bc2) = (1 - beta1^t, 1 - beta2^t) as float32 bits, the values
+    detadamw_f32 divides by at step t. Host-only: needs no GPU."""
+    import numpy as np
+    bc1, bc2 = ctypes.c_float(), ctypes.c_float()
+    st = load().det_adamw_bias_correction(int(step), ctypes.c_float(beta1),
+                                          ctypes.c_float(beta2), ctypes.byref(bc1),
+                                          ctypes.byref(bc2))
+    _check("det_adamw_bias_correction", st)
+    return np.float32(bc1.value), np.float32(bc2.value)
+
+
 def detadamw_f32(p, g, m, v, lr, beta1, beta2, eps, weight_decay, step,
                  profile=None, stream=None):
     """In-place AdamW update of p, m, v (1-D float32 CUDA tensors)."""

@@ -301,17 +301,34 @@ typedef struct det_adamw_hp {
     int64_t step;         /* 1-based step number t (>= 1) */
 } det_adamw_hp;
 
+/* AdamW's bias corrections for step t: *bc1 = 1 - beta1^t and
+ * *bc2 = 1 - beta2^t, where beta^t is the product of t-1 sequential float
+ * multiplications (beta * beta * ... * beta, each product rounded once), and
+ * the difference is rounded once. "MojoLearn 162M" model card, table
+ * "Training": AdamW, beta (0.9, 0.95); the pages print no spelling of the
+ * correction, and this is profile v1's reading. detadamw_f32 divides by these
+ * two values, so a caller can read, check or log exactly the corrections an
+ * update uses.
+ *
+ * A host-only call (no device, no stream); bc1 and bc2 are host pointers.
+ * Errors: DET_ERR_INVALID_ARG for step < 1, a beta outside [0, 1] (or NaN) or
+ * a null pointer; nothing is written then. */
+det_status det_adamw_bias_correction(int64_t step, float beta1, float beta2,
+                                     float *bc1, float *bc2);
+
 /* One AdamW update of n parameters, in place on p, m, v (device arrays of n
  * floats; g read-only). Decoupled decay applied to every element.
  *
- * Profile v1 (a6): bc1 = 1 - beta1^t and bc2 = 1 - beta2^t, with beta^t the
- * product of t-1 sequential float multiplications; then per element
+ * Profile v1 (a6): bc1 and bc2 are det_adamw_bias_correction(hp->step,
+ * hp->beta1, hp->beta2), formed on the host at the call; then per element
  *   m' = fmaf(beta1, m, (1 - beta1) * g)
  *   v' = fmaf(beta2, v, (1 - beta2) * (g * g))
  *   u  = (m' / bc1) / (sqrtf(v' / bc2) + eps)
  *   p' = fmaf(-lr, u, p * (1 - lr * weight_decay))
  * where (1 - beta1), (1 - beta2) and (1 - lr * weight_decay) are rounded to
- * float once each. n may be 0. */
+ * float once each. n may be 0.
+ * Errors: DET_ERR_INVALID_ARG for n < 0, a null hp, hp->step < 1, a beta
+ * outside [0, 1] (or NaN), or null arrays with n > 0. */
 det_status detadamw_f32(const det_profile_v1 *prof, int64_t n, float *p,
                         const float *g, float *m, float *v,
                         const det_adamw_hp *hp, det_stream_t stream);

@@ -35,7 +35,8 @@ def test_header_declares_the_boundary():
                  "detswiglu_bwd_f32", "detsoftmax_causal_bwd_f32", "detrope_bwd_f32",
                  "detembedding_bwd_f32", "detattention_bwd_f32",
                  "detattention_bwd_workspace_bytes",
-                 "detexp_f32", "detlog_f32", "det_profile_default",
+                 "detexp_f32", "detlog_f32", "det_adamw_bias_correction",
+                 "det_profile_default",
                  "det_status_string", "det_watchdog_status"):
         assert want in names
 
@@ -192,8 +193,34 @@ def test_bad_arguments_are_refused_on_the_host(lib):
                                     dummy, 1 << 20, null) == 1
     hp = detlib.AdamWHP(1e-3, 0.9, 0.95, 1e-8, 0.1, 0)
     assert lib.detadamw_f32(p, 4, dummy, dummy, dummy, dummy, ctypes.byref(hp), null) == 1
+    hp = detlib.AdamWHP(1e-3, 1.25, 0.95, 1e-8, 0.1, 3)              # beta outside [0, 1]
+    assert lib.detadamw_f32(p, 4, dummy, dummy, dummy, dummy, ctypes.byref(hp), null) == 1
     assert lib.detexp_f32(p, -1, dummy, dummy, null) == 1
     assert lib.detexp_f32(p, 0, null, null, null) == 0
+
+
+def test_adamw_bias_correction_matches_the_oracle(lib):
+    # a host-only entry point: called here without a GPU, compared bit for bit
+    # with the oracle's own product loop ("MojoLearn 162M" model card, table
+    # "Training": beta (0.9, 0.95))
+    import numpy as np
+
+    import oracle
+    for step in (1, 2, 7, 251, 20000, 5_000_000):
+        for b1, b2 in ((0.9, 0.95), (0.5, 0.999), (0.0, 1.0), (1.0, 0.99999994)):
+            got = detlib.det_adamw_bias_correction(step, b1, b2)
+            want = oracle.adamw_bias_correction(step, b1, b2)
+            assert np.asarray(got, np.float32).view(np.uint32).tolist() == \
+                np.asarray(want, np.float32).view(np.uint32).tolist(), (step, b1, b2)
+    bc1, bc2 = ctypes.c_float(), ctypes.c_float()
+    f = lib.det_adamw_bias_correction
+    assert f(0, ctypes.c_float(0.9), ctypes.c_float(0.95), ctypes.byref(bc1),
+             ctypes.byref(bc2)) == 1                                   # step < 1
+    assert f(3, ctypes.c_float(1.5), ctypes.c_float(0.95), ctypes.byref(bc1),
+             ctypes.byref(bc2)) == 1                                   # beta > 1
+    assert f(3, ctypes.c_float(float("nan")), ctypes.c_float(0.95), ctypes.byref(bc1),
+             ctypes.byref(bc2)) == 1                                   # NaN beta
+    assert f(3, ctypes.c_float(0.9), ctypes.c_float(0.95), None, ctypes.byref(bc2)) == 1
 
 
 def test_binding_refuses_cpu_tensors(lib):
