@@ -1117,23 +1117,59 @@ static __device__ __align__(256) float4 g_static_scratch[kStaticScratchBytes / 1
 
 namespace {
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[64];   // per device: the array's device address, once looked up
+// Per device: the array's device address, and the unique id of the CUDA
+// context it was looked up in. A device reset destroys that context and the
+// module with it; the next context has another id, so the address is looked
+// up again there.
+void *g_scratch_ptr[64];
+unsigned long long g_scratch_ctx[64];
+
+typedef CUresult (*PfnCtxGetCurrent)(CUcontext *);
+typedef CUresult (*PfnCtxGetId)(CUcontext, unsigned long long *);
+PfnCtxGetCurrent g_ctx_get_current = nullptr;
+PfnCtxGetId g_ctx_get_id = nullptr;
+std::once_flag g_ctx_fns_once;
+
+// The unique id of the calling thread's current context (0 if unavailable).
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_fns_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<PfnCtxGetCurrent>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<PfnCtxGetId>(fn);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current && g_ctx_get_id && g_ctx_get_current(&ctx) == CUDA_SUCCESS && ctx &&
+        g_ctx_get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
 }  // namespace
 
 // The device address of g_static_scratch on the current device. Looked up
-// once per device (the host-side name of a __device__ array is not a device
-// address), with that device current.
+// once per device and context (the host-side name of a __device__ array is
+// not a device address), with that device current.
 static cudaError_t static_scratch(void **ptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    // 0 when no context is current yet in this thread (or the driver calls
+    // are missing): the address is then looked up, and again on the next call
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess) return e;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *ptr = g_scratch_ptr[dev];
     return cudaSuccess;

@@ -186,7 +186,10 @@ det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA, int t
  *    streams, or concurrent host threads) race on the array: order them.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current). Make that first call before any
- *    stream capture begins. */
+ *    stream capture begins. A device reset (cudaDeviceReset) unloads the
+ *    library's device code with the context; the first call after it, in
+ *    the new context, looks the address up again, so it too belongs before
+ *    any capture. */
 det_status detgemm_f32_noalloc(const det_profile_v1 *prof, int transA, int transB,
                                int64_t M, int64_t N, int64_t K,
                                const float *A, int64_t lda,

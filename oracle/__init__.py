@@ -38,6 +38,15 @@ _lock = threading.Lock()
 _lib = None
 
 
+def build_variant(defines, out_path: str) -> str:
+    """Compile det_oracle.c with extra -D flags into out_path (the test suite's
+    separating arms, which plant one mistake each). Never the shipped oracle."""
+    cc = os.environ.get("CC", "cc")
+    subprocess.run([cc, *CFLAGS, *[f"-D{d}" for d in defines], _SRC, "-o", str(out_path),
+                    "-lm", "-lpthread"], check=True)
+    return str(out_path)
+
+
 def build(force: bool = False) -> str:
     """Compile det_oracle.c into libdetoracle.so next to it; return the path."""
     if (not force and os.path.exists(_LIB)
@@ -65,7 +74,9 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        # DET_ORACLE_LIB: load another build of det_oracle.c (a separating arm
+        # of the test suite) in place of the shipped one
+        lib = ctypes.CDLL(os.environ.get("DET_ORACLE_LIB") or build())
         f32p = ctypes.POINTER(ctypes.c_float)
         i32p = ctypes.POINTER(ctypes.c_int32)
         i64 = ctypes.c_int64

@@ -24,6 +24,12 @@
  * readings implemented below are the plainest ones and are listed in the
  * repository's design notes.
  *
+ * Separating arms. Blocks under #ifdef SABOTAGE_* plant one plausible mistake
+ * each (a wrong chunk width, a reversed order, roundf for rintf, a contracted
+ * multiply-add, ...). The shipped oracle defines none of them; the test suite
+ * builds each arm into a scratch library and checks that a named pin fails,
+ * so every such pin is shown to separate the rule it guards.
+ *
  * Parity status of each function against something other than itself is kept
  * in the tests (closed forms, exact-rational brute force, double-precision
  * bounds). The bit patterns chosen by readings R14-R18 (exp/log polynomials,
@@ -73,8 +79,13 @@ int detor_fp_env_ok(void) {
  *   LOG2E  = 1/ln 2;  LN2_HI = ln 2;  LN2_LO = ln 2 - LN2_HI (exact difference,
  *   rounded);  E_k = 1/k!  (k = 0..7). */
 static const float LOG2E  = 0x1.715476p+0f;
+#ifndef SABOTAGE_EXP_LN2_SPLIT
 static const float LN2_HI = 0x1.62e430p-1f;
 static const float LN2_LO = -0x1.05c610p-29f;
+#else   /* separating arm: Cody and Waite's split with trailing zero bits */
+static const float LN2_HI = 0x1.62e400p-1f;
+static const float LN2_LO = 0x1.7f7d1cp-20f;
+#endif
 static const float E0 = 0x1p+0f, E1 = 0x1p+0f, E2 = 0x1p-1f;
 static const float E3 = 0x1.555556p-3f, E4 = 0x1.555556p-5f;
 static const float E5 = 0x1.111112p-7f, E6 = 0x1.6c16c2p-10f;
@@ -92,11 +103,16 @@ float detor_exp(float x) {
     /* x = n ln2 + r with n = round-half-even(x / ln2): the tie rule of the
      * reduction is that of rintf in round-to-nearest mode. */
     float t = x * LOG2E;
+#ifndef SABOTAGE_ROUNDF
     float n = rintf(t);
+#else   /* separating arm: ties away from zero */
+    float n = roundf(t);
+#endif
     float r = fmaf(-n, LN2_HI, x);
     r = fmaf(-n, LN2_LO, r);
     /* e^r by Horner on the degree-7 Taylor polynomial, highest term first. */
     float p = E7;
+#ifndef SABOTAGE_EXP_HORNER_UNFUSED
     p = fmaf(p, r, E6);
     p = fmaf(p, r, E5);
     p = fmaf(p, r, E4);
@@ -104,6 +120,15 @@ float detor_exp(float x) {
     p = fmaf(p, r, E2);
     p = fmaf(p, r, E1);
     p = fmaf(p, r, E0);
+#else   /* separating arm: each Horner step a rounded product, then the add */
+    p = p * r + E6;
+    p = p * r + E5;
+    p = p * r + E4;
+    p = p * r + E3;
+    p = p * r + E2;
+    p = p * r + E1;
+    p = p * r + E0;
+#endif
     /* scale by 2^n with exactly one rounding */
     int ni = (int)n;                           /* |n| <= 150, exact */
     if (ni > 127) return (p + p) * pow2f(127);             /* ni == 128 */
@@ -149,7 +174,11 @@ float detor_log(float x) {
     R = fmaf(R, z, T3);
     R = R * z;
     float h = (0.5f * u) * u;
+#ifndef SABOTAGE_CONTRACT_LOG
     float lf = u - (h - s * (h + R));
+#else   /* separating arm: h - s (h + R) contracted into one fmaf */
+    float lf = u - fmaf(-s, h + R, h);
+#endif
     float ef = (float)e;
     return fmaf(ef, LN2_HI, fmaf(ef, LN2_LO, lf));
 }
@@ -245,6 +274,9 @@ typedef struct {
 static void gemm_rows(int64_t lo, int64_t hi, int tix, void *c) {
     (void)tix;
     gemm_ctx *g = (gemm_ctx *)c;
+#ifdef SABOTAGE_CHUNK_REVERSED
+    float part[4096];
+#endif
     for (int64_t i = lo; i < hi; ++i) {
         for (int64_t j = 0; j < g->N; ++j) {
             float total = 0.0f;                   /* K == 0: the empty sum, +0 */
@@ -254,11 +286,26 @@ static void gemm_rows(int64_t lo, int64_t hi, int tix, void *c) {
                 for (int64_t k = c0; k < c1; ++k) {
                     float a = g->transA ? g->A[k * g->lda + i] : g->A[i * g->lda + k];
                     float b = g->transB ? g->B[j * g->ldb + k] : g->B[k * g->ldb + j];
+#ifndef SABOTAGE_FIRST_PRODUCT_SEED
                     acc = fmaf(a, b, acc);        /* ascending k, one rounding each */
+#else   /* separating arm: the chain seeded with the first product */
+                    acc = (k == c0) ? a * b : fmaf(a, b, acc);
+#endif
                 }
+#ifndef SABOTAGE_CHUNK_REVERSED
                 if (c0 == 0) total = acc;         /* first partial taken as is */
                 else total = total + acc;         /* then left to right */
+#else   /* separating arm: partials kept, then added right to left */
+                part[c0 / g->kc] = acc;
+#endif
             }
+#ifdef SABOTAGE_CHUNK_REVERSED
+            {
+                int64_t nc = (g->K + g->kc - 1) / g->kc;
+                if (nc > 0) total = part[nc - 1];
+                for (int64_t c = nc - 2; c >= 0; --c) total = total + part[c];
+            }
+#endif
             g->C[i * g->ldc + j] = total;
         }
     }
@@ -269,6 +316,9 @@ void detor_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
                 float *C, int64_t ldc, int64_t k_chunk, int nthreads) {
     gemm_ctx g = {transA, transB, M, N, K, lda, ldb, ldc, k_chunk, A, B, C};
     if (k_chunk <= 0) return;
+#ifdef SABOTAGE_CHUNK128
+    g.kc = 128;   /* separating arm: chunks half as wide */
+#endif
     parallel_for(M, nthreads, gemm_rows, &g);
 }
 
@@ -517,8 +567,13 @@ static void shard_range(int64_t lo, int64_t hi, int tix, void *c) {
     (void)tix;
     shard_ctx *q = (shard_ctx *)c;
     for (int64_t i = lo; i < hi; ++i) {
+#ifndef SABOTAGE_SHARD_REVERSED
         float t = q->g[i];                        /* shard 0 as is */
         for (int64_t s = 1; s < q->S; ++s) t = t + q->g[s * q->ld + i];
+#else   /* separating arm: right to left */
+        float t = q->g[(q->S - 1) * q->ld + i];
+        for (int64_t s = q->S - 2; s >= 0; --s) t = t + q->g[s * q->ld + i];
+#endif
         q->out[i] = t * q->scale;
     }
 }
@@ -538,7 +593,11 @@ void detor_shardsum(int64_t nshards, int64_t n, const float *shards, int64_t ld,
  * addition is commutative, so all lanes end with the same value: lane 0's. */
 static float butterfly(float *s, int lanes) {
     float t[1024];
+#ifndef SABOTAGE_BUTTERFLY_ORDER
     static const int low[5] = {16, 8, 4, 2, 1};
+#else   /* separating arm: the levels in the opposite order */
+    static const int low[5] = {1, 2, 4, 8, 16};
+#endif
     for (int li = 0; li < 5; ++li) {
         int off = low[li];
         if (off >= lanes) continue;
@@ -571,11 +630,19 @@ static void rms_rows(int64_t lo, int64_t hi, int tix, void *c) {
         const float *x = q->x + r * q->ldx;
         for (int l = 0; l < q->lanes; ++l) s[l] = 0.0f;
         for (int64_t j = 0; j < q->D; ++j) {
+#ifndef SABOTAGE_ELEMENT_OWNERSHIP
             int l = (int)((j / q->group) % q->lanes);
+#else   /* separating arm: chains own single elements, not groups of 4 */
+            int l = (int)(j % q->lanes);
+#endif
             s[l] = fmaf(x[j], x[j], s[l]);        /* each lane: ascending j */
         }
         float ss = butterfly(s, q->lanes);
+#ifndef SABOTAGE_RECIP_D
         float ms = ss / (float)q->D;
+#else   /* separating arm: a multiply by 1/D for the division */
+        float ms = ss * (1.0f / (float)q->D);
+#endif
         float rr = 1.0f / sqrtf(ms + q->eps);
         float *y = q->y + r * q->ldy;
         for (int64_t j = 0; j < q->D; ++j) y[j] = (x[j] * rr) * q->gain[j];
@@ -636,8 +703,12 @@ static void rmsb_rows(int64_t lo, int64_t hi, int tix, void *c) {
         for (int64_t j = 0; j < q->D; ++j) {
             float xhat = x[j] * rr;
             float h = dy[j] * q->gain[j];
+#ifndef SABOTAGE_CONTRACT_RMSBWD
             float p = xhat * qm;
             float d = h - p;
+#else   /* separating arm: h - xhat q contracted into one fmaf */
+            float d = fmaf(-xhat, qm, h);
+#endif
             dx[j] = d * rr;
         }
     }
@@ -648,8 +719,13 @@ static void rmsb_cols(int64_t lo, int64_t hi, int tix, void *c) {
     rmsb_ctx *q = (rmsb_ctx *)c;
     for (int64_t j = lo; j < hi; ++j) {
         float total = 0.0f;                       /* no rows: the empty sum, +0 */
-        for (int64_t c0 = 0; c0 < q->rows; c0 += q->kc) {
-            int64_t c1 = c0 + q->kc < q->rows ? c0 + q->kc : q->rows;
+#ifndef SABOTAGE_ONE_CHAIN_DGAIN
+        const int64_t kc = q->kc;
+#else   /* separating arm: one chain over all rows */
+        const int64_t kc = q->rows > 0 ? q->rows : 1;
+#endif
+        for (int64_t c0 = 0; c0 < q->rows; c0 += kc) {
+            int64_t c1 = c0 + kc < q->rows ? c0 + kc : q->rows;
             float acc = 0.0f;                     /* every chunk starts from +0 */
             for (int64_t i = c0; i < c1; ++i) {
                 float xhat = q->x[i * q->ldx + j] * q->inv[i];
@@ -830,6 +906,9 @@ int64_t detor_xent(int64_t rows, int64_t V, const float *logits, int64_t ld,
     c->V = V; c->ld = ld; c->ldd = ldd; c->x = logits; c->labels = labels;
     c->loss = loss; c->dl = dlogits; c->dscale = dscale;
     c->lanes = lanes; c->group = group;
+#ifdef SABOTAGE_XENT_LANES32
+    c->lanes = 32;   /* separating arm: the RMSNorm's 32 chains */
+#endif
     parallel_for(rows, nthreads, xent_rows, c);
     int64_t total = 0;
     for (int t = 0; t < MAX_THREADS; ++t) total += c->bad[t];
@@ -876,8 +955,13 @@ static void adamw_range(int64_t lo, int64_t hi, int tix, void *c) {
         float g = a->g[i];
         float m = fmaf(a->b1, a->m[i], a->omb1 * g);
         float v = fmaf(a->b2, a->v[i], a->omb2 * (g * g));
+#ifndef SABOTAGE_ADAMW_RECIP_BC
         float mh = m / a->bc1;
         float vh = v / a->bc2;
+#else   /* separating arm: multiplies by the reciprocal corrections */
+        float mh = m * (1.0f / a->bc1);
+        float vh = v * (1.0f / a->bc2);
+#endif
         float u = mh / (sqrtf(vh) + a->eps);
         a->p[i] = fmaf(-a->lr, u, a->p[i] * a->wdf);
         a->m[i] = m;

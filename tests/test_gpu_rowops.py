@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 
 import oracle
+from exp_cases import exp_tie_arguments
 from bitcmp import assert_bitwise
 from bitwise_reproducible_fp32_gb300 import detlib, inputs
 from gpu_util import empty_dev, host, need_gpu, to_dev, torch
@@ -130,23 +131,6 @@ def test_xent_deep_underflow_row(dev):
     loss, _, d = detlib.detxent_f32(to_dev(x), to_dev(lab), want_dlogits=True)
     assert_bitwise(host(loss), loss_w)
     assert_bitwise(host(d), d_w)
-
-
-def exp_tie_arguments():
-    """Floats d <= 0 with fl(d * LOG2E) exactly at a tie k + 1/2 of rint, and
-    their neighbours: where an exp that rounds t = d LOG2E differently (or not
-    at all) picks the other n and lands one ulp away."""
-    log2e = np.float32(1.4426950408889634)
-    out = []
-    for k in range(-151, 0):
-        c = np.float32((k + 0.5) / 1.4426950408889634)
-        bits = c.view(np.int32) + np.arange(-400, 401, dtype=np.int32)
-        d = bits.view(F)
-        t = d * log2e                      # float32 product, rounded once
-        ties = np.nonzero(t == F(k + 0.5))[0]
-        for i in ties:
-            out.extend(d[max(i - 1, 0):i + 2])
-    return np.unique(np.array(out, F))
 
 
 def test_xent_exp_rounding_ties(dev):

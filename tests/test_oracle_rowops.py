@@ -74,25 +74,28 @@ def test_rmsnorm_butterfly_pinned():
     assert inv[0] == F(2.0 ** -6 - 2.0 ** -27)
 
 
-def test_rmsnorm_exact_emulation_tiny():
-    # the whole row computation with exact rationals and hand rounding
-    rng = np.random.default_rng(21)
-    D = 37
-    x = rng.standard_normal((1, D)).astype(F)
+@pytest.mark.parametrize("D,rows", [(37, 6), (3, 40), (5, 40), (7, 40)])
+def test_rmsnorm_exact_emulation_tiny(D, rows):
+    # the whole row computation with exact rationals and hand rounding; many
+    # short rows, so that a one-ulp change anywhere in the row's chain of
+    # operations (ss / D, the square root, 1 / sqrt) reaches inv_rms or y
+    rng = np.random.default_rng(21 + D)
+    x = rng.standard_normal((rows, D)).astype(F)
     g = (1 + 0.02 * rng.standard_normal(D)).astype(F)
     eps = F(1e-6)
-    lanes = [F(0.0)] * 32
-    for j in range(D):
-        lanes[(j // 4) % 32] = ie.fma(x[0, j], x[0, j], lanes[(j // 4) % 32])
-    v = lanes
-    for off in (16, 8, 4, 2, 1):
-        v = [ie.add(v[l], v[l ^ off]) for l in range(32)]
-    ms = ie.div(v[0], F(D))
-    r = ie.div(F(1.0), ie.sqrt(ie.add(ms, eps)))
-    yexp = np.array([ie.mul(ie.mul(x[0, j], r), g[j]) for j in range(D)], F)
     y, inv = oracle.rmsnorm(x, g, eps=eps)
-    assert ie.same_bits(inv[0], r)
-    assert_bitwise(y[0], yexp)
+    for i in range(rows):
+        lanes = [F(0.0)] * 32
+        for j in range(D):
+            lanes[(j // 4) % 32] = ie.fma(x[i, j], x[i, j], lanes[(j // 4) % 32])
+        v = lanes
+        for off in (16, 8, 4, 2, 1):
+            v = [ie.add(v[l], v[l ^ off]) for l in range(32)]
+        ms = ie.div(v[0], F(D))
+        r = ie.div(F(1.0), ie.sqrt(ie.add(ms, eps)))
+        yexp = np.array([ie.mul(ie.mul(x[i, j], r), g[j]) for j in range(D)], F)
+        assert ie.same_bits(inv[i], r), (D, i)
+        assert_bitwise(y[i], yexp)
 
 
 def test_rmsnorm_double_bound():
@@ -170,13 +173,17 @@ def fold_tree(v):
 
 
 def test_xent_tree_restated():
+    # loss and dlogits of whole rows from the restated tree; dlogits carry S
+    # through 1/S into every element, so a tree that sums in another shape
+    # (other chains, another fold) shows there even where log S rounds alike
     rng = np.random.default_rng(31)
-    V = 3000
-    x = (2 * rng.standard_normal((2, V))).astype(F)
-    labels = np.array([5, V - 1], np.int32)
-    loss, _, bad = oracle.xent(x, labels)
+    V, rows = 3000, 6
+    x = (2 * rng.standard_normal((rows, V))).astype(F)
+    labels = rng.integers(0, V, rows).astype(np.int32)
+    dscale = F(0.125)
+    loss, d, bad = oracle.xent(x, labels, with_dlogits=True, dscale=dscale)
     assert bad == 0
-    for r in range(2):
+    for r in range(rows):
         m = x[r].max()
         e = oracle.exp((x[r] - m).astype(F))
         lanes = np.zeros(256, F)
@@ -185,6 +192,10 @@ def test_xent_tree_restated():
         S = fold_tree(lanes)
         want = F(oracle.log1(S) - F(x[r, labels[r]] - m))
         assert ie.same_bits(loss[r], want)
+        onehot = np.zeros(V, F)
+        onehot[labels[r]] = 1.0
+        dwant = ((e * (F(1.0) / S)).astype(F) - onehot).astype(F) * dscale
+        assert_bitwise(d[r], dwant.astype(F))
 
 
 def test_xent_constant_row():

@@ -65,3 +65,48 @@ def test_noalloc_skips_a_transposed_copy_beyond_its_scratch():
     detlib.detgemm_f32_noalloc(Ad, Bd, C)
     torch.cuda.synchronize()
     assert_bitwise(host(C), ref, "no-alloc without the transposed copy")
+
+
+def test_noalloc_empty_contraction_and_argument_checks():
+    need_gpu()
+    # K == 0: the empty sum, +0 in every output, as detgemm_f32 gives
+    A = torch.zeros((5, 0), dtype=torch.float32, device="cuda")
+    B = torch.zeros((0, 7), dtype=torch.float32, device="cuda")
+    C = torch.full((5, 7), float("nan"), dtype=torch.float32, device="cuda")
+    detlib.detgemm_f32_noalloc(A, B, C)
+    torch.cuda.synchronize()
+    assert np.all(host(C).view(np.uint32) == 0)
+    # a row stride below the row length is refused on the host, before any launch
+    import ctypes
+    lib = detlib.load()
+    prof = ctypes.byref(detlib.det_profile_default())
+    Ad = torch.zeros((4, 8), dtype=torch.float32, device="cuda")
+    Bd = torch.zeros((8, 4), dtype=torch.float32, device="cuda")
+    Cd = torch.zeros((4, 4), dtype=torch.float32, device="cuda")
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+    assert lib.detgemm_f32_noalloc(prof, 0, 0, 4, 4, 8, ptr(Ad), 7, ptr(Bd), 4, ptr(Cd), 4,
+                                   None) == 1       # lda < K
+    assert lib.detgemm_f32_noalloc(prof, 0, 0, 4, 4, 8, ptr(Ad), 8, ptr(Bd), 4, None, 4,
+                                   None) == 1       # null C
+
+
+def test_noalloc_on_a_side_stream_after_a_first_call():
+    need_gpu()
+    # the first call (address look-up) happened on the current stream in the
+    # tests above, or happens here; a later call on another stream must give
+    # detgemm_f32's bits
+    rng = np.random.default_rng(2025)
+    M, N, K = 300, 200, 1300          # split K through the scratch
+    A = rng.standard_normal((M, K)).astype(F)
+    B = rng.standard_normal((K, N)).astype(F)
+    Ad, Bd = to_dev(A), to_dev(B)
+    ref = host(detlib.detgemm_f32(Ad, Bd, workspace=detlib.gemm_workspace(M, N, K)))
+    detlib.detgemm_f32_noalloc(Ad, Bd, empty_dev(M, N))
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    C = empty_dev(M, N)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        detlib.detgemm_f32_noalloc(Ad, Bd, C, stream=side)
+    side.synchronize()
+    assert_bitwise(host(C), ref, "no-alloc GEMM on a side stream")
