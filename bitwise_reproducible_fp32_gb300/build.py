@@ -45,6 +45,32 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def build_variant(defines, out_path: str) -> str:
+    """Compile a separate copy of the library with extra -D flags into out_path
+    (the test suite's copy with a shortened GEMM wait). Never the shipped
+    library: LIB is not touched."""
+    work = out_path + ".build"
+    os.makedirs(work, exist_ok=True)
+    dflags = [f"-D{d}" for d in defines]
+
+    def compile_one(src):
+        obj = os.path.join(work, src.replace(".cu", ".o"))
+        cmd = [nvcc(), *common_flags(dflags), "-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-Xlinker", "--no-undefined",
+           "-o", out_path, *objs]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return out_path
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile every translation unit in parallel and link the shared library.
     Returns the library path."""

@@ -165,6 +165,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same phase (test_wait never suspends the thread;
+// try_wait may, for a system-dependent time).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete, giving up after
 // kWaitLimitNs. Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
@@ -182,14 +196,22 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 
 // As mbar_wait_bounded, but also gives up as soon as *abort is set, and sets
 // *abort itself when the time limit passes, so every waiter of the CTA stops.
+// A limit of 0 gives up whenever the phase is not complete at the first,
+// non-blocking look.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
-                                                   volatile int *abort) {
+                                                   volatile int *abort,
+                                                   unsigned long long limit_ns = kWaitLimitNs) {
+    if (limit_ns == 0) {
+        if (mbar_test_wait(bar, parity)) return true;
+        *abort = 1;
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
             return false;
         }
