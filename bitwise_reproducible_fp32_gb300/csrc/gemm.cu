@@ -83,6 +83,17 @@ static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
 
 __device__ unsigned int g_gemm_watchdog;
 
+// The limit of the consumers' wait for a k-tile's operands. The shipped
+// library uses the common bound; the test suite builds a separate copy with
+// DET_TEST_GEMM_WAIT_NS=0, whose consumers give up at the first wait that is
+// not already complete, to run the give-up path (watchdog bit, drain of the
+// copies in flight, skipped stores) on healthy copies.
+#ifdef DET_TEST_GEMM_WAIT_NS
+constexpr unsigned long long kGemmConsumerWaitNs = DET_TEST_GEMM_WAIT_NS;
+#else
+constexpr unsigned long long kGemmConsumerWaitNs = kWaitLimitNs;
+#endif
+
 // Shared-memory float index of element (row r, k) of an operand tile with R
 // rows. KMAJ: rows of 32 k (128 bytes); 16-byte chunk q of row r is stored at
 // chunk q ^ (r & 7), the TMA 128-byte swizzle pattern. Otherwise one row of R
@@ -605,7 +616,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             int ok = 1;
             if (TMA) {
                 ok = mbar_wait_or_abort(smem_u32(&full[s]), uint32_t(it / STAGES) & 1u,
-                                        &abort_flag);
+                                        &abort_flag, kGemmConsumerWaitNs);
             } else {
                 __syncthreads();   // everyone is done with the previous k-tile
                 load_tile_plain<A_KM, BM>(stages,
