@@ -259,8 +259,15 @@ def run_ours(args, rank, world, local_rank):
     c_fwd = [torch.empty(gemm_dims(p)[:2], dtype=torch.float32, device=dev) for p in fwd]
     c_dw = [torch.empty(gemm_dims(p)[:2], dtype=torch.float32, device=dev) for p in dw]
     # caller-owned split-K workspaces (None where the library needs none)
-    ws_fwd = [detlib.gemm_workspace(*gemm_dims(p), p["transA"], p["transB"], device=dev)
-              for p in fwd]
+    # the gate and up projections read the same activations: one group (one
+    # transposed copy of X, one grid for both), as the decoder block runs them
+    names = [p["name"] for p in fwd]
+    gu = (names.index("swiglu_gate"), names.index("swiglu_up"))
+    gu_probs = [dict(A=g_fwd[i][1], B=g_fwd[i][2], C=c_fwd[i]) for i in gu]
+    ws_gu = detlib.gemm_group_workspace(gu_probs, device=dev)
+    ws_fwd = [None if i in gu else
+              detlib.gemm_workspace(*gemm_dims(p), p["transA"], p["transB"], device=dev)
+              for i, p in enumerate(fwd)]
     ws_dw = [detlib.gemm_workspace(*gemm_dims(p), p["transA"], p["transB"], device=dev)
              for p in dw]
     x4, gain4 = up(r4["x"]), up(r4["gain"])
@@ -332,7 +339,7 @@ def run_ours(args, rank, world, local_rank):
     gemm_flops = sum(gemm_flops_fwd) + sum(gemm_flops_dw)
     lm_idx = [p["name"] for p in fwd].index("lm_head")
     # A GEMM is one launch, plus one where it uses its workspace (the split-K
-    # second pass, or the transposed copy of A). Attention is 4 launches a
+    # second pass, or the transposed copy of A); a group reports its own count. Attention is 4 launches a
     # group of heads forward (with the count of V's non-finite values) and 10
     # backward (with those of dO, K and Q). Checked against an ncu launch list
     # of one step.
@@ -351,7 +358,22 @@ def run_ours(args, rank, world, local_rank):
 
     # one block forward: 2 RMSNorms, 5 GEMMs, RoPE, attention, 2 adds, SwiGLU
     g162 = attn_groups_count(bc["batch"], bc["seq"], inputs.N_HEADS)
-    block_launches = (2 + sum(gemm_n(blk.ws[k]) for k in ("qkv", "o", "ff", "ff", "down"))
+    def pair_n(M, N1, N2, K, transA, ws_bytes=None):
+        # launches of a two-product group of one shared A (gate/up, or two
+        # weight gradients of one input), with the group's own workspace when
+        # ws_bytes is None; stand-in tensors carry the shapes
+        e = lambda *sh: torch.empty(sh, dtype=torch.float32, device=dev)  # noqa: E731
+        A = e(K, M) if transA else e(M, K)
+        probs = [dict(A=A, B=e(K, N1), C=e(M, N1), transA=transA),
+                 dict(A=A, B=e(K, N2), C=e(M, N2), transA=transA)]
+        ws = detlib.gemm_group_workspace(probs) if ws_bytes is None else (
+            e(ws_bytes // 4) if ws_bytes else None)
+        return detlib.detgemm_group_launches(probs, ws)
+
+    ntok_blk = bc["batch"] * bc["seq"]
+    gu_blk = pair_n(ntok_blk, bc["W_gate"].shape[1], bc["W_up"].shape[1],
+                    bc["x"].shape[1], False)
+    block_launches = (2 + sum(gemm_n(blk.ws[k]) for k in ("qkv", "o", "down")) + gu_blk
                       + 1 + 4 * g162 + 2 + 1)
     # the byte-level LM step: the embedding, 2 forward blocks (11 launches and
     # the attention), the head GEMM, the cross-entropy and its mean, the head's
@@ -365,15 +387,22 @@ def run_ours(args, rank, world, local_rank):
 
     def dw_n(M, N):
         return 1 + int(detlib.detgemm_workspace_bytes(M, N, ntok_b, True, False) > 0)
-    blk_dw = sum(dw_n(M, N) for M, N in ((f_b, d_b), (d_b, f_b), (d_b, f_b), (d_b, d_b),
-                                         (d_b, 3 * d_b)))
-    byte_lm_launches = (1 + nb * (11 + 4 * gb) + 1 + 2 + dw_n(bl["vocab"], d_b) + 1
+    # W_down's, the W_gate/W_up pair's, W_o's and W_qkv's weight gradients
+    blk_dw = (dw_n(f_b, d_b) + pair_n(d_b, f_b, f_b, ntok_b, True) + dw_n(d_b, d_b)
+              + dw_n(d_b, 3 * d_b))
+    # a forward block: 2 RMSNorms, QKV, out, the gate/up group, down, rotary,
+    # 2 adds, SwiGLU and the attention
+    blk_fwd = 2 + 3 + pair_n(ntok_b, f_b, f_b, d_b, False) + 1 + 2 + 1
+    byte_lm_launches = (1 + nb * (blk_fwd + 4 * gb) + 1 + 2 + dw_n(bl["vocab"], d_b) + 1
                         + nb * (13 + blk_dw + 10 * gb) + 1 + 2 + 7 * nb)
     # the 162M decoder forward: the embedding, 12 blocks as above, the head
     # GEMM (with its transposed copy of the activations), cross-entropy + mean
     decoder_launches = 1 + len(dm_blocks) * block_launches + gemm_n(dm_head_ws) + 2
-    launches_per_step = (1 + sum(gemm_n(w) for w in ws_fwd) + 2 + 2
-                         + sum(gemm_n(w) for w in ws_dw) + 1 + block_launches
+    dw_launches = sum(gemm_n(w) for w in ws_dw)
+    fwd_launches = (sum(gemm_n(w) for i, w in enumerate(ws_fwd) if i not in gu)
+                    + detlib.detgemm_group_launches(gu_probs, ws_gu))
+    launches_per_step = (1 + fwd_launches + 2 + 2
+                         + dw_launches + 1 + block_launches
                          + byte_lm_launches + decoder_launches + 1)
 
     segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "rmsnorm_bwd", "gemm_dw",
@@ -387,7 +416,10 @@ def run_ours(args, rank, world, local_rank):
         detlib.detrmsnorm_f32(x4, gain4, float(r4["eps"]), y=y4, inv_rms=inv4)
         mark(1)
         for i, (p, A, B) in enumerate(g_fwd):
-            if i == lm_idx:
+            if i == lm_idx or i == gu[1]:
+                continue
+            if i == gu[0]:
+                detlib.detgemm_group_f32(gu_probs, workspace=ws_gu)
                 continue
             detlib.detgemm_f32(A, B, c_fwd[i], transA=p["transA"], transB=p["transB"],
                                workspace=ws_fwd[i])
@@ -646,7 +678,21 @@ def e2e_leg(args, dev, host, gemm_flops):
     # one stream, the op runs on the compute stream once they have landed, and
     # its outputs are copied out on a third stream while later ops run
     ops = []
+    names = [p["name"] for p in fwd]
+    gu = (names.index("swiglu_gate"), names.index("swiglu_up"))
     for i, p in enumerate(fwd + dw):
+        if i == gu[1]:
+            continue
+        if i == gu[0]:
+            # the gate and up projections as one group, as in the device-timed step
+            q0, q1 = fwd[gu[0]], fwd[gu[1]]
+            gu_probs = [dict(A=g(q0["A"]), B=g(q0["B"]), C=outs_dev[gu[0]]),
+                        dict(A=g(q1["A"]), B=g(q1["B"]), C=outs_dev[gu[1]])]
+            ws_gu = detlib.gemm_group_workspace(gu_probs, device=dev)
+            ops.append(([pin(q0["A"]), pin(q0["B"]), pin(q1["B"])],
+                        lambda gp=gu_probs, w=ws_gu: detlib.detgemm_group_f32(gp, workspace=w),
+                        [(outs_dev[j], host_outs[j]) for j in gu]))
+            continue
         ops.append(([pin(p["A"]), pin(p["B"])],
                     lambda i=i, p=p: detlib.detgemm_f32(g(p["A"]), g(p["B"]), outs_dev[i],
                                                         transA=p["transA"], transB=p["transB"],

@@ -36,7 +36,14 @@ class Block:
         self.y = e(n, d_model)
         ws = lambda M, N, K: detlib.gemm_workspace(M, N, K, False, False, device=device)  # noqa: E731
         self.ws = {"qkv": ws(n, 3 * d_model, d_model), "o": ws(n, d_model, d_model),
-                   "ff": ws(n, d_ff, d_model), "down": ws(n, d_model, d_ff)}
+                   "down": ws(n, d_model, d_ff)}
+        # the gate and up projections of h2 run as one group (one transposed
+        # copy of h2, one grid for both); the plan needs only shapes and that
+        # both read the same h2, so a stand-in weight serves for the query
+        wq = e(d_model, d_ff)
+        self.ws["gate_up"] = detlib.gemm_group_workspace(
+            [dict(A=self.h2, B=wq, C=self.gate), dict(A=self.h2, B=wq, C=self.up)])
+        del wq
         self.att_ws = e((detlib.detattention_workspace_bytes(batch, seq, heads, self.hd) + 3)
                         // 4)
         self.ws_bwd = {}       # weight-gradient GEMM workspaces, by output shape
@@ -60,8 +67,9 @@ class Block:
         L.detgemm_f32(self.att, w["W_o"], self.o, workspace=self.ws["o"])
         L.detadd_f32(x, self.o, out=self.x1)
         L.detrmsnorm_f32(self.x1, w["g2"], self.eps, y=self.h2, inv_rms=self.inv2)
-        L.detgemm_f32(self.h2, w["W_gate"], self.gate, workspace=self.ws["ff"])
-        L.detgemm_f32(self.h2, w["W_up"], self.up, workspace=self.ws["ff"])
+        L.detgemm_group_f32([dict(A=self.h2, B=w["W_gate"], C=self.gate),
+                             dict(A=self.h2, B=w["W_up"], C=self.up)],
+                            workspace=self.ws["gate_up"])
         L.detswiglu_f32(self.gate, self.up, out=self.s)
         L.detgemm_f32(self.s, w["W_down"], self.dn, workspace=self.ws["down"])
         L.detadd_f32(self.x1, self.dn, out=self.y)
@@ -88,14 +96,24 @@ class Block:
                 self.ws_bwd[(M, N)] = L.gemm_workspace(M, N, n, True, False, device=dy.device)
             return L.detgemm_f32(A, B, transA=True, workspace=self.ws_bwd[(M, N)])
         tB = lambda A, B, C=None: L.detgemm_f32(A, B, C, transB=True)          # noqa: E731
+
+        def tA2(A, B1, B2):
+            # two weight gradients of one input, as one group
+            M, N1, N2 = A.shape[1], B1.shape[1], B2.shape[1]
+            probs = [dict(A=A, B=B1, C=e(M, N1), transA=True),
+                     dict(A=A, B=B2, C=e(M, N2), transA=True)]
+            key = ("pair", M, N1, N2)
+            if key not in self.ws_bwd:
+                self.ws_bwd[key] = L.gemm_group_workspace(probs)
+            L.detgemm_group_f32(probs, workspace=self.ws_bwd[key])
+            return probs[0]["C"], probs[1]["C"]
         # y = x1 + s W_down
         ds = tB(dy, w["W_down"])
         g["W_down"] = tA(self.s, dy)
         d_gate, d_up = L.detswiglu_bwd_f32(self.gate, self.up, ds)
         dh2 = tB(d_gate, w["W_gate"])
         L.detgemm_acc_f32(d_up, w["W_up"], dh2, transB=True)
-        g["W_gate"] = tA(self.h2, d_gate)
-        g["W_up"] = tA(self.h2, d_up)
+        g["W_gate"], g["W_up"] = tA2(self.h2, d_gate, d_up)
         dx1_b, g["g2"] = L.detrmsnorm_bwd_f32(self.x1, w["g2"], self.inv2, dh2)
         dx1 = L.detadd_f32(dy, dx1_b)
         # x1 = x + att W_o

@@ -8,6 +8,7 @@
 // than a weaker result.
 #include <algorithm>
 #include <atomic>
+#include <vector>
 
 #include "det_internal.cuh"
 
@@ -156,6 +157,117 @@ DET_API det_status detgemm_acc_f32(const det_profile_v1 *prof, int transA, int t
                                    det_stream_t stream) {
     return gemm_entry(prof, transA, transB, M, N, K, A, lda, B, ldb, C, ldc, workspace,
                       workspace_bytes, stream, 1);
+}
+
+// ---------------------------------------------------------------- groups of products
+namespace {
+// A problem's arguments as GemmArgs, after detgemm_f32's checks. Returns
+// DET_OK with *empty set when the product has no outputs.
+det_status check_problem(const det_gemm_problem &q, GemmArgs *a, bool *empty) {
+    *empty = false;
+    if (q.M < 0 || q.N < 0 || q.K < 0 || q.M > kDimMax || q.N > kDimMax || q.K > kDimMax)
+        return DET_ERR_INVALID_ARG;
+    if (q.M == 0 || q.N == 0) {
+        *empty = true;
+        return DET_OK;
+    }
+    const int64_t a_row = q.transA ? q.M : q.K, b_row = q.transB ? q.K : q.N;
+    if (q.ldc < q.N || q.lda < std::max<int64_t>(a_row, 1) ||
+        q.ldb < std::max<int64_t>(b_row, 1))
+        return DET_ERR_INVALID_ARG;
+    if (!q.C || (q.K > 0 && (!q.A || !q.B))) return DET_ERR_INVALID_ARG;
+    const int64_t tiles = ((q.M + 127) / 128) * ((q.N + 127) / 128);
+    if (tiles > kDimMax) return DET_ERR_INVALID_ARG;
+    a->M = q.M; a->N = q.N; a->K = q.K; a->lda = q.lda; a->ldb = q.ldb; a->ldc = q.ldc;
+    a->A = q.A; a->B = q.B; a->C = q.C;
+    a->transA = q.transA != 0; a->transB = q.transB != 0;
+    a->accumulate = 0;
+    return DET_OK;
+}
+
+// Runs fn(first, second-or-null) over the problems in pairs (0, 1), (2, 3), ...
+// after checking every problem; empty products are dropped from the pairing.
+template <class Fn>
+det_status for_pairs(const det_profile_v1 *prof, int64_t count,
+                     const det_gemm_problem *probs, Fn fn) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (count < 0 || (count > 0 && !probs)) return DET_ERR_INVALID_ARG;
+    std::vector<GemmArgs> live;
+    for (int64_t i = 0; i < count; ++i) {
+        GemmArgs a;
+        bool empty = false;
+        if ((st = check_problem(probs[i], &a, &empty)) != DET_OK) return st;
+        if (!empty) live.push_back(a);
+    }
+    if (live.empty()) return DET_OK;
+    if ((st = check_device()) != DET_OK) return st;
+    for (size_t i = 0; i < live.size(); i += 2) {
+        const GemmArgs *second = i + 1 < live.size() ? &live[i + 1] : nullptr;
+        if ((st = fn(live[i], second)) != DET_OK) return st;
+    }
+    return DET_OK;
+}
+}  // namespace
+
+DET_API det_status detgemm_group_workspace_bytes(const det_profile_v1 *prof, int64_t count,
+                                                 const det_gemm_problem *problems,
+                                                 size_t *bytes) {
+    if (!bytes) return DET_ERR_INVALID_ARG;
+    size_t need = 0;
+    const det_status st = for_pairs(prof, count, problems,
+                                    [&](const GemmArgs &a, const GemmArgs *b) {
+        const int sms = sm_count_current_device();
+        if (!b) {
+            need = std::max(need, gemm_plan(a.M, a.N, a.K, sms, !a.transA).workspace_bytes);
+        } else {
+            const PairPlan pp = gemm_pair_plan(a, *b, sms);
+            need = std::max(need, pp.pair ? pp.workspace_bytes : pp.separate_bytes);
+        }
+        return DET_OK;
+    });
+    if (st == DET_OK) *bytes = need;
+    return st;
+}
+
+DET_API det_status detgemm_group_launches(const det_profile_v1 *prof, int64_t count,
+                                          const det_gemm_problem *problems,
+                                          size_t workspace_bytes, int64_t *launches) {
+    if (!launches) return DET_ERR_INVALID_ARG;
+    int64_t n = 0;
+    const int sms = sm_count_current_device();
+    // kernels one product issues alone with this much workspace
+    auto alone = [&](const GemmArgs &a) -> int64_t {
+        if (a.K == 0) return 1;
+        const GemmPlan pl = gemm_plan(a.M, a.N, a.K, sms, !a.transA);
+        const bool ws = workspace_bytes >= pl.workspace_bytes;
+        return 1 + int64_t(ws && (pl.split || pl.transpose_a));
+    };
+    const det_status st = for_pairs(prof, count, problems,
+                                    [&](const GemmArgs &a, const GemmArgs *b) {
+        if (!b) {
+            n += alone(a);
+            return DET_OK;
+        }
+        const PairPlan pp = gemm_pair_plan(a, *b, sms);
+        if (pp.pair && workspace_bytes >= pp.workspace_bytes)
+            n += pp.shared_transpose ? 2 : pp.split ? 3 : 1;
+        else
+            n += alone(a) + alone(*b);
+        return DET_OK;
+    });
+    if (st == DET_OK) *launches = n;
+    return st;
+}
+
+DET_API det_status detgemm_group_f32(const det_profile_v1 *prof, int64_t count,
+                                     const det_gemm_problem *problems, void *workspace,
+                                     size_t workspace_bytes, det_stream_t stream) {
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return for_pairs(prof, count, problems, [&](const GemmArgs &a, const GemmArgs *b) {
+        return from_cuda(b ? launch_gemm_pair(a, *b, workspace, workspace_bytes, s)
+                           : launch_gemm(a, workspace, workspace_bytes, s));
+    });
 }
 
 // ---------------------------------------------------------------- block forward
@@ -480,10 +592,12 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
         const HeadOperand P = stacked(S, seq, nh, count);
         cudaError_t r = group_gemm(seq, seq, head_dim, Q, 0, K, 1, S, seq, P.zb, P.zh, count, nh,
                                    1, s);
-        if (r == cudaSuccess)
-            r = launch_softmax_causal(count * seq, seq, S, seq, scale, 0, seq, S, seq, s);
-        // P is +0 above the diagonal: with a finite V the chunks there are skipped
+        // P is +0 above the diagonal: with a finite V (counted first) P V
+        // skips the chunks past each row block, so the softmax writes P's +0
+        // columns only up to that block's end
         if (r == cudaSuccess) r = count_nonfinite_heads(flags, &V, 1, nb * seq, nh * head_dim, s);
+        if (r == cudaSuccess)
+            r = launch_softmax_causal(count * seq, seq, S, seq, scale, 0, seq, S, seq, s, flags);
         if (r == cudaSuccess)
             r = group_gemm(seq, head_dim, seq, P, 0, V, 0, out + b0 * seq * ldout + h0 * head_dim,
                            ldout, seq * ldout, head_dim, count, nh, 0, s, 1, flags);

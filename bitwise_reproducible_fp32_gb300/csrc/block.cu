@@ -203,9 +203,14 @@ __device__ __forceinline__ int64_t kept_columns(int64_t r, int64_t period, int64
 __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
     softmax_causal_kernel(int64_t rows, int64_t cols, const float *s, int64_t lds, float scale,
                           int64_t diag, int64_t period, float *p, int64_t ldp, int vec_s,
-                          int vec_p) {
+                          int vec_p, const int *chunk_zeros) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * kSmaxWarps;
+    // With chunk_zeros given and *chunk_zeros == 0, masked columns are zeroed
+    // only up to the end of the row's 256-row block of queries: the product
+    // that reads P (P V, skipping the +0 chunks past a row block when V is
+    // finite, which *chunk_zeros == 0 says) reads no column beyond it.
+    const bool to_chunk = chunk_zeros != nullptr && *chunk_zeros == 0;
     for (int64_t r = int64_t(blockIdx.x) * kSmaxWarps + (threadIdx.x >> 5); r < rows;
          r += nwarps) {
         const float *sr = s + r * lds;
@@ -217,7 +222,9 @@ __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
             const int64_t rn = r + nwarps;
             prefetch_row_l2(s + rn * lds, kept_columns(rn, period, diag, cols) & ~int64_t(3));
         }
-        zero_masked(pr, nr, cols, lane, vec_p);
+        const int64_t zend =
+            to_chunk ? std::min<int64_t>(cols, ((r % period) / kKChunk + 1) * kKChunk) : cols;
+        zero_masked(pr, nr, zend, lane, vec_p);
         if (nr == 0) continue;     // uniform across the warp
         const int64_t nseg = (nr + 1023) / 1024;
         auto scaled = [&](int64_t j) {
@@ -495,13 +502,13 @@ cudaError_t launch_add(int64_t n, const float *a, const float *b, float *out, cu
 
 cudaError_t launch_softmax_causal(int64_t rows, int64_t cols, const float *sc, int64_t lds,
                                   float scale, int64_t diag, int64_t period, float *p,
-                                  int64_t ldp, cudaStream_t s) {
+                                  int64_t ldp, cudaStream_t s, const int *chunk_zeros) {
     if (rows == 0) return cudaSuccess;
     const int64_t blocks = std::min<int64_t>((rows + kSmaxWarps - 1) / kSmaxWarps,
                                              int64_t(sm_count_current_device()) * 16);
     const int vec_s = al16(sc) && lds % 4 == 0, vec_p = al16(p) && ldp % 4 == 0;
     softmax_causal_kernel<<<unsigned(blocks), 32 * kSmaxWarps, 0, s>>>(
-        rows, cols, sc, lds, scale, diag, period, p, ldp, vec_s, vec_p);
+        rows, cols, sc, lds, scale, diag, period, p, ldp, vec_s, vec_p, chunk_zeros);
     return cudaGetLastError();
 }
 

@@ -48,6 +48,21 @@ struct GemmPlan {
 GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor);
 cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_bytes,
                         cudaStream_t s);
+// Two independent products in one launch where that is faster (else one
+// after the other); each product's bits are launch_gemm's.
+struct PairPlan {
+    int pair;              // 1: one launch for both
+    int split;             // both split K into groups of `group` chunks
+    int shared_transpose;  // both read one transposed copy of their common A
+    int group;
+    GemmPlan p0, p1;       // each product's plan (the pair's when pair == 1)
+    size_t ws0_bytes;      // product 1's partials start here in the workspace
+    size_t workspace_bytes;   // the pair's workspace
+    size_t separate_bytes;    // the workspace of the two run one after the other
+};
+PairPlan gemm_pair_plan(const GemmArgs &a0, const GemmArgs &a1, int sms);
+cudaError_t launch_gemm_pair(const GemmArgs &a0, const GemmArgs &a1, void *workspace,
+                             size_t workspace_bytes, cudaStream_t s);
 // A batch of products of one shape. Product z = zb * inner + zh (z < count)
 // reads op(A) at A + zb * a_zb + zh * a_zh, op(B) likewise, and writes C at
 // C + zb * c_zb + zh * c_zh. The A and B buffers are a_rows x a_cols and
@@ -98,9 +113,13 @@ cudaError_t launch_rmsnorm_bwd(int64_t rows, int64_t D, const float *x, int64_t 
 cudaError_t launch_swiglu(int64_t n, const float *g, const float *u, float *out,
                           cudaStream_t s);
 cudaError_t launch_add(int64_t n, const float *a, const float *b, float *out, cudaStream_t s);
+// chunk_zeros (device, nullable): when it holds 0, masked columns are zeroed
+// only up to the end of each row's 256-row block of queries (the reach of a
+// P V that skips the +0 chunks); otherwise, and when null, all of them.
 cudaError_t launch_softmax_causal(int64_t rows, int64_t cols, const float *sc, int64_t lds,
                                   float scale, int64_t diag, int64_t period, float *p,
-                                  int64_t ldp, cudaStream_t s);
+                                  int64_t ldp, cudaStream_t s,
+                                  const int *chunk_zeros = nullptr);
 cudaError_t launch_rope(int64_t rows, int heads, int head_dim, float *x, int64_t ldx,
                         int64_t seq_len, float theta, int backward, cudaStream_t s);
 cudaError_t launch_swiglu_bwd(int64_t n, const float *g, const float *u, const float *dh,
@@ -127,7 +146,35 @@ void adamw_bias_correction(int64_t step, float beta1, float beta2, float *bc1, f
 
 int sm_count_current_device();
 
+// Launches kern as a programmatic dependent of the work before it on stream s:
+// its launch overlaps the tail of the previous kernel, and the kernel must
+// call grid_dependency_wait() before it touches global memory.
+template <class... KParams, class... Args>
+cudaError_t launch_dependent(void (*kern)(KParams...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, KParams(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- device helpers
+// Waits until the grid this kernel was launched as a programmatic dependent of
+// has completed and its memory operations are visible; returns at once for a
+// plain launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -23,8 +23,10 @@
 //    thread, one CTA per SM (up to 255 registers a thread).
 //  * k-tile 32 divides the 256-wide chunk, so chunk boundaries fall on k-tile
 //    boundaries. Operand tiles arrive by TMA (cp.async.bulk.tensor) into a
-//    2-stage ring (48 KB a stage) with one mbarrier per stage; thread 0 is the
-//    producer. Tiles whose k is contiguous use the 128-byte swizzle, so
+//    2-stage ring (48 KB a stage) with one mbarrier per stage. A stage is
+//    refilled by the last warp to finish with it (a shared counter per stage),
+//    so no warp ever waits for the others; thread 0 only issues the first
+//    stages. Tiles whose k is contiguous use the 128-byte swizzle, so
 //    16-byte loads of 4 consecutive k from 8 different rows are free of bank
 //    conflicts; tiles whose m/n is contiguous are stored plain and read as
 //    float4 along m/n.
@@ -50,6 +52,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "det_internal.cuh"
 
@@ -77,7 +80,7 @@ constexpr int B_FLOATS = BN * BK;               // 4096
 constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
 constexpr int TOTAL_FLOAT4 = THREADS * TM * TN / 4;   // running totals
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_FLOATS * 4 +
-                              size_t(TOTAL_FLOAT4) * 16 + 2 * STAGES * 8;
+                              size_t(TOTAL_FLOAT4) * 16 + STAGES * 8;
 static_assert(kKChunk % BK == 0, "chunk boundaries must fall on k-tiles");
 static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
 
@@ -141,6 +144,10 @@ struct KArgs {
     // op(B) values written before the launch.
     int tri;
     const int *tri_bad;
+    // Two independent products in one launch (the GROUP instances): the
+    // kernel's second KArgs describes the other product; the first units0
+    // work units belong to this one, the rest to the other.
+    int units0;
 };
 
 __device__ __forceinline__ int64_t z_offset(int64_t zb_stride, int64_t zh_stride, int z,
@@ -418,6 +425,8 @@ __device__ __forceinline__ void issue_stage(float *st, uint64_t *bar_ptr,
 // the tiles, the smaller operand's blocks), keeping the working set in L2.
 struct Unit {
     int t, m0, n0, kt0, kt1, z;
+    int prob;          // 0, or 1 for the second product of a two-product launch
+    int nkt;           // k-tiles of that product
 };
 
 __device__ __forceinline__ int causal_row_tiles(int mb, int nt) {
@@ -426,8 +435,16 @@ __device__ __forceinline__ int causal_row_tiles(int mb, int nt) {
 
 // BATCH: the kernel instance for batched products (z, causal and triangular
 // modes); the plain instance compiles none of that in.
-template <bool BATCH>
-__device__ __forceinline__ Unit unit_of(const KArgs &p, int u, int nkt, bool tri_on) {
+template <bool BATCH, bool GROUP>
+__device__ __forceinline__ Unit unit_of(const KArgs &p0, const KArgs &p1, int u, int nkt,
+                                        bool tri_on) {
+    // the product this unit belongs to (a group instance carries two)
+    const bool second = GROUP && u >= p0.units0;
+    const KArgs &p = second ? p1 : p0;
+    if (second) {
+        u -= p0.units0;
+        nkt = (p1.K + BK - 1) / BK;
+    }
     if (BATCH && tri_on) {
         // Triangular products (never split, never causal) differ in work by
         // row tile: units go out in descending work (tri 1: last row tile
@@ -441,6 +458,8 @@ __device__ __forceinline__ Unit unit_of(const KArgs &p, int u, int nkt, bool tri
         const int mb = p.tri == 1 ? p.mt - 1 - level : level;
         const int nb = rest % p.nt;
         Unit w;
+        w.prob = 0;
+        w.nkt = nkt;
         w.z = rest / p.nt;
         w.t = mb * p.nt + nb;
         w.m0 = mb * BM;
@@ -467,6 +486,8 @@ __device__ __forceinline__ Unit unit_of(const KArgs &p, int u, int nkt, bool tri
     } else if (p.m_fast) { mb = t % p.mt; nb = t / p.mt; }
     else                 { nb = t % p.nt; mb = t / p.nt; }
     Unit w;
+    w.prob = second;
+    w.nkt = nkt;
     w.t = t;
     w.z = z;
     w.m0 = mb * BM;
@@ -521,8 +542,9 @@ __device__ __forceinline__ void store_tile(const float (&acc)[TM][TN], float *ba
 // Persistent: CTA b computes tiles b, b + gridDim.x, ... The k-tiles of all its
 // tiles form one sequence through the stage ring, so the loads of the next
 // tile are in flight while the current one finishes and stores.
-// Producer bookkeeping (thread 0 only), kept in shared memory so it costs no
-// registers in the other threads.
+// Producer bookkeeping, kept in shared memory so it costs no registers. One
+// lane at a time touches it: thread 0 for the first stages, then the lane
+// that releases a stage last, which every other lane's release precedes.
 struct Producer {
     int ui;          // index of the unit being issued, among this CTA's units
     int kt;          // next k-tile of that unit
@@ -531,19 +553,28 @@ struct Producer {
     Unit u;
 };
 
-template <bool A_KM, bool B_KM, bool TMA, bool SPLIT, bool BATCH>
+// GROUP: the instance for two products in one grid (plain or split, never
+// batched); the other instances compile none of its per-unit selection in.
+template <bool A_KM, bool B_KM, bool TMA, bool SPLIT, bool BATCH, bool GROUP>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                const __grid_constant__ CUtensorMap tmB, const KArgs p) {
+                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ KArgs p,
+                const __grid_constant__ CUtensorMap tmA2,
+                const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ KArgs p2) {
     __shared__ Producer prod;
     __shared__ volatile int abort_flag;
+    __shared__ int released[STAGES];   // warps done with a stage (last one refills)
     extern __shared__ unsigned char smem_raw[];
     float *smem = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *stages = smem;
     float4 *totals = reinterpret_cast<float4 *>(smem + STAGES * STAGE_FLOATS);
     uint64_t *full = reinterpret_cast<uint64_t *>(totals + TOTAL_FLOAT4);   // data landed
-    uint64_t *empty = full + STAGES;                 // all 8 warps done reading
+
+    // launched as a programmatic dependent of the kernel before it on the
+    // stream: nothing here reads or writes global memory before that grid is
+    // complete (a plain launch passes this at once)
+    grid_dependency_wait();
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -553,12 +584,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int arow = A_KM ? wm * WTM + lm : wm * WTM + lm * 4;
     const int bcol = B_KM ? wn * 32 + ln : wn * 32 + ln * 4;
 
-    const int nunits = p.live_tiles * p.units_per_tile * p.zcount;
+    const int nunits = p.live_tiles * p.units_per_tile * p.zcount +
+                       (GROUP ? p2.live_tiles * p2.units_per_tile : 0);
     const int my_units = (nunits - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);
     const int nkt = (p.K + BK - 1) / BK;
     const bool tri_on = BATCH && p.tri != 0 && *p.tri_bad == 0;
 
-    // producer (thread 0): issues the next k-tile of its unit sequence into a slot
+    // producer: issues the next k-tile of the CTA's unit sequence into a slot
+    // (thread 0 for the first stages, then the last warp done with a stage)
     auto issue_next = [&](int slot) {
         int ar = 0, ac = 0, br = 0, bc = 0;
         if (BATCH && p.zcount > 1) {
@@ -567,12 +600,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             ar = int(ao / p.lda); ac = int(ao % p.lda);
             br = int(bo / p.ldb); bc = int(bo % p.ldb);
         }
-        issue_stage<A_KM, B_KM>(stages + slot * STAGE_FLOATS, &full[slot], &tmA, &tmB,
+        const bool second = GROUP && prod.u.prob;
+        issue_stage<A_KM, B_KM>(stages + slot * STAGE_FLOATS, &full[slot],
+                                second ? &tmA2 : &tmA, second ? &tmB2 : &tmB,
                                 prod.u.m0, prod.u.n0, prod.kt, ar, ac, br, bc);
         ++prod.count;
         if (++prod.kt == prod.u.kt1) {
             if (++prod.ui < my_units) {
-                prod.u = unit_of<BATCH>(p, blockIdx.x + prod.ui * gridDim.x, nkt, tri_on);
+                prod.u = unit_of<BATCH, GROUP>(p, p2, blockIdx.x + prod.ui * gridDim.x, nkt,
+                                               tri_on);
                 prod.kt = prod.u.kt0;
             } else {
                 prod.more = 0;
@@ -583,7 +619,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (tid == 0) {
             for (int s = 0; s < STAGES; ++s) {
                 mbar_init(smem_u32(&full[s]), 1);
-                mbar_init(smem_u32(&empty[s]), THREADS / 32);
+                released[s] = 0;
             }
             abort_flag = 0;
             fence_mbar_init();
@@ -591,7 +627,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             prod.count = 0;
             prod.more = my_units > 0;
             if (prod.more) {
-                prod.u = unit_of<BATCH>(p, blockIdx.x, nkt, tri_on);
+                prod.u = unit_of<BATCH, GROUP>(p, p2, blockIdx.x, nkt, tri_on);
                 prod.kt = prod.u.kt0;
             }
             for (int s = 0; s < STAGES && prod.more; ++s) issue_next(s);
@@ -602,7 +638,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     int64_t it = 0;            // consumer position in the k-tile sequence
     bool aborted = false;
     for (int ui = 0; ui < my_units && !aborted; ++ui) {
-        const Unit w = unit_of<BATCH>(p, blockIdx.x + ui * gridDim.x, nkt, tri_on);
+        const Unit w = unit_of<BATCH, GROUP>(p, p2, blockIdx.x + ui * gridDim.x, nkt, tri_on);
+        const KArgs &q = (GROUP && w.prob) ? p2 : p;   // this unit's product
         float acc[TM][TN];
 #pragma unroll
         for (int r = 0; r < TM; ++r)
@@ -620,16 +657,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
                 __syncthreads();   // everyone is done with the previous k-tile
                 load_tile_plain<A_KM, BM>(stages,
-                                          p.A + (BATCH ? z_offset(p.a_zb, p.a_zh, w.z, p.zinner) : 0),
-                                          p.lda, p.M, p.K, w.m0, kt * BK, tid);
+                                          q.A + (BATCH ? z_offset(p.a_zb, p.a_zh, w.z, p.zinner) : 0),
+                                          q.lda, q.M, q.K, w.m0, kt * BK, tid);
                 load_tile_plain<B_KM, BN>(stages + A_FLOATS,
-                                          p.B + (BATCH ? z_offset(p.b_zb, p.b_zh, w.z, p.zinner) : 0),
-                                          p.ldb,
-                                          p.N, p.K, w.n0, kt * BK, tid);
+                                          q.B + (BATCH ? z_offset(p.b_zb, p.b_zh, w.z, p.zinner) : 0),
+                                          q.ldb,
+                                          q.N, q.K, w.n0, kt * BK, tid);
                 __syncthreads();
             }
             if (ok) {
-                const int kcount = min(BK, p.K - kt * BK);
+                const int kcount = min(BK, q.K - kt * BK);
                 if (kcount == BK) {
 #pragma unroll 1
                     for (int q = 0; q < BK / 4; ++q)
@@ -640,19 +677,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // the unit's last k-tile; a batched tile's chunks run from w.kt0 (0
             // unless skipped) to w.kt1 (nkt unless skipped)
-            const bool last = (SPLIT || !BATCH) ? (kt == nkt - 1) : (kt == w.kt1 - 1);
+            const bool last = (SPLIT || !BATCH) ? (kt == w.nkt - 1) : (kt == w.kt1 - 1);
             const int first_chunk = (SPLIT || !BATCH) ? 0 : w.kt0 / TILES_PER_CHUNK;
             if (((kt + 1) % TILES_PER_CHUNK == 0) || last) {
                 const int chunk = kt / TILES_PER_CHUNK;
                 if (SPLIT) {
                     // split: every chunk partial goes to the workspace
                     if (ok) {
-                        const int ntiles = p.mt * p.nt;
+                        // one base address; the quads sit at constant offsets
+                        float4 *wb = q.W + ws_index(chunk, q.mt * q.nt, w.t, 0, tid);
 #pragma unroll
                         for (int r = 0; r < TM; ++r)
 #pragma unroll
                             for (int h = 0; h < TN / 4; ++h)
-                                __stcg(p.W + ws_index(chunk, ntiles, w.t, r * (TN / 4) + h, tid),
+                                __stcg(wb + (r * (TN / 4) + h) * THREADS,
                                        make_float4(acc[r][4 * h], acc[r][4 * h + 1],
                                                    acc[r][4 * h + 2], acc[r][4 * h + 3]));
                     }
@@ -690,15 +728,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (TMA) {
-                // release the stage: one arrival a warp. No CTA-wide barrier: the
-                // producer (thread 0) waits for the 8 arrivals before refilling
-                // this stage, and the other warps only ever wait for data.
+                // release the stage: the last warp to finish with it refills it,
+                // so no warp ever waits for the others here (the fences order
+                // the producer bookkeeping between successive issuing lanes)
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-                if (tid == 0 && prod.more && !abort_flag) {
-                    if (mbar_wait_or_abort(smem_u32(&empty[s]), uint32_t(it / STAGES) & 1u,
-                                           &abort_flag))
-                        issue_next(s);
+                if (lane == 0) {
+                    __threadfence_block();
+                    if (atomicAdd(&released[s], 1) == THREADS / 32 - 1) {
+                        atomicExch(&released[s], 0);
+                        __threadfence_block();
+                        if (prod.more && !abort_flag) issue_next(s);
+                    }
                 }
                 __syncwarp();
                 if (!ok || abort_flag) { aborted = true; ++it; break; }
@@ -708,13 +748,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         // epilogue (the next unit's loads are already in flight)
         if (!SPLIT)
             store_tile<A_KM, B_KM>(acc,
-                                   p.C + (BATCH ? z_offset(p.c_zb, p.c_zh, w.z, p.zinner) : 0),
-                                   p.ldc,
-                                   p.M, p.N, w.m0, w.n0, arow, bcol,
-                                   p.vec_store, p.accumulate);
+                                   q.C + (BATCH ? z_offset(p.c_zb, p.c_zh, w.z, p.zinner) : 0),
+                                   q.ldc,
+                                   q.M, q.N, w.m0, w.n0, arow, bcol,
+                                   q.vec_store, q.accumulate);
     }
 
-    if (TMA && aborted && tid == 0) {
+    // any warp may have issued the last copies: once every thread is here no
+    // more are issued, and thread 0 drains them
+    __syncthreads();
+    if (TMA && abort_flag && tid == 0) {
         // every warp sees the shared abort flag within one k-tile and leaves its
         // loop. Thread 0 records the event and lets the last copy issued on
         // each stage land before it exits (the CTA's shared memory lives until
@@ -730,6 +773,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // it sums the quad over the chunks and scatters the 4 outputs to the rows and
 // columns the GEMM thread that wrote it owns.
 __global__ void chunk_sum_kernel(KArgs p, int nchunks, int a_km, int b_km) {
+    grid_dependency_wait();
     const int ntiles = p.mt * p.nt;
     const int64_t slots = int64_t(ntiles) * QUADS * THREADS;
     const int64_t cstride = slots;      // one chunk's worth of quads
@@ -779,6 +823,7 @@ __global__ void __launch_bounds__(256)
     transpose_kernel(const float *__restrict__ A, int64_t lda, int M, int K,
                      float *__restrict__ T, int64_t ldt, int vec) {
     __shared__ float tile[kTrTile][kTrTile + 1];
+    grid_dependency_wait();
     const int tid = threadIdx.x;
     const int64_t mtiles = (M + kTrTile - 1) / kTrTile, ktiles = (K + kTrTile - 1) / kTrTile;
     for (int64_t t = blockIdx.x; t < mtiles * ktiles; t += gridDim.x) {
@@ -818,6 +863,7 @@ __global__ void __launch_bounds__(256)
 
 // K == 0: the empty sum, +0 everywhere (C + 0 when accumulating).
 __global__ void fill_zero_kernel(float *C, int64_t ldc, int64_t M, int64_t N, int accum) {
+    grid_dependency_wait();
     const int64_t total = M * N;
     for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total;
          e += int64_t(gridDim.x) * blockDim.x) {
@@ -854,29 +900,47 @@ bool make_map(CUtensorMap *map, const float *base, int64_t inner, int64_t outer,
 
 bool tma_ok(const float *base, int64_t ld) { return tma_operand_ok(base, ld); }
 
+// One product ready to launch: its kernel arguments and tensor maps.
+struct Prepared {
+    KArgs k;
+    CUtensorMap ma, mb;
+    bool tma, a_km, b_km;
+};
+
+// Launches x alone, or x and y (same layout and staging, plain instances
+// only) in one persistent grid whose first units are x's.
 template <bool A_KM, bool B_KM, bool TMA>
-cudaError_t launch_variant(const CUtensorMap &ma, const CUtensorMap &mb, const KArgs &k,
-                           cudaStream_t s) {
+cudaError_t launch_variant(Prepared x, const Prepared *y, cudaStream_t s) {
     // batched products are never split
-    auto kern = k.split ? gemm_kernel<A_KM, B_KM, TMA, true, false>
-                : (k.zcount > 1 || k.causal || k.tri) ? gemm_kernel<A_KM, B_KM, TMA, false, true>
-                                                      : gemm_kernel<A_KM, B_KM, TMA, false, false>;
+    const KArgs &k = x.k;
+    // a two-product launch is never split (gemm_pair_plan)
+    auto kern = y ? gemm_kernel<A_KM, B_KM, TMA, false, false, true>
+                : k.split ? gemm_kernel<A_KM, B_KM, TMA, true, false, false>
+                : (k.zcount > 1 || k.causal || k.tri)
+                    ? gemm_kernel<A_KM, B_KM, TMA, false, true, false>
+                    : gemm_kernel<A_KM, B_KM, TMA, false, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    const int64_t units = int64_t(k.live_tiles) * k.units_per_tile * k.zcount;
+    int64_t units = int64_t(k.live_tiles) * k.units_per_tile * k.zcount;
+    x.k.units0 = int(units);
+    if (y) units += int64_t(y->k.live_tiles) * y->k.units_per_tile;
+    const Prepared &z = y ? *y : x;
     const unsigned grid = unsigned(std::min<int64_t>(units, sm_count_current_device()));
-    kern<<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, k);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, s, x.ma, x.mb, x.k,
+                            z.ma, z.mb, z.k);
 }
 
 template <bool TMA>
-cudaError_t launch_layout(bool a_km, bool b_km, const CUtensorMap &ma,
-                          const CUtensorMap &mb, const KArgs &k, cudaStream_t s) {
-    if (a_km && b_km) return launch_variant<true, true, TMA>(ma, mb, k, s);
-    if (a_km) return launch_variant<true, false, TMA>(ma, mb, k, s);
-    if (b_km) return launch_variant<false, true, TMA>(ma, mb, k, s);
-    return launch_variant<false, false, TMA>(ma, mb, k, s);
+cudaError_t launch_layout(const Prepared &x, const Prepared *y, cudaStream_t s) {
+    if (x.a_km && x.b_km) return launch_variant<true, true, TMA>(x, y, s);
+    if (x.a_km) return launch_variant<true, false, TMA>(x, y, s);
+    if (x.b_km) return launch_variant<false, true, TMA>(x, y, s);
+    return launch_variant<false, false, TMA>(x, y, s);
+}
+
+cudaError_t launch_prepared(const Prepared &x, const Prepared *y, cudaStream_t s) {
+    return x.tma ? launch_layout<true>(x, y, s) : launch_layout<false>(x, y, s);
 }
 
 }  // namespace
@@ -982,6 +1046,65 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor) {
     return pl;
 }
 
+namespace {
+// Kernel arguments and tensor maps of a non-batched product under plan pl
+// (split partials, if any, go to W).
+Prepared prepare(const GemmArgs &a, const GemmPlan &pl, void *W) {
+    Prepared x{};
+    KArgs &k = x.k;
+    k.M = int(a.M); k.N = int(a.N); k.K = int(a.K);
+    k.lda = a.lda; k.ldb = a.ldb; k.ldc = a.ldc;
+    k.A = a.A; k.B = a.B; k.C = a.C;
+    k.mt = int((a.M + BM - 1) / BM);
+    k.nt = int((a.N + BN - 1) / BN);
+    k.m_fast = a.M <= a.N;
+    k.vec_store = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && (a.ldc % 4 == 0);
+    k.split = pl.split;
+    k.units_per_tile = pl.units_per_tile;
+    k.kt_per_unit = pl.kt_per_unit;
+    k.W = static_cast<float4 *>(pl.split ? W : nullptr);
+    k.accumulate = a.accumulate;
+    k.zcount = 1;
+    k.zinner = 1;
+    k.a_zb = k.a_zh = k.b_zb = k.b_zh = k.c_zb = k.c_zh = 0;
+    k.causal = 0;
+    k.live_tiles = k.mt * k.nt;
+    k.tri = 0;
+    k.tri_bad = nullptr;
+    k.units0 = k.live_tiles * k.units_per_tile;
+    // op(A) is k-contiguous when A is not transposed; op(B) when B is.
+    x.a_km = !a.transA;
+    x.b_km = a.transB != 0;
+    x.tma = tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb);
+    if (x.tma) {
+        x.tma = x.a_km ? make_map(&x.ma, a.A, a.K, a.M, a.lda, true, BM)
+                       : make_map(&x.ma, a.A, a.M, a.K, a.lda, false, BM);
+        x.tma = x.tma && (x.b_km ? make_map(&x.mb, a.B, a.K, a.N, a.ldb, true, BN)
+                                 : make_map(&x.mb, a.B, a.N, a.K, a.ldb, false, BN));
+    }
+    return x;
+}
+
+// T (K x M, row stride ldt) = A^T for A (M x K, row stride lda).
+cudaError_t launch_transpose(const float *A, int64_t lda, int64_t M, int64_t K, float *T,
+                             int64_t ldt, int sms, cudaStream_t s) {
+    const int64_t tiles = ((M + kTrTile - 1) / kTrTile) * ((K + kTrTile - 1) / kTrTile);
+    const unsigned blocks = unsigned(std::min<int64_t>(tiles, int64_t(sms) * 8));
+    const int vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (lda % 4 == 0);
+    return launch_dependent(transpose_kernel, dim3(blocks), dim3(256), 0, s, A, lda, int(M),
+                            int(K), T, ldt, vec);
+}
+
+cudaError_t launch_chunk_sum(const Prepared &x, int nchunks, int sms, cudaStream_t s) {
+    const KArgs &k = x.k;
+    const int64_t slots = int64_t(k.mt) * k.nt * QUADS * THREADS;
+    const int64_t blocks =
+        std::max<int64_t>(1, std::min<int64_t>((slots + 255) / 256, int64_t(sms) * 8));
+    return launch_dependent(chunk_sum_kernel, dim3(unsigned(blocks)), dim3(256), 0, s, k,
+                            nchunks, int(x.a_km), int(x.b_km));
+}
+}  // namespace
+
 cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_bytes,
                         cudaStream_t s) {
     if (a.M == 0 || a.N == 0) return cudaSuccess;
@@ -1004,11 +1127,7 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
         // op(A) from the K x M copy: the transA form of the same product
         float *T = static_cast<float *>(workspace);
         const int64_t ldt = transposed_ld(a.M);
-        const int64_t tiles = ((a.M + kTrTile - 1) / kTrTile) * ((a.K + kTrTile - 1) / kTrTile);
-        const unsigned blocks = unsigned(std::min<int64_t>(tiles, int64_t(sms) * 8));
-        const int vec = (reinterpret_cast<uintptr_t>(a.A) % 16 == 0) && (a.lda % 4 == 0);
-        transpose_kernel<<<blocks, 256, 0, s>>>(a.A, a.lda, int(a.M), int(a.K), T, ldt, vec);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_transpose(a.A, a.lda, a.M, a.K, T, ldt, sms, s);
         if (e != cudaSuccess) return e;
         GemmArgs t = a;
         t.A = T;
@@ -1016,43 +1135,185 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
         t.transA = 1;
         return launch_gemm(t, nullptr, 0, s);
     }
-    KArgs k;
-    k.M = int(a.M); k.N = int(a.N); k.K = int(a.K);
-    k.lda = a.lda; k.ldb = a.ldb; k.ldc = a.ldc;
-    k.A = a.A; k.B = a.B; k.C = a.C;
-    k.mt = int((a.M + BM - 1) / BM);
-    k.nt = int((a.N + BN - 1) / BN);
-    k.m_fast = a.M <= a.N;
-    k.vec_store = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && (a.ldc % 4 == 0);
-    k.split = pl.split;
-    k.units_per_tile = pl.units_per_tile;
-    k.kt_per_unit = pl.kt_per_unit;
-    k.W = static_cast<float4 *>(pl.split ? workspace : nullptr);
-    k.accumulate = a.accumulate;
-    k.zcount = 1;
-    k.zinner = 1;
-    k.a_zb = k.a_zh = k.b_zb = k.b_zh = k.c_zb = k.c_zh = 0;
-    k.causal = 0;
-    k.live_tiles = k.mt * k.nt;
-    k.tri = 0;
-    k.tri_bad = nullptr;
-    // op(A) is k-contiguous when A is not transposed; op(B) when B is.
-    const bool a_km = !a.transA, b_km = a.transB != 0;
-    CUtensorMap ma{}, mb{};
-    bool tma = tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb);
-    if (tma) {
-        tma = a_km ? make_map(&ma, a.A, a.K, a.M, a.lda, true, BM)
-                   : make_map(&ma, a.A, a.M, a.K, a.lda, false, BM);
-        tma = tma && (b_km ? make_map(&mb, a.B, a.K, a.N, a.ldb, true, BN)
-                           : make_map(&mb, a.B, a.N, a.K, a.ldb, false, BN));
-    }
-    cudaError_t e = tma ? launch_layout<true>(a_km, b_km, ma, mb, k, s)
-                        : launch_layout<false>(a_km, b_km, ma, mb, k, s);
+    const Prepared x = prepare(a, pl, workspace);
+    cudaError_t e = launch_prepared(x, nullptr, s);
     if (e != cudaSuccess || !pl.split) return e;
-    const int64_t slots = int64_t(k.mt) * k.nt * QUADS * THREADS;
-    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((slots + 255) / 256, int64_t(sms) * 8));
-    chunk_sum_kernel<<<unsigned(blocks), 256, 0, s>>>(k, pl.nchunks, a_km, b_km);
-    return cudaGetLastError();
+    return launch_chunk_sum(x, pl.nchunks, sms, s);
+}
+
+// ---------------------------------------------------------------- two products, one launch
+// Two independent products of the same layout can share one persistent grid:
+// their work units are dealt out together, so the grid's last round is
+// filled from both (a product alone leaves part of the 152 SMs idle when its
+// units do not divide evenly). Both run unsplit, or both split K into groups
+// of the same number of chunks; each product's units, chains, partials and
+// chunk sums are exactly those of its own launch, so the bits are the same.
+namespace {
+constexpr double kKtStepS = 6.0e-6, kHbmBps = 6.0e12, kLaunchS = 5.0e-6;
+
+// The k-tile steps of the busiest CTA when units with the given steps are
+// dealt round-robin (unit u to CTA u mod grid) over min(units, sms) CTAs.
+double busiest_of(const std::vector<int> &steps, int sms) {
+    const int64_t n = int64_t(steps.size());
+    const int64_t grid = std::min<int64_t>(n, sms);
+    double worst = 0.0;
+    for (int64_t b = 0; b < grid; ++b) {
+        double t = 0.0;
+        for (int64_t u = b; u < n; u += grid) t += steps[size_t(u)];
+        worst = std::max(worst, t);
+    }
+    return worst;
+}
+
+// Appends a product's units: T tiles, each split into groups of G chunks
+// (G >= nchunks: one unit over all of K), tiles running fastest.
+void append_units(std::vector<int> &steps, int64_t T, int64_t nkt, int64_t nchunks, int64_t G) {
+    const int64_t S = (nchunks + G - 1) / G;
+    for (int64_t g = 0; g < S; ++g) {
+        const int64_t kt0 = g * G * TILES_PER_CHUNK;
+        const int st = int(std::min<int64_t>(nkt, kt0 + G * TILES_PER_CHUNK) - kt0);
+        for (int64_t t = 0; t < T; ++t) steps.push_back(st);
+    }
+}
+
+struct Shape {
+    int64_t T, nkt, nchunks, cbytes;
+};
+Shape shape_of(const GemmArgs &a) {
+    return {((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN), (a.K + BK - 1) / BK,
+            (a.K + kKChunk - 1) / kKChunk, a.M * a.N * 4};
+}
+
+// Modelled time of a product alone under its own plan.
+double alone_cost(const GemmArgs &a, const GemmPlan &pl, int sms) {
+    const Shape h = shape_of(a);
+    std::vector<int> steps;
+    append_units(steps, h.T, h.nkt, h.nchunks,
+                 pl.split ? pl.kt_per_unit / TILES_PER_CHUNK : h.nchunks);
+    double c = busiest_of(steps, sms) * kKtStepS + kLaunchS;
+    if (pl.split)
+        c += (2.0 * double(pl.workspace_bytes) + double(h.cbytes)) / kHbmBps + kLaunchS;
+    return c;
+}
+}  // namespace
+
+PairPlan gemm_pair_plan(const GemmArgs &a0, const GemmArgs &a1, int sms) {
+    PairPlan pp{};
+    pp.pair = 0;
+    pp.p0 = gemm_plan(a0.M, a0.N, a0.K, sms, !a0.transA);
+    pp.p1 = gemm_plan(a1.M, a1.N, a1.K, sms, !a1.transA);
+    pp.separate_bytes = std::max(pp.p0.workspace_bytes, pp.p1.workspace_bytes);
+    pp.shared_transpose = 0;
+    if (a0.M == 0 || a0.N == 0 || a0.K == 0 || a1.M == 0 || a1.N == 0 || a1.K == 0 ||
+        sms < 1 || (a0.transA != 0) != (a1.transA != 0) ||
+        (a0.transB != 0) != (a1.transB != 0))
+        return pp;
+    const Shape h0 = shape_of(a0), h1 = shape_of(a1);
+    if (pp.p0.transpose_a || pp.p1.transpose_a) {
+        // Products of one A (the gate and up projections of one input), each
+        // of which would read a transposed copy of it: one copy serves both,
+        // and their tiles share one grid.
+        if (!(pp.p0.transpose_a && pp.p1.transpose_a && a0.A == a1.A && a0.lda == a1.lda &&
+              a0.M == a1.M && a0.K == a1.K))
+            return pp;
+        const double copy = kLaunchS + 8.0 * double(a0.M) * double(a0.K) / kHbmBps;
+        std::vector<int> s0, s1, both;
+        append_units(s0, h0.T, h0.nkt, h0.nchunks, h0.nchunks);
+        append_units(s1, h1.T, h1.nkt, h1.nchunks, h1.nchunks);
+        both = s0;
+        both.insert(both.end(), s1.begin(), s1.end());
+        const double separate = busiest_of(s0, sms) * kKtStepS + busiest_of(s1, sms) * kKtStepS +
+                                2.0 * (copy + kLaunchS);
+        const double paired = busiest_of(both, sms) * kKtStepS + copy + kLaunchS;
+        if (paired < 0.97 * separate) {
+            pp.pair = 1;
+            pp.split = 0;
+            pp.shared_transpose = 1;
+            pp.p0 = GemmPlan{};
+            pp.p0.units_per_tile = 1;
+            pp.p0.kt_per_unit = int(h0.nkt);
+            pp.p0.nchunks = int(h0.nchunks);
+            pp.p1 = pp.p0;
+            pp.p1.kt_per_unit = int(h1.nkt);
+            pp.p1.nchunks = int(h1.nchunks);
+            pp.ws0_bytes = 0;
+            pp.workspace_bytes = size_t(a0.K) * size_t(transposed_ld(a0.M)) * 4;
+        }
+        return pp;
+    }
+    const double separate = alone_cost(a0, pp.p0, sms) + alone_cost(a1, pp.p1, sms);
+    double best = 0.97 * separate;
+    // both unsplit
+    {
+        std::vector<int> steps;
+        append_units(steps, h0.T, h0.nkt, h0.nchunks, h0.nchunks);
+        append_units(steps, h1.T, h1.nkt, h1.nchunks, h1.nchunks);
+        const double c = busiest_of(steps, sms) * kKtStepS + kLaunchS;
+        if (c < best) {
+            best = c;
+            pp.pair = 1;
+            pp.split = 0;
+        }
+    }
+    // Split pairs are not taken: measured on the weight-gradient pair
+    // (768 x 2304 and 2048 x 768 over 8,192 tokens), the two-product split
+    // instance ran 5% slower than the two launches, its better balance
+    // outweighed by the per-unit product selection in its loop.
+    if (!pp.pair) return pp;
+    auto set = [&](GemmPlan &pl, const Shape &h) {
+        pl = GemmPlan{};
+        pl.nchunks = int(h.nchunks);
+        pl.split = pp.split;
+        pl.units_per_tile = pp.split ? int((h.nchunks + pp.group - 1) / pp.group) : 1;
+        pl.kt_per_unit = pp.split ? pp.group * TILES_PER_CHUNK : int(h.nkt);
+        pl.workspace_bytes = pp.split ? size_t(h.nchunks * h.T) * BM * BN * 4 : 0;
+    };
+    set(pp.p0, h0);
+    set(pp.p1, h1);
+    pp.ws0_bytes = pp.p0.workspace_bytes;
+    pp.workspace_bytes = pp.p0.workspace_bytes + pp.p1.workspace_bytes;
+    return pp;
+}
+
+cudaError_t launch_gemm_pair(const GemmArgs &a0, const GemmArgs &a1, void *workspace,
+                             size_t workspace_bytes, cudaStream_t s) {
+    const int sms = sm_count_current_device();
+    const PairPlan pp = gemm_pair_plan(a0, a1, sms);
+    const bool ws_ok = pp.workspace_bytes == 0 ||
+                       (workspace != nullptr && workspace_bytes >= pp.workspace_bytes &&
+                        reinterpret_cast<uintptr_t>(workspace) % 16 == 0);
+    if (pp.pair && pp.shared_transpose && ws_ok && !a0.accumulate && !a1.accumulate) {
+        // one transposed copy of the shared A, then both products read it
+        float *T = static_cast<float *>(workspace);
+        const int64_t ldt = transposed_ld(a0.M);
+        cudaError_t e = launch_transpose(a0.A, a0.lda, a0.M, a0.K, T, ldt, sms, s);
+        if (e != cudaSuccess) return e;
+        GemmArgs t0 = a0, t1 = a1;
+        t0.A = t1.A = T;
+        t0.lda = t1.lda = ldt;
+        t0.transA = t1.transA = 1;
+        const Prepared x = prepare(t0, pp.p0, nullptr), y = prepare(t1, pp.p1, nullptr);
+        if (x.tma == y.tma) return launch_prepared(x, &y, s);
+        e = launch_prepared(x, nullptr, s);
+        if (e != cudaSuccess) return e;
+        return launch_prepared(y, nullptr, s);
+    }
+    if (pp.pair && !pp.shared_transpose && ws_ok && !a0.accumulate && !a1.accumulate) {
+        const Prepared x = prepare(a0, pp.p0, workspace);
+        const Prepared y =
+            prepare(a1, pp.p1, static_cast<unsigned char *>(workspace) + pp.ws0_bytes);
+        if (x.tma == y.tma && x.a_km == y.a_km && x.b_km == y.b_km) {
+            cudaError_t e = launch_prepared(x, &y, s);
+            if (e != cudaSuccess || !pp.split) return e;
+            e = launch_chunk_sum(x, pp.p0.nchunks, sms, s);
+            if (e != cudaSuccess) return e;
+            return launch_chunk_sum(y, pp.p1.nchunks, sms, s);
+        }
+    }
+    // one after the other (the workspace serves each in turn)
+    cudaError_t e = launch_gemm(a0, workspace, workspace_bytes, s);
+    if (e != cudaSuccess) return e;
+    return launch_gemm(a1, workspace, workspace_bytes, s);
 }
 
 cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s) {
@@ -1067,8 +1328,8 @@ cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStre
         }
         return cudaGetLastError();
     }
-    const int sms = sm_count_current_device();
-    KArgs k;
+    Prepared x{};
+    KArgs &k = x.k;
     k.M = int(a.M); k.N = int(a.N); k.K = int(a.K);
     k.lda = a.lda; k.ldb = a.ldb; k.ldc = a.ldc;
     k.A = a.A; k.B = a.B; k.C = a.C;
@@ -1097,22 +1358,22 @@ cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStre
             live += std::min<int64_t>(k.nt, (int64_t(mb) * BM + BM - 1) / BN + 1);
     }
     k.live_tiles = int(live);
+    k.units0 = k.live_tiles * k.zcount;
     const bool off4 = bt.a_zb % 4 == 0 && bt.a_zh % 4 == 0 && bt.b_zb % 4 == 0 &&
                       bt.b_zh % 4 == 0;
     k.vec_store = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && (a.ldc % 4 == 0) &&
                   bt.c_zb % 4 == 0 && bt.c_zh % 4 == 0;
-    const bool a_km = !a.transA, b_km = a.transB != 0;
-    CUtensorMap ma{}, mb{};
+    x.a_km = !a.transA;
+    x.b_km = a.transB != 0;
     // one map spans each whole buffer; a product's tile coordinates add its
     // offset's row and column, which TMA needs on a 16-byte boundary
-    bool tma = off4 && tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb) && bt.a_rows < (int64_t(1) << 31) &&
-               bt.b_rows < (int64_t(1) << 31);
-    if (tma) {
-        tma = make_map(&ma, a.A, bt.a_cols, bt.a_rows, a.lda, a_km, BM) &&
-              make_map(&mb, a.B, bt.b_cols, bt.b_rows, a.ldb, b_km, BN);
+    x.tma = off4 && tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb) &&
+            bt.a_rows < (int64_t(1) << 31) && bt.b_rows < (int64_t(1) << 31);
+    if (x.tma) {
+        x.tma = make_map(&x.ma, a.A, bt.a_cols, bt.a_rows, a.lda, x.a_km, BM) &&
+                make_map(&x.mb, a.B, bt.b_cols, bt.b_rows, a.ldb, x.b_km, BN);
     }
-    return tma ? launch_layout<true>(a_km, b_km, ma, mb, k, s)
-               : launch_layout<false>(a_km, b_km, ma, mb, k, s);
+    return launch_prepared(x, nullptr, s);
 }
 
 // ---------------------------------------------------------------- no-allocation variant

@@ -850,6 +850,10 @@ __global__ void __launch_bounds__(kMeanThreads)
     mean_kernel(int64_t n, const float *__restrict__ v, float *out) {
     __shared__ float buf[kMeanBlock];
     const int tid = threadIdx.x;
+    // launched as a programmatic dependent of the kernel that writes v: its
+    // launch overlaps that kernel, and this wait returns once that grid has
+    // completed and its writes are visible (a plain launch returns at once)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float s = 0.0f;
     for (int64_t base = 0; base < n; base += kMeanBlock) {
         const int cnt = int(n - base < kMeanBlock ? n - base : kMeanBlock);
@@ -955,7 +959,21 @@ cudaError_t launch_xent(int64_t rows, int64_t V, const float *logits, int64_t ld
     }
     e = cudaGetLastError();
     if (e != cudaSuccess || !loss_mean) return e;
-    mean_kernel<<<1, kMeanThreads, 0, s>>>(rows, loss, loss_mean);
+    // the mean as a programmatic dependent of the row kernel (its launch
+    // latency hidden behind the rows; griddepcontrol.wait orders the reads)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kMeanThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, mean_kernel, int64_t(rows), static_cast<const float *>(loss),
+                           loss_mean);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

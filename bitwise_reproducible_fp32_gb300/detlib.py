@@ -34,6 +34,15 @@ class Profile(ctypes.Structure):
                 ("lane_group", ctypes.c_uint32), ("flags", ctypes.c_uint32)]
 
 
+class GemmProblem(ctypes.Structure):
+    """det_gemm_problem."""
+    _fields_ = [("transA", ctypes.c_int), ("transB", ctypes.c_int),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("A", ctypes.c_void_p), ("lda", ctypes.c_int64),
+                ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64),
+                ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64)]
+
+
 class AdamWHP(ctypes.Structure):
     """det_adamw_hp."""
     _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float),
@@ -57,6 +66,12 @@ SIGNATURES = [
     ("detshardsum_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _f, _vp, _vp]),
     ("detgemm_workspace_bytes", _int, [_PROF, _int, _int, _i64, _i64, _i64,
                                        ctypes.POINTER(ctypes.c_size_t)]),
+    ("detgemm_group_f32", _int, [_PROF, _i64, ctypes.POINTER(GemmProblem), _vp,
+                                 ctypes.c_size_t, _vp]),
+    ("detgemm_group_workspace_bytes", _int, [_PROF, _i64, ctypes.POINTER(GemmProblem),
+                                             ctypes.POINTER(ctypes.c_size_t)]),
+    ("detgemm_group_launches", _int, [_PROF, _i64, ctypes.POINTER(GemmProblem),
+                                      ctypes.c_size_t, ctypes.POINTER(ctypes.c_int64)]),
     ("detgemm_f32_noalloc", _int, [_PROF, _int, _int, _i64, _i64, _i64, _vp, _i64, _vp,
                                    _i64, _vp, _i64, _vp]),
     ("detrmsnorm_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _vp, _f, _vp, _i64, _vp,
@@ -163,7 +178,8 @@ def _cuda_f32(t, name, ndim=None):
 
 
 def _ld(t):
-    return t.stride(0) if t.dim() == 2 and t.shape[0] > 0 else max(t.shape[-1], 1)
+    # an empty matrix has no row stride to speak of: report its row length
+    return t.stride(0) if t.dim() == 2 and t.numel() > 0 else max(t.shape[-1], 1)
 
 
 # ---------------------------------------------------------------- GEMM
@@ -277,6 +293,73 @@ def detgemm_f32_noalloc(A, B, C, transA=False, transB=False, profile=None, strea
                                     _ld(C), _stream(stream))
     _check("detgemm_f32_noalloc", st)
     return C
+
+
+def _problems(problems):
+    """det_gemm_problem array from dicts with A, B, C (2-D float32 CUDA
+    tensors) and optional transA / transB."""
+    arr = (GemmProblem * len(problems))()
+    for i, q in enumerate(problems):
+        A, B, C = q["A"], q["B"], q["C"]
+        tA, tB = bool(q.get("transA", False)), bool(q.get("transB", False))
+        for t, name in ((A, "A"), (B, "B"), (C, "C")):
+            _cuda_f32(t, name, 2)
+        M, K = (A.shape[1], A.shape[0]) if tA else (A.shape[0], A.shape[1])
+        Kb, N = (B.shape[1], B.shape[0]) if tB else (B.shape[0], B.shape[1])
+        if K != Kb:
+            raise ValueError(f"problem {i}: inner dimensions differ: {K} vs {Kb}")
+        if tuple(C.shape) != (M, N):
+            raise ValueError(f"problem {i}: C must be {M} x {N}")
+        arr[i] = GemmProblem(int(tA), int(tB), M, N, K, A.data_ptr(), _ld(A), B.data_ptr(),
+                             _ld(B), C.data_ptr(), _ld(C))
+    return arr
+
+
+def detgemm_group_workspace_bytes(problems, profile=None) -> int:
+    n = ctypes.c_size_t()
+    arr = _problems(problems)
+    _check("detgemm_group_workspace_bytes",
+           load().detgemm_group_workspace_bytes(_prof(profile), len(problems), arr,
+                                                ctypes.byref(n)))
+    return n.value
+
+
+def detgemm_group_launches(problems, workspace=None, profile=None) -> int:
+    """Kernel launches detgemm_group_f32 makes for these problems with this
+    workspace (a tensor or None)."""
+    n = ctypes.c_int64()
+    arr = _problems(problems)
+    wsn = 0 if workspace is None else workspace.numel() * 4
+    _check("detgemm_group_launches",
+           load().detgemm_group_launches(_prof(profile), len(problems), arr, wsn,
+                                         ctypes.byref(n)))
+    return n.value
+
+
+def gemm_group_workspace(problems, device=None):
+    """A workspace tensor for detgemm_group_f32 on these problems (None when
+    none helps)."""
+    import torch
+    n = detgemm_group_workspace_bytes(problems)
+    if n == 0:
+        return None
+    return torch.empty((n + 3) // 4, dtype=torch.float32,
+                       device=device if device is not None else problems[0]["C"].device)
+
+
+def detgemm_group_f32(problems, workspace=None, profile=None, stream=None):
+    """Independent products C_i = op(A_i) op(B_i), each with detgemm_f32's
+    bits; consecutive pairs may share a launch. problems: dicts with A, B, C
+    (and optional transA, transB). Returns the list of C."""
+    arr = _problems(problems)
+    wsp, wsn = ctypes.c_void_p(), 0
+    if workspace is not None:
+        _cuda_f32(workspace, "workspace")
+        wsp, wsn = _ptr(workspace), workspace.numel() * 4
+    st = load().detgemm_group_f32(_prof(profile), len(problems), arr, wsp, wsn,
+                                  _stream(stream))
+    _check("detgemm_group_f32", st)
+    return [q["C"] for q in problems]
 
 
 # ---------------------------------------------------------------- RMSNorm

@@ -9,6 +9,10 @@ DRAM counters mean something:
             workspace: X is copied transposed first, as in the benchmark)
   qkv       GEMM 8192 x 2304 x 768 (likewise)
   dw_qkv    GEMM X^T dY, 768 x 2304 over 8192 tokens
+  dw_pair   the two weight-gradient GEMMs (768 x 2304 and 2048 x 768 over 8192
+            tokens) as one group, as the benchmark runs them
+  gate_up   the gate and up projections of one 8192 x 768 input (768 x 2048
+            each) as one group: one transposed copy, one grid
   xent      cross-entropy 1024 x 50257 with dlogits and mean
   rmsnorm   RMSNorm 8192 x 768
   rms_bwd   RMSNorm backward 8192 x 768 (dx, dgain)
@@ -32,8 +36,8 @@ def main(argv=None):
     from bitwise_reproducible_fp32_gb300 import build, detlib, inputs
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["lm_head", "qkv", "dw_qkv", "xent", "rmsnorm", "rms_bwd",
-                                    "shardsum", "adamw", "softmax"])
+    ap.add_argument("case", choices=["lm_head", "qkv", "dw_qkv", "dw_pair", "gate_up", "xent",
+                                    "rmsnorm", "rms_bwd", "shardsum", "adamw", "softmax"])
     ap.add_argument("--reps", type=int, default=2)
     a = ap.parse_args(argv)
     build.build()
@@ -58,6 +62,22 @@ def main(argv=None):
         C = torch.empty((p["A"].shape[1], p["B"].shape[1]), dtype=torch.float32, device=dev)
         ws = detlib.gemm_workspace(C.shape[0], C.shape[1], p["A"].shape[0], True, False)
         run = lambda: detlib.detgemm_f32(A, B, C, transA=True, workspace=ws)
+    elif a.case == "dw_pair":
+        probs = []
+        for p in inputs.dw_cfg5():
+            A, B = up(p["A"]), up(p["B"])
+            C = torch.empty((p["A"].shape[1], p["B"].shape[1]), dtype=torch.float32, device=dev)
+            probs.append(dict(A=A, B=B, C=C, transA=True))
+        ws = detlib.gemm_group_workspace(probs)
+        run = lambda: detlib.detgemm_group_f32(probs, workspace=ws)
+    elif a.case == "gate_up":
+        fw = {p["name"]: p for p in inputs.gemm_cfg3()}
+        X = up(fw["swiglu_gate"]["A"])
+        probs = [dict(A=X, B=up(fw[n]["B"]), C=torch.empty((X.shape[0], fw[n]["B"].shape[1]),
+                                                             dtype=torch.float32, device=dev))
+                 for n in ("swiglu_gate", "swiglu_up")]
+        ws = detlib.gemm_group_workspace(probs)
+        run = lambda: detlib.detgemm_group_f32(probs, workspace=ws)
     elif a.case in ("xent", "rmsnorm"):
         r = inputs.rowops_cfg4(rows=1024 if a.case == "xent" else 8192)
         if a.case == "xent":

@@ -117,6 +117,56 @@ det_status detgemm_f32(const det_profile_v1 *prof, int transA, int transB,
                        void *workspace, size_t workspace_bytes,
                        det_stream_t stream);
 
+/* One product of a group (detgemm_group_f32): the arguments of detgemm_f32,
+ * with the same meaning, layout and rules. */
+typedef struct det_gemm_problem {
+    int transA, transB;
+    int64_t M, N, K;
+    const float *A;
+    int64_t lda;
+    const float *B;
+    int64_t ldb;
+    float *C;
+    int64_t ldc;
+} det_gemm_problem;
+
+/* Several independent products in one call, for example the weight gradients
+ * of one layer (dW = X^T dY for each of its weights; "mojolearn" PyPI page,
+ * section "Install": weight gradients contract over the token count). Every
+ * C receives exactly the bits detgemm_f32 would give it: the profile fixes
+ * each output's chains and chunk order, never the schedule.
+ *
+ * problems: count host structs, read during the call. The products are taken
+ * in consecutive pairs (0, 1), (2, 3), ... (an odd last one alone); a pair
+ * of the same transA/transB layout runs as one launch when the library's
+ * model finds that faster -- its work units are dealt out together, which
+ * fills the grid's last round from both products -- and otherwise the two
+ * run one after the other. Each C must not overlap any A, B or other C.
+ * workspace / workspace_bytes: as detgemm_f32's, at least
+ * detgemm_group_workspace_bytes() for the same problems to take the faster
+ * plans (less, or NULL, still gives the same bits). The calls of a group are
+ * asynchronous on `stream`, in order.
+ *
+ * Errors: as detgemm_f32 for any problem (nothing is launched then);
+ * DET_ERR_INVALID_ARG for count < 0 or a null array with count > 0. */
+det_status detgemm_group_f32(const det_profile_v1 *prof, int64_t count,
+                             const det_gemm_problem *problems, void *workspace,
+                             size_t workspace_bytes, det_stream_t stream);
+
+/* Workspace that detgemm_group_f32 can use for these problems on the current
+ * device, written to *bytes (a pair that shares a launch needs the sum of its
+ * split partials; otherwise the largest single need). */
+det_status detgemm_group_workspace_bytes(const det_profile_v1 *prof, int64_t count,
+                                         const det_gemm_problem *problems, size_t *bytes);
+
+/* The number of kernels detgemm_group_f32 launches for these problems with a
+ * workspace of workspace_bytes, written to *launches (for callers that count
+ * or capture launches). Same argument rules; host-only apart from reading the
+ * device's SM count. */
+det_status detgemm_group_launches(const det_profile_v1 *prof, int64_t count,
+                                  const det_gemm_problem *problems, size_t workspace_bytes,
+                                  int64_t *launches);
+
 /* Gradient accumulation (beta = 1): C = C + op(A) op(B). The product is formed
  * exactly as detgemm_f32 forms it (256-wide chunk chains from +0, partials
  * added left to right) and then added to the old C by one rounded addition,

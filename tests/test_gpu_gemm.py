@@ -215,3 +215,97 @@ def test_repeatable_across_runs_and_streams(dev):
 def test_watchdog_clean(dev):
     torch.cuda.synchronize()
     assert detlib.det_watchdog_status() == 0
+
+
+# ---------------------------------------------------------------- groups of products
+def group_case(shapes, seed, layouts=None):
+    """Host operands for products (M, N, K, transA, transB)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i, (M, N, K, tA, tB) in enumerate(shapes):
+        A = rng.standard_normal((K, M) if tA else (M, K)).astype(F)
+        B = rng.standard_normal((N, K) if tB else (K, N)).astype(F)
+        la = layouts[i] if layouts else "dense"
+        out.append(dict(A=A, B=B, transA=tA, transB=tB, layout=la, M=M, N=N))
+    return out
+
+
+def run_group(case, workspace=True):
+    probs = [dict(A=to_dev(c["A"], c["layout"]), B=to_dev(c["B"], c["layout"]),
+                  C=empty_dev(c["M"], c["N"], c["layout"]), transA=c["transA"],
+                  transB=c["transB"]) for c in case]
+    ws = detlib.gemm_group_workspace(probs) if workspace else None
+    detlib.detgemm_group_f32(probs, workspace=ws)
+    torch.cuda.synchronize()
+    return [host(p["C"]) for p in probs]
+
+
+@pytest.mark.parametrize("shapes", [
+    # split pairs (weight-gradient form and plain), an unsplit pair, ragged
+    [(300, 200, 1300, True, False), (129, 77, 2049, True, False)],
+    [(300, 200, 1300, False, False), (129, 77, 2049, False, False)],
+    [(600, 500, 300, True, True), (257, 900, 300, True, True)],
+    [(64, 192, 2048, True, False), (64, 64, 2048, True, False), (172, 64, 2048, True, False)],
+    # layouts differ: run one after the other
+    [(200, 300, 700, True, False), (200, 300, 700, False, True)],
+    # an empty product in the middle, and K = 0
+    [(100, 0, 300, False, False), (130, 90, 600, False, False), (40, 50, 0, False, False)],
+])
+def test_group_equals_the_oracle(dev, shapes):
+    case = group_case(shapes, 77)
+    for use_ws in (True, False):
+        got = run_group(case, workspace=use_ws)
+        for c, g in zip(case, got):
+            want = oracle.gemm(c["A"], c["B"], transA=c["transA"], transB=c["transB"])
+            assert_bitwise(g, want, f"{shapes} workspace={use_ws}")
+
+
+def test_group_plain_load_staging(dev):
+    # operands TMA cannot describe (rows one float off a 16-byte boundary)
+    case = group_case([(300, 200, 1300, True, False), (129, 77, 2049, True, False)], 78,
+                      layouts=["offset", "offset"])
+    for c, g in zip(case, run_group(case)):
+        assert_bitwise(g, oracle.gemm(c["A"], c["B"], transA=True), "offset layout")
+
+
+def test_group_cfg5_dw_pair_full_size(dev):
+    # the two weight-gradient GEMMs of the 162M step in one call, as the
+    # benchmark runs them: sampled rows against the oracle, every bit against
+    # detgemm_f32
+    ps = inputs.dw_cfg5()
+    probs = []
+    for p in ps:
+        A, B = to_dev(p["A"]), to_dev(p["B"])
+        probs.append(dict(A=A, B=B, transA=True, C=torch.empty((p["A"].shape[1], p["B"].shape[1]),
+                                                             dtype=torch.float32, device="cuda")))
+    ws = detlib.gemm_group_workspace(probs)
+    assert ws is not None
+    detlib.detgemm_group_f32(probs, workspace=ws)
+    for p, q in zip(ps, probs):
+        check_rows(p, q["C"], sampled_rows(q["C"].shape[0], 18, 5))
+        alone = detlib.detgemm_f32(q["A"], q["B"], transA=True,
+                                   workspace=detlib.gemm_workspace(*q["C"].shape,
+                                                                   p["A"].shape[0], True, False))
+        assert_bitwise(host(q["C"]), host(alone), p["name"] + ": group vs alone")
+
+
+def test_group_shared_input_takes_one_transposed_copy(dev):
+    # two products of one A (the gate and up projections of one input) large
+    # enough that each alone would read a transposed copy of A: the group
+    # makes one copy for both, and each result is the oracle's
+    rng = np.random.default_rng(79)
+    M, N, K = 8192, 2048, 768          # the 162M block's gate and up projections
+    A = rng.standard_normal((M, K)).astype(F)
+    B1 = (0.02 * rng.standard_normal((K, N))).astype(F)
+    B2 = (0.02 * rng.standard_normal((K, N))).astype(F)
+    Ad = to_dev(A)
+    probs = [dict(A=Ad, B=to_dev(B1), C=empty_dev(M, N)), dict(A=Ad, B=to_dev(B2), C=empty_dev(M, N))]
+    ws = detlib.gemm_group_workspace(probs)
+    assert ws is not None and ws.numel() * 4 >= K * M * 4      # one copy of A
+    assert detlib.detgemm_group_launches(probs, ws) == 2       # the copy, one GEMM
+    detlib.detgemm_group_f32(probs, workspace=ws)
+    torch.cuda.synchronize()
+    rows = sampled_rows(M, 24, 6)
+    for B, q in zip((B1, B2), probs):
+        want = oracle.gemm(np.ascontiguousarray(A[rows]), B)
+        assert_bitwise(host(q["C"][torch.as_tensor(rows, device="cuda")]), want, "shared A")
