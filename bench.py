@@ -268,8 +268,11 @@ def run_ours(args, rank, world, local_rank):
     ws_fwd = [None if i in gu else
               detlib.gemm_workspace(*gemm_dims(p), p["transA"], p["transB"], device=dev)
               for i, p in enumerate(fwd)]
-    ws_dw = [detlib.gemm_workspace(*gemm_dims(p), p["transA"], p["transB"], device=dev)
-             for p in dw]
+    # the two weight-gradient GEMMs as one group: each has its own CTAs in one
+    # grid, so the grid's last round is filled from both
+    dw_probs = [dict(A=A, B=B, C=c_dw[i], transA=p["transA"], transB=p["transB"])
+                for i, (p, A, B) in enumerate(g_dw)]
+    ws_dw = detlib.gemm_group_workspace(dw_probs, device=dev)
     x4, gain4 = up(r4["x"]), up(r4["gain"])
     y4 = torch.empty_like(x4)
     inv4 = torch.empty(x4.shape[0], dtype=torch.float32, device=dev)
@@ -398,7 +401,7 @@ def run_ours(args, rank, world, local_rank):
     # the 162M decoder forward: the embedding, 12 blocks as above, the head
     # GEMM (with its transposed copy of the activations), cross-entropy + mean
     decoder_launches = 1 + len(dm_blocks) * block_launches + gemm_n(dm_head_ws) + 2
-    dw_launches = sum(gemm_n(w) for w in ws_dw)
+    dw_launches = detlib.detgemm_group_launches(dw_probs, ws_dw)
     fwd_launches = (sum(gemm_n(w) for i, w in enumerate(ws_fwd) if i not in gu)
                     + detlib.detgemm_group_launches(gu_probs, ws_gu))
     launches_per_step = (1 + fwd_launches + 2 + 2
@@ -433,9 +436,7 @@ def run_ours(args, rank, world, local_rank):
         mark(4)
         detlib.detrmsnorm_bwd_f32(x4, gain4, inv4, dy4, dx=dx4, dgain=dgain4, workspace=ws_rb)
         mark(5)
-        for i, (p, A, B) in enumerate(g_dw):
-            detlib.detgemm_f32(A, B, c_dw[i], transA=p["transA"], transB=p["transB"],
-                               workspace=ws_dw[i])
+        detlib.detgemm_group_f32(dw_probs, workspace=ws_dw)
         mark(6)
         detlib.detshardsum_f32(shards, scale=1.0 / shards.shape[0], out=gsum)
         mark(7)
@@ -652,7 +653,7 @@ def e2e_leg(args, dev, host, gemm_flops):
     outs_dev = [torch.empty(gemm_dims(p)[:2], dtype=torch.float32, device=dev)
                 for p in fwd + dw]
     wss = [detlib.gemm_workspace(*gemm_dims(p), p["transA"], p["transB"], device=dev)
-           for p in fwd + dw]
+           for p in fwd]
     rows4, D4 = r4["x"].shape
     V = r4["logits"].shape[1]
     y4 = torch.empty((rows4, D4), dtype=torch.float32, device=dev)
@@ -680,7 +681,14 @@ def e2e_leg(args, dev, host, gemm_flops):
     ops = []
     names = [p["name"] for p in fwd]
     gu = (names.index("swiglu_gate"), names.index("swiglu_up"))
-    for i, p in enumerate(fwd + dw):
+    nf = len(fwd)
+    dwp = [dict(A=g(p["A"]), B=g(p["B"]), C=outs_dev[nf + j], transA=p["transA"],
+                transB=p["transB"]) for j, p in enumerate(dw)]
+    ws_dwp = detlib.gemm_group_workspace(dwp, device=dev)
+    ops_dw = ([t for p in dw for t in (pin(p["A"]), pin(p["B"]))],
+              lambda: detlib.detgemm_group_f32(dwp, workspace=ws_dwp),
+              [(outs_dev[nf + j], host_outs[nf + j]) for j in range(len(dw))])
+    for i, p in enumerate(fwd):
         if i == gu[1]:
             continue
         if i == gu[0]:
@@ -698,6 +706,7 @@ def e2e_leg(args, dev, host, gemm_flops):
                                                         transA=p["transA"], transB=p["transB"],
                                                         workspace=wss[i]),
                     [(outs_dev[i], host_outs[i])]))
+    ops.append(ops_dw)          # the weight-gradient GEMMs as one group
     n = len(fwd + dw)
     ops.append(([pin(r4["x"]), pin(r4["gain"])],
                 lambda: detlib.detrmsnorm_f32(g(r4["x"]), g(r4["gain"]), float(r4["eps"]), y=y4,

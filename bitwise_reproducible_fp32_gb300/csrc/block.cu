@@ -222,8 +222,8 @@ __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
             const int64_t rn = r + nwarps;
             prefetch_row_l2(s + rn * lds, kept_columns(rn, period, diag, cols) & ~int64_t(3));
         }
-        const int64_t zend =
-            to_chunk ? std::min<int64_t>(cols, ((r % period) / kKChunk + 1) * kKChunk) : cols;
+        const int64_t chunk_end = ((r % period) / kKChunk + 1) * kKChunk;
+        const int64_t zend = to_chunk && chunk_end < cols ? chunk_end : cols;
         zero_masked(pr, nr, zend, lane, vec_p);
         if (nr == 0) continue;     // uniform across the warp
         const int64_t nseg = (nr + 1023) / 1024;

@@ -52,9 +52,9 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
 // after the other); each product's bits are launch_gemm's.
 struct PairPlan {
     int pair;              // 1: one launch for both
-    int split;             // both split K into groups of `group` chunks
+    int split;             // both split K (each under its own plan)
     int shared_transpose;  // both read one transposed copy of their common A
-    int group;
+    int ctas0, grid;       // the grid's CTAs, the first ctas0 on product 0
     GemmPlan p0, p1;       // each product's plan (the pair's when pair == 1)
     size_t ws0_bytes;      // product 1's partials start here in the workspace
     size_t workspace_bytes;   // the pair's workspace

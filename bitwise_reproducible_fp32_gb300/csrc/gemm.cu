@@ -145,9 +145,10 @@ struct KArgs {
     int tri;
     const int *tri_bad;
     // Two independent products in one launch (the GROUP instances): the
-    // kernel's second KArgs describes the other product; the first units0
-    // work units belong to this one, the rest to the other.
-    int units0;
+    // kernel's second KArgs describes the other product; CTAs below ctas0
+    // work on this one, the rest on the other, each set persistent over its
+    // own product's units.
+    int ctas0;
 };
 
 __device__ __forceinline__ int64_t z_offset(int64_t zb_stride, int64_t zh_stride, int z,
@@ -425,8 +426,6 @@ __device__ __forceinline__ void issue_stage(float *st, uint64_t *bar_ptr,
 // the tiles, the smaller operand's blocks), keeping the working set in L2.
 struct Unit {
     int t, m0, n0, kt0, kt1, z;
-    int prob;          // 0, or 1 for the second product of a two-product launch
-    int nkt;           // k-tiles of that product
 };
 
 __device__ __forceinline__ int causal_row_tiles(int mb, int nt) {
@@ -435,22 +434,15 @@ __device__ __forceinline__ int causal_row_tiles(int mb, int nt) {
 
 // BATCH: the kernel instance for batched products (z, causal and triangular
 // modes); the plain instance compiles none of that in.
-template <bool BATCH, bool GROUP>
-__device__ __forceinline__ Unit unit_of(const KArgs &p0, const KArgs &p1, int u, int nkt,
-                                        bool tri_on) {
-    // the product this unit belongs to (a group instance carries two)
-    const bool second = GROUP && u >= p0.units0;
-    const KArgs &p = second ? p1 : p0;
-    if (second) {
-        u -= p0.units0;
-        nkt = (p1.K + BK - 1) / BK;
-    }
+template <bool BATCH>
+__device__ __forceinline__ Unit unit_of(const KArgs &p, int u, int nkt, bool tri_on,
+                                        int ncta) {
     if (BATCH && tri_on) {
         // Triangular products (never split, never causal) differ in work by
         // row tile: units go out in descending work (tri 1: last row tile
         // first; tri 2: first row tile first), and every other full round of
         // the grid runs backwards, so each CTA's units mix long and short.
-        const int G = int(gridDim.x), U = p.mt * p.nt * p.zcount;
+        const int G = ncta, U = p.mt * p.nt * p.zcount;
         const int j = u / G, b = u - j * G;
         const int r = ((j & 1) && (j + 1) * G <= U) ? j * G + (G - 1 - b) : u;
         const int per = p.zcount * p.nt;
@@ -458,8 +450,6 @@ __device__ __forceinline__ Unit unit_of(const KArgs &p0, const KArgs &p1, int u,
         const int mb = p.tri == 1 ? p.mt - 1 - level : level;
         const int nb = rest % p.nt;
         Unit w;
-        w.prob = 0;
-        w.nkt = nkt;
         w.z = rest / p.nt;
         w.t = mb * p.nt + nb;
         w.m0 = mb * BM;
@@ -486,8 +476,6 @@ __device__ __forceinline__ Unit unit_of(const KArgs &p0, const KArgs &p1, int u,
     } else if (p.m_fast) { mb = t % p.mt; nb = t / p.mt; }
     else                 { nb = t % p.nt; mb = t / p.nt; }
     Unit w;
-    w.prob = second;
-    w.nkt = nkt;
     w.t = t;
     w.z = z;
     w.m0 = mb * BM;
@@ -553,12 +541,13 @@ struct Producer {
     Unit u;
 };
 
-// GROUP: the instance for two products in one grid (plain or split, never
-// batched); the other instances compile none of its per-unit selection in.
+// GROUP: the instance for two products in one grid (never batched): a CTA
+// takes its product once, at entry, from its index; the other instances
+// compile none of that in.
 template <bool A_KM, bool B_KM, bool TMA, bool SPLIT, bool BATCH, bool GROUP>
 __global__ void __launch_bounds__(THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ KArgs p,
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA1,
+                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ KArgs p1,
                 const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ KArgs p2) {
     __shared__ Producer prod;
@@ -576,6 +565,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     // complete (a plain launch passes this at once)
     grid_dependency_wait();
 
+    // this CTA's product, and its place among the CTAs of that product
+    const bool second = GROUP && int(blockIdx.x) >= p1.ctas0;
+    const KArgs &p = second ? p2 : p1;
+    const CUtensorMap *tmA = second ? &tmA2 : &tmA1;
+    const CUtensorMap *tmB = second ? &tmB2 : &tmB1;
+    const int cta = second ? int(blockIdx.x) - p1.ctas0 : int(blockIdx.x);
+    const int ncta = !GROUP ? int(gridDim.x) : second ? int(gridDim.x) - p1.ctas0 : p1.ctas0;
+
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int wm = warp >> 2, wn = warp & 3;     // 2 x 4 warps, warp tile WTM x 32
@@ -584,9 +581,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int arow = A_KM ? wm * WTM + lm : wm * WTM + lm * 4;
     const int bcol = B_KM ? wn * 32 + ln : wn * 32 + ln * 4;
 
-    const int nunits = p.live_tiles * p.units_per_tile * p.zcount +
-                       (GROUP ? p2.live_tiles * p2.units_per_tile : 0);
-    const int my_units = (nunits - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);
+    const int nunits = p.live_tiles * p.units_per_tile * p.zcount;
+    const int my_units = (nunits - cta + ncta - 1) / ncta;
     const int nkt = (p.K + BK - 1) / BK;
     const bool tri_on = BATCH && p.tri != 0 && *p.tri_bad == 0;
 
@@ -600,15 +596,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             ar = int(ao / p.lda); ac = int(ao % p.lda);
             br = int(bo / p.ldb); bc = int(bo % p.ldb);
         }
-        const bool second = GROUP && prod.u.prob;
-        issue_stage<A_KM, B_KM>(stages + slot * STAGE_FLOATS, &full[slot],
-                                second ? &tmA2 : &tmA, second ? &tmB2 : &tmB,
+        issue_stage<A_KM, B_KM>(stages + slot * STAGE_FLOATS, &full[slot], tmA, tmB,
                                 prod.u.m0, prod.u.n0, prod.kt, ar, ac, br, bc);
         ++prod.count;
         if (++prod.kt == prod.u.kt1) {
             if (++prod.ui < my_units) {
-                prod.u = unit_of<BATCH, GROUP>(p, p2, blockIdx.x + prod.ui * gridDim.x, nkt,
-                                               tri_on);
+                prod.u = unit_of<BATCH>(p, cta + prod.ui * ncta, nkt, tri_on, ncta);
                 prod.kt = prod.u.kt0;
             } else {
                 prod.more = 0;
@@ -627,7 +620,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             prod.count = 0;
             prod.more = my_units > 0;
             if (prod.more) {
-                prod.u = unit_of<BATCH, GROUP>(p, p2, blockIdx.x, nkt, tri_on);
+                prod.u = unit_of<BATCH>(p, cta, nkt, tri_on, ncta);
                 prod.kt = prod.u.kt0;
             }
             for (int s = 0; s < STAGES && prod.more; ++s) issue_next(s);
@@ -638,8 +631,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int64_t it = 0;            // consumer position in the k-tile sequence
     bool aborted = false;
     for (int ui = 0; ui < my_units && !aborted; ++ui) {
-        const Unit w = unit_of<BATCH, GROUP>(p, p2, blockIdx.x + ui * gridDim.x, nkt, tri_on);
-        const KArgs &q = (GROUP && w.prob) ? p2 : p;   // this unit's product
+        const Unit w = unit_of<BATCH>(p, cta + ui * ncta, nkt, tri_on, ncta);
         float acc[TM][TN];
 #pragma unroll
         for (int r = 0; r < TM; ++r)
@@ -657,16 +649,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
                 __syncthreads();   // everyone is done with the previous k-tile
                 load_tile_plain<A_KM, BM>(stages,
-                                          q.A + (BATCH ? z_offset(p.a_zb, p.a_zh, w.z, p.zinner) : 0),
-                                          q.lda, q.M, q.K, w.m0, kt * BK, tid);
+                                          p.A + (BATCH ? z_offset(p.a_zb, p.a_zh, w.z, p.zinner) : 0),
+                                          p.lda, p.M, p.K, w.m0, kt * BK, tid);
                 load_tile_plain<B_KM, BN>(stages + A_FLOATS,
-                                          q.B + (BATCH ? z_offset(p.b_zb, p.b_zh, w.z, p.zinner) : 0),
-                                          q.ldb,
-                                          q.N, q.K, w.n0, kt * BK, tid);
+                                          p.B + (BATCH ? z_offset(p.b_zb, p.b_zh, w.z, p.zinner) : 0),
+                                          p.ldb,
+                                          p.N, p.K, w.n0, kt * BK, tid);
                 __syncthreads();
             }
             if (ok) {
-                const int kcount = min(BK, q.K - kt * BK);
+                const int kcount = min(BK, p.K - kt * BK);
                 if (kcount == BK) {
 #pragma unroll 1
                     for (int q = 0; q < BK / 4; ++q)
@@ -677,7 +669,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // the unit's last k-tile; a batched tile's chunks run from w.kt0 (0
             // unless skipped) to w.kt1 (nkt unless skipped)
-            const bool last = (SPLIT || !BATCH) ? (kt == w.nkt - 1) : (kt == w.kt1 - 1);
+            const bool last = (SPLIT || !BATCH) ? (kt == nkt - 1) : (kt == w.kt1 - 1);
             const int first_chunk = (SPLIT || !BATCH) ? 0 : w.kt0 / TILES_PER_CHUNK;
             if (((kt + 1) % TILES_PER_CHUNK == 0) || last) {
                 const int chunk = kt / TILES_PER_CHUNK;
@@ -685,7 +677,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // split: every chunk partial goes to the workspace
                     if (ok) {
                         // one base address; the quads sit at constant offsets
-                        float4 *wb = q.W + ws_index(chunk, q.mt * q.nt, w.t, 0, tid);
+                        float4 *wb = p.W + ws_index(chunk, p.mt * p.nt, w.t, 0, tid);
 #pragma unroll
                         for (int r = 0; r < TM; ++r)
 #pragma unroll
@@ -748,10 +740,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         // epilogue (the next unit's loads are already in flight)
         if (!SPLIT)
             store_tile<A_KM, B_KM>(acc,
-                                   q.C + (BATCH ? z_offset(p.c_zb, p.c_zh, w.z, p.zinner) : 0),
-                                   q.ldc,
-                                   q.M, q.N, w.m0, w.n0, arow, bcol,
-                                   q.vec_store, q.accumulate);
+                                   p.C + (BATCH ? z_offset(p.c_zb, p.c_zh, w.z, p.zinner) : 0),
+                                   p.ldc,
+                                   p.M, p.N, w.m0, w.n0, arow, bcol,
+                                   p.vec_store, p.accumulate);
     }
 
     // any warp may have issued the last copies: once every thread is here no
@@ -907,14 +899,14 @@ struct Prepared {
     bool tma, a_km, b_km;
 };
 
-// Launches x alone, or x and y (same layout and staging, plain instances
-// only) in one persistent grid whose first units are x's.
+// Launches x alone, or x and y (same layout, staging and split mode; never
+// batched) in one grid of `grid` CTAs, the first ctas0 of them on x.
 template <bool A_KM, bool B_KM, bool TMA>
-cudaError_t launch_variant(Prepared x, const Prepared *y, cudaStream_t s) {
-    // batched products are never split
+cudaError_t launch_variant(Prepared x, const Prepared *y, int ctas0, int grid, cudaStream_t s) {
     const KArgs &k = x.k;
-    // a two-product launch is never split (gemm_pair_plan)
-    auto kern = y ? gemm_kernel<A_KM, B_KM, TMA, false, false, true>
+    // batched products are never split or grouped
+    auto kern = y ? (k.split ? gemm_kernel<A_KM, B_KM, TMA, true, false, true>
+                             : gemm_kernel<A_KM, B_KM, TMA, false, false, true>)
                 : k.split ? gemm_kernel<A_KM, B_KM, TMA, true, false, false>
                 : (k.zcount > 1 || k.causal || k.tri)
                     ? gemm_kernel<A_KM, B_KM, TMA, false, true, false>
@@ -922,25 +914,30 @@ cudaError_t launch_variant(Prepared x, const Prepared *y, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    int64_t units = int64_t(k.live_tiles) * k.units_per_tile * k.zcount;
-    x.k.units0 = int(units);
-    if (y) units += int64_t(y->k.live_tiles) * y->k.units_per_tile;
+    if (!y) {
+        const int64_t units = int64_t(k.live_tiles) * k.units_per_tile * k.zcount;
+        grid = int(std::min<int64_t>(units, sm_count_current_device()));
+        ctas0 = grid;
+    }
+    x.k.ctas0 = ctas0;
     const Prepared &z = y ? *y : x;
-    const unsigned grid = unsigned(std::min<int64_t>(units, sm_count_current_device()));
-    return launch_dependent(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, s, x.ma, x.mb, x.k,
-                            z.ma, z.mb, z.k);
+    return launch_dependent(kern, dim3(unsigned(grid)), dim3(THREADS), SMEM_BYTES, s, x.ma,
+                            x.mb, x.k, z.ma, z.mb, z.k);
 }
 
 template <bool TMA>
-cudaError_t launch_layout(const Prepared &x, const Prepared *y, cudaStream_t s) {
-    if (x.a_km && x.b_km) return launch_variant<true, true, TMA>(x, y, s);
-    if (x.a_km) return launch_variant<true, false, TMA>(x, y, s);
-    if (x.b_km) return launch_variant<false, true, TMA>(x, y, s);
-    return launch_variant<false, false, TMA>(x, y, s);
+cudaError_t launch_layout(const Prepared &x, const Prepared *y, int ctas0, int grid,
+                          cudaStream_t s) {
+    if (x.a_km && x.b_km) return launch_variant<true, true, TMA>(x, y, ctas0, grid, s);
+    if (x.a_km) return launch_variant<true, false, TMA>(x, y, ctas0, grid, s);
+    if (x.b_km) return launch_variant<false, true, TMA>(x, y, ctas0, grid, s);
+    return launch_variant<false, false, TMA>(x, y, ctas0, grid, s);
 }
 
-cudaError_t launch_prepared(const Prepared &x, const Prepared *y, cudaStream_t s) {
-    return x.tma ? launch_layout<true>(x, y, s) : launch_layout<false>(x, y, s);
+cudaError_t launch_prepared(const Prepared &x, const Prepared *y, cudaStream_t s,
+                            int ctas0 = 0, int grid = 0) {
+    return x.tma ? launch_layout<true>(x, y, ctas0, grid, s)
+                 : launch_layout<false>(x, y, ctas0, grid, s);
 }
 
 }  // namespace
@@ -1071,7 +1068,7 @@ Prepared prepare(const GemmArgs &a, const GemmPlan &pl, void *W) {
     k.live_tiles = k.mt * k.nt;
     k.tri = 0;
     k.tri_bad = nullptr;
-    k.units0 = k.live_tiles * k.units_per_tile;
+    k.ctas0 = 0;
     // op(A) is k-contiguous when A is not transposed; op(B) when B is.
     x.a_km = !a.transA;
     x.b_km = a.transB != 0;
@@ -1197,6 +1194,32 @@ double alone_cost(const GemmArgs &a, const GemmPlan &pl, int sms) {
 }
 }  // namespace
 
+// The CTAs of a two-product grid of `grid` CTAs are split: c0 for the
+// first product's units, the rest for the second's, each set round-robin over
+// its own units. Returns the k-tile steps of the busiest CTA for the best c0
+// near the split that gives each product its share of the work.
+double partition(const std::vector<int> &s0, const std::vector<int> &s1, int sms, int *c0_out,
+                 int *grid_out) {
+    const int64_t n0 = int64_t(s0.size()), n1 = int64_t(s1.size());
+    const int grid = int(std::min<int64_t>(sms, n0 + n1));
+    double w0 = 0.0, w1 = 0.0;
+    for (int v : s0) w0 += v;
+    for (int v : s1) w1 += v;
+    const int mid = int(std::lround(double(grid) * w0 / (w0 + w1)));
+    double best = 1e300;
+    for (int c0 = std::max(1, mid - 8); c0 <= std::min(grid - 1, mid + 8); ++c0) {
+        const int c1 = grid - c0;
+        if (c0 > n0 || c1 > n1) continue;
+        const double b = std::max(busiest_of(s0, c0), busiest_of(s1, c1));
+        if (b < best) {
+            best = b;
+            *c0_out = c0;
+        }
+    }
+    *grid_out = grid;
+    return best;
+}
+
 PairPlan gemm_pair_plan(const GemmArgs &a0, const GemmArgs &a1, int sms) {
     PairPlan pp{};
     pp.pair = 0;
@@ -1205,7 +1228,7 @@ PairPlan gemm_pair_plan(const GemmArgs &a0, const GemmArgs &a1, int sms) {
     pp.separate_bytes = std::max(pp.p0.workspace_bytes, pp.p1.workspace_bytes);
     pp.shared_transpose = 0;
     if (a0.M == 0 || a0.N == 0 || a0.K == 0 || a1.M == 0 || a1.N == 0 || a1.K == 0 ||
-        sms < 1 || (a0.transA != 0) != (a1.transA != 0) ||
+        sms < 2 || (a0.transA != 0) != (a1.transA != 0) ||
         (a0.transB != 0) != (a1.transB != 0))
         return pp;
     const Shape h0 = shape_of(a0), h1 = shape_of(a1);
@@ -1217,18 +1240,19 @@ PairPlan gemm_pair_plan(const GemmArgs &a0, const GemmArgs &a1, int sms) {
               a0.M == a1.M && a0.K == a1.K))
             return pp;
         const double copy = kLaunchS + 8.0 * double(a0.M) * double(a0.K) / kHbmBps;
-        std::vector<int> s0, s1, both;
+        std::vector<int> s0, s1;
         append_units(s0, h0.T, h0.nkt, h0.nchunks, h0.nchunks);
         append_units(s1, h1.T, h1.nkt, h1.nchunks, h1.nchunks);
-        both = s0;
-        both.insert(both.end(), s1.begin(), s1.end());
         const double separate = busiest_of(s0, sms) * kKtStepS + busiest_of(s1, sms) * kKtStepS +
                                 2.0 * (copy + kLaunchS);
-        const double paired = busiest_of(both, sms) * kKtStepS + copy + kLaunchS;
+        int c0 = 1, grid = 2;
+        const double paired = partition(s0, s1, sms, &c0, &grid) * kKtStepS + copy + kLaunchS;
         if (paired < 0.97 * separate) {
             pp.pair = 1;
             pp.split = 0;
             pp.shared_transpose = 1;
+            pp.ctas0 = c0;
+            pp.grid = grid;
             pp.p0 = GemmPlan{};
             pp.p0.units_per_tile = 1;
             pp.p0.kt_per_unit = int(h0.nkt);
@@ -1241,37 +1265,48 @@ PairPlan gemm_pair_plan(const GemmArgs &a0, const GemmArgs &a1, int sms) {
         }
         return pp;
     }
+    // Both unsplit, or both split K into groups of G chunks (one kernel
+    // instance serves the grid; a common, fine G lets the partition balance).
     const double separate = alone_cost(a0, pp.p0, sms) + alone_cost(a1, pp.p1, sms);
     double best = 0.97 * separate;
-    // both unsplit
-    {
-        std::vector<int> steps;
-        append_units(steps, h0.T, h0.nkt, h0.nchunks, h0.nchunks);
-        append_units(steps, h1.T, h1.nkt, h1.nchunks, h1.nchunks);
-        const double c = busiest_of(steps, sms) * kKtStepS + kLaunchS;
+    // G == 0: both unsplit; a few fine group sizes (coarse groups balance
+    // worse, and each candidate costs the host a pass over the units)
+    for (int64_t G : {int64_t(0), int64_t(1), int64_t(2), int64_t(3), int64_t(4)}) {
+        const int64_t g0 = G ? G : h0.nchunks, g1 = G ? G : h1.nchunks;
+        if (G && ((h0.nchunks + G - 1) / G < 2 || (h1.nchunks + G - 1) / G < 2)) continue;
+        std::vector<int> s0, s1;
+        append_units(s0, h0.T, h0.nkt, h0.nchunks, g0);
+        append_units(s1, h1.T, h1.nkt, h1.nchunks, g1);
+        int c0 = 1, grid = 2;
+        double c = partition(s0, s1, sms, &c0, &grid) * kKtStepS + kLaunchS;
+        const double ws = G ? double(h0.nchunks * h0.T + h1.nchunks * h1.T) * BM * BN * 4.0 : 0.0;
+        if (G) c += (2.0 * ws + double(h0.cbytes + h1.cbytes)) / kHbmBps + 2.0 * kLaunchS;
         if (c < best) {
             best = c;
             pp.pair = 1;
-            pp.split = 0;
+            pp.split = G > 0;
+            pp.ctas0 = c0;
+            pp.grid = grid;
+            auto set = [&](GemmPlan &pl, const Shape &h, int64_t g) {
+                pl = GemmPlan{};
+                pl.nchunks = int(h.nchunks);
+                pl.split = G > 0;
+                pl.units_per_tile = int((h.nchunks + g - 1) / g);
+                pl.kt_per_unit = G ? int(g * TILES_PER_CHUNK) : int(h.nkt);
+                pl.workspace_bytes = G ? size_t(h.nchunks * h.T) * BM * BN * 4 : 0;
+            };
+            set(pp.p0, h0, g0);
+            set(pp.p1, h1, g1);
         }
     }
-    // Split pairs are not taken: measured on the weight-gradient pair
-    // (768 x 2304 and 2048 x 768 over 8,192 tokens), the two-product split
-    // instance ran 5% slower than the two launches, its better balance
-    // outweighed by the per-unit product selection in its loop.
-    if (!pp.pair) return pp;
-    auto set = [&](GemmPlan &pl, const Shape &h) {
-        pl = GemmPlan{};
-        pl.nchunks = int(h.nchunks);
-        pl.split = pp.split;
-        pl.units_per_tile = pp.split ? int((h.nchunks + pp.group - 1) / pp.group) : 1;
-        pl.kt_per_unit = pp.split ? pp.group * TILES_PER_CHUNK : int(h.nkt);
-        pl.workspace_bytes = pp.split ? size_t(h.nchunks * h.T) * BM * BN * 4 : 0;
-    };
-    set(pp.p0, h0);
-    set(pp.p1, h1);
-    pp.ws0_bytes = pp.p0.workspace_bytes;
-    pp.workspace_bytes = pp.p0.workspace_bytes + pp.p1.workspace_bytes;
+    if (!pp.pair) {
+        pp.p0 = gemm_plan(a0.M, a0.N, a0.K, sms, !a0.transA);
+        pp.p1 = gemm_plan(a1.M, a1.N, a1.K, sms, !a1.transA);
+        return pp;
+    }
+    // the partials of the second product follow the first's, 256-byte aligned
+    pp.ws0_bytes = (pp.p0.workspace_bytes + 255) / 256 * 256;
+    pp.workspace_bytes = pp.split ? pp.ws0_bytes + pp.p1.workspace_bytes : 0;
     return pp;
 }
 
@@ -1293,7 +1328,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a0, const GemmArgs &a1, void *works
         t0.lda = t1.lda = ldt;
         t0.transA = t1.transA = 1;
         const Prepared x = prepare(t0, pp.p0, nullptr), y = prepare(t1, pp.p1, nullptr);
-        if (x.tma == y.tma) return launch_prepared(x, &y, s);
+        if (x.tma == y.tma) return launch_prepared(x, &y, s, pp.ctas0, pp.grid);
         e = launch_prepared(x, nullptr, s);
         if (e != cudaSuccess) return e;
         return launch_prepared(y, nullptr, s);
@@ -1303,7 +1338,7 @@ cudaError_t launch_gemm_pair(const GemmArgs &a0, const GemmArgs &a1, void *works
         const Prepared y =
             prepare(a1, pp.p1, static_cast<unsigned char *>(workspace) + pp.ws0_bytes);
         if (x.tma == y.tma && x.a_km == y.a_km && x.b_km == y.b_km) {
-            cudaError_t e = launch_prepared(x, &y, s);
+            cudaError_t e = launch_prepared(x, &y, s, pp.ctas0, pp.grid);
             if (e != cudaSuccess || !pp.split) return e;
             e = launch_chunk_sum(x, pp.p0.nchunks, sms, s);
             if (e != cudaSuccess) return e;
@@ -1358,7 +1393,7 @@ cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStre
             live += std::min<int64_t>(k.nt, (int64_t(mb) * BM + BM - 1) / BN + 1);
     }
     k.live_tiles = int(live);
-    k.units0 = k.live_tiles * k.zcount;
+    k.ctas0 = 0;
     const bool off4 = bt.a_zb % 4 == 0 && bt.a_zh % 4 == 0 && bt.b_zb % 4 == 0 &&
                       bt.b_zh % 4 == 0;
     k.vec_store = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && (a.ldc % 4 == 0) &&
