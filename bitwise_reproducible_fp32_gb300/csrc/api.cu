@@ -520,6 +520,8 @@ cudaError_t group_gemm(int64_t M, int64_t N, int64_t K, const HeadOperand &a, in
     bt.causal = causal;
     bt.tri = tri;
     bt.tri_bad = tri_bad;
+    // a head-wide N (P V, dV, dQ, dK) fills the 64-wide tiles
+    if (N <= 64) return n64::launch_gemm_batched(g, bt, s);
     return launch_gemm_batched(g, bt, s);
 }
 
@@ -838,7 +840,9 @@ DET_API det_status det_watchdog_status(int32_t *code, int clear) {
     if (!code) return DET_ERR_INVALID_ARG;
     unsigned int c = 0, c2 = 0;
     cudaError_t e = gemm_watchdog(&c, clear);
-    unsigned int c3 = 0;
+    unsigned int c3 = 0, c4 = 0;
+    if (e == cudaSuccess) e = n64::gemm_watchdog(&c4, clear);
+    c |= c4;
     if (e == cudaSuccess) e = rowops_watchdog(&c2, clear);
     if (e == cudaSuccess) e = rmsbwd_watchdog(&c3, clear);
     *code = int32_t(c | c2 | c3);

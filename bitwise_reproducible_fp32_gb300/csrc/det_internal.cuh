@@ -87,6 +87,12 @@ cudaError_t launch_count_nonfinite(int64_t rows, int64_t cols, const float *base
                                    int *bad, cudaStream_t s);
 cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s);
 cudaError_t gemm_watchdog(unsigned int *code, int clear);
+// The same batched products with 64-wide CTA tiles (gemm_n64.cu): for N <= 64
+// (a head's width) every warp works on live columns. Same bits.
+namespace n64 {
+cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s);
+cudaError_t gemm_watchdog(unsigned int *code, int clear);
+}  // namespace n64
 cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s);
 
 cudaError_t rowops_watchdog(unsigned int *code, int clear);

@@ -56,7 +56,19 @@
 
 #include "det_internal.cuh"
 
+#ifdef DET_GEMM_SECONDARY_NS
+// A second build of this file (see gemm_n64.cu): its kernels and batched
+// launcher live in their own namespace; the shared helpers, plans and the
+// single-product launchers come from the primary build.
+#define DET_GEMM_PRIMARY 0
+#else
+#define DET_GEMM_PRIMARY 1
+#endif
+
 namespace det {
+#if !DET_GEMM_PRIMARY
+namespace DET_GEMM_SECONDARY_NS {
+#endif
 namespace {
 
 #ifndef DET_GEMM_TM
@@ -65,11 +77,16 @@ namespace {
 #ifndef DET_GEMM_STAGES
 #define DET_GEMM_STAGES 2
 #endif
+#ifndef DET_GEMM_TN
+#define DET_GEMM_TN 8
+#endif
 constexpr int TM = DET_GEMM_TM;                 // outputs a thread: TM x TN
-constexpr int TN = 8;
+constexpr int TN = DET_GEMM_TN;
+static_assert(TN == 4 || TN == 8, "fragment loads take one or two float4 along n");
 constexpr int WTM = 8 * TM;                     // warp tile rows (8 lanes along m)
+constexpr int WTN = 4 * TN;                     // warp tile columns (4 lanes along n)
 constexpr int BM = 2 * WTM;                     // CTA tile rows (op(A) rows)
-constexpr int BN = 128;                         // CTA tile columns
+constexpr int BN = 4 * WTN;                     // CTA tile columns
 constexpr int BK = 32;                          // k-tile
 constexpr int STAGES = DET_GEMM_STAGES;
 static_assert(TM % 4 == 0 && BM <= 256, "TMA box and m/n-contiguous fragment loads");
@@ -197,8 +214,11 @@ __device__ __forceinline__ void mma_group_packed(const float *__restrict__ As,
     for (int kk = 0; kk < 4; ++kk) {
         const float *pb = Bs + (4 * q + kk) * BN + bcol;
         const ulonglong2 lo = *reinterpret_cast<const ulonglong2 *>(pb);
-        const ulonglong2 hi = *reinterpret_cast<const ulonglong2 *>(pb + 16);
-        b[0][kk] = lo.x; b[1][kk] = lo.y; b[2][kk] = hi.x; b[3][kk] = hi.y;
+        b[0][kk] = lo.x; b[1][kk] = lo.y;
+        if (TN == 8) {
+            const ulonglong2 hi = *reinterpret_cast<const ulonglong2 *>(pb + 16);
+            b[TN / 2 - 2][kk] = hi.x; b[TN / 2 - 1][kk] = hi.y;
+        }
     }
     auto row_step = [&](int r, float a, int kk) {
         const f32x2 aa = pack2(a, a);
@@ -257,9 +277,12 @@ __device__ __forceinline__ void mma_group_scalar(const float *__restrict__ As,
         for (int kk = 0; kk < 4; ++kk) {
             const float *pb = Bs + (4 * q + kk) * BN + bcol;
             const float4 lo = *reinterpret_cast<const float4 *>(pb);
-            const float4 hi = *reinterpret_cast<const float4 *>(pb + 16);
             b[0][kk] = lo.x; b[1][kk] = lo.y; b[2][kk] = lo.z; b[3][kk] = lo.w;
-            b[4][kk] = hi.x; b[5][kk] = hi.y; b[6][kk] = hi.z; b[7][kk] = hi.w;
+            if (TN == 8) {
+                const float4 hi = *reinterpret_cast<const float4 *>(pb + 16);
+                b[TN - 4][kk] = hi.x; b[TN - 3][kk] = hi.y; b[TN - 2][kk] = hi.z;
+                b[TN - 1][kk] = hi.w;
+            }
         }
     }
     if (A_KM) {
@@ -317,9 +340,12 @@ __device__ __forceinline__ void mma_group_mpair(const float *__restrict__ As,
         for (int kk = 0; kk < 4; ++kk) {
             const float *pb = Bs + (4 * q + kk) * BN + bcol;
             const float4 lo = *reinterpret_cast<const float4 *>(pb);
-            const float4 hi = *reinterpret_cast<const float4 *>(pb + 16);
             b[0][kk] = lo.x; b[1][kk] = lo.y; b[2][kk] = lo.z; b[3][kk] = lo.w;
-            b[4][kk] = hi.x; b[5][kk] = hi.y; b[6][kk] = hi.z; b[7][kk] = hi.w;
+            if (TN == 8) {
+                const float4 hi = *reinterpret_cast<const float4 *>(pb + 16);
+                b[TN - 4][kk] = hi.x; b[TN - 3][kk] = hi.y; b[TN - 2][kk] = hi.z;
+                b[TN - 1][kk] = hi.w;
+            }
         }
     }
 #pragma unroll
@@ -500,7 +526,7 @@ __device__ __forceinline__ void store_tile(const float (&acc)[TM][TN], float *ba
         float *crow = base + int64_t(i) * ld;
         if (!B_KM && vec) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < TN / 4; ++h) {
                 const int j = n0 + col_of<B_KM>(bcol, 4 * h);
                 if (j + 3 < N) {
                     float4 v = make_float4(acc[r][4 * h], acc[r][4 * h + 1],
@@ -579,7 +605,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int lm = lane >> 2, ln = lane & 3;     // 8 x 4 lanes
 
     const int arow = A_KM ? wm * WTM + lm : wm * WTM + lm * 4;
-    const int bcol = B_KM ? wn * 32 + ln : wn * 32 + ln * 4;
+    const int bcol = B_KM ? wn * WTN + ln : wn * WTN + ln * 4;
 
     const int nunits = p.live_tiles * p.units_per_tile * p.zcount;
     const int my_units = (nunits - cta + ncta - 1) / ncta;
@@ -789,7 +815,7 @@ __global__ void chunk_sum_kernel(KArgs p, int nchunks, int a_km, int b_km) {
         const int wm = warp >> 2, wn = warp & 3, lm = lane >> 2, ln = lane & 3;
         const int r = q / (TN / 4), h = q % (TN / 4);
         const int arow = a_km ? wm * WTM + lm : wm * WTM + lm * 4;
-        const int bcol = b_km ? wn * 32 + ln : wn * 32 + ln * 4;
+        const int bcol = b_km ? wn * WTN + ln : wn * WTN + ln * 4;
         const int i = mb * BM + (a_km ? arow + 8 * r : arow + (r & 3) + (r >> 2) * 32);
         if (i >= p.M) continue;
         float *crow = p.C + int64_t(i) * p.ldc;
@@ -905,12 +931,17 @@ template <bool A_KM, bool B_KM, bool TMA>
 cudaError_t launch_variant(Prepared x, const Prepared *y, int ctas0, int grid, cudaStream_t s) {
     const KArgs &k = x.k;
     // batched products are never split or grouped
+#if DET_GEMM_PRIMARY
     auto kern = y ? (k.split ? gemm_kernel<A_KM, B_KM, TMA, true, false, true>
                              : gemm_kernel<A_KM, B_KM, TMA, false, false, true>)
                 : k.split ? gemm_kernel<A_KM, B_KM, TMA, true, false, false>
                 : (k.zcount > 1 || k.causal || k.tri)
                     ? gemm_kernel<A_KM, B_KM, TMA, false, true, false>
                     : gemm_kernel<A_KM, B_KM, TMA, false, false, false>;
+#else
+    // the second build serves batched products only
+    auto kern = gemm_kernel<A_KM, B_KM, TMA, false, true, false>;
+#endif
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(SMEM_BYTES));
     if (e != cudaSuccess) return e;
@@ -942,6 +973,7 @@ cudaError_t launch_prepared(const Prepared &x, const Prepared *y, cudaStream_t s
 
 }  // namespace
 
+#if DET_GEMM_PRIMARY
 bool make_tensor_map_2d(CUtensorMap *map, const float *base, int64_t inner, int64_t outer,
                         int64_t ld, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
     auto enc = encoder();
@@ -1351,6 +1383,8 @@ cudaError_t launch_gemm_pair(const GemmArgs &a0, const GemmArgs &a1, void *works
     return launch_gemm(a1, workspace, workspace_bytes, s);
 }
 
+#endif  // DET_GEMM_PRIMARY
+
 cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s) {
     if (bt.count == 0 || a.M == 0 || a.N == 0) return cudaSuccess;
     if (a.K == 0) {
@@ -1411,6 +1445,7 @@ cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStre
     return launch_prepared(x, nullptr, s);
 }
 
+#if DET_GEMM_PRIMARY
 // ---------------------------------------------------------------- no-allocation variant
 // Some callers cannot allocate device memory at the moment they multiply: code
 // running inside another framework's memory pool, where every allocation must
@@ -1501,6 +1536,8 @@ cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s
     return launch_gemm(a, scratch, scratch ? kStaticScratchBytes : 0, s);
 }
 
+#endif  // DET_GEMM_PRIMARY
+
 cudaError_t gemm_watchdog(unsigned int *code, int clear) {
     cudaError_t e = cudaMemcpyFromSymbol(code, g_gemm_watchdog, sizeof(unsigned int));
     if (e != cudaSuccess) return e;
@@ -1511,4 +1548,7 @@ cudaError_t gemm_watchdog(unsigned int *code, int clear) {
     return e;
 }
 
+#if !DET_GEMM_PRIMARY
+}  // namespace DET_GEMM_SECONDARY_NS
+#endif
 }  // namespace det
