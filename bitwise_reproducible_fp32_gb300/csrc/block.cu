@@ -124,6 +124,10 @@ __device__ __forceinline__ float butterfly32(float s) {
 // in registers (kSmaxBwdCache) and reads later segments again; the forward
 // reads its row in each pass (see there).
 constexpr int kSmaxMinBlocks = 4;     // the forward: 56 registers a thread
+// The forward stages a row's kept columns in shared memory when they number at
+// most kSmaxStage: a lane's slots are the 16-byte groups it reads in every
+// pass (groups lane, lane + 32, ...), so no pass waits on another lane.
+constexpr int kSmaxStage = 2048;
 constexpr int kSmaxBwdCache = 1;
 constexpr int kSmaxWarps = 8;
 
@@ -194,12 +198,14 @@ __device__ __forceinline__ int64_t kept_columns(int64_t r, int64_t period, int64
 }
 
 // Causal softmax: pass 1 the max of x = s * scale (order free), pass 2 the
-// chains of exp(x - max), pass 3 p = exp(x - max) * (1 / S), the exps formed
-// again (the same bits). Each pass reads the row again: it stays in L1
-// between the passes, and the warp's next row is prefetched into L2. Holding
-// the first 2048 columns in registers instead (128 a thread, two CTAs an SM)
-// measured slower: 416 against 373 us for 48 x 2048 rows of 2048 at 56
-// registers and four CTAs an SM (six or eight CTAs: 399 and 424 us).
+// chains of exp(x - max), pass 3 p = exp(x - max) * (1 / S). A row of at most
+// kSmaxStage kept columns is read from global memory once: pass 1 stores x in
+// the warp's shared-memory slots, pass 2 replaces it by the exps, pass 3
+// scales them. Longer rows read the row again in each pass (it stays in L1
+// between the passes) and form the exps again in pass 3 (the same bits). The
+// warp's next row is prefetched into L2. Holding the first 2048 columns in
+// registers instead (128 a thread, two CTAs an SM) measured slower than the
+// three global passes: 416 against 373 us for 48 x 2048 rows of 2048.
 __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
     softmax_causal_kernel(int64_t rows, int64_t cols, const float *s, int64_t lds, float scale,
                           int64_t diag, int64_t period, float *p, int64_t ldp, int vec_s,
@@ -211,6 +217,8 @@ __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
     // that reads P (P V, skipping the +0 chunks past a row block when V is
     // finite, which *chunk_zeros == 0 says) reads no column beyond it.
     const bool to_chunk = chunk_zeros != nullptr && *chunk_zeros == 0;
+    extern __shared__ float4 smax_slots[];
+    float4 *slots = smax_slots + (threadIdx.x >> 5) * (kSmaxStage / 4);
     for (int64_t r = int64_t(blockIdx.x) * kSmaxWarps + (threadIdx.x >> 5); r < rows;
          r += nwarps) {
         const float *sr = s + r * lds;
@@ -226,6 +234,56 @@ __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
         const int64_t zend = to_chunk && chunk_end < cols ? chunk_end : cols;
         zero_masked(pr, nr, zend, lane, vec_p);
         if (nr == 0) continue;     // uniform across the warp
+        if (vec_s && nr <= kSmaxStage) {
+            // staged: one read of the row; lane l owns groups l + 32 i
+            const int ng = int((nr + 3) / 4);
+            float m = __fmul_rn(sr[0], scale);
+            for (int g = lane; g < ng; g += 32) {
+                float4 v = ld4_kept(sr, 4 * int64_t(g), nr, true);
+                v.x = __fmul_rn(v.x, scale); v.y = __fmul_rn(v.y, scale);
+                v.z = __fmul_rn(v.z, scale); v.w = __fmul_rn(v.w, scale);
+                slots[g] = v;
+                const int j = 4 * g;
+                if (j < nr) m = max_nan2(m, v.x);
+                if (j + 1 < nr) m = max_nan2(m, v.y);
+                if (j + 2 < nr) m = max_nan2(m, v.z);
+                if (j + 3 < nr) m = max_nan2(m, v.w);
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                m = max_nan2(m, __shfl_xor_sync(0xffffffffu, m, off));
+            const bool finite = fabsf(m) <= 0x1.fffffep127f;
+            float c[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) c[w] = 0.0f;
+            // chain lane + 32 w adds groups lane + 32 w + 256 sg, sg ascending
+            for (int sg = 0; 256 * sg < ng; ++sg)
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const int g = lane + 32 * w + 256 * sg;
+                    if (g >= ng) continue;
+                    const float4 v = slots[g];
+                    const float4 e = finite ? exp4(v, m)
+                                            : make_float4(det_exp_call(__fsub_rn(v.x, m)),
+                                                          det_exp_call(__fsub_rn(v.y, m)),
+                                                          det_exp_call(__fsub_rn(v.z, m)),
+                                                          det_exp_call(__fsub_rn(v.w, m)));
+                    slots[g] = e;
+                    const int j = 4 * g;
+                    if (j < nr) c[w] = __fadd_rn(c[w], e.x);
+                    if (j + 1 < nr) c[w] = __fadd_rn(c[w], e.y);
+                    if (j + 2 < nr) c[w] = __fadd_rn(c[w], e.z);
+                    if (j + 3 < nr) c[w] = __fadd_rn(c[w], e.w);
+                }
+            const float inv = __fdiv_rn(1.0f, fold_chains(c));
+            for (int g = lane; g < ng; g += 32) {
+                const float4 e = slots[g];
+                st4_kept(pr, 4 * int64_t(g), nr, vec_p,
+                         make_float4(__fmul_rn(e.x, inv), __fmul_rn(e.y, inv),
+                                     __fmul_rn(e.z, inv), __fmul_rn(e.w, inv)));
+            }
+            continue;
+        }
         const int64_t nseg = (nr + 1023) / 1024;
         auto scaled = [&](int64_t j) {
             float4 v = ld4_kept(sr, j, nr, vec_s);
@@ -507,7 +565,11 @@ cudaError_t launch_softmax_causal(int64_t rows, int64_t cols, const float *sc, i
     const int64_t blocks = std::min<int64_t>((rows + kSmaxWarps - 1) / kSmaxWarps,
                                              int64_t(sm_count_current_device()) * 16);
     const int vec_s = al16(sc) && lds % 4 == 0, vec_p = al16(p) && ldp % 4 == 0;
-    softmax_causal_kernel<<<unsigned(blocks), 32 * kSmaxWarps, 0, s>>>(
+    const size_t smem = size_t(kSmaxWarps) * kSmaxStage * 4;
+    const cudaError_t e = cudaFuncSetAttribute(
+        softmax_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    softmax_causal_kernel<<<unsigned(blocks), 32 * kSmaxWarps, smem, s>>>(
         rows, cols, sc, lds, scale, diag, period, p, ldp, vec_s, vec_p, chunk_zeros);
     return cudaGetLastError();
 }

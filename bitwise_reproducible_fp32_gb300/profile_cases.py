@@ -6,7 +6,8 @@ profiler can capture a chosen launch (ncu -k ... -s ... -c ...).
 Cases keep the device footprint at a few hundred MB, above the 129 MB L2 so
 DRAM counters mean something:
   lm_head   GEMM 1024 x 50257 x 768, weight [50257, 768] transposed (with its
-            workspace: X is copied transposed first, as in the benchmark)
+            workspace: X is copied transposed first, as in the benchmark);
+            --tokens 8192 gives the benchmark's full size (about 1.9 GB)
   qkv       GEMM 8192 x 2304 x 768 (likewise)
   dw_qkv    GEMM X^T dY, 768 x 2304 over 8192 tokens
   dw_pair   the two weight-gradient GEMMs (768 x 2304 and 2048 x 768 over 8192
@@ -39,6 +40,8 @@ def main(argv=None):
     ap.add_argument("case", choices=["lm_head", "qkv", "dw_qkv", "dw_pair", "gate_up", "xent",
                                     "rmsnorm", "rms_bwd", "shardsum", "adamw", "softmax"])
     ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="rows of the lm_head / qkv cases (defaults 1024 / 8192)")
     a = ap.parse_args(argv)
     build.build()
     detlib.load()
@@ -46,7 +49,8 @@ def main(argv=None):
     up = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
 
     if a.case in ("lm_head", "qkv"):
-        probs = {p["name"]: p for p in inputs.gemm_cfg3(tokens=1024 if a.case == "lm_head" else 8192)}
+        tokens = a.tokens or (1024 if a.case == "lm_head" else 8192)
+        probs = {p["name"]: p for p in inputs.gemm_cfg3(tokens=tokens)}
         p = probs[a.case]
         A, B = up(p["A"]), up(p["B"])
         M = p["A"].shape[0]
