@@ -14,11 +14,13 @@ DRAM counters mean something:
             tokens) as one group, as the benchmark runs them
   gate_up   the gate and up projections of one 8192 x 768 input (768 x 2048
             each) as one group: one transposed copy, one grid
-  xent      cross-entropy 1024 x 50257 with dlogits and mean
+  xent      cross-entropy 1024 x 50257 with dlogits and mean; --tokens 8192
+            gives the benchmark's full size (about 3.3 GB)
   rmsnorm   RMSNorm 8192 x 768
   rms_bwd   RMSNorm backward 8192 x 768 (dx, dgain)
   shardsum  fixed-order sum of 64 shard gradients of 768 x 2304
-  adamw     AdamW over 32 Mi parameters
+  adamw     AdamW over 32 Mi parameters; --params 162147840 gives the 162M
+            model's full size (about 2.6 GB)
   softmax   causal softmax of 48 stacked 2048 x 2048 score matrices (the 162M
             block's attention, 4 x 2048 tokens x 12 heads), in place
 Each run is one warm-up launch followed by R launches (default 2).
@@ -41,7 +43,9 @@ def main(argv=None):
                                     "rmsnorm", "rms_bwd", "shardsum", "adamw", "softmax"])
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--tokens", type=int, default=None,
-                    help="rows of the lm_head / qkv cases (defaults 1024 / 8192)")
+                    help="rows of the lm_head / qkv / xent cases (defaults 1024 / 8192 / 1024)")
+    ap.add_argument("--params", type=int, default=32 * 1024 * 1024,
+                    help="parameters of the adamw case")
     a = ap.parse_args(argv)
     build.build()
     detlib.load()
@@ -83,7 +87,7 @@ def main(argv=None):
         ws = detlib.gemm_group_workspace(probs)
         run = lambda: detlib.detgemm_group_f32(probs, workspace=ws)
     elif a.case in ("xent", "rmsnorm"):
-        r = inputs.rowops_cfg4(rows=1024 if a.case == "xent" else 8192)
+        r = inputs.rowops_cfg4(rows=(a.tokens or 1024) if a.case == "xent" else 8192)
         if a.case == "xent":
             X, L = up(r["logits"]), up(r["labels"])
             D = torch.empty_like(X)
@@ -113,7 +117,7 @@ def main(argv=None):
         S = torch.randn((48 * 2048, 2048), generator=g, device=dev) * 4
         run = lambda: detlib.detsoftmax_causal_f32(S, scale=0.125, period=2048, p=S)
     else:
-        w = inputs.adamw_cfg5(n=32 * 1024 * 1024)
+        w = inputs.adamw_cfg5(n=a.params)
         P, G, M_, V_ = (up(w[k]) for k in ("p", "g", "m", "v"))
         hp = {k: w[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")}
         run = lambda: detlib.detadamw_f32(P, G, M_, V_, **hp)
