@@ -46,10 +46,12 @@ from bitwise_reproducible_fp32_gb300 import inputs  # noqa: E402
 
 METRIC = ("bit-exact fixed-order FP32 GEMM TFLOP/s (% FP32 FMA peak); "
           "reduce/AdamW GB/s")
-WORKLOAD = ("162M-decoder FP32 step: RMSNorm 8192x768, forward GEMMs "
+WORKLOAD = ("162M-decoder FP32 step: RMSNorm 8192x768 (once, then 16 times over distinct "
+            "inputs), forward GEMMs "
             "(8192 tokens; 768x2304, 768x768, 2x 768x2048, 2048x768, LM head "
             "768x50257), softmax cross-entropy 8192x50257 with dlogits and mean, "
-            "RMSNorm backward 8192x768 (dx, dgain), dW GEMMs over 8192 tokens "
+            "RMSNorm backward 8192x768 (dx, dgain; once, then 8 times over distinct inputs), "
+            "dW GEMMs over 8192 tokens "
             "(768x2304, 2048x768), fixed-order sum of 64 shard gradients of the "
             "768x2304 weight, one decoder block forward (4x2048 tokens, RoPE, causal "
             "attention 12x64, SwiGLU), one byte-level LM training step (16x128 tokens, "
@@ -85,6 +87,17 @@ def gemm_dims(p):
     K = A.shape[0] if p["transA"] else A.shape[1]
     N = B.shape[0] if p["transB"] else B.shape[1]
     return M, N, K
+
+
+# launches of the RMSNorm forward and backward rows timed back to back
+RMS_RUN = 16
+RMSB_RUN = 8
+
+
+def hbm_row(nbytes, seconds, hbm, **extra):
+    """Rate of an HBM-bound row: algorithmic bytes over seconds a launch."""
+    return {"gbs": nbytes / seconds / 1e9, "frac_hbm": nbytes / seconds / 1e9 / hbm,
+            "ms": seconds * 1e3, **extra}
 
 
 def bytes_rmsnorm(rows, D):
@@ -286,6 +299,14 @@ def run_ours(args, rank, world, local_rank):
     dgain4 = torch.empty(x4.shape[1], dtype=torch.float32, device=dev)
     ws_rb = torch.empty((detlib.detrmsnorm_bwd_workspace_bytes(*x4.shape) + 3) // 4,
                         dtype=torch.float32, device=dev)
+    # RMSNorm runs 12 us and its backward 25 us: besides one launch each, the
+    # step times a run of launches over distinct copies of the inputs (805 MB
+    # and 604 MB in all, several times the L2), so every launch reads from
+    # HBM and the per-launch time is the run's time over its launches
+    rms_runs = [(x4.clone(), torch.empty_like(x4), torch.empty_like(inv4))
+                for _ in range(RMS_RUN)]
+    rmsb_runs = [(x4.clone(), dy4.clone(), torch.empty_like(dx4), torch.empty_like(dgain4))
+                 for _ in range(RMSB_RUN)]
     shards = up(sg)
     gsum = torch.empty(sg.shape[1], dtype=torch.float32, device=dev)
     from bitwise_reproducible_fp32_gb300 import block as blockmod
@@ -404,20 +425,27 @@ def run_ours(args, rank, world, local_rank):
     dw_launches = detlib.detgemm_group_launches(dw_probs, ws_dw)
     fwd_launches = (sum(gemm_n(w) for i, w in enumerate(ws_fwd) if i not in gu)
                     + detlib.detgemm_group_launches(gu_probs, ws_gu))
-    launches_per_step = (1 + fwd_launches + 2 + 2
+    launches_per_step = (1 + RMS_RUN + fwd_launches + 2 + 2 * (1 + RMSB_RUN)
                          + dw_launches + 1 + block_launches
                          + byte_lm_launches + decoder_launches + 1)
 
-    segs = ["rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "rmsnorm_bwd", "gemm_dw",
-            "shard_sum", "block_fwd", "byte_lm_step", "forward_162m", "adamw"]
+    segs = ["rmsnorm_1", "rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "rmsnorm_bwd_1",
+            "rmsnorm_bwd", "gemm_dw", "shard_sum", "block_fwd", "byte_lm_step", "forward_162m",
+            "adamw"]
 
     def step(ev=None):
-        def mark(i):
+        marks = iter(range(len(segs) + 1))
+
+        def mark():
+            i = next(marks)
             if ev is not None:
                 ev[i].record()
-        mark(0)
+        mark()
         detlib.detrmsnorm_f32(x4, gain4, float(r4["eps"]), y=y4, inv_rms=inv4)
-        mark(1)
+        mark()
+        for xr, yr, ir in rms_runs:
+            detlib.detrmsnorm_f32(xr, gain4, float(r4["eps"]), y=yr, inv_rms=ir)
+        mark()
         for i, (p, A, B) in enumerate(g_fwd):
             if i == lm_idx or i == gu[1]:
                 continue
@@ -426,28 +454,31 @@ def run_ours(args, rank, world, local_rank):
                 continue
             detlib.detgemm_f32(A, B, c_fwd[i], transA=p["transA"], transB=p["transB"],
                                workspace=ws_fwd[i])
-        mark(2)
+        mark()
         p, A, B = g_fwd[lm_idx]
         detlib.detgemm_f32(A, B, c_fwd[lm_idx], transA=p["transA"], transB=p["transB"],
                            workspace=ws_fwd[lm_idx])
-        mark(3)
+        mark()
         detlib.detxent_f32(logits, labels, loss=loss, loss_mean=lmean, dlogits=dlog,
                            dscale=1.0 / rows4, dev_status=status)
-        mark(4)
+        mark()
         detlib.detrmsnorm_bwd_f32(x4, gain4, inv4, dy4, dx=dx4, dgain=dgain4, workspace=ws_rb)
-        mark(5)
+        mark()
+        for xr, dyr, dxr, dgr in rmsb_runs:
+            detlib.detrmsnorm_bwd_f32(xr, gain4, inv4, dyr, dx=dxr, dgain=dgr, workspace=ws_rb)
+        mark()
         detlib.detgemm_group_f32(dw_probs, workspace=ws_dw)
-        mark(6)
+        mark()
         detlib.detshardsum_f32(shards, scale=1.0 / shards.shape[0], out=gsum)
-        mark(7)
+        mark()
         blk.forward(bx, bw)
-        mark(8)
+        mark()
         bl_graph.replay()
-        mark(9)
+        mark()
         byte_lm.forward(dmd, dev, blocks=dm_blocks, head_ws=dm_head_ws)
-        mark(10)
+        mark()
         detlib.detadamw_f32(P, G, Mm, Vv, **hp)
-        mark(11)
+        mark()
 
     import torch.distributed as dist
     distributed = world > 1
@@ -521,12 +552,13 @@ def run_ours(args, rank, world, local_rank):
                                "ms": per("gemm_fwd_other") * 1e3},
             "gemm_dw": {"tflops": sum(gemm_flops_dw) / per("gemm_dw") / 1e12,
                         "ms": per("gemm_dw") * 1e3},
-            "rmsnorm": {"gbs": bytes_rmsnorm(rows4, D4) / per("rmsnorm") / 1e9,
-                        "frac_hbm": bytes_rmsnorm(rows4, D4) / per("rmsnorm") / 1e9 / hbm,
-                        "ms": per("rmsnorm") * 1e3},
-            "rmsnorm_bwd": {"gbs": bytes_rmsnorm_bwd(rows4, D4) / per("rmsnorm_bwd") / 1e9,
-                            "frac_hbm": bytes_rmsnorm_bwd(rows4, D4) / per("rmsnorm_bwd") / 1e9 / hbm,
-                            "ms": per("rmsnorm_bwd") * 1e3},
+            "rmsnorm": hbm_row(bytes_rmsnorm(rows4, D4), per("rmsnorm") / RMS_RUN, hbm,
+                               launches=RMS_RUN,
+                               one_launch=hbm_row(bytes_rmsnorm(rows4, D4), per("rmsnorm_1"), hbm)),
+            "rmsnorm_bwd": hbm_row(bytes_rmsnorm_bwd(rows4, D4), per("rmsnorm_bwd") / RMSB_RUN, hbm,
+                                   launches=RMSB_RUN,
+                                   one_launch=hbm_row(bytes_rmsnorm_bwd(rows4, D4),
+                                                      per("rmsnorm_bwd_1"), hbm)),
             "block_fwd": {"tflops": blk.flops() / per("block_fwd") / 1e12,
                           "frac_fp32_peak": blk.flops() / per("block_fwd") / 1e12 / fma_peak,
                           "ms": per("block_fwd") * 1e3},
@@ -576,11 +608,17 @@ def run_ours(args, rank, world, local_rank):
                 "rmsnorm": {"bound": "hbm", "achieved": round(ops["rmsnorm"]["gbs"], 1),
                             "peak": hbm, "unit": "GB/s",
                             "frac": round(ops["rmsnorm"]["frac_hbm"], 4),
-                            "traffic": traffic.get("rmsnorm")},
+                            "traffic": traffic.get("rmsnorm"),
+                            "timing": f"mean of {RMS_RUN} back-to-back launches over distinct "
+                                      "inputs; one launch alone: "
+                                      f"{ops['rmsnorm']['one_launch']['frac_hbm']:.4f}"},
                 "rmsnorm_bwd": {"bound": "hbm", "achieved": round(ops["rmsnorm_bwd"]["gbs"], 1),
                                 "peak": hbm, "unit": "GB/s",
                                 "frac": round(ops["rmsnorm_bwd"]["frac_hbm"], 4),
-                                "traffic": traffic.get("rmsnorm_bwd")},
+                                "traffic": traffic.get("rmsnorm_bwd"),
+                                "timing": f"mean of {RMSB_RUN} back-to-back launches over "
+                                          "distinct inputs; one launch alone: "
+                                          f"{ops['rmsnorm_bwd']['one_launch']['frac_hbm']:.4f}"},
                 "shard_sum": {"bound": "hbm", "achieved": round(ops["shard_sum"]["gbs"], 1),
                               "peak": hbm, "unit": "GB/s",
                               "frac": round(ops["shard_sum"]["frac_hbm"], 4),

@@ -181,6 +181,15 @@ __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Lets the next programmatic dependent grid on the stream be launched now:
+// its CTAs are placed as resources free up and wait in grid_dependency_wait()
+// until this grid has completed. Called after this grid's own wait, so a
+// dependent that reads its inputs before waiting (the RMSNorm backward's dx
+// kernel) still starts after everything before this grid.
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -80,10 +80,6 @@ namespace {
 #ifndef DET_GEMM_TN
 #define DET_GEMM_TN 8
 #endif
-#ifndef DET_GEMM_QUNROLL
-#define DET_GEMM_QUNROLL 1   // k-groups of a k-tile unrolled together
-#endif
-constexpr int kQUnroll = DET_GEMM_QUNROLL;
 constexpr int TM = DET_GEMM_TM;                 // outputs a thread: TM x TN
 constexpr int TN = DET_GEMM_TN;
 static_assert(TN == 4 || TN == 8, "fragment loads take one or two float4 along n");
@@ -690,7 +686,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (ok) {
                 const int kcount = min(BK, p.K - kt * BK);
                 if (kcount == BK) {
-#pragma unroll (kQUnroll)
+#pragma unroll 1
                     for (int q = 0; q < BK / 4; ++q)
                         mma_group<A_KM, B_KM>(As, Bs, q, arow, bcol, lm, ln, acc);
                 } else {

@@ -85,9 +85,12 @@ __global__ void __launch_bounds__(kCols)
     float *ds = xs + kRing * kBoxFloats;
     float *rs = ds + kRing * kBoxFloats;
     uint64_t *bar = reinterpret_cast<uint64_t *>(rs + kKChunk);
-    // the dx kernel may start now (programmatic dependent launch): it only
-    // waits for this grid where it folds the partials
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // this grid is itself a programmatic dependent: once the previous grid
+    // (the producer of x, dy or inv_rms) is complete, the dx kernel may start
+    // (it reads x and dy at once, and waits for this grid only where it folds
+    // the partials)
+    grid_dependency_wait();
+    allow_dependents();
     const int t = threadIdx.x;
     const int64_t c = int64_t(blockIdx.x) / a.ncb;
     const int64_t j0 = (int64_t(blockIdx.x) % a.ncb) * kCols;
@@ -311,8 +314,9 @@ cudaError_t launch_rmsnorm_bwd(int64_t rows, int64_t D, const float *x, int64_t 
     cudaError_t e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kColsSmem));
     if (e != cudaSuccess) return e;
-    ck<<<unsigned(nchunks * ncb), kCols, kColsSmem, s>>>(mx, md, ca);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_dependent(ck, dim3(unsigned(nchunks * ncb)), dim3(kCols), kColsSmem, s, mx, md,
+                         ca);
+    if (e != cudaSuccess) return e;
 
     // 2. dx, and the left-to-right fold of the partials into dgain
     const RowArgs ra{rows, D, ldx, lddy, lddx, x, gain, inv_rms, dy, dx,

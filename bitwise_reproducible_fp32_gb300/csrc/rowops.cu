@@ -767,6 +767,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int n = int(max(int64_t(0), min(per, rows - r0)));
     const int nblk = (n + kRowsPerSlot - 1) / kRowsPerSlot;
     const uint32_t rb = uint32_t(D) * 4u;
+    // launched as a programmatic dependent: wait for the previous grid before
+    // any global access, then let the next dependent grid's CTAs be placed as
+    // this one's retire (each of them waits for this grid in turn)
+    grid_dependency_wait();
+    allow_dependents();
     if (threadIdx.x == 0) {
         for (int k = 0; k < S; ++k) {
             mbar_init(smem_u32(&full[k]), 1);
@@ -913,9 +918,8 @@ cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
                                              int(smem));
         if (e != cudaSuccess) return e;
         const int64_t g = std::min<int64_t>(rows, sm_count_current_device());
-        rmsnorm_stream_kernel<<<unsigned(g), kStreamThreads, smem, s>>>(
-            rows, int(D), x, ldx, gain, eps, y, ldy, inv_rms, S);
-        return cudaGetLastError();
+        return launch_dependent(rmsnorm_stream_kernel, dim3(unsigned(g)), dim3(kStreamThreads),
+                                smem, s, rows, int(D), x, ldx, gain, eps, y, ldy, inv_rms, S);
     }
     if (!vec) {
         rmsnorm_kernel<<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms);
