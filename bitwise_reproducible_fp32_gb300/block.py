@@ -49,9 +49,15 @@ class Block:
         self.ws_bwd = {}       # weight-gradient GEMM workspaces, by output shape
 
     def flops(self):
+        """The forward's algorithmic FLOPs: 2 per multiply-add of the six
+        projections, and of the causal attention's two products counted over
+        the kept scores only (query i against keys 0..i: T(T+1)/2 pairs a
+        head, hd multiply-adds each, for Q K^T and again for P V). Work the
+        kernels do on tiles that straddle the diagonal is not counted."""
         n, D, Fd = self.B * self.T, self.D, self.Fd
         gemm = 2 * n * (D * 3 * D + D * D + 2 * D * Fd + Fd * D)
-        attn = 2 * 2 * self.B * self.H * self.T * self.T * self.hd
+        kept = self.T * (self.T + 1) // 2
+        attn = 2 * 2 * self.B * self.H * kept * self.hd
         return gemm + attn
 
     def forward(self, x, w):

@@ -549,6 +549,31 @@ cudaError_t count_nonfinite_heads(int *flags, const HeadOperand *ops, int n, int
     return e;
 }
 
+// The score product S = Q K^T reads Q and K k-contiguous, where the GEMM runs
+// its scalar FFMA loop. Reading Q from a transposed copy of the whole Q block
+// (heads * head_dim rows of batch * seq queries, m-contiguous) it runs the
+// row-pair loop, with the same bits. The copy (one launch, 8 bytes an element
+// of Q) pays for itself once the sequences are long.
+constexpr int64_t kAttnQCopyMinSeq = 512;
+int64_t attn_qt_ld(int64_t batch, int64_t seq) { return (batch * seq + 3) / 4 * 4; }
+size_t attn_qt_bytes(int64_t batch, int64_t seq, int64_t heads, int64_t head_dim) {
+    if (seq < kAttnQCopyMinSeq) return 0;
+    return (size_t(heads * head_dim) * size_t(attn_qt_ld(batch, seq)) * 4 + 255) / 256 * 256;
+}
+// Q of sequences b0.. and heads h0.. as the score product's op(A), read
+// transposed from QT (row = head_dim index, column = query)
+HeadOperand q_from_copy(const float *QT, int64_t ldt, int64_t batch, int64_t seq, int64_t hd,
+                        int64_t b0, int64_t h0, int64_t head_dim) {
+    HeadOperand o;
+    o.base = QT + h0 * head_dim * ldt + b0 * seq;
+    o.ld = ldt;
+    o.rows = hd - h0 * head_dim;
+    o.cols = (batch - b0) * seq;
+    o.zb = seq;
+    o.zh = head_dim * ldt;
+    return o;
+}
+
 bool attention_args_ok(int64_t batch, int64_t seq, int64_t heads, int64_t head_dim) {
     return batch >= 0 && seq >= 1 && seq <= 65536 && heads >= 1 && heads <= 65536 &&
            head_dim >= 1 && head_dim <= 65536 && batch <= kDimMax / seq &&
@@ -562,7 +587,8 @@ DET_API det_status detattention_workspace_bytes(const det_profile_v1 *prof, int6
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
     if (!bytes || !attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
-    *bytes = attention_groups(batch, seq, heads).score_bytes + kAttnFlagBytes;
+    *bytes = attention_groups(batch, seq, heads).score_bytes + kAttnFlagBytes +
+             attn_qt_bytes(batch, seq, heads, head_dim);
     return DET_OK;
 }
 
@@ -579,21 +605,27 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
     if (!qkv || !out || ldqkv < 3 * hd || ldout < hd) return DET_ERR_INVALID_ARG;
     if ((st = check_device()) != DET_OK) return st;
     const AttnGroups g = attention_groups(batch, seq, heads);
-    if (!workspace || workspace_bytes < g.score_bytes + kAttnFlagBytes ||
+    const size_t qt_bytes = attn_qt_bytes(batch, seq, heads, head_dim);
+    if (!workspace || workspace_bytes < g.score_bytes + kAttnFlagBytes + qt_bytes ||
         reinterpret_cast<uintptr_t>(workspace) % 256)
         return DET_ERR_WORKSPACE;
     float *S = static_cast<float *>(workspace);
     int *flags = reinterpret_cast<int *>(static_cast<char *>(workspace) + g.score_bytes);
+    float *QT = qt_bytes ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                     g.score_bytes + kAttnFlagBytes)
+                         : nullptr;
+    const int64_t ldt = attn_qt_ld(batch, seq);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = for_each_group(batch, heads, g, [&](int64_t b0, int64_t nb, int64_t h0,
-                                                              int64_t nh) {
+    auto group = [&](int64_t b0, int64_t nb, int64_t h0, int64_t nh) {
         const int64_t count = nb * nh;
-        const HeadOperand Q = head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, h0 * head_dim, head_dim);
+        const HeadOperand Q =
+            QT ? q_from_copy(QT, ldt, batch, seq, hd, b0, h0, head_dim)
+               : head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, h0 * head_dim, head_dim);
         const HeadOperand K = head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, hd + h0 * head_dim, head_dim);
         const HeadOperand V = head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, 2 * hd + h0 * head_dim, head_dim);
         const HeadOperand P = stacked(S, seq, nh, count);
-        cudaError_t r = group_gemm(seq, seq, head_dim, Q, 0, K, 1, S, seq, P.zb, P.zh, count, nh,
-                                   1, s);
+        cudaError_t r = group_gemm(seq, seq, head_dim, Q, QT ? 1 : 0, K, 1, S, seq, P.zb, P.zh,
+                                   count, nh, 1, s);
         // P is +0 above the diagonal: with a finite V (counted first) P V
         // skips the chunks past each row block, so the softmax writes P's +0
         // columns only up to that block's end
@@ -604,7 +636,10 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
             r = group_gemm(seq, head_dim, seq, P, 0, V, 0, out + b0 * seq * ldout + h0 * head_dim,
                            ldout, seq * ldout, head_dim, count, nh, 0, s, 1, flags);
         return r;
-    });
+    };
+    cudaError_t e = QT ? launch_transpose_copy(qkv, ldqkv, batch * seq, hd, QT, ldt, s)
+                       : cudaSuccess;
+    if (e == cudaSuccess) e = for_each_group(batch, heads, g, group);
     return from_cuda(e);
 }
 

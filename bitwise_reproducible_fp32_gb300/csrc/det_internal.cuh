@@ -87,6 +87,10 @@ cudaError_t launch_count_nonfinite(int64_t rows, int64_t cols, const float *base
                                    int *bad, cudaStream_t s);
 cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s);
 cudaError_t gemm_watchdog(unsigned int *code, int clear);
+// T (K x M, row stride ldt) = A^T for A (M x K, row stride lda): data movement
+// only, the copy the GEMM takes of a k-contiguous A.
+cudaError_t launch_transpose_copy(const float *A, int64_t lda, int64_t M, int64_t K, float *T,
+                                  int64_t ldt, cudaStream_t s);
 // The same batched products with 64-wide CTA tiles (gemm_n64.cu): for N <= 64
 // (a head's width) every warp works on live columns. Same bits.
 namespace n64 {

@@ -1446,6 +1446,12 @@ cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStre
 }
 
 #if DET_GEMM_PRIMARY
+cudaError_t launch_transpose_copy(const float *A, int64_t lda, int64_t M, int64_t K, float *T,
+                                  int64_t ldt, cudaStream_t s) {
+    if (M == 0 || K == 0) return cudaSuccess;
+    return launch_transpose(A, lda, M, K, T, ldt, sm_count_current_device(), s);
+}
+
 // ---------------------------------------------------------------- no-allocation variant
 // Some callers cannot allocate device memory at the moment they multiply: code
 // running inside another framework's memory pool, where every allocation must

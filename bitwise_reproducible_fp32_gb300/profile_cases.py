@@ -23,6 +23,9 @@ DRAM counters mean something:
             model's full size (about 2.6 GB)
   softmax   causal softmax of 48 stacked 2048 x 2048 score matrices (the 162M
             block's attention, 4 x 2048 tokens x 12 heads), in place
+  attention causal attention of 4 x 2048 tokens, 12 heads of 64 (the 162M
+            block's), from a packed QKV activation
+  block     one decoder block forward at 4 x 2048 tokens (the 162M shape)
 Each run is one warm-up launch followed by R launches (default 2).
 """
 from __future__ import annotations
@@ -40,7 +43,8 @@ def main(argv=None):
 
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["lm_head", "qkv", "dw_qkv", "dw_pair", "gate_up", "xent",
-                                    "rmsnorm", "rms_bwd", "shardsum", "adamw", "softmax"])
+                                    "rmsnorm", "rms_bwd", "shardsum", "adamw", "softmax",
+                                    "attention", "block"])
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--tokens", type=int, default=None,
                     help="rows of the lm_head / qkv / xent cases (defaults 1024 / 8192 / 1024)")
@@ -116,6 +120,22 @@ def main(argv=None):
         g = torch.Generator(device=dev).manual_seed(5)
         S = torch.randn((48 * 2048, 2048), generator=g, device=dev) * 4
         run = lambda: detlib.detsoftmax_causal_f32(S, scale=0.125, period=2048, p=S)
+    elif a.case == "attention":
+        g = torch.Generator(device=dev).manual_seed(6)
+        B, T, H, d = 4, 2048, 12, 64
+        qkv = torch.randn((B * T, 3 * H * d), generator=g, device=dev)
+        out = torch.empty((B * T, H * d), dtype=torch.float32, device=dev)
+        ws = torch.empty((detlib.detattention_workspace_bytes(B, T, H, d) + 3) // 4,
+                         dtype=torch.float32, device=dev)
+        run = lambda: detlib.detattention_f32(qkv, B, T, H, d, out=out, workspace=ws)
+    elif a.case == "block":
+        from bitwise_reproducible_fp32_gb300 import block as blockmod
+        bc = inputs.block_cfg()
+        blk = blockmod.Block(bc["batch"], bc["seq"], bc["x"].shape[1], bc["W_gate"].shape[1],
+                             inputs.N_HEADS, dev)
+        x = up(bc["x"])
+        w = {k: up(bc[k]) for k in ("g1", "W_qkv", "W_o", "g2", "W_gate", "W_up", "W_down")}
+        run = lambda: blk.forward(x, w)
     else:
         w = inputs.adamw_cfg5(n=a.params)
         P, G, M_, V_ = (up(w[k]) for k in ("p", "g", "m", "v"))

@@ -472,9 +472,11 @@ det_status detcos_f32(const det_profile_v1 *prof, int64_t n, const float *x, flo
  * of heads x head_dim, row stride ldout >= heads head_dim). The heads run in
  * groups whose seq x seq score buffers share the workspace (at least
  * detattention_workspace_bytes for the same batch, seq, heads and head_dim,
- * 256-byte aligned; at most about 1 GiB plus 256 bytes): each step is one
- * launch over a group, and the score tiles wholly above the diagonal, which
- * the softmax masks, are not computed. P is +0 above the diagonal, so in
+ * 256-byte aligned: about 1 GiB at most, plus 256 bytes, plus, for seq >= 512,
+ * a transposed copy of the Q block, heads head_dim x batch seq floats, from
+ * which the score product reads Q): each step is one launch over a group, and
+ * the score tiles wholly above the diagonal, which the softmax masks, are not
+ * computed. P is +0 above the diagonal, so in
  * O = P V the 256-wide k-chunks past a row block's last row add +0 partials;
  * they are skipped when the group's V is finite (counted on the device
  * first), which leaves every bit unchanged. Each head's bits are those of

@@ -164,6 +164,22 @@ def test_attention_chunks_above_the_diagonal(dev, poison):
         assert np.isnan(out[:550, 3]).all()           # 0 * inf reached every row before it
 
 
+@pytest.mark.parametrize("B,T,H,d", [(2, 512, 2, 64), (1, 777, 3, 32), (2, 513, 2, 16)])
+def test_attention_score_product_from_the_q_copy(dev, B, T, H, d):
+    # From 512 tokens the score product reads Q from a transposed copy of the
+    # Q block (the GEMM's row-pair loop) instead of Q itself: the same bits.
+    # 777 and 513 tokens put the sequences at column offsets that TMA cannot
+    # take (plain loads); head widths of 16 and 32 leave part of a k-tile past
+    # the head's last column.
+    rng = np.random.default_rng(96 + T)
+    qkv = rng.standard_normal((B * T, 3 * H * d)).astype(F)
+    out = host(detlib.detattention_f32(to_dev(qkv), B, T, H, d, scale=0.25))
+    for b in range(B):
+        for h in range(H):
+            want = attention_oracle(qkv, b, h, T, H, d, 0.25)
+            assert_bitwise(out[b * T:(b + 1) * T, h * d:(h + 1) * d], want, f"b={b} h={h}")
+
+
 def test_attention_162m_shape_sampled_heads(dev):
     # 4 sequences of 2048 tokens, 12 heads of 64, scale 1/8: two heads checked
     rng = np.random.default_rng(95)

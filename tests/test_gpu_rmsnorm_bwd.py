@@ -131,6 +131,35 @@ def test_full_size_8192x768(dev):
     assert_bitwise(host(dg2), dg_w, "dgain from the library's inv_rms")
 
 
+def test_dependent_launches_in_a_chain(dev):
+    """Both kernels of the backward launch as programmatic dependents. Here
+    each backward takes the previous one's dx as its dy, they share one
+    workspace, and the last overwrites the first one's x, with nothing
+    synchronised in between: every result must still be the oracle's."""
+    rows, D = 8192, 768
+    x, g, r, dy = case(rows, D, 91, scale_dy=1e-3)
+    w = np.random.default_rng(92).standard_normal((rows, D)).astype(F)
+    xd, gd, rd, dyd, wd = to_dev(x), to_dev(g), to_dev(r), to_dev(dy), to_dev(w)
+    ws = torch.empty((detlib.detrmsnorm_bwd_workspace_bytes(rows, D) + 3) // 4,
+                     dtype=torch.float32, device=xd.device)
+    dxs = [torch.empty_like(xd) for _ in range(3)]
+    dgs = [torch.empty(D, dtype=torch.float32, device=xd.device) for _ in range(4)]
+    src = dyd
+    for dx, dg in zip(dxs, dgs):
+        detlib.detrmsnorm_bwd_f32(xd, gd, rd, src, dx=dx, dgain=dg, workspace=ws)
+        src = dx
+    # the last one writes its dx over x, which every launch before it read
+    detlib.detrmsnorm_bwd_f32(wd, gd, rd, dyd, dx=xd, dgain=dgs[3], workspace=ws)
+    want = dy
+    for dx, dg in zip(dxs, dgs):
+        want, dg_w = oracle.rmsnorm_bwd(x, g, r, want)
+        assert_bitwise(host(dx), want, "dx")
+        assert_bitwise(host(dg), dg_w, "dgain")
+    dx_w, dg_w = oracle.rmsnorm_bwd(w, g, r, dy)
+    assert_bitwise(host(xd), dx_w, "dx over x")
+    assert_bitwise(host(dgs[3]), dg_w, "dgain")
+
+
 def test_repeatable_and_watchdog_clean(dev):
     x, g, r, dy = case(1024, 768, 45, 1e-3)
     ref = run(x, g, r, dy)

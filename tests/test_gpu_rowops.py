@@ -61,6 +61,36 @@ def test_rmsnorm_cfg4_full(dev):
     assert_bitwise(host(inv), inv_want)
 
 
+def test_rmsnorm_dependent_launches_in_a_chain(dev):
+    """RMSNorm launches as a programmatic dependent of the launch before it.
+    Each of these reads what the one before wrote (y1 = RMSNorm(x), y2 =
+    RMSNorm(y1), ...), and the last overwrites the first one's input while
+    nothing is synchronised in between: every result must still be the
+    oracle's, which holds only if each launch waits for the previous grid
+    before it reads or writes."""
+    rows, D = 8192, 768            # the streamed kernel: one CTA an SM
+    rng = np.random.default_rng(77)
+    x = rng.standard_normal((rows, D)).astype(F)
+    g = (1 + 0.02 * rng.standard_normal(D)).astype(F)
+    w = rng.standard_normal((rows, D)).astype(F)
+    xd, gd, wd = to_dev(x), to_dev(g), to_dev(w)
+    ys = [torch.empty_like(xd) for _ in range(4)]
+    invs = [torch.empty(rows, dtype=torch.float32, device=xd.device) for _ in range(5)]
+    src = xd
+    for y, inv in zip(ys, invs):
+        detlib.detrmsnorm_f32(src, gd, 1e-6, y=y, inv_rms=inv)
+        src = y
+    detlib.detrmsnorm_f32(wd, gd, 1e-6, y=xd, inv_rms=invs[4])   # overwrites x
+    want = x
+    for y, inv in zip(ys, invs):
+        want, inv_want = oracle.rmsnorm(want, g, eps=1e-6)
+        assert_bitwise(host(y), want)
+        assert_bitwise(host(inv), inv_want)
+    wy, winv = oracle.rmsnorm(w, g, eps=1e-6)
+    assert_bitwise(host(xd), wy)
+    assert_bitwise(host(invs[4]), winv)
+
+
 # ----------------------------------------------------------------- cross-entropy
 @pytest.mark.parametrize("rows,V", [(1, 1), (3, 2), (5, 5), (4, 255), (7, 1024),
                                     (6, 1025), (3, 50257)])
