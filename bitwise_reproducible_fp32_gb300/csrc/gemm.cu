@@ -701,21 +701,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int chunk = kt / TILES_PER_CHUNK;
                 if (SPLIT) {
                     // split: every chunk partial goes to the workspace
-                    if (ok) {
-                        // one base address; the quads sit at constant offsets
-                        float4 *wb = p.W + ws_index(chunk, p.mt * p.nt, w.t, 0, tid);
+                    // through the thread's own slots of the totals area, so
+                    // the accumulators are free again before the global stores
 #pragma unroll
-                        for (int r = 0; r < TM; ++r)
+                    for (int r = 0; r < TM; ++r)
 #pragma unroll
-                            for (int h = 0; h < TN / 4; ++h)
-                                __stcg(wb + (r * (TN / 4) + h) * THREADS,
-                                       make_float4(acc[r][4 * h], acc[r][4 * h + 1],
-                                                   acc[r][4 * h + 2], acc[r][4 * h + 3]));
-                    }
+                        for (int h = 0; h < TN / 4; ++h)
+                            totals[(r * (TN / 4) + h) * THREADS + tid] =
+                                make_float4(acc[r][4 * h], acc[r][4 * h + 1],
+                                            acc[r][4 * h + 2], acc[r][4 * h + 3]);
 #pragma unroll
                     for (int r = 0; r < TM; ++r)
 #pragma unroll
                         for (int c = 0; c < TN; ++c) acc[r][c] = 0.0f;
+                    if (ok) {
+                        float4 *wb = p.W + ws_index(chunk, p.mt * p.nt, w.t, 0, tid);
+#pragma unroll 4
+                        for (int q4 = 0; q4 < QUADS; ++q4)
+                            __stcg(wb + q4 * THREADS, totals[q4 * THREADS + tid]);
+                    }
                 } else if (!(chunk == first_chunk && last)) {
                     // fold the finished partial into the running total; after the
                     // last chunk acc holds the result
