@@ -80,26 +80,50 @@ namespace {
 #ifndef DET_GEMM_TN
 #define DET_GEMM_TN 8
 #endif
+#ifndef DET_GEMM_WARPS_M
+#define DET_GEMM_WARPS_M 2
+#endif
+#ifndef DET_GEMM_WARPS_N
+#define DET_GEMM_WARPS_N 4
+#endif
+#ifndef DET_GEMM_CTAS_PER_SM
+#define DET_GEMM_CTAS_PER_SM 1
+#endif
+#ifndef DET_GEMM_TMEM
+#define DET_GEMM_TMEM 0
+#endif
 constexpr int TM = DET_GEMM_TM;                 // outputs a thread: TM x TN
 constexpr int TN = DET_GEMM_TN;
 static_assert(TN == 4 || TN == 8, "fragment loads take one or two float4 along n");
 constexpr int WTM = 8 * TM;                     // warp tile rows (8 lanes along m)
 constexpr int WTN = 4 * TN;                     // warp tile columns (4 lanes along n)
-constexpr int BM = 2 * WTM;                     // CTA tile rows (op(A) rows)
-constexpr int BN = 4 * WTN;                     // CTA tile columns
+constexpr int WARPS_M = DET_GEMM_WARPS_M;       // warps of the CTA along m and n
+constexpr int WARPS_N = DET_GEMM_WARPS_N;
+constexpr int BM = WARPS_M * WTM;               // CTA tile rows (op(A) rows)
+constexpr int BN = WARPS_N * WTN;               // CTA tile columns
 constexpr int BK = 32;                          // k-tile
 constexpr int STAGES = DET_GEMM_STAGES;
-static_assert(TM % 4 == 0 && BM <= 256, "TMA box and m/n-contiguous fragment loads");
-constexpr int THREADS = 256;
+static_assert(TM % 4 == 0 && BM <= 256 && BN <= 256, "TMA boxes and fragment loads");
+constexpr int THREADS = 32 * WARPS_M * WARPS_N;
+constexpr int CTAS_PER_SM = DET_GEMM_CTAS_PER_SM;   // resident CTAs the grid counts on
 constexpr int TILES_PER_CHUNK = kKChunk / BK;   // 8
 constexpr int A_FLOATS = BM * BK;               // 8192
 constexpr int B_FLOATS = BN * BK;               // 4096
 constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
-constexpr int TOTAL_FLOAT4 = THREADS * TM * TN / 4;   // running totals
+// The running chunk totals: in shared memory, or (kTmemTotals) in Tensor
+// Memory, where a thread's TM x TN totals fill TM * TN columns of its lane and
+// the warps sharing a lane quarter (warp % 4) take consecutive column blocks.
+constexpr bool kTmemTotals = DET_GEMM_TMEM != 0;
+constexpr int TOTAL_FLOAT4 = kTmemTotals ? 0 : THREADS * TM * TN / 4;
+constexpr uint32_t kTmemCols = uint32_t(TM * TN) * uint32_t((THREADS / 32 + 3) / 4);
+static_assert(!kTmemTotals || ((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols >= 32 &&
+                               kTmemCols * CTAS_PER_SM <= 512),
+              "a TMEM allocation is a power of two of 32..512 columns, all CTAs of an SM fit");
 constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_FLOATS * 4 +
                               size_t(TOTAL_FLOAT4) * 16 + STAGES * 8;
 static_assert(kKChunk % BK == 0, "chunk boundaries must fall on k-tiles");
-static_assert(SMEM_BYTES <= 232448, "fits the 227 KB opt-in shared memory");
+static_assert(SMEM_BYTES <= 232448 && (SMEM_BYTES + 2048) * CTAS_PER_SM <= 233472,
+              "the CTAs of an SM fit its 228 KB of shared memory");
 
 __device__ unsigned int g_gemm_watchdog;
 
@@ -553,6 +577,36 @@ __device__ __forceinline__ void store_tile(const float (&acc)[TM][TN], float *ba
     }
 }
 
+// The chunk fold with the running totals in Tensor Memory: 32 columns a copy.
+// The first chunk's partial is stored as the total; a later one is added to
+// it, total + partial, and after the last chunk the sum is the result (left
+// in acc). Warp-wide: every lane takes part in the same call.
+__device__ __forceinline__ void fold_tmem(float (&acc)[TM][TN], uint32_t taddr, bool first,
+                                          bool last) {
+    static_assert((TM * TN) % 32 == 0, "whole 32-column copies");
+    __syncwarp();
+#pragma unroll
+    for (int g = 0; g < TM * TN / 32; ++g) {
+        uint32_t v[32];
+        if (first) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                v[i] = __float_as_uint(acc[(32 * g + i) / TN][(32 * g + i) % TN]);
+            tmem_st32(taddr + 32u * g, v);
+        } else {
+            tmem_ld32(taddr + 32u * g, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float &a = acc[(32 * g + i) / TN][(32 * g + i) % TN];
+                const float t = __fadd_rn(__uint_as_float(v[i]), a);
+                if (last) a = t;
+                else v[i] = __float_as_uint(t);
+            }
+            if (!last) tmem_st32(taddr + 32u * g, v);
+        }
+    }
+}
+
 // Persistent: CTA b computes tiles b, b + gridDim.x, ... The k-tiles of all its
 // tiles form one sequence through the stage ring, so the loads of the next
 // tile are in flight while the current one finishes and stores.
@@ -571,7 +625,7 @@ struct Producer {
 // takes its product once, at entry, from its index; the other instances
 // compile none of that in.
 template <bool A_KM, bool B_KM, bool TMA, bool SPLIT, bool BATCH, bool GROUP>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ KArgs p1,
                 const __grid_constant__ CUtensorMap tmA2,
@@ -579,6 +633,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     __shared__ Producer prod;
     __shared__ volatile int abort_flag;
     __shared__ int released[STAGES];   // warps done with a stage (last one refills)
+    __shared__ uint32_t tmem_base;     // the CTA's Tensor Memory (kTmemTotals)
+    static_assert(!(SPLIT && kTmemTotals), "split partials pass through the totals area");
+
     extern __shared__ unsigned char smem_raw[];
     float *smem = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -601,11 +658,21 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int wm = warp >> 2, wn = warp & 3;     // 2 x 4 warps, warp tile WTM x 32
+    const int wm = warp / WARPS_N, wn = warp % WARPS_N;   // warp tile WTM x WTN
     const int lm = lane >> 2, ln = lane & 3;     // 8 x 4 lanes
 
     const int arow = A_KM ? wm * WTM + lm : wm * WTM + lm * 4;
     const int bcol = B_KM ? wn * WTN + ln : wn * WTN + ln * 4;
+
+    if (kTmemTotals) {
+        if (warp == 0) tmem_alloc(smem_u32(&tmem_base), kTmemCols);
+        tmem_fence_before_sync();
+        __syncthreads();
+        tmem_fence_after_sync();
+    }
+    const uint32_t tmem_mine = kTmemTotals ? tmem_base + ((uint32_t(warp & 3) * 32u) << 16) +
+                                                 uint32_t(warp >> 2) * uint32_t(TM * TN)
+                                           : 0u;
 
     const int nunits = p.live_tiles * p.units_per_tile * p.zcount;
     const int my_units = (nunits - cta + ncta - 1) / ncta;
@@ -720,7 +787,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int q4 = 0; q4 < QUADS; ++q4)
                             __stcg(wb + q4 * THREADS, totals[q4 * THREADS + tid]);
                     }
-                } else if (!(chunk == first_chunk && last)) {
+                } else if (kTmemTotals && !(chunk == first_chunk && last)) {
+                    // fold the finished partial into the running total (Tensor
+                    // Memory); after the last chunk acc holds the result
+                    fold_tmem(acc, tmem_mine, chunk == first_chunk, last);
+                    if (!last) {
+#pragma unroll
+                        for (int r = 0; r < TM; ++r)
+#pragma unroll
+                            for (int c = 0; c < TN; ++c) acc[r][c] = 0.0f;
+                    }
+                } else if (!kTmemTotals && !(chunk == first_chunk && last)) {
                     // fold the finished partial into the running total; after the
                     // last chunk acc holds the result
 #pragma unroll
@@ -778,7 +855,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     // any warp may have issued the last copies: once every thread is here no
     // more are issued, and thread 0 drains them
+    if (kTmemTotals) tmem_fence_before_sync();
     __syncthreads();
+    if (kTmemTotals) tmem_fence_after_sync();
     if (TMA && abort_flag && tid == 0) {
         // every warp sees the shared abort flag within one k-tile and leaves its
         // loop. Thread 0 records the event and lets the last copy issued on
@@ -787,6 +866,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         atomicOr(&g_gemm_watchdog, kWatchdogGemm);
         for (int64_t t = prod.count > STAGES ? prod.count - STAGES : 0; t < prod.count; ++t)
             (void)mbar_wait_bounded(smem_u32(&full[t % STAGES]), uint32_t(t / STAGES) & 1u);
+    }
+    if (kTmemTotals && warp == 0) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -816,7 +899,7 @@ __global__ void chunk_sum_kernel(KArgs p, int nchunks, int a_km, int b_km) {
         if (p.m_fast) { mb = tile % p.mt; nb = tile / p.mt; }
         else          { nb = tile % p.nt; mb = tile / p.nt; }
         const int warp = tid >> 5, lane = tid & 31;
-        const int wm = warp >> 2, wn = warp & 3, lm = lane >> 2, ln = lane & 3;
+        const int wm = warp / WARPS_N, wn = warp % WARPS_N, lm = lane >> 2, ln = lane & 3;
         const int r = q / (TN / 4), h = q % (TN / 4);
         const int arow = a_km ? wm * WTM + lm : wm * WTM + lm * 4;
         const int bcol = b_km ? wn * WTN + ln : wn * WTN + ln * 4;
@@ -949,9 +1032,15 @@ cudaError_t launch_variant(Prepared x, const Prepared *y, int ctas0, int grid, c
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(SMEM_BYTES));
     if (e != cudaSuccess) return e;
+    if (CTAS_PER_SM > 1) {
+        // the whole unified L1 as shared memory, so the CTAs of an SM fit
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 int(cudaSharedmemCarveoutMaxShared));
+        if (e != cudaSuccess) return e;
+    }
     if (!y) {
         const int64_t units = int64_t(k.live_tiles) * k.units_per_tile * k.zcount;
-        grid = int(std::min<int64_t>(units, sm_count_current_device()));
+        grid = int(std::min<int64_t>(units, int64_t(sm_count_current_device()) * CTAS_PER_SM));
         ctas0 = grid;
     }
     x.k.ctas0 = ctas0;

@@ -3,14 +3,18 @@
 // dV, dQ, dK over 64-wide heads).
 //
 // Same arithmetic and bits as gemm.cu (every output's chunk chains are one
-// thread's accumulator sequence, whatever the tile): only the thread tile
-// changes, 16 x 4 instead of 16 x 8, so a 256 x 64 CTA tile keeps all eight
-// warps on live columns where the 256 x 128 tile would leave half of them
-// computing columns that are thrown away. The narrower tile loads 20 floats
-// from shared memory a k for 64 FMAs (16 x 8: 24 for 128), so it runs closer
-// to the shared-memory limit; three stages of 40 KB fit beside its 64 KB of
-// running totals.
-#define DET_GEMM_TN 4
-#define DET_GEMM_STAGES 3
+// thread's accumulator sequence, whatever the tile): the thread tile stays 16
+// x 8, and a CTA of 2 x 2 warps covers 256 x 64, so every warp works on live
+// columns where the 256 x 128 tile would leave half of them computing columns
+// that are thrown away. Two such CTAs share an SM (eight warps, as one CTA of
+// gemm.cu): their stages (2 x 40 KB each) fill the shared memory, so the
+// running chunk totals (64 KB a CTA) live in Tensor Memory, 128 of its 512
+// columns a CTA.
+#define DET_GEMM_TN 8
+#define DET_GEMM_WARPS_M 2
+#define DET_GEMM_WARPS_N 2
+#define DET_GEMM_CTAS_PER_SM 2
+#define DET_GEMM_STAGES 2
+#define DET_GEMM_TMEM 1
 #define DET_GEMM_SECONDARY_NS n64
 #include "gemm.cu"

@@ -25,6 +25,7 @@ DRAM counters mean something:
             block's attention, 4 x 2048 tokens x 12 heads), in place
   attention causal attention of 4 x 2048 tokens, 12 heads of 64 (the 162M
             block's), from a packed QKV activation
+  attention_bwd  the backward of that attention (S and P again, dP, dV, dS, dQ, dK)
   block     one decoder block forward at 4 x 2048 tokens (the 162M shape)
 Each run is one warm-up launch followed by R launches (default 2).
 """
@@ -44,7 +45,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["lm_head", "qkv", "dw_qkv", "dw_pair", "gate_up", "xent",
                                     "rmsnorm", "rms_bwd", "shardsum", "adamw", "softmax",
-                                    "attention", "block"])
+                                    "attention", "attention_bwd", "block"])
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--tokens", type=int, default=None,
                     help="rows of the lm_head / qkv / xent cases (defaults 1024 / 8192 / 1024)")
@@ -128,6 +129,15 @@ def main(argv=None):
         ws = torch.empty((detlib.detattention_workspace_bytes(B, T, H, d) + 3) // 4,
                          dtype=torch.float32, device=dev)
         run = lambda: detlib.detattention_f32(qkv, B, T, H, d, out=out, workspace=ws)
+    elif a.case == "attention_bwd":
+        g = torch.Generator(device=dev).manual_seed(6)
+        B, T, H, d = 4, 2048, 12, 64
+        qkv = torch.randn((B * T, 3 * H * d), generator=g, device=dev)
+        dout = torch.randn((B * T, H * d), generator=g, device=dev)
+        dqkv = torch.empty_like(qkv)
+        ws = torch.empty((detlib.detattention_bwd_workspace_bytes(B, T, H, d) + 3) // 4,
+                         dtype=torch.float32, device=dev)
+        run = lambda: detlib.detattention_bwd_f32(qkv, dout, B, T, H, d, dqkv=dqkv, workspace=ws)
     elif a.case == "block":
         from bitwise_reproducible_fp32_gb300 import block as blockmod
         bc = inputs.block_cfg()
