@@ -94,6 +94,11 @@ RMS_RUN = 16
 RMSB_RUN = 8
 
 
+# the end-to-end leg's LM head row blocks and AdamW element blocks
+E2E_LM_ROWS = 1024
+E2E_ADAMW_BLOCKS = 8
+
+
 def hbm_row(nbytes, seconds, hbm, **extra):
     """Rate of an HBM-bound row: algorithmic bytes over seconds a launch."""
     return {"gbs": nbytes / seconds / 1e9, "frac_hbm": nbytes / seconds / 1e9 / hbm,
@@ -715,10 +720,16 @@ def e2e_leg(args, dev, host, gemm_flops):
     P, G, M, Vv = (g(aw[k]) for k in ("p", "g", "m", "v"))
     # (inputs, call, outputs) in step order: each op's inputs are copied in on
     # one stream, the op runs on the compute stream once they have landed, and
-    # its outputs are copied out on a third stream while later ops run
+    # its outputs are copied out on a third stream while later ops run. The
+    # host link carries 5.2 GB in and 5.6 GB out, so the order keeps the
+    # device-to-host stream busy from early on: the LM head first, in row
+    # blocks whose outputs drain while the next blocks run; AdamW in element
+    # blocks that run as their state arrives. A row block of a GEMM, and an
+    # element block of AdamW, compute exactly the bits of the whole call.
     ops = []
     names = [p["name"] for p in fwd]
     gu = (names.index("swiglu_gate"), names.index("swiglu_up"))
+    lm = names.index("lm_head")
     nf = len(fwd)
     dwp = [dict(A=g(p["A"]), B=g(p["B"]), C=outs_dev[nf + j], transA=p["transA"],
                 transB=p["transB"]) for j, p in enumerate(dw)]
@@ -726,8 +737,23 @@ def e2e_leg(args, dev, host, gemm_flops):
     ops_dw = ([t for p in dw for t in (pin(p["A"]), pin(p["B"]))],
               lambda: detlib.detgemm_group_f32(dwp, workspace=ws_dwp),
               [(outs_dev[nf + j], host_outs[nf + j]) for j in range(len(dw))])
+    # the LM head by row blocks of E2E_LM_ROWS tokens (one workspace, reused in
+    # stream order)
+    p_lm = fwd[lm]
+    A_lm, B_lm, C_lm, hC_lm = g(p_lm["A"]), g(p_lm["B"]), outs_dev[lm], host_outs[lm]
+    rows_lm = A_lm.shape[0]
+    blk = min(E2E_LM_ROWS, rows_lm)
+    ws_lm = detlib.gemm_workspace(blk, *gemm_dims(p_lm)[1:], p_lm["transA"], p_lm["transB"],
+                                  device=dev)
+    for r0 in range(0, rows_lm, blk):
+        r1 = min(rows_lm, r0 + blk)
+        ops.append(([pin(p_lm["A"]), pin(p_lm["B"])] if r0 == 0 else [],
+                    lambda r0=r0, r1=r1: detlib.detgemm_f32(
+                        A_lm[r0:r1], B_lm, C_lm[r0:r1], transA=p_lm["transA"],
+                        transB=p_lm["transB"], workspace=ws_lm),
+                    [(C_lm[r0:r1], hC_lm[r0:r1])]))
     for i, p in enumerate(fwd):
-        if i == gu[1]:
+        if i == gu[1] or i == lm:
             continue
         if i == gu[0]:
             # the gate and up projections as one group, as in the device-timed step
@@ -744,7 +770,6 @@ def e2e_leg(args, dev, host, gemm_flops):
                                                         transA=p["transA"], transB=p["transB"],
                                                         workspace=wss[i]),
                     [(outs_dev[i], host_outs[i])]))
-    ops.append(ops_dw)          # the weight-gradient GEMMs as one group
     n = len(fwd + dw)
     ops.append(([pin(r4["x"]), pin(r4["gain"])],
                 lambda: detlib.detrmsnorm_f32(g(r4["x"]), g(r4["gain"]), float(r4["eps"]), y=y4,
@@ -754,15 +779,26 @@ def e2e_leg(args, dev, host, gemm_flops):
                 lambda: detlib.detxent_f32(g(r4["logits"]), g(r4["labels"]), loss=loss,
                                            loss_mean=lmean, dlogits=dlog, dscale=1.0 / rows4),
                 [(loss, host_outs[n + 2]), (lmean, host_outs[n + 3]), (dlog, host_outs[n + 4])]))
+    # AdamW by element blocks: each block's p, g, m, v are copied in as views of
+    # the pinned host arrays, and its p, m, v copied out
+    n_p = P.numel()
+    eb = (n_p + E2E_ADAMW_BLOCKS - 1) // E2E_ADAMW_BLOCKS
+    eb = (eb + 255) // 256 * 256
+    host_pgmv = [pin(aw[k])[0] for k in ("p", "g", "m", "v")]
+    for e0 in range(0, n_p, eb):
+        e1 = min(n_p, e0 + eb)
+        ins = [(h[e0:e1], d[e0:e1]) for h, d in zip(host_pgmv, (P, G, M, Vv))]
+        ops.append((ins,
+                    lambda e0=e0, e1=e1: detlib.detadamw_f32(P[e0:e1], G[e0:e1], M[e0:e1],
+                                                             Vv[e0:e1], **hp),
+                    [(d[e0:e1], h[e0:e1]) for d, h in zip((P, M, Vv), pmv_host)]))
     ops.append(([pin(rb["dy"])],
                 lambda: detlib.detrmsnorm_bwd_f32(g(r4["x"]), g(r4["gain"]), inv4, g(rb["dy"]),
                                                   dx=dx4, dgain=dgain4, workspace=ws_rb),
                 [(dx4, host_outs[n + 5]), (dgain4, host_outs[n + 6])]))
+    ops.append(ops_dw)          # the weight-gradient GEMMs as one group
     ops.append(([pin(sg)], lambda: detlib.detshardsum_f32(g(sg), scale=1.0 / sg.shape[0], out=gsum),
                 [(gsum, host_outs[n + 7])]))
-    ops.append(([pin(aw[k]) for k in ("p", "g", "m", "v")],
-                lambda: detlib.detadamw_f32(P, G, M, Vv, **hp),
-                list(zip((P, M, Vv), pmv_host))))
     comp = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
