@@ -368,25 +368,14 @@ def run_ours(args, rank, world, local_rank):
     gemm_flops = sum(gemm_flops_fwd) + sum(gemm_flops_dw)
     lm_idx = [p["name"] for p in fwd].index("lm_head")
     # A GEMM is one launch, plus one where it uses its workspace (the split-K
-    # second pass, or the transposed copy of A); a group reports its own count. Attention is 4 launches a
-    # group of heads forward (with the count of V's non-finite values) and 10
-    # backward (with those of dO, K and Q). Checked against an ncu launch list
-    # of one step.
+    # second pass, or the transposed copy of A); a group, and the attention,
+    # report their own counts. Checked against an ncu launch list of one step.
     def gemm_n(ws):
         return 1 + int(ws is not None)
 
-    def attn_groups_count(batch, seq, heads):
-        per_head, cap = seq * seq * 4, 1 << 30
-        if heads * per_head <= cap:
-            fit = max(1, min(cap // (heads * per_head), (1 << 20) // heads))
-            gb = -(-batch // -(-batch // fit))
-            return -(-batch // gb)
-        fit = max(1, cap // per_head)
-        gh = -(-heads // -(-heads // fit))
-        return batch * -(-heads // gh)
-
     # one block forward: 2 RMSNorms, 5 GEMMs, RoPE, attention, 2 adds, SwiGLU
-    g162 = attn_groups_count(bc["batch"], bc["seq"], inputs.N_HEADS)
+    attn162 = detlib.detattention_launches(bc["batch"], bc["seq"], inputs.N_HEADS,
+                                           bc["x"].shape[1] // inputs.N_HEADS)
     def pair_n(M, N1, N2, K, transA, ws_bytes=None):
         # launches of a two-product group of one shared A (gate/up, or two
         # weight gradients of one input), with the group's own workspace when
@@ -403,7 +392,7 @@ def run_ours(args, rank, world, local_rank):
     gu_blk = pair_n(ntok_blk, bc["W_gate"].shape[1], bc["W_up"].shape[1],
                     bc["x"].shape[1], False)
     block_launches = (2 + sum(gemm_n(blk.ws[k]) for k in ("qkv", "o", "down")) + gu_blk
-                      + 1 + 4 * g162 + 2 + 1)
+                      + 1 + attn162 + 2 + 1)
     # the byte-level LM step: the embedding, 2 forward blocks (11 launches and
     # the attention), the head GEMM, the cross-entropy and its mean, the head's
     # two backward GEMMs, 2 backward blocks (13 launches, 5 weight-gradient
@@ -411,7 +400,10 @@ def run_ours(args, rank, world, local_rank):
     # AdamW launch per parameter tensor (2 + 7 a block); only the
     # weight-gradient GEMMs (K = all tokens) use workspaces
     nb = len(bl["blocks"])
-    gb = attn_groups_count(bl["batch"], bl["seq"], bl["heads"])
+    hd_b = bl["d"] // bl["heads"]
+    attn_b = detlib.detattention_launches(bl["batch"], bl["seq"], bl["heads"], hd_b)
+    attn_b_bwd = detlib.detattention_launches(bl["batch"], bl["seq"], bl["heads"], hd_b,
+                                              backward=True)
     ntok_b, d_b, f_b = bl["batch"] * bl["seq"], bl["d"], bl["dff"]
 
     def dw_n(M, N):
@@ -422,8 +414,8 @@ def run_ours(args, rank, world, local_rank):
     # a forward block: 2 RMSNorms, QKV, out, the gate/up group, down, rotary,
     # 2 adds, SwiGLU and the attention
     blk_fwd = 2 + 3 + pair_n(ntok_b, f_b, f_b, d_b, False) + 1 + 2 + 1
-    byte_lm_launches = (1 + nb * (blk_fwd + 4 * gb) + 1 + 2 + dw_n(bl["vocab"], d_b) + 1
-                        + nb * (13 + blk_dw + 10 * gb) + 1 + 2 + 7 * nb)
+    byte_lm_launches = (1 + nb * (blk_fwd + attn_b) + 1 + 2 + dw_n(bl["vocab"], d_b) + 1
+                        + nb * (13 + blk_dw + attn_b_bwd) + 1 + 2 + 7 * nb)
     # the 162M decoder forward: the embedding, 12 blocks as above, the head
     # GEMM (with its transposed copy of the activations), cross-entropy + mean
     decoder_launches = 1 + len(dm_blocks) * block_launches + gemm_n(dm_head_ws) + 2

@@ -592,6 +592,27 @@ DET_API det_status detattention_workspace_bytes(const det_profile_v1 *prof, int6
     return DET_OK;
 }
 
+DET_API det_status detattention_launches(const det_profile_v1 *prof, int64_t batch,
+                                         int64_t seq, int64_t heads, int64_t head_dim,
+                                         int backward, int64_t *launches) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (!launches || !attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
+    if (batch == 0) {
+        *launches = 0;
+        return DET_OK;
+    }
+    const AttnGroups g = attention_groups(batch, seq, heads);
+    const int64_t groups = ((batch + g.gb - 1) / g.gb) * ((heads + g.gh - 1) / g.gh);
+    // forward: the Q copy (long sequences), then a group's score product, the
+    // count of V's non-finite values, the softmax and P V; backward: S, the
+    // softmax, dP, the counts of dO's, K's and Q's non-finite values, dV, the
+    // softmax backward, dQ and dK
+    *launches = backward ? 10 * groups
+                         : 4 * groups + (attn_qt_bytes(batch, seq, heads, head_dim) ? 1 : 0);
+    return DET_OK;
+}
+
 DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
                                     int64_t heads, int64_t head_dim, const float *qkv,
                                     int64_t ldqkv, float scale, float *out, int64_t ldout,

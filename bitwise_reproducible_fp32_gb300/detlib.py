@@ -100,6 +100,8 @@ SIGNATURES = [
                                 ctypes.c_size_t, _vp]),
     ("detattention_workspace_bytes", _int, [_PROF, _i64, _i64, _i64, _i64,
                                             ctypes.POINTER(ctypes.c_size_t)]),
+    ("detattention_launches", _int, [_PROF, _i64, _i64, _i64, _i64, ctypes.c_int,
+                                     ctypes.POINTER(ctypes.c_int64)]),
     ("detswiglu_bwd_f32", _int, [_PROF, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("detsoftmax_causal_bwd_f32", _int, [_PROF, _i64, _i64, _vp, _vp, _i64, _f, _i64, _i64,
                                          _vp, _i64, _vp]),
@@ -525,6 +527,16 @@ def detattention_workspace_bytes(batch, seq, heads, head_dim, profile=None) -> i
     _check("detattention_workspace_bytes",
            load().detattention_workspace_bytes(_prof(profile), batch, seq, heads, head_dim,
                                                ctypes.byref(n)))
+    return n.value
+
+
+def detattention_launches(batch, seq, heads, head_dim, backward=False, profile=None) -> int:
+    """Kernel launches detattention_f32 (or, backward=True, detattention_bwd_f32)
+    makes for these sizes."""
+    n = ctypes.c_int64()
+    _check("detattention_launches",
+           load().detattention_launches(_prof(profile), batch, seq, heads, head_dim,
+                                        int(bool(backward)), ctypes.byref(n)))
     return n.value
 
 

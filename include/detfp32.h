@@ -491,6 +491,12 @@ det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, int64_t s
 det_status detattention_workspace_bytes(const det_profile_v1 *prof, int64_t batch,
                                         int64_t seq, int64_t heads, int64_t head_dim,
                                         size_t *bytes);
+/* The number of kernels detattention_f32 (backward 0) or detattention_bwd_f32
+ * (backward 1) launches for these sizes, written to *launches (for callers
+ * that count or capture launches). Same argument rules; host-only. */
+det_status detattention_launches(const det_profile_v1 *prof, int64_t batch, int64_t seq,
+                                 int64_t heads, int64_t head_dim, int backward,
+                                 int64_t *launches);
 
 /* ------------------------------------------------------------------ block backward
  * The backward of the block operations, for the byte-level LM's training step
