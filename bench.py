@@ -56,6 +56,7 @@ WORKLOAD = ("162M-decoder FP32 step: RMSNorm 8192x768 (once, then 16 times over 
             "768x2304 weight, one decoder block forward (4x2048 tokens, RoPE, causal "
             "attention 12x64, SwiGLU), one byte-level LM training step (16x128 tokens, "
             "2 blocks of 64), the 12-layer 162M decoder forward with loss (4x2048 "
+            "tokens), the 162M model's training step (forward, backward, AdamW; 4x2048 "
             "tokens), AdamW 162,147,840 params")
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
@@ -338,6 +339,14 @@ def run_ours(args, rank, world, local_rank):
     dm_head_ws = detlib.gemm_workspace(dm_ntok, dm["vocab"], dm["d"], False, True, device=dev)
     dm_flops = (len(dm_blocks) * dm_blocks[0].flops()
                 + inputs.flops_gemm(dm_ntok, dm["vocab"], dm["d"]))
+    # the 162M model's training step at the same size: the forward above, the
+    # backward and AdamW on all 162,147,840 parameters; every product of the
+    # forward has two of the same size in the backward (dX, dW; for the
+    # attention dP, dV and dQ, dK), so 3x the forward's FLOPs (the backward's
+    # recomputation of the scores is not counted)
+    dm_train_ws = byte_lm.head_workspaces(dmd, dev)
+    dm_train_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    dm_train_flops = 3 * dm_flops
     digests = input_digests(workload_arrays(fwd, dw, r4, rb, sg, bc, bl, dm, aw))
     # the byte-level LM step is launch-bound (120 small launches): it runs as
     # a CUDA graph captured once, after an eager warm-up that builds its
@@ -408,6 +417,18 @@ def run_ours(args, rank, world, local_rank):
 
     def dw_n(M, N):
         return 1 + int(detlib.detgemm_workspace_bytes(M, N, ntok_b, True, False) > 0)
+
+    def tb_n(M, N, K):
+        # an input-gradient GEMM (B transposed) with the workspace its plan asks
+        return 1 + int(detlib.detgemm_workspace_bytes(M, N, K, False, True) > 0)
+
+    def bwd_block_n(ntok, d, f, attn_bwd, dw):
+        # a block's backward: SwiGLU's, the 2 RMSNorm backwards (2 kernels
+        # each), 2 adds and the rotary's backward (8); the input gradients
+        # through W_down, W_gate, W_up (accumulating), W_o and W_qkv; the
+        # weight gradients; the attention's backward
+        return (8 + tb_n(ntok, f, d) + 2 * tb_n(ntok, d, f) + tb_n(ntok, d, d)
+                + tb_n(ntok, d, 3 * d) + dw + attn_bwd)
     # W_down's, the W_gate/W_up pair's, W_o's and W_qkv's weight gradients
     blk_dw = (dw_n(f_b, d_b) + pair_n(d_b, f_b, f_b, ntok_b, True) + dw_n(d_b, d_b)
               + dw_n(d_b, 3 * d_b))
@@ -415,20 +436,36 @@ def run_ours(args, rank, world, local_rank):
     # 2 adds, SwiGLU and the attention
     blk_fwd = 2 + 3 + pair_n(ntok_b, f_b, f_b, d_b, False) + 1 + 2 + 1
     byte_lm_launches = (1 + nb * (blk_fwd + attn_b) + 1 + 2 + dw_n(bl["vocab"], d_b) + 1
-                        + nb * (13 + blk_dw + attn_b_bwd) + 1 + 2 + 7 * nb)
+                        + nb * bwd_block_n(ntok_b, d_b, f_b, attn_b_bwd, blk_dw)
+                        + 1 + 2 + 7 * nb)
     # the 162M decoder forward: the embedding, 12 blocks as above, the head
     # GEMM (with its transposed copy of the activations), cross-entropy + mean
     decoder_launches = 1 + len(dm_blocks) * block_launches + gemm_n(dm_head_ws) + 2
+    # its training step: that forward; the head's dW and dX GEMMs; each
+    # block's backward (as above, with its workspaces); the embedding backward;
+    # AdamW per parameter tensor
+    nb_m, d_m, f_m = len(dm_blocks), dm["d"], dm["dff"]
+
+    def dw_m(M, N):
+        return 1 + int(detlib.detgemm_workspace_bytes(M, N, dm_ntok, True, False) > 0)
+    attn_m_bwd = detlib.detattention_launches(dm["batch"], dm["seq"], dm["heads"],
+                                              d_m // dm["heads"], backward=True)
+    blk_dw_m = (dw_m(f_m, d_m) + pair_n(d_m, f_m, f_m, dm_ntok, True) + dw_m(d_m, d_m)
+                + dw_m(d_m, 3 * d_m))
+    train_launches = (decoder_launches + gemm_n(dm_train_ws["head_dw"])
+                      + gemm_n(dm_train_ws["head_dx"])
+                      + nb_m * bwd_block_n(dm_ntok, d_m, f_m, attn_m_bwd, blk_dw_m)
+                      + 1 + 2 + 7 * nb_m)
     dw_launches = detlib.detgemm_group_launches(dw_probs, ws_dw)
     fwd_launches = (sum(gemm_n(w) for i, w in enumerate(ws_fwd) if i not in gu)
                     + detlib.detgemm_group_launches(gu_probs, ws_gu))
     launches_per_step = (1 + RMS_RUN + fwd_launches + 2 + 2 * (1 + RMSB_RUN)
                          + dw_launches + 1 + block_launches
-                         + byte_lm_launches + decoder_launches + 1)
+                         + byte_lm_launches + decoder_launches + train_launches + 1)
 
     segs = ["rmsnorm_1", "rmsnorm", "gemm_fwd_other", "gemm_lm_head", "xent", "rmsnorm_bwd_1",
             "rmsnorm_bwd", "gemm_dw", "shard_sum", "block_fwd", "byte_lm_step", "forward_162m",
-            "adamw"]
+            "train_162m", "adamw"]
 
     def step(ev=None):
         marks = iter(range(len(segs) + 1))
@@ -473,6 +510,9 @@ def run_ours(args, rank, world, local_rank):
         bl_graph.replay()
         mark()
         byte_lm.forward(dmd, dev, blocks=dm_blocks, head_ws=dm_head_ws)
+        mark()
+        byte_lm.train_step(dmd, dev, inputs.BYTE_LM_HP, status=dm_train_status,
+                           blocks=dm_blocks, ws=dm_train_ws)
         mark()
         detlib.detadamw_f32(P, G, Mm, Vv, **hp)
         mark()
@@ -527,6 +567,8 @@ def run_ours(args, rank, world, local_rank):
         raise SystemExit("cross-entropy reported an out-of-range label")
     if int(bl_status.item()) != 0:
         raise SystemExit("the byte-LM step reported an out-of-range token or label")
+    if int(dm_train_status.item()) != 0:
+        raise SystemExit("the 162M training step reported an out-of-range token or label")
     if detlib.det_watchdog_status() != 0:
         raise SystemExit("a bounded device wait gave up during the run")
 
@@ -565,6 +607,10 @@ def run_ours(args, rank, world, local_rank):
                              "tokens_per_s": dm_ntok / per("forward_162m"),
                              "tflops": dm_flops / per("forward_162m") / 1e12,
                              "frac_fp32_peak": dm_flops / per("forward_162m") / 1e12 / fma_peak},
+            "train_162m": {"ms": per("train_162m") * 1e3,
+                           "tokens_per_s": dm_ntok / per("train_162m"),
+                           "tflops": dm_train_flops / per("train_162m") / 1e12,
+                           "frac_fp32_peak": dm_train_flops / per("train_162m") / 1e12 / fma_peak},
             "shard_sum": {"gbs": bytes_shardsum(*sg.shape) / per("shard_sum") / 1e9,
                           "frac_hbm": bytes_shardsum(*sg.shape) / per("shard_sum") / 1e9 / hbm,
                           "ms": per("shard_sum") * 1e3},

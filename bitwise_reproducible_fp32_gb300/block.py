@@ -101,7 +101,17 @@ class Block:
             if (M, N) not in self.ws_bwd:
                 self.ws_bwd[(M, N)] = L.gemm_workspace(M, N, n, True, False, device=dy.device)
             return L.detgemm_f32(A, B, transA=True, workspace=self.ws_bwd[(M, N)])
-        tB = lambda A, B, C=None: L.detgemm_f32(A, B, C, transB=True)          # noqa: E731
+
+        def tB_ws(A, B):
+            # the input gradients: A k-contiguous, so the GEMM reads a
+            # transposed copy of it where its plan takes one
+            M, N, K = A.shape[0], B.shape[0], A.shape[1]
+            key = ("tB", M, N, K)
+            if key not in self.ws_bwd:
+                self.ws_bwd[key] = L.gemm_workspace(M, N, K, False, True, device=dy.device)
+            return self.ws_bwd[key]
+        tB = lambda A, B, C=None: L.detgemm_f32(A, B, C, transB=True,          # noqa: E731
+                                                workspace=tB_ws(A, B))
 
         def tA2(A, B1, B2):
             # two weight gradients of one input, as one group
@@ -118,7 +128,7 @@ class Block:
         g["W_down"] = tA(self.s, dy)
         d_gate, d_up = L.detswiglu_bwd_f32(self.gate, self.up, ds)
         dh2 = tB(d_gate, w["W_gate"])
-        L.detgemm_acc_f32(d_up, w["W_up"], dh2, transB=True)
+        L.detgemm_acc_f32(d_up, w["W_up"], dh2, transB=True, workspace=tB_ws(d_up, w["W_up"]))
         g["W_gate"], g["W_up"] = tA2(self.h2, d_gate, d_up)
         dx1_b, g["g2"] = L.detrmsnorm_bwd_f32(self.x1, w["g2"], self.inv2, dh2)
         dx1 = L.detadd_f32(dy, dx1_b)

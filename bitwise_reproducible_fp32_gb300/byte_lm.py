@@ -14,7 +14,18 @@ from __future__ import annotations
 PARAMS = ("g1", "W_qkv", "W_o", "g2", "W_gate", "W_up", "W_down")
 
 
-def train_step(c, device, hp, status=None):
+def head_workspaces(c, device):
+    """The three head GEMMs' workspaces of a training step (logits = X W^T,
+    dW = dlogits^T X, dX = dlogits W): the transposed copies and split-K
+    partials their plans use (None where a plan uses none)."""
+    from bitwise_reproducible_fp32_gb300 import detlib as L
+    ntok, d, V = c["batch"] * c["seq"], c["d"], c["vocab"]
+    return {"logits": L.gemm_workspace(ntok, V, d, False, True, device=device),
+            "head_dw": L.gemm_workspace(V, d, ntok, True, False, device=device),
+            "head_dx": L.gemm_workspace(ntok, d, V, False, False, device=device)}
+
+
+def train_step(c, device, hp, status=None, blocks=None, ws=None):
     """One training step. c: the byte_lm_cfg2 tensors on the device; hp: AdamW
     hyperparameters (lr, beta1, beta2, eps, weight_decay, step). The moments
     start at zero. Returns the ordered stage dict: the forward's outputs, the
@@ -22,33 +33,43 @@ def train_step(c, device, hp, status=None):
     status: an int32 device word of one element for the out-of-range token and
     label flag; when given, the step issues no host synchronisation (the
     caller reads the word), so it can be captured in a CUDA graph. Without it
-    the step checks the flag itself and raises."""
+    the step checks the flag itself and raises.
+    blocks / ws: prebuilt make_blocks() and head_workspaces() for repeated
+    steps (built here when omitted; the bits are the same either way)."""
     import torch
 
-    from bitwise_reproducible_fp32_gb300 import block, detlib as L
-    B, T, d = c["batch"], c["seq"], c["d"]
-    ntok = B * T
+    from bitwise_reproducible_fp32_gb300 import detlib as L
+    ntok = c["batch"] * c["seq"]
     check = status is None
     if check:
         status = torch.zeros(1, dtype=torch.int32, device=device)
+    if blocks is None:
+        blocks = make_blocks(c, device)
+    if ws is None:
+        ws = {"logits": None, "head_dw": None, "head_dx": None}
     st = {}
     # forward
     x0 = L.detembedding_f32(c["emb"], c["tokens"], dev_status=status)
     st["embedding"] = x0
-    blocks = [block.Block(B, T, d, c["dff"], c["heads"], device) for _ in c["blocks"]]
     xs = [x0]
     for i, (blk, w) in enumerate(zip(blocks, c["blocks"])):
         xs.append(blk.forward(xs[-1], w))
         st[f"block{i}"] = xs[-1]
-    logits = L.detgemm_f32(xs[-1], c["head"], transB=True)
+    logits = L.detgemm_f32(xs[-1], c["head"], transB=True, workspace=ws["logits"])
     st["logits"] = logits
-    loss, mean, dlogits = L.detxent_f32(logits, c["labels"], want_mean=True, want_dlogits=True,
+    # dlogits rows padded to a multiple of 4 floats: the head's two backward
+    # GEMMs read them through TMA, which wants 16-byte row strides
+    vpad = (c["vocab"] + 3) // 4 * 4
+    dl = torch.empty((ntok, vpad), dtype=torch.float32, device=device)[:, :c["vocab"]]
+    loss, mean, dlogits = L.detxent_f32(logits, c["labels"], want_mean=True, dlogits=dl,
                                         dscale=1.0 / ntok, dev_status=status)
     st["loss"], st["loss_mean"], st["dlogits"] = loss, mean, dlogits
     # backward
-    head_ws = L.gemm_workspace(c["vocab"], d, ntok, True, False, device=device)
+    head_ws = ws["head_dw"]
+    if head_ws is None:
+        head_ws = L.gemm_workspace(c["vocab"], c["d"], ntok, True, False, device=device)
     grads = {"head": L.detgemm_f32(dlogits, xs[-1], transA=True, workspace=head_ws)}
-    dx = L.detgemm_f32(dlogits, c["head"])
+    dx = L.detgemm_f32(dlogits, c["head"], workspace=ws["head_dx"])
     for i in reversed(range(len(blocks))):
         dx, g = blocks[i].backward(xs[i], c["blocks"][i], dx)
         for k in PARAMS:

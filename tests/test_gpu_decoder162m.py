@@ -1,12 +1,13 @@
-"""The 162M decoder's forward ("MojoLearn 162M" model card, table "Compared with
-GPT-3 Small": 12 pre-norm blocks of width 768, 12 heads of 64, SwiGLU 2,048, no
-final norm, untied 50,257-id head) through the same composition as the
-byte-level LM: at the full width with two layers and 256 tokens, every stage
-bit-identical to the oracle's composition; at the full size (12 layers, 4 x
-2,048 tokens), two runs give the same bits stage by stage, and the mean loss
-of a random initialisation sits near log(50,257); and at the full size the
-first 256 tokens of the first and last sequence equal, stage by stage, the
-oracle's composition over those tokens."""
+"""The 162M decoder's forward and training step ("MojoLearn 162M" model card,
+table "Compared with GPT-3 Small": 12 pre-norm blocks of width 768, 12 heads of
+64, SwiGLU 2,048, no final norm, untied 50,257-id head) through the same
+composition as the byte-level LM: at the full width with two layers (256
+tokens forward, 512 for the training step), every stage bit-identical to the
+oracle's composition; at the full size (12 layers, 4 x 2,048 tokens), two runs
+of the forward and of the training step give the same bits stage by stage,
+and the mean loss of a random initialisation sits near log(50,257); and at the
+full size the first 256 tokens of the first and last sequence equal, stage by
+stage, the oracle's composition over those tokens."""
 import numpy as np
 import pytest
 
@@ -75,3 +76,41 @@ def test_full_size_forward_sampled_rows_against_the_oracle(dev):
             if name == "loss_mean":      # a mean over every row: not sampled
                 continue
             assert_bitwise(host(got[name][rows]), want[name], f"{name}, sequence {b}")
+
+
+def test_full_width_two_layers_training_step(dev):
+    # The training step (forward, backward, AdamW on every parameter) at the
+    # 162M width with two layers and 512 tokens, through the prebuilt blocks
+    # and head workspaces the benchmark uses (the attention's Q copy, the
+    # head's transposed copy and split weight gradient): every stage, gradient,
+    # parameter and moment bit-identical to the oracle's composition.
+    c = inputs.decoder_162m(layers=2, batch=1, seq=512)
+    cd = upload(c)
+    device = torch.device("cuda")
+    got = byte_lm.train_step(cd, device, inputs.BYTE_LM_HP, blocks=byte_lm.make_blocks(cd, device),
+                             ws=byte_lm.head_workspaces(cd, device))
+    want = oracle_models.byte_lm_step(c, inputs.BYTE_LM_HP)
+    assert list(got) == list(want)
+    for name in want:
+        assert_bitwise(host(got[name]).reshape(want[name].shape), want[name], name)
+
+
+def test_full_size_training_step_is_reproducible(dev):
+    # The benchmarked training step (12 layers, 4 x 2,048 tokens): two steps
+    # from the same state, one through the benchmark's prebuilt blocks and
+    # workspaces and one building its own, give the same bits at every stage.
+    c = inputs.decoder_162m()
+    cd = upload(c)
+    device = torch.device("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    first = byte_lm.train_step(cd, device, inputs.BYTE_LM_HP, status=status,
+                               blocks=byte_lm.make_blocks(cd, device),
+                               ws=byte_lm.head_workspaces(cd, device))
+    first = {k: v.clone() for k, v in first.items()}
+    second = byte_lm.train_step(cd, device, inputs.BYTE_LM_HP)
+    assert int(status.item()) == 0
+    assert list(first) == list(second)
+    for name in first:
+        assert torch.equal(first[name].view(torch.int32), second[name].view(torch.int32)), name
+    mean = float(first["loss_mean"][0])
+    assert abs(mean - np.log(50257.0)) < 0.5, mean
