@@ -379,8 +379,15 @@ def run_ours(args, rank, world, local_rank):
     # A GEMM is one launch, plus one where it uses its workspace (the split-K
     # second pass, or the transposed copy of A); a group, and the attention,
     # report their own counts. Checked against an ncu launch list of one step.
-    def gemm_n(ws):
-        return 1 + int(ws is not None)
+    def gemm_n(M, N, K, transA=False, transB=False, ws=None):
+        # launches of one GEMM with this workspace: the copy of A, the GEMM,
+        # the split pass, as its plan takes them
+        return detlib.detgemm_launches(M, N, K, transA, transB, ws)
+
+    def planned_n(M, N, K, transA, transB):
+        # ... with the workspace its plan asks for
+        return gemm_n(M, N, K, transA, transB,
+                      detlib.detgemm_workspace_bytes(M, N, K, transA, transB))
 
     # one block forward: 2 RMSNorms, 5 GEMMs, RoPE, attention, 2 adds, SwiGLU
     attn162 = detlib.detattention_launches(bc["batch"], bc["seq"], inputs.N_HEADS,
@@ -400,7 +407,10 @@ def run_ours(args, rank, world, local_rank):
     ntok_blk = bc["batch"] * bc["seq"]
     gu_blk = pair_n(ntok_blk, bc["W_gate"].shape[1], bc["W_up"].shape[1],
                     bc["x"].shape[1], False)
-    block_launches = (2 + sum(gemm_n(blk.ws[k]) for k in ("qkv", "o", "down")) + gu_blk
+    d_blk, f_blk = bc["x"].shape[1], bc["W_gate"].shape[1]
+    block_launches = (2 + gemm_n(ntok_blk, 3 * d_blk, d_blk, ws=blk.ws["qkv"])
+                      + gemm_n(ntok_blk, d_blk, d_blk, ws=blk.ws["o"])
+                      + gemm_n(ntok_blk, d_blk, f_blk, ws=blk.ws["down"]) + gu_blk
                       + 1 + attn162 + 2 + 1)
     # the byte-level LM step: the embedding, 2 forward blocks (11 launches and
     # the attention), the head GEMM, the cross-entropy and its mean, the head's
@@ -416,11 +426,11 @@ def run_ours(args, rank, world, local_rank):
     ntok_b, d_b, f_b = bl["batch"] * bl["seq"], bl["d"], bl["dff"]
 
     def dw_n(M, N):
-        return 1 + int(detlib.detgemm_workspace_bytes(M, N, ntok_b, True, False) > 0)
+        return planned_n(M, N, ntok_b, True, False)
 
     def tb_n(M, N, K):
         # an input-gradient GEMM (B transposed) with the workspace its plan asks
-        return 1 + int(detlib.detgemm_workspace_bytes(M, N, K, False, True) > 0)
+        return planned_n(M, N, K, False, True)
 
     def bwd_block_n(ntok, d, f, attn_bwd, dw):
         # a block's backward: SwiGLU's, the 2 RMSNorm backwards (2 kernels
@@ -440,24 +450,27 @@ def run_ours(args, rank, world, local_rank):
                         + 1 + 2 + 7 * nb)
     # the 162M decoder forward: the embedding, 12 blocks as above, the head
     # GEMM (with its transposed copy of the activations), cross-entropy + mean
-    decoder_launches = 1 + len(dm_blocks) * block_launches + gemm_n(dm_head_ws) + 2
+    decoder_launches = (1 + len(dm_blocks) * block_launches
+                        + gemm_n(dm_ntok, dm["vocab"], dm["d"], False, True, dm_head_ws) + 2)
     # its training step: that forward; the head's dW and dX GEMMs; each
     # block's backward (as above, with its workspaces); the embedding backward;
     # AdamW per parameter tensor
     nb_m, d_m, f_m = len(dm_blocks), dm["d"], dm["dff"]
 
     def dw_m(M, N):
-        return 1 + int(detlib.detgemm_workspace_bytes(M, N, dm_ntok, True, False) > 0)
+        return planned_n(M, N, dm_ntok, True, False)
     attn_m_bwd = detlib.detattention_launches(dm["batch"], dm["seq"], dm["heads"],
                                               d_m // dm["heads"], backward=True)
     blk_dw_m = (dw_m(f_m, d_m) + pair_n(d_m, f_m, f_m, dm_ntok, True) + dw_m(d_m, d_m)
                 + dw_m(d_m, 3 * d_m))
-    train_launches = (decoder_launches + gemm_n(dm_train_ws["head_dw"])
-                      + gemm_n(dm_train_ws["head_dx"])
+    train_launches = (decoder_launches
+                      + gemm_n(dm["vocab"], d_m, dm_ntok, True, False, dm_train_ws["head_dw"])
+                      + gemm_n(dm_ntok, d_m, dm["vocab"], False, False, dm_train_ws["head_dx"])
                       + nb_m * bwd_block_n(dm_ntok, d_m, f_m, attn_m_bwd, blk_dw_m)
                       + 1 + 2 + 7 * nb_m)
     dw_launches = detlib.detgemm_group_launches(dw_probs, ws_dw)
-    fwd_launches = (sum(gemm_n(w) for i, w in enumerate(ws_fwd) if i not in gu)
+    fwd_launches = (sum(gemm_n(*gemm_dims(p), p["transA"], p["transB"], ws_fwd[i])
+                        for i, p in enumerate(fwd) if i not in gu)
                     + detlib.detgemm_group_launches(gu_probs, ws_gu))
     launches_per_step = (1 + RMS_RUN + fwd_launches + 2 + 2 * (1 + RMSB_RUN)
                          + dw_launches + 1 + block_launches

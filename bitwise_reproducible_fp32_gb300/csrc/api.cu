@@ -103,7 +103,6 @@ DET_API const char *det_status_string(int status) {
 DET_API det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA,
                                            int transB, int64_t M, int64_t N, int64_t K,
                                            size_t *bytes) {
-    (void)transB;
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
     if (!bytes || M < 0 || N < 0 || K < 0 || M > kDimMax || N > kDimMax || K > kDimMax)
@@ -111,7 +110,25 @@ DET_API det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int trans
     *bytes = 0;
     if (M == 0 || N == 0 || K == 0) return DET_OK;
     if ((st = check_device()) != DET_OK) return st;
-    *bytes = gemm_plan(M, N, K, sm_count_current_device(), transA == 0).workspace_bytes;
+    *bytes = gemm_plan(M, N, K, sm_count_current_device(), transA == 0, transB != 0 ? 1 : 0)
+                 .workspace_bytes;
+    return DET_OK;
+}
+
+DET_API det_status detgemm_launches(const det_profile_v1 *prof, int transA, int transB,
+                                    int64_t M, int64_t N, int64_t K, size_t workspace_bytes,
+                                    int64_t *launches) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (!launches || M < 0 || N < 0 || K < 0 || M > kDimMax || N > kDimMax || K > kDimMax)
+        return DET_ERR_INVALID_ARG;
+    *launches = 0;
+    if (M == 0 || N == 0) return DET_OK;
+    if ((st = check_device()) != DET_OK) return st;
+    GemmArgs a;
+    a.M = M; a.N = N; a.K = K;
+    a.transA = transA != 0; a.transB = transB != 0;
+    *launches = gemm_launches(a, workspace_bytes);
     return DET_OK;
 }
 
@@ -219,7 +236,8 @@ DET_API det_status detgemm_group_workspace_bytes(const det_profile_v1 *prof, int
                                     [&](const GemmArgs &a, const GemmArgs *b) {
         const int sms = sm_count_current_device();
         if (!b) {
-            need = std::max(need, gemm_plan(a.M, a.N, a.K, sms, !a.transA).workspace_bytes);
+            need = std::max(need, gemm_plan(a.M, a.N, a.K, sms, !a.transA, a.transB ? 1 : 0)
+                                      .workspace_bytes);
         } else {
             const PairPlan pp = gemm_pair_plan(a, *b, sms);
             need = std::max(need, pp.pair ? pp.workspace_bytes : pp.separate_bytes);
@@ -237,12 +255,7 @@ DET_API det_status detgemm_group_launches(const det_profile_v1 *prof, int64_t co
     int64_t n = 0;
     const int sms = sm_count_current_device();
     // kernels one product issues alone with this much workspace
-    auto alone = [&](const GemmArgs &a) -> int64_t {
-        if (a.K == 0) return 1;
-        const GemmPlan pl = gemm_plan(a.M, a.N, a.K, sms, !a.transA);
-        const bool ws = workspace_bytes >= pl.workspace_bytes;
-        return 1 + int64_t(ws && (pl.split || pl.transpose_a));
-    };
+    auto alone = [&](const GemmArgs &a) -> int64_t { return gemm_launches(a, workspace_bytes); };
     const det_status st = for_pairs(prof, count, problems,
                                     [&](const GemmArgs &a, const GemmArgs *b) {
         if (!b) {

@@ -42,10 +42,16 @@ struct GemmPlan {
     int kt_per_unit;       // k-tiles a unit computes
     int nchunks;
     int transpose_a;       // 1: op(A) is read from a K x M copy in the workspace
+    size_t copy_bytes;     // the copy's share of the workspace (first)
+    size_t split_bytes;    // the split partials' share (after the copy)
     size_t workspace_bytes;
 };
-// a_kmajor: op(A) is k-contiguous (transA == 0), the layout a copy can help.
-GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor);
+// a_kmajor: op(A) is k-contiguous (transA == 0), the layout a copy can help;
+// b_kmajor: op(B) is k-contiguous (transB != 0), or -1 for a plan that never
+// pairs a split with a copy (the two-product plans).
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor, int b_kmajor = -1);
+// Kernels launch_gemm launches for a with a caller workspace of this size.
+int64_t gemm_launches(const GemmArgs &a, size_t workspace_bytes);
 cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_bytes,
                         cudaStream_t s);
 // Two independent products in one launch where that is faster (else one

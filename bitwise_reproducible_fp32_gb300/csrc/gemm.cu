@@ -1118,9 +1118,11 @@ double busiest_cta_steps(int64_t T, int64_t S, int64_t G, int64_t nkt, int sms) 
 // floats, so the copy's rows are 16-byte aligned for TMA.
 int64_t transposed_ld(int64_t M) { return (M + 3) / 4 * 4; }
 
-GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor) {
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor, int b_kmajor) {
     GemmPlan pl{};
     pl.transpose_a = 0;
+    pl.copy_bytes = 0;
+    pl.split_bytes = 0;
     const int64_t T = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int64_t nkt = (K + BK - 1) / BK;
     const int64_t nchunks = (K + kKChunk - 1) / kKChunk;
@@ -1140,7 +1142,23 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor) {
         const double cost = launch_s + 8.0 * double(M) * double(K) / hbm_bps;
         if (gain > cost) {
             pl.transpose_a = 1;
-            pl.workspace_bytes = size_t(K) * size_t(transposed_ld(M)) * 4;
+            pl.copy_bytes = pl.workspace_bytes = size_t(K) * size_t(transposed_ld(M)) * 4;
+        }
+    };
+    // A split product may read A from a transposed copy too (the copy first in
+    // the workspace, 256-byte rounded, the partials after it): from A itself
+    // it runs the column-pair loop, or the scalar one when B is k-contiguous as
+    // well (b_kmajor 1), ~8% and ~15% slower. Taken where that gain exceeds
+    // the copy; b_kmajor < 0 (the two-product plans) never takes it.
+    auto consider_split_copy = [&] {
+        if (!a_kmajor || b_kmajor < 0) return;
+        const double frac = b_kmajor ? 0.15 : 0.08;
+        const double gain = frac * 2.0 * double(M) * double(N) * double(K) / 48.0e12;
+        const double cost = launch_s + 8.0 * double(M) * double(K) / hbm_bps;
+        if (gain > cost) {
+            pl.transpose_a = 1;
+            pl.copy_bytes = (size_t(K) * size_t(transposed_ld(M)) * 4 + 255) / 256 * 256;
+            pl.workspace_bytes = pl.copy_bytes + pl.split_bytes;
         }
     };
     // enough tiles to fill every SM several times over: splitting cannot pay
@@ -1161,11 +1179,44 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor) {
             pl.split = 1;
             pl.units_per_tile = int(S_eff);
             pl.kt_per_unit = int(G * TILES_PER_CHUNK);
-            pl.workspace_bytes = size_t(ws);
+            pl.split_bytes = pl.workspace_bytes = size_t(ws);
         }
     }
     if (!pl.split) consider_transpose();
+    else consider_split_copy();
     return pl;
+}
+
+// The plan launch_gemm runs with workspace_bytes at ws (16-byte aligned or
+// null): the split keeps its partials and drops the copy when the workspace
+// holds only the partials; with less, one unit a tile and no copy.
+GemmPlan gemm_plan_for(const GemmArgs &a, int sms, const void *ws, size_t workspace_bytes) {
+    GemmPlan pl = gemm_plan(a.M, a.N, a.K, sms, !a.transA, a.transB ? 1 : 0);
+    const bool usable = ws != nullptr && reinterpret_cast<uintptr_t>(ws) % 16 == 0;
+    if (pl.split && pl.transpose_a && (!usable || workspace_bytes < pl.workspace_bytes)) {
+        pl.transpose_a = 0;
+        pl.copy_bytes = 0;
+        pl.workspace_bytes = pl.split_bytes;
+    }
+    if ((pl.split || pl.transpose_a) && (!usable || workspace_bytes < pl.workspace_bytes)) {
+        const int nchunks = pl.nchunks;
+        pl = GemmPlan{};          // no usable workspace: one unit per tile
+        pl.units_per_tile = 1;
+        pl.kt_per_unit = int((a.K + BK - 1) / BK);
+        pl.nchunks = nchunks;
+    }
+    return pl;
+}
+
+int64_t gemm_launches(const GemmArgs &a, size_t workspace_bytes) {
+    if (a.M == 0 || a.N == 0) return 0;
+    if (a.K == 0) return 1;
+    // any non-null aligned address stands for a caller workspace of that size
+    const GemmPlan pl = gemm_plan_for(a, sm_count_current_device(),
+                                      workspace_bytes ? reinterpret_cast<const void *>(256)
+                                                      : nullptr,
+                                      workspace_bytes);
+    return 1 + int64_t(pl.transpose_a) + int64_t(pl.split);
 }
 
 namespace {
@@ -1237,16 +1288,10 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
         return cudaGetLastError();
     }
     const int sms = sm_count_current_device();
-    GemmPlan pl = gemm_plan(a.M, a.N, a.K, sms, !a.transA);
-    if ((pl.split || pl.transpose_a) &&
-        (workspace == nullptr || workspace_bytes < pl.workspace_bytes ||
-         reinterpret_cast<uintptr_t>(workspace) % 16 != 0)) {
-        pl = GemmPlan{};          // no usable workspace: one unit per tile
-        pl.units_per_tile = 1;
-        pl.kt_per_unit = int((a.K + BK - 1) / BK);
-    }
+    const GemmPlan pl = gemm_plan_for(a, sms, workspace, workspace_bytes);
     if (pl.transpose_a) {
-        // op(A) from the K x M copy: the transA form of the same product
+        // op(A) from the K x M copy: the transA form of the same product, its
+        // split partials (if any) in the workspace after the copy
         float *T = static_cast<float *>(workspace);
         const int64_t ldt = transposed_ld(a.M);
         cudaError_t e = launch_transpose(a.A, a.lda, a.M, a.K, T, ldt, sms, s);
@@ -1255,7 +1300,9 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
         t.A = T;
         t.lda = ldt;
         t.transA = 1;
-        return launch_gemm(t, nullptr, 0, s);
+        if (!pl.split) return launch_gemm(t, nullptr, 0, s);
+        return launch_gemm(t, static_cast<char *>(workspace) + pl.copy_bytes,
+                           workspace_bytes - pl.copy_bytes, s);
     }
     const Prepared x = prepare(a, pl, workspace);
     cudaError_t e = launch_prepared(x, nullptr, s);
@@ -1618,8 +1665,9 @@ static cudaError_t static_scratch(void **ptr) {
 
 cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s) {
     *too_big = false;
-    const GemmPlan pl = gemm_plan(a.M, a.N, a.K, sm_count_current_device(), !a.transA);
-    if (pl.split && pl.workspace_bytes > kStaticScratchBytes) {
+    const GemmPlan pl = gemm_plan(a.M, a.N, a.K, sm_count_current_device(), !a.transA,
+                                  a.transB ? 1 : 0);
+    if (pl.split && pl.split_bytes > kStaticScratchBytes) {
         *too_big = true;
         return cudaSuccess;
     }

@@ -70,6 +70,8 @@ SIGNATURES = [
                                  ctypes.c_size_t, _vp]),
     ("detgemm_group_workspace_bytes", _int, [_PROF, _i64, ctypes.POINTER(GemmProblem),
                                              ctypes.POINTER(ctypes.c_size_t)]),
+    ("detgemm_launches", _int, [_PROF, _int, _int, _i64, _i64, _i64, ctypes.c_size_t,
+                                ctypes.POINTER(ctypes.c_int64)]),
     ("detgemm_group_launches", _int, [_PROF, _i64, ctypes.POINTER(GemmProblem),
                                       ctypes.c_size_t, ctypes.POINTER(ctypes.c_int64)]),
     ("detgemm_f32_noalloc", _int, [_PROF, _int, _int, _i64, _i64, _i64, _vp, _i64, _vp,
@@ -191,6 +193,23 @@ def detgemm_workspace_bytes(M, N, K, transA=False, transB=False, profile=None) -
            load().detgemm_workspace_bytes(_prof(profile), int(bool(transA)),
                                           int(bool(transB)), int(M), int(N), int(K),
                                           ctypes.byref(n)))
+    return n.value
+
+
+def detgemm_launches(M, N, K, transA=False, transB=False, workspace=None,
+                     profile=None) -> int:
+    """Kernel launches detgemm_f32 makes for this shape with this workspace (a
+    tensor, a size in bytes, or None)."""
+    n = ctypes.c_int64()
+    if workspace is None:
+        wsn = 0
+    elif isinstance(workspace, int):
+        wsn = workspace
+    else:
+        wsn = workspace.numel() * 4
+    _check("detgemm_launches",
+           load().detgemm_launches(_prof(profile), int(bool(transA)), int(bool(transB)),
+                                   int(M), int(N), int(K), wsn, ctypes.byref(n)))
     return n.value
 
 

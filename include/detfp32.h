@@ -204,13 +204,23 @@ det_status detshardsum_f32(const det_profile_v1 *prof, int64_t nshards, int64_t 
                            det_stream_t stream);
 
 /* Workspace that detgemm_f32 can use for this shape and layout on the
- * current device, written to *bytes: the split-K chunk partials when
- * splitting K helps, else, for a large product with transA == 0, the
- * transposed copy of A (K x M, rows padded to 4 floats); 0 when neither
- * helps. Same argument rules as detgemm_f32; a host-only query apart from
- * reading the device's SM count. */
+ * current device, written to *bytes: for a large product with transA == 0,
+ * the transposed copy of A (K x M, rows padded to 4 floats) where it pays,
+ * and the split-K chunk partials where splitting K helps (after the copy,
+ * which is then rounded up to 256 bytes); 0 when neither helps. A smaller
+ * workspace that holds the partials alone gives the split without the copy.
+ * Same argument rules as detgemm_f32; a host-only query apart from reading
+ * the device's SM count. */
 det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA, int transB,
                                    int64_t M, int64_t N, int64_t K, size_t *bytes);
+
+/* The number of kernels detgemm_f32 launches for this shape and layout with a
+ * workspace of workspace_bytes (1 to 3: the transposed copy of A, the GEMM,
+ * the split-K second pass), written to *launches, for callers that count or
+ * capture launches. Same argument rules; host-only apart from reading the
+ * device's SM count. */
+det_status detgemm_launches(const det_profile_v1 *prof, int transA, int transB, int64_t M,
+                            int64_t N, int64_t K, size_t workspace_bytes, int64_t *launches);
 
 /* detgemm_f32 for callers that cannot allocate device memory when they
  * multiply: code that runs inside another framework's memory pool, where
