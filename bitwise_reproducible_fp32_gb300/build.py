@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libdetfp32.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["gemm.cu", "gemm_n64.cu", "rowops.cu", "rmsbwd.cu", "shardsum.cu", "block.cu",
+SOURCES = ["gemm.cu", "gemm_n64.cu", "gemm_m128.cu", "rowops.cu", "rmsbwd.cu", "shardsum.cu", "block.cu",
            "adamw.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NUMERICS = ["-fmad=false", "-ftz=false", "-prec-div=true", "-prec-sqrt=true"]

@@ -533,7 +533,9 @@ cudaError_t group_gemm(int64_t M, int64_t N, int64_t K, const HeadOperand &a, in
     bt.causal = causal;
     bt.tri = tri;
     bt.tri_bad = tri_bad;
-    // a head-wide N (P V, dV, dQ, dK) fills the 64-wide tiles
+    // a head-wide N (P V, dV, dQ, dK) fills the 64-wide tiles; the triangular
+    // ones take 128-row tiles, whose shorter units balance the CTAs' loads
+    if (N <= 64 && tri) return m128::launch_gemm_batched(g, bt, s);
     if (N <= 64) return n64::launch_gemm_batched(g, bt, s);
     return launch_gemm_batched(g, bt, s);
 }
@@ -618,11 +620,11 @@ DET_API det_status detattention_launches(const det_profile_v1 *prof, int64_t bat
     const AttnGroups g = attention_groups(batch, seq, heads);
     const int64_t groups = ((batch + g.gb - 1) / g.gb) * ((heads + g.gh - 1) / g.gh);
     // forward: the Q copy (long sequences), then a group's score product, the
-    // count of V's non-finite values, the softmax and P V; backward: S, the
-    // softmax, dP, the counts of dO's, K's and Q's non-finite values, dV, the
-    // softmax backward, dQ and dK
-    *launches = backward ? 10 * groups
-                         : 4 * groups + (attn_qt_bytes(batch, seq, heads, head_dim) ? 1 : 0);
+    // count of V's non-finite values, the softmax and P V; backward: the Q and
+    // dO copies (long sequences), then S, the softmax, dP, the counts of dO's,
+    // K's and Q's non-finite values, dV, the softmax backward, dQ and dK
+    const int64_t copies = attn_qt_bytes(batch, seq, heads, head_dim) ? 1 : 0;
+    *launches = backward ? 10 * groups + 2 * copies : 4 * groups + copies;
     return DET_OK;
 }
 
@@ -691,7 +693,8 @@ DET_API det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, 
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
     if (!bytes || !attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
-    *bytes = 2 * attention_groups(batch, seq, heads).score_bytes + kAttnFlagBytes;
+    *bytes = 2 * attention_groups(batch, seq, heads).score_bytes + kAttnFlagBytes +
+             2 * attn_qt_bytes(batch, seq, heads, head_dim);
     return DET_OK;
 }
 
@@ -710,15 +713,30 @@ DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batc
         return DET_ERR_INVALID_ARG;
     if ((st = check_device()) != DET_OK) return st;
     const AttnGroups g = attention_groups(batch, seq, heads);
-    if (!workspace || workspace_bytes < 2 * g.score_bytes + kAttnFlagBytes ||
+    const size_t qt_bytes = attn_qt_bytes(batch, seq, heads, head_dim);
+    if (!workspace ||
+        workspace_bytes < 2 * g.score_bytes + kAttnFlagBytes + 2 * qt_bytes ||
         reinterpret_cast<uintptr_t>(workspace) % 256)
         return DET_ERR_WORKSPACE;
     float *Pb = static_cast<float *>(workspace);
     float *dPb = reinterpret_cast<float *>(static_cast<char *>(workspace) + g.score_bytes);
     int *flags = reinterpret_cast<int *>(static_cast<char *>(workspace) + 2 * g.score_bytes);
+    // long sequences: the score products read Q and dO from transposed copies
+    // (the row-pair loop, as in the forward), with the same bits
+    float *QT = qt_bytes ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                     2 * g.score_bytes + kAttnFlagBytes)
+                         : nullptr;
+    float *dOT = qt_bytes ? reinterpret_cast<float *>(reinterpret_cast<char *>(QT) + qt_bytes)
+                          : nullptr;
+    const int64_t ldt = attn_qt_ld(batch, seq);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = for_each_group(batch, heads, g, [&](int64_t b0, int64_t nb, int64_t h0,
-                                                              int64_t nh) {
+    cudaError_t e = cudaSuccess;
+    if (QT) {
+        e = launch_transpose_copy(qkv, ldqkv, batch * seq, hd, QT, ldt, s);
+        if (e == cudaSuccess) e = launch_transpose_copy(dout, lddout, batch * seq, hd, dOT, ldt, s);
+    }
+    if (e == cudaSuccess) e = for_each_group(batch, heads, g, [&](int64_t b0, int64_t nb,
+                                                                  int64_t h0, int64_t nh) {
         const int64_t count = nb * nh;
         auto in = [&](const float *buf, int64_t ld, int64_t width, int64_t col) {
             return head_operand(buf, ld, width, batch, seq, b0, col + h0 * head_dim, head_dim);
@@ -726,15 +744,18 @@ DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batc
         const HeadOperand Q = in(qkv, ldqkv, 3 * hd, 0), K = in(qkv, ldqkv, 3 * hd, hd);
         const HeadOperand V = in(qkv, ldqkv, 3 * hd, 2 * hd), dO = in(dout, lddout, hd, 0);
         const HeadOperand P = stacked(Pb, seq, nh, count), dP = stacked(dPb, seq, nh, count);
+        const HeadOperand Qs = QT ? q_from_copy(QT, ldt, batch, seq, hd, b0, h0, head_dim) : Q;
+        const HeadOperand dOs =
+            dOT ? q_from_copy(dOT, ldt, batch, seq, hd, b0, h0, head_dim) : dO;
         float *dbase = dqkv + b0 * seq * lddqkv + h0 * head_dim;
         const int64_t dzb = seq * lddqkv;
-        cudaError_t r = group_gemm(seq, seq, head_dim, Q, 0, K, 1, Pb, seq, P.zb, P.zh, count,
-                                   nh, 1, s);
+        cudaError_t r = group_gemm(seq, seq, head_dim, Qs, QT ? 1 : 0, K, 1, Pb, seq, P.zb,
+                                   P.zh, count, nh, 1, s);
         if (r == cudaSuccess)
             r = launch_softmax_causal(count * seq, seq, Pb, seq, scale, 0, seq, Pb, seq, s);
         if (r == cudaSuccess)
-            r = group_gemm(seq, seq, head_dim, dO, 0, V, 1, dPb, seq, dP.zb, dP.zh, count, nh, 1,
-                           s);
+            r = group_gemm(seq, seq, head_dim, dOs, dOT ? 1 : 0, V, 1, dPb, seq, dP.zb, dP.zh,
+                           count, nh, 1, s);
         // P and dS are +0 above the diagonal, so P^T and dS^T below it: with
         // finite dO, K and Q (flags 0, 1, 2) the chunks there are skipped
         const HeadOperand finite[3] = {dO, K, Q};
@@ -912,8 +933,12 @@ DET_API det_status det_watchdog_status(int32_t *code, int clear) {
     unsigned int c3 = 0, c4 = 0;
     if (e == cudaSuccess) e = n64::gemm_watchdog(&c4, clear);
     c |= c4;
+    if (e == cudaSuccess) e = m128::gemm_watchdog(&c4, clear);
+    c |= c4;
     if (e == cudaSuccess) e = rowops_watchdog(&c2, clear);
     if (e == cudaSuccess) e = rmsbwd_watchdog(&c3, clear);
-    *code = int32_t(c | c2 | c3);
+    unsigned int c5 = 0;
+    if (e == cudaSuccess) e = block_watchdog(&c5, clear);
+    *code = int32_t(c | c2 | c3 | c5);
     return from_cuda(e);
 }

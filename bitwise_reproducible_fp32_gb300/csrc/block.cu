@@ -28,7 +28,13 @@
 #include "det_math.cuh"
 
 namespace det {
+
+// Set when a bounded wait of the bulk-staged causal softmax gave up.
+__device__ unsigned int g_block_watchdog;
+
 namespace {
+
+constexpr unsigned kWatchdogSoftmax = 16u;   // det_watchdog_status bit 4
 
 constexpr int kSmaxChains = 32 * 8;       // 8 chains a lane of a warp
 static_assert(kSmaxChains == kXentLanes, "the 256 chains of the row reductions");
@@ -341,6 +347,135 @@ __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
     }
 }
 
+// One staged row of the bulk kernel: the passes and every arithmetic step of
+// softmax_causal_kernel's staged path (the same bits) on the row's kept
+// columns s[0 .. nr) in slots: pass 1 the max of x = s * scale, pass 2
+// e = exp(x - m) into the slots and the chains, pass 3 p = e * (1 / S) to pr.
+__device__ __forceinline__ void softmax_row_from_slots(float4 *slots, int64_t nr, float *pr,
+                                                       float scale, int lane, bool vec_p) {
+    const int ng = int((nr + 3) / 4);
+    float m = __fmul_rn(reinterpret_cast<const float *>(slots)[0], scale);
+    for (int g = lane; g < ng; g += 32) {
+        float4 v = slots[g];
+        v.x = __fmul_rn(v.x, scale); v.y = __fmul_rn(v.y, scale);
+        v.z = __fmul_rn(v.z, scale); v.w = __fmul_rn(v.w, scale);
+        const int j = 4 * g;
+        if (j < nr) m = max_nan2(m, v.x);
+        if (j + 1 < nr) m = max_nan2(m, v.y);
+        if (j + 2 < nr) m = max_nan2(m, v.z);
+        if (j + 3 < nr) m = max_nan2(m, v.w);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        m = max_nan2(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const bool finite = fabsf(m) <= 0x1.fffffep127f;
+    float c[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) c[w] = 0.0f;
+    // chain lane + 32 w adds groups lane + 32 w + 256 sg, sg ascending
+    for (int sg = 0; 256 * sg < ng; ++sg)
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const int g = lane + 32 * w + 256 * sg;
+            if (g >= ng) continue;
+            float4 v = slots[g];
+            v.x = __fmul_rn(v.x, scale); v.y = __fmul_rn(v.y, scale);
+            v.z = __fmul_rn(v.z, scale); v.w = __fmul_rn(v.w, scale);
+            const float4 e = finite ? exp4(v, m)
+                                    : make_float4(det_exp_call(__fsub_rn(v.x, m)),
+                                                  det_exp_call(__fsub_rn(v.y, m)),
+                                                  det_exp_call(__fsub_rn(v.z, m)),
+                                                  det_exp_call(__fsub_rn(v.w, m)));
+            slots[g] = e;
+            const int j = 4 * g;
+            if (j < nr) c[w] = __fadd_rn(c[w], e.x);
+            if (j + 1 < nr) c[w] = __fadd_rn(c[w], e.y);
+            if (j + 2 < nr) c[w] = __fadd_rn(c[w], e.z);
+            if (j + 3 < nr) c[w] = __fadd_rn(c[w], e.w);
+        }
+    const float inv = __fdiv_rn(1.0f, fold_chains(c));
+    for (int g = lane; g < ng; g += 32) {
+        const float4 e = slots[g];
+        st4_kept(pr, 4 * int64_t(g), nr, vec_p,
+                 make_float4(__fmul_rn(e.x, inv), __fmul_rn(e.y, inv), __fmul_rn(e.z, inv),
+                             __fmul_rn(e.w, inv)));
+    }
+}
+
+// The causal softmax for rows of at most kSmaxStage columns, 16-byte aligned
+// (the attention's score rows): each warp keeps two row buffers in shared
+// memory, and its lane 0 brings the warp's next row in by one bulk copy
+// (cp.async.bulk, completing on the buffer's mbarrier) while the warp works
+// on the current one, so a warp's HBM reads are in flight back to back with
+// no load instructions of its own. The row's arithmetic is
+// softmax_row_from_slots. (Pairs of rows, i and period - 1 - i, a copy of
+// about twice the bytes an item, measured 7% slower.) A wait for a copy gives
+// up after kWaitLimitNs: the kernel then sets kWatchdogSoftmax, lets its
+// copies in flight land (bounded) and returns.
+constexpr int kSmaxBulkWarps = 4;    // 64 KB of buffers a block, 3 blocks an SM
+constexpr int kSmaxBulkBlocksPerSm = 3;
+__global__ void __launch_bounds__(32 * kSmaxBulkWarps)
+    softmax_causal_bulk_kernel(int64_t rows, int64_t cols, const float *s, int64_t lds,
+                               float scale, int64_t diag, int64_t period, float *p,
+                               int64_t ldp, int vec_p, const int *chunk_zeros) {
+    extern __shared__ float4 smax_bufs[];
+    __shared__ uint64_t sbar[kSmaxBulkWarps][2];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    float4 *bufs = smax_bufs + wib * 2 * (kSmaxStage / 4);
+    const uint32_t bar0 = smem_u32(&sbar[wib][0]), bar1 = smem_u32(&sbar[wib][1]);
+    const int64_t nwarps = int64_t(gridDim.x) * kSmaxBulkWarps;
+    const int64_t first = int64_t(blockIdx.x) * kSmaxBulkWarps + wib;
+    const bool to_chunk = chunk_zeros != nullptr && *chunk_zeros == 0;
+    if (lane == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar1, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    // lane 0: row r's kept columns, rounded up to whole 16-byte groups (within
+    // the row's cols, a multiple of 4), into buffer b; the proxy fence orders
+    // the warp's earlier shared-memory accesses to that buffer before the copy
+    auto issue = [&](int64_t r, int b) {
+        const int64_t nr = kept_columns(r, period, diag, cols);
+        if (nr == 0) return;
+        const uint32_t bytes = uint32_t((nr + 3) & ~int64_t(3)) * 4u;
+        const uint32_t bar = b ? bar1 : bar0;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(smem_u32(bufs + b * (kSmaxStage / 4)), s + r * lds, bytes, bar);
+    };
+    if (lane == 0 && first < rows) issue(first, 0);
+    uint32_t ph = 0;   // bit b: the parity of the next wait on buffer b
+    int k = 0;
+    for (int64_t r = first; r < rows; r += nwarps, ++k) {
+        const int b = k & 1;
+        // the other buffer held the previous row, which the warp is done with
+        if (lane == 0 && r + nwarps < rows) issue(r + nwarps, b ^ 1);
+        const int64_t nr = kept_columns(r, period, diag, cols);
+        float *pr = p + r * ldp;
+        if (nr > 0) {
+            const bool ok = mbar_wait_bounded(b ? bar1 : bar0, (ph >> b) & 1u);
+            ph ^= 1u << b;
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) {
+                    atomicOr(&g_block_watchdog, kWatchdogSoftmax);
+                    (void)mbar_wait_bounded(b ? bar1 : bar0, ((ph >> b) & 1u) ^ 1u);
+                    if (r + nwarps < rows && kept_columns(r + nwarps, period, diag, cols) > 0)
+                        (void)mbar_wait_bounded(b ? bar0 : bar1, (ph >> (b ^ 1)) & 1u);
+                }
+                __syncwarp();
+                return;
+            }
+        }
+        const int64_t chunk_end = ((r % period) / kKChunk + 1) * kKChunk;
+        const int64_t zend = to_chunk && chunk_end < cols ? chunk_end : cols;
+        zero_masked(pr, nr, zend, lane, vec_p);
+        if (nr > 0)   // uniform across the warp
+            softmax_row_from_slots(bufs + b * (kSmaxStage / 4), nr, pr, scale, lane, vec_p);
+        __syncwarp();
+    }
+}
+
 // Softmax backward: dot = the chains of fmaf(dP_j, P_j, .) over the kept
 // columns, folded as the forward's sum; dS_j = (P_j (dP_j - dot)) scale;
 // masked columns +0. ds may be dp itself (each dS_j is written after dP_j is
@@ -543,6 +678,16 @@ bool al16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
 }  // namespace
 
+cudaError_t block_watchdog(unsigned int *code, int clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_block_watchdog, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    if (clear && *code) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_block_watchdog, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
+
 cudaError_t launch_swiglu(int64_t n, const float *g, const float *u, float *out,
                           cudaStream_t s) {
     if (n == 0) return cudaSuccess;
@@ -565,6 +710,22 @@ cudaError_t launch_softmax_causal(int64_t rows, int64_t cols, const float *sc, i
     const int64_t blocks = std::min<int64_t>((rows + kSmaxWarps - 1) / kSmaxWarps,
                                              int64_t(sm_count_current_device()) * 16);
     const int vec_s = al16(sc) && lds % 4 == 0, vec_p = al16(p) && ldp % 4 == 0;
+    if (vec_s && cols <= kSmaxStage && cols % 4 == 0) {
+        // every row fits a buffer, and a copy rounded up to whole 16-byte
+        // groups stays within the row's columns: the bulk-staged kernel,
+        // persistent
+        const size_t bsmem = size_t(kSmaxBulkWarps) * 2 * kSmaxStage * 4;
+        const int64_t bblocks = std::min<int64_t>(
+            (rows + kSmaxBulkWarps - 1) / kSmaxBulkWarps,
+            int64_t(sm_count_current_device()) * kSmaxBulkBlocksPerSm);
+        cudaError_t eb = cudaFuncSetAttribute(softmax_causal_bulk_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              int(bsmem));
+        if (eb != cudaSuccess) return eb;
+        softmax_causal_bulk_kernel<<<unsigned(bblocks), 32 * kSmaxBulkWarps, bsmem, s>>>(
+            rows, cols, sc, lds, scale, diag, period, p, ldp, vec_p, chunk_zeros);
+        return cudaGetLastError();
+    }
     const size_t smem = size_t(kSmaxWarps) * kSmaxStage * 4;
     const cudaError_t e = cudaFuncSetAttribute(
         softmax_causal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));

@@ -24,7 +24,9 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Watchdog bits (det_watchdog_status).
 constexpr unsigned int kWatchdogGemm = 1u;   // GEMM operand staging
-// bit 1 (2u): cross-entropy row staging, defined in rowops.cu
+// bit 1 (2u): cross-entropy row staging, defined in rowops.cu; bit 2 (4u):
+// RMSNorm-backward staging (rmsbwd.cu); bit 3 (8u): RMSNorm row staging
+// (rowops.cu); bit 4 (16u): causal-softmax row staging (block.cu)
 
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error; arguments are validated by
@@ -103,10 +105,18 @@ namespace n64 {
 cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s);
 cudaError_t gemm_watchdog(unsigned int *code, int clear);
 }  // namespace n64
+// The same batched products with 128 x 64 CTA tiles (gemm_m128.cu): the
+// triangular products of N <= 64 (causal attention's P V, dV, dQ, dK), whose
+// row blocks differ in work, in units half as long. Same bits.
+namespace m128 {
+cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s);
+cudaError_t gemm_watchdog(unsigned int *code, int clear);
+}  // namespace m128
 cudaError_t launch_gemm_noalloc(const GemmArgs &a, bool *too_big, cudaStream_t s);
 
 cudaError_t rowops_watchdog(unsigned int *code, int clear);
 cudaError_t rmsbwd_watchdog(unsigned int *code, int clear);
+cudaError_t block_watchdog(unsigned int *code, int clear);
 
 // 2-D fp32 TMA descriptor over a row-major matrix: inner = contiguous extent,
 // outer = rows, ld = row stride (elements); out-of-range boxes read zeros.

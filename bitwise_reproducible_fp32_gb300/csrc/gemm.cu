@@ -57,7 +57,7 @@
 #include "det_internal.cuh"
 
 #ifdef DET_GEMM_SECONDARY_NS
-// A second build of this file (see gemm_n64.cu): its kernels and batched
+// Another build of this file (gemm_n64.cu, gemm_m128.cu): its kernels and batched
 // launcher live in their own namespace; the shared helpers, plans and the
 // single-product launchers come from the primary build.
 #define DET_GEMM_PRIMARY 0
@@ -172,6 +172,12 @@ struct KArgs {
     int zcount;        // 1: a single product
     int zinner;
     int64_t a_zb, a_zh, b_zb, b_zh, c_zb, c_zh;
+    // The TMA coordinates of those offsets: offset / ld and offset % ld split
+    // into the parts of zb and zh (the launcher takes TMA only when the
+    // column parts never carry into the next row), so the producer needs no
+    // 64-bit division: row = (z / zinner) * X_rb + (z % zinner) * X_rh, and
+    // column likewise.
+    int a_rb, a_cb, a_rh, a_ch, b_rb, b_cb, b_rh, b_ch;
     // Causal: only the tiles holding some output with j <= i are computed
     // (row-major over those tiles); the others are left unwritten.
     int causal;
@@ -577,6 +583,78 @@ __device__ __forceinline__ void store_tile(const float (&acc)[TM][TN], float *ba
     }
 }
 
+// The epilogue through shared memory, for op(A) m-contiguous and op(B)
+// k-contiguous (the LM head on its copy of X, the attention's score
+// product). A thread's columns are 4 apart there, so direct stores write 16
+// scattered bytes of 8 rows an instruction. Here the warp's 128 x 32 result
+// first goes to the warp's own slots of the totals area (float4 slots
+// q * THREADS + 32 * warp + lane, q = 0..31: 32 runs of 128 floats, 4 rows
+// each), with the 16-byte groups of a row XOR-swizzled by (row / 4) mod 8 so
+// that the scalar writes and the 16-byte reads are both conflict-free; it
+// then leaves as whole 128-byte rows, four rows a store instruction. Only
+// the store pattern changes: each output is the same value, written once
+// (with accum, C + result as store_tile adds it). The slots belong to the
+// warp's own threads, whose chunk folds are done; the area is free again
+// after the final __syncwarp.
+constexpr bool kStagedEpilogue = !kTmemTotals && TM == 16 && TN == 8 && WTM == 128 &&
+                                 WTN == 32;
+__device__ __forceinline__ void store_tile_staged(const float (&acc)[TM][TN], float *area,
+                                                  float *base, int64_t ld, int M, int N, int r0,
+                                                  int c0, int accum) {
+    // the thread's place is read here, not passed in, so that the compiler
+    // does not keep these offsets live through the main loop
+    uint32_t tidx;
+    asm volatile("mov.u32 %0, %%tid.x;" : "=r"(tidx));
+    const int lane = int(tidx & 31u), warp = int(tidx >> 5);
+    const int lm = lane >> 2, ln = lane & 3;
+    float *mine = area + warp * 128;
+    __syncwarp();
+    {
+        // thread rows 4 lm + (r & 3) + 32 (r >> 2), columns ln + 4c: row run
+        // lm + 8 (r >> 2), row in run r & 3, swizzled column ln + 4 (c ^ lm)
+        float *t = mine + lm * (THREADS * 4) + ln;
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            float *tc = t + 4 * (c ^ lm);
+#pragma unroll
+            for (int r = 0; r < TM; ++r)
+                tc[(r >> 2) * 8 * (THREADS * 4) + (r & 3) * 32] = acc[r][c];
+        }
+    }
+    __syncwarp();
+    // lane: row 4 s + (lane >> 3) of the warp tile, columns 4 (lane & 7) .. + 3
+    const int rl = lane >> 3, g = lane & 7;
+    const int col = c0 + 4 * g;
+    const bool full = col + 3 < N;
+    float *crow = base + int64_t(r0 + rl) * ld + col;
+#pragma unroll 1
+    for (int s0 = 0; s0 < 8; ++s0) {
+        const float *src = mine + s0 * (THREADS * 4) + rl * 32 + 4 * (g ^ s0);
+        float *dst0 = crow + int64_t(4 * s0) * ld;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int s = s0 + 8 * t;
+            if (r0 + rl + 4 * s >= M) continue;
+            float4 v = *reinterpret_cast<const float4 *>(src + 8 * t * (THREADS * 4));
+            float *dst = dst0 + int64_t(32 * t) * ld;
+            if (full) {
+                if (accum) {
+                    const float4 o = *reinterpret_cast<const float4 *>(dst);
+                    v = make_float4(__fadd_rn(o.x, v.x), __fadd_rn(o.y, v.y),
+                                    __fadd_rn(o.z, v.z), __fadd_rn(o.w, v.w));
+                }
+                *reinterpret_cast<float4 *>(dst) = v;
+            } else {
+                const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (col + e < N) dst[e] = accum ? __fadd_rn(dst[e], vv[e]) : vv[e];
+            }
+        }
+    }
+    __syncwarp();
+}
+
 // The chunk fold with the running totals in Tensor Memory: 32 columns a copy.
 // The first chunk's partial is stored as the total; a later one is added to
 // it, total + partial, and after the last chunk the sum is the result (left
@@ -684,10 +762,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     auto issue_next = [&](int slot) {
         int ar = 0, ac = 0, br = 0, bc = 0;
         if (BATCH && p.zcount > 1) {
-            const int64_t ao = z_offset(p.a_zb, p.a_zh, prod.u.z, p.zinner);
-            const int64_t bo = z_offset(p.b_zb, p.b_zh, prod.u.z, p.zinner);
-            ar = int(ao / p.lda); ac = int(ao % p.lda);
-            br = int(bo / p.ldb); bc = int(bo % p.ldb);
+            const int zb = prod.u.z / p.zinner, zh = prod.u.z - zb * p.zinner;
+            ar = zb * p.a_rb + zh * p.a_rh; ac = zb * p.a_cb + zh * p.a_ch;
+            br = zb * p.b_rb + zh * p.b_rh; bc = zb * p.b_cb + zh * p.b_ch;
         }
         issue_stage<A_KM, B_KM>(stages + slot * STAGE_FLOATS, &full[slot], tmA, tmB,
                                 prod.u.m0, prod.u.n0, prod.kt, ar, ac, br, bc);
@@ -845,12 +922,21 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         }
         if (aborted) break;
         // epilogue (the next unit's loads are already in flight)
-        if (!SPLIT)
+        if constexpr (!SPLIT && kStagedEpilogue && !A_KM && B_KM) {
+            float *cbase = p.C + (BATCH ? z_offset(p.c_zb, p.c_zh, w.z, p.zinner) : 0);
+            if (p.vec_store)
+                store_tile_staged(acc, reinterpret_cast<float *>(totals), cbase, p.ldc, p.M,
+                                  p.N, w.m0 + wm * WTM, w.n0 + wn * WTN, p.accumulate);
+            else
+                store_tile<A_KM, B_KM>(acc, cbase, p.ldc, p.M, p.N, w.m0, w.n0, arow, bcol, 0,
+                                       p.accumulate);
+        } else if constexpr (!SPLIT) {
             store_tile<A_KM, B_KM>(acc,
                                    p.C + (BATCH ? z_offset(p.c_zb, p.c_zh, w.z, p.zinner) : 0),
                                    p.ldc,
                                    p.M, p.N, w.m0, w.n0, arow, bcol,
                                    p.vec_store, p.accumulate);
+        }
     }
 
     // any warp may have issued the last copies: once every thread is here no
@@ -1525,6 +1611,22 @@ cudaError_t launch_gemm_pair(const GemmArgs &a0, const GemmArgs &a1, void *works
 
 #endif  // DET_GEMM_PRIMARY
 
+// The TMA row and column parts of an operand's per-product offsets
+// zb * (z / inner) + zh * (z % inner) in a buffer of row stride ld (KArgs);
+// false when a column part could carry into the next row or a part would not
+// fit an int (the launch then stages by plain loads, which take the offsets
+// as they are).
+static bool split_offsets(int64_t zb, int64_t zh, int64_t ld, int64_t count, int64_t inner,
+                          int *rb, int *cb, int *rh, int *ch) {
+    const int64_t nzb = (count + inner - 1) / inner, nzh = std::min(count, inner);
+    const int64_t r_b = zb / ld, c_b = zb % ld, r_h = zh / ld, c_h = zh % ld;
+    const int64_t lim = int64_t(1) << 31;
+    if ((nzb - 1) * c_b + (nzh - 1) * c_h >= ld) return false;
+    if ((nzb - 1) * r_b + (nzh - 1) * r_h >= lim) return false;
+    *rb = int(r_b); *cb = int(c_b); *rh = int(r_h); *ch = int(c_h);
+    return true;
+}
+
 cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s) {
     if (bt.count == 0 || a.M == 0 || a.N == 0) return cudaSuccess;
     if (a.K == 0) {
@@ -1577,7 +1679,11 @@ cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStre
     // one map spans each whole buffer; a product's tile coordinates add its
     // offset's row and column, which TMA needs on a 16-byte boundary
     x.tma = off4 && tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb) &&
-            bt.a_rows < (int64_t(1) << 31) && bt.b_rows < (int64_t(1) << 31);
+            bt.a_rows < (int64_t(1) << 31) && bt.b_rows < (int64_t(1) << 31) &&
+            split_offsets(bt.a_zb, bt.a_zh, a.lda, bt.count, bt.inner, &k.a_rb, &k.a_cb,
+                          &k.a_rh, &k.a_ch) &&
+            split_offsets(bt.b_zb, bt.b_zh, a.ldb, bt.count, bt.inner, &k.b_rb, &k.b_cb,
+                          &k.b_rh, &k.b_ch);
     if (x.tma) {
         x.tma = make_map(&x.ma, a.A, bt.a_cols, bt.a_rows, a.lda, x.a_km, BM) &&
                 make_map(&x.mb, a.B, bt.b_cols, bt.b_rows, a.ldb, x.b_km, BN);

@@ -439,8 +439,12 @@ det_status detadd_f32(const det_profile_v1 *prof, int64_t n, const float *a,
  * ascending order) folded by the xor butterfly, p = e * (1 / S). Masked
  * columns are +0; a row that keeps no column is +0 throughout.
  * scores: rows x cols, lds >= cols; p: rows x cols, ldp >= cols; p may equal
- * scores when ldp == lds (in place). period >= 1 (the rows of one square score
- * matrix: its query index is r mod period). */
+ * scores when ldp == lds (in place) and must not otherwise overlap it.
+ * period >= 1 (the rows of one square score matrix: its query index is
+ * r mod period). With 16-byte aligned scores, lds and cols multiples of 4 and
+ * cols <= 2048, each row comes into shared memory by one bulk copy; a wait for
+ * a copy that gives up after 2 s sets bit 4 of det_watchdog_status() and
+ * leaves the remaining rows unwritten. */
 det_status detsoftmax_causal_f32(const det_profile_v1 *prof, int64_t rows, int64_t cols,
                                  const float *scores, int64_t lds, float scale, int64_t diag,
                                  int64_t period, float *p, int64_t ldp, det_stream_t stream);
@@ -556,8 +560,10 @@ det_status detembedding_bwd_f32(const det_profile_v1 *prof, int64_t ntok, int64_
  * heads as in detattention_f32; dV, dQ and dK skip the +0 chunks of P and dS
  * when dO, K and Q are finite. The workspace (at least
  * detattention_bwd_workspace_bytes, 256-byte aligned) holds two score
- * buffers of a group. dqkv must not overlap qkv, dout or the workspace.
- * Errors as detattention_f32. */
+ * buffers of a group and, for seq >= 512, transposed copies of the Q block
+ * and of dout (heads head_dim x batch seq floats each), from which the two
+ * score products read Q and dO. dqkv must not overlap qkv, dout or the
+ * workspace. Errors as detattention_f32. */
 det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
                                 int64_t heads, int64_t head_dim, const float *qkv,
                                 int64_t ldqkv, const float *dout, int64_t lddout, float scale,
@@ -570,7 +576,8 @@ det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t 
 /* Reads, and optionally clears, the current device's watchdog word.
  * *code == 0 means no bounded device wait has ever given up; otherwise bit k
  * identifies the kernel family that gave up (bit 0: GEMM operand staging,
- * bit 1: cross-entropy row staging, bit 2: RMSNorm-backward tile staging).
+ * bit 1: cross-entropy row staging, bit 2: RMSNorm-backward tile staging,
+ * bit 3: RMSNorm row staging, bit 4: causal-softmax row staging).
  * This call synchronises the device (it copies from device memory). */
 det_status det_watchdog_status(int32_t *code, int clear);
 

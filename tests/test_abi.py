@@ -176,7 +176,7 @@ def test_bad_arguments_are_refused_on_the_host(lib):
     assert lib.detattention_workspace_bytes(p, 4, 2048, 12, 64, ctypes.byref(n)) == 0
     assert n.value == 48 * 2048 * 2048 * 4 + 256 + 768 * 8192 * 4   # + counts, Q copy
     assert lib.detattention_bwd_workspace_bytes(p, 4, 2048, 12, 64, ctypes.byref(n)) == 0
-    assert n.value == 2 * 48 * 2048 * 2048 * 4 + 256
+    assert n.value == 2 * 48 * 2048 * 2048 * 4 + 256 + 2 * 768 * 8192 * 4   # + Q, dO copies
     assert lib.detattention_workspace_bytes(p, 16, 128, 4, 16, ctypes.byref(n)) == 0
     assert n.value == 64 * 128 * 128 * 4 + 256
     # 8 sequences of 8192 tokens x 12 heads (3 GiB of scores) go 4 heads at a time
@@ -184,17 +184,20 @@ def test_bad_arguments_are_refused_on_the_host(lib):
     assert n.value == 4 * 8192 * 8192 * 4 + 256 + 768 * 65536 * 4
     assert lib.detattention_workspace_bytes(p, 1, 0, 12, 64, ctypes.byref(n)) == 1
     # launches: 4 a group forward (+ the Q copy from 512 tokens), 10 backward
+    # (+ the Q and dO copies from 512 tokens)
     k = ctypes.c_int64(0)
     assert lib.detattention_launches(p, 4, 2048, 12, 64, 0, ctypes.byref(k)) == 0
     assert k.value == 5
     assert lib.detattention_launches(p, 4, 2048, 12, 64, 1, ctypes.byref(k)) == 0
+    assert k.value == 12
+    assert lib.detattention_launches(p, 16, 128, 4, 16, 1, ctypes.byref(k)) == 0
     assert k.value == 10
     assert lib.detattention_launches(p, 16, 128, 4, 16, 0, ctypes.byref(k)) == 0
     assert k.value == 4
     assert lib.detattention_launches(p, 8, 8192, 12, 64, 0, ctypes.byref(k)) == 0
     assert k.value == 8 * 3 * 4 + 1
     assert lib.detattention_launches(p, 8, 8192, 12, 64, 1, ctypes.byref(k)) == 0
-    assert k.value == 8 * 3 * 10
+    assert k.value == 8 * 3 * 10 + 2
     assert lib.detattention_launches(p, 0, 2048, 12, 64, 0, ctypes.byref(k)) == 0
     assert k.value == 0
     assert lib.detattention_launches(p, 1, 0, 12, 64, 0, ctypes.byref(k)) == 1

@@ -113,7 +113,10 @@ def attention_bwd_oracle(qkv, dout, b, h, seq, heads, d, scale):
     # 3 chunks of k: dV, dQ and dK skip the +0 chunks of P and dS when dO, K and
     # Q are finite, and must take them all when one holds an inf or a NaN
     (1, 600, 2, 16, None, None), (1, 600, 2, 16, None, "dout"), (1, 600, 2, 16, None, "k"),
-    (1, 600, 2, 16, None, "q")])
+    (1, 600, 2, 16, None, "q"),
+    # from 512 tokens the score products read Q and dO from transposed copies,
+    # here with a ragged token count (the copies' row stride padded to 4)
+    (3, 513, 2, 32, None, None)])
 def test_attention_bwd(dev, B, T, H, d, checks, poison):
     rng = np.random.default_rng(T + H)
     qkv = rng.standard_normal((B * T, 3 * H * d)).astype(F)

@@ -79,6 +79,47 @@ def test_softmax_batched_by_period_in_place_and_specials(dev):
     assert_bitwise(host(sd), want)
 
 
+@pytest.mark.parametrize("diag", [0, -3, 5])
+def test_softmax_bulk_staged_rows_cycle_both_buffers(dev, diag):
+    # 16-byte aligned rows of at most 2048 columns (a multiple of 4) take the
+    # bulk-staged kernel; 6 x 512 rows are more than its warps, so each warp
+    # runs several rows through both of its buffers, in place, with special
+    # rows among them and (diag < 0) rows that keep no column
+    rng = np.random.default_rng(1000 + diag)
+    mats = [(4 * rng.standard_normal((512, 512))).astype(F) for _ in range(6)]
+    mats[1][10, 3] = F(np.nan)
+    mats[1][11, :] = F(-np.inf)
+    mats[2][12, 5] = F(np.inf)
+    mats[2][13, 0] = F(-np.inf)
+    mats[4][300, :200] = F(88.0)
+    stack = np.concatenate(mats)
+    sd = to_dev(stack)
+    detlib.detsoftmax_causal_f32(sd, scale=0.125, diag=diag, period=512, p=sd)
+    want = np.concatenate([oracle.softmax_causal(m, scale=0.125, diag=diag) for m in mats])
+    assert_bitwise(host(sd), want, f"diag={diag}")
+    assert detlib.det_watchdog_status() == 0
+
+
+@pytest.mark.parametrize("diag", [0, -1])
+def test_softmax_bulk_staged_odd_period(dev, diag):
+    # an odd period; cols (a multiple of 4) wider than the period
+    rng = np.random.default_rng(31 - diag)
+    mats = [(4 * rng.standard_normal((257, 260))).astype(F) for _ in range(3)]
+    got = detlib.detsoftmax_causal_f32(to_dev(np.concatenate(mats)), scale=0.125, diag=diag,
+                                       period=257)
+    want = np.concatenate([oracle.softmax_causal(m, scale=0.125, diag=diag) for m in mats])
+    assert_bitwise(host(got), want, f"diag={diag}")
+
+
+def test_softmax_bulk_staged_out_of_place_padded(dev):
+    rng = np.random.default_rng(77)
+    s = (4 * rng.standard_normal((4000, 2048))).astype(F)
+    want = np.concatenate([oracle.softmax_causal(s[:2000], scale=0.125),
+                           oracle.softmax_causal(s[2000:], scale=0.125)])
+    got = detlib.detsoftmax_causal_f32(to_dev(s, "padded"), scale=0.125, period=2000)
+    assert_bitwise(host(got), want)
+
+
 def test_rope_on_the_packed_qkv_layout(dev):
     # 2 sequences of 300 tokens, 6 heads of 64: Q and K (12 heads) turned in
     # place inside rows of [Q | K | V]; V untouched
