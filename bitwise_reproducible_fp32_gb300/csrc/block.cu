@@ -349,57 +349,89 @@ __global__ void __launch_bounds__(32 * kSmaxWarps, kSmaxMinBlocks)
 
 // One staged row of the bulk kernel: the passes and every arithmetic step of
 // softmax_causal_kernel's staged path (the same bits) on the row's kept
-// columns s[0 .. nr) in slots: pass 1 the max of x = s * scale, pass 2
-// e = exp(x - m) into the slots and the chains, pass 3 p = e * (1 / S) to pr.
+// columns s[0 .. nr) in slots: pass 1 the max of x = s * scale, pass 2a
+// e = exp(x - m) into the slots, pass 2b the chains, pass 3 p = e * (1 / S)
+// to pr. A lane touches only the groups g = lane (mod 32) in every pass, so
+// no pass waits on another lane. The loops over whole groups run without
+// per-group conditions (four exps in flight a lane in pass 2a): with the
+// conditions inside the unrolled loop the compiler ran the exps one after
+// another, and the warps stalled on their dependent steps. The products by
+// scale and by 1/S are packed pairs (each half rounded as __fmul_rn).
+__device__ __forceinline__ float4 scaled4(float4 v, f32x2 sc2) {
+    float4 r;
+    unpack2(mul2(pack2(v.x, v.y), sc2), r.x, r.y);
+    unpack2(mul2(pack2(v.z, v.w), sc2), r.z, r.w);
+    return r;
+}
 __device__ __forceinline__ void softmax_row_from_slots(float4 *slots, int64_t nr, float *pr,
                                                        float scale, int lane, bool vec_p) {
-    const int ng = int((nr + 3) / 4);
+    const int ng = int((nr + 3) / 4);     // groups holding a kept column
+    const int nfull = int(nr / 4);        // groups of 4 kept columns
+    const f32x2 sc2 = splat2(scale);
+    // pass 1: the max (order free: NaN wins, a +0/-0 tie is bit-inert)
     float m = __fmul_rn(reinterpret_cast<const float *>(slots)[0], scale);
-    for (int g = lane; g < ng; g += 32) {
-        float4 v = slots[g];
-        v.x = __fmul_rn(v.x, scale); v.y = __fmul_rn(v.y, scale);
-        v.z = __fmul_rn(v.z, scale); v.w = __fmul_rn(v.w, scale);
-        const int j = 4 * g;
-        if (j < nr) m = max_nan2(m, v.x);
+    for (int g = lane; g < nfull; g += 32) {
+        const float4 v = scaled4(slots[g], sc2);
+        m = max_nan2(m, max_nan2(max_nan2(v.x, v.y), max_nan2(v.z, v.w)));
+    }
+    if (nfull < ng && lane == (nfull & 31)) {
+        const float4 v = scaled4(slots[nfull], sc2);
+        const int64_t j = 4 * int64_t(nfull);
+        m = max_nan2(m, v.x);
         if (j + 1 < nr) m = max_nan2(m, v.y);
         if (j + 2 < nr) m = max_nan2(m, v.z);
-        if (j + 3 < nr) m = max_nan2(m, v.w);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
         m = max_nan2(m, __shfl_xor_sync(0xffffffffu, m, off));
-    const bool finite = fabsf(m) <= 0x1.fffffep127f;
+    // pass 2a: e = exp(x - m) in place for every group (a partial group's
+    // other columns are formed too and never used)
+    if (fabsf(m) <= 0x1.fffffep127f) {
+        int g = lane;
+        for (; g + 96 < ng; g += 128) {
+            const float4 v0 = scaled4(slots[g], sc2), v1 = scaled4(slots[g + 32], sc2);
+            const float4 v2 = scaled4(slots[g + 64], sc2), v3 = scaled4(slots[g + 96], sc2);
+            slots[g] = exp4(v0, m);
+            slots[g + 32] = exp4(v1, m);
+            slots[g + 64] = exp4(v2, m);
+            slots[g + 96] = exp4(v3, m);
+        }
+        for (; g < ng; g += 32) slots[g] = exp4(scaled4(slots[g], sc2), m);
+    } else {
+        for (int g = lane; g < ng; g += 32) {
+            const float4 v = scaled4(slots[g], sc2);
+            slots[g] = make_float4(det_exp_call(__fsub_rn(v.x, m)), det_exp_call(__fsub_rn(v.y, m)),
+                                   det_exp_call(__fsub_rn(v.z, m)),
+                                   det_exp_call(__fsub_rn(v.w, m)));
+        }
+    }
+    // pass 2b: chain lane + 32 w adds groups lane + 32 w + 256 sg, sg ascending
     float c[8];
 #pragma unroll
     for (int w = 0; w < 8; ++w) c[w] = 0.0f;
-    // chain lane + 32 w adds groups lane + 32 w + 256 sg, sg ascending
-    for (int sg = 0; 256 * sg < ng; ++sg)
+    int sg = 0;
+    for (; 256 * sg + 255 < nfull; ++sg)
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const float4 e = slots[lane + 32 * w + 256 * sg];
+            c[w] = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(c[w], e.x), e.y), e.z), e.w);
+        }
+    for (; 256 * sg < ng; ++sg)
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
             const int g = lane + 32 * w + 256 * sg;
             if (g >= ng) continue;
-            float4 v = slots[g];
-            v.x = __fmul_rn(v.x, scale); v.y = __fmul_rn(v.y, scale);
-            v.z = __fmul_rn(v.z, scale); v.w = __fmul_rn(v.w, scale);
-            const float4 e = finite ? exp4(v, m)
-                                    : make_float4(det_exp_call(__fsub_rn(v.x, m)),
-                                                  det_exp_call(__fsub_rn(v.y, m)),
-                                                  det_exp_call(__fsub_rn(v.z, m)),
-                                                  det_exp_call(__fsub_rn(v.w, m)));
-            slots[g] = e;
-            const int j = 4 * g;
-            if (j < nr) c[w] = __fadd_rn(c[w], e.x);
+            const float4 e = slots[g];
+            const int64_t j = 4 * int64_t(g);
+            c[w] = __fadd_rn(c[w], e.x);
             if (j + 1 < nr) c[w] = __fadd_rn(c[w], e.y);
             if (j + 2 < nr) c[w] = __fadd_rn(c[w], e.z);
             if (j + 3 < nr) c[w] = __fadd_rn(c[w], e.w);
         }
-    const float inv = __fdiv_rn(1.0f, fold_chains(c));
-    for (int g = lane; g < ng; g += 32) {
-        const float4 e = slots[g];
-        st4_kept(pr, 4 * int64_t(g), nr, vec_p,
-                 make_float4(__fmul_rn(e.x, inv), __fmul_rn(e.y, inv), __fmul_rn(e.z, inv),
-                             __fmul_rn(e.w, inv)));
-    }
+    const f32x2 inv2 = splat2(__fdiv_rn(1.0f, fold_chains(c)));
+    // pass 3: p = e * (1 / S)
+    for (int g = lane; g < ng; g += 32)
+        st4_kept(pr, 4 * int64_t(g), nr, vec_p, scaled4(slots[g], inv2));
 }
 
 // The causal softmax for rows of at most kSmaxStage columns, 16-byte aligned

@@ -104,6 +104,11 @@ const char *det_status_string(int status);
  *   bytes, every output's chunks are computed by one thread from A in place.
  *   The result bits are the same either way; only the speed differs. Calls
  *   that share a workspace must be ordered (one stream).
+ * Speed: the kernel stages A and B by TMA when each is 16-byte aligned with a
+ *   row stride that is a multiple of 4 floats; otherwise it stages them with
+ *   plain loads, about four times slower (same bits). A k-contiguous A read
+ *   through its transposed copy needs only the copy aligned. Pad rows that
+ *   would miss this (a 50,257-wide logits row to a stride of 50,260).
  *
  * Errors: DET_ERR_INVALID_ARG for negative sizes, a dimension >= 2^31, an ld
  * below its row length or null pointers with nonzero sizes. A TMA wait that

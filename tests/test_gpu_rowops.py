@@ -93,7 +93,7 @@ def test_rmsnorm_dependent_launches_in_a_chain(dev):
 
 # ----------------------------------------------------------------- cross-entropy
 @pytest.mark.parametrize("rows,V", [(1, 1), (3, 2), (5, 5), (4, 255), (7, 1024),
-                                    (6, 1025), (3, 50257)])
+                                    (6, 1025), (5, 1601), (3, 7777), (3, 50257)])
 @pytest.mark.parametrize("layout", ["dense", "offset"])
 def test_xent_shapes(dev, rows, V, layout):
     rng = np.random.default_rng(rows * 7919 + V)
