@@ -47,6 +47,8 @@ struct GemmPlan {
     size_t copy_bytes;     // the copy's share of the workspace (first)
     size_t split_bytes;    // the split partials' share (after the copy)
     size_t workspace_bytes;
+    int64_t head_rows;     // > 0: rows [0, head_rows) as an unsplit launch of their
+                           // own, the rest as a product with its own plan
 };
 // a_kmajor: op(A) is k-contiguous (transA == 0), the layout a copy can help;
 // b_kmajor: op(B) is k-contiguous (transB != 0), or -1 for a plan that never

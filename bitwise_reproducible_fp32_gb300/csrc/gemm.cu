@@ -1268,7 +1268,38 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor, int 
             pl.split_bytes = pl.workspace_bytes = size_t(ws);
         }
     }
-    if (!pl.split) consider_transpose();
+    // Unsplit head rows: where a split plan is chosen but the tiles fill the
+    // SMs less than twice over, the first row blocks that make one round (at
+    // most a tile an SM) run unsplit in a launch of their own, and only the
+    // tiles after them are split by their own plan, so only their partials
+    // cross HBM. Same bits: every output's chunks and their left-to-right sum
+    // are the same whichever launch computes them.
+    auto consider_head = [&] {
+        const int64_t nt = (N + BN - 1) / BN, mt = (M + BM - 1) / BM;
+        const int64_t mb1 = int64_t(sms) / nt;
+        if (!pl.split || T >= 2 * int64_t(sms) || mb1 < 1 || mb1 >= mt) return;
+        const int64_t M1 = mb1 * BM;
+        const GemmPlan tail = gemm_plan(M - M1, N, K, sms, false, -1);
+        const int64_t T2 = (mt - mb1) * nt;
+        double tail_cost = launch_s;
+        if (tail.split) {
+            const int64_t G = tail.kt_per_unit / TILES_PER_CHUNK;
+            tail_cost += busiest_cta_steps(T2, tail.units_per_tile, G, nkt, sms) * kt_step_s +
+                         (2.0 * double(tail.split_bytes) + double(M - M1) * double(N) * 4.0) /
+                             hbm_bps + launch_s;
+        } else {
+            tail_cost += busiest_cta_steps(T2, 1, nchunks, nkt, sms) * kt_step_s;
+        }
+        const double cost = double(nkt) * kt_step_s + launch_s + tail_cost;
+        if (cost < 0.97 * best) {
+            best = cost;
+            pl.head_rows = M1;
+            pl.split_bytes = pl.workspace_bytes = tail.workspace_bytes;
+            if (!tail.split) pl.split = 0;
+        }
+    };
+    consider_head();
+    if (!pl.split && !pl.head_rows) consider_transpose();
     else consider_split_copy();
     return pl;
 }
@@ -1279,12 +1310,14 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor, int 
 GemmPlan gemm_plan_for(const GemmArgs &a, int sms, const void *ws, size_t workspace_bytes) {
     GemmPlan pl = gemm_plan(a.M, a.N, a.K, sms, !a.transA, a.transB ? 1 : 0);
     const bool usable = ws != nullptr && reinterpret_cast<uintptr_t>(ws) % 16 == 0;
-    if (pl.split && pl.transpose_a && (!usable || workspace_bytes < pl.workspace_bytes)) {
+    if ((pl.split || pl.head_rows) && pl.transpose_a &&
+        (!usable || workspace_bytes < pl.workspace_bytes)) {
         pl.transpose_a = 0;
         pl.copy_bytes = 0;
         pl.workspace_bytes = pl.split_bytes;
     }
-    if ((pl.split || pl.transpose_a) && (!usable || workspace_bytes < pl.workspace_bytes)) {
+    if ((pl.split || pl.transpose_a || pl.head_rows) &&
+        (!usable || workspace_bytes < pl.workspace_bytes)) {
         const int nchunks = pl.nchunks;
         pl = GemmPlan{};          // no usable workspace: one unit per tile
         pl.units_per_tile = 1;
@@ -1292,6 +1325,25 @@ GemmPlan gemm_plan_for(const GemmArgs &a, int sms, const void *ws, size_t worksp
         pl.nchunks = nchunks;
     }
     return pl;
+}
+
+// The two products of a plan with head rows: rows [0, head_rows) and the rest.
+void head_and_tail(const GemmArgs &a, int64_t head_rows, GemmArgs *h, GemmArgs *t) {
+    *h = a;
+    *t = a;
+    h->M = head_rows;
+    t->M = a.M - head_rows;
+    t->A = a.transA ? a.A + head_rows : a.A + head_rows * a.lda;
+    t->C = a.C + head_rows * a.ldc;
+}
+
+// The transA form of a over its K x M copy T (row stride transposed_ld(M)).
+GemmArgs over_copy(const GemmArgs &a, const float *T) {
+    GemmArgs t = a;
+    t.A = T;
+    t.lda = transposed_ld(a.M);
+    t.transA = 1;
+    return t;
 }
 
 int64_t gemm_launches(const GemmArgs &a, size_t workspace_bytes) {
@@ -1302,7 +1354,16 @@ int64_t gemm_launches(const GemmArgs &a, size_t workspace_bytes) {
                                       workspace_bytes ? reinterpret_cast<const void *>(256)
                                                       : nullptr,
                                       workspace_bytes);
-    return 1 + int64_t(pl.transpose_a) + int64_t(pl.split);
+    // as launch_gemm runs the plan
+    if (pl.transpose_a)
+        return 1 + gemm_launches(over_copy(a, a.A),
+                                 pl.split || pl.head_rows ? workspace_bytes - pl.copy_bytes : 0);
+    if (pl.head_rows) {
+        GemmArgs h, t;
+        head_and_tail(a, pl.head_rows, &h, &t);
+        return gemm_launches(h, 0) + gemm_launches(t, workspace_bytes);
+    }
+    return 1 + int64_t(pl.split);
 }
 
 namespace {
@@ -1379,16 +1440,20 @@ cudaError_t launch_gemm(const GemmArgs &a, void *workspace, size_t workspace_byt
         // op(A) from the K x M copy: the transA form of the same product, its
         // split partials (if any) in the workspace after the copy
         float *T = static_cast<float *>(workspace);
-        const int64_t ldt = transposed_ld(a.M);
-        cudaError_t e = launch_transpose(a.A, a.lda, a.M, a.K, T, ldt, sms, s);
+        cudaError_t e = launch_transpose(a.A, a.lda, a.M, a.K, T, transposed_ld(a.M), sms, s);
         if (e != cudaSuccess) return e;
-        GemmArgs t = a;
-        t.A = T;
-        t.lda = ldt;
-        t.transA = 1;
-        if (!pl.split) return launch_gemm(t, nullptr, 0, s);
+        const GemmArgs t = over_copy(a, T);
+        if (!pl.split && !pl.head_rows) return launch_gemm(t, nullptr, 0, s);
         return launch_gemm(t, static_cast<char *>(workspace) + pl.copy_bytes,
                            workspace_bytes - pl.copy_bytes, s);
+    }
+    if (pl.head_rows) {
+        // the head unsplit (no workspace), then the rest with its own plan
+        GemmArgs h, t;
+        head_and_tail(a, pl.head_rows, &h, &t);
+        cudaError_t e = launch_gemm(h, nullptr, 0, s);
+        if (e != cudaSuccess) return e;
+        return launch_gemm(t, workspace, workspace_bytes, s);
     }
     const Prepared x = prepare(a, pl, workspace);
     cudaError_t e = launch_prepared(x, nullptr, s);

@@ -220,8 +220,9 @@ det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA, int t
                                    int64_t M, int64_t N, int64_t K, size_t *bytes);
 
 /* The number of kernels detgemm_f32 launches for this shape and layout with a
- * workspace of workspace_bytes (1 to 3: the transposed copy of A, the GEMM,
- * the split-K second pass), written to *launches, for callers that count or
+ * workspace of workspace_bytes (1 to 4: the transposed copy of A; the GEMM,
+ * or the GEMM of the first rows unsplit and then of the rest; the split-K
+ * second pass), written to *launches, for callers that count or
  * capture launches. Same argument rules; host-only apart from reading the
  * device's SM count. */
 det_status detgemm_launches(const det_profile_v1 *prof, int transA, int transB, int64_t M,

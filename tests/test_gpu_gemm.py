@@ -186,6 +186,37 @@ def test_cfg3_full_size_sampled(dev):
         del C
 
 
+@pytest.mark.parametrize("M,K,transA,transB", [(8000, 2048, 0, 1), (8192, 768, 0, 0),
+                                             (7937, 2304, 1, 1)])
+def test_unsplit_head_rows_and_split_tail(dev, M, K, transA, transB):
+    # 768-wide outputs over 8,000-odd rows fill the 152 SMs once and a little
+    # more: the first row blocks that make one round run unsplit in a launch
+    # of their own and only the rest is split (only its partials cross HBM);
+    # every output keeps detgemm_f32's bits, with or without the workspace,
+    # and with beta = 1
+    N = 768
+    rng = np.random.default_rng(M + K)
+    A = rng.standard_normal((K, M) if transA else (M, K)).astype(F)
+    B = rng.standard_normal((N, K) if transB else (K, N)).astype(F)
+    wsn = detlib.detgemm_workspace_bytes(M, N, K, bool(transA), bool(transB))
+    split_alone = detlib.detgemm_launches(M, N, K, bool(transA), bool(transB), wsn)
+    assert split_alone >= 3                  # head, tail and its split pass
+    ws = detlib.gemm_workspace(M, N, K, bool(transA), bool(transB))
+    Ad, Bd = to_dev(A, "padded"), to_dev(B, "padded")
+    C = detlib.detgemm_f32(Ad, Bd, transA=bool(transA), transB=bool(transB), workspace=ws)
+    C2 = detlib.detgemm_f32(Ad, Bd, transA=bool(transA), transB=bool(transB))
+    assert_bitwise(host(C2), host(C), "with vs without workspace")
+    rows = np.array(sorted({0, 255, 256, 6143, 6144, 6399, 6400, 6401, 7423, M - 257, M - 1} |
+                           set(np.random.default_rng(5).choice(M, 12, replace=False).tolist())))
+    Asub = np.ascontiguousarray(A[:, rows] if transA else A[rows])
+    want = oracle.gemm(Asub, B, transA=bool(transA), transB=bool(transB))
+    assert_bitwise(host(C[torch.as_tensor(rows, device="cuda")]), want, "sampled rows")
+    C0 = rng.standard_normal((M, N)).astype(F)
+    Cacc = to_dev(C0)
+    detlib.detgemm_acc_f32(Ad, Bd, Cacc, transA=bool(transA), transB=bool(transB), workspace=ws)
+    assert_bitwise(host(Cacc)[rows], oracle.add(C0[rows], want), "accumulate")
+
+
 def test_cfg5_dw_full_size_sampled(dev):
     for p in inputs.dw_cfg5():
         M, N, K = p["A"].shape[1], p["B"].shape[1], p["A"].shape[0]
