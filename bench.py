@@ -422,7 +422,7 @@ def run_ours(args, rank, world, local_rank):
     hd_b = bl["d"] // bl["heads"]
     attn_b = detlib.detattention_launches(bl["batch"], bl["seq"], bl["heads"], hd_b)
     attn_b_bwd = detlib.detattention_launches(bl["batch"], bl["seq"], bl["heads"], hd_b,
-                                              backward=True)
+                                              backward=True, saved=True)
     ntok_b, d_b, f_b = bl["batch"] * bl["seq"], bl["d"], bl["dff"]
 
     def dw_n(M, N):
@@ -460,7 +460,7 @@ def run_ours(args, rank, world, local_rank):
     def dw_m(M, N):
         return planned_n(M, N, dm_ntok, True, False)
     attn_m_bwd = detlib.detattention_launches(dm["batch"], dm["seq"], dm["heads"],
-                                              d_m // dm["heads"], backward=True)
+                                              d_m // dm["heads"], backward=True, saved=True)
     blk_dw_m = (dw_m(f_m, d_m) + pair_n(d_m, f_m, f_m, dm_ntok, True) + dw_m(d_m, d_m)
                 + dw_m(d_m, 3 * d_m))
     train_launches = (decoder_launches

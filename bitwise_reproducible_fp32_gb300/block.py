@@ -135,7 +135,9 @@ class Block:
         # x1 = x + att W_o
         d_att = tB(dx1, w["W_o"])
         g["W_o"] = tA(self.att, dx1)
-        dqkv = L.detattention_bwd_f32(self.qkv, d_att, self.B, self.T, self.H, self.hd)
+        # P from the forward (still in this block's attention workspace)
+        dqkv = L.detattention_bwd_saved_f32(self.qkv, d_att, self.B, self.T, self.H, self.hd,
+                                            self.att_ws)
         L.detrope_bwd_f32(dqkv, heads=2 * self.H, head_dim=self.hd, seq_len=self.T,
                           theta=self.theta)
         dh = tB(dqkv, w["W_qkv"])

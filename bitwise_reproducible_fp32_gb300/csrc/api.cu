@@ -624,6 +624,13 @@ DET_API det_status detattention_launches(const det_profile_v1 *prof, int64_t bat
     // dO copies (long sequences), then S, the softmax, dP, the counts of dO's,
     // K's and Q's non-finite values, dV, the softmax backward, dQ and dK
     const int64_t copies = attn_qt_bytes(batch, seq, heads, head_dim) ? 1 : 0;
+    if (backward == 2 && groups == 1) {
+        // detattention_bwd_saved_f32 with the forward's P: the dO copy, the
+        // counts, the +0 fill past the chunks (when dO is not finite), dP, dV,
+        // the softmax backward, dQ and dK
+        *launches = 9 + copies;
+        return DET_OK;
+    }
     *launches = backward ? 10 * groups + 2 * copies : 4 * groups + copies;
     return DET_OK;
 }
@@ -698,12 +705,15 @@ DET_API det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, 
     return DET_OK;
 }
 
-DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
-                                        int64_t heads, int64_t head_dim, const float *qkv,
-                                        int64_t ldqkv, const float *dout, int64_t lddout,
-                                        float scale, float *dqkv, int64_t lddqkv,
-                                        void *workspace, size_t workspace_bytes,
-                                        det_stream_t stream) {
+namespace {
+// The backward of detattention_f32 (detattention_bwd_f32's operation); with
+// Psaved (the forward's workspace, all heads in one group) P is read from it
+// instead of recomputed.
+det_status attention_bwd(const det_profile_v1 *prof, int64_t batch, int64_t seq, int64_t heads,
+                         int64_t head_dim, const float *qkv, int64_t ldqkv, const float *dout,
+                         int64_t lddout, float scale, float *Psaved, float *dqkv,
+                         int64_t lddqkv, void *workspace, size_t workspace_bytes,
+                         det_stream_t stream) {
     det_status st = check_profile(prof);
     if (st != DET_OK) return st;
     if (!attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
@@ -718,7 +728,9 @@ DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batc
         workspace_bytes < 2 * g.score_bytes + kAttnFlagBytes + 2 * qt_bytes ||
         reinterpret_cast<uintptr_t>(workspace) % 256)
         return DET_ERR_WORKSPACE;
-    float *Pb = static_cast<float *>(workspace);
+    // the forward's P covers every head only when they ran as one group
+    const bool saved = Psaved != nullptr && g.gb >= batch && g.gh >= heads;
+    float *Pb = saved ? Psaved : static_cast<float *>(workspace);
     float *dPb = reinterpret_cast<float *>(static_cast<char *>(workspace) + g.score_bytes);
     int *flags = reinterpret_cast<int *>(static_cast<char *>(workspace) + 2 * g.score_bytes);
     // long sequences: the score products read Q and dO from transposed copies
@@ -732,7 +744,7 @@ DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batc
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if (QT) {
-        e = launch_transpose_copy(qkv, ldqkv, batch * seq, hd, QT, ldt, s);
+        if (!saved) e = launch_transpose_copy(qkv, ldqkv, batch * seq, hd, QT, ldt, s);
         if (e == cudaSuccess) e = launch_transpose_copy(dout, lddout, batch * seq, hd, dOT, ldt, s);
     }
     if (e == cudaSuccess) e = for_each_group(batch, heads, g, [&](int64_t b0, int64_t nb,
@@ -749,17 +761,28 @@ DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batc
             dOT ? q_from_copy(dOT, ldt, batch, seq, hd, b0, h0, head_dim) : dO;
         float *dbase = dqkv + b0 * seq * lddqkv + h0 * head_dim;
         const int64_t dzb = seq * lddqkv;
-        cudaError_t r = group_gemm(seq, seq, head_dim, Qs, QT ? 1 : 0, K, 1, Pb, seq, P.zb,
-                                   P.zh, count, nh, 1, s);
-        if (r == cudaSuccess)
-            r = launch_softmax_causal(count * seq, seq, Pb, seq, scale, 0, seq, Pb, seq, s);
-        if (r == cudaSuccess)
-            r = group_gemm(seq, seq, head_dim, dOs, dOT ? 1 : 0, V, 1, dPb, seq, dP.zb, dP.zh,
-                           count, nh, 1, s);
         // P and dS are +0 above the diagonal, so P^T and dS^T below it: with
         // finite dO, K and Q (flags 0, 1, 2) the chunks there are skipped
         const HeadOperand finite[3] = {dO, K, Q};
-        if (r == cudaSuccess) r = count_nonfinite_heads(flags, finite, 3, nb * seq, nh * head_dim, s);
+        cudaError_t r = cudaSuccess;
+        if (saved) {
+            // the forward wrote P's +0 columns up to the end of each row's
+            // 256-row block (when its V was finite); dV reads past that only
+            // when dO is not finite, and then this fills the rest with +0
+            r = count_nonfinite_heads(flags, finite, 3, nb * seq, nh * head_dim, s);
+            if (r == cudaSuccess)
+                r = launch_zero_past_chunks(count * seq, seq, seq, Pb, seq, flags, s);
+        } else {
+            r = group_gemm(seq, seq, head_dim, Qs, QT ? 1 : 0, K, 1, Pb, seq, P.zb, P.zh, count,
+                           nh, 1, s);
+            if (r == cudaSuccess)
+                r = launch_softmax_causal(count * seq, seq, Pb, seq, scale, 0, seq, Pb, seq, s);
+        }
+        if (r == cudaSuccess)
+            r = group_gemm(seq, seq, head_dim, dOs, dOT ? 1 : 0, V, 1, dPb, seq, dP.zb, dP.zh,
+                           count, nh, 1, s);
+        if (r == cudaSuccess && !saved)
+            r = count_nonfinite_heads(flags, finite, 3, nb * seq, nh * head_dim, s);
         if (r == cudaSuccess)   // dV = P^T dO
             r = group_gemm(seq, head_dim, seq, P, 1, dO, 0, dbase + 2 * hd, lddqkv, dzb,
                            head_dim, count, nh, 0, s, 2, flags);
@@ -770,11 +793,45 @@ DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batc
             r = group_gemm(seq, head_dim, seq, dP, 0, K, 0, dbase, lddqkv, dzb, head_dim, count,
                            nh, 0, s, 1, flags + 1);
         if (r == cudaSuccess)   // dK = dS^T Q
-            r = group_gemm(seq, head_dim, seq, dP, 1, Q, 0, dbase + hd, lddqkv, dzb, head_dim,
-                           count, nh, 0, s, 2, flags + 2);
+            r = group_gemm(seq, head_dim, seq, dP, 1, Q, 0, dbase + hd, lddqkv, dzb,
+                           head_dim, count, nh, 0, s, 2, flags + 2);
         return r;
     });
     return from_cuda(e);
+}
+}  // namespace
+
+DET_API det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
+                                        int64_t heads, int64_t head_dim, const float *qkv,
+                                        int64_t ldqkv, const float *dout, int64_t lddout,
+                                        float scale, float *dqkv, int64_t lddqkv,
+                                        void *workspace, size_t workspace_bytes,
+                                        det_stream_t stream) {
+    return attention_bwd(prof, batch, seq, heads, head_dim, qkv, ldqkv, dout, lddout, scale,
+                         nullptr, dqkv, lddqkv, workspace, workspace_bytes, stream);
+}
+
+DET_API det_status detattention_bwd_saved_f32(const det_profile_v1 *prof, int64_t batch,
+                                              int64_t seq, int64_t heads, int64_t head_dim,
+                                              const float *qkv, int64_t ldqkv, const float *dout,
+                                              int64_t lddout, float scale, void *fwd_workspace,
+                                              size_t fwd_workspace_bytes, float *dqkv,
+                                              int64_t lddqkv, void *workspace,
+                                              size_t workspace_bytes, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (!attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
+    if (batch == 0) return DET_OK;
+    // the forward's workspace as detattention_f32 lays it out: the group's
+    // P first
+    const AttnGroups g = attention_groups(batch, seq, heads);
+    if (!fwd_workspace || reinterpret_cast<uintptr_t>(fwd_workspace) % 256 ||
+        fwd_workspace_bytes < g.score_bytes + kAttnFlagBytes +
+                                  attn_qt_bytes(batch, seq, heads, head_dim))
+        return DET_ERR_WORKSPACE;
+    return attention_bwd(prof, batch, seq, heads, head_dim, qkv, ldqkv, dout, lddout, scale,
+                         static_cast<float *>(fwd_workspace), dqkv, lddqkv, workspace,
+                         workspace_bytes, stream);
 }
 
 DET_API det_status detshardsum_f32(const det_profile_v1 *prof, int64_t nshards, int64_t n,

@@ -577,6 +577,22 @@ __global__ void __launch_bounds__(32 * kSmaxWarps)
     }
 }
 
+// +0 in columns chunk_end .. cols-1 of each row, chunk_end the end of the
+// row's 256-row block of queries (what a softmax given chunk_zeros left
+// unwritten), when *flag is not 0; nothing otherwise (the kernel reads the
+// flag first). A warp a row.
+__global__ void __launch_bounds__(256)
+    zero_past_chunks_kernel(int64_t rows, int64_t cols, int64_t period, float *p, int64_t ld,
+                            const int *flag, int vec) {
+    if (*flag == 0) return;
+    const int lane = threadIdx.x & 31;
+    for (int64_t r = blockIdx.x * 8 + (threadIdx.x >> 5); r < rows;
+         r += int64_t(gridDim.x) * 8) {
+        const int64_t chunk_end = ((r % period) / kKChunk + 1) * kKChunk;
+        if (chunk_end < cols) zero_masked(p + r * ld, chunk_end, cols, lane, vec);
+    }
+}
+
 // Counts the non-finite values of a rows x cols block (row stride ld) into
 // *bad: a warp a row, one atomic add a warp that saw any.
 __global__ void __launch_bounds__(256)
@@ -791,6 +807,15 @@ cudaError_t launch_softmax_causal_bwd(int64_t rows, int64_t cols, const float *p
     const int vec_in = al16(p) && al16(dp) && ld % 4 == 0, vec_out = al16(ds) && ldd % 4 == 0;
     softmax_causal_bwd_kernel<<<unsigned(blocks), 32 * kSmaxWarps, 0, s>>>(
         rows, cols, p, dp, ld, scale, diag, period, ds, ldd, vec_in, vec_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero_past_chunks(int64_t rows, int64_t cols, int64_t period, float *p,
+                                   int64_t ld, const int *flag, cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((rows + 7) / 8, int64_t(sm_count_current_device()) * 8);
+    const int vec = al16(p) && ld % 4 == 0;
+    zero_past_chunks_kernel<<<unsigned(blocks), 256, 0, s>>>(rows, cols, period, p, ld, flag, vec);
     return cudaGetLastError();
 }
 

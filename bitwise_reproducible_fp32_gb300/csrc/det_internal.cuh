@@ -93,6 +93,11 @@ struct GemmBatch {
 };
 // Counts into *bad (atomically) the non-finite values of a rows x cols block
 // at base (row stride ld). *bad must be zeroed before.
+// +0 in each row's columns from the end of its 256-row block of queries on
+// (what launch_softmax_causal with chunk_zeros left unwritten), only when
+// *flag (device) is not 0.
+cudaError_t launch_zero_past_chunks(int64_t rows, int64_t cols, int64_t period, float *p,
+                                   int64_t ld, const int *flag, cudaStream_t s);
 cudaError_t launch_count_nonfinite(int64_t rows, int64_t cols, const float *base, int64_t ld,
                                    int *bad, cudaStream_t s);
 cudaError_t launch_gemm_batched(const GemmArgs &a, const GemmBatch &bt, cudaStream_t s);

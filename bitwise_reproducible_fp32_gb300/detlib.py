@@ -113,6 +113,9 @@ SIGNATURES = [
                                     _vp, _i64, _vp, ctypes.c_size_t, _vp]),
     ("detattention_bwd_workspace_bytes", _int, [_PROF, _i64, _i64, _i64, _i64,
                                                 ctypes.POINTER(ctypes.c_size_t)]),
+    ("detattention_bwd_saved_f32", _int, [_PROF, _i64, _i64, _i64, _i64, _vp, _i64, _vp,
+                                          _i64, _f, _vp, ctypes.c_size_t, _vp, _i64, _vp,
+                                          ctypes.c_size_t, _vp]),
     ("det_watchdog_status", _int, [ctypes.POINTER(ctypes.c_int32), _int]),
 ]
 
@@ -549,13 +552,15 @@ def detattention_workspace_bytes(batch, seq, heads, head_dim, profile=None) -> i
     return n.value
 
 
-def detattention_launches(batch, seq, heads, head_dim, backward=False, profile=None) -> int:
-    """Kernel launches detattention_f32 (or, backward=True, detattention_bwd_f32)
-    makes for these sizes."""
+def detattention_launches(batch, seq, heads, head_dim, backward=False, saved=False,
+                          profile=None) -> int:
+    """Kernel launches detattention_f32 (or, backward=True, detattention_bwd_f32;
+    with saved=True as well, detattention_bwd_saved_f32) makes for these sizes."""
     n = ctypes.c_int64()
+    mode = (2 if saved else 1) if backward else 0
     _check("detattention_launches",
            load().detattention_launches(_prof(profile), batch, seq, heads, head_dim,
-                                        int(bool(backward)), ctypes.byref(n)))
+                                        mode, ctypes.byref(n)))
     return n.value
 
 
@@ -670,6 +675,32 @@ def detattention_bwd_f32(qkv, dout, batch, seq, heads, head_dim, scale=None, dqk
                                      _ptr(dqkv), _ld(dqkv), _ptr(workspace),
                                      workspace.numel() * 4, _stream(stream))
     _check("detattention_bwd_f32", st)
+    return dqkv
+
+
+def detattention_bwd_saved_f32(qkv, dout, batch, seq, heads, head_dim, fwd_workspace,
+                               scale=None, dqkv=None, workspace=None, profile=None,
+                               stream=None):
+    """detattention_bwd_f32 reading P from fwd_workspace, the workspace of the
+    detattention_f32 call on the same qkv (unchanged since). Returns dqkv."""
+    import torch
+    _cuda_f32(qkv, "qkv", 2)
+    _cuda_f32(dout, "dout", 2)
+    dqkv = torch.empty_like(qkv) if dqkv is None else dqkv
+    _cuda_f32(dqkv, "dqkv", 2)
+    if scale is None:
+        scale = 1.0 / float(head_dim) ** 0.5
+    if workspace is None:
+        workspace = torch.empty(
+            (detattention_bwd_workspace_bytes(batch, seq, heads, head_dim, profile) + 3) // 4,
+            dtype=torch.float32, device=qkv.device)
+    st = load().detattention_bwd_saved_f32(_prof(profile), batch, seq, heads, head_dim,
+                                           _ptr(qkv), _ld(qkv), _ptr(dout), _ld(dout),
+                                           ctypes.c_float(scale), _ptr(fwd_workspace),
+                                           fwd_workspace.numel() * fwd_workspace.element_size(),
+                                           _ptr(dqkv), _ld(dqkv), _ptr(workspace),
+                                           workspace.numel() * 4, _stream(stream))
+    _check("detattention_bwd_saved_f32", st)
     return dqkv
 
 

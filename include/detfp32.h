@@ -511,9 +511,10 @@ det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, int64_t s
 det_status detattention_workspace_bytes(const det_profile_v1 *prof, int64_t batch,
                                         int64_t seq, int64_t heads, int64_t head_dim,
                                         size_t *bytes);
-/* The number of kernels detattention_f32 (backward 0) or detattention_bwd_f32
- * (backward 1) launches for these sizes, written to *launches (for callers
- * that count or capture launches). Same argument rules; host-only. */
+/* The number of kernels detattention_f32 (backward 0), detattention_bwd_f32
+ * (backward 1) or detattention_bwd_saved_f32 (backward 2) launches for these
+ * sizes, written to *launches (for callers that count or capture launches).
+ * Same argument rules; host-only. */
 det_status detattention_launches(const det_profile_v1 *prof, int64_t batch, int64_t seq,
                                  int64_t heads, int64_t head_dim, int backward,
                                  int64_t *launches);
@@ -578,6 +579,28 @@ det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batch, int64
 det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t batch,
                                             int64_t seq, int64_t heads, int64_t head_dim,
                                             size_t *bytes);
+
+/* detattention_bwd_f32, reading P from the forward instead of recomputing it.
+ * fwd_workspace / fwd_workspace_bytes: the workspace of the detattention_f32
+ * call that read the same qkv with the same batch, seq, heads, head_dim and
+ * scale, with nothing written to it since. When that call ran every head as
+ * one group (its score buffers fit the 1 GiB cap; detattention_launches then
+ * reports 4 or 5), the workspace still holds P for every head, and the
+ * backward skips S = Q K^T and the softmax; otherwise it recomputes them as
+ * detattention_bwd_f32 does. The results are the same bits either way (P is
+ * the same function of the same inputs). The forward wrote P's +0 columns up
+ * to the end of each row's 256-row block when its V was finite; when dout is
+ * not finite, the backward first fills the rest of those rows with +0 in
+ * fwd_workspace, which it may therefore write. workspace: at least
+ * detattention_bwd_workspace_bytes. Errors as detattention_bwd_f32, and
+ * DET_ERR_WORKSPACE for a null, misaligned or short fwd_workspace. */
+det_status detattention_bwd_saved_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
+                                      int64_t heads, int64_t head_dim, const float *qkv,
+                                      int64_t ldqkv, const float *dout, int64_t lddout,
+                                      float scale, void *fwd_workspace,
+                                      size_t fwd_workspace_bytes, float *dqkv, int64_t lddqkv,
+                                      void *workspace, size_t workspace_bytes,
+                                      det_stream_t stream);
 
 /* Reads, and optionally clears, the current device's watchdog word.
  * *code == 0 means no bounded device wait has ever given up; otherwise bit k

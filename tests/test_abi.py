@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
                  "detattention_f32", "detattention_workspace_bytes", "detembedding_f32",
                  "detswiglu_bwd_f32", "detsoftmax_causal_bwd_f32", "detrope_bwd_f32",
                  "detembedding_bwd_f32", "detattention_bwd_f32",
-                 "detattention_bwd_workspace_bytes",
+                 "detattention_bwd_workspace_bytes", "detattention_bwd_saved_f32",
                  "detexp_f32", "detlog_f32", "det_adamw_bias_correction",
                  "det_profile_default",
                  "det_status_string", "det_watchdog_status"):
@@ -192,6 +192,15 @@ def test_bad_arguments_are_refused_on_the_host(lib):
     assert k.value == 12
     assert lib.detattention_launches(p, 16, 128, 4, 16, 1, ctypes.byref(k)) == 0
     assert k.value == 10
+    # the backward with the forward's P (one group): no S, no softmax, one +0
+    # fill; the dO copy from 512 tokens
+    assert lib.detattention_launches(p, 4, 2048, 12, 64, 2, ctypes.byref(k)) == 0
+    assert k.value == 10
+    assert lib.detattention_launches(p, 16, 128, 4, 16, 2, ctypes.byref(k)) == 0
+    assert k.value == 9
+    # several groups: P is not all in the forward's workspace, so it recomputes
+    assert lib.detattention_launches(p, 8, 8192, 12, 64, 2, ctypes.byref(k)) == 0
+    assert k.value == 8 * 3 * 10 + 2
     assert lib.detattention_launches(p, 16, 128, 4, 16, 0, ctypes.byref(k)) == 0
     assert k.value == 4
     assert lib.detattention_launches(p, 8, 8192, 12, 64, 0, ctypes.byref(k)) == 0
@@ -211,6 +220,10 @@ def test_bad_arguments_are_refused_on_the_host(lib):
     assert lib.detembedding_bwd_f32(p, 4, 8, dummy, dummy, 8, 10, dummy, 7, null) == 1
     assert lib.detattention_bwd_f32(p, 1, 16, 2, 8, dummy, 48, dummy, 16, one, dummy, 47,
                                     dummy, 1 << 20, null) == 1
+    assert lib.detattention_bwd_saved_f32(p, 1, 16, 2, 8, dummy, 48, dummy, 16, one, null,
+                                          1 << 20, dummy, 48, dummy, 1 << 20, null) == 5
+    assert lib.detattention_bwd_saved_f32(p, 1, 16, 2, 8, dummy, 48, dummy, 16, one, dummy,
+                                          16, dummy, 48, dummy, 1 << 20, null) == 5
     hp = detlib.AdamWHP(1e-3, 0.9, 0.95, 1e-8, 0.1, 0)
     assert lib.detadamw_f32(p, 4, dummy, dummy, dummy, dummy, ctypes.byref(hp), null) == 1
     hp = detlib.AdamWHP(1e-3, 1.25, 0.95, 1e-8, 0.1, 3)              # beta outside [0, 1]

@@ -137,3 +137,41 @@ def test_attention_bwd(dev, B, T, H, d, checks, poison):
         assert_bitwise(got[r, h * d:(h + 1) * d], dQ, f"dQ b={b} h={h}")
         assert_bitwise(got[r, hd + h * d:hd + (h + 1) * d], dK, f"dK b={b} h={h}")
         assert_bitwise(got[r, 2 * hd + h * d:2 * hd + (h + 1) * d], dV, f"dV b={b} h={h}")
+
+
+@pytest.mark.parametrize("B,T,H,d,poison", [
+    (2, 100, 3, 16, None), (1, 600, 2, 16, None), (1, 600, 2, 16, "dout"),
+    (1, 600, 2, 16, "v"), (1, 600, 2, 16, "k"), (3, 513, 2, 32, None),
+    (4, 2048, 12, 64, None)])
+def test_attention_bwd_with_the_forwards_p(dev, B, T, H, d, poison):
+    # detattention_bwd_saved_f32 reads P from the forward's workspace instead
+    # of recomputing it: the same bits as detattention_bwd_f32. A non-finite
+    # dO makes dV take every chunk, so the rows' +0 columns past their chunk
+    # (which the forward leaves unwritten when V is finite) are filled first;
+    # a non-finite V makes the forward write them all
+    rng = np.random.default_rng(T * 3 + H)
+    qkv = rng.standard_normal((B * T, 3 * H * d)).astype(F)
+    dout = rng.standard_normal((B * T, H * d)).astype(F)
+    if poison == "dout":
+        dout[500, 3] = np.inf
+    elif poison == "v":
+        qkv[300, 2 * H * d + 5] = np.inf
+    elif poison == "k":
+        qkv[520, H * d + 2] = np.nan
+    qd, dod = to_dev(qkv), to_dev(dout)
+    fws = torch.empty((detlib.detattention_workspace_bytes(B, T, H, d) + 3) // 4,
+                      device="cuda").fill_(float("nan"))
+    detlib.detattention_f32(qd, B, T, H, d, workspace=fws)
+    got = host(detlib.detattention_bwd_saved_f32(qd, dod, B, T, H, d, fws))
+    want = host(detlib.detattention_bwd_f32(qd, dod, B, T, H, d))
+    assert_bitwise(got, want, "saved P against recomputed P")
+    scale = 1.0 / np.sqrt(d)
+    hd = H * d
+    for b, h in ([(0, 0), (B - 1, H - 1)] if T >= 2048 else [(0, 0), (B - 1, H - 1), (0, H - 1)]):
+        dQ, dK, dV = attention_bwd_oracle(qkv, dout, b, h, T, H, d, float(F(scale)))
+        r = slice(b * T, (b + 1) * T)
+        assert_bitwise(got[r, h * d:(h + 1) * d], dQ, f"dQ b={b} h={h}")
+        assert_bitwise(got[r, hd + h * d:hd + (h + 1) * d], dK, f"dK b={b} h={h}")
+        assert_bitwise(got[r, 2 * hd + h * d:2 * hd + (h + 1) * d], dV, f"dV b={b} h={h}")
+    assert detlib.det_watchdog_status() == 0
+
