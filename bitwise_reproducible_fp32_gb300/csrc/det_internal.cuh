@@ -49,6 +49,9 @@ struct GemmPlan {
     size_t workspace_bytes;
     int64_t head_rows;     // > 0: rows [0, head_rows) as an unsplit launch of their
                            // own, the rest as a product with its own plan
+    int transpose_b;       // 1: op(B) is read from a K x N copy of B (N x K), first
+                           // in the workspace; the rest of the plan follows it
+    size_t copy_b_bytes;   // that copy's share of the workspace
 };
 // a_kmajor: op(A) is k-contiguous (transA == 0), the layout a copy can help;
 // b_kmajor: op(B) is k-contiguous (transB != 0), or -1 for a plan that never

@@ -100,7 +100,8 @@ const char *det_status_string(int status);
  *   different CTAs: each chunk partial P_c is written to the workspace and a
  *   second kernel adds them left to right. For a large product with transA ==
  *   0 it may instead copy A transposed (K x M) into the workspace and read
- *   that copy, which its FFMA loop consumes faster. With NULL, or too few
+ *   that copy, which its FFMA loop consumes faster; likewise B (N x K, to
+ *   K x N) for transB != 0. With NULL, or too few
  *   bytes, every output's chunks are computed by one thread from A in place.
  *   The result bits are the same either way; only the speed differs. Calls
  *   that share a workspace must be ordered (one stream).
@@ -220,9 +221,9 @@ det_status detgemm_workspace_bytes(const det_profile_v1 *prof, int transA, int t
                                    int64_t M, int64_t N, int64_t K, size_t *bytes);
 
 /* The number of kernels detgemm_f32 launches for this shape and layout with a
- * workspace of workspace_bytes (1 to 4: the transposed copy of A; the GEMM,
- * or the GEMM of the first rows unsplit and then of the rest; the split-K
- * second pass), written to *launches, for callers that count or
+ * workspace of workspace_bytes (1 to 5: the transposed copies of B and of A;
+ * the GEMM, or the GEMM of the first rows unsplit and then of the rest; the
+ * split-K second pass), written to *launches, for callers that count or
  * capture launches. Same argument rules; host-only apart from reading the
  * device's SM count. */
 det_status detgemm_launches(const det_profile_v1 *prof, int transA, int transB, int64_t M,

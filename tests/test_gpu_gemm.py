@@ -83,10 +83,14 @@ def test_split_plan_is_used_where_it_helps(dev):
     assert detlib.detgemm_workspace_bytes(768, 2304, 8192, True, False) > 0
     assert detlib.detgemm_workspace_bytes(2048, 768, 8192, True, False) > 0
     # plenty of tiles: the LM head does not split, but reads a transposed copy
+    # of its k-contiguous W (768 x 50,260 floats, 256-byte rounded, first) and
     # of X (768 x 8192 floats) from the workspace
-    assert detlib.detgemm_workspace_bytes(8192, 50257, 768, False, True) == 768 * 8192 * 4
-    # ... which an m-contiguous A does not need
-    assert detlib.detgemm_workspace_bytes(8192, 50257, 768, True, True) == 0
+    wcopy = (768 * 50260 * 4 + 255) // 256 * 256
+    assert detlib.detgemm_workspace_bytes(8192, 50257, 768, False, True) == wcopy + 768 * 8192 * 4
+    # ... of which an m-contiguous A needs only the first
+    assert detlib.detgemm_workspace_bytes(8192, 50257, 768, True, True) == wcopy
+    # and an n-contiguous B neither
+    assert detlib.detgemm_workspace_bytes(8192, 50257, 768, True, False) == 0
     # one chunk and a small product: neither
     assert detlib.detgemm_workspace_bytes(64, 64, 256) == 0
 
@@ -103,6 +107,28 @@ def test_transposed_a_copy_same_bits(dev, M, N, K, transB):
     # an A whose rows are not 16-byte aligned: the copy moves it element by
     # element, and the GEMM then stages the aligned copy by TMA
     run_case(M, N, K, False, bool(transB), "offset", "padded", "padded", M + K + transB + 2)
+
+
+@pytest.mark.parametrize("M,N,K,transA", [(8192, 2047, 768, 0), (4099, 1537, 2304, 1),
+                                           (8192, 770, 2048, 0)])
+def test_transposed_b_copy_same_bits(dev, M, N, K, transA):
+    # a k-contiguous B (transB) of a product large enough is copied transposed
+    # (K x N, row stride N rounded up to 4) into the workspace first; the bits
+    # equal those of the product read in place (no workspace) and the oracle
+    wsn = detlib.detgemm_workspace_bytes(M, N, K, bool(transA), True)
+    assert wsn >= K * ((N + 3) // 4 * 4) * 4
+    rng = np.random.default_rng(M + N + K)
+    A = rng.standard_normal((K, M) if transA else (M, K)).astype(F)
+    B = rng.standard_normal((N, K)).astype(F)
+    Ad, Bd = to_dev(A, "padded"), to_dev(B, "offset")
+    ws = detlib.gemm_workspace(M, N, K, bool(transA), True)
+    C = detlib.detgemm_f32(Ad, Bd, transA=bool(transA), transB=True, workspace=ws)
+    C2 = detlib.detgemm_f32(Ad, Bd, transA=bool(transA), transB=True)
+    assert_bitwise(host(C2), host(C), "with vs without workspace")
+    rows = sampled_rows(M, 16, 9)
+    Asub = np.ascontiguousarray(A[:, rows] if transA else A[rows])
+    assert_bitwise(host(C[torch.as_tensor(rows, device="cuda")]),
+                   oracle.gemm(Asub, B, transA=bool(transA), transB=True), "sampled rows")
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 200, 1300), (129, 77, 2049), (512, 384, 4096),
