@@ -564,19 +564,30 @@ cudaError_t count_nonfinite_heads(int *flags, const HeadOperand *ops, int n, int
     return e;
 }
 
-// The score product S = Q K^T reads Q and K k-contiguous, where the GEMM runs
-// its scalar FFMA loop. Reading Q from a transposed copy of the whole Q block
-// (heads * head_dim rows of batch * seq queries, m-contiguous) it runs the
-// row-pair loop, with the same bits. The copy (one launch, 8 bytes an element
-// of Q) pays for itself once the sequences are long.
+// The score products (S = Q K^T, and the backward's dP = dO V^T) read both
+// operands k-contiguous, where the GEMM runs its scalar FFMA loop. Reading the
+// left one from a transposed copy of its whole block (heads * head_dim rows of
+// batch * seq tokens, m-contiguous) and the right one from a copy of its own
+// (n-contiguous) the GEMM runs the row-pair loop with direct 16-byte stores,
+// with the same bits. A copy (one launch for the forward's Q and K, one a
+// block in the backward; 8 bytes an element) pays for itself once the
+// sequences are long.
 constexpr int64_t kAttnQCopyMinSeq = 512;
 int64_t attn_qt_ld(int64_t batch, int64_t seq) { return (batch * seq + 3) / 4 * 4; }
+// one block's copy
 size_t attn_qt_bytes(int64_t batch, int64_t seq, int64_t heads, int64_t head_dim) {
     if (seq < kAttnQCopyMinSeq) return 0;
     return (size_t(heads * head_dim) * size_t(attn_qt_ld(batch, seq)) * 4 + 255) / 256 * 256;
 }
-// Q of sequences b0.. and heads h0.. as the score product's op(A), read
-// transposed from QT (row = head_dim index, column = query)
+// the forward's copy of the Q and K blocks (2 heads * head_dim rows)
+size_t attn_qkt_bytes(int64_t batch, int64_t seq, int64_t heads, int64_t head_dim) {
+    if (seq < kAttnQCopyMinSeq) return 0;
+    return (size_t(2 * heads * head_dim) * size_t(attn_qt_ld(batch, seq)) * 4 + 255) / 256 *
+           256;
+}
+// The heads h0.. of sequences b0.. of a block copied transposed into QT (row =
+// head_dim index, column = token): op(A) of a score product (m-contiguous), or
+// its op(B) (n-contiguous)
 HeadOperand q_from_copy(const float *QT, int64_t ldt, int64_t batch, int64_t seq, int64_t hd,
                         int64_t b0, int64_t h0, int64_t head_dim) {
     HeadOperand o;
@@ -603,7 +614,7 @@ DET_API det_status detattention_workspace_bytes(const det_profile_v1 *prof, int6
     if (st != DET_OK) return st;
     if (!bytes || !attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
     *bytes = attention_groups(batch, seq, heads).score_bytes + kAttnFlagBytes +
-             attn_qt_bytes(batch, seq, heads, head_dim);
+             attn_qkt_bytes(batch, seq, heads, head_dim);
     return DET_OK;
 }
 
@@ -619,19 +630,20 @@ DET_API det_status detattention_launches(const det_profile_v1 *prof, int64_t bat
     }
     const AttnGroups g = attention_groups(batch, seq, heads);
     const int64_t groups = ((batch + g.gb - 1) / g.gb) * ((heads + g.gh - 1) / g.gh);
-    // forward: the Q copy (long sequences), then a group's score product, the
-    // count of V's non-finite values, the softmax and P V; backward: the Q and
-    // dO copies (long sequences), then S, the softmax, dP, the counts of dO's,
-    // K's and Q's non-finite values, dV, the softmax backward, dQ and dK
+    // forward: the Q and K copy (long sequences), then a group's score
+    // product, the count of V's non-finite values, the softmax and P V;
+    // backward: the Q, dO and V copies (long sequences), then S, the softmax,
+    // dP, the counts of dO's, K's and Q's non-finite values, dV, the softmax
+    // backward, dQ and dK
     const int64_t copies = attn_qt_bytes(batch, seq, heads, head_dim) ? 1 : 0;
     if (backward == 2 && groups == 1) {
-        // detattention_bwd_saved_f32 with the forward's P: the dO copy, the
-        // counts, the +0 fill past the chunks (when dO is not finite), dP, dV,
-        // the softmax backward, dQ and dK
-        *launches = 9 + copies;
+        // detattention_bwd_saved_f32 with the forward's P: the dO and V
+        // copies, the counts, the +0 fill past the chunks (when dO is not
+        // finite), dP, dV, the softmax backward, dQ and dK
+        *launches = 9 + 2 * copies;
         return DET_OK;
     }
-    *launches = backward ? 10 * groups + 2 * copies : 4 * groups + copies;
+    *launches = backward ? 10 * groups + 3 * copies : 4 * groups + copies;
     return DET_OK;
 }
 
@@ -648,7 +660,7 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
     if (!qkv || !out || ldqkv < 3 * hd || ldout < hd) return DET_ERR_INVALID_ARG;
     if ((st = check_device()) != DET_OK) return st;
     const AttnGroups g = attention_groups(batch, seq, heads);
-    const size_t qt_bytes = attn_qt_bytes(batch, seq, heads, head_dim);
+    const size_t qt_bytes = attn_qkt_bytes(batch, seq, heads, head_dim);
     if (!workspace || workspace_bytes < g.score_bytes + kAttnFlagBytes + qt_bytes ||
         reinterpret_cast<uintptr_t>(workspace) % 256)
         return DET_ERR_WORKSPACE;
@@ -661,14 +673,17 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     auto group = [&](int64_t b0, int64_t nb, int64_t h0, int64_t nh) {
         const int64_t count = nb * nh;
+        // Q and K from the copy (rows 0.. and hd..), or in place
         const HeadOperand Q =
             QT ? q_from_copy(QT, ldt, batch, seq, hd, b0, h0, head_dim)
                : head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, h0 * head_dim, head_dim);
-        const HeadOperand K = head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, hd + h0 * head_dim, head_dim);
+        const HeadOperand K =
+            QT ? q_from_copy(QT + hd * ldt, ldt, batch, seq, hd, b0, h0, head_dim)
+               : head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, hd + h0 * head_dim, head_dim);
         const HeadOperand V = head_operand(qkv, ldqkv, 3 * hd, batch, seq, b0, 2 * hd + h0 * head_dim, head_dim);
         const HeadOperand P = stacked(S, seq, nh, count);
-        cudaError_t r = group_gemm(seq, seq, head_dim, Q, QT ? 1 : 0, K, 1, S, seq, P.zb, P.zh,
-                                   count, nh, 1, s);
+        cudaError_t r = group_gemm(seq, seq, head_dim, Q, QT ? 1 : 0, K, QT ? 0 : 1, S, seq, P.zb,
+                                   P.zh, count, nh, 1, s);
         // P is +0 above the diagonal: with a finite V (counted first) P V
         // skips the chunks past each row block, so the softmax writes P's +0
         // columns only up to that block's end
@@ -680,7 +695,7 @@ DET_API det_status detattention_f32(const det_profile_v1 *prof, int64_t batch, i
                            ldout, seq * ldout, head_dim, count, nh, 0, s, 1, flags);
         return r;
     };
-    cudaError_t e = QT ? launch_transpose_copy(qkv, ldqkv, batch * seq, hd, QT, ldt, s)
+    cudaError_t e = QT ? launch_transpose_copy(qkv, ldqkv, batch * seq, 2 * hd, QT, ldt, s)
                        : cudaSuccess;
     if (e == cudaSuccess) e = for_each_group(batch, heads, g, group);
     return from_cuda(e);
@@ -701,7 +716,7 @@ DET_API det_status detattention_bwd_workspace_bytes(const det_profile_v1 *prof, 
     if (st != DET_OK) return st;
     if (!bytes || !attention_args_ok(batch, seq, heads, head_dim)) return DET_ERR_INVALID_ARG;
     *bytes = 2 * attention_groups(batch, seq, heads).score_bytes + kAttnFlagBytes +
-             2 * attn_qt_bytes(batch, seq, heads, head_dim);
+             3 * attn_qt_bytes(batch, seq, heads, head_dim);
     return DET_OK;
 }
 
@@ -725,7 +740,7 @@ det_status attention_bwd(const det_profile_v1 *prof, int64_t batch, int64_t seq,
     const AttnGroups g = attention_groups(batch, seq, heads);
     const size_t qt_bytes = attn_qt_bytes(batch, seq, heads, head_dim);
     if (!workspace ||
-        workspace_bytes < 2 * g.score_bytes + kAttnFlagBytes + 2 * qt_bytes ||
+        workspace_bytes < 2 * g.score_bytes + kAttnFlagBytes + 3 * qt_bytes ||
         reinterpret_cast<uintptr_t>(workspace) % 256)
         return DET_ERR_WORKSPACE;
     // the forward's P covers every head only when they ran as one group
@@ -740,12 +755,16 @@ det_status attention_bwd(const det_profile_v1 *prof, int64_t batch, int64_t seq,
                          : nullptr;
     float *dOT = qt_bytes ? reinterpret_cast<float *>(reinterpret_cast<char *>(QT) + qt_bytes)
                           : nullptr;
+    float *VT = qt_bytes ? reinterpret_cast<float *>(reinterpret_cast<char *>(dOT) + qt_bytes)
+                         : nullptr;
     const int64_t ldt = attn_qt_ld(batch, seq);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if (QT) {
         if (!saved) e = launch_transpose_copy(qkv, ldqkv, batch * seq, hd, QT, ldt, s);
         if (e == cudaSuccess) e = launch_transpose_copy(dout, lddout, batch * seq, hd, dOT, ldt, s);
+        if (e == cudaSuccess)
+            e = launch_transpose_copy(qkv + 2 * hd, ldqkv, batch * seq, hd, VT, ldt, s);
     }
     if (e == cudaSuccess) e = for_each_group(batch, heads, g, [&](int64_t b0, int64_t nb,
                                                                   int64_t h0, int64_t nh) {
@@ -759,6 +778,7 @@ det_status attention_bwd(const det_profile_v1 *prof, int64_t batch, int64_t seq,
         const HeadOperand Qs = QT ? q_from_copy(QT, ldt, batch, seq, hd, b0, h0, head_dim) : Q;
         const HeadOperand dOs =
             dOT ? q_from_copy(dOT, ldt, batch, seq, hd, b0, h0, head_dim) : dO;
+        const HeadOperand Vs = VT ? q_from_copy(VT, ldt, batch, seq, hd, b0, h0, head_dim) : V;
         float *dbase = dqkv + b0 * seq * lddqkv + h0 * head_dim;
         const int64_t dzb = seq * lddqkv;
         // P and dS are +0 above the diagonal, so P^T and dS^T below it: with
@@ -779,8 +799,8 @@ det_status attention_bwd(const det_profile_v1 *prof, int64_t batch, int64_t seq,
                 r = launch_softmax_causal(count * seq, seq, Pb, seq, scale, 0, seq, Pb, seq, s);
         }
         if (r == cudaSuccess)
-            r = group_gemm(seq, seq, head_dim, dOs, dOT ? 1 : 0, V, 1, dPb, seq, dP.zb, dP.zh,
-                           count, nh, 1, s);
+            r = group_gemm(seq, seq, head_dim, dOs, dOT ? 1 : 0, Vs, VT ? 0 : 1, dPb, seq, dP.zb,
+                           dP.zh, count, nh, 1, s);
         if (r == cudaSuccess && !saved)
             r = count_nonfinite_heads(flags, finite, 3, nb * seq, nh * head_dim, s);
         if (r == cudaSuccess)   // dV = P^T dO
@@ -827,7 +847,7 @@ DET_API det_status detattention_bwd_saved_f32(const det_profile_v1 *prof, int64_
     const AttnGroups g = attention_groups(batch, seq, heads);
     if (!fwd_workspace || reinterpret_cast<uintptr_t>(fwd_workspace) % 256 ||
         fwd_workspace_bytes < g.score_bytes + kAttnFlagBytes +
-                                  attn_qt_bytes(batch, seq, heads, head_dim))
+                                  attn_qkt_bytes(batch, seq, heads, head_dim))
         return DET_ERR_WORKSPACE;
     return attention_bwd(prof, batch, seq, heads, head_dim, qkv, ldqkv, dout, lddout, scale,
                          static_cast<float *>(fwd_workspace), dqkv, lddqkv, workspace,

@@ -494,8 +494,9 @@ det_status detcos_f32(const det_profile_v1 *prof, int64_t n, const float *x, flo
  * groups whose seq x seq score buffers share the workspace (at least
  * detattention_workspace_bytes for the same batch, seq, heads and head_dim,
  * 256-byte aligned: about 1 GiB at most, plus 256 bytes, plus, for seq >= 512,
- * a transposed copy of the Q block, heads head_dim x batch seq floats, from
- * which the score product reads Q): each step is one launch over a group, and
+ * a transposed copy of the Q and K blocks, 2 heads head_dim x batch seq
+ * floats, from which the score product reads Q and K): each step is one
+ * launch over a group, and
  * the score tiles wholly above the diagonal, which the softmax masks, are not
  * computed. P is +0 above the diagonal, so in
  * O = P V the 256-wide k-chunks past a row block's last row add +0 partials;
@@ -568,10 +569,10 @@ det_status detembedding_bwd_f32(const det_profile_v1 *prof, int64_t ntok, int64_
  * heads as in detattention_f32; dV, dQ and dK skip the +0 chunks of P and dS
  * when dO, K and Q are finite. The workspace (at least
  * detattention_bwd_workspace_bytes, 256-byte aligned) holds two score
- * buffers of a group and, for seq >= 512, transposed copies of the Q block
- * and of dout (heads head_dim x batch seq floats each), from which the two
- * score products read Q and dO. dqkv must not overlap qkv, dout or the
- * workspace. Errors as detattention_f32. */
+ * buffers of a group and, for seq >= 512, transposed copies of the Q block,
+ * of dout and of the V block (heads head_dim x batch seq floats each), from
+ * which S = Q K^T reads Q and dP = dO V^T reads dO and V. dqkv must not
+ * overlap qkv, dout or the workspace. Errors as detattention_f32. */
 det_status detattention_bwd_f32(const det_profile_v1 *prof, int64_t batch, int64_t seq,
                                 int64_t heads, int64_t head_dim, const float *qkv,
                                 int64_t ldqkv, const float *dout, int64_t lddout, float scale,

@@ -170,43 +170,44 @@ def test_bad_arguments_are_refused_on_the_host(lib):
     assert at(p, 0, 16, 2, 8, null, 48, one, null, 16, null, 0, null) == 0
     # workspace queries (host only): the score buffers of one group of heads,
     # all 48 heads of 4 x 2048 tokens fitting the 1 GiB cap, 16 x 128 tokens
-    # too, and from 512 tokens a transposed copy of the Q block (heads x
-    # head_dim rows of batch x seq floats)
+    # too, and from 512 tokens a transposed copy of the Q and K blocks (2 x
+    # heads x head_dim rows of batch x seq floats); the backward's copies of
+    # the Q, dO and V blocks
     n = ctypes.c_size_t(0)
     assert lib.detattention_workspace_bytes(p, 4, 2048, 12, 64, ctypes.byref(n)) == 0
-    assert n.value == 48 * 2048 * 2048 * 4 + 256 + 768 * 8192 * 4   # + counts, Q copy
+    assert n.value == 48 * 2048 * 2048 * 4 + 256 + 2 * 768 * 8192 * 4   # + counts, Q/K copy
     assert lib.detattention_bwd_workspace_bytes(p, 4, 2048, 12, 64, ctypes.byref(n)) == 0
-    assert n.value == 2 * 48 * 2048 * 2048 * 4 + 256 + 2 * 768 * 8192 * 4   # + Q, dO copies
+    assert n.value == 2 * 48 * 2048 * 2048 * 4 + 256 + 3 * 768 * 8192 * 4   # + Q, dO, V copies
     assert lib.detattention_workspace_bytes(p, 16, 128, 4, 16, ctypes.byref(n)) == 0
     assert n.value == 64 * 128 * 128 * 4 + 256
     # 8 sequences of 8192 tokens x 12 heads (3 GiB of scores) go 4 heads at a time
     assert lib.detattention_workspace_bytes(p, 8, 8192, 12, 64, ctypes.byref(n)) == 0
-    assert n.value == 4 * 8192 * 8192 * 4 + 256 + 768 * 65536 * 4
+    assert n.value == 4 * 8192 * 8192 * 4 + 256 + 2 * 768 * 65536 * 4
     assert lib.detattention_workspace_bytes(p, 1, 0, 12, 64, ctypes.byref(n)) == 1
-    # launches: 4 a group forward (+ the Q copy from 512 tokens), 10 backward
-    # (+ the Q and dO copies from 512 tokens)
+    # launches: 4 a group forward (+ the Q/K copy from 512 tokens), 10 backward
+    # (+ the Q, dO and V copies from 512 tokens)
     k = ctypes.c_int64(0)
     assert lib.detattention_launches(p, 4, 2048, 12, 64, 0, ctypes.byref(k)) == 0
     assert k.value == 5
     assert lib.detattention_launches(p, 4, 2048, 12, 64, 1, ctypes.byref(k)) == 0
-    assert k.value == 12
+    assert k.value == 13
     assert lib.detattention_launches(p, 16, 128, 4, 16, 1, ctypes.byref(k)) == 0
     assert k.value == 10
     # the backward with the forward's P (one group): no S, no softmax, one +0
-    # fill; the dO copy from 512 tokens
+    # fill; the dO and V copies from 512 tokens
     assert lib.detattention_launches(p, 4, 2048, 12, 64, 2, ctypes.byref(k)) == 0
-    assert k.value == 10
+    assert k.value == 11
     assert lib.detattention_launches(p, 16, 128, 4, 16, 2, ctypes.byref(k)) == 0
     assert k.value == 9
     # several groups: P is not all in the forward's workspace, so it recomputes
     assert lib.detattention_launches(p, 8, 8192, 12, 64, 2, ctypes.byref(k)) == 0
-    assert k.value == 8 * 3 * 10 + 2
+    assert k.value == 8 * 3 * 10 + 3
     assert lib.detattention_launches(p, 16, 128, 4, 16, 0, ctypes.byref(k)) == 0
     assert k.value == 4
     assert lib.detattention_launches(p, 8, 8192, 12, 64, 0, ctypes.byref(k)) == 0
     assert k.value == 8 * 3 * 4 + 1
     assert lib.detattention_launches(p, 8, 8192, 12, 64, 1, ctypes.byref(k)) == 0
-    assert k.value == 8 * 3 * 10 + 2
+    assert k.value == 8 * 3 * 10 + 3
     assert lib.detattention_launches(p, 0, 2048, 12, 64, 0, ctypes.byref(k)) == 0
     assert k.value == 0
     assert lib.detattention_launches(p, 1, 0, 12, 64, 0, ctypes.byref(k)) == 1
