@@ -408,11 +408,14 @@ def run_ours(args, rank, world, local_rank):
     gu_blk = pair_n(ntok_blk, bc["W_gate"].shape[1], bc["W_up"].shape[1],
                     bc["x"].shape[1], False)
     d_blk, f_blk = bc["x"].shape[1], bc["W_gate"].shape[1]
+    # a forward block: the first RMSNorm and the fused residual add + second
+    # RMSNorm (2), QKV, out, down, the gate/up group, the rotary, the
+    # attention, the second residual add and SwiGLU
     block_launches = (2 + gemm_n(ntok_blk, 3 * d_blk, d_blk, ws=blk.ws["qkv"])
                       + gemm_n(ntok_blk, d_blk, d_blk, ws=blk.ws["o"])
                       + gemm_n(ntok_blk, d_blk, f_blk, ws=blk.ws["down"]) + gu_blk
-                      + 1 + attn162 + 2 + 1)
-    # the byte-level LM step: the embedding, 2 forward blocks (11 launches and
+                      + 1 + attn162 + 1 + 1)
+    # the byte-level LM step: the embedding, 2 forward blocks (10 launches and
     # the attention), the head GEMM, the cross-entropy and its mean, the head's
     # two backward GEMMs, 2 backward blocks (13 launches, 5 weight-gradient
     # GEMMs and the attention's backward), the embedding backward, and one
@@ -442,15 +445,18 @@ def run_ours(args, rank, world, local_rank):
     # W_down's, the W_gate/W_up pair's, W_o's and W_qkv's weight gradients
     blk_dw = (dw_n(f_b, d_b) + pair_n(d_b, f_b, f_b, ntok_b, True) + dw_n(d_b, d_b)
               + dw_n(d_b, 3 * d_b))
-    # a forward block: 2 RMSNorms, QKV, out, the gate/up group, down, rotary,
-    # 2 adds, SwiGLU and the attention
-    blk_fwd = 2 + 3 + pair_n(ntok_b, f_b, f_b, d_b, False) + 1 + 2 + 1
-    byte_lm_launches = (1 + nb * (blk_fwd + attn_b) + 1 + 2 + dw_n(bl["vocab"], d_b) + 1
+    # a forward block: the RMSNorm and the fused add + RMSNorm, QKV, out, the
+    # gate/up group, down, rotary, the second add, SwiGLU and the attention
+    blk_fwd = 2 + 3 + pair_n(ntok_b, f_b, f_b, d_b, False) + 1 + 1 + 1
+    # (all blocks but the last leave their second residual add to the next
+    # block's first kernel: one launch fewer a block boundary)
+    byte_lm_launches = (1 + nb * (blk_fwd + attn_b) - (nb - 1) + 1 + 2
+                        + dw_n(bl["vocab"], d_b) + 1
                         + nb * bwd_block_n(ntok_b, d_b, f_b, attn_b_bwd, blk_dw)
                         + 1 + 2 + 7 * nb)
     # the 162M decoder forward: the embedding, 12 blocks as above, the head
     # GEMM (with its transposed copy of the activations), cross-entropy + mean
-    decoder_launches = (1 + len(dm_blocks) * block_launches
+    decoder_launches = (1 + len(dm_blocks) * block_launches - (len(dm_blocks) - 1)
                         + gemm_n(dm_ntok, dm["vocab"], dm["d"], False, True, dm_head_ws) + 2)
     # its training step: that forward; the head's dW and dX GEMMs; each
     # block's backward (as above, with its workspaces); the embedding backward;

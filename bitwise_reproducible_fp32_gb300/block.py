@@ -60,26 +60,40 @@ class Block:
         attn = 2 * 2 * self.B * self.H * kept * self.hd
         return gemm + attn
 
-    def forward(self, x, w):
+    def forward(self, x, w, residual=None, defer_add=False):
         """x: (batch * seq) x d_model; w: g1, W_qkv, W_o, g2, W_gate, W_up,
-        W_down (device tensors). Returns y (this object's buffer)."""
+        W_down (device tensors). Returns y (this object's buffer).
+        residual: (x1, dn) of the block before, which deferred its last add:
+        x is then that block's y buffer, and this block forms x = x1 + dn
+        there together with its first RMSNorm (one kernel, the same bits).
+        defer_add: leave y = x1 + dn to the next block (its residual)."""
         from bitwise_reproducible_fp32_gb300 import detlib as L
-        L.detrmsnorm_f32(x, w["g1"], self.eps, y=self.h, inv_rms=self.inv1)
+        if residual is not None:
+            L.detadd_rmsnorm_f32(residual[0], residual[1], w["g1"], self.eps, x=x, y=self.h,
+                                 inv_rms=self.inv1)
+        else:
+            L.detrmsnorm_f32(x, w["g1"], self.eps, y=self.h, inv_rms=self.inv1)
         L.detgemm_f32(self.h, w["W_qkv"], self.qkv, workspace=self.ws["qkv"])
         L.detrope_f32(self.qkv, heads=2 * self.H, head_dim=self.hd, seq_len=self.T,
                       theta=self.theta)
         L.detattention_f32(self.qkv, self.B, self.T, self.H, self.hd, out=self.att,
                            workspace=self.att_ws)
         L.detgemm_f32(self.att, w["W_o"], self.o, workspace=self.ws["o"])
-        L.detadd_f32(x, self.o, out=self.x1)
-        L.detrmsnorm_f32(self.x1, w["g2"], self.eps, y=self.h2, inv_rms=self.inv2)
+        # x1 = x + o and h2 = RMSNorm(x1), one kernel
+        L.detadd_rmsnorm_f32(x, self.o, w["g2"], self.eps, x=self.x1, y=self.h2,
+                             inv_rms=self.inv2)
         L.detgemm_group_f32([dict(A=self.h2, B=w["W_gate"], C=self.gate),
                              dict(A=self.h2, B=w["W_up"], C=self.up)],
                             workspace=self.ws["gate_up"])
         L.detswiglu_f32(self.gate, self.up, out=self.s)
         L.detgemm_f32(self.s, w["W_down"], self.dn, workspace=self.ws["down"])
-        L.detadd_f32(self.x1, self.dn, out=self.y)
+        if not defer_add:
+            L.detadd_f32(self.x1, self.dn, out=self.y)
         return self.y
+
+    def residual(self):
+        """The pair whose sum is y, for a next block given defer_add."""
+        return self.x1, self.dn
 
     def backward(self, x, w, dy):
         """Gradients of the block's forward from dy (the gradient of its

@@ -52,8 +52,13 @@ def train_step(c, device, hp, status=None, blocks=None, ws=None):
     x0 = L.detembedding_f32(c["emb"], c["tokens"], dev_status=status)
     st["embedding"] = x0
     xs = [x0]
+    # each block but the last leaves its last residual add to the next block,
+    # which forms it together with its first RMSNorm (the same bits)
+    pending = None
     for i, (blk, w) in enumerate(zip(blocks, c["blocks"])):
-        xs.append(blk.forward(xs[-1], w))
+        last = i == len(blocks) - 1
+        xs.append(blk.forward(xs[-1], w, residual=pending, defer_add=not last))
+        pending = None if last else blk.residual()
         st[f"block{i}"] = xs[-1]
     logits = L.detgemm_f32(xs[-1], c["head"], transB=True, workspace=ws["logits"])
     st["logits"] = logits
@@ -120,8 +125,13 @@ def forward(c, device, blocks=None, head_ws=None):
     if head_ws is None:
         head_ws = L.gemm_workspace(c["batch"] * c["seq"], c["vocab"], c["d"], False, True,
                                    device=device)
+    pending = None
     for i, (blk, w) in enumerate(zip(blocks, c["blocks"])):
-        x = blk.forward(x, w)          # each block owns its output buffer
+        # each block owns its output buffer; all but the last leave their last
+        # residual add to the next block's first kernel
+        last = i == len(blocks) - 1
+        x = blk.forward(x, w, residual=pending, defer_add=not last)
+        pending = None if last else blk.residual()
         st[f"block{i}"] = x
     logits = L.detgemm_f32(x, c["head"], transB=True, workspace=head_ws)
     st["logits"] = logits

@@ -912,6 +912,31 @@ DET_API det_status detrmsnorm_f32(const det_profile_v1 *prof, int64_t rows, int6
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+DET_API det_status detadd_rmsnorm_f32(const det_profile_v1 *prof, int64_t rows, int64_t D,
+                                      const float *a, const float *b, float *x,
+                                      const float *gain, float eps, float *y, int64_t ldy,
+                                      float *inv_rms, det_stream_t stream) {
+    det_status st = check_profile(prof);
+    if (st != DET_OK) return st;
+    if (rows < 0 || D < 1 || D > kDimMax || rows > kDimMax) return DET_ERR_INVALID_ARG;
+    if (rows == 0) return DET_OK;
+    if (ldy < D || !a || !b || !x || !gain || !y) return DET_ERR_INVALID_ARG;
+    // x must not overlap a, b or y (it is written while they are read)
+    const int64_t n = rows * D;
+    auto overlap = [n](const float *p, const float *q) { return p < q + n && q < p + n; };
+    if (overlap(x, a) || overlap(x, b) || (y < x + n && x < y + (rows - 1) * ldy + D))
+        return DET_ERR_INVALID_ARG;
+    if ((st = check_device()) != DET_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_add_rmsnorm(rows, D, a, b, x, D, gain, eps, y, ldy, inv_rms, s);
+    if (e == cudaErrorNotSupported) {
+        (void)cudaGetLastError();
+        e = launch_add(n, a, b, x, s);
+        if (e == cudaSuccess) e = launch_rmsnorm(rows, D, x, D, gain, eps, y, ldy, inv_rms, s);
+    }
+    return from_cuda(e);
+}
+
 DET_API det_status detrmsnorm_bwd_workspace_bytes(const det_profile_v1 *prof, int64_t rows,
                                                   int64_t D, size_t *bytes) {
     det_status st = check_profile(prof);

@@ -134,6 +134,12 @@ bool make_tensor_map_2d(CUtensorMap *map, const float *base, int64_t inner, int6
                         int64_t ld, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 // Whether TMA can describe a matrix at base with row stride ld (16-byte rules).
 bool tma_operand_ok(const float *base, int64_t ld);
+// x = a + b (dense rows of D), then the RMSNorm of x into y, in one kernel
+// (the streamed RMSNorm with a second input); cudaErrorNotSupported when the
+// rows do not meet its alignment, and the caller runs the two apart.
+cudaError_t launch_add_rmsnorm(int64_t rows, int64_t D, const float *a, const float *b,
+                               float *x, int64_t ldx, const float *gain, float eps, float *y,
+                               int64_t ldy, float *inv_rms, cudaStream_t s);
 cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
                            const float *gain, float eps, float *y, int64_t ldy,
                            float *inv_rms, cudaStream_t s);

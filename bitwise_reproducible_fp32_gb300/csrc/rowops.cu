@@ -744,21 +744,32 @@ constexpr size_t kStreamSmemBudget = 200 * 1024;
 constexpr unsigned kWatchdogRmsNorm = 8u;
 constexpr int kRowsPerSlot = 3;            // rows a slot: one bulk copy
 
-__host__ __device__ constexpr size_t stream_smem(int D, int S) {
-    return 128 + size_t(S * kRowsPerSlot + 1) * size_t(D) * 4 + size_t(2 * S + 1) * 8;
+// inputs: 1, or 2 for the fused residual add (a slot then holds a's rows and
+// b's rows)
+__host__ __device__ constexpr size_t stream_smem(int D, int S, int inputs = 1) {
+    return 128 + size_t(inputs * S * kRowsPerSlot + 1) * size_t(D) * 4 + size_t(2 * S + 1) * 8;
 }
 
+// With b_in given (the fused residual add), a slot holds the rows of x and of
+// b_in (two bulk copies on its mbarrier; both dense with row stride ldx), each
+// consumer forms v = x + b_in (one rounding), writes it to xs (row stride
+// ldxs) and normalises v: the bits of detadd_f32 followed by detrmsnorm_f32
+// on its output.
 __global__ void __launch_bounds__(kStreamThreads, 1)
     rmsnorm_stream_kernel(int64_t rows, int D, const float *__restrict__ x, int64_t ldx,
                           const float *__restrict__ gain, float eps, float *__restrict__ y,
-                          int64_t ldy, float *__restrict__ inv_rms, int S) {
+                          int64_t ldy, float *__restrict__ inv_rms, int S,
+                          const float *__restrict__ b_in, float *__restrict__ xs,
+                          int64_t ldxs) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ volatile int abort_flag;
     float4 *gs = reinterpret_cast<float4 *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int ng = D >> 2;
+    const int inputs = b_in != nullptr ? 2 : 1;
     float4 *ring = gs + ng;
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + size_t(S) * kRowsPerSlot * ng);
+    float4 *ring_b = ring + size_t(S) * kRowsPerSlot * ng;   // b's rows (fused add)
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + size_t(inputs) * S * kRowsPerSlot * ng);
     uint64_t *empty = full + S;
     uint64_t *gbar = empty + S;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -793,10 +804,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                                                   uint32_t(b / S - 1) & 1u, &abort_flag))
                     break;
                 const int k = min(kRowsPerSlot, n - b * kRowsPerSlot);
-                mbar_arrive_expect_tx(smem_u32(&full[slot]), rb * uint32_t(k));
+                mbar_arrive_expect_tx(smem_u32(&full[slot]), rb * uint32_t(k) * uint32_t(inputs));
                 float4 *dst = ring + size_t(slot) * kRowsPerSlot * ng;
-                const float *src = x + (r0 + int64_t(b) * kRowsPerSlot) * ldx;
-                bulk_load(smem_u32(dst), src, rb * uint32_t(k), smem_u32(&full[slot]));
+                const int64_t row0 = r0 + int64_t(b) * kRowsPerSlot;
+                bulk_load(smem_u32(dst), x + row0 * ldx, rb * uint32_t(k), smem_u32(&full[slot]));
+                if (inputs == 2)
+                    bulk_load(smem_u32(ring_b + size_t(slot) * kRowsPerSlot * ng),
+                              b_in + row0 * ldx, rb * uint32_t(k), smem_u32(&full[slot]));
                 issued = b + 1;
             }
         }
@@ -806,10 +820,24 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             const int b = i / kRowsPerSlot, slot = b % S;
             if (!mbar_wait_or_abort(smem_u32(&full[slot]), uint32_t(b / S) & 1u, &abort_flag))
                 break;
-            const float4 *xr = ring + (size_t(slot) * kRowsPerSlot + i % kRowsPerSlot) * ng;
+            const size_t off = (size_t(slot) * kRowsPerSlot + i % kRowsPerSlot) * ng;
+            const float4 *xr = ring + off, *br = ring_b + off;
+            const int64_t row = r0 + i;
+            // the row's values: x, or x + b (written out once)
+            auto value = [&](int g) {
+                float4 v = xr[g];
+                if (inputs == 2) {
+                    const float4 u = br[g];
+                    v = make_float4(__fadd_rn(v.x, u.x), __fadd_rn(v.y, u.y), __fadd_rn(v.z, u.z),
+                                    __fadd_rn(v.w, u.w));
+                }
+                return v;
+            };
+            float4 *xsr = inputs == 2 ? reinterpret_cast<float4 *>(xs + row * ldxs) : nullptr;
             float s = 0.0f;
             for (int g = lane; g < ng; g += 32) {
-                const float4 v = xr[g];
+                const float4 v = value(g);
+                if (inputs == 2) xsr[g] = v;
                 s = __fmaf_rn(v.x, v.x, s);
                 s = __fmaf_rn(v.y, v.y, s);
                 s = __fmaf_rn(v.z, v.z, s);
@@ -817,10 +845,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             }
             const float ss = warp_butterfly_sum(s);
             const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, Df), eps)));
-            const int64_t row = r0 + i;
             float4 *yr = reinterpret_cast<float4 *>(y + row * ldy);
             for (int g = lane; g < ng; g += 32) {
-                const float4 v = xr[g], gg = gs[g];
+                const float4 v = value(g), gg = gs[g];
                 __stcs(yr + g, make_float4(__fmul_rn(__fmul_rn(v.x, r), gg.x),
                                            __fmul_rn(__fmul_rn(v.y, r), gg.y),
                                            __fmul_rn(__fmul_rn(v.z, r), gg.z),
@@ -919,7 +946,9 @@ cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
         if (e != cudaSuccess) return e;
         const int64_t g = std::min<int64_t>(rows, sm_count_current_device());
         return launch_dependent(rmsnorm_stream_kernel, dim3(unsigned(g)), dim3(kStreamThreads),
-                                smem, s, rows, int(D), x, ldx, gain, eps, y, ldy, inv_rms, S);
+                                smem, s, rows, int(D), x, ldx, gain, eps, y, ldy, inv_rms, S,
+                                static_cast<const float *>(nullptr), static_cast<float *>(nullptr),
+                                int64_t(0));
     }
     if (!vec) {
         rmsnorm_kernel<<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms);
@@ -939,6 +968,28 @@ cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
         default: rmsnorm_vec_kernel<8, 1><<<grid, block, 0, s>>>(rows, D, x, ldx, gain, eps, y, ldy, inv_rms); break;
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_add_rmsnorm(int64_t rows, int64_t D, const float *a, const float *b,
+                               float *x, int64_t ldx, const float *gain, float eps, float *y,
+                               int64_t ldy, float *inv_rms, cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    auto al16 = [](const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+    const int S = int(std::min<int64_t>(
+        kStreamMaxSlots, ((int64_t(kStreamSmemBudget) - 256) / (4 * D) - 1) / (2 * kRowsPerSlot)));
+    if ((D % 4 == 0) && (ldx % 4 == 0) && (ldy % 4 == 0) && al16(a) && al16(b) && al16(x) &&
+        al16(y) && al16(gain) && S >= 4) {
+        const size_t smem = stream_smem(int(D), S, 2);
+        cudaError_t e = cudaFuncSetAttribute(rmsnorm_stream_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
+        if (e != cudaSuccess) return e;
+        const int64_t g = std::min<int64_t>(rows, sm_count_current_device());
+        return launch_dependent(rmsnorm_stream_kernel, dim3(unsigned(g)), dim3(kStreamThreads),
+                                smem, s, rows, int(D), a, D, gain, eps, y, ldy, inv_rms, S, b, x,
+                                ldx);
+    }
+    return cudaErrorNotSupported;   // the caller runs the add and the RMSNorm apart
 }
 
 cudaError_t launch_xent(int64_t rows, int64_t V, const float *logits, int64_t ld,

@@ -92,6 +92,8 @@ SIGNATURES = [
     ("detlog_f32", _int, [_PROF, _i64, _vp, _vp, _vp]),
     ("detswiglu_f32", _int, [_PROF, _i64, _vp, _vp, _vp, _vp]),
     ("detadd_f32", _int, [_PROF, _i64, _vp, _vp, _vp, _vp]),
+    ("detadd_rmsnorm_f32", _int, [_PROF, _i64, _i64, _vp, _vp, _vp, _vp, _f, _vp, _i64, _vp,
+                                  _vp]),
     ("detsoftmax_causal_f32", _int, [_PROF, _i64, _i64, _vp, _i64, _f, _i64, _i64, _vp, _i64,
                                      _vp]),
     ("detrope_f32", _int, [_PROF, _i64, _i64, _i64, _vp, _i64, _i64, _f, _vp]),
@@ -404,6 +406,35 @@ def detrmsnorm_f32(x, gain, eps=1e-6, y=None, inv_rms=None, want_inv_rms=True,
                                _stream(stream))
     _check("detrmsnorm_f32", st)
     return y, inv_rms
+
+
+def detadd_rmsnorm_f32(a, b, gain, eps=1e-6, x=None, y=None, inv_rms=None, want_inv_rms=True,
+                       profile=None, stream=None):
+    """x = a + b, then (y, inv_rms) = the RMSNorm of x, as detadd_f32 and
+    detrmsnorm_f32 give them (a, b, x dense rows x D). Returns (x, y, inv_rms
+    or None)."""
+    import torch
+    _cuda_f32(a, "a", 2)
+    _cuda_f32(b, "b", 2)
+    _cuda_f32(gain, "gain", 1)
+    rows, D = a.shape
+    if tuple(b.shape) != (rows, D) or _ld(a) != D or _ld(b) != D:
+        raise ValueError("a and b must be dense rows of the same shape")
+    if x is None:
+        x = torch.empty((rows, D), dtype=torch.float32, device=a.device)
+    _cuda_f32(x, "x", 2)
+    if _ld(x) != D:
+        raise ValueError("x must be dense")
+    if y is None:
+        y = torch.empty((rows, D), dtype=torch.float32, device=a.device)
+    _cuda_f32(y, "y", 2)
+    if inv_rms is None and want_inv_rms:
+        inv_rms = torch.empty(rows, dtype=torch.float32, device=a.device)
+    st = load().detadd_rmsnorm_f32(_prof(profile), rows, D, _ptr(a), _ptr(b), _ptr(x),
+                                   _ptr(gain), ctypes.c_float(eps), _ptr(y), _ld(y),
+                                   _ptr(inv_rms), _stream(stream))
+    _check("detadd_rmsnorm_f32", st)
+    return x, y, inv_rms
 
 
 def detrmsnorm_bwd_workspace_bytes(rows, D, profile=None) -> int:

@@ -439,6 +439,18 @@ det_status detswiglu_f32(const det_profile_v1 *prof, int64_t n, const float *gat
 det_status detadd_f32(const det_profile_v1 *prof, int64_t n, const float *a,
                       const float *b, float *out, det_stream_t stream);
 
+/* The residual add and the RMSNorm that follows it, in one kernel where the
+ * rows allow: x = a + b (detadd_f32's bits, rows x D, all three dense with row
+ * stride D), then y = detrmsnorm_f32(x) with gain, eps, y's row stride ldy
+ * and inv_rms (nullable) as there: the same bits as the two calls. x must
+ * not overlap a, b or y. With 16-byte aligned rows and D a multiple of 4 it
+ * is one launch (the streamed RMSNorm reads a's and b's rows by bulk copy
+ * and writes x once); otherwise the two operations run apart. */
+det_status detadd_rmsnorm_f32(const det_profile_v1 *prof, int64_t rows, int64_t D,
+                              const float *a, const float *b, float *x, const float *gain,
+                              float eps, float *y, int64_t ldy, float *inv_rms,
+                              det_stream_t stream);
+
 /* Causal softmax of attention scores, row by row: row r keeps the columns
  * j <= (r mod period) + diag of x = scores * scale (one rounding); then the
  * cross-entropy's spelling: m = the row max (NaN-propagating), e = exp(x - m),

@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
                  "detsoftmax_causal_f32", "detrope_f32", "detsin_f32", "detcos_f32",
                  "detattention_f32", "detattention_workspace_bytes", "detembedding_f32",
                  "detswiglu_bwd_f32", "detsoftmax_causal_bwd_f32", "detrope_bwd_f32",
-                 "detembedding_bwd_f32", "detattention_bwd_f32",
+                 "detembedding_bwd_f32", "detattention_bwd_f32", "detadd_rmsnorm_f32",
                  "detattention_bwd_workspace_bytes", "detattention_bwd_saved_f32",
                  "detexp_f32", "detlog_f32", "det_adamw_bias_correction",
                  "det_profile_default",

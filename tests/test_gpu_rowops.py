@@ -53,6 +53,33 @@ def test_rmsnorm_crafted_rows_and_in_place(dev):
     assert_bitwise(host(xd), y_want)
 
 
+@pytest.mark.parametrize("rows,D,offset", [(8192, 768, 0), (1000, 768, 0), (7, 4096, 0),
+                                           (33, 130, 0), (64, 768, 1), (3, 4, 0)])
+def test_add_rmsnorm_equals_add_then_rmsnorm(dev, rows, D, offset):
+    # x = a + b and y = RMSNorm(x) in one call: the fused streamed kernel for
+    # aligned rows with D a multiple of 4, the two operations apart otherwise
+    # (D = 130, or rows one float past a 16-byte boundary); the bits of
+    # detadd_f32 then detrmsnorm_f32
+    rng = np.random.default_rng(rows + D + offset)
+    a = rng.standard_normal((rows, D)).astype(F)
+    b = rng.standard_normal((rows, D)).astype(F)
+    a[0, :3] = [np.inf, -np.inf, 0.0]
+    b[0, :3] = [1.0, 2.0, -0.0]
+    g = (1 + 0.02 * rng.standard_normal(D)).astype(F)
+    x_want = oracle.add(a, b)
+    y_want, inv_want = oracle.rmsnorm(x_want, g, eps=1e-6)
+
+    def dense(m):
+        buf = torch.full((m.size + 4,), float("nan"), device="cuda")
+        buf[offset:offset + m.size] = torch.from_numpy(m.ravel()).cuda()
+        return buf[offset:offset + m.size].view(rows, D)
+    x, y, inv = detlib.detadd_rmsnorm_f32(dense(a), dense(b), to_dev(g), 1e-6,
+                                          x=dense(np.zeros_like(a)))
+    assert_bitwise(host(x), x_want)
+    assert_bitwise(host(y), y_want)
+    assert_bitwise(host(inv), inv_want)
+
+
 def test_rmsnorm_cfg4_full(dev):
     r = inputs.rowops_cfg4(vocab=8)   # x and gain as in the full config
     y, inv = detlib.detrmsnorm_f32(to_dev(r["x"]), to_dev(r["gain"]), float(r["eps"]))
