@@ -1213,13 +1213,15 @@ GemmPlan gemm_plan_core(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor,
 // values as 16-byte rows of 4 columns, and the epilogue stores 16-byte groups
 // directly (measured on the LM head, 11.03 -> 10.70 ms, and the backward's
 // input-gradient products, 3-5%). Taken where that gain, at ~48 TFLOP/s,
-// exceeds the copy's launch and its read and write at HBM speed; the copy
-// comes first in the workspace, and the product over it has its own plan.
+// exceeds one and a half times the copy's launch and its read and write at
+// HBM speed (a product over a few rows of a large B, such as a row block of
+// the LM head, is better off reading B in place); the copy comes first in the
+// workspace, and the product over it has its own plan.
 GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int sms, bool a_kmajor, int b_kmajor) {
     if (b_kmajor == 1 && M > 0 && N > 0 && K > 0) {
         const double gain = 0.035 * 2.0 * double(M) * double(N) * double(K) / 48.0e12;
         const double cost = 5.0e-6 + 8.0 * double(N) * double(K) / 6.0e12;
-        if (gain > cost) {
+        if (gain > 1.5 * cost) {
             GemmPlan pl = gemm_plan_core(M, N, K, sms, a_kmajor, 0);
             pl.transpose_b = 1;
             pl.copy_b_bytes = (size_t(K) * size_t(transposed_ld(N)) * 4 + 255) / 256 * 256;
