@@ -732,17 +732,40 @@ __global__ void __launch_bounds__(kXsThreads, 1)
 // into a ring of shared-memory slots of 3 rows, one 1-D bulk copy a slot
 // (many small copies measured slower: 3 KB copies ran at 20 us for the
 // 8192 x 768 case, 9 KB copies at 12.4), refilling a slot as soon as its
-// rows are released (empty mbarrier, one arrival a row); 16 consumer warps
-// each take every 16th row: the 32 chains and the butterfly over the slot,
+// rows are released (empty mbarrier, one arrival a row); 15 consumer warps
+// each take every 15th row: the 32 chains and the butterfly over the slot,
 // then y = (x r) g straight to global memory. Rows are requested in order, so
 // the first rows are written while later ones are still arriving. Same
 // operations and order as rmsnorm_vec_kernel.
-constexpr int kStreamConsumers = 16;
+// A consumer's wait on a slot names only the parity of the phase it wants,
+// and a wait for phase q passes at once while phase q - 1 is still pending
+// (a parity wait cannot tell q from q - 2). So a warp must never wait on a
+// slot whose previous copy it has not itself seen land: the 15 consumers form
+// 5 groups of 3 (a slot's rows), group g taking the slots' blocks g, g + 5,
+// g + 10, ..., and the slot count is a multiple of 5, so the block a slot held
+// before block b (block b - S) is one the same warp consumed. (Bulk copies can
+// land out of order; with 16 consumers a warp could reach block b while block
+// b - S was still in flight, and read the slot's old rows.)
+constexpr int kStreamConsumers = 15;
 constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;
-constexpr int kStreamMaxSlots = 64;
+constexpr int kStreamMaxSlots = 60;
 constexpr size_t kStreamSmemBudget = 200 * 1024;
 constexpr unsigned kWatchdogRmsNorm = 8u;
 constexpr int kRowsPerSlot = 3;            // rows a slot: one bulk copy
+constexpr int kStreamGroups = kStreamConsumers / kRowsPerSlot;
+static_assert(kStreamConsumers % kRowsPerSlot == 0, "a slot's rows go to one group of warps");
+static_assert(kStreamMaxSlots % kStreamGroups == 0, "slot counts are multiples of the groups");
+
+// The ring's slot count for rows of D floats and 1 or 2 inputs: as many as
+// the shared-memory budget holds, rounded down to a multiple of the consumer
+// groups (0 when fewer than one slot a group fit).
+constexpr int stream_slots(int64_t D, int inputs) {
+    const int64_t fit = ((int64_t(kStreamSmemBudget) - 256) / (4 * D) - 1) /
+                        (int64_t(inputs) * kRowsPerSlot);
+    const int64_t s = (fit < kStreamMaxSlots ? fit : kStreamMaxSlots) / kStreamGroups *
+                      kStreamGroups;
+    return s > 0 ? int(s) : 0;
+}
 
 // inputs: 1, or 2 for the fused residual add (a slot then holds a's rows and
 // b's rows)
@@ -934,11 +957,10 @@ cudaError_t launch_rmsnorm(int64_t rows, int64_t D, const float *x, int64_t ldx,
     const int64_t blocks = (rows + kRmsWarps - 1) / kRmsWarps;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     const dim3 grid{unsigned(blocks)}, block{unsigned(kRmsWarps * 32)};
-    // streamed: dense aligned rows, D % 4 == 0, and room for at least 4 slots
-    const int S = int(std::min<int64_t>(
-        kStreamMaxSlots, ((int64_t(kStreamSmemBudget) - 256) / (4 * D) - 1) / kRowsPerSlot));
+    // streamed: dense aligned rows, D % 4 == 0, and room for a slot a group
+    const int S = stream_slots(D, 1);
     if ((D % 4 == 0) && ldx == D && (ldy % 4 == 0) && al16(x) && al16(y) && al16(gain) &&
-        S >= 4) {
+        S >= kStreamGroups) {
         const size_t smem = stream_smem(int(D), S);
         cudaError_t e = cudaFuncSetAttribute(rmsnorm_stream_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -975,10 +997,9 @@ cudaError_t launch_add_rmsnorm(int64_t rows, int64_t D, const float *a, const fl
                                int64_t ldy, float *inv_rms, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
     auto al16 = [](const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
-    const int S = int(std::min<int64_t>(
-        kStreamMaxSlots, ((int64_t(kStreamSmemBudget) - 256) / (4 * D) - 1) / (2 * kRowsPerSlot)));
+    const int S = stream_slots(D, 2);
     if ((D % 4 == 0) && (ldx % 4 == 0) && (ldy % 4 == 0) && al16(a) && al16(b) && al16(x) &&
-        al16(y) && al16(gain) && S >= 4) {
+        al16(y) && al16(gain) && S >= kStreamGroups) {
         const size_t smem = stream_smem(int(D), S, 2);
         cudaError_t e = cudaFuncSetAttribute(rmsnorm_stream_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -53,6 +53,34 @@ def test_rmsnorm_crafted_rows_and_in_place(dev):
     assert_bitwise(host(xd), y_want)
 
 
+def test_streamed_rmsnorm_repeats_bit_for_bit(dev):
+    # The streamed RMSNorm (plain and with the fused add) at 8192 x 768, 200
+    # launches each on the same inputs: every repeat gives the first one's
+    # bits, and the first matches the oracle. A consumer warp that read a ring
+    # slot before its copy landed would show here as a repeat that differs.
+    rng = np.random.default_rng(77)
+    a = rng.standard_normal((8192, 768)).astype(F)
+    b = rng.standard_normal((8192, 768)).astype(F)
+    g = (1 + 0.02 * rng.standard_normal(768)).astype(F)
+    ad, bd, gd = to_dev(a), to_dev(b), to_dev(g)
+    y0, _ = detlib.detrmsnorm_f32(ad, gd, 1e-6)
+    x1, y1, _ = detlib.detadd_rmsnorm_f32(ad, bd, gd, 1e-6)
+    y0, x1, y1 = y0.clone(), x1.clone(), y1.clone()
+    y, xs, ys = torch.empty_like(y0), torch.empty_like(x1), torch.empty_like(y1)
+    bad = torch.zeros((), dtype=torch.int64, device="cuda")
+    for _ in range(200):
+        detlib.detrmsnorm_f32(ad, gd, 1e-6, y=y)
+        detlib.detadd_rmsnorm_f32(ad, bd, gd, 1e-6, x=xs, y=ys)
+        bad += (y.view(torch.int32) != y0.view(torch.int32)).sum()
+        bad += (xs.view(torch.int32) != x1.view(torch.int32)).sum()
+        bad += (ys.view(torch.int32) != y1.view(torch.int32)).sum()
+    assert int(bad) == 0
+    assert_bitwise(host(y0), oracle.rmsnorm(a, g, eps=1e-6)[0])
+    x_want = oracle.add(a, b)
+    assert_bitwise(host(x1), x_want)
+    assert_bitwise(host(y1), oracle.rmsnorm(x_want, g, eps=1e-6)[0])
+
+
 @pytest.mark.parametrize("rows,D,offset", [(8192, 768, 0), (1000, 768, 0), (7, 4096, 0),
                                            (33, 130, 0), (64, 768, 1), (3, 4, 0)])
 def test_add_rmsnorm_equals_add_then_rmsnorm(dev, rows, D, offset):
