@@ -729,29 +729,30 @@ __global__ void __launch_bounds__(kXsThreads, 1)
 // ---------------------------------------------------------------- RMSNorm, streamed
 // For dense rows (row stride D, 16-byte aligned, D % 4 == 0): one persistent
 // CTA per SM takes a contiguous block of rows. A producer lane streams them
-// into a ring of shared-memory slots of 3 rows, one 1-D bulk copy a slot
+// into a ring of shared-memory slots of 4 rows, one 1-D bulk copy a slot
 // (many small copies measured slower: 3 KB copies ran at 20 us for the
 // 8192 x 768 case, 9 KB copies at 12.4), refilling a slot as soon as its
-// rows are released (empty mbarrier, one arrival a row); 15 consumer warps
-// each take every 15th row: the 32 chains and the butterfly over the slot,
+// rows are released (empty mbarrier, one arrival a row); 16 consumer warps
+// each take every 16th row: the 32 chains and the butterfly over the slot,
 // then y = (x r) g straight to global memory. Rows are requested in order, so
 // the first rows are written while later ones are still arriving. Same
 // operations and order as rmsnorm_vec_kernel.
 // A consumer's wait on a slot names only the parity of the phase it wants,
 // and a wait for phase q passes at once while phase q - 1 is still pending
 // (a parity wait cannot tell q from q - 2). So a warp must never wait on a
-// slot whose previous copy it has not itself seen land: the 15 consumers form
-// 5 groups of 3 (a slot's rows), group g taking the slots' blocks g, g + 5,
-// g + 10, ..., and the slot count is a multiple of 5, so the block a slot held
+// slot whose previous copy it has not itself seen land: the 16 consumers form
+// 4 groups of 4 (a slot's rows), group g taking the slots' blocks g, g + 4,
+// g + 8, ..., and the slot count is a multiple of 4, so the block a slot held
 // before block b (block b - S) is one the same warp consumed. (Bulk copies can
-// land out of order; with 16 consumers a warp could reach block b while block
-// b - S was still in flight, and read the slot's old rows.)
-constexpr int kStreamConsumers = 15;
+// land out of order; with 3-row slots and 16 consumers a warp could reach
+// block b while block b - S was still in flight, and read the slot's old
+// rows.)
+constexpr int kStreamConsumers = 16;
 constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;
-constexpr int kStreamMaxSlots = 60;
+constexpr int kStreamMaxSlots = 64;
 constexpr size_t kStreamSmemBudget = 200 * 1024;
 constexpr unsigned kWatchdogRmsNorm = 8u;
-constexpr int kRowsPerSlot = 3;            // rows a slot: one bulk copy
+constexpr int kRowsPerSlot = 4;            // rows a slot: one bulk copy
 constexpr int kStreamGroups = kStreamConsumers / kRowsPerSlot;
 static_assert(kStreamConsumers % kRowsPerSlot == 0, "a slot's rows go to one group of warps");
 static_assert(kStreamMaxSlots % kStreamGroups == 0, "slot counts are multiples of the groups");
