@@ -844,21 +844,35 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
             if (((kt + 1) % TILES_PER_CHUNK == 0) || last) {
                 const int chunk = kt / TILES_PER_CHUNK;
                 if (SPLIT) {
-                    // split: every chunk partial goes to the workspace
-                    // through the thread's own slots of the totals area, so
-                    // the accumulators are free again before the global stores
+                    // split: chunk partials go to the workspace through the
+                    // thread's own slots of the totals area, so the
+                    // accumulators are free again before the global stores.
+                    // The tile's first chunk group (k from 0) keeps the left
+                    // fold's running total there instead and writes it once,
+                    // at its last chunk: the second pass starts from it.
+                    const bool prefix = w.kt0 == 0;
 #pragma unroll
                     for (int r = 0; r < TM; ++r)
 #pragma unroll
-                        for (int h = 0; h < TN / 4; ++h)
-                            totals[(r * (TN / 4) + h) * THREADS + tid] =
-                                make_float4(acc[r][4 * h], acc[r][4 * h + 1],
-                                            acc[r][4 * h + 2], acc[r][4 * h + 3]);
+                        for (int h = 0; h < TN / 4; ++h) {
+                            float4 &t = totals[(r * (TN / 4) + h) * THREADS + tid];
+                            const float *a4 = &acc[r][4 * h];
+                            if (!prefix || chunk == 0) {
+                                t = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                            } else {
+                                float4 v = t;
+                                v.x = __fadd_rn(v.x, a4[0]);
+                                v.y = __fadd_rn(v.y, a4[1]);
+                                v.z = __fadd_rn(v.z, a4[2]);
+                                v.w = __fadd_rn(v.w, a4[3]);
+                                t = v;
+                            }
+                        }
 #pragma unroll
                     for (int r = 0; r < TM; ++r)
 #pragma unroll
                         for (int c = 0; c < TN; ++c) acc[r][c] = 0.0f;
-                    if (ok) {
+                    if (ok && (!prefix || kt == w.kt1 - 1)) {
                         float4 *wb = p.W + ws_index(chunk, p.mt * p.nt, w.t, 0, tid);
 #pragma unroll 4
                         for (int q4 = 0; q4 < QUADS; ++q4)
@@ -960,7 +974,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
 }
 
 // Split-K second pass: C[i,j] = ((P_0 + P_1) + P_2) + ... over the chunk
-// partials in the workspace, left to right. One thread per workspace quad:
+// partials in the workspace, left to right. The first chunk group's slot
+// holds that group's running total (the fold's prefix, in the slot of its
+// last chunk g - 1), so the sum starts there. One thread per workspace quad:
 // it sums the quad over the chunks and scatters the 4 outputs to the rows and
 // columns the GEMM thread that wrote it owns.
 __global__ void chunk_sum_kernel(KArgs p, int nchunks, int a_km, int b_km) {
@@ -968,10 +984,11 @@ __global__ void chunk_sum_kernel(KArgs p, int nchunks, int a_km, int b_km) {
     const int ntiles = p.mt * p.nt;
     const int64_t slots = int64_t(ntiles) * QUADS * THREADS;
     const int64_t cstride = slots;      // one chunk's worth of quads
+    const int c0 = min(nchunks, p.kt_per_unit / TILES_PER_CHUNK) - 1;
     for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < slots;
          e += int64_t(gridDim.x) * blockDim.x) {
-        float4 t = __ldcs(p.W + e);
-        for (int c = 1; c < nchunks; ++c) {
+        float4 t = __ldcs(p.W + c0 * cstride + e);
+        for (int c = c0 + 1; c < nchunks; ++c) {
             const float4 v = __ldcs(p.W + c * cstride + e);
             t.x = __fadd_rn(t.x, v.x);
             t.y = __fadd_rn(t.y, v.y);
