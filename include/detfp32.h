@@ -97,8 +97,9 @@ const char *det_status_string(int status);
  * workspace / workspace_bytes: optional device scratch (16-byte aligned, not
  *   overlapping A, B or C). With at least detgemm_workspace_bytes() bytes the
  *   library may cut K into groups of whole 256-wide chunks computed by
- *   different CTAs: each chunk partial P_c is written to the workspace and a
- *   second kernel adds them left to right. For a large product with transA ==
+ *   different CTAs: each chunk partial P_c (the first group's running total
+ *   as one) is written to the workspace and a second kernel adds them left
+ *   to right. For a large product with transA ==
  *   0 it may instead copy A transposed (K x M) into the workspace and read
  *   that copy, which its FFMA loop consumes faster; likewise B (N x K, to
  *   K x N) for transB != 0. With NULL, or too few
